@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the PRISM memory-recurrence forward on GB300.
+
+Metric: tokens/s of one PRISM layer forward (B*T tokens, all heads) at the
+16K-token sequential-recommendation shape (B=2, H=4, T=16384, dk=dv=64, L=4,
+bf16 io), plus the achieved fraction of the roofline of the binding resource.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one prism_forward over the whole synthetic batch (inputs resident in
+HBM).  L2 is flushed (a 512 MiB write) before every timed step and the step is
+timed alone with CUDA events on the launch stream.  N > 1 runs one independent
+replica per GPU (the path has no exchange step), launched by torchrun; rank 0
+prints one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "PRISM layer fwd tokens/s on 1 GB300 (T=16K) + % of HBM/tensor roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bit masks
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+    0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+    0x80: "hw_power_brake_slowdown", 0x100: "display_clocks_setting",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="seqrec_16k")
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 portable fp32 kernels, 2 tensor-core path")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic work of the path, per (token, head)
+def alg_bytes_per_token_head(w):
+    io = 2 if w.dtype == "bf16" else 4
+    return io * (2 * w.dk + 2 * w.dv + w.R * w.dk) + 4 * (2 + 2 * w.R)
+
+
+def alg_flops_per_token_head(w):
+    # sequential form: S k, rank-1 correction, L outer products, S q  ->  2 d^2 (L + 3) for dk = dv = d
+    return 2 * w.dk * w.dv * (w.L + 3)
+
+
+def kernel_alg_bytes(name, w):
+    """Bytes a kernel must move at minimum (each of its inputs read once, each output written
+    once), for one launch over the whole workload."""
+    io = 2 if w.dtype == "bf16" else 4
+    th = w.B * w.H * w.T
+    nc = -(-w.T // 64)
+    chunks = w.B * w.H * nc
+    R = w.R
+    q = k = th * w.dk * io
+    v = out = th * w.dv * io
+    u = th * R * w.dk * io
+    gates = th * 4 * (2 + 2 * R)
+    X = th * R * w.dv * 4
+    lam = th * 4
+    Tm = chunks * 64 * 64 * 4
+    W = th * w.dk * 4
+    Up = Vt = th * w.dv * 4
+    S0 = chunks * w.dv * w.dk * 4
+    table = {
+        "simt_prep": v + th * 4 * 2 * R + X,
+        "simt_chunk_solve": k + th * 8 + lam + Tm,
+        "simt_wy": k + v + th * 4 + u + X + lam + Tm + W + Up,
+        "simt_state": k + u + X + lam + W + Up + S0 + Vt,
+        "simt_out": q + k + u + X + lam + S0 + Vt + out,
+    }
+    return table.get(name, q + k + v + u + gates + out)
+
+
+def traffic_from_profiles(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel source (the summary records the source digest); else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_digest():
+        return None
+    return float(m.group(1))
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ssm_sequence_layer_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".h")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+               "--format=csv,noheader,nounits", "-lms", "200"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 3:
+                try:
+                    self.samples.append((float(parts[0]), float(parts[1]), int(parts[2], 16)))
+                except ValueError:
+                    pass
+
+    def stop(self):
+        time.sleep(0.25)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [s[0] for s in self.samples]
+        reasons = set()
+        for s in self.samples:
+            for bit, name in THROTTLE_BITS.items():
+                if s[2] & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[1] for s in self.samples),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(w, inp, seconds_target, nthreads):
+    """Time the oracle on the first Ts tokens of every sequence, Ts sized so the run takes
+    about `seconds_target` seconds.  Returns (tokens/s, Ts, seconds)."""
+    from oracle import prism_oracle
+
+    def run(Ts):
+        sub = {k: (v[:, :, :Ts] if hasattr(v, "shape") and k != "conv_w" else v) for k, v in inp.items()}
+        t0 = time.perf_counter()
+        prism_oracle.forward(sub["q"], sub["k"], sub["v"], sub["beta"], sub["alpha"], sub["u"], sub["gamma"],
+                             sub["eta"], sub["conv_w"], sub["L"], nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    Ts = min(w.T, 256)
+    dt = run(Ts)
+    Ts = int(min(w.T, max(Ts, Ts * seconds_target / max(dt, 1e-3))))
+    dt = run(Ts)
+    return w.B * Ts / dt, Ts, dt
+
+
+def cpu_threads(w):
+    return max(1, min(len(os.sched_getaffinity(0)), w.B * w.H))
+
+
+# ------------------------------------------------------------------------------------------------
+def run_reference(args, w):
+    """The oracle as the reference arm: each step is the oracle over the first Ts tokens of
+    every sequence of the workload, on the host cores."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from oracle import prism_oracle
+    from ssm_sequence_layer_gb300.inputs import make_workload_inputs
+    inp = make_workload_inputs(w)
+    nthreads = cpu_threads(w)
+    Ts = min(w.T, 1024)
+    sub = {k: (v[:, :, :Ts].contiguous() if hasattr(v, "shape") and k != "conv_w" else v) for k, v in inp.items()}
+    import numpy as np
+    sub = {k: (v.double().numpy() if hasattr(v, "double") else v) for k, v in sub.items()}
+
+    def step():
+        prism_oracle.forward(sub["q"], sub["k"], sub["v"], sub["beta"], sub["alpha"], sub["u"], sub["gamma"],
+                             sub["eta"], sub["conv_w"], sub["L"], nthreads=nthreads)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = w.B * Ts * args.steps / dt
+    sample = f"oracle over the first {Ts} tokens of all {w.B * w.H} (batch, head) sequences per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")},
+                   "io": w.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    del np
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+
+    from ssm_sequence_layer_gb300 import binding as Bd
+    from ssm_sequence_layer_gb300 import build as cuda_build
+    from ssm_sequence_layer_gb300.inputs import make_workload_inputs
+
+    world, rank, local = dist_setup(args)
+    if rank == 0:
+        cuda_build.build()
+    barrier(world)
+    steps, warm = args.steps, max(args.warmup, 3)
+    inp_cpu = make_workload_inputs(w, seed=0)
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp_cpu.items()}
+    out = torch.empty_like(dev["v"])
+    stream = torch.cuda.current_stream()
+    plan = Bd.Plan.for_inputs(dev, path=args.path if args.path else None)
+    plan.set_option(Bd.PRISM_OPT_TIMING, 1)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+    for _ in range(warm):
+        flush.zero_()
+        plan.forward(dev, out, stream)
+    torch.cuda.synchronize()
+    plan.last_device_status()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    per_kernel = {}
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        plan.forward(dev, out, stream)
+        ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        kt = plan.kernel_times()
+        launches += len(kt)
+        for name, ms in kt:
+            per_kernel.setdefault(name, []).append(ms)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    plan.last_device_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_local = sum(step_ms) / steps
+    ms = max_over_ranks(ms_local, world)
+    tokens_per_step = w.B * w.T
+    value = tokens_per_step * world / (ms / 1e3)
+
+    peaks, peak_kind = load_peaks()
+    # dominant kernel: largest share of the measured kernel time
+    tot = {n: sum(v) for n, v in per_kernel.items()}
+    dom = max(tot, key=tot.get)
+    dom_ms = tot[dom] / len(per_kernel[dom])
+    dom_bytes = kernel_alg_bytes(dom, w)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    path_bytes = alg_bytes_per_token_head(w) * w.B * w.H * w.T
+    path_achieved = path_bytes / (ms_local / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": traffic_from_profiles(dom, w.name),
+                "alg_bytes_per_launch": dom_bytes, "kernel_ms": dom_ms, "peak_source": f"{peak_kind} hbm_gbs"}
+    kernels = {n: {"ms_mean": tot[n] / len(per_kernel[n]), "share": tot[n] / sum(tot.values())} for n in tot}
+    path_roofline = {"achieved": path_achieved, "unit": "GB/s", "frac": path_achieved / hbm,
+                     "alg_bytes_per_step": path_bytes,
+                     "tensor_frac": alg_flops_per_token_head(w) * w.B * w.H * w.T / (ms_local / 1e3) / 1e12
+                     / float(peaks["bf16_tflops"])}
+
+    # end to end through the host entry point (pinned host buffers, copies inside the timed region)
+    e2e = None
+    if not args.no_e2e:
+        host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in inp_cpu.items()}
+        hout = torch.empty_like(host["v"]).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for k, v in host.items()
+                  if torch.is_tensor(v) and (w.L > 1 or k not in ("u", "gamma", "eta")))
+        d2h = hout.numel() * hout.element_size()
+        for _ in range(2):
+            plan.forward_host(host, hout, stream)
+        e2e_ms = []
+        for _ in range(max(3, min(steps, 20))):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            plan.forward_host(host, hout, stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            e2e_ms.append(a.elapsed_time(b))
+        e2e_ms_mean = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+        e2e = {"value": tokens_per_step * world / (e2e_ms_mean / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_mean}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = cpu_threads(w)
+        v, Ts, dt = oracle_sample(w, inp_cpu, args.cpu_seconds, nthreads)
+        cpu = {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+               "sample": f"fp64 oracle over the first {Ts} tokens of all {w.B * w.H} sequences ({dt:.1f} s)"}
+    plan.close()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")},
+                       "io": w.dtype, "l2": "flushed by a 512 MiB write before every timed step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roofline, "path_roofline": path_roofline, "kernels": kernels,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    from ssm_sequence_layer_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,167 @@
+/*
+ * prism.h -- C ABI of the GB300 (sm_103a) PRISM memory-recurrence forward.
+ *
+ * The operation ("PRISM: Parallel Residual Iterative Sequence Model",
+ * arXiv 2602.10796; reading notes at liuzhao09.github.io/papers/prism.html,
+ * sections 2.2 "Write-Forget Decoupling" and 2.3 "Input-Anchored
+ * Simulation"; Tencent article at youzy.cn, part 03 "PRISM", items two to
+ * four).  Per (batch b, head h), for t = 0..T-1, with R = L - 1:
+ *
+ *   h_t     = sum_{j=0..3} w_j (.) v_{t-j}              (v_{<0} = 0)
+ *   g_t     = GELU'(h_t),   e_t = v_t - GELU(h_t)        (exact erf GELU)
+ *   r_{t,1} = e_t,  r_{t,l+1} = r_{t,l} (.) (1 - eta_{t,l} g_t)
+ *   S_t     = alpha_t S_{t-1} (I - beta_t k_t k_t^T)
+ *             + beta_t v_t k_t^T + sum_{l=1..R} gamma_{t,l} (g_t (.) r_{t,l}) u_{t,l}^T
+ *   o_t     = S_t q_t,     S_0 = 0,   S_t in R^{dv x dk}
+ *
+ * With L = 1 this is the gated delta rule (GDN).  The sequence is evaluated in
+ * 64-token chunks (a WY/UT form of the products of the rank-1 transitions)
+ * with segment-parallel state passing; the result equals the sequential
+ * definition up to floating-point rounding.
+ *
+ * Tensor layouts (all row-major and contiguous, caller-owned device memory):
+ *   q, k    [B,H,T,dk]   io dtype        v, out [B,H,T,dv]   io dtype
+ *   u       [B,H,T,R,dk] io dtype        conv_w [H,4,dv]     io dtype
+ *           (slot l-1 holds level l; tap j of conv_w multiplies v_{t-j})
+ *   beta, alpha [B,H,T]  float32         gamma, eta [B,H,T,R] float32
+ *           (eta[..., R-1] is never read: it would only shape a residual
+ *            that no level uses)
+ * The io dtype is fixed by the plan (float32 or bfloat16); `out` has the io
+ * dtype unless PRISM_OPT_OUT_DTYPE selects float32.  Every io tensor and `out`
+ * must start on a 16-byte boundary, every float32 gate tensor on 4 bytes.
+ *
+ * Errors.  Every call returns a prism_status.  Argument errors are reported
+ * before anything is launched.  A failed launch returns PRISM_ERR_CUDA.
+ * Conditions detected on the device (an internal bound check, a bounded
+ * wait that expired) are written to a status word in the plan's workspace;
+ * read it with prism_plan_last_device_status() after synchronising the
+ * stream.  prism_last_error_message() gives a one-line description of the
+ * last error reported on the calling thread.
+ *
+ * Only NVIDIA sm_103 devices (GB300) are supported; there is no CPU path.
+ */
+#ifndef PRISM_GB300_H
+#define PRISM_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* the CUDA runtime's cudaStream_t is a pointer to this */
+
+#if defined(__GNUC__)
+#define PRISM_API __attribute__((visibility("default")))
+#else
+#define PRISM_API
+#endif
+
+typedef enum prism_status {
+    PRISM_OK = 0,
+    PRISM_ERR_INVALID_ARG = 1, /* null pointer, bad size, L differs from the plan's */
+    PRISM_ERR_UNSUPPORTED = 2, /* a size outside dk,dv in {64,128}, 1 <= L <= 16 */
+    PRISM_ERR_MISALIGNED = 3,  /* a tensor not aligned as stated above */
+    PRISM_ERR_ARCH = 4,        /* current device is not sm_103 */
+    PRISM_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+    PRISM_ERR_TIMEOUT = 6,     /* a bounded device-side wait expired */
+    PRISM_ERR_DEVICE = 7       /* a device-side bound check failed */
+} prism_status;
+
+typedef enum prism_dtype {
+    PRISM_F32 = 0,  /* q, k, v, u, conv_w, out in float32 (fp32 arithmetic throughout) */
+    PRISM_BF16 = 1  /* ... in bfloat16; tensor-core operands bf16, accumulation fp32 */
+} prism_dtype;
+
+typedef enum prism_option {
+    PRISM_OPT_SEGMENTS = 0,  /* segments per sequence for the state passing; 0 = automatic */
+    PRISM_OPT_PATH = 1,      /* 0 = automatic, 1 = portable fp32 kernels, 2 = tensor-core path */
+    PRISM_OPT_WAIT_NS = 2,   /* bound of any device-side wait in ns; 0 = default (100 ms) */
+    PRISM_OPT_TIMING = 3,    /* 1 = record CUDA events around each kernel (see prism_plan_kernel_times) */
+    PRISM_OPT_OUT_DTYPE = 4  /* prism_dtype of `out`; default = the plan's io dtype.  float32 output
+                                keeps the fp32-accumulated result unrounded (bf16 io only changes
+                                the inputs and the tensor-core operands) */
+} prism_option;
+
+/* Duration of one kernel launch of the last forward (see prism_plan_kernel_times). */
+typedef struct prism_kernel_time {
+    const char *name; /* static string naming the kernel */
+    float ms;         /* event-measured duration on the launch stream; -1 if timing was off */
+} prism_kernel_time;
+
+typedef struct prism_plan_s *prism_plan_t;
+
+/*
+ * prism_plan -- validate the problem sizes, bind the plan to the current CUDA
+ * device and allocate its workspace (device memory owned by the plan until
+ * prism_plan_destroy).  B, H >= 1, T >= 1; dk, dv in {64, 128}; 1 <= L <= 16.
+ * On success *out_plan receives the handle; on error it is set to NULL.
+ * A plan may be used by one stream at a time.
+ */
+PRISM_API prism_status prism_plan(int B, int H, int T, int dk, int dv, int L, prism_dtype io,
+                        prism_plan_t *out_plan);
+
+/* Set a plan option (see prism_option).  Takes effect at the next forward. */
+PRISM_API prism_status prism_plan_set_option(prism_plan_t plan, prism_option opt, long long value);
+
+/*
+ * prism_forward -- enqueue the forward on `stream` (NULL = the legacy default
+ * stream) and return without synchronising.  All pointers are device pointers
+ * in the layouts above; they are only read (out is only written) and are not
+ * retained after the call.  L must equal the plan's L.  With L = 1, u, gamma
+ * and eta are not read and may be NULL.
+ */
+PRISM_API prism_status prism_forward(prism_plan_t plan, const void *q, const void *k, const void *v,
+                           const float *beta, const float *alpha, const void *u,
+                           const float *gamma, const float *eta, const void *conv_w, int L,
+                           void *out, struct CUstream_st *stream);
+
+/*
+ * prism_forward_host -- the same forward for callers whose tensors live in
+ * host memory (pinned memory makes the copies asynchronous and faster).  The
+ * inputs are copied into device buffers owned by the plan (allocated on the
+ * first call), the forward runs on `stream`, the output is copied back to
+ * `out`, and the call returns after the stream has drained.
+ */
+PRISM_API prism_status prism_forward_host(prism_plan_t plan, const void *q, const void *k, const void *v,
+                                const float *beta, const float *alpha, const void *u,
+                                const float *gamma, const float *eta, const void *conv_w, int L,
+                                void *out, struct CUstream_st *stream);
+
+/* Free the plan and its workspace.  NULL is accepted. */
+PRISM_API prism_status prism_plan_destroy(prism_plan_t plan);
+
+/* Bytes of device workspace the plan holds (informational). */
+PRISM_API size_t prism_workspace_bytes(prism_plan_t plan);
+
+/*
+ * Read and clear the plan's device status word.  Call after the stream used
+ * by the last forward has been synchronised.  Returns PRISM_OK, or
+ * PRISM_ERR_TIMEOUT / PRISM_ERR_DEVICE as recorded by the kernels.
+ */
+PRISM_API prism_status prism_plan_last_device_status(prism_plan_t plan);
+
+/*
+ * prism_plan_kernel_times -- per-kernel durations of the last forward.  With
+ * PRISM_OPT_TIMING = 1 each forward records a CUDA event pair around every
+ * kernel it launches, on the launch stream.  After that stream has been
+ * synchronised, this fills up to `max` entries of `out` (which may be NULL
+ * when max = 0) and returns the number of kernels the last forward launched,
+ * or -1 on error.
+ */
+PRISM_API int prism_plan_kernel_times(prism_plan_t plan, prism_kernel_time *out, int max);
+
+/* Static description of a status code. */
+PRISM_API const char *prism_status_string(prism_status s);
+
+/* One-line description of the last error returned on the calling thread. */
+PRISM_API const char *prism_last_error_message(void);
+
+/* Version of this library, "major.minor.patch". */
+PRISM_API const char *prism_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PRISM_GB300_H */

@@ -6,11 +6,4 @@ library on first use and raises if it is missing -- there is no CPU fallback.
 """
 from .inputs import WORKLOADS, Workload, make_inputs, make_workload_inputs  # noqa: F401
 
-__all__ = ["WORKLOADS", "Workload", "make_inputs", "make_workload_inputs", "binding"]
-
-
-def __getattr__(name):
-    if name == "binding":
-        from . import binding as _b
-        return _b
-    raise AttributeError(name)
+__all__ = ["WORKLOADS", "Workload", "make_inputs", "make_workload_inputs"]

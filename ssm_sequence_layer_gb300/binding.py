@@ -1,0 +1,251 @@
+"""Thin ctypes binding of the C ABI in ``include/prism.h``.
+
+Argument marshalling only: every step of the forward runs in the CUDA library
+``libprism_gb300.so``.  The functions keep the C names.  Tensors are passed as
+``torch.Tensor`` (device memory for ``prism_forward``, host memory for
+``prism_forward_host``) or as raw integer addresses.  There is no fallback: if
+the library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+PRISM_OK = 0
+PRISM_ERR_INVALID_ARG = 1
+PRISM_ERR_UNSUPPORTED = 2
+PRISM_ERR_MISALIGNED = 3
+PRISM_ERR_ARCH = 4
+PRISM_ERR_CUDA = 5
+PRISM_ERR_TIMEOUT = 6
+PRISM_ERR_DEVICE = 7
+
+PRISM_F32 = 0
+PRISM_BF16 = 1
+
+PRISM_OPT_SEGMENTS = 0
+PRISM_OPT_PATH = 1
+PRISM_OPT_WAIT_NS = 2
+PRISM_OPT_TIMING = 3
+PRISM_OPT_OUT_DTYPE = 4
+
+EXPORTED = ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
+            "prism_plan_destroy", "prism_workspace_bytes", "prism_plan_last_device_status",
+            "prism_status_string", "prism_last_error_message", "prism_version", "prism_plan_kernel_times")
+
+
+class prism_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("ms", ctypes.c_float)]
+
+_lock = threading.Lock()
+_LIB = None
+
+
+class PrismError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{prism_status_string(status)} -- {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _LIB
+    with _lock:
+        if _LIB is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"{os.path.basename(path)} is not built; run "
+                                   "`python -m ssm_sequence_layer_gb300.build` (needs nvcc)")
+            L = ctypes.CDLL(path)
+            vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+            L.prism_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(vp)]
+            L.prism_plan_set_option.argtypes = [vp, i, ctypes.c_longlong]
+            fwd = [vp, vp, vp, vp, f, f, vp, f, f, vp, i, vp, vp]
+            L.prism_forward.argtypes = fwd
+            L.prism_forward_host.argtypes = fwd
+            L.prism_plan_destroy.argtypes = [vp]
+            L.prism_workspace_bytes.argtypes = [vp]
+            L.prism_workspace_bytes.restype = ctypes.c_size_t
+            L.prism_plan_last_device_status.argtypes = [vp]
+            L.prism_status_string.argtypes = [i]
+            L.prism_status_string.restype = ctypes.c_char_p
+            L.prism_last_error_message.restype = ctypes.c_char_p
+            L.prism_version.restype = ctypes.c_char_p
+            L.prism_plan_kernel_times.argtypes = [vp, ctypes.POINTER(prism_kernel_time), i]
+            L.prism_plan_kernel_times.restype = ctypes.c_int
+            for name in ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
+                         "prism_plan_destroy", "prism_plan_last_device_status"):
+                getattr(L, name).restype = ctypes.c_int
+            _LIB = L
+    return _LIB
+
+
+def _check(status):
+    if status != PRISM_OK:
+        raise PrismError(status, prism_last_error_message())
+    return status
+
+
+def _addr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream  # torch.cuda.Stream
+
+
+def prism_status_string(status: int) -> str:
+    return lib().prism_status_string(int(status)).decode()
+
+
+def prism_last_error_message() -> str:
+    return lib().prism_last_error_message().decode()
+
+
+def prism_version() -> str:
+    return lib().prism_version().decode()
+
+
+def prism_plan(B, H, T, dk, dv, L, io=PRISM_BF16) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().prism_plan(B, H, T, dk, dv, L, int(io), ctypes.byref(h)))
+    return h.value
+
+
+def prism_plan_set_option(plan, opt, value):
+    return _check(lib().prism_plan_set_option(plan, int(opt), int(value)))
+
+
+def prism_plan_destroy(plan):
+    return _check(lib().prism_plan_destroy(plan))
+
+
+def prism_workspace_bytes(plan) -> int:
+    return int(lib().prism_workspace_bytes(plan))
+
+
+def prism_plan_last_device_status(plan):
+    return _check(lib().prism_plan_last_device_status(plan))
+
+
+def prism_plan_kernel_times(plan, max_kernels=16):
+    """[(name, ms), ...] of the last forward (ms = -1 when timing was off)."""
+    buf = (prism_kernel_time * max_kernels)()
+    n = lib().prism_plan_kernel_times(plan, buf, max_kernels)
+    if n < 0:
+        raise PrismError(PRISM_ERR_INVALID_ARG, prism_last_error_message())
+    return [(buf[i].name.decode(), float(buf[i].ms)) for i in range(min(n, max_kernels))]
+
+
+def prism_forward(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, out, stream=None):
+    return _check(lib().prism_forward(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha), _addr(u),
+                                      _addr(gamma), _addr(eta), _addr(conv_w), int(L), _addr(out),
+                                      _stream(stream)))
+
+
+def prism_forward_host(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, out, stream=None):
+    return _check(lib().prism_forward_host(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha),
+                                           _addr(u), _addr(gamma), _addr(eta), _addr(conv_w), int(L), _addr(out),
+                                           _stream(stream)))
+
+
+# ------------------------------------------------------------------------------------------------
+class Plan:
+    """Owns a ``prism_plan_t``; ``forward`` marshals a dict of tensors into ``prism_forward``."""
+
+    def __init__(self, B, H, T, dk, dv, L, io="bf16", segments=None, path=None, out=None):
+        self.shape = (B, H, T, dk, dv, L)
+        self.io = io
+        self.out = out or io
+        self.handle = prism_plan(B, H, T, dk, dv, L, PRISM_BF16 if io == "bf16" else PRISM_F32)
+        if self.out != io:
+            prism_plan_set_option(self.handle, PRISM_OPT_OUT_DTYPE, PRISM_BF16 if self.out == "bf16" else PRISM_F32)
+        if segments is not None:
+            prism_plan_set_option(self.handle, PRISM_OPT_SEGMENTS, segments)
+        if path is not None:
+            prism_plan_set_option(self.handle, PRISM_OPT_PATH, path)
+
+    @classmethod
+    def for_inputs(cls, inp, **kw):
+        B, H, T, dk = inp["q"].shape
+        dv = inp["v"].shape[-1]
+        io = "bf16" if str(inp["q"].dtype).endswith("bfloat16") else "f32"
+        return cls(B, H, T, dk, dv, inp["L"], io=io, **kw)
+
+    def set_option(self, opt, value):
+        prism_plan_set_option(self.handle, opt, value)
+
+    def workspace_bytes(self):
+        return prism_workspace_bytes(self.handle)
+
+    def _tensors(self, inp):
+        L = inp["L"]
+        lv = L > 1
+        return (inp["q"], inp["k"], inp["v"], inp["beta"], inp["alpha"], inp["u"] if lv else None,
+                inp["gamma"] if lv else None, inp["eta"] if lv else None, inp["conv_w"], L)
+
+    def forward(self, inp, out=None, stream=None):
+        """Device tensors in, device tensor out (allocated if not given)."""
+        import torch
+        ts = self._tensors(inp)
+        for t in ts[:-1]:
+            if t is not None and (not t.is_cuda or not t.is_contiguous()):
+                raise ValueError("prism_forward takes contiguous CUDA tensors")
+        if out is None:
+            out = torch.empty(inp["v"].shape, dtype=self._out_torch_dtype(), device=inp["v"].device)
+        prism_forward(self.handle, *ts, out, stream)
+        return out
+
+    def _out_torch_dtype(self):
+        import torch
+        return torch.bfloat16 if self.out == "bf16" else torch.float32
+
+    def forward_host(self, inp, out=None, stream=None):
+        """Host tensors in (pinned for speed), host tensor out; synchronous."""
+        import torch
+        ts = self._tensors(inp)
+        for t in ts[:-1]:
+            if t is not None and (t.is_cuda or not t.is_contiguous()):
+                raise ValueError("prism_forward_host takes contiguous host tensors")
+        if out is None:
+            out = torch.empty(inp["v"].shape, dtype=self._out_torch_dtype())
+        prism_forward_host(self.handle, *ts, out, stream)
+        return out
+
+    def kernel_times(self):
+        return prism_plan_kernel_times(self.handle)
+
+    def last_device_status(self):
+        return prism_plan_last_device_status(self.handle)
+
+    def close(self):
+        if self.handle:
+            prism_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()

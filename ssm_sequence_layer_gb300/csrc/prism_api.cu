@@ -1,0 +1,367 @@
+// Host side of the C ABI declared in include/prism.h: argument validation, the
+// plan (shape, device, workspace) and the launch sequence on the caller's stream.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "prism_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "no error";
+
+prism_status fail(prism_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+prism_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(PRISM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t io_size(prism_dtype io) { return io == PRISM_BF16 ? 2 : 4; }
+
+prism_status check_sizes(int B, int H, int T, int dk, int dv, int L, prism_dtype io)
+{
+    if (B < 1 || H < 1 || T < 1)
+        return fail(PRISM_ERR_INVALID_ARG, "B, H and T must be >= 1 (got B=%d H=%d T=%d)", B, H, T);
+    if (L < 1) return fail(PRISM_ERR_INVALID_ARG, "L must be >= 1 (got %d)", L);
+    if (io != PRISM_F32 && io != PRISM_BF16) return fail(PRISM_ERR_INVALID_ARG, "unknown io dtype %d", (int)io);
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128))
+        return fail(PRISM_ERR_UNSUPPORTED, "dk and dv must be 64 or 128 (got dk=%d dv=%d)", dk, dv);
+    if (L > 16) return fail(PRISM_ERR_UNSUPPORTED, "L must be <= 16 (got %d)", L);
+    const long long BH = (long long)B * H;
+    if (BH > 65535) return fail(PRISM_ERR_UNSUPPORTED, "B*H must be <= 65535 (got %lld)", BH);
+    if ((long long)T > (1LL << 30)) return fail(PRISM_ERR_UNSUPPORTED, "T too large (%d)", T);
+    return PRISM_OK;
+}
+
+prism_status check_device(int *device, int *sms)
+{
+    cudaError_t e = cudaGetDevice(device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *device))) return cuda_fail(e, "attr");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *device))) return cuda_fail(e, "attr");
+    if ((e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *device))) return cuda_fail(e, "attr");
+    if (major != 10 || minor != 3)
+        return fail(PRISM_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103 only", *device, major,
+                    minor);
+    return PRISM_OK;
+}
+
+prism_status check_forward_args(const prism_plan_s *p, const void *q, const void *k, const void *v,
+                                const float *beta, const float *alpha, const void *u, const float *gamma,
+                                const float *eta, const void *conv_w, int L, const void *out)
+{
+    if (!p) return fail(PRISM_ERR_INVALID_ARG, "plan is NULL");
+    if (L != p->shape.L) return fail(PRISM_ERR_INVALID_ARG, "L=%d differs from the plan's L=%d", L, p->shape.L);
+    if (!q || !k || !v || !beta || !alpha || !conv_w || !out)
+        return fail(PRISM_ERR_INVALID_ARG, "q, k, v, beta, alpha, conv_w and out must not be NULL");
+    if (p->shape.R > 0 && (!u || !gamma || !eta))
+        return fail(PRISM_ERR_INVALID_ARG, "u, gamma and eta must not be NULL when L > 1");
+    const void *io_ptrs[] = {q, k, v, conv_w, out, p->shape.R > 0 ? u : nullptr};
+    const char *io_names[] = {"q", "k", "v", "conv_w", "out", "u"};
+    for (int i = 0; i < 6; ++i)
+        if (io_ptrs[i] && !aligned(io_ptrs[i], 16))
+            return fail(PRISM_ERR_MISALIGNED, "%s is not 16-byte aligned", io_names[i]);
+    const void *f_ptrs[] = {beta, alpha, p->shape.R > 0 ? gamma : nullptr, p->shape.R > 0 ? eta : nullptr};
+    const char *f_names[] = {"beta", "alpha", "gamma", "eta"};
+    for (int i = 0; i < 4; ++i)
+        if (f_ptrs[i] && !aligned(f_ptrs[i], 4))
+            return fail(PRISM_ERR_MISALIGNED, "%s is not 4-byte aligned", f_names[i]);
+    return PRISM_OK;
+}
+
+// Byte sizes of the call's tensors, in the order q, k, v, beta, alpha, u, gamma, eta, conv_w, out.
+void tensor_bytes(const prism_plan_s *p, size_t nb[10])
+{
+    const prism::Shape &s = p->shape;
+    const size_t e = io_size(p->io), th = (size_t)s.BH * s.T;
+    nb[0] = th * s.dk * e;
+    nb[1] = th * s.dk * e;
+    nb[2] = th * s.dv * e;
+    nb[3] = th * 4;
+    nb[4] = th * 4;
+    nb[5] = th * s.R * s.dk * e;
+    nb[6] = th * s.R * 4;
+    nb[7] = th * s.R * 4;
+    nb[8] = (size_t)s.H * 4 * s.dv * e;
+    nb[9] = th * s.dv * io_size(p->out_dtype);
+}
+
+// 1 = portable fp32 kernels, 2 = tensor-core path
+int resolve_path(const prism_plan_s *p)
+{
+    if (p->opt_path == 1) return 1;
+    if (p->opt_path == 2) return 2;
+    return prism::tc_supported(p->shape, p->io) ? 2 : 1;
+}
+
+void free_workspaces(prism_plan_s *p)
+{
+    if (p->ws_simt) cudaFree(p->ws_simt);
+    if (p->ws_tc) cudaFree(p->ws_tc);
+    if (p->d_status) cudaFree(p->d_status);
+    p->ws_simt = p->ws_tc = nullptr;
+    p->d_status = nullptr;
+}
+
+prism_status ensure_workspace(prism_plan_s *p, int path)
+{
+    cudaError_t e;
+    if (path == 1) {
+        if (p->ws_simt) return PRISM_OK;
+        const size_t bytes = prism::simt_workspace_bytes(p->shape);
+        if ((e = cudaMalloc(&p->ws_simt, bytes)) != cudaSuccess) {
+            p->ws_simt = nullptr;
+            return cuda_fail(e, "workspace allocation (portable path)");
+        }
+        p->ws_simt_bytes = bytes;
+        prism::simt_carve(p->shape, p->ws_simt, &p->simt);
+        return PRISM_OK;
+    }
+    const int P = prism::tc_segments(p->shape, p->sm_count, p->opt_segments);
+    if (p->ws_tc && p->tcw.P == P) return PRISM_OK;
+    if (p->ws_tc) {
+        cudaFree(p->ws_tc);
+        p->ws_tc = nullptr;
+        p->ws_tc_bytes = 0;
+    }
+    const size_t bytes = prism::tc_workspace_bytes(p->shape, P);
+    if ((e = cudaMalloc(&p->ws_tc, bytes)) != cudaSuccess) {
+        p->ws_tc = nullptr;
+        return cuda_fail(e, "workspace allocation (tensor-core path)");
+    }
+    p->ws_tc_bytes = bytes;
+    prism::tc_carve(p->shape, P, p->ws_tc, &p->tcw);
+    return PRISM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *prism_version(void) { return "0.1.0"; }
+
+const char *prism_last_error_message(void) { return g_err; }
+
+const char *prism_status_string(prism_status s)
+{
+    switch (s) {
+    case PRISM_OK: return "PRISM_OK";
+    case PRISM_ERR_INVALID_ARG: return "PRISM_ERR_INVALID_ARG: invalid argument";
+    case PRISM_ERR_UNSUPPORTED: return "PRISM_ERR_UNSUPPORTED: unsupported problem size";
+    case PRISM_ERR_MISALIGNED: return "PRISM_ERR_MISALIGNED: misaligned tensor";
+    case PRISM_ERR_ARCH: return "PRISM_ERR_ARCH: device is not sm_103";
+    case PRISM_ERR_CUDA: return "PRISM_ERR_CUDA: CUDA runtime error";
+    case PRISM_ERR_TIMEOUT: return "PRISM_ERR_TIMEOUT: a bounded device wait expired";
+    case PRISM_ERR_DEVICE: return "PRISM_ERR_DEVICE: a device-side check failed";
+    }
+    return "unknown prism_status";
+}
+
+prism_status prism_plan(int B, int H, int T, int dk, int dv, int L, prism_dtype io, prism_plan_t *out_plan)
+{
+    if (!out_plan) return fail(PRISM_ERR_INVALID_ARG, "out_plan is NULL");
+    *out_plan = nullptr;
+    prism_status st = check_sizes(B, H, T, dk, dv, L, io);
+    if (st != PRISM_OK) return st;
+    int device = 0, sms = 0;
+    if ((st = check_device(&device, &sms)) != PRISM_OK) return st;
+
+    prism_plan_s *p = new (std::nothrow) prism_plan_s();
+    if (!p) return fail(PRISM_ERR_INVALID_ARG, "out of host memory");
+    prism::Shape &s = p->shape;
+    s.B = B; s.H = H; s.T = T; s.dk = dk; s.dv = dv; s.L = L; s.R = L - 1;
+    s.NC = (T + prism::kChunk - 1) / prism::kChunk;
+    s.BH = B * H;
+    p->io = io;
+    p->out_dtype = io;
+    p->device = device;
+    p->sm_count = sms;
+
+    cudaError_t e = prism::simt_prepare(s, io);
+    if (e == cudaSuccess && prism::tc_supported(s, io)) e = prism::tc_prepare();
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "kernel attribute setup");
+    }
+    if ((e = cudaMalloc(&p->d_status, 256)) != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "status word allocation");
+    }
+    if ((e = cudaMemset(p->d_status, 0, sizeof(int))) != cudaSuccess) {
+        cudaFree(p->d_status);
+        delete p;
+        return cuda_fail(e, "status word init");
+    }
+    // workspace of the path the plan uses by default
+    st = ensure_workspace(p, resolve_path(p));
+    if (st != PRISM_OK) {
+        cudaFree(p->d_status);
+        delete p;
+        return st;
+    }
+    for (int i = 0; i < 2 * prism::kMaxTimedKernels; ++i) {
+        if ((e = cudaEventCreate(&p->timer.ev[i])) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(p->timer.ev[j]);
+            free_workspaces(p);
+            delete p;
+            return cuda_fail(e, "event creation");
+        }
+    }
+    *out_plan = p;
+    return PRISM_OK;
+}
+
+prism_status prism_plan_set_option(prism_plan_t p, prism_option opt, long long value)
+{
+    if (!p) return fail(PRISM_ERR_INVALID_ARG, "plan is NULL");
+    switch (opt) {
+    case PRISM_OPT_SEGMENTS:
+        if (value < 0) return fail(PRISM_ERR_INVALID_ARG, "segments must be >= 0");
+        p->opt_segments = value;
+        return PRISM_OK;
+    case PRISM_OPT_PATH:
+        if (value < 0 || value > 2) return fail(PRISM_ERR_INVALID_ARG, "path must be 0, 1 or 2");
+        p->opt_path = value;
+        return PRISM_OK;
+    case PRISM_OPT_WAIT_NS:
+        if (value < 0) return fail(PRISM_ERR_INVALID_ARG, "wait bound must be >= 0");
+        p->opt_wait_ns = value;
+        return PRISM_OK;
+    case PRISM_OPT_OUT_DTYPE:
+        if (value != PRISM_F32 && value != PRISM_BF16) return fail(PRISM_ERR_INVALID_ARG, "unknown out dtype");
+        p->out_dtype = (prism_dtype)value;
+        return PRISM_OK;
+    case PRISM_OPT_TIMING:
+        if (value != 0 && value != 1) return fail(PRISM_ERR_INVALID_ARG, "timing must be 0 or 1");
+        p->opt_timing = value;
+        return PRISM_OK;
+    }
+    return fail(PRISM_ERR_INVALID_ARG, "unknown option %d", (int)opt);
+}
+
+prism_status prism_forward(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,
+                           const float *alpha, const void *u, const float *gamma, const float *eta,
+                           const void *conv_w, int L, void *out, struct CUstream_st *stream)
+{
+    prism_status st = check_forward_args(p, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, out);
+    if (st != PRISM_OK) return st;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != p->device)
+        return fail(PRISM_ERR_INVALID_ARG, "current device %d differs from the plan's device %d", dev, p->device);
+    const int path = resolve_path(p);
+    if (path == 2 && !prism::tc_supported(p->shape, p->io))
+        return fail(PRISM_ERR_UNSUPPORTED, "the tensor-core path takes bf16 io, dk = dv = 64 and L <= 4");
+    if ((st = ensure_workspace(p, path)) != PRISM_OK) return st;
+    prism::ForwardArgs a{q, k, v, u, conv_w, beta, alpha, gamma, eta, out};
+    p->timer.on = p->opt_timing != 0;
+    p->timer.reset((cudaStream_t)stream);
+    if (path == 2)
+        e = prism::tc_forward(p->shape, a, p->out_dtype == PRISM_F32, p->tcw, p->d_status, p->opt_wait_ns, p->timer);
+    else
+        e = prism::simt_forward(p->shape, p->io, p->out_dtype, a, p->simt, p->d_status, p->timer);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return PRISM_OK;
+}
+
+prism_status prism_forward_host(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,
+                                const float *alpha, const void *u, const float *gamma, const float *eta,
+                                const void *conv_w, int L, void *out, struct CUstream_st *stream)
+{
+    if (!p) return fail(PRISM_ERR_INVALID_ARG, "plan is NULL");
+    size_t nb[10];
+    tensor_bytes(p, nb);
+    size_t off[10], total = 0;
+    for (int i = 0; i < 10; ++i) {
+        off[i] = total;
+        total += (nb[i] + 255) & ~(size_t)255;
+    }
+    if (p->stage_bytes < total) {
+        if (p->stage) cudaFree(p->stage);
+        p->stage = nullptr;
+        p->stage_bytes = 0;
+        cudaError_t e = cudaMalloc(&p->stage, total);
+        if (e != cudaSuccess) return cuda_fail(e, "staging allocation");
+        p->stage_bytes = total;
+    }
+    const void *src[9] = {q, k, v, beta, alpha, u, gamma, eta, conv_w};
+    void *dst[10];
+    for (int i = 0; i < 10; ++i) dst[i] = (char *)p->stage + off[i];
+    // validate the host pointers like device ones before copying anything
+    prism_status st = check_forward_args(p, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, out);
+    if (st != PRISM_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    for (int i = 0; i < 9; ++i) {
+        if (nb[i] == 0 || !src[i]) continue;
+        cudaError_t e = cudaMemcpyAsync(dst[i], src[i], nb[i], cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    }
+    const bool lvl = p->shape.R > 0;
+    st = prism_forward(p, dst[0], dst[1], dst[2], (const float *)dst[3], (const float *)dst[4],
+                       lvl ? dst[5] : nullptr, lvl ? (const float *)dst[6] : nullptr,
+                       lvl ? (const float *)dst[7] : nullptr, dst[8], L, dst[9], stream);
+    if (st != PRISM_OK) return st;
+    cudaError_t e = cudaMemcpyAsync(out, dst[9], nb[9], cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    return PRISM_OK;
+}
+
+prism_status prism_plan_destroy(prism_plan_t p)
+{
+    if (!p) return PRISM_OK;
+    for (int i = 0; i < 2 * prism::kMaxTimedKernels; ++i)
+        if (p->timer.ev[i]) cudaEventDestroy(p->timer.ev[i]);
+    free_workspaces(p);
+    cudaError_t e2 = p->stage ? cudaFree(p->stage) : cudaSuccess;
+    delete p;
+    if (e2 != cudaSuccess) return cuda_fail(e2, "staging free");
+    return PRISM_OK;
+}
+
+size_t prism_workspace_bytes(prism_plan_t p) { return p ? p->ws_simt_bytes + p->ws_tc_bytes : 0; }
+
+int prism_plan_kernel_times(prism_plan_t p, prism_kernel_time *out, int max)
+{
+    if (!p || max < 0 || (max > 0 && !out)) {
+        fail(PRISM_ERR_INVALID_ARG, "bad arguments to prism_plan_kernel_times");
+        return -1;
+    }
+    const int n = p->timer.n;
+    for (int i = 0; i < n && i < max && i < prism::kMaxTimedKernels; ++i) {
+        out[i].name = p->timer.names[i];
+        out[i].ms = -1.f;
+        if (p->timer.on) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, p->timer.ev[2 * i], p->timer.ev[2 * i + 1]) == cudaSuccess) out[i].ms = ms;
+        }
+    }
+    return n;
+}
+
+prism_status prism_plan_last_device_status(prism_plan_t p)
+{
+    if (!p) return fail(PRISM_ERR_INVALID_ARG, "plan is NULL");
+    int word = 0;
+    cudaError_t e = cudaMemcpy(&word, p->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (word == prism::kDevOk) return PRISM_OK;
+    if ((e = cudaMemset(p->d_status, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, "status clear");
+    if (word == prism::kDevTimeout) return fail(PRISM_ERR_TIMEOUT, "a bounded device wait expired");
+    return fail(PRISM_ERR_DEVICE, "device-side check failed (code %d)", word);
+}
+
+}  // extern "C"

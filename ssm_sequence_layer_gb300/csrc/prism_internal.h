@@ -1,0 +1,116 @@
+// Internal declarations shared by the host library and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/prism.h"
+
+namespace prism {
+
+constexpr int kChunk = 64;  // tokens per chunk of the WY/UT evaluation
+
+// Device status word values (written by kernels, read by prism_plan_last_device_status).
+enum DeviceStatus : int {
+    kDevOk = 0,
+    kDevBounds = 1,   // an internal index check failed
+    kDevTimeout = 2,  // a bounded wait expired
+};
+
+// Pointers of one forward call (device memory, layouts as in prism.h).
+struct ForwardArgs {
+    const void *q, *k, *v, *u, *conv_w;
+    const float *beta, *alpha, *gamma, *eta;
+    void *out;
+};
+
+// Problem shape shared by all kernels.
+struct Shape {
+    int B, H, T, dk, dv, L, R, NC, BH;
+};
+
+// Workspace of the portable fp32 path: one buffer per intermediate.
+struct SimtWorkspace {
+    float *X;    // [BH][T][R][dv]   injection factors x_{t,l}
+    float *lam;  // [BH][T]          chunk-local cumulative log decay
+    float *Tm;   // [BH][NC][C][C]   (I + A)^{-1} per chunk
+    float *W;    // [BH][NC*C][dk]   W = T diag(beta Gamma) K
+    float *Up;   // [BH][NC*C][dv]   U' = T (diag(beta) V - M X)
+    float *S0;   // [BH][NC][dv][dk] state entering each chunk
+    float *Vt;   // [BH][NC*C][dv]   V~ = U' - W S0^T
+};
+
+// Records CUDA events around each kernel launch of one forward (when enabled) and
+// counts the launches.  Events are recorded on the launch stream.
+constexpr int kMaxTimedKernels = 16;
+struct KernelTimer {
+    cudaEvent_t ev[2 * kMaxTimedKernels];
+    const char *names[kMaxTimedKernels];
+    int n;
+    bool on;
+    cudaStream_t stream;
+    void reset(cudaStream_t s) { n = 0; stream = s; }
+    void begin(const char *name)
+    {
+        if (n < kMaxTimedKernels) {
+            names[n] = name;
+            if (on) cudaEventRecord(ev[2 * n], stream);
+        }
+    }
+    void end()
+    {
+        if (on && n < kMaxTimedKernels) cudaEventRecord(ev[2 * n + 1], stream);
+        ++n;
+    }
+};
+
+// Workspace of the tensor-core path.
+struct TcWorkspace {
+    float *zsum;             // [BH][P][128][64]  segment maps Z = [N; M]
+    float *sstart;           // [BH][P][64][64]   state entering each segment
+    float *stash_o;          // [BH][NC][64][64]  o0 per chunk (segments >= 1)
+    __nv_bfloat16 *stash_q;  // [BH][NC][64][64]  Qhat per chunk (segments >= 1)
+    int P;                   // segments per sequence
+};
+
+bool tc_supported(const Shape &s, prism_dtype io);
+int tc_segments(const Shape &s, int sm_count, long long opt);
+size_t tc_workspace_bytes(const Shape &s, int P);
+void tc_carve(const Shape &s, int P, void *base, TcWorkspace *w);
+cudaError_t tc_prepare();
+cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const TcWorkspace &w, int *d_status,
+                       long long wait_ns, KernelTimer &tm);
+
+size_t simt_workspace_bytes(const Shape &s);
+void simt_carve(const Shape &s, void *base, SimtWorkspace *w);
+cudaError_t simt_prepare(const Shape &s, prism_dtype io);
+cudaError_t simt_forward(const Shape &s, prism_dtype io, prism_dtype out, const ForwardArgs &a,
+                         const SimtWorkspace &w, int *d_status, KernelTimer &timer);
+
+}  // namespace prism
+
+struct prism_plan_s {
+    prism::Shape shape;
+    prism_dtype io;
+    int device;
+    int sm_count;
+    long long opt_segments;
+    long long opt_path;
+    long long opt_wait_ns;
+    long long opt_timing;
+    prism_dtype out_dtype;
+    prism::KernelTimer timer;
+    // device memory (owned): status word, and one workspace per path, allocated on first use
+    int *d_status;
+    void *ws_simt;
+    size_t ws_simt_bytes;
+    prism::SimtWorkspace simt;
+    void *ws_tc;
+    size_t ws_tc_bytes;
+    prism::TcWorkspace tcw;
+    // device staging buffers for prism_forward_host (owned, allocated on first use)
+    void *stage;
+    size_t stage_bytes;
+};

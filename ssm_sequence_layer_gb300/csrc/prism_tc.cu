@@ -1,0 +1,783 @@
+// Tensor-core path of the PRISM memory-recurrence forward (sm_103a: tcgen05 + TMA).
+//
+// Shapes: dk = dv = 64, 1 <= L <= 4, bf16 io, chunks of C = 64 tokens.
+//
+// Three kernels:
+//   segment  one CTA per (sequence, segment of consecutive chunks).  For every chunk it runs
+//            the prep (anchor, gain, residual chain), the Gram tiles, the UT/WY solve, the WY
+//            factors and the chunk's state map S -> S M_c + N_c, and carries the augmented state
+//            Z = [N; M] (the segment's map S_start -> S_start M + N) through the segment.  The
+//            output of a chunk is o = o0 + Qhat S_start^T: o0 and Qhat are exact given Z, so the
+//            first segment of a sequence (S_start = 0) writes o directly and the others stash
+//            (o0, Qhat) for the fix-up.
+//   combine  per sequence, S_start of segment p from the maps of segments 0..p-1 (associative
+//            combine of the input-only affine maps, notes on PRISM section 2.1).
+//   fixup    o = o0 + Qhat S_start^T for the chunks of segments >= 1.
+//
+// Chunk algebra (local index i, j; lambda_i = sum_{m<=i} ln alpha_m; lc = lambda_{C-1};
+// e^{x} factors are taken relative to the chunk end so that every stored factor is <= 1
+// or is a row factor e^{lambda_i - lc} >= 1 bounded by the chunk's total decay):
+//   A_ij  = beta_i e^{lambda_i - lambda_j} k_i.k_j           (j < i)   -> T = (I + A)^{-1}
+//   PK_l  = beta_i e^{lambda_i - lc} k_i.u_{j,l}              (j < i)
+//   PQ_l  = e^{lambda_i - lc} q_i.u_{j,l},   G = e^{lambda_i - lc} q_i.k_j   (j <= i)
+//   Xs_l  = e^{lc - lambda_j} x_{j,l}                          (x = gamma g (.) r, the prep)
+//   RHS   = diag(beta) V - sum_l PK_l Xs_l
+//   [U'^T; W^T] = [RHS | diag(beta Gamma) K]^T T^T              (Gamma_i = e^{lambda_i})
+//   UWs   = [U'^T; W^T] diag(e^{lc - lambda_j})
+//   D4    = UWs G^T + [Xs^T; 0] PQ^T  = [O_loc^T ; (G~ W)^T]    (G~ = Q K^T o D, D incl. diag)
+//   D5    = UWs [K] + [Xs^T; 0] [U]   = [N_c ; W^T K']
+//   Qt    = Q~^T = diag(Gamma) Q^T - (G~ W)^T,   M_c = Gamma_C I - W^T K'
+//   Z    <- Z M_c + [N_c; 0],   [o0^T ; Qhat^T] = Z Qt + [O_loc^T ; 0]   (Z before the update)
+// All matrix products above run on tcgen05.mma (bf16 operands in 128B-swizzled shared memory,
+// fp32 accumulators in tensor memory); operands come from TMA or from the epilogues.
+#include <cudaTypedefs.h>
+
+#include "prism_internal.h"
+#include "tc_ptx.h"
+
+namespace prism {
+namespace tc {
+
+constexpr int C = kChunk;
+constexpr int D = 64;       // dk = dv
+constexpr int RMAX = 3;     // refinement levels handled (L <= 4)
+constexpr int NT = 256;     // threads per CTA
+constexpr uint32_t TILE = 8192;  // 64 rows x 128 B
+
+// shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_Q = 0;                    // Q tile, then K, U0..U2 (contiguous: [Q;K] and [K;U] operands)
+constexpr uint32_t OFF_K = OFF_Q + TILE;
+constexpr uint32_t OFF_U = OFF_K + TILE;
+constexpr uint32_t OFF_V0 = OFF_U + RMAX * TILE;  // two V stages, 72 rows x 128 B (8-row halo), unswizzled
+constexpr uint32_t VBYTES = 72 * 128;
+constexpr uint32_t OFF_V1 = OFF_V0 + 10240;
+constexpr uint32_t OFF_E = OFF_V1 + 10240;        // [PK0|PQ0|PK1|PQ1|PK2|PQ2|G]; later Qt, Mc
+constexpr uint32_t OFF_G = OFF_E + 6 * TILE;
+constexpr uint32_t OFF_AKK = OFF_E + 7 * TILE;    // A (fp32, stride 68); later RHS|BGK; later UWs
+constexpr uint32_t LDA = 68;
+constexpr uint32_t OFF_T32 = OFF_AKK + 64 * LDA * 4;
+constexpr uint32_t OFF_TB = OFF_T32 + 64 * LDA * 4;  // T (bf16 tile)
+constexpr uint32_t OFF_XS = OFF_TB + TILE;            // Xs0..Xs2
+constexpr uint32_t OFF_ZERO = OFF_XS + RMAX * TILE;   // zero tile
+constexpr uint32_t OFF_ZA = OFF_ZERO + TILE;          // Z (128 rows, bf16, K-major)
+constexpr uint32_t OFF_SC = OFF_ZA + 2 * TILE;        // per-token scalars
+constexpr uint32_t SC_FLOATS = 64 * 6 + 64 * RMAX * 2 + 3 * 256 + 8;
+constexpr uint32_t SMEM_BYTES = OFF_SC + SC_FLOATS * 4 + 1024;  // + alignment slack
+
+static_assert(OFF_AKK % 1024 == 0 && OFF_TB % 1024 == 0 && OFF_XS % 1024 == 0 && OFF_ZA % 1024 == 0, "align");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// TMEM column map
+constexpr uint32_t TM_D1 = 0, TM_D2 = 256, TM_D3 = 320, TM_D4 = 384, TM_D5 = 448, TM_D6 = 0, TM_D7 = 64;
+
+struct SegParams {
+    const float *beta, *alpha, *gamma, *eta;
+    const __nv_bfloat16 *conv_w;
+    void *out;              // bf16, or fp32 when out_f32
+    float *zsum;            // [BH][P][128][64]
+    float *stash_o;         // [BH][NC][64][64]  o0 (token-major)
+    __nv_bfloat16 *stash_q; // [BH][NC][64][64]  Qhat (token-major)
+    int *status;
+    int H, T, R, NC, P;
+    int out_f32;
+    unsigned long long wait_ns;  // bound of every wait on an mbarrier
+};
+
+__device__ __forceinline__ void set_status(int *st, int code) { atomicCAS(st, 0, code); }
+
+__device__ __forceinline__ uint32_t pack2(float a, float b)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// write 32 consecutive fp32 values (columns col0..col0+31 of row `row`) as bf16 into a
+// [rows][64] SW128 tile
+__device__ __forceinline__ void st_row32(uint8_t *tile, int row, int col0, const float (&v)[32])
+{
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint4 w;
+        w.x = pack2(v[8 * g + 0], v[8 * g + 1]);
+        w.y = pack2(v[8 * g + 2], v[8 * g + 3]);
+        w.z = pack2(v[8 * g + 4], v[8 * g + 5]);
+        w.w = pack2(v[8 * g + 6], v[8 * g + 7]);
+        *reinterpret_cast<uint4 *>(tile + sw128(row, col0 + 8 * g)) = w;
+    }
+}
+
+__device__ __forceinline__ float ld_bf(const uint8_t *tile, int row, int col)
+{
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128(row, col)));
+}
+
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(NT, 1)
+    segment_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_u, SegParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint32_t tmem_base_s;
+    __shared__ __align__(8) uint64_t mbar[4];  // 0: MMA, 1: Q/K/U, 2,3: V stages
+    __shared__ int abort_s;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;  // TMEM lane owned in epilogues
+    const int bh = blockIdx.x / p.P, seg = blockIdx.x % p.P;
+    const int h = bh % p.H;
+    const int R = p.R;
+    const int c_begin = (int)(((long long)seg * p.NC) / p.P);
+    const int c_end = (int)(((long long)(seg + 1) * p.NC) / p.P);
+
+    float *sc = reinterpret_cast<float *>(sm + OFF_SC);
+    float *s_beta = sc;             // 64
+    float *s_lam = sc + 64;         // 64
+    float *s_rowf = sc + 128;       // e^{lambda_i - lc}
+    float *s_colf = sc + 192;       // e^{lc - lambda_i}
+    float *s_gam = sc + 256;        // Gamma_i = e^{lambda_i}
+    float *s_bg = sc + 320;         // beta_i Gamma_i
+    float *s_gc = sc + 384;         // gamma_{i,l} e^{lc - lambda_i}   [64][RMAX]
+    float *s_eta = s_gc + 64 * RMAX;  // [64][RMAX]
+    float *s_xtmp = s_eta + 64 * RMAX;  // 3 x 256 scratch of the solve
+    float *s_misc = s_xtmp + 3 * 256;   // [0] = lc
+
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t mb_mma = smem_u32(&mbar[0]), mb_qku = smem_u32(&mbar[1]);
+    const uint32_t mb_v[2] = {smem_u32(&mbar[2]), smem_u32(&mbar[3])};
+
+    if (tid == 0) {
+        abort_s = 0;
+        mbar_init(mb_mma, 1);
+        mbar_init(mb_qku, 1);
+        mbar_init(mb_v[0], 1);
+        mbar_init(mb_v[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_u);
+    }
+    // zero tile, and Z = [0; I] (segments >= 1) or 0 (segment 0)
+    for (int e = tid; e < (int)(TILE / 16); e += NT) reinterpret_cast<uint4 *>(sm + OFF_ZERO)[e] = make_uint4(0, 0, 0, 0);
+    for (int e = tid; e < 128 * 64; e += NT) {
+        const int r = e >> 6, m = e & 63;
+        const float z = (seg > 0 && r >= 64 && (r - 64) == m) ? 1.f : 0.f;
+        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_ZA + sw128(r, m)) = __float2bfloat16_rn(z);
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 512);
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_base_s;
+
+    uint32_t ph_mma = 0, ph_qku = 0, ph_v[2] = {0, 0};
+    uint32_t pending = 0;  // issuer's view (thread 0): 1 MMA, 2 Q/K/U load, 4/8 V loads in flight
+    const uint32_t qku_bytes = (2 + R) * TILE;
+
+    auto issue_qku = [&](int c) {
+        mbar_expect_tx(mb_qku, qku_bytes);
+        tma_load_3d(sbase + OFF_Q, &tm_q, mb_qku, 0, c * C, bh);
+        tma_load_3d(sbase + OFF_K, &tm_k, mb_qku, 0, c * C, bh);
+        for (int l = 0; l < R; ++l) tma_load_4d(sbase + OFF_U + l * TILE, &tm_u, mb_qku, 0, l, c * C, bh);
+        pending |= 2u;
+    };
+    auto issue_v = [&](int c, int stage) {
+        mbar_expect_tx(mb_v[stage], VBYTES);
+        tma_load_3d(sbase + (stage ? OFF_V1 : OFF_V0), &tm_v, mb_v[stage], 0, c * C - 8, bh);
+        pending |= 4u << stage;
+    };
+    // collective bounded wait on an mbarrier phase; on expiry the CTA records the timeout
+    // status and leaves the chunk loop (the phase is kept so the drain can wait for it)
+    auto wait_all = [&](uint32_t mb, uint32_t &phase, uint32_t bit) -> bool {
+        const bool ok = mbar_wait(mb, phase, p.wait_ns);
+        if (ok) {
+            phase ^= 1u;
+            pending &= ~bit;
+        } else {
+            abort_s = 1;
+            set_status(p.status, kDevTimeout);
+        }
+        __syncthreads();
+        return abort_s == 0;
+    };
+
+    if (tid == 0 && c_begin < c_end) {
+        issue_v(c_begin, 0);
+        issue_qku(c_begin);
+    }
+    const float w0 = __bfloat162float(p.conv_w[((size_t)h * 4 + 0) * D + (tid & 63)]);
+    const float w1 = __bfloat162float(p.conv_w[((size_t)h * 4 + 1) * D + (tid & 63)]);
+    const float w2 = __bfloat162float(p.conv_w[((size_t)h * 4 + 2) * D + (tid & 63)]);
+    const float w3 = __bfloat162float(p.conv_w[((size_t)h * 4 + 3) * D + (tid & 63)]);
+
+    bool alive = true;
+    for (int c = c_begin; c < c_end && alive; ++c) {
+        const int stage = (c - c_begin) & 1;
+        const int t0 = c * C;
+        const int n = min(C, p.T - t0);
+        const size_t tok0 = (size_t)bh * p.T + t0;
+
+        // ---- P0: gates and decay factors ------------------------------------------------------
+        if (tid < 64) {
+            const bool valid = tid < n;
+            s_beta[tid] = valid ? p.beta[tok0 + tid] : 0.f;
+            s_lam[tid] = valid ? logf(p.alpha[tok0 + tid]) : 0.f;
+        }
+        for (int e = tid; e < 64 * RMAX; e += NT) {
+            const int i = e / RMAX, l = e % RMAX;
+            const bool valid = (i < n) && (l < R);
+            s_gc[e] = valid ? p.gamma[(tok0 + i) * R + l] : 0.f;
+            s_eta[e] = valid ? p.eta[(tok0 + i) * R + l] : 0.f;
+        }
+        __syncthreads();
+        if (warp == 0) {  // inclusive scan of 64 log-decays, two per lane
+            const float a0 = s_lam[2 * lane], a1 = s_lam[2 * lane + 1];
+            float s = a0 + a1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, s, off);
+                if (lane >= off) s += y;
+            }
+            s_lam[2 * lane + 1] = s;
+            s_lam[2 * lane] = s - a1;
+        }
+        __syncthreads();
+        const float lc = s_lam[63];
+        if (tid < 64) {
+            const float li = s_lam[tid];
+            s_rowf[tid] = __expf(li - lc);
+            s_colf[tid] = __expf(lc - li);
+            s_gam[tid] = __expf(li);
+            s_bg[tid] = s_beta[tid] * __expf(li);
+            if (tid == 0) {
+                s_misc[0] = lc;
+                if (-lc > 80.f) set_status(p.status, kDevBounds);  // decay beyond the factorised range
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < 64 * RMAX; e += NT) s_gc[e] *= s_colf[e / RMAX];
+
+        // ---- P1: prep -> Xs tiles ---------------------------------------------------------------
+        if (!wait_all(mb_v[stage], ph_v[stage], 4u << stage)) break;
+        if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
+        {
+            const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + (stage ? OFF_V1 : OFF_V0));
+            const int ch = tid & 63;
+            for (int i = tid >> 6; i < 64; i += NT / 64) {
+                const float v0 = __bfloat162float(vb[(i + 8) * 64 + ch]);
+                const float v1 = __bfloat162float(vb[(i + 7) * 64 + ch]);
+                const float v2 = __bfloat162float(vb[(i + 6) * 64 + ch]);
+                const float v3 = __bfloat162float(vb[(i + 5) * 64 + ch]);
+                const float a = fmaf(w0, v0, fmaf(w1, v1, fmaf(w2, v2, w3 * v3)));
+                const float Phi = 0.5f * erfcf(-a * 0.70710678118654752f);
+                const float phi = 0.39894228040143268f * __expf(-0.5f * a * a);
+                const float g = fmaf(a, phi, Phi);
+                float r = v0 - a * Phi;
+                for (int l = 0; l < R; ++l) {
+                    const float x = s_gc[i * RMAX + l] * g * r;
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_XS + l * TILE + sw128(i, ch)) = __float2bfloat16_rn(x);
+                    r *= 1.f - s_eta[i * RMAX + l] * g;
+                }
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+
+        // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T ----------------------------------------------
+        if (!wait_all(mb_qku, ph_qku, 2u)) break;
+        const int N1 = 64 * (1 + R);
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t id = idesc_bf16(128, N1, 0, 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + TM_D1, sdesc(sbase + OFF_Q + s * 32, 16, 1024), sdesc(sbase + OFF_K + s * 32, 16, 1024),
+                         id, s > 0);
+            mma_commit(mb_mma);
+            pending |= 1u;
+        }
+        if (!wait_all(mb_mma, ph_mma, 1u)) break;
+        fence_after_sync();
+
+        // ---- E1: masks and decay factors -> A (fp32), PK_l, PQ_l, G (bf16 tiles) ---------------
+        {
+            const int i = row & 63;
+            const bool qside = row < 64;
+            const float rf = s_rowf[i];
+            const float bi = s_beta[i];
+            const int nblk = N1 / 64;  // 64-column blocks: 0 = keys, 1.. = levels
+            for (int blk = 0; blk < nblk; ++blk) {
+                const int col0 = blk * 64 + half * 32;
+                float v[32];
+                tmem_ld32(tmem + TM_D1 + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0, v);
+                const int j0 = half * 32;
+                if (qside) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) v[q] = (j0 + q <= i) ? v[q] * rf : 0.f;
+                    uint8_t *tile = sm + (blk == 0 ? OFF_G : OFF_E + (blk - 1) * 2 * TILE + TILE);
+                    st_row32(tile, i, j0, v);
+                } else if (blk == 0) {
+                    float *A = reinterpret_cast<float *>(sm + OFF_AKK);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) A[i * LDA + j0 + q] = (j0 + q < i) ? v[q] * bi * rf * s_colf[j0 + q] : 0.f;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) v[q] = (j0 + q < i) ? v[q] * bi * rf : 0.f;
+                    st_row32(sm + OFF_E + (blk - 1) * 2 * TILE, i, j0, v);
+                }
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- P3: MX = sum_l PK_l Xs_l (MMA, in flight) while the CTA solves T = (I + A)^{-1} -------
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t id = idesc_bf16(128, 64, 0, 1);
+            for (int l = 0; l < R; ++l)
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tmem + TM_D2, sdesc(sbase + OFF_E + l * 2 * TILE + s * 32, 16, 1024),
+                             sdesc(sbase + OFF_XS + l * TILE + s * 2048, TILE, 1024), id, (l | s) != 0);
+            mma_commit(mb_mma);
+            pending |= 1u;
+        }
+        {
+            const float *A = reinterpret_cast<const float *>(sm + OFF_AKK);
+            float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
+            if (tid < 64) {  // diagonal 16x16 blocks by forward substitution, one column per thread
+                const int b = tid >> 4, cc = tid & 15, o = 16 * b;
+                float t[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float x = (r == cc) ? 1.f : 0.f;
+                    if (r > cc) {
+                        float s = 0.f;
+#pragma unroll
+                        for (int j = 0; j < r; ++j)
+                            if (j >= cc) s = fmaf(A[(o + r) * LDA + o + j], t[j], s);
+                        x = -s;
+                    }
+                    t[r] = x;
+                    T32[(o + r) * LDA + o + cc] = x;
+                }
+            }
+            __syncthreads();
+            for (int d = 1; d < 4; ++d) {  // off-diagonal blocks, one block diagonal at a time
+                const int nb = 4 - d;
+                for (int e = tid; e < nb * 256; e += NT) {  // X = sum_k A[bi][k] T[k][bj]
+                    const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                    const int bi = b + d, bj = b;
+                    float s = 0.f;
+                    for (int k = 16 * bj; k < 16 * bi; ++k) s = fmaf(A[(16 * bi + r) * LDA + k], T32[k * LDA + 16 * bj + cc], s);
+                    s_xtmp[e] = s;
+                }
+                __syncthreads();
+                for (int e = tid; e < nb * 256; e += NT) {  // T[bi][bj] = -T[bi][bi] X
+                    const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                    const int bi = b + d, bj = b;
+                    float s = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        s = fmaf(T32[(16 * bi + r) * LDA + 16 * bi + k], s_xtmp[(b << 8) + (k << 4) + cc], s);
+                    T32[(16 * bi + r) * LDA + 16 * bj + cc] = -s;
+                }
+                __syncthreads();
+            }
+            for (int e = tid; e < 64 * 8; e += NT) {  // T (bf16, [i][j], zero above the diagonal)
+                const int i = e >> 3, g = e & 7;
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = (8 * g + q <= i) ? T32[i * LDA + 8 * g + q] : 0.f;
+                uint4 w;
+                w.x = pack2(v[0], v[1]);
+                w.y = pack2(v[2], v[3]);
+                w.z = pack2(v[4], v[5]);
+                w.w = pack2(v[6], v[7]);
+                *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128(i, 8 * g)) = w;
+            }
+        }
+        if (!wait_all(mb_mma, ph_mma, 1u)) break;
+        fence_after_sync();
+
+        // ---- E2: RHS = diag(beta) V - MX, and diag(beta Gamma) K -------------------------------
+        {
+            const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + (stage ? OFF_V1 : OFF_V0));
+            if (quad < 2) {  // lanes 0..63 hold MX rows
+                const int i = row, j0 = half * 32;
+                float v[32];
+                tmem_ld32(tmem + TM_D2 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+                const float bi = s_beta[i];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = bi * __bfloat162float(vb[(i + 8) * 64 + j0 + q]) - v[q];
+                st_row32(sm + OFF_AKK, i, j0, v);  // RHS tile (A is dead after the solve)
+            } else {
+                const int tt = (half ? 64 : 0) + (tid & 63);  // 0..127 over the warps of quads 2, 3
+                const int j = tt >> 1, m0 = (tt & 1) * 32;
+                float v[32];
+                const float s = s_bg[j];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = s * ld_bf(sm + OFF_K, j, m0 + q);
+                st_row32(sm + OFF_AKK + TILE, j, m0, v);  // BGK tile
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- P4: [U'^T ; W^T] = [RHS | BGK]^T T^T -------------------------------------------------
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t id = idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + TM_D3, sdesc(sbase + OFF_AKK + s * 2048, TILE, 1024), sdesc(sbase + OFF_TB + s * 32, 16, 1024),
+                         id, s > 0);
+            mma_commit(mb_mma);
+            pending |= 1u;
+        }
+        if (!wait_all(mb_mma, ph_mma, 1u)) break;
+        fence_after_sync();
+
+        // ---- E3: UWs = [U'^T; W^T] diag(e^{lc - lambda_j}) ---------------------------------------
+        {
+            const int j0 = half * 32;
+            float v[32];
+            tmem_ld32(tmem + TM_D3 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] *= s_colf[j0 + q];
+            fence_before_sync();
+            __syncthreads();  // every thread has read D3; RHS|BGK are dead (MMA done)
+            st_row32(sm + OFF_AKK, row, j0, v);
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- P5: D4 = UWs [G; PQ]^T-part, D5 = UWs [K; U]-part ------------------------------------
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t idk = idesc_bf16(128, 64, 0, 0), idx = idesc_bf16(128, 64, 1, 0);
+            const uint32_t idk5 = idesc_bf16(128, 64, 0, 1), idx5 = idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t a = sdesc(sbase + OFF_AKK + s * 32, 16, 1024);
+                mma_bf16(tmem + TM_D4, a, sdesc(sbase + OFF_G + s * 32, 16, 1024), idk, s > 0);
+                mma_bf16(tmem + TM_D5, a, sdesc(sbase + OFF_K + s * 2048, TILE, 1024), idk5, s > 0);
+            }
+            for (int l = 0; l < R; ++l) {
+                const uint32_t xs = OFF_XS + l * TILE;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t a = sdesc(sbase + xs + s * 2048, OFF_ZERO - xs, 1024);
+                    mma_bf16(tmem + TM_D4, a, sdesc(sbase + OFF_E + l * 2 * TILE + TILE + s * 32, 16, 1024), idx, 1);
+                    mma_bf16(tmem + TM_D5, a, sdesc(sbase + OFF_U + l * TILE + s * 2048, TILE, 1024), idx5, 1);
+                }
+            }
+            mma_commit(mb_mma);
+            pending |= 1u;
+        }
+        if (!wait_all(mb_mma, ph_mma, 1u)) break;
+        fence_after_sync();
+
+        // ---- E4: Qt = diag(Gamma) Q^T - (G~W)^T ;  Mc = Gamma_C I - W^T K' -------------------------
+        if (quad >= 2) {
+            const int m = row - 64, j0 = half * 32;
+            float v[32];
+            tmem_ld32(tmem + TM_D4 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = s_gam[j0 + q] * ld_bf(sm + OFF_Q, j0 + q, m) - v[q];
+            st_row32(sm + OFF_E, m, j0, v);  // Qt [m][i]
+            tmem_ld32(tmem + TM_D5 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+            const float gC = __expf(lc);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = ((j0 + q) == m ? gC : 0.f) - v[q];
+            st_row32(sm + OFF_E + TILE, m, j0, v);  // Mc [m][m']
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after_sync();
+            if (c + 1 < c_end) issue_qku(c + 1);  // Q, K, U of this chunk are no longer read
+            // ---- P6: D6 = Z Mc, D7 = Z Qt ------------------------------------------------------
+            const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t a = sdesc(sbase + OFF_ZA + s * 32, 16, 1024);
+                mma_bf16(tmem + TM_D6, a, sdesc(sbase + OFF_E + TILE + s * 2048, TILE, 1024), id, s > 0);
+                mma_bf16(tmem + TM_D7, a, sdesc(sbase + OFF_E + s * 2048, TILE, 1024), id, s > 0);
+            }
+            mma_commit(mb_mma);
+            pending |= 1u;
+        }
+        if (!wait_all(mb_mma, ph_mma, 1u)) break;
+        fence_after_sync();
+
+        // ---- E5: Z <- Z Mc + [N_c; 0];  o0 / Qhat ------------------------------------------------
+        {
+            const int j0 = half * 32;
+            const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+            float z[32], nc[32], o[32], ol[32];
+            tmem_ld32(tmem + TM_D6 + lane_off + (uint32_t)j0, z);
+            tmem_ld32(tmem + TM_D5 + lane_off + (uint32_t)j0, nc);
+            tmem_ld32(tmem + TM_D7 + lane_off + (uint32_t)j0, o);
+            tmem_ld32(tmem + TM_D4 + lane_off + (uint32_t)j0, ol);
+            if (row < 64) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) z[q] += nc[q];
+            }
+            fence_before_sync();
+            __syncthreads();  // MMAs reading ZA are complete (waited above); all rows loaded
+            st_row32(sm + OFF_ZA, row, j0, z);
+            if (c + 1 == c_end) {
+                float *zs = p.zsum + (((size_t)bh * p.P + seg) * 128 + row) * 64 + j0;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) zs[q] = z[q];
+            }
+            // outputs: row < 64 -> o0^T[c][i] = D7 + O_loc^T ; row >= 64 -> Qhat^T[m][i]
+            if (row < 64) {
+                const int cc = row;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int i = j0 + q;
+                    if (i < n) {
+                        const float val = o[q] + ol[q];
+                        if (seg == 0) {
+                            if (p.out_f32)
+                                reinterpret_cast<float *>(p.out)[(tok0 + i) * D + cc] = val;
+                            else
+                                reinterpret_cast<__nv_bfloat16 *>(p.out)[(tok0 + i) * D + cc] = __float2bfloat16_rn(val);
+                        } else
+                            p.stash_o[(((size_t)bh * p.NC + c) * 64 + i) * 64 + cc] = val;
+                    }
+                }
+            } else if (seg > 0) {
+                const int m = row - 64;
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                    p.stash_q[(((size_t)bh * p.NC + c) * 64 + j0 + q) * 64 + m] = __float2bfloat16_rn(o[q]);
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        alive = abort_s == 0;
+    }
+
+    // drain: after an expired wait, let every copy and MMA still in flight land (bounded by
+    // one second each) before the CTA releases its shared and tensor memory
+    if (tid == 0 && pending) {
+        const uint64_t drain_ns = 1000000000ull;
+        if (pending & 1u) (void)mbar_wait(mb_mma, ph_mma, drain_ns);
+        if (pending & 2u) (void)mbar_wait(mb_qku, ph_qku, drain_ns);
+        if (pending & 4u) (void)mbar_wait(mb_v[0], ph_v[0], drain_ns);
+        if (pending & 8u) (void)mbar_wait(mb_v[1], ph_v[1], drain_ns);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------------------------
+// combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1}, 16 value rows per block
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ zsum, float *__restrict__ sstart, int P)
+{
+    __shared__ float S[16][65];
+    __shared__ float M[64][65];
+    const int bh = blockIdx.x, r0 = blockIdx.y * 16, tid = threadIdx.x;
+    for (int e = tid; e < 16 * 64; e += 256) S[e >> 6][e & 63] = 0.f;
+    for (int e = tid; e < 16 * 64; e += 256)
+        sstart[(((size_t)bh * P + 0) * 64 + r0 + (e >> 6)) * 64 + (e & 63)] = 0.f;
+    for (int sp = 1; sp < P; ++sp) {
+        __syncthreads();
+        const float *z = zsum + ((size_t)bh * P + sp - 1) * 128 * 64;
+        for (int e = tid; e < 64 * 64; e += 256) M[e >> 6][e & 63] = z[64 * 64 + e];
+        __syncthreads();
+        float acc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = tid + 256 * q, r = e >> 6, cc = e & 63;
+            float s = z[(r0 + r) * 64 + cc];
+            for (int m = 0; m < 64; ++m) s = fmaf(S[r][m], M[m][cc], s);
+            acc[q] = s;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = tid + 256 * q, r = e >> 6, cc = e & 63;
+            S[r][cc] = acc[q];
+            sstart[(((size_t)bh * P + sp) * 64 + r0 + r) * 64 + cc] = acc[q];
+        }
+    }
+}
+
+// fixup: o = o0 + Qhat S_start^T for the chunks of segments >= 1
+__global__ void __launch_bounds__(256) fixup_kernel(const float *__restrict__ stash_o, const __nv_bfloat16 *__restrict__ stash_q,
+                                                    const float *__restrict__ sstart, void *__restrict__ out, int out_f32,
+                                                    int T, int NC, int P)
+{
+    __shared__ float St[64][65];  // St[m][c] = S_start[c][m]
+    __shared__ float Qh[64][65];
+    const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+    // segment of chunk c: the largest p with begin(p) <= c
+    int seg = (int)(((long long)c * P) / NC);
+    while (seg + 1 < P && ((long long)(seg + 1) * NC) / P <= c) ++seg;
+    while (seg > 0 && ((long long)seg * NC) / P > c) --seg;
+    if (seg == 0) return;
+    const int t0 = c * 64, n = min(64, T - t0);
+    const float *S = sstart + ((size_t)bh * P + seg) * 64 * 64;
+    const size_t chunk = (size_t)bh * NC + c;
+    for (int e = tid; e < 64 * 64; e += 256) {
+        St[e & 63][e >> 6] = S[e];
+        Qh[e >> 6][e & 63] = __bfloat162float(stash_q[chunk * 4096 + e]);
+    }
+    __syncthreads();
+    for (int e = tid; e < 64 * 64; e += 256) {
+        const int i = e >> 6, cc = e & 63;
+        if (i >= n) continue;
+        float s = stash_o[chunk * 4096 + e];
+        for (int m = 0; m < 64; ++m) s = fmaf(Qh[i][m], St[m][cc], s);
+        const size_t o = ((size_t)bh * T + t0 + i) * 64 + cc;
+        if (out_f32)
+            reinterpret_cast<float *>(out)[o] = s;
+        else
+            reinterpret_cast<__nv_bfloat16 *>(out)[o] = __float2bfloat16_rn(s);
+    }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    }
+    return fn;
+}
+
+bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides_bytes,
+            const cuuint32_t *box, CUtensorMapSwizzle sw)
+{
+    auto fn = get_encode();
+    if (!fn) return false;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides_bytes, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_supported(const Shape &s, prism_dtype io)
+{
+    return io == PRISM_BF16 && s.dk == 64 && s.dv == 64 && s.L >= 1 && s.L <= 1 + tc::RMAX;
+}
+
+int tc_segments(const Shape &s, int sm_count, long long opt)
+{
+    int P = opt > 0 ? (int)opt : sm_count / (s.BH > 0 ? s.BH : 1);
+    if (P < 1) P = 1;
+    if (P > s.NC) P = s.NC;
+    return P;
+}
+
+size_t tc_workspace_bytes(const Shape &s, int P)
+{
+    const size_t BH = s.BH, NC = s.NC;
+    return BH * P * 128 * 64 * 4 + BH * P * 64 * 64 * 4 + BH * NC * 4096 * 4 + BH * NC * 4096 * 2 + 4 * 256;
+}
+
+void tc_carve(const Shape &s, int P, void *base, TcWorkspace *w)
+{
+    const size_t BH = s.BH, NC = s.NC;
+    uintptr_t p = ((uintptr_t)base + 255) & ~(uintptr_t)255;
+    w->zsum = (float *)p;
+    p += BH * P * 128 * 64 * 4;
+    p = (p + 255) & ~(uintptr_t)255;
+    w->sstart = (float *)p;
+    p += BH * P * 64 * 64 * 4;
+    p = (p + 255) & ~(uintptr_t)255;
+    w->stash_o = (float *)p;
+    p += BH * NC * 4096 * 4;
+    p = (p + 255) & ~(uintptr_t)255;
+    w->stash_q = (__nv_bfloat16 *)p;
+    w->P = P;
+}
+
+cudaError_t tc_prepare()
+{
+    return cudaFuncSetAttribute(tc::segment_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES);
+}
+
+cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const TcWorkspace &w, int *d_status,
+                       long long wait_ns, KernelTimer &tm)
+{
+    using namespace tc;
+    CUtensorMap mq, mk, mv, mu;
+    const cuuint64_t BH = s.BH, T = s.T;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)D, T, BH};
+        cuuint64_t str[2] = {(cuuint64_t)D * 2, T * D * 2};
+        cuuint32_t box[3] = {64, 64, 1};
+        if (!encode(&mq, a.q, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!encode(&mk, a.k, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        cuuint32_t vbox[3] = {64, 72, 1};
+        if (!encode(&mv, a.v, 3, dims, str, vbox, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+    }
+    if (s.R > 0) {
+        cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)s.R, T, BH};
+        cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)s.R * D * 2, T * s.R * D * 2};
+        cuuint32_t box[4] = {64, 1, 64, 1};
+        if (!encode(&mu, a.u, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    } else {
+        mu = mk;  // never read with L = 1
+    }
+    SegParams p;
+    p.beta = a.beta;
+    p.alpha = a.alpha;
+    p.gamma = a.gamma;
+    p.eta = a.eta;
+    p.conv_w = (const __nv_bfloat16 *)a.conv_w;
+    p.out = a.out;
+    p.out_f32 = out_f32 ? 1 : 0;
+    p.zsum = w.zsum;
+    p.stash_o = w.stash_o;
+    p.stash_q = w.stash_q;
+    p.status = d_status;
+    p.H = s.H;
+    p.T = s.T;
+    p.R = s.R;
+    p.NC = s.NC;
+    p.P = w.P;
+    p.wait_ns = wait_ns > 0 ? (unsigned long long)wait_ns : 100000000ull;
+    cudaStream_t st = tm.stream;
+    tm.begin("tc_segment");
+    segment_kernel<<<s.BH * w.P, NT, SMEM_BYTES, st>>>(mq, mk, mv, mu, p);
+    tm.end();
+    if (w.P > 1) {
+        tm.begin("tc_combine");
+        combine_kernel<<<dim3(s.BH, 4), 256, 0, st>>>(w.zsum, w.sstart, w.P);
+        tm.end();
+        tm.begin("tc_fixup");
+        fixup_kernel<<<dim3(s.NC, s.BH), 256, 0, st>>>(w.stash_o, w.stash_q, w.sstart, a.out, p.out_f32, s.T, s.NC,
+                                                        w.P);
+        tm.end();
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace prism

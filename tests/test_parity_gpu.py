@@ -1,0 +1,200 @@
+"""GPU parity: prism_forward (through the C ABI) against the fp64 oracle, element by
+element on the same seeded inputs.
+
+Bars (max |o - o_ref| / rms(o_ref) over the compared outputs): 1e-4 for float32
+io (fp32 arithmetic), 2e-2 for bfloat16 io (bf16 tensor-core operands, fp32
+accumulation).  The oracle consumes the bf16-rounded inputs upcast to fp64, so
+the error measured is the kernels' own.
+"""
+import numpy as np
+import pytest
+import torch
+
+from ssm_sequence_layer_gb300 import binding as B
+from ssm_sequence_layer_gb300 import build
+from ssm_sequence_layer_gb300.inputs import WORKLOADS, make_inputs, make_workload_inputs, select_heads
+from tests.gpu_util import TOL, gpu_forward, io_of, oracle_forward, rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+# ------------------------------------------------------------------------------------------------
+# the five named workloads at their full sizes
+@pytest.mark.parametrize("name", ["tiny_fp32", "gdn_degenerate", "lm130m_layer", "seqrec_16k"])
+def test_workload_parity_full(oracle_mod, name):
+    w = WORKLOADS[name]
+    inp = make_workload_inputs(w)
+    out = gpu_forward(inp)
+    ref = oracle_forward(oracle_mod, inp)["out"]
+    err = rel_err(out, ref)
+    print(f"{name}: rel err {err:.3e}")
+    assert err <= TOL[w.dtype]
+
+
+def test_long_memory_workload_sampled_heads(oracle_mod):
+    """64K tokens x 16 heads x L = 8: the oracle recomputes three whole heads."""
+    w = WORKLOADS["long_64k"]
+    inp = make_workload_inputs(w)
+    out = gpu_forward(inp)
+    heads = [(0, 0), (0, 7), (0, 15)]
+    ref = oracle_forward(oracle_mod, select_heads(inp, heads))["out"][0]
+    got = np.stack([out[b, h] for b, h in heads])
+    err = rel_err(got, ref)
+    print(f"long_64k sampled heads: rel err {err:.3e}")
+    assert err <= TOL[w.dtype]
+    assert np.all(np.isfinite(out))
+
+
+# ------------------------------------------------------------------------------------------------
+# edge shapes: ragged tails, a single token, one sequence, every (dk, dv), L in {1, 2, 8}
+EDGE = [
+    # (B, H, T, dk, dv, L, dtype)
+    (1, 1, 1, 64, 64, 1, "f32"),
+    (1, 1, 3, 64, 64, 2, "f32"),
+    (1, 1, 4, 64, 128, 8, "f32"),
+    (1, 2, 63, 128, 64, 2, "f32"),
+    (2, 1, 64, 64, 64, 8, "f32"),
+    (1, 1, 65, 128, 128, 1, "f32"),
+    (1, 2, 130, 64, 64, 3, "f32"),
+    (1, 1, 1, 128, 128, 8, "bf16"),
+    (1, 1, 65, 64, 128, 2, "bf16"),
+    (2, 2, 130, 128, 64, 8, "bf16"),
+    (1, 1, 257, 64, 64, 16, "bf16"),
+    (3, 1, 200, 128, 128, 4, "bf16"),
+]
+
+
+@pytest.mark.parametrize("B_,H,T,dk,dv,L,dt", EDGE)
+def test_edge_shapes(oracle_mod, B_, H, T, dk, dv, L, dt):
+    inp = make_inputs(B_, H, T, dk, dv, L, dtype=dt, seed=100 + T + L)
+    out = gpu_forward(inp)
+    ref = oracle_forward(oracle_mod, inp)["out"]
+    assert rel_err(out, ref) <= TOL[dt]
+
+
+def test_long_memory_decay_small_case(oracle_mod):
+    inp = make_inputs(1, 2, 1000, 64, 64, 4, dtype="f32", seed=5, alpha_div=64.0)
+    assert rel_err(gpu_forward(inp), oracle_forward(oracle_mod, inp)["out"]) <= TOL["f32"]
+
+
+# ------------------------------------------------------------------------------------------------
+# special cases of the method
+def test_zero_write_gates_give_exact_zero():
+    inp = make_inputs(1, 2, 150, 64, 64, 3, dtype="bf16", seed=7)
+    inp["beta"].zero_()
+    inp["gamma"].zero_()
+    out = gpu_forward(inp)
+    assert np.all(out == 0.0)
+
+
+def test_last_eta_slot_is_not_read(oracle_mod):
+    inp = make_inputs(1, 2, 100, 64, 64, 4, dtype="f32", seed=8)
+    ref = gpu_forward(inp)
+    inp["eta"][..., -1] = float("nan")
+    out = gpu_forward(inp)
+    assert np.array_equal(out, ref)
+
+
+def test_gdn_degenerate_matches_delta_rule_loop():
+    """L = 1 against an independent delta-rule loop (fp64, torch on the CPU)."""
+    inp = make_inputs(1, 1, 70, 64, 64, 1, dtype="f32", seed=9)
+    q, k, v = (inp[n][0, 0].double() for n in ("q", "k", "v"))
+    be, al = inp["beta"][0, 0].double(), inp["alpha"][0, 0].double()
+    S = torch.zeros(64, 64, dtype=torch.float64)
+    ref = []
+    for t in range(70):
+        S = al[t] * S + be[t] * torch.outer(v[t] - al[t] * S @ k[t], k[t])
+        ref.append(S @ q[t])
+    ref = torch.stack(ref).numpy()
+    assert rel_err(gpu_forward(inp)[0, 0], ref) <= TOL["f32"]
+
+
+def test_sequences_in_a_batch_are_independent():
+    inp = make_inputs(3, 2, 90, 64, 64, 3, dtype="bf16", seed=10)
+    full = gpu_forward(inp)
+    one = {k: (v[1:2] if torch.is_tensor(v) and k != "conv_w" else v) for k, v in inp.items()}
+    part = gpu_forward(one)
+    assert rel_err(part[0], full[1]) <= 1e-6
+
+
+def test_bitwise_deterministic():
+    inp = make_inputs(2, 2, 300, 128, 128, 4, dtype="bf16", seed=11)
+    d = to_device(inp)
+    with B.Plan.for_inputs(d) as p:
+        a = p.forward(d)
+        b = p.forward(d)
+        torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------------------------------------
+# the two GPU paths, segment counts and output dtypes
+@pytest.mark.parametrize("T,L", [(64, 1), (200, 2), (1000, 4), (4097, 3)])
+def test_tensor_core_path_matches_portable_path(T, L):
+    inp = make_inputs(2, 2, T, 64, 64, L, dtype="bf16", seed=20 + L)
+    tc = gpu_forward(inp, path=2)
+    pt = gpu_forward(inp, path=1)
+    assert rel_err(tc, pt) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("segments", [1, 2, 3, 7, 16])
+def test_segment_count_invariance(oracle_mod, segments):
+    inp = make_inputs(1, 2, 1000, 64, 64, 4, dtype="bf16", seed=30)
+    ref = oracle_forward(oracle_mod, inp)["out"]
+    out = gpu_forward(inp, path=2, segments=segments)
+    assert rel_err(out, ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_bf16_output_is_the_rounded_fp32_output(path):
+    inp = make_inputs(1, 2, 300, 64, 64, 3, dtype="bf16", seed=31)
+    d = to_device(inp)
+    with B.Plan.for_inputs(d, path=path, out="f32") as p32, B.Plan.for_inputs(d, path=path) as p16:
+        o32 = p32.forward(d)
+        o16 = p16.forward(d)
+        torch.cuda.synchronize()
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+
+
+def test_host_entry_point_matches_device_entry_point():
+    inp = make_inputs(1, 2, 200, 64, 64, 3, dtype="bf16", seed=12)
+    d = to_device(inp)
+    with B.Plan.for_inputs(d) as p:
+        dev = p.forward(d).cpu()
+        host_in = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in inp.items()}
+        host = p.forward_host(host_in)
+    assert torch.equal(dev, host)
+
+
+# ------------------------------------------------------------------------------------------------
+# argument errors on a real device
+def test_misaligned_tensor_is_rejected():
+    inp = to_device(make_inputs(1, 1, 64, 64, 64, 2, dtype="bf16", seed=13))
+    with B.Plan.for_inputs(inp) as p:
+        buf = torch.empty(inp["q"].numel() + 8, dtype=torch.bfloat16, device="cuda")
+        shifted = buf[1:1 + inp["q"].numel()].view_as(inp["q"])   # 2-byte offset
+        bad = dict(inp, q=shifted)
+        with pytest.raises(B.PrismError) as ei:
+            p.forward(bad)
+        assert ei.value.status == B.PRISM_ERR_MISALIGNED
+
+
+def test_wrong_L_is_rejected():
+    inp = to_device(make_inputs(1, 1, 64, 64, 64, 3, dtype="bf16", seed=14))
+    with B.Plan(1, 1, 64, 64, 64, 2, io="bf16") as p:
+        with pytest.raises(B.PrismError) as ei:
+            p.forward(inp)
+        assert ei.value.status == B.PRISM_ERR_INVALID_ARG
+
+
+def test_plan_reports_workspace_and_clean_status():
+    with B.Plan(2, 2, 1000, 64, 64, 4) as p:
+        assert p.workspace_bytes() > 0
+        p.last_device_status()
