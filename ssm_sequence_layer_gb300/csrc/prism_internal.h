@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -71,7 +72,7 @@ struct TcWorkspace {
     float *zsum;             // [BH][P][128][64]  segment maps Z = [N; M]
     float *sstart;           // [BH][P][64][64]   state entering each segment
     float *stash_o;          // [BH][NC][64][64]  o0 per chunk (segments >= 1)
-    __nv_bfloat16 *stash_q;  // [BH][NC][64][64]  Qhat per chunk (segments >= 1)
+    __half *stash_q;         // [BH][NC][64][64]  Qhat per chunk (segments >= 1)
     int P;                   // segments per sequence
 };
 

@@ -15,21 +15,27 @@
 //   fixup    o = o0 + Qhat S_start^T for the chunks of segments >= 1.
 //
 // Chunk algebra (local index i, j; lambda_i = sum_{m<=i} ln alpha_m; lc = lambda_{C-1};
-// e^{x} factors are taken relative to the chunk end so that every stored factor is <= 1
-// or is a row factor e^{lambda_i - lc} >= 1 bounded by the chunk's total decay):
-//   A_ij  = beta_i e^{lambda_i - lambda_j} k_i.k_j           (j < i)   -> T = (I + A)^{-1}
-//   PK_l  = beta_i e^{lambda_i - lc} k_i.u_{j,l}              (j < i)
-//   PQ_l  = e^{lambda_i - lc} q_i.u_{j,l},   G = e^{lambda_i - lc} q_i.k_j   (j <= i)
-//   Xs_l  = e^{lc - lambda_j} x_{j,l}                          (x = gamma g (.) r, the prep)
-//   RHS   = diag(beta) V - sum_l PK_l Xs_l
-//   [U'^T; W^T] = [RHS | diag(beta Gamma) K]^T T^T              (Gamma_i = e^{lambda_i})
-//   UWs   = [U'^T; W^T] diag(e^{lc - lambda_j})
-//   D4    = UWs G^T + [Xs^T; 0] PQ^T  = [O_loc^T ; (G~ W)^T]    (G~ = Q K^T o D, D incl. diag)
-//   D5    = UWs [K] + [Xs^T; 0] [U]   = [N_c ; W^T K']
+// rowf_i = e^{lambda_i - lc} >= 1, colf_j = e^{lc - lambda_j} <= 1, Gamma_i = e^{lambda_i}):
+//   A_ij  = beta_i rowf_i colf_j k_i.k_j            (j < i)   -> T = (I + A)^{-1}   (fp32 solve)
+//   PK_l  = k_i.u_{j,l} (j < i);  PQ_l = q_i.u_{j,l}, G = q_i.k_j (j <= i)      (unscaled scores)
+//   Xs_l  = colf_j x_{j,l}                             (x = gamma g (.) r, the prep)
+//   RHS   = diag(beta) V - diag(beta rowf) sum_l PK_l Xs_l
+//   [U'^T; W^T] = [RHS | diag(beta Gamma) K]^T T^T
+//   UWs   = [U'^T; W^T] diag(colf)
+//   D4    = (UWs G^T + [Xs^T; 0] PQ^T) diag(rowf) = [O_loc^T ; (G~ W)^T]   (G~ = Q K^T o D)
+//   D5    = UWs K + [Xs^T; 0] U         = [N_c ; W^T K']
 //   Qt    = Q~^T = diag(Gamma) Q^T - (G~ W)^T,   M_c = Gamma_C I - W^T K'
 //   Z    <- Z M_c + [N_c; 0],   [o0^T ; Qhat^T] = Z Qt + [O_loc^T ; 0]   (Z before the update)
-// All matrix products above run on tcgen05.mma (bf16 operands in 128B-swizzled shared memory,
-// fp32 accumulators in tensor memory); operands come from TMA or from the epilogues.
+// The decay factors of every masked product multiply to e^{lambda_i - lambda_j} <= 1; a
+// chunk whose total decay exceeds 80 nats (rowf would leave fp32 range) sets the status word.
+// All matrix products above run on tcgen05.mma (fp16 operands in 128B-swizzled shared memory,
+// fp32 accumulators in tensor memory); operands come from TMA or from the epilogues.  The bf16
+// input tiles are converted to fp16 in place (exact for unit-scale rows): fp16's 10-bit
+// mantissa keeps the computed operands (scores, Xs, T, U'/W, Q~, M_c, Z) 8x closer to fp32
+// than bf16 would, at the same tensor-core rate.  Row factors >= 1 (e^{lambda_i - lc},
+// beta_i) are kept out of the operands and applied to the accumulators in the epilogues, so
+// every fp16 operand stays of order one.
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "prism_internal.h"
@@ -76,7 +82,7 @@ struct SegParams {
     void *out;              // bf16, or fp32 when out_f32
     float *zsum;            // [BH][P][128][64]
     float *stash_o;         // [BH][NC][64][64]  o0 (token-major)
-    __nv_bfloat16 *stash_q; // [BH][NC][64][64]  Qhat (token-major)
+    __half *stash_q;        // [BH][NC][64][64]  Qhat (token-major)
     int *status;
     int H, T, R, NC, P;
     int out_f32;
@@ -87,11 +93,11 @@ __device__ __forceinline__ void set_status(int *st, int code) { atomicCAS(st, 0,
 
 __device__ __forceinline__ uint32_t pack2(float a, float b)
 {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// write 32 consecutive fp32 values (columns col0..col0+31 of row `row`) as bf16 into a
+// write 32 consecutive fp32 values (columns col0..col0+31 of row `row`) as fp16 into a
 // [rows][64] SW128 tile
 __device__ __forceinline__ void st_row32(uint8_t *tile, int row, int col0, const float (&v)[32])
 {
@@ -106,9 +112,25 @@ __device__ __forceinline__ void st_row32(uint8_t *tile, int row, int col0, const
     }
 }
 
-__device__ __forceinline__ float ld_bf(const uint8_t *tile, int row, int col)
+__device__ __forceinline__ float ld_h(const uint8_t *tile, int row, int col)
 {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128(row, col)));
+    return __half2float(*reinterpret_cast<const __half *>(tile + sw128(row, col)));
+}
+
+// in-place bf16 -> fp16 conversion of `bytes` bytes of tiles (layout unchanged)
+__device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes, int tid)
+{
+    for (uint32_t e = tid; e < bytes / 16; e += NT) {
+        uint4 w = reinterpret_cast<uint4 *>(base)[e];
+        uint32_t *pw = &w.x;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&pw[q]);
+            const float2 f = __bfloat1622float2(b);
+            pw[q] = pack2(f.x, f.y);
+        }
+        reinterpret_cast<uint4 *>(base)[e] = w;
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -164,7 +186,7 @@ __global__ void __launch_bounds__(NT, 1)
     for (int e = tid; e < 128 * 64; e += NT) {
         const int r = e >> 6, m = e & 63;
         const float z = (seg > 0 && r >= 64 && (r - 64) == m) ? 1.f : 0.f;
-        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_ZA + sw128(r, m)) = __float2bfloat16_rn(z);
+        *reinterpret_cast<__half *>(sm + OFF_ZA + sw128(r, m)) = __float2half_rn(z);
     }
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 512);
     fence_async_smem();
@@ -278,7 +300,7 @@ __global__ void __launch_bounds__(NT, 1)
                 float r = v0 - a * Phi;
                 for (int l = 0; l < R; ++l) {
                     const float x = s_gc[i * RMAX + l] * g * r;
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_XS + l * TILE + sw128(i, ch)) = __float2bfloat16_rn(x);
+                    *reinterpret_cast<__half *>(sm + OFF_XS + l * TILE + sw128(i, ch)) = __float2half_rn(x);
                     r *= 1.f - s_eta[i * RMAX + l] * g;
                 }
             }
@@ -288,13 +310,16 @@ __global__ void __launch_bounds__(NT, 1)
 
         // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T ----------------------------------------------
         if (!wait_all(mb_qku, ph_qku, 2u)) break;
+        tiles_bf16_to_f16(sm + OFF_Q, (2 + R) * TILE, tid);
+        fence_async_smem();
+        __syncthreads();
         const int N1 = 64 * (1 + R);
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t id = idesc_bf16(128, N1, 0, 0);
+            const uint32_t id = idesc_f16(128, N1, 0, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + TM_D1, sdesc(sbase + OFF_Q + s * 32, 16, 1024), sdesc(sbase + OFF_K + s * 32, 16, 1024),
+                mma_f16(tmem + TM_D1, sdesc(sbase + OFF_Q + s * 32, 16, 1024), sdesc(sbase + OFF_K + s * 32, 16, 1024),
                          id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
@@ -316,7 +341,7 @@ __global__ void __launch_bounds__(NT, 1)
                 const int j0 = half * 32;
                 if (qside) {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] = (j0 + q <= i) ? v[q] * rf : 0.f;
+                    for (int q = 0; q < 32; ++q) v[q] = (j0 + q <= i) ? v[q] : 0.f;
                     uint8_t *tile = sm + (blk == 0 ? OFF_G : OFF_E + (blk - 1) * 2 * TILE + TILE);
                     st_row32(tile, i, j0, v);
                 } else if (blk == 0) {
@@ -325,7 +350,7 @@ __global__ void __launch_bounds__(NT, 1)
                     for (int q = 0; q < 32; ++q) A[i * LDA + j0 + q] = (j0 + q < i) ? v[q] * bi * rf * s_colf[j0 + q] : 0.f;
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] = (j0 + q < i) ? v[q] * bi * rf : 0.f;
+                    for (int q = 0; q < 32; ++q) v[q] = (j0 + q < i) ? v[q] : 0.f;
                     st_row32(sm + OFF_E + (blk - 1) * 2 * TILE, i, j0, v);
                 }
             }
@@ -337,11 +362,11 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- P3: MX = sum_l PK_l Xs_l (MMA, in flight) while the CTA solves T = (I + A)^{-1} -------
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t id = idesc_bf16(128, 64, 0, 1);
+            const uint32_t id = idesc_f16(128, 64, 0, 1);
             for (int l = 0; l < R; ++l)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_bf16(tmem + TM_D2, sdesc(sbase + OFF_E + l * 2 * TILE + s * 32, 16, 1024),
+                    mma_f16(tmem + TM_D2, sdesc(sbase + OFF_E + l * 2 * TILE + s * 32, 16, 1024),
                              sdesc(sbase + OFF_XS + l * TILE + s * 2048, TILE, 1024), id, (l | s) != 0);
             mma_commit(mb_mma);
             pending |= 1u;
@@ -410,10 +435,15 @@ __global__ void __launch_bounds__(NT, 1)
             if (quad < 2) {  // lanes 0..63 hold MX rows
                 const int i = row, j0 = half * 32;
                 float v[32];
-                tmem_ld32(tmem + TM_D2 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
-                const float bi = s_beta[i];
+                if (R > 0) {
+                    tmem_ld32(tmem + TM_D2 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+                } else {
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] = bi * __bfloat162float(vb[(i + 8) * 64 + j0 + q]) - v[q];
+                    for (int q = 0; q < 32; ++q) v[q] = 0.f;  // no levels: M X = 0 (D2 is never written)
+                }
+                const float bi = s_beta[i], brf = s_beta[i] * s_rowf[i];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = bi * __bfloat162float(vb[(i + 8) * 64 + j0 + q]) - brf * v[q];
                 st_row32(sm + OFF_AKK, i, j0, v);  // RHS tile (A is dead after the solve)
             } else {
                 const int tt = (half ? 64 : 0) + (tid & 63);  // 0..127 over the warps of quads 2, 3
@@ -421,7 +451,7 @@ __global__ void __launch_bounds__(NT, 1)
                 float v[32];
                 const float s = s_bg[j];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] = s * ld_bf(sm + OFF_K, j, m0 + q);
+                for (int q = 0; q < 32; ++q) v[q] = s * ld_h(sm + OFF_K, j, m0 + q);
                 st_row32(sm + OFF_AKK + TILE, j, m0, v);  // BGK tile
             }
         }
@@ -432,10 +462,10 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- P4: [U'^T ; W^T] = [RHS | BGK]^T T^T -------------------------------------------------
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t id = idesc_bf16(128, 64, 1, 0);
+            const uint32_t id = idesc_f16(128, 64, 1, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + TM_D3, sdesc(sbase + OFF_AKK + s * 2048, TILE, 1024), sdesc(sbase + OFF_TB + s * 32, 16, 1024),
+                mma_f16(tmem + TM_D3, sdesc(sbase + OFF_AKK + s * 2048, TILE, 1024), sdesc(sbase + OFF_TB + s * 32, 16, 1024),
                          id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
@@ -461,21 +491,21 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- P5: D4 = UWs [G; PQ]^T-part, D5 = UWs [K; U]-part ------------------------------------
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t idk = idesc_bf16(128, 64, 0, 0), idx = idesc_bf16(128, 64, 1, 0);
-            const uint32_t idk5 = idesc_bf16(128, 64, 0, 1), idx5 = idesc_bf16(128, 64, 1, 1);
+            const uint32_t idk = idesc_f16(128, 64, 0, 0), idx = idesc_f16(128, 64, 1, 0);
+            const uint32_t idk5 = idesc_f16(128, 64, 0, 1), idx5 = idesc_f16(128, 64, 1, 1);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint64_t a = sdesc(sbase + OFF_AKK + s * 32, 16, 1024);
-                mma_bf16(tmem + TM_D4, a, sdesc(sbase + OFF_G + s * 32, 16, 1024), idk, s > 0);
-                mma_bf16(tmem + TM_D5, a, sdesc(sbase + OFF_K + s * 2048, TILE, 1024), idk5, s > 0);
+                mma_f16(tmem + TM_D4, a, sdesc(sbase + OFF_G + s * 32, 16, 1024), idk, s > 0);
+                mma_f16(tmem + TM_D5, a, sdesc(sbase + OFF_K + s * 2048, TILE, 1024), idk5, s > 0);
             }
             for (int l = 0; l < R; ++l) {
                 const uint32_t xs = OFF_XS + l * TILE;
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
                     const uint64_t a = sdesc(sbase + xs + s * 2048, OFF_ZERO - xs, 1024);
-                    mma_bf16(tmem + TM_D4, a, sdesc(sbase + OFF_E + l * 2 * TILE + TILE + s * 32, 16, 1024), idx, 1);
-                    mma_bf16(tmem + TM_D5, a, sdesc(sbase + OFF_U + l * TILE + s * 2048, TILE, 1024), idx5, 1);
+                    mma_f16(tmem + TM_D4, a, sdesc(sbase + OFF_E + l * 2 * TILE + TILE + s * 32, 16, 1024), idx, 1);
+                    mma_f16(tmem + TM_D5, a, sdesc(sbase + OFF_U + l * TILE + s * 2048, TILE, 1024), idx5, 1);
                 }
             }
             mma_commit(mb_mma);
@@ -490,7 +520,7 @@ __global__ void __launch_bounds__(NT, 1)
             float v[32];
             tmem_ld32(tmem + TM_D4 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = s_gam[j0 + q] * ld_bf(sm + OFF_Q, j0 + q, m) - v[q];
+            for (int q = 0; q < 32; ++q) v[q] = s_gam[j0 + q] * ld_h(sm + OFF_Q, j0 + q, m) - s_rowf[j0 + q] * v[q];
             st_row32(sm + OFF_E, m, j0, v);  // Qt [m][i]
             tmem_ld32(tmem + TM_D5 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
             const float gC = __expf(lc);
@@ -505,12 +535,12 @@ __global__ void __launch_bounds__(NT, 1)
             fence_after_sync();
             if (c + 1 < c_end) issue_qku(c + 1);  // Q, K, U of this chunk are no longer read
             // ---- P6: D6 = Z Mc, D7 = Z Qt ------------------------------------------------------
-            const uint32_t id = idesc_bf16(128, 64, 0, 1);
+            const uint32_t id = idesc_f16(128, 64, 0, 1);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint64_t a = sdesc(sbase + OFF_ZA + s * 32, 16, 1024);
-                mma_bf16(tmem + TM_D6, a, sdesc(sbase + OFF_E + TILE + s * 2048, TILE, 1024), id, s > 0);
-                mma_bf16(tmem + TM_D7, a, sdesc(sbase + OFF_E + s * 2048, TILE, 1024), id, s > 0);
+                mma_f16(tmem + TM_D6, a, sdesc(sbase + OFF_E + TILE + s * 2048, TILE, 1024), id, s > 0);
+                mma_f16(tmem + TM_D7, a, sdesc(sbase + OFF_E + s * 2048, TILE, 1024), id, s > 0);
             }
             mma_commit(mb_mma);
             pending |= 1u;
@@ -542,11 +572,13 @@ __global__ void __launch_bounds__(NT, 1)
             // outputs: row < 64 -> o0^T[c][i] = D7 + O_loc^T ; row >= 64 -> Qhat^T[m][i]
             if (row < 64) {
                 const int cc = row;
+                bool finite = true;
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int i = j0 + q;
                     if (i < n) {
-                        const float val = o[q] + ol[q];
+                        const float val = o[q] + s_rowf[i] * ol[q];
+                        finite = finite && isfinite(val);
                         if (seg == 0) {
                             if (p.out_f32)
                                 reinterpret_cast<float *>(p.out)[(tok0 + i) * D + cc] = val;
@@ -556,11 +588,12 @@ __global__ void __launch_bounds__(NT, 1)
                             p.stash_o[(((size_t)bh * p.NC + c) * 64 + i) * 64 + cc] = val;
                     }
                 }
+                if (!finite) set_status(p.status, kDevBounds);  // outside the fp16 operand range
             } else if (seg > 0) {
                 const int m = row - 64;
 #pragma unroll
                 for (int q = 0; q < 32; ++q)
-                    p.stash_q[(((size_t)bh * p.NC + c) * 64 + j0 + q) * 64 + m] = __float2bfloat16_rn(o[q]);
+                    p.stash_q[(((size_t)bh * p.NC + c) * 64 + j0 + q) * 64 + m] = __float2half_rn(o[q]);
             }
         }
         fence_async_smem();
@@ -584,45 +617,67 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1}, 16 value rows per block
+// combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} (fp32), 8 value rows per block; the map
+// of the next segment is prefetched into registers while the current step computes
+constexpr int CB_ROWS = 8;
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ zsum, float *__restrict__ sstart, int P)
 {
-    __shared__ float S[16][65];
-    __shared__ float M[64][65];
-    const int bh = blockIdx.x, r0 = blockIdx.y * 16, tid = threadIdx.x;
-    for (int e = tid; e < 16 * 64; e += 256) S[e >> 6][e & 63] = 0.f;
-    for (int e = tid; e < 16 * 64; e += 256)
-        sstart[(((size_t)bh * P + 0) * 64 + r0 + (e >> 6)) * 64 + (e & 63)] = 0.f;
+    __shared__ __align__(16) float M[2][64][68];
+    __shared__ float S[CB_ROWS][68];
+    const int bh = blockIdx.x, r0 = blockIdx.y * CB_ROWS, tid = threadIdx.x;
+    const int r = tid >> 5, c0 = tid & 31;  // outputs (r, c0) and (r, c0 + 32)
+    S[r][c0] = 0.f;
+    S[r][c0 + 32] = 0.f;
+    float *dst0 = sstart + ((size_t)bh * P * 64 + r0 + r) * 64;
+    dst0[c0] = 0.f;
+    dst0[c0 + 32] = 0.f;
+    if (P < 2) return;
+    // M_{p-1} is rows 64..127 of segment p-1's map; each thread moves 4 float4 of it
+    float4 pre[4];
+    auto load_m = [&](int sp) {
+        const float4 *src = reinterpret_cast<const float4 *>(zsum + ((size_t)bh * P + sp) * 128 * 64 + 64 * 64);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) pre[q] = src[tid + 256 * q];
+    };
+    auto store_m = [&](int buf) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = (tid + 256 * q) * 4;
+            *reinterpret_cast<float4 *>(&M[buf][e >> 6][e & 63]) = pre[q];
+        }
+    };
+    load_m(0);
+    store_m(0);
+    __syncthreads();
     for (int sp = 1; sp < P; ++sp) {
-        __syncthreads();
-        const float *z = zsum + ((size_t)bh * P + sp - 1) * 128 * 64;
-        for (int e = tid; e < 64 * 64; e += 256) M[e >> 6][e & 63] = z[64 * 64 + e];
-        __syncthreads();
-        float acc[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = tid + 256 * q, r = e >> 6, cc = e & 63;
-            float s = z[(r0 + r) * 64 + cc];
-            for (int m = 0; m < 64; ++m) s = fmaf(S[r][m], M[m][cc], s);
-            acc[q] = s;
+        const int buf = (sp - 1) & 1;
+        if (sp + 1 < P) load_m(sp);  // map of segment sp, used at step sp + 1
+        const float *N = zsum + ((size_t)bh * P + sp - 1) * 128 * 64 + (size_t)(r0 + r) * 64;
+        float a0 = N[c0], a1 = N[c0 + 32];
+#pragma unroll 16
+        for (int m = 0; m < 64; ++m) {
+            const float sv = S[r][m];
+            a0 = fmaf(sv, M[buf][m][c0], a0);
+            a1 = fmaf(sv, M[buf][m][c0 + 32], a1);
         }
         __syncthreads();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = tid + 256 * q, r = e >> 6, cc = e & 63;
-            S[r][cc] = acc[q];
-            sstart[(((size_t)bh * P + sp) * 64 + r0 + r) * 64 + cc] = acc[q];
-        }
+        S[r][c0] = a0;
+        S[r][c0 + 32] = a1;
+        float *dst = sstart + (((size_t)bh * P + sp) * 64 + r0 + r) * 64;
+        dst[c0] = a0;
+        dst[c0 + 32] = a1;
+        if (sp + 1 < P) store_m(buf ^ 1);
+        __syncthreads();
     }
 }
 
-// fixup: o = o0 + Qhat S_start^T for the chunks of segments >= 1
-__global__ void __launch_bounds__(256) fixup_kernel(const float *__restrict__ stash_o, const __nv_bfloat16 *__restrict__ stash_q,
+// fixup: o = o0 + Qhat S_start^T for the chunks of segments >= 1; 4x4 outputs per thread
+__global__ void __launch_bounds__(256) fixup_kernel(const float *__restrict__ stash_o, const __half *__restrict__ stash_q,
                                                     const float *__restrict__ sstart, void *__restrict__ out, int out_f32,
                                                     int T, int NC, int P)
 {
-    __shared__ float St[64][65];  // St[m][c] = S_start[c][m]
-    __shared__ float Qh[64][65];
+    __shared__ __align__(16) float St[64][68];  // St[m][c] = S_start[c][m]
+    __shared__ __align__(16) float Qt[64][68];  // Qt[m][i] = Qhat[i][m]
     const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     // segment of chunk c: the largest p with begin(p) <= c
     int seg = (int)(((long long)c * P) / NC);
@@ -634,19 +689,45 @@ __global__ void __launch_bounds__(256) fixup_kernel(const float *__restrict__ st
     const size_t chunk = (size_t)bh * NC + c;
     for (int e = tid; e < 64 * 64; e += 256) {
         St[e & 63][e >> 6] = S[e];
-        Qh[e >> 6][e & 63] = __bfloat162float(stash_q[chunk * 4096 + e]);
+        Qt[e & 63][e >> 6] = __half2float(stash_q[chunk * 4096 + e]);
     }
     __syncthreads();
-    for (int e = tid; e < 64 * 64; e += 256) {
-        const int i = e >> 6, cc = e & 63;
+    const int i0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const float4 o = *reinterpret_cast<const float4 *>(stash_o + (chunk * 64 + i0 + a) * 64 + c0);
+        acc[a][0] = o.x;
+        acc[a][1] = o.y;
+        acc[a][2] = o.z;
+        acc[a][3] = o.w;
+    }
+#pragma unroll 8
+    for (int m = 0; m < 64; ++m) {
+        const float4 qa = *reinterpret_cast<const float4 *>(&Qt[m][i0]);
+        const float4 sb = *reinterpret_cast<const float4 *>(&St[m][c0]);
+        const float qv[4] = {qa.x, qa.y, qa.z, qa.w}, sv[4] = {sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qv[a], sv[b], acc[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int i = i0 + a;
         if (i >= n) continue;
-        float s = stash_o[chunk * 4096 + e];
-        for (int m = 0; m < 64; ++m) s = fmaf(Qh[i][m], St[m][cc], s);
-        const size_t o = ((size_t)bh * T + t0 + i) * 64 + cc;
-        if (out_f32)
-            reinterpret_cast<float *>(out)[o] = s;
-        else
-            reinterpret_cast<__nv_bfloat16 *>(out)[o] = __float2bfloat16_rn(s);
+        const size_t o = ((size_t)bh * T + t0 + i) * 64 + c0;
+        if (out_f32) {
+            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + o) =
+                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[a][0], acc[a][1]);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[a][2], acc[a][3]);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t *>(&lo);
+            w.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + o) = w;
+        }
     }
 }
 
@@ -714,7 +795,7 @@ void tc_carve(const Shape &s, int P, void *base, TcWorkspace *w)
     w->stash_o = (float *)p;
     p += BH * NC * 4096 * 4;
     p = (p + 255) & ~(uintptr_t)255;
-    w->stash_q = (__nv_bfloat16 *)p;
+    w->stash_q = (__half *)p;
     w->P = P;
 }
 
@@ -770,7 +851,7 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
     tm.end();
     if (w.P > 1) {
         tm.begin("tc_combine");
-        combine_kernel<<<dim3(s.BH, 4), 256, 0, st>>>(w.zsum, w.sstart, w.P);
+        combine_kernel<<<dim3(s.BH, 64 / CB_ROWS), 256, 0, st>>>(w.zsum, w.sstart, w.P);
         tm.end();
         tm.begin("tc_fixup");
         fixup_kernel<<<dim3(s.NC, s.BH), 256, 0, st>>>(w.stash_o, w.stash_q, w.sstart, a.out, p.out_f32, s.T, s.NC,
