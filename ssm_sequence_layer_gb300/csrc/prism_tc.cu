@@ -41,6 +41,24 @@
 #include "prism_internal.h"
 #include "tc_ptx.h"
 
+// Developer tracing: with -DPRISM_PHASE_TIMERS the segment kernel accumulates clock64()
+// cycles per phase of its chunk loop (thread 0 of every CTA) into prism_tc_phase_cycles.
+#ifdef PRISM_PHASE_TIMERS
+__device__ unsigned long long prism_tc_phase_cycles[16];
+#define PHASE_MARK(k)                                         \
+    do {                                                      \
+        if (threadIdx.x == 0) {                               \
+            const long long now_ = clock64();                 \
+            ph_acc[k] += (unsigned long long)(now_ - ph_last); \
+            ph_last = now_;                                   \
+        }                                                     \
+    } while (0)
+#else
+#define PHASE_MARK(k) \
+    do {              \
+    } while (0)
+#endif
+
 namespace prism {
 namespace tc {
 
@@ -235,6 +253,29 @@ __global__ void __launch_bounds__(NT, 1)
     const float w2 = __bfloat162float(p.conv_w[((size_t)h * 4 + 2) * D + (tid & 63)]);
     const float w3 = __bfloat162float(p.conv_w[((size_t)h * 4 + 3) * D + (tid & 63)]);
 
+    // gates of one chunk, one value per thread: beta/alpha for tid < 64, gamma/eta slot tid
+    float pf_beta = 0.f, pf_alpha = 1.f, pf_gam = 0.f, pf_eta = 0.f;
+    auto load_gates = [&](int c) {
+        const int n = min(C, p.T - c * C);
+        const size_t tok0 = (size_t)bh * p.T + (size_t)c * C;
+        if (tid < 64) {
+            const bool valid = tid < n;
+            pf_beta = valid ? p.beta[tok0 + tid] : 0.f;
+            pf_alpha = valid ? p.alpha[tok0 + tid] : 1.f;
+        }
+        if (tid < 64 * RMAX) {
+            const int i = tid / RMAX, l = tid % RMAX;
+            const bool valid = (i < n) && (l < R);
+            pf_gam = valid ? p.gamma[(tok0 + i) * R + l] : 0.f;
+            pf_eta = valid ? p.eta[(tok0 + i) * R + l] : 0.f;
+        }
+    };
+    if (c_begin < c_end) load_gates(c_begin);
+
+#ifdef PRISM_PHASE_TIMERS
+    unsigned long long ph_acc[16] = {0};
+    long long ph_last = clock64();
+#endif
     bool alive = true;
     for (int c = c_begin; c < c_end && alive; ++c) {
         const int stage = (c - c_begin) & 1;
@@ -242,18 +283,16 @@ __global__ void __launch_bounds__(NT, 1)
         const int n = min(C, p.T - t0);
         const size_t tok0 = (size_t)bh * p.T + t0;
 
-        // ---- P0: gates and decay factors ------------------------------------------------------
+        // ---- P0: gates (prefetched into registers one chunk ahead) and decay factors ----------
         if (tid < 64) {
-            const bool valid = tid < n;
-            s_beta[tid] = valid ? p.beta[tok0 + tid] : 0.f;
-            s_lam[tid] = valid ? logf(p.alpha[tok0 + tid]) : 0.f;
+            s_beta[tid] = pf_beta;
+            s_lam[tid] = logf(pf_alpha);
         }
-        for (int e = tid; e < 64 * RMAX; e += NT) {
-            const int i = e / RMAX, l = e % RMAX;
-            const bool valid = (i < n) && (l < R);
-            s_gc[e] = valid ? p.gamma[(tok0 + i) * R + l] : 0.f;
-            s_eta[e] = valid ? p.eta[(tok0 + i) * R + l] : 0.f;
+        if (tid < 64 * RMAX) {
+            s_gc[tid] = pf_gam;
+            s_eta[tid] = pf_eta;
         }
+        if (c + 1 < c_end) load_gates(c + 1);
         __syncthreads();
         if (warp == 0) {  // inclusive scan of 64 log-decays, two per lane
             const float a0 = s_lam[2 * lane], a1 = s_lam[2 * lane + 1];
@@ -282,6 +321,7 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         for (int e = tid; e < 64 * RMAX; e += NT) s_gc[e] *= s_colf[e / RMAX];
 
+        PHASE_MARK(0);
         // ---- P1: prep -> Xs tiles ---------------------------------------------------------------
         if (!wait_all(mb_v[stage], ph_v[stage], 4u << stage)) break;
         if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
@@ -308,6 +348,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_async_smem();
         __syncthreads();
 
+        PHASE_MARK(1);
         // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T ----------------------------------------------
         if (!wait_all(mb_qku, ph_qku, 2u)) break;
         tiles_bf16_to_f16(sm + OFF_Q, (2 + R) * TILE, tid);
@@ -327,6 +368,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
 
+        PHASE_MARK(2);
         // ---- E1: masks and decay factors -> A (fp32), PK_l, PQ_l, G (bf16 tiles) ---------------
         {
             const int i = row & 63;
@@ -359,6 +401,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_before_sync();
         __syncthreads();
 
+        PHASE_MARK(3);
         // ---- P3: MX = sum_l PK_l Xs_l (MMA, in flight) while the CTA solves T = (I + A)^{-1} -------
         if (tid == 0) {
             fence_after_sync();
@@ -429,6 +472,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
 
+        PHASE_MARK(4);
         // ---- E2: RHS = diag(beta) V - MX, and diag(beta Gamma) K -------------------------------
         {
             const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + (stage ? OFF_V1 : OFF_V0));
@@ -459,6 +503,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_before_sync();
         __syncthreads();
 
+        PHASE_MARK(5);
         // ---- P4: [U'^T ; W^T] = [RHS | BGK]^T T^T -------------------------------------------------
         if (tid == 0) {
             fence_after_sync();
@@ -473,6 +518,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
 
+        PHASE_MARK(6);
         // ---- E3: UWs = [U'^T; W^T] diag(e^{lc - lambda_j}) ---------------------------------------
         {
             const int j0 = half * 32;
@@ -488,6 +534,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_before_sync();
         __syncthreads();
 
+        PHASE_MARK(7);
         // ---- P5: D4 = UWs [G; PQ]^T-part, D5 = UWs [K; U]-part ------------------------------------
         if (tid == 0) {
             fence_after_sync();
@@ -514,6 +561,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
 
+        PHASE_MARK(8);
         // ---- E4: Qt = diag(Gamma) Q^T - (G~W)^T ;  Mc = Gamma_C I - W^T K' -------------------------
         if (quad >= 2) {
             const int m = row - 64, j0 = half * 32;
@@ -548,6 +596,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
 
+        PHASE_MARK(9);
         // ---- E5: Z <- Z Mc + [N_c; 0];  o0 / Qhat ------------------------------------------------
         {
             const int j0 = half * 32;
@@ -600,7 +649,12 @@ __global__ void __launch_bounds__(NT, 1)
         fence_before_sync();
         __syncthreads();
         alive = abort_s == 0;
+        PHASE_MARK(10);
     }
+#ifdef PRISM_PHASE_TIMERS
+    if (tid == 0)
+        for (int k = 0; k < 11; ++k) atomicAdd(&prism_tc_phase_cycles[k], ph_acc[k]);
+#endif
 
     // drain: after an expired wait, let every copy and MMA still in flight land (bounded by
     // one second each) before the CTA releases its shared and tensor memory
@@ -862,3 +916,16 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
 }
 
 }  // namespace prism
+
+#ifdef PRISM_PHASE_TIMERS
+// developer tracing build only: copy out (and optionally clear) the per-phase cycle totals
+extern "C" __attribute__((visibility("default"))) int prism_debug_phase_cycles(unsigned long long *out16, int reset)
+{
+    if (cudaMemcpyFromSymbol(out16, prism_tc_phase_cycles, sizeof(unsigned long long) * 16) != cudaSuccess) return -1;
+    if (reset) {
+        unsigned long long z[16] = {0};
+        if (cudaMemcpyToSymbol(prism_tc_phase_cycles, z, sizeof(z)) != cudaSuccess) return -1;
+    }
+    return 0;
+}
+#endif
