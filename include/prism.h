@@ -157,6 +157,41 @@ PRISM_API const char *prism_status_string(prism_status s);
 /* One-line description of the last error returned on the calling thread. */
 PRISM_API const char *prism_last_error_message(void);
 
+/*
+ * prism_forward_noalloc -- the forward for callers that cannot allocate device memory
+ * while they run.  The method's pages have no counterpart to this entry point; it is an
+ * engineering variant of prism_forward (tensor-core path) that needs no plan.
+ *
+ * Who needs it: code that runs inside a device-memory allocator or pool hook (a nested
+ * cudaMalloc would recurse or deadlock), real-time loops whose memory is reserved up front
+ * and must not grow, and hosts that forbid allocation after start-up.  prism_plan
+ * allocates workspace; this call allocates nothing.  Its scratch (segment maps, segment
+ * start states, a per-chunk stash, a status word) is one fixed array of
+ * PRISM_NOALLOC_SCRATCH_BYTES compiled into the library: every GPU that loads the library
+ * holds that array until the process exits.
+ *
+ * Sizes and tensors are those of prism_forward (layouts at the top of this file), with
+ * bf16 io and out, dk = dv = 64 and 1 <= L <= 4.  The scratch needs 24 KiB per 64-token
+ * chunk of all sequences plus 48 KiB per sequence and segment; the call uses as many
+ * segments as prism_forward would, fewer if they do not fit, and returns
+ * PRISM_ERR_UNSUPPORTED (with a message) when even one segment per sequence does not fit
+ * -- about 170K token-heads.
+ *
+ * The first call on each device resolves the array's device address and sets a kernel
+ * attribute; make that first call before any stream capture.  All calls share the one
+ * array, which keeps the last call's contents: calls that can overlap on the GPU
+ * (different streams or host threads) race on it and must be serialised by the caller.
+ * With device_status = NULL the call returns once the work is enqueued on `stream`;
+ * otherwise it waits for `stream`, stores the device status word (0 = no condition) in
+ * *device_status and returns PRISM_ERR_TIMEOUT or PRISM_ERR_DEVICE if one was recorded.
+ */
+#define PRISM_NOALLOC_SCRATCH_BYTES (64u << 20)
+PRISM_API prism_status prism_forward_noalloc(int B, int H, int T, int dk, int dv, int L, const void *q,
+                                             const void *k, const void *v, const float *beta,
+                                             const float *alpha, const void *u, const float *gamma,
+                                             const float *eta, const void *conv_w, void *out,
+                                             struct CUstream_st *stream, int *device_status);
+
 /* Version of this library, "major.minor.patch". */
 PRISM_API const char *prism_version(void);
 

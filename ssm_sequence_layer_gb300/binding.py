@@ -34,7 +34,8 @@ PRISM_OPT_OUT_DTYPE = 4
 
 EXPORTED = ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
             "prism_plan_destroy", "prism_workspace_bytes", "prism_plan_last_device_status",
-            "prism_status_string", "prism_last_error_message", "prism_version", "prism_plan_kernel_times")
+            "prism_status_string", "prism_last_error_message", "prism_version", "prism_plan_kernel_times",
+            "prism_forward_noalloc")
 
 
 class prism_kernel_time(ctypes.Structure):
@@ -79,6 +80,9 @@ def lib():
             L.prism_last_error_message.restype = ctypes.c_char_p
             L.prism_version.restype = ctypes.c_char_p
             L.prism_plan_kernel_times.argtypes = [vp, ctypes.POINTER(prism_kernel_time), i]
+            L.prism_forward_noalloc.argtypes = [i] * 6 + [vp, vp, vp, f, f, vp, f, f, vp, vp, vp,
+                                                          ctypes.POINTER(ctypes.c_int)]
+            L.prism_forward_noalloc.restype = ctypes.c_int
             L.prism_plan_kernel_times.restype = ctypes.c_int
             for name in ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
                          "prism_plan_destroy", "prism_plan_last_device_status"):
@@ -162,6 +166,17 @@ def prism_forward_host(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, out
     return _check(lib().prism_forward_host(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha),
                                            _addr(u), _addr(gamma), _addr(eta), _addr(conv_w), int(L), _addr(out),
                                            _stream(stream)))
+
+
+def prism_forward_noalloc(B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, conv_w, out, stream=None,
+                          wait=True):
+    """The allocation-free forward (see include/prism.h).  With wait=True the call waits for
+    the stream and returns the device status word (0 = no condition recorded)."""
+    status = ctypes.c_int(0)
+    _check(lib().prism_forward_noalloc(B, H, T, dk, dv, L, _addr(q), _addr(k), _addr(v), _addr(beta),
+                                       _addr(alpha), _addr(u), _addr(gamma), _addr(eta), _addr(conv_w), _addr(out),
+                                       _stream(stream), ctypes.byref(status) if wait else None))
+    return status.value
 
 
 # ------------------------------------------------------------------------------------------------

@@ -148,6 +148,8 @@ prism_status ensure_workspace(prism_plan_s *p, int path)
 
 }  // namespace
 
+void prism_set_error_message(const char *msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 extern "C" {
 
 const char *prism_version(void) { return "0.1.0"; }

@@ -92,6 +92,9 @@ cudaError_t simt_forward(const Shape &s, prism_dtype io, prism_dtype out, const 
 
 }  // namespace prism
 
+// Sets the message prism_last_error_message() returns on the calling thread.
+void prism_set_error_message(const char *msg);
+
 struct prism_plan_s {
     prism::Shape shape;
     prism_dtype io;
