@@ -135,6 +135,23 @@ __device__ __forceinline__ float ld_h(const uint8_t *tile, int row, int col)
     return __half2float(*reinterpret_cast<const __half *>(tile + sw128(row, col)));
 }
 
+// Gain g = GELU'(a) = Phi(a) + a phi(a) and Phi(a), for the exact-erf GELU.  Phi uses the
+// rational approximation of erf from Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26 (|error| <= 1.5e-7), which shares the Gaussian factor e^{-a^2/2} with phi.
+__device__ __forceinline__ void gelu_gain(float a, float &g, float &Phi)
+{
+    const float x = fabsf(a) * 0.70710678118654752f;
+    const float t = __fdividef(1.f, fmaf(0.3275911f, x, 1.f));
+    const float E = __expf(-0.5f * a * a);
+    float poly = fmaf(t, 1.061405429f, -1.453152027f);
+    poly = fmaf(t, poly, 1.421413741f);
+    poly = fmaf(t, poly, -0.284496736f);
+    poly = fmaf(t, poly, 0.254829592f);
+    const float erfx = 1.f - poly * t * E;
+    Phi = 0.5f + copysignf(0.5f * erfx, a);
+    g = fmaf(a, 0.39894228040143268f * E, Phi);
+}
+
 // in-place bf16 -> fp16 conversion of `bytes` bytes of tiles (layout unchanged)
 __device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes, int tid)
 {
@@ -231,14 +248,16 @@ __global__ void __launch_bounds__(NT, 1)
     };
     // collective bounded wait on an mbarrier phase; on expiry the CTA records the timeout
     // status and leaves the chunk loop (the phase is kept so the drain can wait for it)
+    // (thread 0 polls; the rest of the CTA waits at the barrier, issuing nothing)
     auto wait_all = [&](uint32_t mb, uint32_t &phase, uint32_t bit) -> bool {
-        const bool ok = mbar_wait(mb, phase, p.wait_ns);
-        if (ok) {
-            phase ^= 1u;
-            pending &= ~bit;
-        } else {
-            abort_s = 1;
-            set_status(p.status, kDevTimeout);
+        if (tid == 0) {
+            if (mbar_wait(mb, phase, p.wait_ns)) {
+                phase ^= 1u;
+                pending &= ~bit;
+            } else {
+                abort_s = 1;
+                set_status(p.status, kDevTimeout);
+            }
         }
         __syncthreads();
         return abort_s == 0;
@@ -248,10 +267,11 @@ __global__ void __launch_bounds__(NT, 1)
         issue_v(c_begin, 0);
         issue_qku(c_begin);
     }
-    const float w0 = __bfloat162float(p.conv_w[((size_t)h * 4 + 0) * D + (tid & 63)]);
-    const float w1 = __bfloat162float(p.conv_w[((size_t)h * 4 + 1) * D + (tid & 63)]);
-    const float w2 = __bfloat162float(p.conv_w[((size_t)h * 4 + 2) * D + (tid & 63)]);
-    const float w3 = __bfloat162float(p.conv_w[((size_t)h * 4 + 3) * D + (tid & 63)]);
+    const __nv_bfloat162 *cw2 = reinterpret_cast<const __nv_bfloat162 *>(p.conv_w) + (size_t)h * 4 * (D / 2) + (tid & 31);
+    const float2 w0 = __bfloat1622float2(cw2[0 * (D / 2)]);
+    const float2 w1 = __bfloat1622float2(cw2[1 * (D / 2)]);
+    const float2 w2 = __bfloat1622float2(cw2[2 * (D / 2)]);
+    const float2 w3 = __bfloat1622float2(cw2[3 * (D / 2)]);
 
     // gates of one chunk, one value per thread: beta/alpha for tid < 64, gamma/eta slot tid
     float pf_beta = 0.f, pf_alpha = 1.f, pf_gam = 0.f, pf_eta = 0.f;
@@ -322,34 +342,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int e = tid; e < 64 * RMAX; e += NT) s_gc[e] *= s_colf[e / RMAX];
 
         PHASE_MARK(0);
-        // ---- P1: prep -> Xs tiles ---------------------------------------------------------------
-        if (!wait_all(mb_v[stage], ph_v[stage], 4u << stage)) break;
-        if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
-        {
-            const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + (stage ? OFF_V1 : OFF_V0));
-            const int ch = tid & 63;
-            for (int i = tid >> 6; i < 64; i += NT / 64) {
-                const float v0 = __bfloat162float(vb[(i + 8) * 64 + ch]);
-                const float v1 = __bfloat162float(vb[(i + 7) * 64 + ch]);
-                const float v2 = __bfloat162float(vb[(i + 6) * 64 + ch]);
-                const float v3 = __bfloat162float(vb[(i + 5) * 64 + ch]);
-                const float a = fmaf(w0, v0, fmaf(w1, v1, fmaf(w2, v2, w3 * v3)));
-                const float Phi = 0.5f * erfcf(-a * 0.70710678118654752f);
-                const float phi = 0.39894228040143268f * __expf(-0.5f * a * a);
-                const float g = fmaf(a, phi, Phi);
-                float r = v0 - a * Phi;
-                for (int l = 0; l < R; ++l) {
-                    const float x = s_gc[i * RMAX + l] * g * r;
-                    *reinterpret_cast<__half *>(sm + OFF_XS + l * TILE + sw128(i, ch)) = __float2half_rn(x);
-                    r *= 1.f - s_eta[i * RMAX + l] * g;
-                }
-            }
-        }
-        fence_async_smem();
-        __syncthreads();
-
-        PHASE_MARK(1);
-        // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T ----------------------------------------------
+        // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T (runs while the CTA does the prep) ----------
         if (!wait_all(mb_qku, ph_qku, 2u)) break;
         tiles_bf16_to_f16(sm + OFF_Q, (2 + R) * TILE, tid);
         fence_async_smem();
@@ -361,10 +354,42 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_f16(tmem + TM_D1, sdesc(sbase + OFF_Q + s * 32, 16, 1024), sdesc(sbase + OFF_K + s * 32, 16, 1024),
-                         id, s > 0);
+                        id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
         }
+
+        PHASE_MARK(1);
+        // ---- P1: prep -> Xs tiles (two channels x 8 tokens per thread) --------------------------
+        if (!wait_all(mb_v[stage], ph_v[stage], 4u << stage)) break;
+        if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
+        {
+            const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stage ? OFF_V1 : OFF_V0));
+            const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
+#pragma unroll 2
+            for (int k = 0; k < 8; ++k) {
+                const int i = tg + 8 * k;
+                const float2 v0 = __bfloat1622float2(vb[(i + 8) * 32 + cp]);
+                const float2 v1 = __bfloat1622float2(vb[(i + 7) * 32 + cp]);
+                const float2 v2 = __bfloat1622float2(vb[(i + 6) * 32 + cp]);
+                const float2 v3 = __bfloat1622float2(vb[(i + 5) * 32 + cp]);
+                const float a0 = fmaf(w0.x, v0.x, fmaf(w1.x, v1.x, fmaf(w2.x, v2.x, w3.x * v3.x)));
+                const float a1 = fmaf(w0.y, v0.y, fmaf(w1.y, v1.y, fmaf(w2.y, v2.y, w3.y * v3.y)));
+                float g0, g1, Phi0, Phi1;
+                gelu_gain(a0, g0, Phi0);
+                gelu_gain(a1, g1, Phi1);
+                float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
+                for (int l = 0; l < R; ++l) {
+                    const float gc = s_gc[i * RMAX + l], et = s_eta[i * RMAX + l];
+                    *reinterpret_cast<uint32_t *>(sm + OFF_XS + l * TILE + sw128(i, 2 * cp)) =
+                        pack2(gc * g0 * r0, gc * g1 * r1);
+                    r0 *= 1.f - et * g0;
+                    r1 *= 1.f - et * g1;
+                }
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
 
@@ -415,57 +440,79 @@ __global__ void __launch_bounds__(NT, 1)
             pending |= 1u;
         }
         {
+            // T = (I + A)^{-1} by 16x16 blocks: diagonal blocks by forward substitution, then the
+            // block diagonals below them, T[bi][bj] = -T[bi][bi] sum_{k=bj..bi-1} A[bi][k] T[k][bj]
             const float *A = reinterpret_cast<const float *>(sm + OFF_AKK);
             float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
-            if (tid < 64) {  // diagonal 16x16 blocks by forward substitution, one column per thread
-                const int b = tid >> 4, cc = tid & 15, o = 16 * b;
+            if (tid < 64) {  // one column of one diagonal block per thread
+                const int o = 16 * (tid >> 4), cc = tid & 15;
                 float t[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
-                    float x = (r == cc) ? 1.f : 0.f;
-                    if (r > cc) {
-                        float s = 0.f;
+                    // t[j] = 0 for j < cc, so the sum may run over all j < r
+                    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                        for (int j = 0; j < r; ++j)
-                            if (j >= cc) s = fmaf(A[(o + r) * LDA + o + j], t[j], s);
-                        x = -s;
+                    for (int j = 0; j + 1 < r; j += 2) {
+                        s0 = fmaf(A[(o + r) * LDA + o + j], t[j], s0);
+                        s1 = fmaf(A[(o + r) * LDA + o + j + 1], t[j + 1], s1);
                     }
-                    t[r] = x;
-                    T32[(o + r) * LDA + o + cc] = x;
+                    if (r & 1) s0 = fmaf(A[(o + r) * LDA + o + r - 1], t[r - 1], s0);
+                    t[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -(s0 + s1));
+                    T32[(o + r) * LDA + o + cc] = t[r];
                 }
             }
             __syncthreads();
-            for (int d = 1; d < 4; ++d) {  // off-diagonal blocks, one block diagonal at a time
-                const int nb = 4 - d;
-                for (int e = tid; e < nb * 256; e += NT) {  // X = sum_k A[bi][k] T[k][bj]
-                    const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            for (int d = 1; d < 4; ++d) {
+                const int items = (4 - d) * 64;  // (block, row, 4-column group)
+                if (tid < items) {                // X = sum_k A[bi][k] T[k][bj]
+                    const int b = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
                     const int bi = b + d, bj = b;
-                    float s = 0.f;
-                    for (int k = 16 * bj; k < 16 * bi; ++k) s = fmaf(A[(16 * bi + r) * LDA + k], T32[k * LDA + 16 * bj + cc], s);
-                    s_xtmp[e] = s;
+                    const float *arow = A + (16 * bi + r) * LDA;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                    for (int k = 16 * bj; k < 16 * bi; ++k) {
+                        const float a = arow[k];
+                        const float4 tv = *reinterpret_cast<const float4 *>(T32 + k * LDA + 16 * bj + c4);
+                        acc.x = fmaf(a, tv.x, acc.x);
+                        acc.y = fmaf(a, tv.y, acc.y);
+                        acc.z = fmaf(a, tv.z, acc.z);
+                        acc.w = fmaf(a, tv.w, acc.w);
+                    }
+                    *reinterpret_cast<float4 *>(s_xtmp + (b << 8) + (r << 4) + c4) = acc;
                 }
                 __syncthreads();
-                for (int e = tid; e < nb * 256; e += NT) {  // T[bi][bj] = -T[bi][bi] X
-                    const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                if (tid < items) {  // T[bi][bj] = -T[bi][bi] X
+                    const int b = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
                     const int bi = b + d, bj = b;
-                    float s = 0.f;
+                    const float *trow = T32 + (16 * bi + r) * LDA + 16 * bi;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        s = fmaf(T32[(16 * bi + r) * LDA + 16 * bi + k], s_xtmp[(b << 8) + (k << 4) + cc], s);
-                    T32[(16 * bi + r) * LDA + 16 * bj + cc] = -s;
+                    for (int k = 0; k < 16; ++k) {
+                        const float a = trow[k];
+                        const float4 xv = *reinterpret_cast<const float4 *>(s_xtmp + (b << 8) + (k << 4) + c4);
+                        acc.x = fmaf(a, xv.x, acc.x);
+                        acc.y = fmaf(a, xv.y, acc.y);
+                        acc.z = fmaf(a, xv.z, acc.z);
+                        acc.w = fmaf(a, xv.w, acc.w);
+                    }
+                    *reinterpret_cast<float4 *>(T32 + (16 * bi + r) * LDA + 16 * bj + c4) =
+                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
                 __syncthreads();
             }
-            for (int e = tid; e < 64 * 8; e += NT) {  // T (bf16, [i][j], zero above the diagonal)
+            for (int e = tid; e < 64 * 8; e += NT) {  // T (fp16, [i][j], zero above the diagonal)
                 const int i = e >> 3, g = e & 7;
-                float v[8];
+                const float4 lo = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g);
+                const float4 hi = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g + 4);
+                const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                float m[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = (8 * g + q <= i) ? T32[i * LDA + 8 * g + q] : 0.f;
+                for (int q = 0; q < 8; ++q) m[q] = (8 * g + q <= i) ? v[q] : 0.f;
                 uint4 w;
-                w.x = pack2(v[0], v[1]);
-                w.y = pack2(v[2], v[3]);
-                w.z = pack2(v[4], v[5]);
-                w.w = pack2(v[6], v[7]);
+                w.x = pack2(m[0], m[1]);
+                w.y = pack2(m[2], m[3]);
+                w.z = pack2(m[4], m[5]);
+                w.w = pack2(m[6], m[7]);
                 *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128(i, 8 * g)) = w;
             }
         }
