@@ -65,7 +65,8 @@ namespace tc {
 constexpr int C = kChunk;
 constexpr int D = 64;       // dk = dv
 constexpr int RMAX = 3;     // refinement levels handled (L <= 4)
-constexpr int NT = 256;     // threads per CTA
+constexpr int NT = 512;     // threads per CTA: 16 warps, 4 per TMEM lane quarter
+constexpr int CW = 64 / (NT / 128);  // columns of a 64-column TMEM block each thread handles
 constexpr uint32_t TILE = 8192;  // 64 rows x 128 B
 
 // shared memory map (bytes from a 1024-aligned base)
@@ -78,7 +79,8 @@ constexpr uint32_t OFF_V1 = OFF_V0 + 10240;
 constexpr uint32_t OFF_E = OFF_V1 + 10240;        // [PK0|PQ0|PK1|PQ1|PK2|PQ2|G]; later Qt, Mc
 constexpr uint32_t OFF_G = OFF_E + 6 * TILE;
 constexpr uint32_t OFF_AKK = OFF_E + 7 * TILE;    // A (fp32, stride 68); later RHS|BGK; later UWs
-constexpr uint32_t LDA = 68;
+constexpr uint32_t LDA = 68;    // row stride (floats) of T32 (float4 rows)
+constexpr uint32_t LDAA = 65;   // row stride (floats) of A (conflict-free column writes)
 constexpr uint32_t OFF_T32 = OFF_AKK + 64 * LDA * 4;
 constexpr uint32_t OFF_TB = OFF_T32 + 64 * LDA * 4;  // T (bf16 tile)
 constexpr uint32_t OFF_XS = OFF_TB + TILE;            // Xs0..Xs2
@@ -115,12 +117,13 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// write 32 consecutive fp32 values (columns col0..col0+31 of row `row`) as fp16 into a
-// [rows][64] SW128 tile
-__device__ __forceinline__ void st_row32(uint8_t *tile, int row, int col0, const float (&v)[32])
+// write N consecutive fp32 values (columns col0..col0+N-1 of row `row`, col0 a multiple of 8)
+// as fp16 into a [rows][64] SW128 tile
+template <int N>
+__device__ __forceinline__ void st_row(uint8_t *tile, int row, int col0, const float (&v)[N])
 {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < N / 8; ++g) {
         uint4 w;
         w.x = pack2(v[8 * g + 0], v[8 * g + 1]);
         w.y = pack2(v[8 * g + 2], v[8 * g + 3]);
@@ -152,6 +155,24 @@ __device__ __forceinline__ void gelu_gain(float a, float &g, float &Phi)
     g = fmaf(a, 0.39894228040143268f * E, Phi);
 }
 
+// round to tf32 (the operand format of mma.sync .tf32)
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// D += A B for one m16n8k8 tile (A 16x8 row-major, B 8x8 column-major, tf32 in, fp32 accumulate)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // in-place bf16 -> fp16 conversion of `bytes` bytes of tiles (layout unchanged)
 __device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes, int tid)
 {
@@ -180,7 +201,7 @@ __global__ void __launch_bounds__(NT, 1)
     __shared__ int abort_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
+    const int quad = warp & 3, sub = warp >> 2;  // TMEM lane quarter, epilogue column slice
     const int row = quad * 32 + lane;  // TMEM lane owned in epilogues
     const int bh = blockIdx.x / p.P, seg = blockIdx.x % p.P;
     const int h = bh % p.H;
@@ -198,7 +219,6 @@ __global__ void __launch_bounds__(NT, 1)
     float *s_gc = sc + 384;         // gamma_{i,l} e^{lc - lambda_i}   [64][RMAX]
     float *s_eta = s_gc + 64 * RMAX;  // [64][RMAX]
     float *s_xtmp = s_eta + 64 * RMAX;  // 3 x 256 scratch of the solve
-    float *s_misc = s_xtmp + 3 * 256;   // [0] = lc
 
     const uint32_t sbase = smem_u32(sm);
     const uint32_t mb_mma = smem_u32(&mbar[0]), mb_qku = smem_u32(&mbar[1]);
@@ -273,15 +293,18 @@ __global__ void __launch_bounds__(NT, 1)
     const float2 w2 = __bfloat1622float2(cw2[2 * (D / 2)]);
     const float2 w3 = __bfloat1622float2(cw2[3 * (D / 2)]);
 
-    // gates of one chunk, one value per thread: beta/alpha for tid < 64, gamma/eta slot tid
-    float pf_beta = 0.f, pf_alpha = 1.f, pf_gam = 0.f, pf_eta = 0.f;
+    // gates of one chunk: lane l of warp 0 holds beta/alpha of tokens 2l, 2l+1; thread tid < 192
+    // holds gamma/eta slot tid
+    float pf_b0 = 0.f, pf_b1 = 0.f, pf_a0 = 1.f, pf_a1 = 1.f, pf_gam = 0.f, pf_eta = 0.f;
     auto load_gates = [&](int c) {
         const int n = min(C, p.T - c * C);
         const size_t tok0 = (size_t)bh * p.T + (size_t)c * C;
-        if (tid < 64) {
-            const bool valid = tid < n;
-            pf_beta = valid ? p.beta[tok0 + tid] : 0.f;
-            pf_alpha = valid ? p.alpha[tok0 + tid] : 1.f;
+        if (warp == 0) {
+            const int i0 = 2 * lane, i1 = 2 * lane + 1;
+            pf_b0 = i0 < n ? p.beta[tok0 + i0] : 0.f;
+            pf_b1 = i1 < n ? p.beta[tok0 + i1] : 0.f;
+            pf_a0 = i0 < n ? p.alpha[tok0 + i0] : 1.f;
+            pf_a1 = i1 < n ? p.alpha[tok0 + i1] : 1.f;
         }
         if (tid < 64 * RMAX) {
             const int i = tid / RMAX, l = tid % RMAX;
@@ -304,9 +327,30 @@ __global__ void __launch_bounds__(NT, 1)
         const size_t tok0 = (size_t)bh * p.T + t0;
 
         // ---- P0: gates (prefetched into registers one chunk ahead) and decay factors ----------
-        if (tid < 64) {
-            s_beta[tid] = pf_beta;
-            s_lam[tid] = logf(pf_alpha);
+        if (warp == 0) {  // inclusive scan of the 64 log-decays, two per lane, in registers
+            const float la0 = logf(pf_a0), la1 = logf(pf_a1);
+            float s = la0 + la1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, s, off);
+                if (lane >= off) s += y;
+            }
+            const float l1 = s, l0 = s - la1;
+            const float lcw = __shfl_sync(0xffffffffu, s, 31);
+            const int i0 = 2 * lane, i1 = i0 + 1;
+            s_beta[i0] = pf_b0;
+            s_beta[i1] = pf_b1;
+            s_lam[i0] = l0;
+            s_lam[i1] = l1;
+            s_rowf[i0] = __expf(l0 - lcw);
+            s_rowf[i1] = __expf(l1 - lcw);
+            s_colf[i0] = __expf(lcw - l0);
+            s_colf[i1] = __expf(lcw - l1);
+            s_gam[i0] = __expf(l0);
+            s_gam[i1] = __expf(l1);
+            s_bg[i0] = pf_b0 * __expf(l0);
+            s_bg[i1] = pf_b1 * __expf(l1);
+            if (lane == 31 && -lcw > 80.f) set_status(p.status, kDevBounds);  // beyond the factorised range
         }
         if (tid < 64 * RMAX) {
             s_gc[tid] = pf_gam;
@@ -314,32 +358,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         if (c + 1 < c_end) load_gates(c + 1);
         __syncthreads();
-        if (warp == 0) {  // inclusive scan of 64 log-decays, two per lane
-            const float a0 = s_lam[2 * lane], a1 = s_lam[2 * lane + 1];
-            float s = a0 + a1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, s, off);
-                if (lane >= off) s += y;
-            }
-            s_lam[2 * lane + 1] = s;
-            s_lam[2 * lane] = s - a1;
-        }
-        __syncthreads();
         const float lc = s_lam[63];
-        if (tid < 64) {
-            const float li = s_lam[tid];
-            s_rowf[tid] = __expf(li - lc);
-            s_colf[tid] = __expf(lc - li);
-            s_gam[tid] = __expf(li);
-            s_bg[tid] = s_beta[tid] * __expf(li);
-            if (tid == 0) {
-                s_misc[0] = lc;
-                if (-lc > 80.f) set_status(p.status, kDevBounds);  // decay beyond the factorised range
-            }
-        }
-        __syncthreads();
-        for (int e = tid; e < 64 * RMAX; e += NT) s_gc[e] *= s_colf[e / RMAX];
 
         PHASE_MARK(0);
         // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T (runs while the CTA does the prep) ----------
@@ -367,8 +386,8 @@ __global__ void __launch_bounds__(NT, 1)
             const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stage ? OFF_V1 : OFF_V0));
             const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
 #pragma unroll 2
-            for (int k = 0; k < 8; ++k) {
-                const int i = tg + 8 * k;
+            for (int k = 0; k < 64 / (NT / 32); ++k) {
+                const int i = tg + (NT / 32) * k;
                 const float2 v0 = __bfloat1622float2(vb[(i + 8) * 32 + cp]);
                 const float2 v1 = __bfloat1622float2(vb[(i + 7) * 32 + cp]);
                 const float2 v2 = __bfloat1622float2(vb[(i + 6) * 32 + cp]);
@@ -379,8 +398,9 @@ __global__ void __launch_bounds__(NT, 1)
                 gelu_gain(a0, g0, Phi0);
                 gelu_gain(a1, g1, Phi1);
                 float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
+                const float cf = s_colf[i];
                 for (int l = 0; l < R; ++l) {
-                    const float gc = s_gc[i * RMAX + l], et = s_eta[i * RMAX + l];
+                    const float gc = s_gc[i * RMAX + l] * cf, et = s_eta[i * RMAX + l];
                     *reinterpret_cast<uint32_t *>(sm + OFF_XS + l * TILE + sw128(i, 2 * cp)) =
                         pack2(gc * g0 * r0, gc * g1 * r1);
                     r0 *= 1.f - et * g0;
@@ -402,23 +422,23 @@ __global__ void __launch_bounds__(NT, 1)
             const float bi = s_beta[i];
             const int nblk = N1 / 64;  // 64-column blocks: 0 = keys, 1.. = levels
             for (int blk = 0; blk < nblk; ++blk) {
-                const int col0 = blk * 64 + half * 32;
-                float v[32];
-                tmem_ld32(tmem + TM_D1 + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0, v);
-                const int j0 = half * 32;
+                const int col0 = blk * 64 + sub * CW;
+                float v[CW];
+                tmem_ld(tmem + TM_D1 + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0, v);
+                const int j0 = sub * CW;
                 if (qside) {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] = (j0 + q <= i) ? v[q] : 0.f;
+                    for (int q = 0; q < CW; ++q) v[q] = (j0 + q <= i) ? v[q] : 0.f;
                     uint8_t *tile = sm + (blk == 0 ? OFF_G : OFF_E + (blk - 1) * 2 * TILE + TILE);
-                    st_row32(tile, i, j0, v);
+                    st_row(tile, i, j0, v);
                 } else if (blk == 0) {
                     float *A = reinterpret_cast<float *>(sm + OFF_AKK);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) A[i * LDA + j0 + q] = (j0 + q < i) ? v[q] * bi * rf * s_colf[j0 + q] : 0.f;
+                    for (int q = 0; q < CW; ++q) A[i * LDAA + j0 + q] = (j0 + q < i) ? v[q] * bi * rf * s_colf[j0 + q] : 0.f;
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] = (j0 + q < i) ? v[q] : 0.f;
-                    st_row32(sm + OFF_E + (blk - 1) * 2 * TILE, i, j0, v);
+                    for (int q = 0; q < CW; ++q) v[q] = (j0 + q < i) ? v[q] : 0.f;
+                    st_row(sm + OFF_E + (blk - 1) * 2 * TILE, i, j0, v);
                 }
             }
         }
@@ -453,53 +473,69 @@ __global__ void __launch_bounds__(NT, 1)
                     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                     for (int j = 0; j + 1 < r; j += 2) {
-                        s0 = fmaf(A[(o + r) * LDA + o + j], t[j], s0);
-                        s1 = fmaf(A[(o + r) * LDA + o + j + 1], t[j + 1], s1);
+                        s0 = fmaf(A[(o + r) * LDAA + o + j], t[j], s0);
+                        s1 = fmaf(A[(o + r) * LDAA + o + j + 1], t[j + 1], s1);
                     }
-                    if (r & 1) s0 = fmaf(A[(o + r) * LDA + o + r - 1], t[r - 1], s0);
+                    if (r & 1) s0 = fmaf(A[(o + r) * LDAA + o + r - 1], t[r - 1], s0);
                     t[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -(s0 + s1));
                     T32[(o + r) * LDA + o + cc] = t[r];
                 }
             }
             __syncthreads();
+            PHASE_MARK(11);
+            // block diagonals below: one warp per 16x16 block, products on mma.sync (tf32 in,
+            // fp32 accumulate); X goes through the warp's scratch to become a B operand
             for (int d = 1; d < 4; ++d) {
-                const int items = (4 - d) * 64;  // (block, row, 4-column group)
-                if (tid < items) {                // X = sum_k A[bi][k] T[k][bj]
-                    const int b = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-                    const int bi = b + d, bj = b;
-                    const float *arow = A + (16 * bi + r) * LDA;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                    for (int k = 16 * bj; k < 16 * bi; ++k) {
-                        const float a = arow[k];
-                        const float4 tv = *reinterpret_cast<const float4 *>(T32 + k * LDA + 16 * bj + c4);
-                        acc.x = fmaf(a, tv.x, acc.x);
-                        acc.y = fmaf(a, tv.y, acc.y);
-                        acc.z = fmaf(a, tv.z, acc.z);
-                        acc.w = fmaf(a, tv.w, acc.w);
-                    }
-                    *reinterpret_cast<float4 *>(s_xtmp + (b << 8) + (r << 4) + c4) = acc;
-                }
-                __syncthreads();
-                if (tid < items) {  // T[bi][bj] = -T[bi][bi] X
-                    const int b = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-                    const int bi = b + d, bj = b;
-                    const float *trow = T32 + (16 * bi + r) * LDA + 16 * bi;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (warp < 4 - d) {
+                    const int bj = warp, bi = warp + d;
+                    const int gq = lane >> 2, tq = lane & 3;
+                    float *X = s_xtmp + warp * 256;  // [16][16]
+                    float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int kb = bj; kb < bi; ++kb) {  // X = sum_kb A[bi][kb] T[kb][bj]
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const float a = trow[k];
-                        const float4 xv = *reinterpret_cast<const float4 *>(s_xtmp + (b << 8) + (k << 4) + c4);
-                        acc.x = fmaf(a, xv.x, acc.x);
-                        acc.y = fmaf(a, xv.y, acc.y);
-                        acc.z = fmaf(a, xv.z, acc.z);
-                        acc.w = fmaf(a, xv.w, acc.w);
+                        for (int ks = 0; ks < 2; ++ks) {
+                            const float *ar = A + (16 * bi + gq) * LDAA + 16 * kb + 8 * ks + tq;
+                            const uint32_t a0 = to_tf32(ar[0]), a1 = to_tf32(ar[8 * LDAA]);
+                            const uint32_t a2 = to_tf32(ar[4]), a3 = to_tf32(ar[8 * LDAA + 4]);
+#pragma unroll
+                            for (int nt = 0; nt < 2; ++nt) {
+                                const float *br = T32 + (16 * kb + 8 * ks + tq) * LDA + 16 * bj + 8 * nt + gq;
+                                mma_tf32(c[nt], a0, a1, a2, a3, to_tf32(br[0]), to_tf32(br[4 * LDA]));
+                            }
+                        }
                     }
-                    *reinterpret_cast<float4 *>(T32 + (16 * bi + r) * LDA + 16 * bj + c4) =
-                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        X[gq * 16 + 8 * nt + 2 * tq] = c[nt][0];
+                        X[gq * 16 + 8 * nt + 2 * tq + 1] = c[nt][1];
+                        X[(gq + 8) * 16 + 8 * nt + 2 * tq] = c[nt][2];
+                        X[(gq + 8) * 16 + 8 * nt + 2 * tq + 1] = c[nt][3];
+                    }
+                    __syncwarp();
+                    float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // T[bi][bi] X
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const float *ar = T32 + (16 * bi + gq) * LDA + 16 * bi + 8 * ks + tq;
+                        const uint32_t a0 = to_tf32(ar[0]), a1 = to_tf32(ar[8 * LDA]);
+                        const uint32_t a2 = to_tf32(ar[4]), a3 = to_tf32(ar[8 * LDA + 4]);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const float *br = X + (8 * ks + tq) * 16 + 8 * nt + gq;
+                            mma_tf32(e[nt], a0, a1, a2, a3, to_tf32(br[0]), to_tf32(br[4 * 16]));
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        float *tr = T32 + (16 * bi + gq) * LDA + 16 * bj + 8 * nt + 2 * tq;
+                        tr[0] = -e[nt][0];
+                        tr[1] = -e[nt][1];
+                        tr[8 * LDA] = -e[nt][2];
+                        tr[8 * LDA + 1] = -e[nt][3];
+                    }
                 }
                 __syncthreads();
             }
+            PHASE_MARK(12);
             for (int e = tid; e < 64 * 8; e += NT) {  // T (fp16, [i][j], zero above the diagonal)
                 const int i = e >> 3, g = e & 7;
                 const float4 lo = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g);
@@ -515,6 +551,7 @@ __global__ void __launch_bounds__(NT, 1)
                 w.w = pack2(m[6], m[7]);
                 *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128(i, 8 * g)) = w;
             }
+            PHASE_MARK(13);
         }
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
@@ -524,26 +561,26 @@ __global__ void __launch_bounds__(NT, 1)
         {
             const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + (stage ? OFF_V1 : OFF_V0));
             if (quad < 2) {  // lanes 0..63 hold MX rows
-                const int i = row, j0 = half * 32;
-                float v[32];
+                const int i = row, j0 = sub * CW;
+                float v[CW];
                 if (R > 0) {
-                    tmem_ld32(tmem + TM_D2 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+                    tmem_ld(tmem + TM_D2 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] = 0.f;  // no levels: M X = 0 (D2 is never written)
+                    for (int q = 0; q < CW; ++q) v[q] = 0.f;  // no levels: M X = 0 (D2 is never written)
                 }
                 const float bi = s_beta[i], brf = s_beta[i] * s_rowf[i];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] = bi * __bfloat162float(vb[(i + 8) * 64 + j0 + q]) - brf * v[q];
-                st_row32(sm + OFF_AKK, i, j0, v);  // RHS tile (A is dead after the solve)
+                for (int q = 0; q < CW; ++q) v[q] = bi * __bfloat162float(vb[(i + 8) * 64 + j0 + q]) - brf * v[q];
+                st_row(sm + OFF_AKK, i, j0, v);  // RHS tile (A is dead after the solve)
             } else {
-                const int tt = (half ? 64 : 0) + (tid & 63);  // 0..127 over the warps of quads 2, 3
-                const int j = tt >> 1, m0 = (tt & 1) * 32;
-                float v[32];
+                const int tt = sub * 64 + (quad - 2) * 32 + lane;  // 0..255 over the warps of quads 2, 3
+                const int j = tt >> 2, m0 = (tt & 3) * CW;
+                float v[CW];
                 const float s = s_bg[j];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] = s * ld_h(sm + OFF_K, j, m0 + q);
-                st_row32(sm + OFF_AKK + TILE, j, m0, v);  // BGK tile
+                for (int q = 0; q < CW; ++q) v[q] = s * ld_h(sm + OFF_K, j, m0 + q);
+                st_row(sm + OFF_AKK + TILE, j, m0, v);  // BGK tile
             }
         }
         fence_async_smem();
@@ -568,14 +605,14 @@ __global__ void __launch_bounds__(NT, 1)
         PHASE_MARK(6);
         // ---- E3: UWs = [U'^T; W^T] diag(e^{lc - lambda_j}) ---------------------------------------
         {
-            const int j0 = half * 32;
-            float v[32];
-            tmem_ld32(tmem + TM_D3 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+            const int j0 = sub * CW;
+            float v[CW];
+            tmem_ld(tmem + TM_D3 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] *= s_colf[j0 + q];
+            for (int q = 0; q < CW; ++q) v[q] *= s_colf[j0 + q];
             fence_before_sync();
             __syncthreads();  // every thread has read D3; RHS|BGK are dead (MMA done)
-            st_row32(sm + OFF_AKK, row, j0, v);
+            st_row(sm + OFF_AKK, row, j0, v);
         }
         fence_async_smem();
         fence_before_sync();
@@ -608,27 +645,36 @@ __global__ void __launch_bounds__(NT, 1)
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
 
+        if (tid == 0 && c + 1 < c_end) {  // K and U of this chunk are no longer read: reload them now
+            mbar_add_tx(mb_qku, (1 + R) * TILE);
+            tma_load_3d(sbase + OFF_K, &tm_k, mb_qku, 0, (c + 1) * C, bh);
+            for (int l = 0; l < R; ++l) tma_load_4d(sbase + OFF_U + l * TILE, &tm_u, mb_qku, 0, l, (c + 1) * C, bh);
+            pending |= 2u;
+        }
         PHASE_MARK(8);
         // ---- E4: Qt = diag(Gamma) Q^T - (G~W)^T ;  Mc = Gamma_C I - W^T K' -------------------------
         if (quad >= 2) {
-            const int m = row - 64, j0 = half * 32;
-            float v[32];
-            tmem_ld32(tmem + TM_D4 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+            const int m = row - 64, j0 = sub * CW;
+            float v[CW];
+            tmem_ld(tmem + TM_D4 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = s_gam[j0 + q] * ld_h(sm + OFF_Q, j0 + q, m) - s_rowf[j0 + q] * v[q];
-            st_row32(sm + OFF_E, m, j0, v);  // Qt [m][i]
-            tmem_ld32(tmem + TM_D5 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+            for (int q = 0; q < CW; ++q) v[q] = s_gam[j0 + q] * ld_h(sm + OFF_Q, j0 + q, m) - s_rowf[j0 + q] * v[q];
+            st_row(sm + OFF_E, m, j0, v);  // Qt [m][i]
+            tmem_ld(tmem + TM_D5 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
             const float gC = __expf(lc);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = ((j0 + q) == m ? gC : 0.f) - v[q];
-            st_row32(sm + OFF_E + TILE, m, j0, v);  // Mc [m][m']
+            for (int q = 0; q < CW; ++q) v[q] = ((j0 + q) == m ? gC : 0.f) - v[q];
+            st_row(sm + OFF_E + TILE, m, j0, v);  // Mc [m][m']
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             fence_after_sync();
-            if (c + 1 < c_end) issue_qku(c + 1);  // Q, K, U of this chunk are no longer read
+            if (c + 1 < c_end) {  // Q of this chunk is no longer read: its reload completes the phase
+                mbar_expect_tx(mb_qku, TILE);
+                tma_load_3d(sbase + OFF_Q, &tm_q, mb_qku, 0, (c + 1) * C, bh);
+            }
             // ---- P6: D6 = Z Mc, D7 = Z Qt ------------------------------------------------------
             const uint32_t id = idesc_f16(128, 64, 0, 1);
 #pragma unroll
@@ -646,51 +692,68 @@ __global__ void __launch_bounds__(NT, 1)
         PHASE_MARK(9);
         // ---- E5: Z <- Z Mc + [N_c; 0];  o0 / Qhat ------------------------------------------------
         {
-            const int j0 = half * 32;
+            const int j0 = sub * CW;
             const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-            float z[32], nc[32], o[32], ol[32];
-            tmem_ld32(tmem + TM_D6 + lane_off + (uint32_t)j0, z);
-            tmem_ld32(tmem + TM_D5 + lane_off + (uint32_t)j0, nc);
-            tmem_ld32(tmem + TM_D7 + lane_off + (uint32_t)j0, o);
-            tmem_ld32(tmem + TM_D4 + lane_off + (uint32_t)j0, ol);
+            float z[CW], nc[CW], o[CW], ol[CW];
+            tmem_ld(tmem + TM_D6 + lane_off + (uint32_t)j0, z);
+            tmem_ld(tmem + TM_D5 + lane_off + (uint32_t)j0, nc);
+            tmem_ld(tmem + TM_D7 + lane_off + (uint32_t)j0, o);
+            tmem_ld(tmem + TM_D4 + lane_off + (uint32_t)j0, ol);
             if (row < 64) {
 #pragma unroll
-                for (int q = 0; q < 32; ++q) z[q] += nc[q];
+                for (int q = 0; q < CW; ++q) z[q] += nc[q];
             }
             fence_before_sync();
             __syncthreads();  // MMAs reading ZA are complete (waited above); all rows loaded
-            st_row32(sm + OFF_ZA, row, j0, z);
+            st_row(sm + OFF_ZA, row, j0, z);
             if (c + 1 == c_end) {
                 float *zs = p.zsum + (((size_t)bh * p.P + seg) * 128 + row) * 64 + j0;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) zs[q] = z[q];
+                for (int q = 0; q < CW; ++q) zs[q] = z[q];
             }
-            // outputs: row < 64 -> o0^T[c][i] = D7 + O_loc^T ; row >= 64 -> Qhat^T[m][i]
+            // outputs: row < 64 -> o0^T[c][i] = D7 + O_loc^T ; row >= 64 -> Qhat^T[m][i].  They are
+            // transposed through shared memory (region E: Qt and Mc are no longer read) and
+            // written with 16-byte stores: o0 as [i][c] fp32, Qhat as [i][m] fp16.
+            float *so = reinterpret_cast<float *>(sm + OFF_E);                // [64][64] fp32
+            __half *sq = reinterpret_cast<__half *>(sm + OFF_E + 2 * TILE);   // [64][64] fp16
             if (row < 64) {
-                const int cc = row;
-                bool finite = true;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int i = j0 + q;
-                    if (i < n) {
-                        const float val = o[q] + s_rowf[i] * ol[q];
-                        finite = finite && isfinite(val);
-                        if (seg == 0) {
-                            if (p.out_f32)
-                                reinterpret_cast<float *>(p.out)[(tok0 + i) * D + cc] = val;
-                            else
-                                reinterpret_cast<__nv_bfloat16 *>(p.out)[(tok0 + i) * D + cc] = __float2bfloat16_rn(val);
-                        } else
-                            p.stash_o[(((size_t)bh * p.NC + c) * 64 + i) * 64 + cc] = val;
-                    }
-                }
-                if (!finite) set_status(p.status, kDevBounds);  // outside the fp16 operand range
+                for (int q = 0; q < CW; ++q) so[(j0 + q) * 64 + row] = o[q] + s_rowf[j0 + q] * ol[q];
             } else if (seg > 0) {
-                const int m = row - 64;
 #pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    p.stash_q[(((size_t)bh * p.NC + c) * 64 + j0 + q) * 64 + m] = __float2half_rn(o[q]);
+                for (int q = 0; q < CW; ++q) sq[(j0 + q) * 64 + row - 64] = __float2half_rn(o[q]);
             }
+        }
+        __syncthreads();
+        {
+            const float *so = reinterpret_cast<const float *>(sm + OFF_E);
+            bool finite = true;
+            for (int e = tid; e < 64 * 16; e += NT) {  // 16-byte groups of 4 outputs
+                const int i = e >> 4, c4 = (e & 15) * 4;
+                if (i >= n) continue;
+                const float4 v = *reinterpret_cast<const float4 *>(so + i * 64 + c4);
+                finite = finite && isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w);
+                const size_t o = (tok0 + i) * D + c4;
+                if (seg == 0) {
+                    if (p.out_f32) {
+                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o) = v;
+                    } else {
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                        uint2 w;
+                        w.x = *reinterpret_cast<uint32_t *>(&lo);
+                        w.y = *reinterpret_cast<uint32_t *>(&hi);
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + o) = w;
+                    }
+                } else {
+                    *reinterpret_cast<float4 *>(p.stash_o + (((size_t)bh * p.NC + c) * 64 + i) * 64 + c4) = v;
+                }
+            }
+            if (seg > 0) {
+                const uint4 *sq = reinterpret_cast<const uint4 *>(sm + OFF_E + 2 * TILE);
+                uint4 *dq = reinterpret_cast<uint4 *>(p.stash_q + ((size_t)bh * p.NC + c) * 4096);
+                for (int e = tid; e < 512; e += NT) dq[e] = sq[e];
+            }
+            if (!finite) set_status(p.status, kDevBounds);  // outside the fp16 operand range
         }
         fence_async_smem();
         fence_before_sync();
@@ -700,7 +763,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
 #ifdef PRISM_PHASE_TIMERS
     if (tid == 0)
-        for (int k = 0; k < 11; ++k) atomicAdd(&prism_tc_phase_cycles[k], ph_acc[k]);
+        for (int k = 0; k < 14; ++k) atomicAdd(&prism_tc_phase_cycles[k], ph_acc[k]);
 #endif
 
     // drain: after an expired wait, let every copy and MMA still in flight land (bounded by
@@ -719,7 +782,8 @@ __global__ void __launch_bounds__(NT, 1)
 
 // ---------------------------------------------------------------------------------------------
 // combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} (fp32), 8 value rows per block; the map
-// of the next segment is prefetched into registers while the current step computes
+// (M and this block's rows of N) of the next segment is prefetched into registers while the
+// current step computes
 constexpr int CB_ROWS = 8;
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ zsum, float *__restrict__ sstart, int P)
 {
@@ -733,12 +797,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
     dst0[c0] = 0.f;
     dst0[c0 + 32] = 0.f;
     if (P < 2) return;
-    // M_{p-1} is rows 64..127 of segment p-1's map; each thread moves 4 float4 of it
+    // M_{p-1} is rows 64..127 of segment p-1's map; each thread moves 4 float4 of it and the
+    // two N values it adds
     float4 pre[4];
-    auto load_m = [&](int sp) {
-        const float4 *src = reinterpret_cast<const float4 *>(zsum + ((size_t)bh * P + sp) * 128 * 64 + 64 * 64);
+    float pn0, pn1;
+    auto load_map = [&](int sp) {
+        const float *z = zsum + ((size_t)bh * P + sp) * 128 * 64;
+        const float4 *src = reinterpret_cast<const float4 *>(z + 64 * 64);
 #pragma unroll
         for (int q = 0; q < 4; ++q) pre[q] = src[tid + 256 * q];
+        pn0 = z[(r0 + r) * 64 + c0];
+        pn1 = z[(r0 + r) * 64 + c0 + 32];
     };
     auto store_m = [&](int buf) {
 #pragma unroll
@@ -747,14 +816,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
             *reinterpret_cast<float4 *>(&M[buf][e >> 6][e & 63]) = pre[q];
         }
     };
-    load_m(0);
+    load_map(0);
     store_m(0);
+    float n0 = pn0, n1 = pn1;
     __syncthreads();
     for (int sp = 1; sp < P; ++sp) {
         const int buf = (sp - 1) & 1;
-        if (sp + 1 < P) load_m(sp);  // map of segment sp, used at step sp + 1
-        const float *N = zsum + ((size_t)bh * P + sp - 1) * 128 * 64 + (size_t)(r0 + r) * 64;
-        float a0 = N[c0], a1 = N[c0 + 32];
+        if (sp + 1 < P) load_map(sp);  // map of segment sp, used at step sp + 1
+        float a0 = n0, a1 = n1;
 #pragma unroll 16
         for (int m = 0; m < 64; ++m) {
             const float sv = S[r][m];
@@ -767,67 +836,93 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
         float *dst = sstart + (((size_t)bh * P + sp) * 64 + r0 + r) * 64;
         dst[c0] = a0;
         dst[c0 + 32] = a1;
-        if (sp + 1 < P) store_m(buf ^ 1);
+        if (sp + 1 < P) {
+            store_m(buf ^ 1);
+            n0 = pn0;
+            n1 = pn1;
+        }
         __syncthreads();
     }
 }
 
-// fixup: o = o0 + Qhat S_start^T for the chunks of segments >= 1; 4x4 outputs per thread
-__global__ void __launch_bounds__(256) fixup_kernel(const float *__restrict__ stash_o, const __half *__restrict__ stash_q,
+// fixup: o = o0 + Qhat S_start^T for the chunks of segments >= 1.  One CTA per (sequence,
+// segment >= 1); the 64x64x64 product of each chunk runs on mma.sync m16n8k16 (fp16 in, fp32
+// accumulate): A = Qhat [i][m] straight from the stash, B[m][c] = S_start[c][m] from shared
+// memory, C initialised with o0.  16 warps: warp w owns rows 16 (w & 3).. and columns 16 (w >> 2)..
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(512) fixup_kernel(const float *__restrict__ stash_o, const __half *__restrict__ stash_q,
                                                     const float *__restrict__ sstart, void *__restrict__ out, int out_f32,
                                                     int T, int NC, int P)
 {
-    __shared__ __align__(16) float St[64][68];  // St[m][c] = S_start[c][m]
-    __shared__ __align__(16) float Qt[64][68];  // Qt[m][i] = Qhat[i][m]
-    const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
-    // segment of chunk c: the largest p with begin(p) <= c
-    int seg = (int)(((long long)c * P) / NC);
-    while (seg + 1 < P && ((long long)(seg + 1) * NC) / P <= c) ++seg;
-    while (seg > 0 && ((long long)seg * NC) / P > c) --seg;
-    if (seg == 0) return;
-    const int t0 = c * 64, n = min(64, T - t0);
+    __shared__ __align__(16) __half Sh[64][72];  // Sh[c][m] = S_start[c][m] (fp16, padded rows)
+    const int bh = blockIdx.x, seg = blockIdx.y + 1, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+    const int c_begin = (int)(((long long)seg * NC) / P), c_end = (int)(((long long)(seg + 1) * NC) / P);
     const float *S = sstart + ((size_t)bh * P + seg) * 64 * 64;
-    const size_t chunk = (size_t)bh * NC + c;
-    for (int e = tid; e < 64 * 64; e += 256) {
-        St[e & 63][e >> 6] = S[e];
-        Qt[e & 63][e >> 6] = __half2float(stash_q[chunk * 4096 + e]);
+    for (int e = tid; e < 64 * 32; e += 512) {
+        const float2 v = reinterpret_cast<const float2 *>(S)[e];
+        *reinterpret_cast<__half2 *>(&Sh[e >> 5][(e & 31) * 2]) = __floats2half2_rn(v.x, v.y);
     }
     __syncthreads();
-    const int i0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
-    float acc[4][4];
+    const int rt = warp & 3, ct = warp >> 2;  // row tile (16 rows), column pair (2 x 8 columns)
+    // B fragments (k = m, n = c): constant over the chunks of the segment
+    uint32_t bf[4][2][2];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const float4 o = *reinterpret_cast<const float4 *>(stash_o + (chunk * 64 + i0 + a) * 64 + c0);
-        acc[a][0] = o.x;
-        acc[a][1] = o.y;
-        acc[a][2] = o.z;
-        acc[a][3] = o.w;
-    }
-#pragma unroll 8
-    for (int m = 0; m < 64; ++m) {
-        const float4 qa = *reinterpret_cast<const float4 *>(&Qt[m][i0]);
-        const float4 sb = *reinterpret_cast<const float4 *>(&St[m][c0]);
-        const float qv[4] = {qa.x, qa.y, qa.z, qa.w}, sv[4] = {sb.x, sb.y, sb.z, sb.w};
+    for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int nt = 0; nt < 2; ++nt) {
+            const int cn = 16 * ct + 8 * nt + gq;
+            bf[ks][nt][0] = *reinterpret_cast<const uint32_t *>(&Sh[cn][16 * ks + 2 * tq]);
+            bf[ks][nt][1] = *reinterpret_cast<const uint32_t *>(&Sh[cn][16 * ks + 2 * tq + 8]);
+        }
+    for (int c = c_begin; c < c_end; ++c) {
+        const size_t chunk = (size_t)bh * NC + c;
+        const int t0 = c * 64, n = min(64, T - t0);
+        const int i0 = 16 * rt + gq, i1 = i0 + 8;
+        const uint32_t *qa = reinterpret_cast<const uint32_t *>(stash_q + chunk * 4096);
+        float acc[2][4];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qv[a], sv[b], acc[a][b]);
-    }
+        for (int nt = 0; nt < 2; ++nt) {
+            const int cc = 16 * ct + 8 * nt + 2 * tq;
+            const float2 o0 = *reinterpret_cast<const float2 *>(stash_o + (chunk * 64 + i0) * 64 + cc);
+            const float2 o1 = *reinterpret_cast<const float2 *>(stash_o + (chunk * 64 + i1) * 64 + cc);
+            acc[nt][0] = o0.x;
+            acc[nt][1] = o0.y;
+            acc[nt][2] = o1.x;
+            acc[nt][3] = o1.y;
+        }
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int i = i0 + a;
-        if (i >= n) continue;
-        const size_t o = ((size_t)bh * T + t0 + i) * 64 + c0;
-        if (out_f32) {
-            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + o) =
-                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-        } else {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[a][0], acc[a][1]);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[a][2], acc[a][3]);
-            uint2 w;
-            w.x = *reinterpret_cast<uint32_t *>(&lo);
-            w.y = *reinterpret_cast<uint32_t *>(&hi);
-            *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + o) = w;
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t a[4];
+            a[0] = qa[(i0 * 64 + 16 * ks + 2 * tq) >> 1];
+            a[1] = qa[(i1 * 64 + 16 * ks + 2 * tq) >> 1];
+            a[2] = qa[(i0 * 64 + 16 * ks + 2 * tq + 8) >> 1];
+            a[3] = qa[(i1 * 64 + 16 * ks + 2 * tq + 8) >> 1];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], a, bf[ks][nt][0], bf[ks][nt][1]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int cc = 16 * ct + 8 * nt + 2 * tq;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int i = h2 ? i1 : i0;
+                if (i >= n) continue;
+                const size_t o = ((size_t)bh * T + t0 + i) * 64 + cc;
+                const float x = acc[nt][2 * h2], y = acc[nt][2 * h2 + 1];
+                if (out_f32)
+                    *reinterpret_cast<float2 *>(reinterpret_cast<float *>(out) + o) = make_float2(x, y);
+                else
+                    *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(out) + o) =
+                        __floats2bfloat162_rn(x, y);
+            }
         }
     }
 }
@@ -955,8 +1050,8 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
         combine_kernel<<<dim3(s.BH, 64 / CB_ROWS), 256, 0, st>>>(w.zsum, w.sstart, w.P);
         tm.end();
         tm.begin("tc_fixup");
-        fixup_kernel<<<dim3(s.NC, s.BH), 256, 0, st>>>(w.stash_o, w.stash_q, w.sstart, a.out, p.out_f32, s.T, s.NC,
-                                                        w.P);
+        fixup_kernel<<<dim3(s.BH, w.P - 1), 512, 0, st>>>(w.stash_o, w.stash_q, w.sstart, a.out, p.out_f32, s.T, s.NC,
+                                                           w.P);
         tm.end();
     }
     return cudaGetLastError();

@@ -65,8 +65,21 @@ __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fenc
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// 32 lanes x 32 consecutive columns (fp32) from TMEM into 32 registers per thread.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+// 32 lanes x N consecutive columns (fp32) from TMEM into N registers per thread (N = 16, 32).
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[32])
 {
     uint32_t r[32];
     asm volatile(
@@ -91,6 +104,13 @@ __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count)
 __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+
+// Adds `bytes` to the barrier's expected transaction count without arriving (a later
+// arrive.expect_tx completes the phase's arrival).
+__device__ __forceinline__ void mbar_add_tx(uint32_t mbar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns()
