@@ -192,19 +192,13 @@ def dist_setup(args):
 
 
 def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    from ssm_sequence_layer_gb300.replicas import barrier as _barrier
+    _barrier(world)
 
 
 def max_over_ranks(x, world):
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from ssm_sequence_layer_gb300.replicas import max_over_ranks as _max
+    return _max(x, world, device="cuda")
 
 
 def oracle_sample(w, inp, seconds_target, nthreads):

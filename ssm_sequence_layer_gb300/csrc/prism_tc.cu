@@ -385,31 +385,39 @@ __global__ void __launch_bounds__(NT, 1)
         {
             const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stage ? OFF_V1 : OFF_V0));
             const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
-#pragma unroll 2
-            for (int k = 0; k < 64 / (NT / 32); ++k) {
+            constexpr int TPT = 64 / (NT / 32);     // tokens per thread
+#pragma unroll
+            for (int k = 0; k < TPT; ++k) {
                 const int i = tg + (NT / 32) * k;
                 const float2 v0 = __bfloat1622float2(vb[(i + 8) * 32 + cp]);
                 const float2 v1 = __bfloat1622float2(vb[(i + 7) * 32 + cp]);
                 const float2 v2 = __bfloat1622float2(vb[(i + 6) * 32 + cp]);
                 const float2 v3 = __bfloat1622float2(vb[(i + 5) * 32 + cp]);
+                const float cf = s_colf[i];
+                float gcl[RMAX], etl[RMAX];
+#pragma unroll
+                for (int l = 0; l < RMAX; ++l) {
+                    gcl[l] = s_gc[i * RMAX + l] * cf;
+                    etl[l] = s_eta[i * RMAX + l];
+                }
                 const float a0 = fmaf(w0.x, v0.x, fmaf(w1.x, v1.x, fmaf(w2.x, v2.x, w3.x * v3.x)));
                 const float a1 = fmaf(w0.y, v0.y, fmaf(w1.y, v1.y, fmaf(w2.y, v2.y, w3.y * v3.y)));
                 float g0, g1, Phi0, Phi1;
                 gelu_gain(a0, g0, Phi0);
                 gelu_gain(a1, g1, Phi1);
                 float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
-                const float cf = s_colf[i];
-                for (int l = 0; l < R; ++l) {
-                    const float gc = s_gc[i * RMAX + l] * cf, et = s_eta[i * RMAX + l];
-                    *reinterpret_cast<uint32_t *>(sm + OFF_XS + l * TILE + sw128(i, 2 * cp)) =
-                        pack2(gc * g0 * r0, gc * g1 * r1);
-                    r0 *= 1.f - et * g0;
-                    r1 *= 1.f - et * g1;
+                uint8_t *xs = sm + OFF_XS + sw128(i, 2 * cp);
+#pragma unroll
+                for (int l = 0; l < RMAX; ++l) {
+                    if (l < R) *reinterpret_cast<uint32_t *>(xs + l * TILE) = pack2(gcl[l] * g0 * r0, gcl[l] * g1 * r1);
+                    r0 *= 1.f - etl[l] * g0;
+                    r1 *= 1.f - etl[l] * g1;
                 }
             }
         }
         fence_async_smem();
         __syncthreads();
+        PHASE_MARK(14);
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
 
@@ -421,24 +429,38 @@ __global__ void __launch_bounds__(NT, 1)
             const float rf = s_rowf[i];
             const float bi = s_beta[i];
             const int nblk = N1 / 64;  // 64-column blocks: 0 = keys, 1.. = levels
-            for (int blk = 0; blk < nblk; ++blk) {
-                const int col0 = blk * 64 + sub * CW;
-                float v[CW];
-                tmem_ld(tmem + TM_D1 + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0, v);
-                const int j0 = sub * CW;
-                if (qside) {
 #pragma unroll
-                    for (int q = 0; q < CW; ++q) v[q] = (j0 + q <= i) ? v[q] : 0.f;
-                    uint8_t *tile = sm + (blk == 0 ? OFF_G : OFF_E + (blk - 1) * 2 * TILE + TILE);
-                    st_row(tile, i, j0, v);
-                } else if (blk == 0) {
-                    float *A = reinterpret_cast<float *>(sm + OFF_AKK);
+            for (int b2 = 0; b2 < 4; b2 += 2) {  // two 64-column blocks per TMEM wait
+                if (b2 >= nblk) break;
+                uint32_t rr[2][CW];
 #pragma unroll
-                    for (int q = 0; q < CW; ++q) A[i * LDAA + j0 + q] = (j0 + q < i) ? v[q] * bi * rf * s_colf[j0 + q] : 0.f;
-                } else {
+                for (int u = 0; u < 2; ++u)
+                    if (b2 + u < nblk)
+                        tmem_ld_nowait(tmem + TM_D1 + ((uint32_t)(quad * 32) << 16) + (uint32_t)((b2 + u) * 64 + sub * CW),
+                                       rr[u]);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < CW; ++q) v[q] = (j0 + q < i) ? v[q] : 0.f;
-                    st_row(sm + OFF_E + (blk - 1) * 2 * TILE, i, j0, v);
+                for (int u = 0; u < 2; ++u) {
+                    const int blk = b2 + u;
+                    if (blk >= nblk) break;
+                    float v[CW];
+                    u2f(rr[u], v);
+                    const int j0 = sub * CW;
+                    if (qside) {
+#pragma unroll
+                        for (int q = 0; q < CW; ++q) v[q] = (j0 + q <= i) ? v[q] : 0.f;
+                        uint8_t *tile = sm + (blk == 0 ? OFF_G : OFF_E + (blk - 1) * 2 * TILE + TILE);
+                        st_row(tile, i, j0, v);
+                    } else if (blk == 0) {
+                        float *A = reinterpret_cast<float *>(sm + OFF_AKK);
+#pragma unroll
+                        for (int q = 0; q < CW; ++q)
+                            A[i * LDAA + j0 + q] = (j0 + q < i) ? v[q] * bi * rf * s_colf[j0 + q] : 0.f;
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < CW; ++q) v[q] = (j0 + q < i) ? v[q] : 0.f;
+                        st_row(sm + OFF_E + (blk - 1) * 2 * TILE, i, j0, v);
+                    }
                 }
             }
         }
@@ -655,12 +677,20 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- E4: Qt = diag(Gamma) Q^T - (G~W)^T ;  Mc = Gamma_C I - W^T K' -------------------------
         if (quad >= 2) {
             const int m = row - 64, j0 = sub * CW;
-            float v[CW];
-            tmem_ld(tmem + TM_D4 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+            float v[CW], v5[CW];
+            {
+                uint32_t r4[CW], r5[CW];
+                tmem_ld_nowait(tmem + TM_D4 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, r4);
+                tmem_ld_nowait(tmem + TM_D5 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, r5);
+                tmem_wait_ld();
+                u2f(r4, v);
+                u2f(r5, v5);
+            }
 #pragma unroll
             for (int q = 0; q < CW; ++q) v[q] = s_gam[j0 + q] * ld_h(sm + OFF_Q, j0 + q, m) - s_rowf[j0 + q] * v[q];
             st_row(sm + OFF_E, m, j0, v);  // Qt [m][i]
-            tmem_ld(tmem + TM_D5 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
+#pragma unroll
+            for (int q = 0; q < CW; ++q) v[q] = v5[q];
             const float gC = __expf(lc);
 #pragma unroll
             for (int q = 0; q < CW; ++q) v[q] = ((j0 + q) == m ? gC : 0.f) - v[q];
@@ -695,16 +725,25 @@ __global__ void __launch_bounds__(NT, 1)
             const int j0 = sub * CW;
             const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
             float z[CW], nc[CW], o[CW], ol[CW];
-            tmem_ld(tmem + TM_D6 + lane_off + (uint32_t)j0, z);
-            tmem_ld(tmem + TM_D5 + lane_off + (uint32_t)j0, nc);
-            tmem_ld(tmem + TM_D7 + lane_off + (uint32_t)j0, o);
-            tmem_ld(tmem + TM_D4 + lane_off + (uint32_t)j0, ol);
+            {
+                uint32_t r0[CW], r1[CW], r2[CW], r3[CW];
+                tmem_ld_nowait(tmem + TM_D6 + lane_off + (uint32_t)j0, r0);
+                tmem_ld_nowait(tmem + TM_D5 + lane_off + (uint32_t)j0, r1);
+                tmem_ld_nowait(tmem + TM_D7 + lane_off + (uint32_t)j0, r2);
+                tmem_ld_nowait(tmem + TM_D4 + lane_off + (uint32_t)j0, r3);
+                tmem_wait_ld();
+                u2f(r0, z);
+                u2f(r1, nc);
+                u2f(r2, o);
+                u2f(r3, ol);
+            }
             if (row < 64) {
 #pragma unroll
                 for (int q = 0; q < CW; ++q) z[q] += nc[q];
             }
             fence_before_sync();
             __syncthreads();  // MMAs reading ZA are complete (waited above); all rows loaded
+            PHASE_MARK(15);
             st_row(sm + OFF_ZA, row, j0, z);
             if (c + 1 == c_end) {
                 float *zs = p.zsum + (((size_t)bh * p.P + seg) * 128 + row) * 64 + j0;
@@ -763,7 +802,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
 #ifdef PRISM_PHASE_TIMERS
     if (tid == 0)
-        for (int k = 0; k < 14; ++k) atomicAdd(&prism_tc_phase_cycles[k], ph_acc[k]);
+        for (int k = 0; k < 16; ++k) atomicAdd(&prism_tc_phase_cycles[k], ph_acc[k]);
 #endif
 
     // drain: after an expired wait, let every copy and MMA still in flight land (bounded by
