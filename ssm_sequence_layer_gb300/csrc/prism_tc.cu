@@ -29,8 +29,9 @@
 // The decay factors of every masked product multiply to e^{lambda_i - lambda_j} <= 1; a
 // chunk whose total decay exceeds 80 nats (rowf would leave fp32 range) sets the status word.
 // All matrix products above run on tcgen05.mma (fp16 operands in 128B-swizzled shared memory,
-// fp32 accumulators in tensor memory); operands come from TMA or from the epilogues.  The bf16
-// input tiles are converted to fp16 in place (exact for unit-scale rows): fp16's 10-bit
+// fp32 accumulators in tensor memory); operands come from TMA or from the epilogues.  The Gram
+// runs on the bf16 input tiles; K and U are then converted to fp16 in place (exact for
+// unit-scale rows) for the state-side products: fp16's 10-bit
 // mantissa keeps the computed operands (scores, Xs, T, U'/W, Q~, M_c, Z) 8x closer to fp32
 // than bf16 would, at the same tensor-core rate.  Row factors >= 1 (e^{lambda_i - lc},
 // beta_i) are kept out of the operands and applied to the accumulators in the epilogues, so
@@ -86,12 +87,19 @@ constexpr uint32_t OFF_TB = OFF_T32 + 64 * LDA * 4;  // T (bf16 tile)
 constexpr uint32_t OFF_XS = OFF_TB + TILE;            // Xs0..Xs2
 constexpr uint32_t OFF_ZERO = OFF_XS + RMAX * TILE;   // zero tile
 constexpr uint32_t OFF_ZA = OFF_ZERO + TILE;          // Z (128 rows, bf16, K-major)
-constexpr uint32_t OFF_SC = OFF_ZA + 2 * TILE;        // per-token scalars
-constexpr uint32_t SC_FLOATS = 64 * 6 + 64 * RMAX * 2 + 3 * 256 + 8;
+constexpr uint32_t OFF_BGK = OFF_ZA + 2 * TILE;       // diag(beta Gamma) K (fp16 tile)
+constexpr uint32_t OFF_SC = OFF_BGK + TILE;           // per-token scalars
+constexpr uint32_t SC_SET = 64 * 6 + 64 * RMAX * 2;         // per-token scalars of one chunk
+constexpr uint32_t XTMP_FLOATS = 4 * 256;                     // solve scratch: 4 warps x 32 x 8
+constexpr uint32_t SC_FLOATS = 2 * SC_SET + XTMP_FLOATS;       // two chunks' sets + solve scratch
 constexpr uint32_t SMEM_BYTES = OFF_SC + SC_FLOATS * 4 + 1024;  // + alignment slack
 
-static_assert(OFF_AKK % 1024 == 0 && OFF_TB % 1024 == 0 && OFF_XS % 1024 == 0 && OFF_ZA % 1024 == 0, "align");
+static_assert(OFF_AKK % 1024 == 0 && OFF_TB % 1024 == 0 && OFF_XS % 1024 == 0 && OFF_ZA % 1024 == 0 &&
+                  OFF_BGK % 1024 == 0,
+              "align");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// the solve's scratch: level 1 uses 4 warps x 16 x 8 floats, level 2 4 warps x 32 x 8 floats
+static_assert(4 * 128 <= XTMP_FLOATS && 4 * 256 <= XTMP_FLOATS, "solve scratch");
 
 // TMEM column map
 constexpr uint32_t TM_D1 = 0, TM_D2 = 256, TM_D3 = 320, TM_D4 = 384, TM_D5 = 448, TM_D6 = 0, TM_D7 = 64;
@@ -101,7 +109,7 @@ struct SegParams {
     const __nv_bfloat16 *conv_w;
     void *out;              // bf16, or fp32 when out_f32
     float *zsum;            // [BH][P][128][64]
-    float *stash_o;         // [BH][NC][64][64]  o0 (token-major)
+    void *stash_o;          // [BH][NC][64][64]  o0 (token-major; fp32 for fp32 output, else fp16)
     __half *stash_q;        // [BH][NC][64][64]  Qhat (token-major)
     int *status;
     int H, T, R, NC, P;
@@ -133,9 +141,9 @@ __device__ __forceinline__ void st_row(uint8_t *tile, int row, int col0, const f
     }
 }
 
-__device__ __forceinline__ float ld_h(const uint8_t *tile, int row, int col)
+__device__ __forceinline__ float ld_bf(const uint8_t *tile, int row, int col)
 {
-    return __half2float(*reinterpret_cast<const __half *>(tile + sw128(row, col)));
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128(row, col)));
 }
 
 // Gain g = GELU'(a) = Phi(a) + a phi(a) and Phi(a), for the exact-erf GELU.  Phi uses the
@@ -171,6 +179,73 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// m16n8k8 tf32 fragments of fp32 matrices in shared memory (row-major, row stride ld):
+// A: 16 rows from r0, 8 columns from k0; B: 8 rows (k) from k0, 8 columns (n) from n0.
+struct Frag {
+    int gq, tq;  // lane / 4, lane % 4
+};
+__device__ __forceinline__ void frag_a(const Frag &f, const float *M, int ld, int r0, int k0, uint32_t (&a)[4])
+{
+    const float *p = M + (r0 + f.gq) * ld + k0 + f.tq;
+    a[0] = to_tf32(p[0]);
+    a[1] = to_tf32(p[8 * ld]);
+    a[2] = to_tf32(p[4]);
+    a[3] = to_tf32(p[8 * ld + 4]);
+}
+__device__ __forceinline__ void frag_b(const Frag &f, const float *M, int ld, int k0, int n0, uint32_t &b0, uint32_t &b1)
+{
+    const float *p = M + (k0 + f.tq) * ld + n0 + f.gq;
+    b0 = to_tf32(p[0]);
+    b1 = to_tf32(p[4 * ld]);
+}
+__device__ __forceinline__ void frag_c_load(const Frag &f, const float *M, int ld, int r0, int n0, float (&c)[4])
+{
+    const float *p = M + (r0 + f.gq) * ld + n0 + 2 * f.tq;
+    c[0] = p[0];
+    c[1] = p[1];
+    c[2] = p[8 * ld];
+    c[3] = p[8 * ld + 1];
+}
+__device__ __forceinline__ void frag_c_store(const Frag &f, float *M, int ld, int r0, int n0, const float (&c)[4], float sgn)
+{
+    float *p = M + (r0 + f.gq) * ld + n0 + 2 * f.tq;
+    p[0] = sgn * c[0];
+    p[1] = sgn * c[1];
+    p[8 * ld] = sgn * c[2];
+    p[8 * ld + 1] = sgn * c[3];
+}
+
+// C (16x16, stride ldc) = init + A (16x16, stride lda) B (16x16, stride ldb), one warp; all reads
+// happen before the warp's writes, so C may alias A or the initial value (in-place update).
+__device__ __forceinline__ void mm16_warp(const Frag &f, float *Cm, int ldc, const float *Am, int lda, const float *Bm,
+                                          int ldb, bool init_from_c)
+{
+    float c[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        if (init_from_c) {
+            frag_c_load(f, Cm, ldc, 0, 8 * nt, c[nt]);
+        } else {
+            c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        uint32_t a[4];
+        frag_a(f, Am, lda, 0, 8 * ks, a);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1;
+            frag_b(f, Bm, ldb, 8 * ks, 8 * nt, b0, b1);
+            mma_tf32(c[nt], a[0], a[1], a[2], a[3], b0, b1);
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) frag_c_store(f, Cm, ldc, 0, 8 * nt, c[nt], 1.f);
+    __syncwarp();
 }
 
 // in-place bf16 -> fp16 conversion of `bytes` bytes of tiles (layout unchanged)
@@ -210,15 +285,11 @@ __global__ void __launch_bounds__(NT, 1)
     const int c_end = (int)(((long long)(seg + 1) * p.NC) / p.P);
 
     float *sc = reinterpret_cast<float *>(sm + OFF_SC);
-    float *s_beta = sc;             // 64
-    float *s_lam = sc + 64;         // 64
-    float *s_rowf = sc + 128;       // e^{lambda_i - lc}
-    float *s_colf = sc + 192;       // e^{lc - lambda_i}
-    float *s_gam = sc + 256;        // Gamma_i = e^{lambda_i}
-    float *s_bg = sc + 320;         // beta_i Gamma_i
-    float *s_gc = sc + 384;         // gamma_{i,l} e^{lc - lambda_i}   [64][RMAX]
-    float *s_eta = s_gc + 64 * RMAX;  // [64][RMAX]
-    float *s_xtmp = s_eta + 64 * RMAX;  // 3 x 256 scratch of the solve
+    // per-token scalars, one set per chunk parity (the next chunk's set is filled while the
+    // state-side MMAs of the current one run):
+    //   beta | lambda | rowf = e^{lambda_i - lc} | colf = e^{lc - lambda_i} | Gamma_i | beta_i Gamma_i
+    //   | gamma [64][RMAX] | eta [64][RMAX]
+    float *s_xtmp = sc + 2 * SC_SET;  // XTMP_FLOATS of scratch for the solve
 
     const uint32_t sbase = smem_u32(sm);
     const uint32_t mb_mma = smem_u32(&mbar[0]), mb_qku = smem_u32(&mbar[1]);
@@ -269,6 +340,26 @@ __global__ void __launch_bounds__(NT, 1)
     // collective bounded wait on an mbarrier phase; on expiry the CTA records the timeout
     // status and leaves the chunk loop (the phase is kept so the drain can wait for it)
     // (thread 0 polls; the rest of the CTA waits at the barrier, issuing nothing)
+    auto wait_two = [&](uint32_t mb0, uint32_t &ph0, uint32_t bit0, uint32_t mb1, uint32_t &ph1, uint32_t bit1) -> bool {
+        if (tid == 0) {
+            const bool ok0 = mbar_wait(mb0, ph0, p.wait_ns);
+            const bool ok1 = ok0 && mbar_wait(mb1, ph1, p.wait_ns);
+            if (ok0) {
+                ph0 ^= 1u;
+                pending &= ~bit0;
+            }
+            if (ok1) {
+                ph1 ^= 1u;
+                pending &= ~bit1;
+            }
+            if (!ok1) {
+                abort_s = 1;
+                set_status(p.status, kDevTimeout);
+            }
+        }
+        __syncthreads();
+        return abort_s == 0;
+    };
     auto wait_all = [&](uint32_t mb, uint32_t &phase, uint32_t bit) -> bool {
         if (tid == 0) {
             if (mbar_wait(mb, phase, p.wait_ns)) {
@@ -314,6 +405,38 @@ __global__ void __launch_bounds__(NT, 1)
         }
     };
     if (c_begin < c_end) load_gates(c_begin);
+    // gates in registers -> one set of per-token scalars (no barrier inside)
+    auto fill_scalars = [&](float *set) {
+        if (warp == 0) {  // inclusive scan of the 64 log-decays, two per lane, in registers
+            const float la0 = logf(pf_a0), la1 = logf(pf_a1);
+            float s = la0 + la1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, s, off);
+                if (lane >= off) s += y;
+            }
+            const float l1 = s, l0 = s - la1;
+            const float lcw = __shfl_sync(0xffffffffu, s, 31);
+            const int i0 = 2 * lane, i1 = i0 + 1;
+            set[i0] = pf_b0;
+            set[i1] = pf_b1;
+            set[64 + i0] = l0;
+            set[64 + i1] = l1;
+            set[128 + i0] = __expf(l0 - lcw);
+            set[128 + i1] = __expf(l1 - lcw);
+            set[192 + i0] = __expf(lcw - l0);
+            set[192 + i1] = __expf(lcw - l1);
+            set[256 + i0] = __expf(l0);
+            set[256 + i1] = __expf(l1);
+            set[320 + i0] = pf_b0 * __expf(l0);
+            set[320 + i1] = pf_b1 * __expf(l1);
+            if (lane == 31 && -lcw > 80.f) set_status(p.status, kDevBounds);  // beyond the factorised range
+        }
+        if (tid < 64 * RMAX) {
+            set[384 + tid] = pf_gam;
+            set[384 + 64 * RMAX + tid] = pf_eta;
+        }
+    };
 
 #ifdef PRISM_PHASE_TIMERS
     unsigned long long ph_acc[16] = {0};
@@ -326,50 +449,25 @@ __global__ void __launch_bounds__(NT, 1)
         const int n = min(C, p.T - t0);
         const size_t tok0 = (size_t)bh * p.T + t0;
 
-        // ---- P0: gates (prefetched into registers one chunk ahead) and decay factors ----------
-        if (warp == 0) {  // inclusive scan of the 64 log-decays, two per lane, in registers
-            const float la0 = logf(pf_a0), la1 = logf(pf_a1);
-            float s = la0 + la1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, s, off);
-                if (lane >= off) s += y;
-            }
-            const float l1 = s, l0 = s - la1;
-            const float lcw = __shfl_sync(0xffffffffu, s, 31);
-            const int i0 = 2 * lane, i1 = i0 + 1;
-            s_beta[i0] = pf_b0;
-            s_beta[i1] = pf_b1;
-            s_lam[i0] = l0;
-            s_lam[i1] = l1;
-            s_rowf[i0] = __expf(l0 - lcw);
-            s_rowf[i1] = __expf(l1 - lcw);
-            s_colf[i0] = __expf(lcw - l0);
-            s_colf[i1] = __expf(lcw - l1);
-            s_gam[i0] = __expf(l0);
-            s_gam[i1] = __expf(l1);
-            s_bg[i0] = pf_b0 * __expf(l0);
-            s_bg[i1] = pf_b1 * __expf(l1);
-            if (lane == 31 && -lcw > 80.f) set_status(p.status, kDevBounds);  // beyond the factorised range
+        float *const set = sc + (c & 1) * SC_SET;
+        float *const s_beta = set, *const s_lam = set + 64, *const s_rowf = set + 128, *const s_colf = set + 192;
+        float *const s_gam = set + 256, *const s_bg = set + 320, *const s_gc = set + 384;
+        float *const s_eta = s_gc + 64 * RMAX;
+        if (c == c_begin) {  // the first chunk's scalars; later ones are filled during the previous chunk
+            fill_scalars(set);
+            if (c + 1 < c_end) load_gates(c + 1);
+            __syncthreads();
         }
-        if (tid < 64 * RMAX) {
-            s_gc[tid] = pf_gam;
-            s_eta[tid] = pf_eta;
-        }
-        if (c + 1 < c_end) load_gates(c + 1);
-        __syncthreads();
         const float lc = s_lam[63];
 
         PHASE_MARK(0);
         // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T (runs while the CTA does the prep) ----------
-        if (!wait_all(mb_qku, ph_qku, 2u)) break;
-        tiles_bf16_to_f16(sm + OFF_Q, (2 + R) * TILE, tid);
-        fence_async_smem();
-        __syncthreads();
+        if (!wait_two(mb_qku, ph_qku, 2u, mb_v[stage], ph_v[stage], 4u << stage)) break;
+        if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
         const int N1 = 64 * (1 + R);
-        if (tid == 0) {
+        if (tid == 0) {  // the input tiles are still bf16 here (exact values); the Gram runs on them
             fence_after_sync();
-            const uint32_t id = idesc_f16(128, N1, 0, 0);
+            const uint32_t id = idesc_bf16(128, N1, 0, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_f16(tmem + TM_D1, sdesc(sbase + OFF_Q + s * 32, 16, 1024), sdesc(sbase + OFF_K + s * 32, 16, 1024),
@@ -380,8 +478,6 @@ __global__ void __launch_bounds__(NT, 1)
 
         PHASE_MARK(1);
         // ---- P1: prep -> Xs tiles (two channels x 8 tokens per thread) --------------------------
-        if (!wait_all(mb_v[stage], ph_v[stage], 4u << stage)) break;
-        if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
         {
             const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stage ? OFF_V1 : OFF_V0));
             const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
@@ -415,11 +511,26 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
         }
+        {  // diag(beta Gamma) K, one 16-byte group of 8 per thread (K still bf16)
+            const int j = tid >> 3, m0 = (tid & 7) * 8;
+            uint4 w = *reinterpret_cast<const uint4 *>(sm + OFF_K + sw128(j, m0));
+            uint32_t *pw = &w.x;
+            const float sbg = s_bg[j];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pw[q]));
+                pw[q] = pack2(sbg * f.x, sbg * f.y);
+            }
+            *reinterpret_cast<uint4 *>(sm + OFF_BGK + sw128(j, m0)) = w;
+        }
         fence_async_smem();
         __syncthreads();
         PHASE_MARK(14);
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
+        // the Gram has read K and U: convert them to fp16 in place for the state-side MMA (their
+        // fence and barrier are E1's)
+        tiles_bf16_to_f16(sm + OFF_K, (1 + R) * TILE, tid);
 
         PHASE_MARK(2);
         // ---- E1: masks and decay factors -> A (fp32), PK_l, PQ_l, G (bf16 tiles) ---------------
@@ -486,77 +597,103 @@ __global__ void __launch_bounds__(NT, 1)
             // block diagonals below them, T[bi][bj] = -T[bi][bi] sum_{k=bj..bi-1} A[bi][k] T[k][bj]
             const float *A = reinterpret_cast<const float *>(sm + OFF_AKK);
             float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
-            if (tid < 64) {  // one column of one diagonal block per thread
-                const int o = 16 * (tid >> 4), cc = tid & 15;
-                float t[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    // t[j] = 0 for j < cc, so the sum may run over all j < r
-                    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                    for (int j = 0; j + 1 < r; j += 2) {
-                        s0 = fmaf(A[(o + r) * LDAA + o + j], t[j], s0);
-                        s1 = fmaf(A[(o + r) * LDAA + o + j + 1], t[j + 1], s1);
-                    }
-                    if (r & 1) s0 = fmaf(A[(o + r) * LDAA + o + r - 1], t[r - 1], s0);
-                    t[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -(s0 + s1));
-                    T32[(o + r) * LDA + o + cc] = t[r];
+            const Frag fr{lane >> 2, lane & 3};
+            if (warp < 4) {
+                // diagonal block b: (I + N)^{-1} = (I - N)(I + N^2)(I + N^4)(I + N^8) (N strictly lower,
+                // N^16 = 0), on mma.sync; scratch in the unused upper blocks of T32 and A
+                const int b = warp, o = 16 * b;
+                const int ub = (b == 3) ? 0 : o, un = (b == 3) ? 48 : o + 16;  // an upper block (ub, un)
+                const float *N = A + o * LDAA + o;
+                float *Td = T32 + o * LDA + o;
+                float *P0 = T32 + ub * LDA + un;
+                float *P1 = const_cast<float *>(A) + ub * LDAA + un;
+                for (int e = lane; e < 256; e += 32) {
+                    const int r = e >> 4, cc = e & 15;
+                    Td[r * LDA + cc] = (r == cc ? 1.f : 0.f) - N[r * LDAA + cc];
                 }
+                mm16_warp(fr, P0, LDA, N, LDAA, N, LDAA, false);    // P0 = N^2
+                mm16_warp(fr, Td, LDA, Td, LDA, P0, LDA, true);     // T += T N^2
+                mm16_warp(fr, P1, LDAA, P0, LDA, P0, LDA, false);   // P1 = N^4
+                mm16_warp(fr, Td, LDA, Td, LDA, P1, LDAA, true);    // T += T N^4
+                mm16_warp(fr, P0, LDA, P1, LDAA, P1, LDAA, false);  // P0 = N^8
+                mm16_warp(fr, Td, LDA, Td, LDA, P0, LDA, true);     // T += T N^8
             }
             __syncthreads();
             PHASE_MARK(11);
-            // block diagonals below: one warp per 16x16 block, products on mma.sync (tf32 in,
-            // fp32 accumulate); X goes through the warp's scratch to become a B operand
-            for (int d = 1; d < 4; ++d) {
-                if (warp < 4 - d) {
-                    const int bj = warp, bi = warp + d;
-                    const int gq = lane >> 2, tq = lane & 3;
-                    float *X = s_xtmp + warp * 256;  // [16][16]
-                    float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    for (int kb = bj; kb < bi; ++kb) {  // X = sum_kb A[bi][kb] T[kb][bj]
+            if (warp < 4) {
+                // 16 -> 32: T[1][0] = -T[1][1] A[1][0] T[0][0], T[3][2] likewise; warp w owns one
+                // 8-column tile of one block
+                const int pb = warp >> 1, nt = warp & 1;         // block pair (0: rows 16.., 1: rows 48..)
+                const int ri = 16 + 32 * pb, cj = 32 * pb;        // block (ri, cj) below the diagonal
+                float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-                            const float *ar = A + (16 * bi + gq) * LDAA + 16 * kb + 8 * ks + tq;
-                            const uint32_t a0 = to_tf32(ar[0]), a1 = to_tf32(ar[8 * LDAA]);
-                            const uint32_t a2 = to_tf32(ar[4]), a3 = to_tf32(ar[8 * LDAA + 4]);
+                for (int ks = 0; ks < 2; ++ks) {                 // X = A[ri][cj] T[cj][cj] (cols 8 nt..)
+                    uint32_t a[4], b0, b1;
+                    frag_a(fr, A, LDAA, ri, cj + 8 * ks, a);
+                    frag_b(fr, T32, LDA, cj + 8 * ks, cj + 8 * nt, b0, b1);
+                    mma_tf32(x, a[0], a[1], a[2], a[3], b0, b1);
+                }
+                float *X = s_xtmp + warp * 128;                   // 16 x 8
+                X[fr.gq * 8 + 2 * fr.tq] = x[0];
+                X[fr.gq * 8 + 2 * fr.tq + 1] = x[1];
+                X[(fr.gq + 8) * 8 + 2 * fr.tq] = x[2];
+                X[(fr.gq + 8) * 8 + 2 * fr.tq + 1] = x[3];
+                __syncwarp();
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                            for (int nt = 0; nt < 2; ++nt) {
-                                const float *br = T32 + (16 * kb + 8 * ks + tq) * LDA + 16 * bj + 8 * nt + gq;
-                                mma_tf32(c[nt], a0, a1, a2, a3, to_tf32(br[0]), to_tf32(br[4 * LDA]));
-                            }
-                        }
-                    }
+                for (int ks = 0; ks < 2; ++ks) {                 // T[ri][cj] = -T[ri][ri] X
+                    uint32_t a[4], b0, b1;
+                    frag_a(fr, T32, LDA, ri, ri + 8 * ks, a);
+                    frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
+                    mma_tf32(y, a[0], a[1], a[2], a[3], b0, b1);
+                }
+                frag_c_store(fr, T32, LDA, ri, cj + 8 * nt, y, -1.f);
+            }
+            __syncthreads();
+            if (warp < 4) {
+                // 32 -> 64: T[32:64][0:32] = -T[32:64][32:64] A[32:64][0:32] T[0:32][0:32]; warp w owns
+                // the 8-column tile 8 w of the 32x32 block (both 16-row halves)
+                const int n0 = 8 * warp;
+                float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                // T_lo[k][n] = 0 for k < 16 <= n: block (0,1) of T32 holds scratch, so skip it
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        X[gq * 16 + 8 * nt + 2 * tq] = c[nt][0];
-                        X[gq * 16 + 8 * nt + 2 * tq + 1] = c[nt][1];
-                        X[(gq + 8) * 16 + 8 * nt + 2 * tq] = c[nt][2];
-                        X[(gq + 8) * 16 + 8 * nt + 2 * tq + 1] = c[nt][3];
-                    }
-                    __syncwarp();
-                    float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // T[bi][bi] X
+                for (int ks = 0; ks < 4; ++ks) {                 // X = A_lo T_lo
+                    if (n0 >= 16 && ks < 2) continue;
+                    uint32_t b0, b1;
+                    frag_b(fr, T32, LDA, 8 * ks, n0, b0, b1);
 #pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const float *ar = T32 + (16 * bi + gq) * LDA + 16 * bi + 8 * ks + tq;
-                        const uint32_t a0 = to_tf32(ar[0]), a1 = to_tf32(ar[8 * LDA]);
-                        const uint32_t a2 = to_tf32(ar[4]), a3 = to_tf32(ar[8 * LDA + 4]);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            const float *br = X + (8 * ks + tq) * 16 + 8 * nt + gq;
-                            mma_tf32(e[nt], a0, a1, a2, a3, to_tf32(br[0]), to_tf32(br[4 * 16]));
-                        }
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        float *tr = T32 + (16 * bi + gq) * LDA + 16 * bj + 8 * nt + 2 * tq;
-                        tr[0] = -e[nt][0];
-                        tr[1] = -e[nt][1];
-                        tr[8 * LDA] = -e[nt][2];
-                        tr[8 * LDA + 1] = -e[nt][3];
+                    for (int mt = 0; mt < 2; ++mt) {
+                        uint32_t a[4];
+                        frag_a(fr, A, LDAA, 32 + 16 * mt, 8 * ks, a);
+                        mma_tf32(x[mt], a[0], a[1], a[2], a[3], b0, b1);
                     }
                 }
-                __syncthreads();
+                float *X = s_xtmp + warp * 256;                   // 32 x 8
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    X[(16 * mt + fr.gq) * 8 + 2 * fr.tq] = x[mt][0];
+                    X[(16 * mt + fr.gq) * 8 + 2 * fr.tq + 1] = x[mt][1];
+                    X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq] = x[mt][2];
+                    X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq + 1] = x[mt][3];
+                }
+                __syncwarp();
+                float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {                 // T_lower = -T_hi X
+                    uint32_t b0, b1;
+                    frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        if (mt == 0 && ks >= 2) continue;  // T_hi[0:16][16:32] = 0 (block (2,3) holds scratch)
+                        uint32_t a[4];
+                        frag_a(fr, T32, LDA, 32 + 16 * mt, 32 + 8 * ks, a);
+                        mma_tf32(y[mt], a[0], a[1], a[2], a[3], b0, b1);
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) frag_c_store(fr, T32, LDA, 32 + 16 * mt, n0, y[mt], -1.f);
             }
+            __syncthreads();
             PHASE_MARK(12);
             for (int e = tid; e < 64 * 8; e += NT) {  // T (fp16, [i][j], zero above the diagonal)
                 const int i = e >> 3, g = e & 7;
@@ -579,7 +716,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_after_sync();
 
         PHASE_MARK(4);
-        // ---- E2: RHS = diag(beta) V - MX, and diag(beta Gamma) K -------------------------------
+        // ---- E2: RHS = diag(beta) V - MX (diag(beta Gamma) K was formed during the prep) ---------
         {
             const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + (stage ? OFF_V1 : OFF_V0));
             if (quad < 2) {  // lanes 0..63 hold MX rows
@@ -595,14 +732,6 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int q = 0; q < CW; ++q) v[q] = bi * __bfloat162float(vb[(i + 8) * 64 + j0 + q]) - brf * v[q];
                 st_row(sm + OFF_AKK, i, j0, v);  // RHS tile (A is dead after the solve)
-            } else {
-                const int tt = sub * 64 + (quad - 2) * 32 + lane;  // 0..255 over the warps of quads 2, 3
-                const int j = tt >> 2, m0 = (tt & 3) * CW;
-                float v[CW];
-                const float s = s_bg[j];
-#pragma unroll
-                for (int q = 0; q < CW; ++q) v[q] = s * ld_h(sm + OFF_K, j, m0 + q);
-                st_row(sm + OFF_AKK + TILE, j, m0, v);  // BGK tile
             }
         }
         fence_async_smem();
@@ -616,7 +745,8 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t id = idesc_f16(128, 64, 1, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_D3, sdesc(sbase + OFF_AKK + s * 2048, TILE, 1024), sdesc(sbase + OFF_TB + s * 32, 16, 1024),
+                mma_f16(tmem + TM_D3, sdesc(sbase + OFF_AKK + s * 2048, OFF_BGK - OFF_AKK, 1024),
+                        sdesc(sbase + OFF_TB + s * 32, 16, 1024),
                          id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
@@ -632,9 +762,7 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_ld(tmem + TM_D3 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
 #pragma unroll
             for (int q = 0; q < CW; ++q) v[q] *= s_colf[j0 + q];
-            fence_before_sync();
-            __syncthreads();  // every thread has read D3; RHS|BGK are dead (MMA done)
-            st_row(sm + OFF_AKK, row, j0, v);
+            st_row(sm + OFF_AKK, row, j0, v);  // over RHS: MMA3, its only reader, has completed
         }
         fence_async_smem();
         fence_before_sync();
@@ -664,6 +792,10 @@ __global__ void __launch_bounds__(NT, 1)
             mma_commit(mb_mma);
             pending |= 1u;
         }
+        if (c + 1 < c_end) {  // next chunk's per-token scalars while the MMAs run
+            fill_scalars(sc + ((c + 1) & 1) * SC_SET);
+            if (c + 2 < c_end) load_gates(c + 2);
+        }
         if (!wait_all(mb_mma, ph_mma, 1u)) break;
         fence_after_sync();
 
@@ -687,7 +819,7 @@ __global__ void __launch_bounds__(NT, 1)
                 u2f(r5, v5);
             }
 #pragma unroll
-            for (int q = 0; q < CW; ++q) v[q] = s_gam[j0 + q] * ld_h(sm + OFF_Q, j0 + q, m) - s_rowf[j0 + q] * v[q];
+            for (int q = 0; q < CW; ++q) v[q] = s_gam[j0 + q] * ld_bf(sm + OFF_Q, j0 + q, m) - s_rowf[j0 + q] * v[q];
             st_row(sm + OFF_E, m, j0, v);  // Qt [m][i]
 #pragma unroll
             for (int q = 0; q < CW; ++q) v[q] = v5[q];
@@ -741,10 +873,10 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int q = 0; q < CW; ++q) z[q] += nc[q];
             }
-            fence_before_sync();
-            __syncthreads();  // MMAs reading ZA are complete (waited above); all rows loaded
+            // ZA and the region holding Qt/Mc are rewritten below: MMA6/7, their readers, are complete
             PHASE_MARK(15);
             st_row(sm + OFF_ZA, row, j0, z);
+            fence_async_smem();  // ZA is the next chunk's MMA operand; nothing after this needs the fence
             if (c + 1 == c_end) {
                 float *zs = p.zsum + (((size_t)bh * p.P + seg) * 128 + row) * 64 + j0;
 #pragma unroll
@@ -783,8 +915,16 @@ __global__ void __launch_bounds__(NT, 1)
                         w.y = *reinterpret_cast<uint32_t *>(&hi);
                         *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + o) = w;
                     }
+                } else if (p.out_f32) {
+                    *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.stash_o) +
+                                                (((size_t)bh * p.NC + c) * 64 + i) * 64 + c4) = v;
                 } else {
-                    *reinterpret_cast<float4 *>(p.stash_o + (((size_t)bh * p.NC + c) * 64 + i) * 64 + c4) = v;
+                    __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+                    uint2 w;
+                    w.x = *reinterpret_cast<uint32_t *>(&lo);
+                    w.y = *reinterpret_cast<uint32_t *>(&hi);
+                    *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(p.stash_o) +
+                                               (((size_t)bh * p.NC + c) * 64 + i) * 64 + c4) = w;
                 }
             }
             if (seg > 0) {
@@ -794,7 +934,6 @@ __global__ void __launch_bounds__(NT, 1)
             }
             if (!finite) set_status(p.status, kDevBounds);  // outside the fp16 operand range
         }
-        fence_async_smem();
         fence_before_sync();
         __syncthreads();
         alive = abort_s == 0;
@@ -820,74 +959,92 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} (fp32), 8 value rows per block; the map
-// (M and this block's rows of N) of the next segment is prefetched into registers while the
-// current step computes
+// combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} (fp32), 8 value rows per block.  The maps
+// stream through a ring of CB_STAGES shared-memory stages filled by bulk copies (16 KB of M and
+// this block's 2 KB of N per segment), so the serial chain never waits on global memory latency.
 constexpr int CB_ROWS = 8;
-__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ zsum, float *__restrict__ sstart, int P)
+constexpr int CB_STAGES = 4;
+constexpr int CB_THREADS = 128;  // 8 rows x 16 groups of 4 columns
+constexpr int CB_STAGE_FLOATS = 64 * 64 + CB_ROWS * 64;
+constexpr size_t CB_SMEM = (size_t)CB_STAGES * CB_STAGE_FLOATS * 4 + 128;
+
+__global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__restrict__ zsum, float *__restrict__ sstart,
+                                                             int P, int *status, unsigned long long wait_ns)
 {
-    __shared__ __align__(16) float M[2][64][68];
-    __shared__ float S[CB_ROWS][68];
+    extern __shared__ __align__(128) float ring[];  // [CB_STAGES][M 64x64 | N 8x64]
+    __shared__ __align__(8) uint64_t mb[CB_STAGES];
+    __shared__ float S[CB_ROWS][65];
+    __shared__ int abort_s;
     const int bh = blockIdx.x, r0 = blockIdx.y * CB_ROWS, tid = threadIdx.x;
-    const int r = tid >> 5, c0 = tid & 31;  // outputs (r, c0) and (r, c0 + 32)
-    S[r][c0] = 0.f;
-    S[r][c0 + 32] = 0.f;
-    float *dst0 = sstart + ((size_t)bh * P * 64 + r0 + r) * 64;
-    dst0[c0] = 0.f;
-    dst0[c0 + 32] = 0.f;
+    const int r = tid >> 4, c4 = (tid & 15) * 4;  // outputs (r, c4 .. c4 + 3)
+    float *dst0 = sstart + ((size_t)bh * P * 64 + r0 + r) * 64 + c4;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        S[r][c4 + q] = 0.f;
+        dst0[q] = 0.f;
+    }
     if (P < 2) return;
-    // M_{p-1} is rows 64..127 of segment p-1's map; each thread moves 4 float4 of it and the
-    // two N values it adds
-    float4 pre[4];
-    float pn0, pn1;
-    auto load_map = [&](int sp) {
+    const int nmaps = P - 1;  // maps of segments 0..P-2 are used
+    auto issue = [&](int sp) {
+        const int st = sp % CB_STAGES;
+        const uint32_t m = prism::tc::smem_u32(&mb[st]);
         const float *z = zsum + ((size_t)bh * P + sp) * 128 * 64;
-        const float4 *src = reinterpret_cast<const float4 *>(z + 64 * 64);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) pre[q] = src[tid + 256 * q];
-        pn0 = z[(r0 + r) * 64 + c0];
-        pn1 = z[(r0 + r) * 64 + c0 + 32];
+        float *dst = ring + (size_t)st * CB_STAGE_FLOATS;
+        prism::tc::mbar_expect_tx(m, (64 * 64 + CB_ROWS * 64) * 4);
+        prism::tc::bulk_load(prism::tc::smem_u32(dst), z + 64 * 64, 64 * 64 * 4, m);
+        prism::tc::bulk_load(prism::tc::smem_u32(dst + 64 * 64), z + r0 * 64, CB_ROWS * 64 * 4, m);
     };
-    auto store_m = [&](int buf) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = (tid + 256 * q) * 4;
-            *reinterpret_cast<float4 *>(&M[buf][e >> 6][e & 63]) = pre[q];
-        }
-    };
-    load_map(0);
-    store_m(0);
-    float n0 = pn0, n1 = pn1;
+    if (tid == 0) {
+        abort_s = 0;
+        for (int st = 0; st < CB_STAGES; ++st) prism::tc::mbar_init(prism::tc::smem_u32(&mb[st]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int sp = 0; sp < nmaps && sp < CB_STAGES; ++sp) issue(sp);
+    }
     __syncthreads();
+    int issued = min(nmaps, CB_STAGES);
     for (int sp = 1; sp < P; ++sp) {
-        const int buf = (sp - 1) & 1;
-        if (sp + 1 < P) load_map(sp);  // map of segment sp, used at step sp + 1
-        float a0 = n0, a1 = n1;
-#pragma unroll 16
-        for (int m = 0; m < 64; ++m) {
-            const float sv = S[r][m];
-            a0 = fmaf(sv, M[buf][m][c0], a0);
-            a1 = fmaf(sv, M[buf][m][c0 + 32], a1);
+        const int k = sp - 1, st = k % CB_STAGES;
+        if (tid == 0 && !prism::tc::mbar_wait(prism::tc::smem_u32(&mb[st]), (uint32_t)((k / CB_STAGES) & 1), wait_ns)) {
+            abort_s = 1;
+            atomicCAS(status, 0, kDevTimeout);
         }
         __syncthreads();
-        S[r][c0] = a0;
-        S[r][c0 + 32] = a1;
-        float *dst = sstart + (((size_t)bh * P + sp) * 64 + r0 + r) * 64;
-        dst[c0] = a0;
-        dst[c0 + 32] = a1;
-        if (sp + 1 < P) {
-            store_m(buf ^ 1);
-            n0 = pn0;
-            n1 = pn1;
+        if (abort_s) break;
+        const float *M = ring + (size_t)st * CB_STAGE_FLOATS;
+        const float4 nv = *reinterpret_cast<const float4 *>(M + 64 * 64 + r * 64 + c4);
+        float a0 = nv.x, a1 = nv.y, a2 = nv.z, a3 = nv.w;
+        float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;  // second accumulator set: shorter FMA chains
+#pragma unroll 8
+        for (int m = 0; m < 64; m += 2) {
+            const float s0 = S[r][m], s1 = S[r][m + 1];
+            const float4 m0 = *reinterpret_cast<const float4 *>(M + m * 64 + c4);
+            const float4 m1 = *reinterpret_cast<const float4 *>(M + (m + 1) * 64 + c4);
+            a0 = fmaf(s0, m0.x, a0); a1 = fmaf(s0, m0.y, a1); a2 = fmaf(s0, m0.z, a2); a3 = fmaf(s0, m0.w, a3);
+            b0 = fmaf(s1, m1.x, b0); b1 = fmaf(s1, m1.y, b1); b2 = fmaf(s1, m1.z, b2); b3 = fmaf(s1, m1.w, b3);
         }
+        a0 += b0; a1 += b1; a2 += b2; a3 += b3;
+        __syncthreads();  // every thread is done with S and with this stage
+        float *dst = sstart + (((size_t)bh * P + sp) * 64 + r0 + r) * 64 + c4;
+        S[r][c4] = a0;
+        S[r][c4 + 1] = a1;
+        S[r][c4 + 2] = a2;
+        S[r][c4 + 3] = a3;
+        *reinterpret_cast<float4 *>(dst) = make_float4(a0, a1, a2, a3);
+        if (tid == 0 && issued < nmaps) issue(issued++);
         __syncthreads();
     }
+    // after an expired wait: let the copies still in flight land before the block exits
+    if (tid == 0 && abort_s)
+        for (int k = 0; k < issued; ++k)
+            (void)prism::tc::mbar_wait(prism::tc::smem_u32(&mb[k % CB_STAGES]), (uint32_t)((k / CB_STAGES) & 1),
+                                       1000000000ull);
 }
 
-// fixup: o = o0 + Qhat S_start^T for the chunks of segments >= 1.  One CTA per (sequence,
-// segment >= 1); the 64x64x64 product of each chunk runs on mma.sync m16n8k16 (fp16 in, fp32
-// accumulate): A = Qhat [i][m] straight from the stash, B[m][c] = S_start[c][m] from shared
-// memory, C initialised with o0.  16 warps: warp w owns rows 16 (w & 3).. and columns 16 (w >> 2)..
+// fixup: o = o0 + Qhat S_start^T for the chunks of segments >= 1, one CTA of 4 warps per chunk
+// (many chunks in flight per SM).  The 64x64x64 product runs on mma.sync m16n8k16 (fp16 in,
+// fp32 accumulate): A = Qhat [i][m] straight from the stash, B[m][c] = S_start[c][m] converted
+// to fp16 in shared memory, C initialised with o0 (fp32, or fp16 when the output is bf16).
+// Warp w owns rows 16 w .. 16 w + 15 and all 64 columns.
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
     asm volatile(
@@ -896,72 +1053,81 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__global__ void __launch_bounds__(512) fixup_kernel(const float *__restrict__ stash_o, const __half *__restrict__ stash_q,
+__global__ void __launch_bounds__(128) fixup_kernel(const void *__restrict__ stash_o, const __half *__restrict__ stash_q,
                                                     const float *__restrict__ sstart, void *__restrict__ out, int out_f32,
                                                     int T, int NC, int P)
 {
     __shared__ __align__(16) __half Sh[64][72];  // Sh[c][m] = S_start[c][m] (fp16, padded rows)
-    const int bh = blockIdx.x, seg = blockIdx.y + 1, tid = threadIdx.x;
+    const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+    // segment of chunk c: the largest p with begin(p) <= c
+    int seg = (int)(((long long)c * P) / NC);
+    while (seg + 1 < P && ((long long)(seg + 1) * NC) / P <= c) ++seg;
+    while (seg > 0 && ((long long)seg * NC) / P > c) --seg;
+    if (seg == 0) return;
     const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-    const int c_begin = (int)(((long long)seg * NC) / P), c_end = (int)(((long long)(seg + 1) * NC) / P);
     const float *S = sstart + ((size_t)bh * P + seg) * 64 * 64;
-    for (int e = tid; e < 64 * 32; e += 512) {
-        const float2 v = reinterpret_cast<const float2 *>(S)[e];
-        *reinterpret_cast<__half2 *>(&Sh[e >> 5][(e & 31) * 2]) = __floats2half2_rn(v.x, v.y);
+    for (int e = tid; e < 64 * 16; e += 128) {
+        const float4 v = reinterpret_cast<const float4 *>(S)[e];
+        __half2 *d = reinterpret_cast<__half2 *>(&Sh[e >> 4][(e & 15) * 4]);
+        d[0] = __floats2half2_rn(v.x, v.y);
+        d[1] = __floats2half2_rn(v.z, v.w);
+    }
+    const size_t chunk = (size_t)bh * NC + c;
+    const int t0 = c * 64, n = min(64, T - t0);
+    const int i0 = 16 * warp + gq, i1 = i0 + 8;
+    // A fragments for the 4 k-steps (Qhat rows i0, i1)
+    const uint32_t *qa = reinterpret_cast<const uint32_t *>(stash_q + chunk * 4096);
+    uint32_t a[4][4];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        a[ks][0] = qa[(i0 * 64 + 16 * ks + 2 * tq) >> 1];
+        a[ks][1] = qa[(i1 * 64 + 16 * ks + 2 * tq) >> 1];
+        a[ks][2] = qa[(i0 * 64 + 16 * ks + 2 * tq + 8) >> 1];
+        a[ks][3] = qa[(i1 * 64 + 16 * ks + 2 * tq + 8) >> 1];
+    }
+    float acc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+        const int cc = 8 * nt + 2 * tq;
+        float2 o0, o1;
+        if (out_f32) {
+            const float *so = reinterpret_cast<const float *>(stash_o) + chunk * 4096;
+            o0 = *reinterpret_cast<const float2 *>(so + i0 * 64 + cc);
+            o1 = *reinterpret_cast<const float2 *>(so + i1 * 64 + cc);
+        } else {
+            const __half *so = reinterpret_cast<const __half *>(stash_o) + chunk * 4096;
+            o0 = __half22float2(*reinterpret_cast<const __half2 *>(so + i0 * 64 + cc));
+            o1 = __half22float2(*reinterpret_cast<const __half2 *>(so + i1 * 64 + cc));
+        }
+        acc[nt][0] = o0.x;
+        acc[nt][1] = o0.y;
+        acc[nt][2] = o1.x;
+        acc[nt][3] = o1.y;
     }
     __syncthreads();
-    const int rt = warp & 3, ct = warp >> 2;  // row tile (16 rows), column pair (2 x 8 columns)
-    // B fragments (k = m, n = c): constant over the chunks of the segment
-    uint32_t bf[4][2][2];
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int cn = 16 * ct + 8 * nt + gq;
-            bf[ks][nt][0] = *reinterpret_cast<const uint32_t *>(&Sh[cn][16 * ks + 2 * tq]);
-            bf[ks][nt][1] = *reinterpret_cast<const uint32_t *>(&Sh[cn][16 * ks + 2 * tq + 8]);
-        }
-    for (int c = c_begin; c < c_end; ++c) {
-        const size_t chunk = (size_t)bh * NC + c;
-        const int t0 = c * 64, n = min(64, T - t0);
-        const int i0 = 16 * rt + gq, i1 = i0 + 8;
-        const uint32_t *qa = reinterpret_cast<const uint32_t *>(stash_q + chunk * 4096);
-        float acc[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int cc = 16 * ct + 8 * nt + 2 * tq;
-            const float2 o0 = *reinterpret_cast<const float2 *>(stash_o + (chunk * 64 + i0) * 64 + cc);
-            const float2 o1 = *reinterpret_cast<const float2 *>(stash_o + (chunk * 64 + i1) * 64 + cc);
-            acc[nt][0] = o0.x;
-            acc[nt][1] = o0.y;
-            acc[nt][2] = o1.x;
-            acc[nt][3] = o1.y;
+        for (int nt = 0; nt < 8; ++nt) {
+            const int cn = 8 * nt + gq;
+            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&Sh[cn][16 * ks + 2 * tq]);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&Sh[cn][16 * ks + 2 * tq + 8]);
+            mma_f16_16816(acc[nt], a[ks], b0, b1);
         }
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t a[4];
-            a[0] = qa[(i0 * 64 + 16 * ks + 2 * tq) >> 1];
-            a[1] = qa[(i1 * 64 + 16 * ks + 2 * tq) >> 1];
-            a[2] = qa[(i0 * 64 + 16 * ks + 2 * tq + 8) >> 1];
-            a[3] = qa[(i1 * 64 + 16 * ks + 2 * tq + 8) >> 1];
+    for (int nt = 0; nt < 8; ++nt) {
+        const int cc = 8 * nt + 2 * tq;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], a, bf[ks][nt][0], bf[ks][nt][1]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int cc = 16 * ct + 8 * nt + 2 * tq;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int i = h2 ? i1 : i0;
-                if (i >= n) continue;
-                const size_t o = ((size_t)bh * T + t0 + i) * 64 + cc;
-                const float x = acc[nt][2 * h2], y = acc[nt][2 * h2 + 1];
-                if (out_f32)
-                    *reinterpret_cast<float2 *>(reinterpret_cast<float *>(out) + o) = make_float2(x, y);
-                else
-                    *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(out) + o) =
-                        __floats2bfloat162_rn(x, y);
-            }
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int i = h2 ? i1 : i0;
+            if (i >= n) continue;
+            const size_t o = ((size_t)bh * T + t0 + i) * 64 + cc;
+            const float x = acc[nt][2 * h2], y = acc[nt][2 * h2 + 1];
+            if (out_f32)
+                *reinterpret_cast<float2 *>(reinterpret_cast<float *>(out) + o) = make_float2(x, y);
+            else
+                *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(out) + o) =
+                    __floats2bfloat162_rn(x, y);
         }
     }
 }
@@ -1036,7 +1202,9 @@ void tc_carve(const Shape &s, int P, void *base, TcWorkspace *w)
 
 cudaError_t tc_prepare()
 {
-    return cudaFuncSetAttribute(tc::segment_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(tc::segment_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(tc::combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::CB_SMEM);
 }
 
 cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const TcWorkspace &w, int *d_status,
@@ -1086,11 +1254,11 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
     tm.end();
     if (w.P > 1) {
         tm.begin("tc_combine");
-        combine_kernel<<<dim3(s.BH, 64 / CB_ROWS), 256, 0, st>>>(w.zsum, w.sstart, w.P);
+        combine_kernel<<<dim3(s.BH, 64 / CB_ROWS), CB_THREADS, CB_SMEM, st>>>(w.zsum, w.sstart, w.P, d_status, p.wait_ns);
         tm.end();
         tm.begin("tc_fixup");
-        fixup_kernel<<<dim3(s.BH, w.P - 1), 512, 0, st>>>(w.stash_o, w.stash_q, w.sstart, a.out, p.out_f32, s.T, s.NC,
-                                                           w.P);
+        fixup_kernel<<<dim3(s.NC, s.BH), 128, 0, st>>>(w.stash_o, w.stash_q, w.sstart, a.out, p.out_f32, s.T, s.NC,
+                                                        w.P);
         tm.end();
     }
     return cudaGetLastError();

@@ -29,11 +29,16 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16 with fp16 A and B (the same type on both
-// sides) and fp32 accumulation.
+// sides) and fp32 accumulation; idesc_bf16: the same with bf16 A and B.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, int b_mn_major)
 {
     return (1u << 4) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major)
+{
+    return idesc_f16(M, N, a_mn_major, b_mn_major) | (1u << 7) | (1u << 10);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum)
@@ -181,6 +186,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
             "r"(dst),
         "l"((uint64_t)map), "r"(mbar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
+}
+
+// Untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a multiple of 16),
+// completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"((uint64_t)src), "r"(bytes), "r"(mbar)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
