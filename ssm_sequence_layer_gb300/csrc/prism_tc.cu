@@ -141,6 +141,13 @@ __device__ __forceinline__ void st_row(uint8_t *tile, int row, int col0, const f
     }
 }
 
+// Descriptor of the tile at byte offset `off` of the CTA's 1024-aligned shared-memory base,
+// built by adding the offset fields to a descriptor of the base (all fields stay in range).
+__device__ __forceinline__ uint64_t dsc(uint64_t base, uint32_t off, uint32_t lbo, uint32_t sbo)
+{
+    return base + (uint64_t)(off >> 4) + ((uint64_t)(lbo >> 4) << 16) + ((uint64_t)(sbo >> 4) << 32);
+}
+
 __device__ __forceinline__ float ld_bf(const uint8_t *tile, int row, int col)
 {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128(row, col)));
@@ -292,6 +299,7 @@ __global__ void __launch_bounds__(NT, 1)
     float *s_xtmp = sc + 2 * SC_SET;  // XTMP_FLOATS of scratch for the solve
 
     const uint32_t sbase = smem_u32(sm);
+    const uint64_t dbase = sdesc(sbase, 0, 0);
     const uint32_t mb_mma = smem_u32(&mbar[0]), mb_qku = smem_u32(&mbar[1]);
     const uint32_t mb_v[2] = {smem_u32(&mbar[2]), smem_u32(&mbar[3])};
 
@@ -470,7 +478,7 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t id = idesc_bf16(128, N1, 0, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_D1, sdesc(sbase + OFF_Q + s * 32, 16, 1024), sdesc(sbase + OFF_K + s * 32, 16, 1024),
+                mma_f16(tmem + TM_D1, dsc(dbase, OFF_Q + s * 32, 16, 1024), dsc(dbase, OFF_K + s * 32, 16, 1024),
                         id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
@@ -587,8 +595,8 @@ __global__ void __launch_bounds__(NT, 1)
             for (int l = 0; l < R; ++l)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(tmem + TM_D2, sdesc(sbase + OFF_E + l * 2 * TILE + s * 32, 16, 1024),
-                             sdesc(sbase + OFF_XS + l * TILE + s * 2048, TILE, 1024), id, (l | s) != 0);
+                    mma_f16(tmem + TM_D2, dsc(dbase, OFF_E + l * 2 * TILE + s * 32, 16, 1024),
+                             dsc(dbase, OFF_XS + l * TILE + s * 2048, TILE, 1024), id, (l | s) != 0);
             mma_commit(mb_mma);
             pending |= 1u;
         }
@@ -598,25 +606,22 @@ __global__ void __launch_bounds__(NT, 1)
             const float *A = reinterpret_cast<const float *>(sm + OFF_AKK);
             float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
             const Frag fr{lane >> 2, lane & 3};
-            if (warp < 4) {
-                // diagonal block b: (I + N)^{-1} = (I - N)(I + N^2)(I + N^4)(I + N^8) (N strictly lower,
-                // N^16 = 0), on mma.sync; scratch in the unused upper blocks of T32 and A
-                const int b = warp, o = 16 * b;
-                const int ub = (b == 3) ? 0 : o, un = (b == 3) ? 48 : o + 16;  // an upper block (ub, un)
-                const float *N = A + o * LDAA + o;
-                float *Td = T32 + o * LDA + o;
-                float *P0 = T32 + ub * LDA + un;
-                float *P1 = const_cast<float *>(A) + ub * LDAA + un;
-                for (int e = lane; e < 256; e += 32) {
-                    const int r = e >> 4, cc = e & 15;
-                    Td[r * LDA + cc] = (r == cc ? 1.f : 0.f) - N[r * LDAA + cc];
+            if (tid < 64) {  // diagonal 16x16 blocks by forward substitution, one column per thread
+                const int o = 16 * (tid >> 4), cc = tid & 15;
+                float t[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    // t[j] = 0 for j < cc, so the sum may run over all j < r
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int j = 0; j + 1 < r; j += 2) {
+                        s0 = fmaf(A[(o + r) * LDAA + o + j], t[j], s0);
+                        s1 = fmaf(A[(o + r) * LDAA + o + j + 1], t[j + 1], s1);
+                    }
+                    if (r & 1) s0 = fmaf(A[(o + r) * LDAA + o + r - 1], t[r - 1], s0);
+                    t[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -(s0 + s1));
+                    T32[(o + r) * LDA + o + cc] = t[r];
                 }
-                mm16_warp(fr, P0, LDA, N, LDAA, N, LDAA, false);    // P0 = N^2
-                mm16_warp(fr, Td, LDA, Td, LDA, P0, LDA, true);     // T += T N^2
-                mm16_warp(fr, P1, LDAA, P0, LDA, P0, LDA, false);   // P1 = N^4
-                mm16_warp(fr, Td, LDA, Td, LDA, P1, LDAA, true);    // T += T N^4
-                mm16_warp(fr, P0, LDA, P1, LDAA, P1, LDAA, false);  // P0 = N^8
-                mm16_warp(fr, Td, LDA, Td, LDA, P0, LDA, true);     // T += T N^8
             }
             __syncthreads();
             PHASE_MARK(11);
@@ -655,7 +660,7 @@ __global__ void __launch_bounds__(NT, 1)
                 // the 8-column tile 8 w of the 32x32 block (both 16-row halves)
                 const int n0 = 8 * warp;
                 float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                // T_lo[k][n] = 0 for k < 16 <= n: block (0,1) of T32 holds scratch, so skip it
+                // T_lo[k][n] = 0 for k < 16 <= n: block (0,1) of T32 is never written, so skip it
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {                 // X = A_lo T_lo
                     if (n0 >= 16 && ks < 2) continue;
@@ -684,7 +689,7 @@ __global__ void __launch_bounds__(NT, 1)
                     frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
 #pragma unroll
                     for (int mt = 0; mt < 2; ++mt) {
-                        if (mt == 0 && ks >= 2) continue;  // T_hi[0:16][16:32] = 0 (block (2,3) holds scratch)
+                        if (mt == 0 && ks >= 2) continue;  // T_hi[0:16][16:32] = 0 (block (2,3) is never written)
                         uint32_t a[4];
                         frag_a(fr, T32, LDA, 32 + 16 * mt, 32 + 8 * ks, a);
                         mma_tf32(y[mt], a[0], a[1], a[2], a[3], b0, b1);
@@ -745,8 +750,8 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t id = idesc_f16(128, 64, 1, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_D3, sdesc(sbase + OFF_AKK + s * 2048, OFF_BGK - OFF_AKK, 1024),
-                        sdesc(sbase + OFF_TB + s * 32, 16, 1024),
+                mma_f16(tmem + TM_D3, dsc(dbase, OFF_AKK + s * 2048, OFF_BGK - OFF_AKK, 1024),
+                        dsc(dbase, OFF_TB + s * 32, 16, 1024),
                          id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
@@ -776,17 +781,17 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t idk5 = idesc_f16(128, 64, 0, 1), idx5 = idesc_f16(128, 64, 1, 1);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const uint64_t a = sdesc(sbase + OFF_AKK + s * 32, 16, 1024);
-                mma_f16(tmem + TM_D4, a, sdesc(sbase + OFF_G + s * 32, 16, 1024), idk, s > 0);
-                mma_f16(tmem + TM_D5, a, sdesc(sbase + OFF_K + s * 2048, TILE, 1024), idk5, s > 0);
+                const uint64_t a = dsc(dbase, OFF_AKK + s * 32, 16, 1024);
+                mma_f16(tmem + TM_D4, a, dsc(dbase, OFF_G + s * 32, 16, 1024), idk, s > 0);
+                mma_f16(tmem + TM_D5, a, dsc(dbase, OFF_K + s * 2048, TILE, 1024), idk5, s > 0);
             }
             for (int l = 0; l < R; ++l) {
                 const uint32_t xs = OFF_XS + l * TILE;
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
-                    const uint64_t a = sdesc(sbase + xs + s * 2048, OFF_ZERO - xs, 1024);
-                    mma_f16(tmem + TM_D4, a, sdesc(sbase + OFF_E + l * 2 * TILE + TILE + s * 32, 16, 1024), idx, 1);
-                    mma_f16(tmem + TM_D5, a, sdesc(sbase + OFF_U + l * TILE + s * 2048, TILE, 1024), idx5, 1);
+                    const uint64_t a = dsc(dbase, xs + s * 2048, OFF_ZERO - xs, 1024);
+                    mma_f16(tmem + TM_D4, a, dsc(dbase, OFF_E + l * 2 * TILE + TILE + s * 32, 16, 1024), idx, 1);
+                    mma_f16(tmem + TM_D5, a, dsc(dbase, OFF_U + l * TILE + s * 2048, TILE, 1024), idx5, 1);
                 }
             }
             mma_commit(mb_mma);
@@ -841,9 +846,9 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t id = idesc_f16(128, 64, 0, 1);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const uint64_t a = sdesc(sbase + OFF_ZA + s * 32, 16, 1024);
-                mma_f16(tmem + TM_D6, a, sdesc(sbase + OFF_E + TILE + s * 2048, TILE, 1024), id, s > 0);
-                mma_f16(tmem + TM_D7, a, sdesc(sbase + OFF_E + s * 2048, TILE, 1024), id, s > 0);
+                const uint64_t a = dsc(dbase, OFF_ZA + s * 32, 16, 1024);
+                mma_f16(tmem + TM_D6, a, dsc(dbase, OFF_E + TILE + s * 2048, TILE, 1024), id, s > 0);
+                mma_f16(tmem + TM_D7, a, dsc(dbase, OFF_E + s * 2048, TILE, 1024), id, s > 0);
             }
             mma_commit(mb_mma);
             pending |= 1u;
