@@ -172,7 +172,7 @@ PRISM_API const char *prism_last_error_message(void);
  *
  * Sizes and tensors are those of prism_forward (layouts at the top of this file), with
  * bf16 io and out, dk = dv = 64 and 1 <= L <= 4.  The scratch needs 24 KiB per 64-token
- * chunk of all sequences plus 48 KiB per sequence and segment; the call uses as many
+ * chunk of all sequences plus 40 KiB per sequence and segment; the call uses as many
  * segments as prism_forward would, fewer if they do not fit, and returns
  * PRISM_ERR_UNSUPPORTED (with a message) when even one segment per sequence does not fit
  * -- about 170K token-heads.

@@ -70,7 +70,7 @@ struct KernelTimer {
 // Workspace of the tensor-core path.
 struct TcWorkspace {
     float *zsum;             // [BH][P][128][64]  segment maps Z = [N; M]
-    float *sstart;           // [BH][P][64][64]   state entering each segment
+    __half *sstart;          // [BH][P][64][64]   state entering each segment (fp16, fix-up operand)
     void *stash_o;           // [BH][NC][64][64]  o0 per chunk (segments >= 1), fp32 or fp16
     __half *stash_q;         // [BH][NC][64][64]  Qhat per chunk (segments >= 1)
     int P;                   // segments per sequence

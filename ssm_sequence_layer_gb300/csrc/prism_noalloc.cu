@@ -99,7 +99,7 @@ extern "C" prism_status prism_forward_noalloc(int B, int H, int T, int dk, int d
     if (prism::tc_workspace_bytes(s, P) > avail)
         return noalloc_fail(PRISM_ERR_UNSUPPORTED,
                             "problem too large for the fixed scratch (needs 24 KiB per 64-token chunk "
-                            "of all sequences plus 48 KiB per sequence; 64 MiB in total)");
+                            "of all sequences plus 40 KiB per sequence and segment; 64 MiB in total)");
 
     int *d_status = (int *)scratch;
     prism::TcWorkspace w;

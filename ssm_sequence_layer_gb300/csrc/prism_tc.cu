@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(NT, 1)
         const float lc = s_lam[63];
 
         PHASE_MARK(0);
-        // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T (runs while the CTA does the prep) ----------
+        // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T ------------------------------------------------
         if (!wait_two(mb_qku, ph_qku, 2u, mb_v[stage], ph_v[stage], 4u << stage)) break;
         if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
         const int N1 = 64 * (1 + R);
@@ -482,6 +482,15 @@ __global__ void __launch_bounds__(NT, 1)
                         id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
+            // the Gram is waited for here, before this warp joins the prep: measured faster
+            // than letting it run under the prep (the prep slows the tensor core's operand reads)
+            if (mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
+                ph_mma ^= 1u;
+                pending &= ~1u;
+            } else {
+                abort_s = 1;
+                set_status(p.status, kDevTimeout);
+            }
         }
 
         PHASE_MARK(1);
@@ -534,7 +543,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_async_smem();
         __syncthreads();
         PHASE_MARK(14);
-        if (!wait_all(mb_mma, ph_mma, 1u)) break;
+        if (abort_s) break;
         fence_after_sync();
         // the Gram has read K and U: convert them to fp16 in place for the state-side MMA (their
         // fence and barrier are E1's)
@@ -964,29 +973,34 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} (fp32), 8 value rows per block.  The maps
-// stream through a ring of CB_STAGES shared-memory stages filled by bulk copies (16 KB of M and
-// this block's 2 KB of N per segment), so the serial chain never waits on global memory latency.
+// combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} in fp32, 8 value rows per block, written
+// out as fp16 (the fix-up's MMA operand).  The maps stream through a ring of CB_STAGES
+// shared-memory stages filled by bulk copies (16 KB of M and this block's 2 KB of N per
+// segment), so the serial chain never waits on global memory latency.  Warp w owns rows 2w and
+// 2w + 1, lane l columns 2l and 2l + 1; the running rows are double-buffered in shared memory,
+// so one barrier per segment orders both the row exchange and the reuse of a ring stage.
 constexpr int CB_ROWS = 8;
 constexpr int CB_STAGES = 4;
-constexpr int CB_THREADS = 128;  // 8 rows x 16 groups of 4 columns
+constexpr int CB_THREADS = 128;
 constexpr int CB_STAGE_FLOATS = 64 * 64 + CB_ROWS * 64;
 constexpr size_t CB_SMEM = (size_t)CB_STAGES * CB_STAGE_FLOATS * 4 + 128;
 
-__global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__restrict__ zsum, float *__restrict__ sstart,
+__global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__restrict__ zsum, __half *__restrict__ sstart,
                                                              int P, int *status, unsigned long long wait_ns)
 {
     extern __shared__ __align__(128) float ring[];  // [CB_STAGES][M 64x64 | N 8x64]
     __shared__ __align__(8) uint64_t mb[CB_STAGES];
-    __shared__ float S[CB_ROWS][65];
+    __shared__ __align__(16) float S[2][CB_ROWS][64];
     __shared__ int abort_s;
     const int bh = blockIdx.x, r0 = blockIdx.y * CB_ROWS, tid = threadIdx.x;
-    const int r = tid >> 4, c4 = (tid & 15) * 4;  // outputs (r, c4 .. c4 + 3)
-    float *dst0 = sstart + ((size_t)bh * P * 64 + r0 + r) * 64 + c4;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        S[r][c4 + q] = 0.f;
-        dst0[q] = 0.f;
+    const int w = tid >> 5, l = tid & 31;
+    const int ra = 2 * w, rb = 2 * w + 1, c2 = 2 * l;  // rows ra, rb; columns c2, c2 + 1
+    {
+        __half2 *d0 = reinterpret_cast<__half2 *>(sstart + ((size_t)bh * P * 64 + r0 + ra) * 64 + c2);
+        d0[0] = __floats2half2_rn(0.f, 0.f);
+        d0[32] = __floats2half2_rn(0.f, 0.f);
+        *reinterpret_cast<float2 *>(&S[0][ra][c2]) = make_float2(0.f, 0.f);
+        *reinterpret_cast<float2 *>(&S[0][rb][c2]) = make_float2(0.f, 0.f);
     }
     if (P < 2) return;
     const int nmaps = P - 1;  // maps of segments 0..P-2 are used
@@ -1005,38 +1019,43 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         for (int sp = 0; sp < nmaps && sp < CB_STAGES; ++sp) issue(sp);
     }
-    __syncthreads();
     int issued = min(nmaps, CB_STAGES);
-    for (int sp = 1; sp < P; ++sp) {
-        const int k = sp - 1, st = k % CB_STAGES;
+    for (int k = 0; k < nmaps; ++k) {
+        const int st = k % CB_STAGES, buf = k & 1;
         if (tid == 0 && !prism::tc::mbar_wait(prism::tc::smem_u32(&mb[st]), (uint32_t)((k / CB_STAGES) & 1), wait_ns)) {
             abort_s = 1;
             atomicCAS(status, 0, kDevTimeout);
         }
-        __syncthreads();
+        __syncthreads();  // stage k landed; rows of step k - 1 written; stage of step k - 1 free
         if (abort_s) break;
-        const float *M = ring + (size_t)st * CB_STAGE_FLOATS;
-        const float4 nv = *reinterpret_cast<const float4 *>(M + 64 * 64 + r * 64 + c4);
-        float a0 = nv.x, a1 = nv.y, a2 = nv.z, a3 = nv.w;
-        float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;  // second accumulator set: shorter FMA chains
-#pragma unroll 8
-        for (int m = 0; m < 64; m += 2) {
-            const float s0 = S[r][m], s1 = S[r][m + 1];
-            const float4 m0 = *reinterpret_cast<const float4 *>(M + m * 64 + c4);
-            const float4 m1 = *reinterpret_cast<const float4 *>(M + (m + 1) * 64 + c4);
-            a0 = fmaf(s0, m0.x, a0); a1 = fmaf(s0, m0.y, a1); a2 = fmaf(s0, m0.z, a2); a3 = fmaf(s0, m0.w, a3);
-            b0 = fmaf(s1, m1.x, b0); b1 = fmaf(s1, m1.y, b1); b2 = fmaf(s1, m1.z, b2); b3 = fmaf(s1, m1.w, b3);
+        if (tid == 0 && k > 0 && issued < nmaps) {  // refill the stage step k - 1 read
+            prism::tc::fence_async_smem();
+            issue(issued++);
         }
-        a0 += b0; a1 += b1; a2 += b2; a3 += b3;
-        __syncthreads();  // every thread is done with S and with this stage
-        float *dst = sstart + (((size_t)bh * P + sp) * 64 + r0 + r) * 64 + c4;
-        S[r][c4] = a0;
-        S[r][c4 + 1] = a1;
-        S[r][c4 + 2] = a2;
-        S[r][c4 + 3] = a3;
-        *reinterpret_cast<float4 *>(dst) = make_float4(a0, a1, a2, a3);
-        if (tid == 0 && issued < nmaps) issue(issued++);
-        __syncthreads();
+        const float *M = ring + (size_t)st * CB_STAGE_FLOATS;
+        const float2 na = *reinterpret_cast<const float2 *>(M + 64 * 64 + ra * 64 + c2);
+        const float2 nb = *reinterpret_cast<const float2 *>(M + 64 * 64 + rb * 64 + c2);
+        float a0 = na.x, a1 = na.y, b0 = nb.x, b1 = nb.y;
+        float e0 = 0.f, e1 = 0.f, f0 = 0.f, f1 = 0.f;  // second accumulator set: shorter FMA chains
+#pragma unroll 4
+        for (int m = 0; m < 64; m += 4) {
+            const float4 sa = *reinterpret_cast<const float4 *>(&S[buf][ra][m]);
+            const float4 sb = *reinterpret_cast<const float4 *>(&S[buf][rb][m]);
+            const float2 m0 = *reinterpret_cast<const float2 *>(M + (m + 0) * 64 + c2);
+            const float2 m1 = *reinterpret_cast<const float2 *>(M + (m + 1) * 64 + c2);
+            const float2 m2 = *reinterpret_cast<const float2 *>(M + (m + 2) * 64 + c2);
+            const float2 m3 = *reinterpret_cast<const float2 *>(M + (m + 3) * 64 + c2);
+            a0 = fmaf(sa.x, m0.x, a0); a1 = fmaf(sa.x, m0.y, a1); b0 = fmaf(sb.x, m0.x, b0); b1 = fmaf(sb.x, m0.y, b1);
+            e0 = fmaf(sa.y, m1.x, e0); e1 = fmaf(sa.y, m1.y, e1); f0 = fmaf(sb.y, m1.x, f0); f1 = fmaf(sb.y, m1.y, f1);
+            a0 = fmaf(sa.z, m2.x, a0); a1 = fmaf(sa.z, m2.y, a1); b0 = fmaf(sb.z, m2.x, b0); b1 = fmaf(sb.z, m2.y, b1);
+            e0 = fmaf(sa.w, m3.x, e0); e1 = fmaf(sa.w, m3.y, e1); f0 = fmaf(sb.w, m3.x, f0); f1 = fmaf(sb.w, m3.y, f1);
+        }
+        a0 += e0; a1 += e1; b0 += f0; b1 += f1;
+        *reinterpret_cast<float2 *>(&S[buf ^ 1][ra][c2]) = make_float2(a0, a1);
+        *reinterpret_cast<float2 *>(&S[buf ^ 1][rb][c2]) = make_float2(b0, b1);
+        __half2 *d = reinterpret_cast<__half2 *>(sstart + (((size_t)bh * P + k + 1) * 64 + r0 + ra) * 64 + c2);
+        d[0] = __floats2half2_rn(a0, a1);
+        d[32] = __floats2half2_rn(b0, b1);
     }
     // after an expired wait: let the copies still in flight land before the block exits
     if (tid == 0 && abort_s)
@@ -1046,10 +1065,11 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
 }
 
 // fixup: o = o0 + Qhat S_start^T for the chunks of segments >= 1, one CTA of 4 warps per chunk
-// (many chunks in flight per SM).  The 64x64x64 product runs on mma.sync m16n8k16 (fp16 in,
-// fp32 accumulate): A = Qhat [i][m] straight from the stash, B[m][c] = S_start[c][m] converted
-// to fp16 in shared memory, C initialised with o0 (fp32, or fp16 when the output is bf16).
-// Warp w owns rows 16 w .. 16 w + 15 and all 64 columns.
+// (many chunks in flight per SM).  Qhat, S_start (fp16) and o0 are copied into padded
+// shared-memory rows with 16-byte cp.async (coalesced, no register staging); the 64x64x64
+// product runs on mma.sync m16n8k16 (fp16 in, fp32 accumulate) with A = Qhat [i][m],
+// B[m][c] = S_start[c][m] and C initialised with o0; the result goes back over o0's rows and
+// leaves as coalesced 16-byte stores.  Warp w owns rows 16 w .. 16 w + 15 and all 64 columns.
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
     asm volatile(
@@ -1058,81 +1078,121 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__global__ void __launch_bounds__(128) fixup_kernel(const void *__restrict__ stash_o, const __half *__restrict__ stash_q,
-                                                    const float *__restrict__ sstart, void *__restrict__ out, int out_f32,
-                                                    int T, int NC, int P)
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src)
 {
-    __shared__ __align__(16) __half Sh[64][72];  // Sh[c][m] = S_start[c][m] (fp16, padded rows)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+
+constexpr int FX_LDH = 72;  // row stride (halves) of the fp16 tiles: conflict-free fragment reads
+constexpr int FX_LDF = 72;  // row stride (floats) of the fp32 o0 tile
+
+__global__ void __launch_bounds__(128) fixup_kernel(const void *__restrict__ stash_o, const __half *__restrict__ stash_q,
+                                                    const __half *__restrict__ sstart, void *__restrict__ out,
+                                                    int out_f32, int T, int NC, int P)
+{
+    __shared__ __align__(16) __half Qs[64 * FX_LDH];             // Qhat [i][m]
+    __shared__ __align__(16) __half Ss[64 * FX_LDH];             // S_start [c][m]
+    __shared__ __align__(16) float Os[64 * FX_LDF];              // o0 / out [i][c] (fp32, or fp16 in the first half)
     const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     // segment of chunk c: the largest p with begin(p) <= c
     int seg = (int)(((long long)c * P) / NC);
     while (seg + 1 < P && ((long long)(seg + 1) * NC) / P <= c) ++seg;
     while (seg > 0 && ((long long)seg * NC) / P > c) --seg;
     if (seg == 0) return;
-    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-    const float *S = sstart + ((size_t)bh * P + seg) * 64 * 64;
-    for (int e = tid; e < 64 * 16; e += 128) {
-        const float4 v = reinterpret_cast<const float4 *>(S)[e];
-        __half2 *d = reinterpret_cast<__half2 *>(&Sh[e >> 4][(e & 15) * 4]);
-        d[0] = __floats2half2_rn(v.x, v.y);
-        d[1] = __floats2half2_rn(v.z, v.w);
-    }
     const size_t chunk = (size_t)bh * NC + c;
     const int t0 = c * 64, n = min(64, T - t0);
+    {
+        const __half *gq = stash_q + chunk * 4096;
+        const __half *gs = sstart + ((size_t)bh * P + seg) * 4096;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // 512 16-byte groups per tile: row e >> 3, group e & 7
+            const int e = tid + 128 * k, r = e >> 3, g = (e & 7) * 8;
+            cp_async16(Qs + r * FX_LDH + g, gq + r * 64 + g);
+            cp_async16(Ss + r * FX_LDH + g, gs + r * 64 + g);
+        }
+        if (out_f32) {
+            const float *go = reinterpret_cast<const float *>(stash_o) + chunk * 4096;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int e = tid + 128 * k, r = e >> 4, g = (e & 15) * 4;
+                cp_async16(Os + r * FX_LDF + g, go + r * 64 + g);
+            }
+        } else {
+            const __half *go = reinterpret_cast<const __half *>(stash_o) + chunk * 4096;
+            __half *oh = reinterpret_cast<__half *>(Os);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = tid + 128 * k, r = e >> 3, g = (e & 7) * 8;
+                cp_async16(oh + r * FX_LDH + g, go + r * 64 + g);
+            }
+        }
+        asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
     const int i0 = 16 * warp + gq, i1 = i0 + 8;
-    // A fragments for the 4 k-steps (Qhat rows i0, i1)
-    const uint32_t *qa = reinterpret_cast<const uint32_t *>(stash_q + chunk * 4096);
     uint32_t a[4][4];
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
-        a[ks][0] = qa[(i0 * 64 + 16 * ks + 2 * tq) >> 1];
-        a[ks][1] = qa[(i1 * 64 + 16 * ks + 2 * tq) >> 1];
-        a[ks][2] = qa[(i0 * 64 + 16 * ks + 2 * tq + 8) >> 1];
-        a[ks][3] = qa[(i1 * 64 + 16 * ks + 2 * tq + 8) >> 1];
+        a[ks][0] = *reinterpret_cast<const uint32_t *>(Qs + i0 * FX_LDH + 16 * ks + 2 * tq);
+        a[ks][1] = *reinterpret_cast<const uint32_t *>(Qs + i1 * FX_LDH + 16 * ks + 2 * tq);
+        a[ks][2] = *reinterpret_cast<const uint32_t *>(Qs + i0 * FX_LDH + 16 * ks + 2 * tq + 8);
+        a[ks][3] = *reinterpret_cast<const uint32_t *>(Qs + i1 * FX_LDH + 16 * ks + 2 * tq + 8);
     }
+    __half *oh = reinterpret_cast<__half *>(Os);
     float acc[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
         const int cc = 8 * nt + 2 * tq;
         float2 o0, o1;
         if (out_f32) {
-            const float *so = reinterpret_cast<const float *>(stash_o) + chunk * 4096;
-            o0 = *reinterpret_cast<const float2 *>(so + i0 * 64 + cc);
-            o1 = *reinterpret_cast<const float2 *>(so + i1 * 64 + cc);
+            o0 = *reinterpret_cast<const float2 *>(Os + i0 * FX_LDF + cc);
+            o1 = *reinterpret_cast<const float2 *>(Os + i1 * FX_LDF + cc);
         } else {
-            const __half *so = reinterpret_cast<const __half *>(stash_o) + chunk * 4096;
-            o0 = __half22float2(*reinterpret_cast<const __half2 *>(so + i0 * 64 + cc));
-            o1 = __half22float2(*reinterpret_cast<const __half2 *>(so + i1 * 64 + cc));
+            o0 = __half22float2(*reinterpret_cast<const __half2 *>(oh + i0 * FX_LDH + cc));
+            o1 = __half22float2(*reinterpret_cast<const __half2 *>(oh + i1 * FX_LDH + cc));
         }
         acc[nt][0] = o0.x;
         acc[nt][1] = o0.y;
         acc[nt][2] = o1.x;
         acc[nt][3] = o1.y;
     }
-    __syncthreads();
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
             const int cn = 8 * nt + gq;
-            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&Sh[cn][16 * ks + 2 * tq]);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&Sh[cn][16 * ks + 2 * tq + 8]);
+            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(Ss + cn * FX_LDH + 16 * ks + 2 * tq);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(Ss + cn * FX_LDH + 16 * ks + 2 * tq + 8);
             mma_f16_16816(acc[nt], a[ks], b0, b1);
         }
+    // the result replaces o0 at the same positions (each position is read and written by one
+    // thread), in the output's element type
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
         const int cc = 8 * nt + 2 * tq;
+        if (out_f32) {
+            *reinterpret_cast<float2 *>(Os + i0 * FX_LDF + cc) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2 *>(Os + i1 * FX_LDF + cc) = make_float2(acc[nt][2], acc[nt][3]);
+        } else {
+            *reinterpret_cast<__nv_bfloat162 *>(oh + i0 * FX_LDH + cc) = __floats2bfloat162_rn(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<__nv_bfloat162 *>(oh + i1 * FX_LDH + cc) = __floats2bfloat162_rn(acc[nt][2], acc[nt][3]);
+        }
+    }
+    __syncthreads();
+    if (out_f32) {
+        float *go = reinterpret_cast<float *>(out) + ((size_t)bh * T + t0) * 64;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int i = h2 ? i1 : i0;
-            if (i >= n) continue;
-            const size_t o = ((size_t)bh * T + t0 + i) * 64 + cc;
-            const float x = acc[nt][2 * h2], y = acc[nt][2 * h2 + 1];
-            if (out_f32)
-                *reinterpret_cast<float2 *>(reinterpret_cast<float *>(out) + o) = make_float2(x, y);
-            else
-                *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(out) + o) =
-                    __floats2bfloat162_rn(x, y);
+        for (int k = 0; k < 8; ++k) {
+            const int e = tid + 128 * k, r = e >> 4, g = (e & 15) * 4;
+            if (r < n) *reinterpret_cast<float4 *>(go + r * 64 + g) = *reinterpret_cast<const float4 *>(Os + r * FX_LDF + g);
+        }
+    } else {
+        __nv_bfloat16 *go = reinterpret_cast<__nv_bfloat16 *>(out) + ((size_t)bh * T + t0) * 64;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int e = tid + 128 * k, r = e >> 3, g = (e & 7) * 8;
+            if (r < n) *reinterpret_cast<uint4 *>(go + r * 64 + g) = *reinterpret_cast<const uint4 *>(oh + r * FX_LDH + g);
         }
     }
 }
@@ -1185,7 +1245,7 @@ int tc_segments(const Shape &s, int sm_count, long long opt)
 size_t tc_workspace_bytes(const Shape &s, int P)
 {
     const size_t BH = s.BH, NC = s.NC;
-    return BH * P * 128 * 64 * 4 + BH * P * 64 * 64 * 4 + BH * NC * 4096 * 4 + BH * NC * 4096 * 2 + 4 * 256;
+    return BH * P * 128 * 64 * 4 + BH * P * 64 * 64 * 2 + BH * NC * 4096 * 4 + BH * NC * 4096 * 2 + 4 * 256;
 }
 
 void tc_carve(const Shape &s, int P, void *base, TcWorkspace *w)
@@ -1195,8 +1255,8 @@ void tc_carve(const Shape &s, int P, void *base, TcWorkspace *w)
     w->zsum = (float *)p;
     p += BH * P * 128 * 64 * 4;
     p = (p + 255) & ~(uintptr_t)255;
-    w->sstart = (float *)p;
-    p += BH * P * 64 * 64 * 4;
+    w->sstart = (__half *)p;
+    p += BH * P * 64 * 64 * 2;
     p = (p + 255) & ~(uintptr_t)255;
     w->stash_o = (float *)p;
     p += BH * NC * 4096 * 4;
