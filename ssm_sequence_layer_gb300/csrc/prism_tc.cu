@@ -17,7 +17,8 @@
 // Chunk algebra (local index i, j; lambda_i = sum_{m<=i} ln alpha_m; lc = lambda_{C-1};
 // rowf_i = e^{lambda_i - lc} >= 1, colf_j = e^{lc - lambda_j} <= 1, Gamma_i = e^{lambda_i}):
 //   A_ij  = beta_i rowf_i colf_j k_i.k_j            (j < i)   -> T = (I + A)^{-1}   (fp32 solve)
-//   PK_l  = k_i.u_{j,l} (j < i);  PQ_l = q_i.u_{j,l}, G = q_i.k_j (j <= i)      (unscaled scores)
+//   PK_l  = k_i.u_{j,l} (j < i);  PQ_l = q_i.u_{j,l}, G = q_i.k_j (j <= i)      (unscaled scores,
+//           computed and stored transposed, [j][i], from Grams with key/direction rows)
 //   Xs_l  = colf_j x_{j,l}                             (x = gamma g (.) r, the prep)
 //   RHS   = diag(beta) V - diag(beta rowf) sum_l PK_l Xs_l
 //   [U'^T; W^T] = [RHS | diag(beta Gamma) K]^T T^T
@@ -77,7 +78,7 @@ constexpr uint32_t OFF_U = OFF_K + TILE;
 constexpr uint32_t OFF_V0 = OFF_U + RMAX * TILE;  // two V stages, 72 rows x 128 B (8-row halo), unswizzled
 constexpr uint32_t VBYTES = 72 * 128;
 constexpr uint32_t OFF_V1 = OFF_V0 + 10240;
-constexpr uint32_t OFF_E = OFF_V1 + 10240;        // [PK0|PQ0|PK1|PQ1|PK2|PQ2|G]; later Qt, Mc
+constexpr uint32_t OFF_E = OFF_V1 + 10240;        // [PK0|PQ0^T|PK1|PQ1^T|PK2|PQ2^T|G^T]; later Qt, Mc
 constexpr uint32_t OFF_G = OFF_E + 6 * TILE;
 constexpr uint32_t OFF_AKK = OFF_E + 7 * TILE;    // A (fp32, stride 68); later RHS|BGK; later UWs
 constexpr uint32_t LDA = 68;    // row stride (floats) of T32 (float4 rows)
@@ -102,7 +103,8 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(4 * 128 <= XTMP_FLOATS && 4 * 256 <= XTMP_FLOATS, "solve scratch");
 
 // TMEM column map
-constexpr uint32_t TM_D1 = 0, TM_D2 = 256, TM_D3 = 320, TM_D4 = 384, TM_D5 = 448, TM_D6 = 0, TM_D7 = 64;
+constexpr uint32_t TM_D1 = 0, TM_D2 = 256, TM_D3 = 320, TM_D5 = 384, TM_D4 = 448, TM_D7 = 0, TM_D6 = 64;
+static_assert(TM_D4 == TM_D5 + 64 && TM_D6 == TM_D7 + 64, "D5|D4 and D7|D6 are written by one N = 128 MMA each");
 
 struct SegParams {
     const float *beta, *alpha, *gamma, *eta;
@@ -392,21 +394,25 @@ __global__ void __launch_bounds__(NT, 1)
     const float2 w2 = __bfloat1622float2(cw2[2 * (D / 2)]);
     const float2 w3 = __bfloat1622float2(cw2[3 * (D / 2)]);
 
-    // gates of one chunk: lane l of warp 0 holds beta/alpha of tokens 2l, 2l+1; thread tid < 192
-    // holds gamma/eta slot tid
+    // gates of one chunk: lane l of warp 1 holds beta/alpha of tokens 2l, 2l+1; thread
+    // 256 + s (s < 192) holds gamma/eta slot s.  Warp 0 (thread 0 issues the MMAs) is left out,
+    // so the next chunk's scalars are not held up behind an MMA issue sequence.
+    constexpr int SCAN_WARP = 1, GATE_T0 = 256;
+    static_assert(GATE_T0 + 64 * RMAX <= NT, "gate threads");
+    const int gt = tid - GATE_T0;
     float pf_b0 = 0.f, pf_b1 = 0.f, pf_a0 = 1.f, pf_a1 = 1.f, pf_gam = 0.f, pf_eta = 0.f;
     auto load_gates = [&](int c) {
         const int n = min(C, p.T - c * C);
         const size_t tok0 = (size_t)bh * p.T + (size_t)c * C;
-        if (warp == 0) {
+        if (warp == SCAN_WARP) {
             const int i0 = 2 * lane, i1 = 2 * lane + 1;
             pf_b0 = i0 < n ? p.beta[tok0 + i0] : 0.f;
             pf_b1 = i1 < n ? p.beta[tok0 + i1] : 0.f;
             pf_a0 = i0 < n ? p.alpha[tok0 + i0] : 1.f;
             pf_a1 = i1 < n ? p.alpha[tok0 + i1] : 1.f;
         }
-        if (tid < 64 * RMAX) {
-            const int i = tid / RMAX, l = tid % RMAX;
+        if (gt >= 0 && gt < 64 * RMAX) {
+            const int i = gt / RMAX, l = gt % RMAX;
             const bool valid = (i < n) && (l < R);
             pf_gam = valid ? p.gamma[(tok0 + i) * R + l] : 0.f;
             pf_eta = valid ? p.eta[(tok0 + i) * R + l] : 0.f;
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (c_begin < c_end) load_gates(c_begin);
     // gates in registers -> one set of per-token scalars (no barrier inside)
     auto fill_scalars = [&](float *set) {
-        if (warp == 0) {  // inclusive scan of the 64 log-decays, two per lane, in registers
+        if (warp == SCAN_WARP) {  // inclusive scan of the 64 log-decays, two per lane, in registers
             const float la0 = logf(pf_a0), la1 = logf(pf_a1);
             float s = la0 + la1;
 #pragma unroll
@@ -440,9 +446,9 @@ __global__ void __launch_bounds__(NT, 1)
             set[320 + i1] = pf_b1 * __expf(l1);
             if (lane == 31 && -lcw > 80.f) set_status(p.status, kDevBounds);  // beyond the factorised range
         }
-        if (tid < 64 * RMAX) {
-            set[384 + tid] = pf_gam;
-            set[384 + 64 * RMAX + tid] = pf_eta;
+        if (gt >= 0 && gt < 64 * RMAX) {
+            set[384 + gt] = pf_gam;
+            set[384 + 64 * RMAX + gt] = pf_eta;
         }
     };
 
@@ -469,17 +475,23 @@ __global__ void __launch_bounds__(NT, 1)
         const float lc = s_lam[63];
 
         PHASE_MARK(0);
-        // ---- P2: Gram tiles  D1 = [Q; K] [K; U]^T ------------------------------------------------
+        // ---- P2: Gram tiles  D1 = [K; U_0] [Q; K]^T,  D1' = [U_1; U_2] [Q; K]^T ------------------
+        // (rows are key/direction tokens j, columns query/key tokens i: the score tiles come out
+        // transposed, [j][i], which is the operand form the later products read)
         if (!wait_two(mb_qku, ph_qku, 2u, mb_v[stage], ph_v[stage], 4u << stage)) break;
         if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
-        const int N1 = 64 * (1 + R);
         if (tid == 0) {  // the input tiles are still bf16 here (exact values); the Gram runs on them
             fence_after_sync();
-            const uint32_t id = idesc_bf16(128, N1, 0, 0);
+            const uint32_t id = idesc_bf16(128, 128, 0, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_D1, dsc(dbase, OFF_Q + s * 32, 16, 1024), dsc(dbase, OFF_K + s * 32, 16, 1024),
+                mma_f16(tmem + TM_D1, dsc(dbase, OFF_K + s * 32, 16, 1024), dsc(dbase, OFF_Q + s * 32, 16, 1024),
                         id, s > 0);
+            if (R >= 2)
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(tmem + TM_D1 + 128, dsc(dbase, OFF_U + TILE + s * 32, 16, 1024),
+                            dsc(dbase, OFF_Q + s * 32, 16, 1024), id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
             // the Gram is waited for here, before this warp joins the prep: measured faster
@@ -550,44 +562,45 @@ __global__ void __launch_bounds__(NT, 1)
         tiles_bf16_to_f16(sm + OFF_K, (1 + R) * TILE, tid);
 
         PHASE_MARK(2);
-        // ---- E1: masks and decay factors -> A (fp32), PK_l, PQ_l, G (bf16 tiles) ---------------
+        // ---- E1: masks and decay factors -> A (fp32), PK_l^T, PQ_l^T, G^T (fp16 tiles) ----------
+        // TMEM lanes 0..63 hold key rows k_j, 64..127 direction rows u_{j,0} (D1) and u_{j,1},
+        // u_{j,2} (D1'); column block 0/2 holds the query side q_i, 1/3 the key side k_i.
         {
-            const int i = row & 63;
-            const bool qside = row < 64;
-            const float rf = s_rowf[i];
-            const float bi = s_beta[i];
-            const int nblk = N1 / 64;  // 64-column blocks: 0 = keys, 1.. = levels
+            const int r = row & 63;
+            const bool upper = row >= 64;
+            const int nblk = R >= 2 ? 4 : 2;
+            const bool skip = upper && R == 0;  // u_0 rows do not exist
+            const float rf = s_rowf[r];
+            const float br = s_beta[r];
+            const int j0 = sub * CW;
 #pragma unroll
             for (int b2 = 0; b2 < 4; b2 += 2) {  // two 64-column blocks per TMEM wait
-                if (b2 >= nblk) break;
+                if (b2 >= nblk || skip) break;
+                if (b2 == 2 && upper && R < 3) break;  // u_2 rows do not exist
                 uint32_t rr[2][CW];
 #pragma unroll
                 for (int u = 0; u < 2; ++u)
-                    if (b2 + u < nblk)
-                        tmem_ld_nowait(tmem + TM_D1 + ((uint32_t)(quad * 32) << 16) + (uint32_t)((b2 + u) * 64 + sub * CW),
-                                       rr[u]);
+                    tmem_ld_nowait(tmem + TM_D1 + ((uint32_t)(quad * 32) << 16) + (uint32_t)((b2 + u) * 64 + j0), rr[u]);
                 tmem_wait_ld();
+                const int l = b2 ? (upper ? 2 : 1) : 0;  // direction level of an upper / D1' row
+                const bool keyrow = b2 == 0 && !upper;
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const int blk = b2 + u;
-                    if (blk >= nblk) break;
                     float v[CW];
                     u2f(rr[u], v);
-                    const int j0 = sub * CW;
-                    if (qside) {
+                    if (u == 0) {  // query side: G^T (key rows) or PQ_l^T, kept where i >= j
 #pragma unroll
-                        for (int q = 0; q < CW; ++q) v[q] = (j0 + q <= i) ? v[q] : 0.f;
-                        uint8_t *tile = sm + (blk == 0 ? OFF_G : OFF_E + (blk - 1) * 2 * TILE + TILE);
-                        st_row(tile, i, j0, v);
-                    } else if (blk == 0) {
+                        for (int q = 0; q < CW; ++q) v[q] = (j0 + q >= r) ? v[q] : 0.f;
+                        st_row(sm + (keyrow ? OFF_G : OFF_E + (2 * l + 1) * TILE), r, j0, v);
+                    } else if (keyrow) {  // A_ij = beta_i rowf_i colf_j k_i.k_j (j < i), from k_j.k_i
                         float *A = reinterpret_cast<float *>(sm + OFF_AKK);
 #pragma unroll
                         for (int q = 0; q < CW; ++q)
-                            A[i * LDAA + j0 + q] = (j0 + q < i) ? v[q] * bi * rf * s_colf[j0 + q] : 0.f;
-                    } else {
+                            A[r * LDAA + j0 + q] = (j0 + q < r) ? v[q] * br * rf * s_colf[j0 + q] : 0.f;
+                    } else {  // PK_l^T, kept where i > j
 #pragma unroll
-                        for (int q = 0; q < CW; ++q) v[q] = (j0 + q < i) ? v[q] : 0.f;
-                        st_row(sm + OFF_E + (blk - 1) * 2 * TILE, i, j0, v);
+                        for (int q = 0; q < CW; ++q) v[q] = (j0 + q > r) ? v[q] : 0.f;
+                        st_row(sm + OFF_E + 2 * l * TILE, r, j0, v);
                     }
                 }
             }
@@ -600,11 +613,13 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- P3: MX = sum_l PK_l Xs_l (MMA, in flight) while the CTA solves T = (I + A)^{-1} -------
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t id = idesc_f16(128, 64, 0, 1);
+            // A = PK_l^T in MN-major form; its second 64-row atom (lanes 64..127, never read)
+            // points at the next tile
+            const uint32_t id = idesc_f16(128, 64, 1, 1);
             for (int l = 0; l < R; ++l)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(tmem + TM_D2, dsc(dbase, OFF_E + l * 2 * TILE + s * 32, 16, 1024),
+                    mma_f16(tmem + TM_D2, dsc(dbase, OFF_E + l * 2 * TILE + s * 2048, TILE, 1024),
                              dsc(dbase, OFF_XS + l * TILE + s * 2048, TILE, 1024), id, (l | s) != 0);
             mma_commit(mb_mma);
             pending |= 1u;
@@ -615,8 +630,9 @@ __global__ void __launch_bounds__(NT, 1)
             const float *A = reinterpret_cast<const float *>(sm + OFF_AKK);
             float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
             const Frag fr{lane >> 2, lane & 3};
-            if (tid < 64) {  // diagonal 16x16 blocks by forward substitution, one column per thread
-                const int o = 16 * (tid >> 4), cc = tid & 15;
+            if (tid >= 64 && tid < 128) {  // diagonal 16x16 blocks by forward substitution, one
+                // column per thread (warps 2-3: warp 0 is issuing the MX products meanwhile)
+                const int o = 16 * ((tid - 64) >> 4), cc = tid & 15;
                 float t[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
@@ -783,25 +799,20 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
 
         PHASE_MARK(7);
-        // ---- P5: D4 = UWs [G; PQ]^T-part, D5 = UWs [K; U]-part ------------------------------------
+        // ---- P5: [D5 | D4] = UWs [K | G^T] + sum_l [Xs_l^T; 0] [U_l | PQ_l^T]  (N = 128) ----------
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t idk = idesc_f16(128, 64, 0, 0), idx = idesc_f16(128, 64, 1, 0);
-            const uint32_t idk5 = idesc_f16(128, 64, 0, 1), idx5 = idesc_f16(128, 64, 1, 1);
+            const uint32_t idk = idesc_f16(128, 128, 0, 1), idx = idesc_f16(128, 128, 1, 1);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t a = dsc(dbase, OFF_AKK + s * 32, 16, 1024);
-                mma_f16(tmem + TM_D4, a, dsc(dbase, OFF_G + s * 32, 16, 1024), idk, s > 0);
-                mma_f16(tmem + TM_D5, a, dsc(dbase, OFF_K + s * 2048, TILE, 1024), idk5, s > 0);
-            }
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + TM_D5, dsc(dbase, OFF_AKK + s * 32, 16, 1024),
+                        dsc(dbase, OFF_K + s * 2048, OFF_G - OFF_K, 1024), idk, s > 0);
             for (int l = 0; l < R; ++l) {
-                const uint32_t xs = OFF_XS + l * TILE;
+                const uint32_t xs = OFF_XS + l * TILE, ub = OFF_U + l * TILE, pq = OFF_E + l * 2 * TILE + TILE;
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t a = dsc(dbase, xs + s * 2048, OFF_ZERO - xs, 1024);
-                    mma_f16(tmem + TM_D4, a, dsc(dbase, OFF_E + l * 2 * TILE + TILE + s * 32, 16, 1024), idx, 1);
-                    mma_f16(tmem + TM_D5, a, dsc(dbase, OFF_U + l * TILE + s * 2048, TILE, 1024), idx5, 1);
-                }
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(tmem + TM_D5, dsc(dbase, xs + s * 2048, OFF_ZERO - xs, 1024),
+                            dsc(dbase, ub + s * 2048, pq - ub, 1024), idx, 1);
             }
             mma_commit(mb_mma);
             pending |= 1u;
@@ -851,14 +862,12 @@ __global__ void __launch_bounds__(NT, 1)
                 mbar_expect_tx(mb_qku, TILE);
                 tma_load_3d(sbase + OFF_Q, &tm_q, mb_qku, 0, (c + 1) * C, bh);
             }
-            // ---- P6: D6 = Z Mc, D7 = Z Qt ------------------------------------------------------
-            const uint32_t id = idesc_f16(128, 64, 0, 1);
+            // ---- P6: [D7 | D6] = Z [Qt | Mc]  (N = 128) ------------------------------------------
+            const uint32_t id = idesc_f16(128, 128, 0, 1);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t a = dsc(dbase, OFF_ZA + s * 32, 16, 1024);
-                mma_f16(tmem + TM_D6, a, dsc(dbase, OFF_E + TILE + s * 2048, TILE, 1024), id, s > 0);
-                mma_f16(tmem + TM_D7, a, dsc(dbase, OFF_E + s * 2048, TILE, 1024), id, s > 0);
-            }
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + TM_D7, dsc(dbase, OFF_ZA + s * 32, 16, 1024), dsc(dbase, OFF_E + s * 2048, TILE, 1024),
+                        id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
         }
