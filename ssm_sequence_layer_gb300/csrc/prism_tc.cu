@@ -46,12 +46,13 @@
 // Developer tracing: with -DPRISM_PHASE_TIMERS the segment kernel accumulates clock64()
 // cycles per phase of its chunk loop (thread 0 of every CTA) into prism_tc_phase_cycles.
 #ifdef PRISM_PHASE_TIMERS
-__device__ unsigned long long prism_tc_phase_cycles[16];
+constexpr int kPhaseSlots = 24;
+__device__ unsigned long long prism_tc_phase_cycles[kPhaseSlots];
 #define PHASE_MARK(k)                                         \
     do {                                                      \
         if (threadIdx.x == 0) {                               \
             const long long now_ = clock64();                 \
-            ph_acc[k] += (unsigned long long)(now_ - ph_last); \
+            ph_acc_s[k] += (unsigned long long)(now_ - ph_last); \
             ph_last = now_;                                   \
         }                                                     \
     } while (0)
@@ -209,14 +210,6 @@ __device__ __forceinline__ void frag_b(const Frag &f, const float *M, int ld, in
     b0 = to_tf32(p[0]);
     b1 = to_tf32(p[4 * ld]);
 }
-__device__ __forceinline__ void frag_c_load(const Frag &f, const float *M, int ld, int r0, int n0, float (&c)[4])
-{
-    const float *p = M + (r0 + f.gq) * ld + n0 + 2 * f.tq;
-    c[0] = p[0];
-    c[1] = p[1];
-    c[2] = p[8 * ld];
-    c[3] = p[8 * ld + 1];
-}
 __device__ __forceinline__ void frag_c_store(const Frag &f, float *M, int ld, int r0, int n0, const float (&c)[4], float sgn)
 {
     float *p = M + (r0 + f.gq) * ld + n0 + 2 * f.tq;
@@ -226,41 +219,10 @@ __device__ __forceinline__ void frag_c_store(const Frag &f, float *M, int ld, in
     p[8 * ld + 1] = sgn * c[3];
 }
 
-// C (16x16, stride ldc) = init + A (16x16, stride lda) B (16x16, stride ldb), one warp; all reads
-// happen before the warp's writes, so C may alias A or the initial value (in-place update).
-__device__ __forceinline__ void mm16_warp(const Frag &f, float *Cm, int ldc, const float *Am, int lda, const float *Bm,
-                                          int ldb, bool init_from_c)
-{
-    float c[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        if (init_from_c) {
-            frag_c_load(f, Cm, ldc, 0, 8 * nt, c[nt]);
-        } else {
-            c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
-        }
-    }
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        uint32_t a[4];
-        frag_a(f, Am, lda, 0, 8 * ks, a);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            uint32_t b0, b1;
-            frag_b(f, Bm, ldb, 8 * ks, 8 * nt, b0, b1);
-            mma_tf32(c[nt], a[0], a[1], a[2], a[3], b0, b1);
-        }
-    }
-    __syncwarp();
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) frag_c_store(f, Cm, ldc, 0, 8 * nt, c[nt], 1.f);
-    __syncwarp();
-}
-
 // in-place bf16 -> fp16 conversion of `bytes` bytes of tiles (layout unchanged)
-__device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes, int tid)
+__device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes, int t, int nthreads)
 {
-    for (uint32_t e = tid; e < bytes / 16; e += NT) {
+    for (uint32_t e = t; e < bytes / 16; e += nthreads) {
         uint4 w = reinterpret_cast<uint4 *>(base)[e];
         uint32_t *pw = &w.x;
 #pragma unroll
@@ -272,6 +234,9 @@ __device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes,
         reinterpret_cast<uint4 *>(base)[e] = w;
     }
 }
+
+// barrier over `n` threads (whole warps) of the CTA; ids 1.. (0 is __syncthreads')
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(NT, 1)
@@ -453,7 +418,10 @@ __global__ void __launch_bounds__(NT, 1)
     };
 
 #ifdef PRISM_PHASE_TIMERS
-    unsigned long long ph_acc[16] = {0};
+    // per-phase totals in shared memory (registers would crowd the kernel's own)
+    __shared__ unsigned long long ph_acc_s[kPhaseSlots];
+    if (tid == 0)
+        for (int k = 0; k < kPhaseSlots; ++k) ph_acc_s[k] = 0;
     long long ph_last = clock64();
 #endif
     bool alive = true;
@@ -557,9 +525,6 @@ __global__ void __launch_bounds__(NT, 1)
         PHASE_MARK(14);
         if (abort_s) break;
         fence_after_sync();
-        // the Gram has read K and U: convert them to fp16 in place for the state-side MMA (their
-        // fence and barrier are E1's)
-        tiles_bf16_to_f16(sm + OFF_K, (1 + R) * TILE, tid);
 
         PHASE_MARK(2);
         // ---- E1: masks and decay factors -> A (fp32), PK_l^T, PQ_l^T, G^T (fp16 tiles) ----------
@@ -610,7 +575,10 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
 
         PHASE_MARK(3);
-        // ---- P3: MX = sum_l PK_l Xs_l (MMA, in flight) while the CTA solves T = (I + A)^{-1} -------
+        // ---- P3: MX = sum_l PK_l Xs_l on the tensor core.  Meanwhile the warps of TMEM lane
+        // quarters 2-3 solve T = (I + A)^{-1}, and those of quarters 0-1 (thread 0 among them)
+        // wait for MX, form the RHS (E2) and convert K and U to fp16.  The two groups of 256
+        // threads sync on named barriers 1 and 2 and meet again at the CTA barrier before P4.
         if (tid == 0) {
             fence_after_sync();
             // A = PK_l^T in MN-major form; its second 64-row atom (lanes 64..127, never read)
@@ -624,132 +592,142 @@ __global__ void __launch_bounds__(NT, 1)
             mma_commit(mb_mma);
             pending |= 1u;
         }
-        {
-            // T = (I + A)^{-1} by 16x16 blocks: diagonal blocks by forward substitution, then the
-            // block diagonals below them, T[bi][bj] = -T[bi][bi] sum_{k=bj..bi-1} A[bi][k] T[k][bj]
-            const float *A = reinterpret_cast<const float *>(sm + OFF_AKK);
-            float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
-            const Frag fr{lane >> 2, lane & 3};
-            if (tid >= 64 && tid < 128) {  // diagonal 16x16 blocks by forward substitution, one
-                // column per thread (warps 2-3: warp 0 is issuing the MX products meanwhile)
-                const int o = 16 * ((tid - 64) >> 4), cc = tid & 15;
-                float t[16];
+        PHASE_MARK(11);
+        if (quad >= 2) {
+            {
+                // T = (I + A)^{-1} by 16x16 blocks: diagonal blocks by forward substitution, then the
+                // block diagonals below them, T[bi][bj] = -T[bi][bi] sum_{k=bj..bi-1} A[bi][k] T[k][bj]
+                const int sw = ((warp >> 2) << 1) | (warp & 1);  // solver warp 0..7: warps 2,3,6,7,10,11,14,15
+                const int stid = sw * 32 + lane;
+                const float *A = reinterpret_cast<const float *>(sm + OFF_AKK);
+                float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
+                const Frag fr{lane >> 2, lane & 3};
+                if (tid >= 64 && tid < 128) {  // diagonal 16x16 blocks by forward substitution, one
+                    // column per thread (warps 2-3)
+                    const int o = 16 * ((tid - 64) >> 4), cc = tid & 15;
+                    float t[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    // t[j] = 0 for j < cc, so the sum may run over all j < r
-                    float s0 = 0.f, s1 = 0.f;
+                    for (int r = 0; r < 16; ++r) {
+                        // t[j] = 0 for j < cc, so the sum may run over all j < r
+                        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                    for (int j = 0; j + 1 < r; j += 2) {
-                        s0 = fmaf(A[(o + r) * LDAA + o + j], t[j], s0);
-                        s1 = fmaf(A[(o + r) * LDAA + o + j + 1], t[j + 1], s1);
+                        for (int j = 0; j + 1 < r; j += 2) {
+                            s0 = fmaf(A[(o + r) * LDAA + o + j], t[j], s0);
+                            s1 = fmaf(A[(o + r) * LDAA + o + j + 1], t[j + 1], s1);
+                        }
+                        if (r & 1) s0 = fmaf(A[(o + r) * LDAA + o + r - 1], t[r - 1], s0);
+                        t[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -(s0 + s1));
+                        T32[(o + r) * LDA + o + cc] = t[r];
                     }
-                    if (r & 1) s0 = fmaf(A[(o + r) * LDAA + o + r - 1], t[r - 1], s0);
-                    t[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -(s0 + s1));
-                    T32[(o + r) * LDA + o + cc] = t[r];
                 }
-            }
-            __syncthreads();
-            PHASE_MARK(11);
-            if (warp < 4) {
-                // 16 -> 32: T[1][0] = -T[1][1] A[1][0] T[0][0], T[3][2] likewise; warp w owns one
-                // 8-column tile of one block
-                const int pb = warp >> 1, nt = warp & 1;         // block pair (0: rows 16.., 1: rows 48..)
-                const int ri = 16 + 32 * pb, cj = 32 * pb;        // block (ri, cj) below the diagonal
-                float x[4] = {0.f, 0.f, 0.f, 0.f};
+                named_bar(1, NT / 2);
+                if (sw < 4) {
+                    // 16 -> 32: T[1][0] = -T[1][1] A[1][0] T[0][0], T[3][2] likewise; solver warp sw
+                    // owns one 8-column tile of one block
+                    const int pb = sw >> 1, nt = sw & 1;         // block pair (0: rows 16.., 1: rows 48..)
+                    const int ri = 16 + 32 * pb, cj = 32 * pb;        // block (ri, cj) below the diagonal
+                    float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {                 // X = A[ri][cj] T[cj][cj] (cols 8 nt..)
-                    uint32_t a[4], b0, b1;
-                    frag_a(fr, A, LDAA, ri, cj + 8 * ks, a);
-                    frag_b(fr, T32, LDA, cj + 8 * ks, cj + 8 * nt, b0, b1);
-                    mma_tf32(x, a[0], a[1], a[2], a[3], b0, b1);
+                    for (int ks = 0; ks < 2; ++ks) {                 // X = A[ri][cj] T[cj][cj] (cols 8 nt..)
+                        uint32_t a[4], b0, b1;
+                        frag_a(fr, A, LDAA, ri, cj + 8 * ks, a);
+                        frag_b(fr, T32, LDA, cj + 8 * ks, cj + 8 * nt, b0, b1);
+                        mma_tf32(x, a[0], a[1], a[2], a[3], b0, b1);
+                    }
+                    float *X = s_xtmp + sw * 128;                     // 16 x 8
+                    X[fr.gq * 8 + 2 * fr.tq] = x[0];
+                    X[fr.gq * 8 + 2 * fr.tq + 1] = x[1];
+                    X[(fr.gq + 8) * 8 + 2 * fr.tq] = x[2];
+                    X[(fr.gq + 8) * 8 + 2 * fr.tq + 1] = x[3];
+                    __syncwarp();
+                    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {                 // T[ri][cj] = -T[ri][ri] X
+                        uint32_t a[4], b0, b1;
+                        frag_a(fr, T32, LDA, ri, ri + 8 * ks, a);
+                        frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
+                        mma_tf32(y, a[0], a[1], a[2], a[3], b0, b1);
+                    }
+                    frag_c_store(fr, T32, LDA, ri, cj + 8 * nt, y, -1.f);
                 }
-                float *X = s_xtmp + warp * 128;                   // 16 x 8
-                X[fr.gq * 8 + 2 * fr.tq] = x[0];
-                X[fr.gq * 8 + 2 * fr.tq + 1] = x[1];
-                X[(fr.gq + 8) * 8 + 2 * fr.tq] = x[2];
-                X[(fr.gq + 8) * 8 + 2 * fr.tq + 1] = x[3];
-                __syncwarp();
-                float y[4] = {0.f, 0.f, 0.f, 0.f};
+                named_bar(1, NT / 2);
+                if (sw < 4) {
+                    // 32 -> 64: T[32:64][0:32] = -T[32:64][32:64] A[32:64][0:32] T[0:32][0:32]; solver
+                    // warp sw owns the 8-column tile 8 sw of the 32x32 block (both 16-row halves)
+                    const int n0 = 8 * sw;
+                    float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    // T_lo[k][n] = 0 for k < 16 <= n: block (0,1) of T32 is never written, so skip it
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {                 // T[ri][cj] = -T[ri][ri] X
-                    uint32_t a[4], b0, b1;
-                    frag_a(fr, T32, LDA, ri, ri + 8 * ks, a);
-                    frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
-                    mma_tf32(y, a[0], a[1], a[2], a[3], b0, b1);
-                }
-                frag_c_store(fr, T32, LDA, ri, cj + 8 * nt, y, -1.f);
-            }
-            __syncthreads();
-            if (warp < 4) {
-                // 32 -> 64: T[32:64][0:32] = -T[32:64][32:64] A[32:64][0:32] T[0:32][0:32]; warp w owns
-                // the 8-column tile 8 w of the 32x32 block (both 16-row halves)
-                const int n0 = 8 * warp;
-                float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                // T_lo[k][n] = 0 for k < 16 <= n: block (0,1) of T32 is never written, so skip it
+                    for (int ks = 0; ks < 4; ++ks) {                 // X = A_lo T_lo
+                        if (n0 >= 16 && ks < 2) continue;
+                        uint32_t b0, b1;
+                        frag_b(fr, T32, LDA, 8 * ks, n0, b0, b1);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {                 // X = A_lo T_lo
-                    if (n0 >= 16 && ks < 2) continue;
-                    uint32_t b0, b1;
-                    frag_b(fr, T32, LDA, 8 * ks, n0, b0, b1);
+                        for (int mt = 0; mt < 2; ++mt) {
+                            uint32_t a[4];
+                            frag_a(fr, A, LDAA, 32 + 16 * mt, 8 * ks, a);
+                            mma_tf32(x[mt], a[0], a[1], a[2], a[3], b0, b1);
+                        }
+                    }
+                    float *X = s_xtmp + sw * 256;                     // 32 x 8
 #pragma unroll
                     for (int mt = 0; mt < 2; ++mt) {
-                        uint32_t a[4];
-                        frag_a(fr, A, LDAA, 32 + 16 * mt, 8 * ks, a);
-                        mma_tf32(x[mt], a[0], a[1], a[2], a[3], b0, b1);
+                        X[(16 * mt + fr.gq) * 8 + 2 * fr.tq] = x[mt][0];
+                        X[(16 * mt + fr.gq) * 8 + 2 * fr.tq + 1] = x[mt][1];
+                        X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq] = x[mt][2];
+                        X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq + 1] = x[mt][3];
                     }
-                }
-                float *X = s_xtmp + warp * 256;                   // 32 x 8
+                    __syncwarp();
+                    float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    X[(16 * mt + fr.gq) * 8 + 2 * fr.tq] = x[mt][0];
-                    X[(16 * mt + fr.gq) * 8 + 2 * fr.tq + 1] = x[mt][1];
-                    X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq] = x[mt][2];
-                    X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq + 1] = x[mt][3];
-                }
-                __syncwarp();
-                float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int ks = 0; ks < 4; ++ks) {                 // T_lower = -T_hi X
+                        uint32_t b0, b1;
+                        frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {                 // T_lower = -T_hi X
-                    uint32_t b0, b1;
-                    frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        if (mt == 0 && ks >= 2) continue;  // T_hi[0:16][16:32] = 0 (block (2,3) is never written)
-                        uint32_t a[4];
-                        frag_a(fr, T32, LDA, 32 + 16 * mt, 32 + 8 * ks, a);
-                        mma_tf32(y[mt], a[0], a[1], a[2], a[3], b0, b1);
+                        for (int mt = 0; mt < 2; ++mt) {
+                            if (mt == 0 && ks >= 2) continue;  // T_hi[0:16][16:32] = 0 (block (2,3) is never written)
+                            uint32_t a[4];
+                            frag_a(fr, T32, LDA, 32 + 16 * mt, 32 + 8 * ks, a);
+                            mma_tf32(y[mt], a[0], a[1], a[2], a[3], b0, b1);
+                        }
                     }
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) frag_c_store(fr, T32, LDA, 32 + 16 * mt, n0, y[mt], -1.f);
                 }
+                named_bar(1, NT / 2);
+                for (int e = stid; e < 64 * 8; e += NT / 2) {  // T (fp16, [i][j], zero above the diagonal)
+                    const int i = e >> 3, g = e & 7;
+                    const float4 lo = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g);
+                    const float4 hi = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g + 4);
+                    const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    float m[8];
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) frag_c_store(fr, T32, LDA, 32 + 16 * mt, n0, y[mt], -1.f);
+                    for (int q = 0; q < 8; ++q) m[q] = (8 * g + q <= i) ? v[q] : 0.f;
+                    uint4 w;
+                    w.x = pack2(m[0], m[1]);
+                    w.y = pack2(m[2], m[3]);
+                    w.z = pack2(m[4], m[5]);
+                    w.w = pack2(m[6], m[7]);
+                    *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128(i, 8 * g)) = w;
+                }
             }
-            __syncthreads();
-            PHASE_MARK(12);
-            for (int e = tid; e < 64 * 8; e += NT) {  // T (fp16, [i][j], zero above the diagonal)
-                const int i = e >> 3, g = e & 7;
-                const float4 lo = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g);
-                const float4 hi = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g + 4);
-                const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                float m[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) m[q] = (8 * g + q <= i) ? v[q] : 0.f;
-                uint4 w;
-                w.x = pack2(m[0], m[1]);
-                w.y = pack2(m[2], m[3]);
-                w.z = pack2(m[4], m[5]);
-                w.w = pack2(m[6], m[7]);
-                *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128(i, 8 * g)) = w;
+        } else {
+            if (tid == 0) {
+                if (mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
+                    ph_mma ^= 1u;
+                    pending &= ~1u;
+                } else {
+                    abort_s = 1;
+                    set_status(p.status, kDevTimeout);
+                }
             }
-            PHASE_MARK(13);
-        }
-        if (!wait_all(mb_mma, ph_mma, 1u)) break;
-        fence_after_sync();
-
-        PHASE_MARK(4);
-        // ---- E2: RHS = diag(beta) V - MX (diag(beta Gamma) K was formed during the prep) ---------
-        {
-            const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + (stage ? OFF_V1 : OFF_V0));
-            if (quad < 2) {  // lanes 0..63 hold MX rows
+            named_bar(2, NT / 2);
+            PHASE_MARK(4);
+            if (abort_s == 0) {
+                fence_after_sync();
+                // ---- E2: RHS = diag(beta) V - MX (diag(beta Gamma) K was formed during the prep) -----
+                // (lanes 0..63 hold the MX rows)
+                const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + (stage ? OFF_V1 : OFF_V0));
                 const int i = row, j0 = sub * CW;
                 float v[CW];
                 if (R > 0) {
@@ -761,12 +739,17 @@ __global__ void __launch_bounds__(NT, 1)
                 const float bi = s_beta[i], brf = s_beta[i] * s_rowf[i];
 #pragma unroll
                 for (int q = 0; q < CW; ++q) v[q] = bi * __bfloat162float(vb[(i + 8) * 64 + j0 + q]) - brf * v[q];
-                st_row(sm + OFF_AKK, i, j0, v);  // RHS tile (A is dead after the solve)
+                st_row(sm + OFF_E, i, j0, v);  // RHS tile, over PK_0^T (MX, its reader, is complete)
+                PHASE_MARK(12);
+                // K and U to fp16 in place for the state-side products (the Gram has read them)
+                tiles_bf16_to_f16(sm + OFF_K, (1 + R) * TILE, (warp >> 2) * 64 + (warp & 1) * 32 + lane, NT / 2);
+                PHASE_MARK(13);
             }
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
+        if (abort_s) break;
 
         PHASE_MARK(5);
         // ---- P4: [U'^T ; W^T] = [RHS | BGK]^T T^T -------------------------------------------------
@@ -775,7 +758,7 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t id = idesc_f16(128, 64, 1, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_D3, dsc(dbase, OFF_AKK + s * 2048, OFF_BGK - OFF_AKK, 1024),
+                mma_f16(tmem + TM_D3, dsc(dbase, OFF_E + s * 2048, OFF_BGK - OFF_E, 1024),
                         dsc(dbase, OFF_TB + s * 32, 16, 1024),
                          id, s > 0);
             mma_commit(mb_mma);
@@ -792,7 +775,7 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_ld(tmem + TM_D3 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
 #pragma unroll
             for (int q = 0; q < CW; ++q) v[q] *= s_colf[j0 + q];
-            st_row(sm + OFF_AKK, row, j0, v);  // over RHS: MMA3, its only reader, has completed
+            st_row(sm + OFF_AKK, row, j0, v);  // over A (the solve is complete)
         }
         fence_async_smem();
         fence_before_sync();
@@ -918,7 +901,9 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int q = 0; q < CW; ++q) sq[(j0 + q) * 64 + row - 64] = __float2half_rn(o[q]);
             }
         }
+        PHASE_MARK(16);
         __syncthreads();
+        PHASE_MARK(17);
         {
             const float *so = reinterpret_cast<const float *>(sm + OFF_E);
             bool finite = true;
@@ -950,12 +935,14 @@ __global__ void __launch_bounds__(NT, 1)
                                                (((size_t)bh * p.NC + c) * 64 + i) * 64 + c4) = w;
                 }
             }
+            PHASE_MARK(18);
             if (seg > 0) {
                 const uint4 *sq = reinterpret_cast<const uint4 *>(sm + OFF_E + 2 * TILE);
                 uint4 *dq = reinterpret_cast<uint4 *>(p.stash_q + ((size_t)bh * p.NC + c) * 4096);
                 for (int e = tid; e < 512; e += NT) dq[e] = sq[e];
             }
             if (!finite) set_status(p.status, kDevBounds);  // outside the fp16 operand range
+            PHASE_MARK(19);
         }
         fence_before_sync();
         __syncthreads();
@@ -964,7 +951,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
 #ifdef PRISM_PHASE_TIMERS
     if (tid == 0)
-        for (int k = 0; k < 16; ++k) atomicAdd(&prism_tc_phase_cycles[k], ph_acc[k]);
+        for (int k = 0; k < kPhaseSlots; ++k) atomicAdd(&prism_tc_phase_cycles[k], ph_acc_s[k]);
 #endif
 
     // drain: after an expired wait, let every copy and MMA still in flight land (bounded by
@@ -1342,11 +1329,12 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
 
 #ifdef PRISM_PHASE_TIMERS
 // developer tracing build only: copy out (and optionally clear) the per-phase cycle totals
-extern "C" __attribute__((visibility("default"))) int prism_debug_phase_cycles(unsigned long long *out16, int reset)
+extern "C" __attribute__((visibility("default"))) int prism_debug_phase_cycles(unsigned long long *out, int reset)
 {
-    if (cudaMemcpyFromSymbol(out16, prism_tc_phase_cycles, sizeof(unsigned long long) * 16) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(out, prism_tc_phase_cycles, sizeof(unsigned long long) * kPhaseSlots) != cudaSuccess)
+        return -1;
     if (reset) {
-        unsigned long long z[16] = {0};
+        unsigned long long z[kPhaseSlots] = {0};
         if (cudaMemcpyToSymbol(prism_tc_phase_cycles, z, sizeof(z)) != cudaSuccess) return -1;
     }
     return 0;
