@@ -295,6 +295,10 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = tmem_base_s;
+    // the set-up above touches no global memory; everything below may depend on the previous
+    // kernel in the stream (inputs, or the workspace a previous forward's fix-up still reads)
+    grid_dependency_wait();
+    allow_dependent_launch();
 
     uint32_t ph_mma = 0, ph_qku = 0, ph_v[2] = {0, 0};
     uint32_t pending = 0;  // issuer's view (thread 0): 1 MMA, 2 Q/K/U load, 4/8 V loads in flight
@@ -972,12 +976,15 @@ __global__ void __launch_bounds__(NT, 1)
 // combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} in fp32, 8 value rows per block, written
 // out as fp16 (the fix-up's MMA operand).  The maps stream through a ring of CB_STAGES
 // shared-memory stages filled by bulk copies (16 KB of M and this block's 2 KB of N per
-// segment), so the serial chain never waits on global memory latency.  Warp w owns rows 2w and
-// 2w + 1, lane l columns 2l and 2l + 1; the running rows are double-buffered in shared memory,
-// so one barrier per segment orders both the row exchange and the reuse of a ring stage.
+// segment), so the serial chain never waits on global memory latency.  Each step's 8x64x64
+// product is split over the sum index: thread (kq, rg, lane) accumulates rows 4 rg .. 4 rg + 3,
+// columns 2 lane, 2 lane + 1 over m in [16 kq, 16 kq + 16); the four partial sums meet in shared
+// memory.  The running rows are double-buffered, so two barriers per segment order the row
+// exchange, the partial sums and the reuse of a ring stage.
 constexpr int CB_ROWS = 8;
 constexpr int CB_STAGES = 4;
-constexpr int CB_THREADS = 128;
+constexpr int CB_KQ = 4;                       // parts of the sum index
+constexpr int CB_THREADS = CB_KQ * 2 * 32;     // x 2 row groups x 32 column pairs
 constexpr int CB_STAGE_FLOATS = 64 * 64 + CB_ROWS * 64;
 constexpr size_t CB_SMEM = (size_t)CB_STAGES * CB_STAGE_FLOATS * 4 + 128;
 
@@ -987,17 +994,15 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
     extern __shared__ __align__(128) float ring[];  // [CB_STAGES][M 64x64 | N 8x64]
     __shared__ __align__(8) uint64_t mb[CB_STAGES];
     __shared__ __align__(16) float S[2][CB_ROWS][64];
+    __shared__ __align__(16) float part[CB_KQ][CB_ROWS][64];
     __shared__ int abort_s;
     const int bh = blockIdx.x, r0 = blockIdx.y * CB_ROWS, tid = threadIdx.x;
-    const int w = tid >> 5, l = tid & 31;
-    const int ra = 2 * w, rb = 2 * w + 1, c2 = 2 * l;  // rows ra, rb; columns c2, c2 + 1
-    {
-        __half2 *d0 = reinterpret_cast<__half2 *>(sstart + ((size_t)bh * P * 64 + r0 + ra) * 64 + c2);
-        d0[0] = __floats2half2_rn(0.f, 0.f);
-        d0[32] = __floats2half2_rn(0.f, 0.f);
-        *reinterpret_cast<float2 *>(&S[0][ra][c2]) = make_float2(0.f, 0.f);
-        *reinterpret_cast<float2 *>(&S[0][rb][c2]) = make_float2(0.f, 0.f);
-    }
+    const int kq = tid >> 6, rg = (tid >> 5) & 1, l = tid & 31, c2 = 2 * l;
+    const int rr = tid >> 5;  // the row this thread reduces (columns c2, c2 + 1)
+    prism::tc::grid_dependency_wait();  // the segment maps of the segment kernel
+    prism::tc::allow_dependent_launch();
+    *reinterpret_cast<__half2 *>(sstart + ((size_t)bh * P * 64 + r0 + rr) * 64 + c2) = __floats2half2_rn(0.f, 0.f);
+    *reinterpret_cast<float2 *>(&S[0][rr][c2]) = make_float2(0.f, 0.f);
     if (P < 2) return;
     const int nmaps = P - 1;  // maps of segments 0..P-2 are used
     auto issue = [&](int sp) {
@@ -1016,12 +1021,23 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
         for (int sp = 0; sp < nmaps && sp < CB_STAGES; ++sp) issue(sp);
     }
     int issued = min(nmaps, CB_STAGES);
+#ifdef PRISM_PHASE_TIMERS
+    const bool trace = tid == 0 && blockIdx.x == 0 && blockIdx.y == 0;
+    unsigned long long t_wait = 0;
+    const long long t_begin = clock64();
+#endif
     for (int k = 0; k < nmaps; ++k) {
         const int st = k % CB_STAGES, buf = k & 1;
+#ifdef PRISM_PHASE_TIMERS
+        const long long tw0 = clock64();
+#endif
         if (tid == 0 && !prism::tc::mbar_wait(prism::tc::smem_u32(&mb[st]), (uint32_t)((k / CB_STAGES) & 1), wait_ns)) {
             abort_s = 1;
             atomicCAS(status, 0, kDevTimeout);
         }
+#ifdef PRISM_PHASE_TIMERS
+        if (trace) t_wait += clock64() - tw0;
+#endif
         __syncthreads();  // stage k landed; rows of step k - 1 written; stage of step k - 1 free
         if (abort_s) break;
         if (tid == 0 && k > 0 && issued < nmaps) {  // refill the stage step k - 1 read
@@ -1029,30 +1045,45 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
             issue(issued++);
         }
         const float *M = ring + (size_t)st * CB_STAGE_FLOATS;
-        const float2 na = *reinterpret_cast<const float2 *>(M + 64 * 64 + ra * 64 + c2);
-        const float2 nb = *reinterpret_cast<const float2 *>(M + 64 * 64 + rb * 64 + c2);
-        float a0 = na.x, a1 = na.y, b0 = nb.x, b1 = nb.y;
-        float e0 = 0.f, e1 = 0.f, f0 = 0.f, f1 = 0.f;  // second accumulator set: shorter FMA chains
-#pragma unroll 4
-        for (int m = 0; m < 64; m += 4) {
-            const float4 sa = *reinterpret_cast<const float4 *>(&S[buf][ra][m]);
-            const float4 sb = *reinterpret_cast<const float4 *>(&S[buf][rb][m]);
-            const float2 m0 = *reinterpret_cast<const float2 *>(M + (m + 0) * 64 + c2);
-            const float2 m1 = *reinterpret_cast<const float2 *>(M + (m + 1) * 64 + c2);
-            const float2 m2 = *reinterpret_cast<const float2 *>(M + (m + 2) * 64 + c2);
-            const float2 m3 = *reinterpret_cast<const float2 *>(M + (m + 3) * 64 + c2);
-            a0 = fmaf(sa.x, m0.x, a0); a1 = fmaf(sa.x, m0.y, a1); b0 = fmaf(sb.x, m0.x, b0); b1 = fmaf(sb.x, m0.y, b1);
-            e0 = fmaf(sa.y, m1.x, e0); e1 = fmaf(sa.y, m1.y, e1); f0 = fmaf(sb.y, m1.x, f0); f1 = fmaf(sb.y, m1.y, f1);
-            a0 = fmaf(sa.z, m2.x, a0); a1 = fmaf(sa.z, m2.y, a1); b0 = fmaf(sb.z, m2.x, b0); b1 = fmaf(sb.z, m2.y, b1);
-            e0 = fmaf(sa.w, m3.x, e0); e1 = fmaf(sa.w, m3.y, e1); f0 = fmaf(sb.w, m3.x, f0); f1 = fmaf(sb.w, m3.y, f1);
+        float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+        for (int m = 16 * kq; m < 16 * kq + 16; m += 4) {
+            float4 sv[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sv[r] = *reinterpret_cast<const float4 *>(&S[buf][4 * rg + r][m]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 mv = *reinterpret_cast<const float2 *>(M + (m + q) * 64 + c2);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float sq = q == 0 ? sv[r].x : q == 1 ? sv[r].y : q == 2 ? sv[r].z : sv[r].w;
+                    acc[r][0] = fmaf(sq, mv.x, acc[r][0]);
+                    acc[r][1] = fmaf(sq, mv.y, acc[r][1]);
+                }
+            }
         }
-        a0 += e0; a1 += e1; b0 += f0; b1 += f1;
-        *reinterpret_cast<float2 *>(&S[buf ^ 1][ra][c2]) = make_float2(a0, a1);
-        *reinterpret_cast<float2 *>(&S[buf ^ 1][rb][c2]) = make_float2(b0, b1);
-        __half2 *d = reinterpret_cast<__half2 *>(sstart + (((size_t)bh * P + k + 1) * 64 + r0 + ra) * 64 + c2);
-        d[0] = __floats2half2_rn(a0, a1);
-        d[32] = __floats2half2_rn(b0, b1);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float2 *>(&part[kq][4 * rg + r][c2]) = make_float2(acc[r][0], acc[r][1]);
+        __syncthreads();
+        float2 o = *reinterpret_cast<const float2 *>(M + 64 * 64 + rr * 64 + c2);  // N_p
+#pragma unroll
+        for (int q = 0; q < CB_KQ; ++q) {
+            const float2 v = *reinterpret_cast<const float2 *>(&part[q][rr][c2]);
+            o.x += v.x;
+            o.y += v.y;
+        }
+        *reinterpret_cast<float2 *>(&S[buf ^ 1][rr][c2]) = o;
+        *reinterpret_cast<__half2 *>(sstart + (((size_t)bh * P + k + 1) * 64 + r0 + rr) * 64 + c2) =
+            __floats2half2_rn(o.x, o.y);
     }
+#ifdef PRISM_PHASE_TIMERS
+    if (trace) {  // combine tracing: block (0, 0), thread 0: map waits and the whole chain
+        atomicAdd(&prism_tc_phase_cycles[20], t_wait);
+        atomicAdd(&prism_tc_phase_cycles[21], (unsigned long long)(clock64() - t_begin));
+        atomicAdd(&prism_tc_phase_cycles[22], (unsigned long long)nmaps);
+    }
+#endif
     // after an expired wait: let the copies still in flight land before the block exits
     if (tid == 0 && abort_s)
         for (int k = 0; k < issued; ++k)
@@ -1094,6 +1125,8 @@ __global__ void __launch_bounds__(128) fixup_kernel(const void *__restrict__ sta
     int seg = (int)(((long long)c * P) / NC);
     while (seg + 1 < P && ((long long)(seg + 1) * NC) / P <= c) ++seg;
     while (seg > 0 && ((long long)seg * NC) / P > c) --seg;
+    grid_dependency_wait();  // the stash of the segment kernel and S_start of the combine
+    allow_dependent_launch();
     if (seg == 0) return;
     const size_t chunk = (size_t)bh * NC + c;
     const int t0 = c * 64, n = min(64, T - t0);
@@ -1310,17 +1343,39 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
     p.P = w.P;
     p.wait_ns = wait_ns > 0 ? (unsigned long long)wait_ns : 100000000ull;
     cudaStream_t st = tm.stream;
+    // programmatic stream serialization: each kernel's blocks may be scheduled while the previous
+    // kernel drains; the kernels wait (griddepcontrol.wait) before touching memory it produces
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     tm.begin("tc_segment");
-    segment_kernel<<<s.BH * w.P, NT, SMEM_BYTES, st>>>(mq, mk, mv, mu, p);
+    cfg.gridDim = dim3(s.BH * w.P);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, segment_kernel, mq, mk, mv, mu, p);
     tm.end();
+    if (e != cudaSuccess) return e;
     if (w.P > 1) {
         tm.begin("tc_combine");
-        combine_kernel<<<dim3(s.BH, 64 / CB_ROWS), CB_THREADS, CB_SMEM, st>>>(w.zsum, w.sstart, w.P, d_status, p.wait_ns);
+        cfg.gridDim = dim3(s.BH, 64 / CB_ROWS);
+        cfg.blockDim = dim3(CB_THREADS);
+        cfg.dynamicSmemBytes = CB_SMEM;
+        e = cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)w.zsum, w.sstart, (int)w.P, d_status,
+                               (unsigned long long)p.wait_ns);
         tm.end();
+        if (e != cudaSuccess) return e;
         tm.begin("tc_fixup");
-        fixup_kernel<<<dim3(s.NC, s.BH), 128, 0, st>>>(w.stash_o, w.stash_q, w.sstart, a.out, p.out_f32, s.T, s.NC,
-                                                        w.P);
+        cfg.gridDim = dim3(s.NC, s.BH);
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, fixup_kernel, (const void *)w.stash_o, (const __half *)w.stash_q,
+                               (const __half *)w.sstart, a.out, (int)p.out_f32, (int)s.T, (int)s.NC, (int)w.P);
         tm.end();
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

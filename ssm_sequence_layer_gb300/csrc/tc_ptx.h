@@ -120,6 +120,14 @@ __device__ __forceinline__ void u2f(const uint32_t (&r)[N], float (&v)[N])
     for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// ---- programmatic dependent launch ---------------------------------------------------------------
+// wait until the grids this one depends on (earlier kernels in the stream) have completed and their
+// memory is visible; a no-op when the kernel was launched without programmatic serialization
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// let the next kernel in the stream (if launched with programmatic serialization) start launching
+// its blocks; it still waits in grid_dependency_wait() for this grid to complete
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---- mbarriers --------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count)
 {
