@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_3d(sbase + (stage ? OFF_V1 : OFF_V0), &tm_v, mb_v[stage], 0, c * C - 8, bh);
         pending |= 4u << stage;
     };
-    // collective bounded wait on an mbarrier phase; on expiry the CTA records the timeout
+    // collective bounded wait on two mbarrier phases; on expiry the CTA records the timeout
     // status and leaves the chunk loop (the phase is kept so the drain can wait for it)
     // (thread 0 polls; the rest of the CTA waits at the barrier, issuing nothing)
     auto wait_two = [&](uint32_t mb0, uint32_t &ph0, uint32_t bit0, uint32_t mb1, uint32_t &ph1, uint32_t bit1) -> bool {
@@ -339,18 +339,17 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         return abort_s == 0;
     };
-    auto wait_all = [&](uint32_t mb, uint32_t &phase, uint32_t bit) -> bool {
-        if (tid == 0) {
-            if (mbar_wait(mb, phase, p.wait_ns)) {
-                phase ^= 1u;
-                pending &= ~bit;
-            } else {
-                abort_s = 1;
-                set_status(p.status, kDevTimeout);
-            }
+    // every thread waits for the MMA barrier itself, so no CTA barrier follows; an expired wait
+    // is recorded and the CTA leaves the chunk loop at its next barrier (thread 0 keeps the MMA
+    // pending for the drain)
+    auto wait_mma = [&]() {
+        if (mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
+            ph_mma ^= 1u;
+            if (tid == 0) pending &= ~1u;
+        } else {
+            abort_s = 1;
+            set_status(p.status, kDevTimeout);
         }
-        __syncthreads();
-        return abort_s == 0;
     };
 
     if (tid == 0 && c_begin < c_end) {
@@ -469,7 +468,6 @@ __global__ void __launch_bounds__(NT, 1)
             // the Gram is waited for here, before this warp joins the prep: measured faster
             // than letting it run under the prep (the prep slows the tensor core's operand reads)
             if (mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
-                ph_mma ^= 1u;
                 pending &= ~1u;
             } else {
                 abort_s = 1;
@@ -528,6 +526,7 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         PHASE_MARK(14);
         if (abort_s) break;
+        ph_mma ^= 1u;  // every thread's copy of the MMA barrier phase (thread 0 waited for it)
         fence_after_sync();
 
         PHASE_MARK(2);
@@ -718,7 +717,6 @@ __global__ void __launch_bounds__(NT, 1)
         } else {
             if (tid == 0) {
                 if (mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
-                    ph_mma ^= 1u;
                     pending &= ~1u;
                 } else {
                     abort_s = 1;
@@ -754,6 +752,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_before_sync();
         __syncthreads();
         if (abort_s) break;
+        ph_mma ^= 1u;  // MX completed (thread 0 waited for it)
 
         PHASE_MARK(5);
         // ---- P4: [U'^T ; W^T] = [RHS | BGK]^T T^T -------------------------------------------------
@@ -768,7 +767,7 @@ __global__ void __launch_bounds__(NT, 1)
             mma_commit(mb_mma);
             pending |= 1u;
         }
-        if (!wait_all(mb_mma, ph_mma, 1u)) break;
+        wait_mma();
         fence_after_sync();
 
         PHASE_MARK(6);
@@ -784,6 +783,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
+        if (abort_s) break;
 
         PHASE_MARK(7);
         // ---- P5: [D5 | D4] = UWs [K | G^T] + sum_l [Xs_l^T; 0] [U_l | PQ_l^T]  (N = 128) ----------
@@ -808,10 +808,10 @@ __global__ void __launch_bounds__(NT, 1)
             fill_scalars(sc + ((c + 1) & 1) * SC_SET);
             if (c + 2 < c_end) load_gates(c + 2);
         }
-        if (!wait_all(mb_mma, ph_mma, 1u)) break;
+        wait_mma();
         fence_after_sync();
 
-        if (tid == 0 && c + 1 < c_end) {  // K and U of this chunk are no longer read: reload them now
+        if (tid == 0 && c + 1 < c_end && abort_s == 0) {  // K and U of this chunk are no longer read: reload them now
             mbar_add_tx(mb_qku, (1 + R) * TILE);
             tma_load_3d(sbase + OFF_K, &tm_k, mb_qku, 0, (c + 1) * C, bh);
             for (int l = 0; l < R; ++l) tma_load_4d(sbase + OFF_U + l * TILE, &tm_u, mb_qku, 0, l, (c + 1) * C, bh);
@@ -843,6 +843,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
+        if (abort_s) break;
         if (tid == 0) {
             fence_after_sync();
             if (c + 1 < c_end) {  // Q of this chunk is no longer read: its reload completes the phase
@@ -858,7 +859,7 @@ __global__ void __launch_bounds__(NT, 1)
             mma_commit(mb_mma);
             pending |= 1u;
         }
-        if (!wait_all(mb_mma, ph_mma, 1u)) break;
+        wait_mma();
         fence_after_sync();
 
         PHASE_MARK(9);
