@@ -81,9 +81,8 @@ constexpr uint32_t VBYTES = 72 * 128;
 constexpr uint32_t OFF_V1 = OFF_V0 + 10240;
 constexpr uint32_t OFF_E = OFF_V1 + 10240;        // [PK0|PQ0^T|PK1|PQ1^T|PK2|PQ2^T|G^T]; later Qt, Mc
 constexpr uint32_t OFF_G = OFF_E + 6 * TILE;
-constexpr uint32_t OFF_AKK = OFF_E + 7 * TILE;    // A (fp32, stride 68); later RHS|BGK; later UWs
-constexpr uint32_t LDA = 68;    // row stride (floats) of T32 (float4 rows)
-constexpr uint32_t LDAA = 65;   // row stride (floats) of A (conflict-free column writes)
+constexpr uint32_t OFF_AKK = OFF_E + 7 * TILE;    // A (fp32, row stride LDA); later UWs
+constexpr uint32_t LDA = 68;    // row stride (floats) of A and T32 (float4 rows, conflict-free fragments)
 constexpr uint32_t OFF_T32 = OFF_AKK + 64 * LDA * 4;
 constexpr uint32_t OFF_TB = OFF_T32 + 64 * LDA * 4;  // T (bf16 tile)
 constexpr uint32_t OFF_XS = OFF_TB + TILE;            // Xs0..Xs2
@@ -561,10 +560,18 @@ __global__ void __launch_bounds__(NT, 1)
                         for (int q = 0; q < CW; ++q) v[q] = (j0 + q >= r) ? v[q] : 0.f;
                         st_row(sm + (keyrow ? OFF_G : OFF_E + (2 * l + 1) * TILE), r, j0, v);
                     } else if (keyrow) {  // A_ij = beta_i rowf_i colf_j k_i.k_j (j < i), from k_j.k_i
-                        float *A = reinterpret_cast<float *>(sm + OFF_AKK);
+                        float4 *A4 = reinterpret_cast<float4 *>(sm + OFF_AKK + (r * LDA + j0) * 4);
+                        const float4 *cf4 = reinterpret_cast<const float4 *>(s_colf + j0);
+                        const float brf = br * rf;
 #pragma unroll
-                        for (int q = 0; q < CW; ++q)
-                            A[r * LDAA + j0 + q] = (j0 + q < r) ? v[q] * br * rf * s_colf[j0 + q] : 0.f;
+                        for (int g = 0; g < CW / 4; ++g) {
+                            const float4 cf = cf4[g];
+                            const int j = j0 + 4 * g;
+                            A4[g] = make_float4(j + 0 < r ? v[4 * g + 0] * brf * cf.x : 0.f,
+                                                j + 1 < r ? v[4 * g + 1] * brf * cf.y : 0.f,
+                                                j + 2 < r ? v[4 * g + 2] * brf * cf.z : 0.f,
+                                                j + 3 < r ? v[4 * g + 3] * brf * cf.w : 0.f);
+                        }
                     } else {  // PK_l^T, kept where i > j
 #pragma unroll
                         for (int q = 0; q < CW; ++q) v[q] = (j0 + q > r) ? v[q] : 0.f;
@@ -615,10 +622,10 @@ __global__ void __launch_bounds__(NT, 1)
                         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                         for (int j = 0; j + 1 < r; j += 2) {
-                            s0 = fmaf(A[(o + r) * LDAA + o + j], t[j], s0);
-                            s1 = fmaf(A[(o + r) * LDAA + o + j + 1], t[j + 1], s1);
+                            s0 = fmaf(A[(o + r) * LDA + o + j], t[j], s0);
+                            s1 = fmaf(A[(o + r) * LDA + o + j + 1], t[j + 1], s1);
                         }
-                        if (r & 1) s0 = fmaf(A[(o + r) * LDAA + o + r - 1], t[r - 1], s0);
+                        if (r & 1) s0 = fmaf(A[(o + r) * LDA + o + r - 1], t[r - 1], s0);
                         t[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -(s0 + s1));
                         T32[(o + r) * LDA + o + cc] = t[r];
                     }
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {                 // X = A[ri][cj] T[cj][cj] (cols 8 nt..)
                         uint32_t a[4], b0, b1;
-                        frag_a(fr, A, LDAA, ri, cj + 8 * ks, a);
+                        frag_a(fr, A, LDA, ri, cj + 8 * ks, a);
                         frag_b(fr, T32, LDA, cj + 8 * ks, cj + 8 * nt, b0, b1);
                         mma_tf32(x, a[0], a[1], a[2], a[3], b0, b1);
                     }
@@ -668,7 +675,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                         for (int mt = 0; mt < 2; ++mt) {
                             uint32_t a[4];
-                            frag_a(fr, A, LDAA, 32 + 16 * mt, 8 * ks, a);
+                            frag_a(fr, A, LDA, 32 + 16 * mt, 8 * ks, a);
                             mma_tf32(x[mt], a[0], a[1], a[2], a[3], b0, b1);
                         }
                     }
