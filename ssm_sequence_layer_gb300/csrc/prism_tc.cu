@@ -73,18 +73,19 @@ constexpr int CW = 64 / (NT / 128);  // columns of a 64-column TMEM block each t
 constexpr uint32_t TILE = 8192;  // 64 rows x 128 B
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_Q = 0;                    // Q tile, then K, U0..U2 (contiguous: [Q;K] and [K;U] operands)
-constexpr uint32_t OFF_K = OFF_Q + TILE;
-constexpr uint32_t OFF_U = OFF_K + TILE;
-constexpr uint32_t OFF_V0 = OFF_U + RMAX * TILE;  // two V stages, 72 rows x 128 B (8-row halo), unswizzled
+constexpr uint32_t OFF_V0 = 0;                   // two V stages, 72 rows x 128 B (8-row halo), unswizzled
 constexpr uint32_t VBYTES = 72 * 128;
 constexpr uint32_t OFF_V1 = OFF_V0 + 10240;
-constexpr uint32_t OFF_E = OFF_V1 + 10240;        // [PK0|PQ0^T|PK1|PQ1^T|PK2|PQ2^T|G^T]; later Qt, Mc
+constexpr uint32_t OFF_Q = OFF_V1 + 10240;        // Q tile, then K, U0..U2 (contiguous: [Q;K] and [K;U] operands;
+constexpr uint32_t OFF_K = OFF_Q + TILE;          // the tile below Q is the first atom of the Q^T copy)
+constexpr uint32_t OFF_U = OFF_K + TILE;
+constexpr uint32_t OFF_E = OFF_U + RMAX * TILE;   // [PK0|PQ0^T|PK1|PQ1^T|PK2|PQ2^T|G^T]; later Qt, Mc
 constexpr uint32_t OFF_G = OFF_E + 6 * TILE;
 constexpr uint32_t OFF_AKK = OFF_E + 7 * TILE;    // A (fp32, row stride LDA); later UWs
 constexpr uint32_t LDA = 68;    // row stride (floats) of A and T32 (float4 rows, conflict-free fragments)
 constexpr uint32_t OFF_T32 = OFF_AKK + 64 * LDA * 4;
-constexpr uint32_t OFF_TB = OFF_T32 + 64 * LDA * 4;  // T (bf16 tile)
+constexpr uint32_t OFF_TB = OFF_T32 + 64 * LDA * 4;  // bf16 identity (written once): B of the Q^T copy
+constexpr uint32_t OFF_TF = OFF_E + 2 * TILE;        // T (fp16), over PK_1^T (free once MX completed)
 constexpr uint32_t OFF_XS = OFF_TB + TILE;            // Xs0..Xs2
 constexpr uint32_t OFF_ZERO = OFF_XS + RMAX * TILE;   // zero tile
 constexpr uint32_t OFF_ZA = OFF_ZERO + TILE;          // Z (128 rows, bf16, K-major)
@@ -95,7 +96,8 @@ constexpr uint32_t XTMP_FLOATS = 4 * 256;                     // solve scratch: 
 constexpr uint32_t SC_FLOATS = 2 * SC_SET + XTMP_FLOATS;       // two chunks' sets + solve scratch
 constexpr uint32_t SMEM_BYTES = OFF_SC + SC_FLOATS * 4 + 1024;  // + alignment slack
 
-static_assert(OFF_AKK % 1024 == 0 && OFF_TB % 1024 == 0 && OFF_XS % 1024 == 0 && OFF_ZA % 1024 == 0 &&
+static_assert(OFF_Q % 1024 == 0 && OFF_Q >= TILE && OFF_E % 1024 == 0 && OFF_AKK % 1024 == 0 && OFF_TB % 1024 == 0 &&
+                  OFF_XS % 1024 == 0 && OFF_ZA % 1024 == 0 &&
                   OFF_BGK % 1024 == 0,
               "align");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -104,6 +106,7 @@ static_assert(4 * 128 <= XTMP_FLOATS && 4 * 256 <= XTMP_FLOATS, "solve scratch")
 
 // TMEM column map
 constexpr uint32_t TM_D1 = 0, TM_D2 = 256, TM_D3 = 320, TM_D5 = 384, TM_D4 = 448, TM_D7 = 0, TM_D6 = 64;
+constexpr uint32_t TM_QT = 128;  // Q^T (lanes 64..127), copied from P3 to E4 in the Gram's upper columns
 static_assert(TM_D4 == TM_D5 + 64 && TM_D6 == TM_D7 + 64, "D5|D4 and D7|D6 are written by one N = 128 MMA each");
 
 struct SegParams {
@@ -281,8 +284,14 @@ __global__ void __launch_bounds__(NT, 1)
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_u);
     }
-    // zero tile, and Z = [0; I] (segments >= 1) or 0 (segment 0)
+    // zero tile, bf16 identity, and Z = [0; I] (segments >= 1) or 0 (segment 0)
     for (int e = tid; e < (int)(TILE / 16); e += NT) reinterpret_cast<uint4 *>(sm + OFF_ZERO)[e] = make_uint4(0, 0, 0, 0);
+    {
+        const int i = tid >> 3, g = tid & 7;  // row i, 16-byte group g (8 columns)
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if ((i >> 3) == g) reinterpret_cast<__nv_bfloat16 *>(&w)[i & 7] = __float2bfloat16_rn(1.f);
+        *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128(i, 8 * g)) = w;
+    }
     for (int e = tid; e < 128 * 64; e += NT) {
         const int r = e >> 6, m = e & 63;
         const float z = (seg > 0 && r >= 64 && (r - 64) == m) ? 1.f : 0.f;
@@ -301,6 +310,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     uint32_t ph_mma = 0, ph_qku = 0, ph_v[2] = {0, 0};
     uint32_t pending = 0;  // issuer's view (thread 0): 1 MMA, 2 Q/K/U load, 4/8 V loads in flight
+    bool qku_unarmed = false;  // thread 0: the next chunk's Q load is in flight, its phase's arrival not yet made
     const uint32_t qku_bytes = (2 + R) * TILE;
 
     auto issue_qku = [&](int c) {
@@ -599,6 +609,14 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int s = 0; s < 4; ++s)
                     mma_f16(tmem + TM_D2, dsc(dbase, OFF_E + l * 2 * TILE + s * 2048, TILE, 1024),
                              dsc(dbase, OFF_XS + l * TILE + s * 2048, TILE, 1024), id, (l | s) != 0);
+            // [Y; Q^T] I -> Q^T in lanes 64..127 (exact: bf16 times one), so that E4 needs no Q
+            // tile and Q's buffer can take the next chunk's tile right after this.  The first
+            // atom Y is the tile below Q (V data); lanes 0..63 of these columns are never read.
+            const uint32_t idq = idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + TM_QT, dsc(dbase, OFF_Q - TILE + s * 2048, TILE, 1024),
+                        dsc(dbase, OFF_TB + s * 32, 16, 1024), idq, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
         }
@@ -704,6 +722,10 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                     for (int mt = 0; mt < 2; ++mt) frag_c_store(fr, T32, LDA, 32 + 16 * mt, n0, y[mt], -1.f);
                 }
+                if (tid == 64 && !mbar_wait(mb_mma, ph_mma, p.wait_ns)) {  // MX has read PK_1^T (T's slot)
+                    abort_s = 1;
+                    set_status(p.status, kDevTimeout);
+                }
                 named_bar(1, NT / 2);
                 for (int e = stid; e < 64 * 8; e += NT / 2) {  // T (fp16, [i][j], zero above the diagonal)
                     const int i = e >> 3, g = e & 7;
@@ -718,13 +740,19 @@ __global__ void __launch_bounds__(NT, 1)
                     w.y = pack2(m[2], m[3]);
                     w.z = pack2(m[4], m[5]);
                     w.w = pack2(m[6], m[7]);
-                    *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128(i, 8 * g)) = w;
+                    *reinterpret_cast<uint4 *>(sm + OFF_TF + sw128(i, 8 * g)) = w;
                 }
             }
         } else {
             if (tid == 0) {
                 if (mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
                     pending &= ~1u;
+                    if (c + 1 < c_end) {  // Q was last read by the copy above: reload it now
+                        mbar_add_tx(mb_qku, TILE);
+                        tma_load_3d(sbase + OFF_Q, &tm_q, mb_qku, 0, (c + 1) * C, bh);
+                        pending |= 2u;
+                        qku_unarmed = true;
+                    }
                 } else {
                     abort_s = 1;
                     set_status(p.status, kDevTimeout);
@@ -769,7 +797,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_f16(tmem + TM_D3, dsc(dbase, OFF_E + s * 2048, OFF_BGK - OFF_E, 1024),
-                        dsc(dbase, OFF_TB + s * 32, 16, 1024),
+                        dsc(dbase, OFF_TF + s * 32, 16, 1024),
                          id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
@@ -818,8 +846,9 @@ __global__ void __launch_bounds__(NT, 1)
         wait_mma();
         fence_after_sync();
 
-        if (tid == 0 && c + 1 < c_end && abort_s == 0) {  // K and U of this chunk are no longer read: reload them now
-            mbar_add_tx(mb_qku, (1 + R) * TILE);
+        if (tid == 0 && c + 1 < c_end && abort_s == 0) {  // K and U of this chunk are no longer read: their
+            mbar_expect_tx(mb_qku, (1 + R) * TILE);             // reload completes the phase
+            qku_unarmed = false;
             tma_load_3d(sbase + OFF_K, &tm_k, mb_qku, 0, (c + 1) * C, bh);
             for (int l = 0; l < R; ++l) tma_load_4d(sbase + OFF_U + l * TILE, &tm_u, mb_qku, 0, l, (c + 1) * C, bh);
             pending |= 2u;
@@ -830,15 +859,16 @@ __global__ void __launch_bounds__(NT, 1)
             const int m = row - 64, j0 = sub * CW;
             float v[CW], v5[CW];
             {
-                uint32_t r4[CW], r5[CW];
+                uint32_t r4[CW], r5[CW], rq[CW];
                 tmem_ld_nowait(tmem + TM_D4 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, r4);
                 tmem_ld_nowait(tmem + TM_D5 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, r5);
+                tmem_ld_nowait(tmem + TM_QT + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, rq);
                 tmem_wait_ld();
                 u2f(r4, v);
                 u2f(r5, v5);
-            }
 #pragma unroll
-            for (int q = 0; q < CW; ++q) v[q] = s_gam[j0 + q] * ld_bf(sm + OFF_Q, j0 + q, m) - s_rowf[j0 + q] * v[q];
+                for (int q = 0; q < CW; ++q) v[q] = s_gam[j0 + q] * __uint_as_float(rq[q]) - s_rowf[j0 + q] * v[q];
+            }
             st_row(sm + OFF_E, m, j0, v);  // Qt [m][i]
 #pragma unroll
             for (int q = 0; q < CW; ++q) v[q] = v5[q];
@@ -853,10 +883,6 @@ __global__ void __launch_bounds__(NT, 1)
         if (abort_s) break;
         if (tid == 0) {
             fence_after_sync();
-            if (c + 1 < c_end) {  // Q of this chunk is no longer read: its reload completes the phase
-                mbar_expect_tx(mb_qku, TILE);
-                tma_load_3d(sbase + OFF_Q, &tm_q, mb_qku, 0, (c + 1) * C, bh);
-            }
             // ---- P6: [D7 | D6] = Z [Qt | Mc]  (N = 128) ------------------------------------------
             const uint32_t id = idesc_f16(128, 128, 0, 1);
 #pragma unroll
@@ -971,6 +997,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid == 0 && pending) {
         const uint64_t drain_ns = 1000000000ull;
         if (pending & 1u) (void)mbar_wait(mb_mma, ph_mma, drain_ns);
+        if (qku_unarmed) mbar_arrive(mb_qku);  // the phase's arrival, so that it completes when Q lands
         if (pending & 2u) (void)mbar_wait(mb_qku, ph_qku, drain_ns);
         if (pending & 4u) (void)mbar_wait(mb_v[0], ph_v[0], drain_ns);
         if (pending & 8u) (void)mbar_wait(mb_v[1], ph_v[1], drain_ns);

@@ -139,6 +139,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes)
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
 }
 
+// plain arrival (one count) on the barrier's current phase
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+
 // Adds `bytes` to the barrier's expected transaction count without arriving (a later
 // arrive.expect_tx completes the phase's arrival).
 __device__ __forceinline__ void mbar_add_tx(uint32_t mbar, uint32_t bytes)
