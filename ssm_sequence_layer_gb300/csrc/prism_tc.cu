@@ -325,22 +325,13 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_3d(sbase + (stage ? OFF_V1 : OFF_V0), &tm_v, mb_v[stage], 0, c * C - 8, bh);
         pending |= 4u << stage;
     };
-    // collective bounded wait on two mbarrier phases; on expiry the CTA records the timeout
-    // status and leaves the chunk loop (the phase is kept so the drain can wait for it)
-    // (thread 0 polls; the rest of the CTA waits at the barrier, issuing nothing)
-    auto wait_two = [&](uint32_t mb0, uint32_t &ph0, uint32_t bit0, uint32_t mb1, uint32_t &ph1, uint32_t bit1) -> bool {
+    // collective bounded wait on one mbarrier phase (thread 0 polls, then a CTA barrier)
+    auto wait_one = [&](uint32_t mb, uint32_t &phase, uint32_t bit) -> bool {
         if (tid == 0) {
-            const bool ok0 = mbar_wait(mb0, ph0, p.wait_ns);
-            const bool ok1 = ok0 && mbar_wait(mb1, ph1, p.wait_ns);
-            if (ok0) {
-                ph0 ^= 1u;
-                pending &= ~bit0;
-            }
-            if (ok1) {
-                ph1 ^= 1u;
-                pending &= ~bit1;
-            }
-            if (!ok1) {
+            if (mbar_wait(mb, phase, p.wait_ns)) {
+                phase ^= 1u;
+                pending &= ~bit;
+            } else {
                 abort_s = 1;
                 set_status(p.status, kDevTimeout);
             }
@@ -429,6 +420,45 @@ __global__ void __launch_bounds__(NT, 1)
         }
     };
 
+    // prep of chunk cc (P1): anchor, gain and residual chain -> Xs tiles, two channels x 4 tokens
+    // per thread, from the V stage stg and the chunk's per-token scalars.  It runs in the
+    // previous chunk's tail, while that chunk's last MMAs are in flight.
+    auto prep = [&](int cc, int stg) {
+        const float *pset = sc + (cc & 1) * SC_SET;
+        const float *p_colf = pset + 192, *p_gc = pset + 384, *p_eta = pset + 384 + 64 * RMAX;
+        const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stg ? OFF_V1 : OFF_V0));
+        const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
+        constexpr int TPT = 64 / (NT / 32);     // tokens per thread
+#pragma unroll
+        for (int k = 0; k < TPT; ++k) {
+            const int i = tg + (NT / 32) * k;
+            const float2 v0 = __bfloat1622float2(vb[(i + 8) * 32 + cp]);
+            const float2 v1 = __bfloat1622float2(vb[(i + 7) * 32 + cp]);
+            const float2 v2 = __bfloat1622float2(vb[(i + 6) * 32 + cp]);
+            const float2 v3 = __bfloat1622float2(vb[(i + 5) * 32 + cp]);
+            const float cf = p_colf[i];
+            float gcl[RMAX], etl[RMAX];
+#pragma unroll
+            for (int l = 0; l < RMAX; ++l) {
+                gcl[l] = p_gc[i * RMAX + l] * cf;
+                etl[l] = p_eta[i * RMAX + l];
+            }
+            const float a0 = fmaf(w0.x, v0.x, fmaf(w1.x, v1.x, fmaf(w2.x, v2.x, w3.x * v3.x)));
+            const float a1 = fmaf(w0.y, v0.y, fmaf(w1.y, v1.y, fmaf(w2.y, v2.y, w3.y * v3.y)));
+            float g0, g1, Phi0, Phi1;
+            gelu_gain(a0, g0, Phi0);
+            gelu_gain(a1, g1, Phi1);
+            float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
+            uint8_t *xs = sm + OFF_XS + sw128(i, 2 * cp);
+#pragma unroll
+            for (int l = 0; l < RMAX; ++l) {
+                if (l < R) *reinterpret_cast<uint32_t *>(xs + l * TILE) = pack2(gcl[l] * g0 * r0, gcl[l] * g1 * r1);
+                r0 *= 1.f - etl[l] * g0;
+                r1 *= 1.f - etl[l] * g1;
+            }
+        }
+    };
+
 #ifdef PRISM_PHASE_TIMERS
     // per-phase totals in shared memory (registers would crowd the kernel's own)
     __shared__ unsigned long long ph_acc_s[kPhaseSlots];
@@ -447,10 +477,12 @@ __global__ void __launch_bounds__(NT, 1)
         float *const s_beta = set, *const s_lam = set + 64, *const s_rowf = set + 128, *const s_colf = set + 192;
         float *const s_gam = set + 256, *const s_bg = set + 320, *const s_gc = set + 384;
         float *const s_eta = s_gc + 64 * RMAX;
-        if (c == c_begin) {  // the first chunk's scalars; later ones are filled during the previous chunk
+        if (c == c_begin) {  // the first chunk's scalars and prep; later ones run in the previous chunk
             fill_scalars(set);
             if (c + 1 < c_end) load_gates(c + 1);
-            __syncthreads();
+            if (!wait_one(mb_v[stage], ph_v[stage], 4u << stage)) break;
+            prep(c, stage);
+            fence_async_smem();
         }
         const float lc = s_lam[63];
 
@@ -458,7 +490,7 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- P2: Gram tiles  D1 = [K; U_0] [Q; K]^T,  D1' = [U_1; U_2] [Q; K]^T ------------------
         // (rows are key/direction tokens j, columns query/key tokens i: the score tiles come out
         // transposed, [j][i], which is the operand form the later products read)
-        if (!wait_two(mb_qku, ph_qku, 2u, mb_v[stage], ph_v[stage], 4u << stage)) break;
+        if (!wait_one(mb_qku, ph_qku, 2u)) break;
         if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
         if (tid == 0) {  // the input tiles are still bf16 here (exact values); the Gram runs on them
             fence_after_sync();
@@ -474,8 +506,6 @@ __global__ void __launch_bounds__(NT, 1)
                             dsc(dbase, OFF_Q + s * 32, 16, 1024), id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
-            // the Gram is waited for here, before this warp joins the prep: measured faster
-            // than letting it run under the prep (the prep slows the tensor core's operand reads)
             if (mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
                 pending &= ~1u;
             } else {
@@ -485,40 +515,6 @@ __global__ void __launch_bounds__(NT, 1)
         }
 
         PHASE_MARK(1);
-        // ---- P1: prep -> Xs tiles (two channels x 8 tokens per thread) --------------------------
-        {
-            const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stage ? OFF_V1 : OFF_V0));
-            const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
-            constexpr int TPT = 64 / (NT / 32);     // tokens per thread
-#pragma unroll
-            for (int k = 0; k < TPT; ++k) {
-                const int i = tg + (NT / 32) * k;
-                const float2 v0 = __bfloat1622float2(vb[(i + 8) * 32 + cp]);
-                const float2 v1 = __bfloat1622float2(vb[(i + 7) * 32 + cp]);
-                const float2 v2 = __bfloat1622float2(vb[(i + 6) * 32 + cp]);
-                const float2 v3 = __bfloat1622float2(vb[(i + 5) * 32 + cp]);
-                const float cf = s_colf[i];
-                float gcl[RMAX], etl[RMAX];
-#pragma unroll
-                for (int l = 0; l < RMAX; ++l) {
-                    gcl[l] = s_gc[i * RMAX + l] * cf;
-                    etl[l] = s_eta[i * RMAX + l];
-                }
-                const float a0 = fmaf(w0.x, v0.x, fmaf(w1.x, v1.x, fmaf(w2.x, v2.x, w3.x * v3.x)));
-                const float a1 = fmaf(w0.y, v0.y, fmaf(w1.y, v1.y, fmaf(w2.y, v2.y, w3.y * v3.y)));
-                float g0, g1, Phi0, Phi1;
-                gelu_gain(a0, g0, Phi0);
-                gelu_gain(a1, g1, Phi1);
-                float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
-                uint8_t *xs = sm + OFF_XS + sw128(i, 2 * cp);
-#pragma unroll
-                for (int l = 0; l < RMAX; ++l) {
-                    if (l < R) *reinterpret_cast<uint32_t *>(xs + l * TILE) = pack2(gcl[l] * g0 * r0, gcl[l] * g1 * r1);
-                    r0 *= 1.f - etl[l] * g0;
-                    r1 *= 1.f - etl[l] * g1;
-                }
-            }
-        }
         {  // diag(beta Gamma) K, one 16-byte group of 8 per thread (K still bf16)
             const int j = tid >> 3, m0 = (tid & 7) * 8;
             uint4 w = *reinterpret_cast<const uint4 *>(sm + OFF_K + sw128(j, m0));
@@ -533,7 +529,6 @@ __global__ void __launch_bounds__(NT, 1)
         }
         fence_async_smem();
         __syncthreads();
-        PHASE_MARK(14);
         if (abort_s) break;
         ph_mma ^= 1u;  // every thread's copy of the MMA barrier phase (thread 0 waited for it)
         fence_after_sync();
@@ -877,6 +872,15 @@ __global__ void __launch_bounds__(NT, 1)
             for (int q = 0; q < CW; ++q) v[q] = ((j0 + q) == m ? gC : 0.f) - v[q];
             st_row(sm + OFF_E + TILE, m, j0, v);  // Mc [m][m']
         }
+        if (tid == 0 && c + 1 < c_end) {  // the next chunk's V (issued at this chunk's start) for its prep
+            if (mbar_wait(mb_v[stage ^ 1], ph_v[stage ^ 1], p.wait_ns)) {
+                ph_v[stage ^ 1] ^= 1u;
+                pending &= ~(4u << (stage ^ 1));
+            } else {
+                abort_s = 1;
+                set_status(p.status, kDevTimeout);
+            }
+        }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -892,6 +896,11 @@ __global__ void __launch_bounds__(NT, 1)
             mma_commit(mb_mma);
             pending |= 1u;
         }
+        if (c + 1 < c_end) {  // the next chunk's prep while MMA6 runs (Xs of this chunk is dead)
+            prep(c + 1, stage ^ 1);
+            fence_async_smem();
+        }
+        PHASE_MARK(14);
         wait_mma();
         fence_after_sync();
 
