@@ -475,8 +475,7 @@ __global__ void __launch_bounds__(NT, 1)
 
         float *const set = sc + (c & 1) * SC_SET;
         float *const s_beta = set, *const s_lam = set + 64, *const s_rowf = set + 128, *const s_colf = set + 192;
-        float *const s_gam = set + 256, *const s_bg = set + 320, *const s_gc = set + 384;
-        float *const s_eta = s_gc + 64 * RMAX;
+        float *const s_gam = set + 256, *const s_bg = set + 320;  // (gamma, eta at 384.. are the prep's)
         if (c == c_begin) {  // the first chunk's scalars and prep; later ones run in the previous chunk
             fill_scalars(set);
             if (c + 1 < c_end) load_gates(c + 1);
@@ -1067,7 +1066,7 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
     int issued = min(nmaps, CB_STAGES);
 #ifdef PRISM_PHASE_TIMERS
     const bool trace = tid == 0 && blockIdx.x == 0 && blockIdx.y == 0;
-    unsigned long long t_wait = 0;
+    unsigned long long t_wait = 0, t_comp = 0, t_barb = 0;
     const long long t_begin = clock64();
 #endif
     for (int k = 0; k < nmaps; ++k) {
@@ -1089,6 +1088,9 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
             issue(issued++);
         }
         const float *M = ring + (size_t)st * CB_STAGE_FLOATS;
+#ifdef PRISM_PHASE_TIMERS
+        const long long tc0 = clock64();
+#endif
         float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
         for (int m = 16 * kq; m < 16 * kq + 16; m += 4) {
@@ -1109,7 +1111,16 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
 #pragma unroll
         for (int r = 0; r < 4; ++r)
             *reinterpret_cast<float2 *>(&part[kq][4 * rg + r][c2]) = make_float2(acc[r][0], acc[r][1]);
+#ifdef PRISM_PHASE_TIMERS
+        const long long tc1 = clock64();
+#endif
         __syncthreads();
+#ifdef PRISM_PHASE_TIMERS
+        if (trace) {
+            t_comp += tc1 - tc0;
+            t_barb += clock64() - tc1;
+        }
+#endif
         float2 o = *reinterpret_cast<const float2 *>(M + 64 * 64 + rr * 64 + c2);  // N_p
 #pragma unroll
         for (int q = 0; q < CB_KQ; ++q) {
@@ -1125,7 +1136,8 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
     if (trace) {  // combine tracing: block (0, 0), thread 0: map waits and the whole chain
         atomicAdd(&prism_tc_phase_cycles[20], t_wait);
         atomicAdd(&prism_tc_phase_cycles[21], (unsigned long long)(clock64() - t_begin));
-        atomicAdd(&prism_tc_phase_cycles[22], (unsigned long long)nmaps);
+        atomicAdd(&prism_tc_phase_cycles[22], t_comp);
+        atomicAdd(&prism_tc_phase_cycles[23], t_barb);
     }
 #endif
     // after an expired wait: let the copies still in flight land before the block exits
