@@ -151,6 +151,22 @@ def test_segment_count_invariance(oracle_mod, segments):
     assert rel_err(out, ref) <= TOL["bf16"]
 
 
+def test_bf16_output_with_segments_matches_fp32_output():
+    """Several segments: the per-chunk o0 stash is fp16 when the output is bf16, so the bf16
+    output differs from the fp32 output by that rounding and the final one only."""
+    inp = make_inputs(1, 2, 1300, 64, 64, 3, dtype="bf16", seed=32)
+    d = to_device(inp)
+    with B.Plan.for_inputs(d, out="f32", path=2, segments=5) as p32, B.Plan.for_inputs(d, path=2, segments=5) as p16:
+        o32 = p32.forward(d)
+        o16 = p16.forward(d)
+        torch.cuda.synchronize()
+    a16 = o16.float().cpu().numpy().astype(np.float64)
+    a32 = o32.cpu().numpy().astype(np.float64)
+    rms = np.sqrt(np.mean(a32 * a32))
+    # bf16 rounding (2^-9 relative) plus the fp16 stash (2^-11 relative to o0)
+    assert np.max(np.abs(a16 - a32) / (np.abs(a32) + rms)) <= 4e-3
+
+
 @pytest.mark.parametrize("path,segments", [(1, None), (2, 1)])
 def test_bf16_output_is_the_rounded_fp32_output(path, segments):
     """bf16 output = the fp32 result rounded to bf16, bit for bit: the computation is the same
