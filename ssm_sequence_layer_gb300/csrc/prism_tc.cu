@@ -308,6 +308,9 @@ __global__ void __launch_bounds__(NT, 1)
     grid_dependency_wait();
     allow_dependent_launch();
 
+    // the inputs stream through once: let their L2 lines go first, so that the per-chunk stash
+    // (read back by the fix-up) stays in L2
+    const uint64_t l2ef = l2_evict_first_policy();
     uint32_t ph_mma = 0, ph_qku = 0, ph_v[2] = {0, 0};
     uint32_t pending = 0;  // issuer's view (thread 0): 1 MMA, 2 Q/K/U load, 4/8 V loads in flight
     bool qku_unarmed = false;  // thread 0: the next chunk's Q load is in flight, its phase's arrival not yet made
@@ -315,14 +318,14 @@ __global__ void __launch_bounds__(NT, 1)
 
     auto issue_qku = [&](int c) {
         mbar_expect_tx(mb_qku, qku_bytes);
-        tma_load_3d(sbase + OFF_Q, &tm_q, mb_qku, 0, c * C, bh);
-        tma_load_3d(sbase + OFF_K, &tm_k, mb_qku, 0, c * C, bh);
-        for (int l = 0; l < R; ++l) tma_load_4d(sbase + OFF_U + l * TILE, &tm_u, mb_qku, 0, l, c * C, bh);
+        tma_load_3d_hint(sbase + OFF_Q, &tm_q, mb_qku, 0, c * C, bh, l2ef);
+        tma_load_3d_hint(sbase + OFF_K, &tm_k, mb_qku, 0, c * C, bh, l2ef);
+        for (int l = 0; l < R; ++l) tma_load_4d_hint(sbase + OFF_U + l * TILE, &tm_u, mb_qku, 0, l, c * C, bh, l2ef);
         pending |= 2u;
     };
     auto issue_v = [&](int c, int stage) {
         mbar_expect_tx(mb_v[stage], VBYTES);
-        tma_load_3d(sbase + (stage ? OFF_V1 : OFF_V0), &tm_v, mb_v[stage], 0, c * C - 8, bh);
+        tma_load_3d_hint(sbase + (stage ? OFF_V1 : OFF_V0), &tm_v, mb_v[stage], 0, c * C - 8, bh, l2ef);
         pending |= 4u << stage;
     };
     // collective bounded wait on one mbarrier phase (thread 0 polls, then a CTA barrier)
@@ -743,7 +746,7 @@ __global__ void __launch_bounds__(NT, 1)
                     pending &= ~1u;
                     if (c + 1 < c_end) {  // Q was last read by the copy above: reload it now
                         mbar_add_tx(mb_qku, TILE);
-                        tma_load_3d(sbase + OFF_Q, &tm_q, mb_qku, 0, (c + 1) * C, bh);
+                        tma_load_3d_hint(sbase + OFF_Q, &tm_q, mb_qku, 0, (c + 1) * C, bh, l2ef);
                         pending |= 2u;
                         qku_unarmed = true;
                     }
@@ -843,8 +846,8 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 0 && c + 1 < c_end && abort_s == 0) {  // K and U of this chunk are no longer read: their
             mbar_expect_tx(mb_qku, (1 + R) * TILE);             // reload completes the phase
             qku_unarmed = false;
-            tma_load_3d(sbase + OFF_K, &tm_k, mb_qku, 0, (c + 1) * C, bh);
-            for (int l = 0; l < R; ++l) tma_load_4d(sbase + OFF_U + l * TILE, &tm_u, mb_qku, 0, l, (c + 1) * C, bh);
+            tma_load_3d_hint(sbase + OFF_K, &tm_k, mb_qku, 0, (c + 1) * C, bh, l2ef);
+            for (int l = 0; l < R; ++l) tma_load_4d_hint(sbase + OFF_U + l * TILE, &tm_u, mb_qku, 0, l, (c + 1) * C, bh, l2ef);
             pending |= 2u;
         }
         PHASE_MARK(8);
