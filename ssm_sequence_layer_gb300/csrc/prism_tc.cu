@@ -359,11 +359,8 @@ __global__ void __launch_bounds__(NT, 1)
         issue_v(c_begin, 0);
         issue_qku(c_begin);
     }
+    // this thread's two conv channels (re-read from L1 by every prep: no registers held across the loop)
     const __nv_bfloat162 *cw2 = reinterpret_cast<const __nv_bfloat162 *>(p.conv_w) + (size_t)h * 4 * (D / 2) + (tid & 31);
-    const float2 w0 = __bfloat1622float2(cw2[0 * (D / 2)]);
-    const float2 w1 = __bfloat1622float2(cw2[1 * (D / 2)]);
-    const float2 w2 = __bfloat1622float2(cw2[2 * (D / 2)]);
-    const float2 w3 = __bfloat1622float2(cw2[3 * (D / 2)]);
 
     // gates of one chunk: lane l of warp 1 holds beta/alpha of tokens 2l, 2l+1; thread
     // 256 + s (s < 192) holds gamma/eta slot s.  Warp 0 (thread 0 issues the MMAs) is left out,
@@ -427,6 +424,10 @@ __global__ void __launch_bounds__(NT, 1)
     // per thread, from the V stage stg and the chunk's per-token scalars.  It runs in the
     // previous chunk's tail, while that chunk's last MMAs are in flight.
     auto prep = [&](int cc, int stg) {
+        const float2 w0 = __bfloat1622float2(cw2[0 * (D / 2)]);
+        const float2 w1 = __bfloat1622float2(cw2[1 * (D / 2)]);
+        const float2 w2 = __bfloat1622float2(cw2[2 * (D / 2)]);
+        const float2 w3 = __bfloat1622float2(cw2[3 * (D / 2)]);
         const float *pset = sc + (cc & 1) * SC_SET;
         const float *p_colf = pset + 192, *p_gc = pset + 384, *p_eta = pset + 384 + 64 * RMAX;
         const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stg ? OFF_V1 : OFF_V0));
