@@ -143,6 +143,18 @@ def test_tensor_core_path_matches_portable_path(T, L):
     assert rel_err(tc, pt) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("B_,H,T,L,segments", [(1, 1, 1, 1, None), (1, 3, 17, 2, None), (2, 1, 63, 3, None),
+                                               (1, 1, 65, 4, 2), (3, 1, 129, 4, 3), (1, 2, 192, 2, 5)])
+def test_tensor_core_path_short_and_ragged_sequences(oracle_mod, B_, H, T, L, segments):
+    """The tensor-core path on sequences shorter than a chunk, ragged tails and more segments
+    than one CTA per chunk would give, against the oracle."""
+    inp = make_inputs(B_, H, T, 64, 64, L, dtype="bf16", seed=40 + T + L)
+    ref = oracle_forward(oracle_mod, inp)["out"]
+    kw = {} if segments is None else dict(segments=segments)
+    out = gpu_forward(inp, path=2, **kw)
+    assert rel_err(out, ref) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("segments", [1, 2, 3, 7, 16])
 def test_segment_count_invariance(oracle_mod, segments):
     inp = make_inputs(1, 2, 1000, 64, 64, 4, dtype="bf16", seed=30)
