@@ -22,7 +22,7 @@
 //   Xs_l  = colf_j x_{j,l}                             (x = gamma g (.) r, the prep)
 //   RHS   = diag(beta) V - diag(beta rowf) sum_l PK_l Xs_l
 //   [U'^T; W^T] = [RHS | diag(beta Gamma) K]^T T^T
-//   UWs   = [U'^T; W^T] diag(colf)
+//   UWs   = [U'^T; W^T] diag(colf) = [RHS | diag(beta Gamma) K]^T (diag(colf) T)^T   (one MMA)
 //   D4    = (UWs G^T + [Xs^T; 0] PQ^T) diag(rowf) = [O_loc^T ; (G~ W)^T]   (G~ = Q K^T o D)
 //   D5    = UWs K + [Xs^T; 0] U         = [N_c ; W^T K']
 //   Qt    = Q~^T = diag(Gamma) Q^T - (G~ W)^T,   M_c = Gamma_C I - W^T K'
@@ -725,14 +725,17 @@ __global__ void __launch_bounds__(NT, 1)
                     set_status(p.status, kDevTimeout);
                 }
                 named_bar(1, NT / 2);
-                for (int e = stid; e < 64 * 8; e += NT / 2) {  // T (fp16, [i][j], zero above the diagonal)
+                // T is stored as diag(colf) T (row i scaled by colf_i = e^{lc - lambda_i}), so that
+                // MMA3 yields [U'^T; W^T] diag(colf) = UWs directly
+                for (int e = stid; e < 64 * 8; e += NT / 2) {  // (fp16, [i][j], zero above the diagonal)
                     const int i = e >> 3, g = e & 7;
+                    const float cfi = s_colf[i];
                     const float4 lo = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g);
                     const float4 hi = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g + 4);
                     const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
                     float m[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) m[q] = (8 * g + q <= i) ? v[q] : 0.f;
+                    for (int q = 0; q < 8; ++q) m[q] = (8 * g + q <= i) ? v[q] * cfi : 0.f;
                     uint4 w;
                     w.x = pack2(m[0], m[1]);
                     w.y = pack2(m[2], m[3]);
@@ -804,13 +807,11 @@ __global__ void __launch_bounds__(NT, 1)
         fence_after_sync();
 
         PHASE_MARK(6);
-        // ---- E3: UWs = [U'^T; W^T] diag(e^{lc - lambda_j}) ---------------------------------------
+        // ---- E3: UWs = [U'^T; W^T] diag(e^{lc - lambda_j}) (the scaling rode on T) -> fp16 --------
         {
             const int j0 = sub * CW;
             float v[CW];
             tmem_ld(tmem + TM_D3 + ((uint32_t)(quad * 32) << 16) + (uint32_t)j0, v);
-#pragma unroll
-            for (int q = 0; q < CW; ++q) v[q] *= s_colf[j0 + q];
             st_row(sm + OFF_AKK, row, j0, v);  // over A (the solve is complete)
         }
         fence_async_smem();
