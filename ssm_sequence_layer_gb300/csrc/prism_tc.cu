@@ -237,6 +237,50 @@ __device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes,
     }
 }
 
+// prep of one chunk (P1): anchor, gain and residual chain -> Xs tiles, two channels x 4 tokens per
+// thread, from V stage `stg` and the chunk's per-token scalars `pset`.  Kept out of line: the
+// segment kernel calls it at two places, and one copy of its code keeps the loop body smaller.
+__device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __nv_bfloat162 *cw2, int stg, int R)
+{
+    const int tid = threadIdx.x;
+    const float2 w0 = __bfloat1622float2(cw2[0 * (D / 2)]);
+    const float2 w1 = __bfloat1622float2(cw2[1 * (D / 2)]);
+    const float2 w2 = __bfloat1622float2(cw2[2 * (D / 2)]);
+    const float2 w3 = __bfloat1622float2(cw2[3 * (D / 2)]);
+    const float *p_colf = pset + 192, *p_gc = pset + 384, *p_eta = pset + 384 + 64 * RMAX;
+    const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stg ? OFF_V1 : OFF_V0));
+    const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
+    constexpr int TPT = 64 / (NT / 32);     // tokens per thread
+#pragma unroll
+    for (int k = 0; k < TPT; ++k) {
+        const int i = tg + (NT / 32) * k;
+        const float2 v0 = __bfloat1622float2(vb[(i + 8) * 32 + cp]);
+        const float2 v1 = __bfloat1622float2(vb[(i + 7) * 32 + cp]);
+        const float2 v2 = __bfloat1622float2(vb[(i + 6) * 32 + cp]);
+        const float2 v3 = __bfloat1622float2(vb[(i + 5) * 32 + cp]);
+        const float cf = p_colf[i];
+        float gcl[RMAX], etl[RMAX];
+#pragma unroll
+        for (int l = 0; l < RMAX; ++l) {
+            gcl[l] = p_gc[i * RMAX + l] * cf;
+            etl[l] = p_eta[i * RMAX + l];
+        }
+        const float a0 = fmaf(w0.x, v0.x, fmaf(w1.x, v1.x, fmaf(w2.x, v2.x, w3.x * v3.x)));
+        const float a1 = fmaf(w0.y, v0.y, fmaf(w1.y, v1.y, fmaf(w2.y, v2.y, w3.y * v3.y)));
+        float g0, g1, Phi0, Phi1;
+        gelu_gain(a0, g0, Phi0);
+        gelu_gain(a1, g1, Phi1);
+        float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
+        uint8_t *xs = sm + OFF_XS + sw128(i, 2 * cp);
+#pragma unroll
+        for (int l = 0; l < RMAX; ++l) {
+            if (l < R) *reinterpret_cast<uint32_t *>(xs + l * TILE) = pack2(gcl[l] * g0 * r0, gcl[l] * g1 * r1);
+            r0 *= 1.f - etl[l] * g0;
+            r1 *= 1.f - etl[l] * g1;
+        }
+    }
+}
+
 // barrier over `n` threads (whole warps) of the CTA; ids 1.. (0 is __syncthreads')
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
@@ -423,45 +467,7 @@ __global__ void __launch_bounds__(NT, 1)
     // prep of chunk cc (P1): anchor, gain and residual chain -> Xs tiles, two channels x 4 tokens
     // per thread, from the V stage stg and the chunk's per-token scalars.  It runs in the
     // previous chunk's tail, while that chunk's last MMAs are in flight.
-    auto prep = [&](int cc, int stg) {
-        const float2 w0 = __bfloat1622float2(cw2[0 * (D / 2)]);
-        const float2 w1 = __bfloat1622float2(cw2[1 * (D / 2)]);
-        const float2 w2 = __bfloat1622float2(cw2[2 * (D / 2)]);
-        const float2 w3 = __bfloat1622float2(cw2[3 * (D / 2)]);
-        const float *pset = sc + (cc & 1) * SC_SET;
-        const float *p_colf = pset + 192, *p_gc = pset + 384, *p_eta = pset + 384 + 64 * RMAX;
-        const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stg ? OFF_V1 : OFF_V0));
-        const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
-        constexpr int TPT = 64 / (NT / 32);     // tokens per thread
-#pragma unroll
-        for (int k = 0; k < TPT; ++k) {
-            const int i = tg + (NT / 32) * k;
-            const float2 v0 = __bfloat1622float2(vb[(i + 8) * 32 + cp]);
-            const float2 v1 = __bfloat1622float2(vb[(i + 7) * 32 + cp]);
-            const float2 v2 = __bfloat1622float2(vb[(i + 6) * 32 + cp]);
-            const float2 v3 = __bfloat1622float2(vb[(i + 5) * 32 + cp]);
-            const float cf = p_colf[i];
-            float gcl[RMAX], etl[RMAX];
-#pragma unroll
-            for (int l = 0; l < RMAX; ++l) {
-                gcl[l] = p_gc[i * RMAX + l] * cf;
-                etl[l] = p_eta[i * RMAX + l];
-            }
-            const float a0 = fmaf(w0.x, v0.x, fmaf(w1.x, v1.x, fmaf(w2.x, v2.x, w3.x * v3.x)));
-            const float a1 = fmaf(w0.y, v0.y, fmaf(w1.y, v1.y, fmaf(w2.y, v2.y, w3.y * v3.y)));
-            float g0, g1, Phi0, Phi1;
-            gelu_gain(a0, g0, Phi0);
-            gelu_gain(a1, g1, Phi1);
-            float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
-            uint8_t *xs = sm + OFF_XS + sw128(i, 2 * cp);
-#pragma unroll
-            for (int l = 0; l < RMAX; ++l) {
-                if (l < R) *reinterpret_cast<uint32_t *>(xs + l * TILE) = pack2(gcl[l] * g0 * r0, gcl[l] * g1 * r1);
-                r0 *= 1.f - etl[l] * g0;
-                r1 *= 1.f - etl[l] * g1;
-            }
-        }
-    };
+    auto prep = [&](int cc, int stg) { prep_chunk(sm, sc + (cc & 1) * SC_SET, cw2, stg, R); };
 
 #ifdef PRISM_PHASE_TIMERS
     // per-phase totals in shared memory (registers would crowd the kernel's own)
