@@ -12,7 +12,8 @@
  * Simulation"; the Tencent article at youzy.cn, part 03 "PRISM" items
  * two to four):
  *
- *   anchor    h_t = sum_{j=0..3} w_j (.) v_{t-j}        (zero before t = 0)
+ *   anchor    h_t = sum_{j=0..3} w_j (.) v_{t-j}        (v_{t-j} for t - j < 0 from
+ *             the optional history v_hist, else zero)
  *             The short causal convolution over v is the input-local proxy
  *             that stands in for S_{t-1} k_t (notes, section 2.3).
  *   gain      g_t = GELU'(h_t) = Phi(h_t) + h_t phi(h_t)  (exact erf GELU)
@@ -40,6 +41,11 @@
  *   X_out   [B,H,T,R,dv]  injection factors x_{t,l} = gamma_{t,l} g_t (.) r_{t,l}
  *   h_out, g_out, e_out [B,H,T,dv]  anchor, gain and residual
  *   S_init  [B,H,dv,dk]   optional initial state (NULL means S_0 = 0)
+ *   v_hist  [B,H,3,dv]    optional left context of the convolution: slot j holds
+ *                         v_{j-3} (oldest first), the last three tokens before this
+ *                         call's first one (NULL means zeros).  With S_init it lets
+ *                         a sequence be evaluated in consecutive calls: the result
+ *                         equals one call over the whole sequence.
  *
  * Build: gcc -O2 -fno-fast-math -shared -fPIC prism_oracle.c -lm -lpthread
  */
@@ -51,7 +57,7 @@
 
 typedef struct {
     int B, H, T, dk, dv, L;
-    const double *q, *k, *v, *beta, *alpha, *u, *gamma, *eta, *conv_w, *S_init;
+    const double *q, *k, *v, *beta, *alpha, *u, *gamma, *eta, *conv_w, *v_hist, *S_init;
     double *out, *S_final, *X_out, *h_out, *g_out, *e_out;
     int nthreads;
     int thread_id;
@@ -71,6 +77,7 @@ static void run_head(const oracle_args *a, int b, int h)
     const double *gamma = R > 0 ? a->gamma + bh * T * R : NULL;
     const double *eta = R > 0 ? a->eta + bh * T * R : NULL;
     const double *w = a->conv_w + (size_t)h * 4 * dv;
+    const double *vh = a->v_hist ? a->v_hist + bh * 3 * dv : NULL;
     double *out = a->out + bh * T * dv;
 
     double *S = calloc((size_t)dv * dk, sizeof(double));
@@ -95,6 +102,7 @@ static void run_head(const oracle_args *a, int b, int h)
             double acc = 0.0;
             for (int j = 0; j < 4; ++j)
                 if (t - j >= 0) acc += w[j * dv + c] * v[(size_t)(t - j) * dv + c];
+                else if (vh) acc += w[j * dv + c] * vh[(size_t)(3 + t - j) * dv + c];
             anchor[c] = acc;
             double Phi = 0.5 * (1.0 + erf(acc * inv_sqrt2));
             double phi = exp(-0.5 * acc * acc) * inv_sqrt2pi;
@@ -158,7 +166,7 @@ int prism_oracle_forward_f64(int B, int H, int T, int dk, int dv, int L,
                              const double *q, const double *k, const double *v,
                              const double *beta, const double *alpha,
                              const double *u, const double *gamma, const double *eta,
-                             const double *conv_w, const double *S_init,
+                             const double *conv_w, const double *v_hist, const double *S_init,
                              double *out, double *S_final, double *X_out,
                              double *h_out, double *g_out, double *e_out, int nthreads)
 {
@@ -170,7 +178,7 @@ int prism_oracle_forward_f64(int B, int H, int T, int dk, int dv, int L,
     if (nthreads < 1) nthreads = 1;
     if (nthreads > units) nthreads = units;
 
-    oracle_args base = {B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, conv_w, S_init,
+    oracle_args base = {B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, conv_w, v_hist, S_init,
                         out, S_final, X_out, h_out, g_out, e_out, nthreads, 0};
     if (nthreads == 1) {
         worker(&base);

@@ -43,7 +43,7 @@ def _open(path):
     lib = ctypes.CDLL(path)
     dp = ctypes.POINTER(ctypes.c_double)
     lib.prism_oracle_forward_f64.restype = ctypes.c_int
-    lib.prism_oracle_forward_f64.argtypes = [ctypes.c_int] * 6 + [dp] * 10 + [dp] * 6 + [ctypes.c_int]
+    lib.prism_oracle_forward_f64.argtypes = [ctypes.c_int] * 6 + [dp] * 11 + [dp] * 6 + [ctypes.c_int]
     return lib
 
 
@@ -69,14 +69,16 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def forward(q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None,
+def forward(q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None, v_hist=None,
             want_state=False, want_x=False, want_hge=False, nthreads=None):
-    """Run the oracle.  Arrays follow the layouts in ``prism_oracle.c``.
+    """Run the oracle.  Arrays follow the layouts in ``prism_oracle.c``; ``S_init``
+    [B,H,dv,dk] and ``v_hist`` [B,H,3,dv] (v_{-3}, v_{-2}, v_{-1}) carry a sequence over
+    from a previous call.
 
     Returns a dict with ``out`` [B,H,T,dv] and, on request, ``S_final``
     [B,H,dv,dk], ``X`` [B,H,T,R,dv] and ``h``/``g``/``e`` [B,H,T,dv], all fp64.
     """
-    return _forward(_load(), q, k, v, beta, alpha, u, gamma, eta, conv_w, L, S_init=S_init,
+    return _forward(_load(), q, k, v, beta, alpha, u, gamma, eta, conv_w, L, S_init=S_init, v_hist=v_hist,
                     want_state=want_state, want_x=want_x, want_hge=want_hge, nthreads=nthreads)
 
 
@@ -91,7 +93,7 @@ class OracleLib:
         return _forward(self._lib, *args, **kw)
 
 
-def _forward(lib, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None,
+def _forward(lib, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None, v_hist=None,
              want_state=False, want_x=False, want_hge=False, nthreads=None):
     q, k, v = _f64(q), _f64(k), _f64(v)
     beta, alpha, conv_w = _f64(beta), _f64(alpha), _f64(conv_w)
@@ -108,6 +110,9 @@ def _forward(lib, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None
     S_init = _f64(S_init)
     if S_init is not None:
         assert S_init.shape == (B, H, dv, dk)
+    v_hist = _f64(v_hist)
+    if v_hist is not None:
+        assert v_hist.shape == (B, H, 3, dv)
     out = np.zeros((B, H, T, dv))
     S_final = np.zeros((B, H, dv, dk)) if want_state else None
     X = np.zeros((B, H, T, max(R, 0), dv)) if (want_x and R > 0) else None
@@ -118,7 +123,7 @@ def _forward(lib, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None
         nthreads = len(os.sched_getaffinity(0))
     rc = lib.prism_oracle_forward_f64(
         B, H, T, dk, dv, L, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(u),
-        _ptr(gamma), _ptr(eta), _ptr(conv_w), _ptr(S_init), _ptr(out), _ptr(S_final), _ptr(X),
+        _ptr(gamma), _ptr(eta), _ptr(conv_w), _ptr(v_hist), _ptr(S_init), _ptr(out), _ptr(S_final), _ptr(X),
         _ptr(hh), _ptr(gg), _ptr(ee), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")

@@ -34,6 +34,9 @@ MUTATIONS = [
     ("chain sign", "r[i] *= (1.0 - et * g[i]);", "r[i] *= (1.0 + et * g[i]);"),
     ("chain without gain", "double x = gm * g[i] * r[i];", "double x = gm * r[i];"),
     ("direction slot shifted", "ul = u + ((size_t)t * R + (l - 1)) * dk;", "ul = u + ((size_t)t * R + (R - l)) * dk;"),
+    ("history in reverse order", "vh[(size_t)(3 + t - j) * dv + c]", "vh[(size_t)(j - t - 1) * dv + c]"),
+    ("history ignored", "else if (vh) acc +=", "else if (0) acc +="),
+    ("initial state ignored", "    if (a->S_init)\n", "    if (0)\n"),
     ("readout dropped", "        /* readout from the post-update state */",
      "        /* readout from the post-update state */\n        if (0)"),
 ]
@@ -53,6 +56,8 @@ def _pin_suite(mod):
         ("recall", lambda: pins.test_exact_recall_with_orthonormal_keys(mod)),
         ("linattn", lambda: pins.test_no_forget_no_delta_is_causal_linear_attention(mod)),
         ("zeroconv", lambda: pins.test_zero_conv_gives_half_gain(mod)),
+        ("inert", lambda: pins.test_history_equals_prepended_inert_tokens(mod)),
+        ("split", lambda: pins.test_split_calls_with_history_and_state(mod, (2, 3, 29))),
     ]
     for name, fn in cases:
         try:

@@ -261,6 +261,63 @@ def test_split_call_with_initial_state(oracle_mod):
     np.testing.assert_allclose(b["out"], full["out"][:, :, t0:], rtol=1e-12, atol=1e-13)
 
 
+def _cut(inp, sl):
+    return {kk: (vv[:, :, sl] if isinstance(vv, np.ndarray) and kk != "conv_w" else vv) for kk, vv in inp.items()}
+
+
+def _history(v_part, prev=None):
+    """The three tokens before the next call: v_{-3..-1} from the tokens seen so far (zeros
+    before the sequence start)."""
+    B, H, _, dv = v_part.shape
+    prev = np.zeros((B, H, 3, dv)) if prev is None else prev
+    return np.concatenate([prev, v_part], axis=2)[:, :, -3:]
+
+
+def test_history_equals_prepended_inert_tokens(oracle_mod):
+    """v_hist holds v_{-3}, v_{-2}, v_{-1}: a run with it (and an initial state) equals a run on
+    the sequence with those three tokens prepended as inert tokens -- alpha = 1 and beta =
+    gamma = 0 leave S unchanged whatever their q, k and u -- from the same initial state."""
+    inp = f64_inputs(B=1, H=2, T=12, dk=5, dv=4, L=3, seed=16)
+    rng = np.random.default_rng(16)
+    hist = rng.standard_normal((1, 2, 3, 4))
+    S0 = rng.standard_normal((1, 2, 4, 5)) * 0.3
+    res = run(oracle_mod, inp, S_init=S0, v_hist=hist, want_state=True)
+    pre = {}
+    for kk, vv in inp.items():
+        if not isinstance(vv, np.ndarray) or kk == "conv_w":
+            pre[kk] = vv
+            continue
+        filler = rng.standard_normal(vv.shape[:2] + (3,) + vv.shape[3:])
+        if kk == "v":
+            filler = hist
+        elif kk == "alpha":
+            filler = np.ones_like(filler)
+        elif kk in ("beta", "gamma"):
+            filler = np.zeros_like(filler)
+        pre[kk] = np.concatenate([filler, vv], axis=2)
+    ref = run(oracle_mod, pre, S_init=S0, want_state=True)
+    np.testing.assert_allclose(res["out"], ref["out"][:, :, 3:], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(res["S_final"], ref["S_final"], rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("cuts", [(17,), (1, 2, 5), (2, 3, 29)])
+def test_split_calls_with_history_and_state(oracle_mod, cuts):
+    """With a non-zero convolution, consecutive calls that carry S_final into S_init and the
+    last three tokens into v_hist reproduce one call over the whole sequence, including calls
+    shorter than the convolution window."""
+    inp = f64_inputs(B=1, H=2, T=30, dk=5, dv=4, L=3, seed=17)
+    assert np.abs(inp["conv_w"]).min() > 0
+    full = run(oracle_mod, inp, want_state=True)
+    S, hist, outs, t = None, None, [], 0
+    for t1 in list(cuts) + [30]:
+        part = _cut(inp, slice(t, t1))
+        r = run(oracle_mod, part, S_init=S, v_hist=hist, want_state=True)
+        outs.append(r["out"])
+        S, hist, t = r["S_final"], _history(part["v"], hist), t1
+    np.testing.assert_allclose(np.concatenate(outs, axis=2), full["out"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(S, full["S_final"], rtol=1e-12, atol=1e-13)
+
+
 def test_state_stays_bounded_long_memory(oracle_mod):
     """beta in (0,1), ||k|| = 1, alpha < 1: the transition is a contraction, so
     ||S_t|| <= max_t ||B_t|| / (1 - max alpha) (notes, section 2.2 stability remark)."""
