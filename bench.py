@@ -45,7 +45,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="seqrec_16k")
+    ap.add_argument("--workload", default=None, help="default seqrec_16k (forward) or decode_lm130m (decode)")
+    ap.add_argument("--mode", choices=["forward", "decode"], default="forward",
+                    help="forward: prism_forward over whole sequences (the headline); decode: one "
+                         "prism_decode_step (one token per sequence) over a serving batch")
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 portable fp32 kernels, 2 tensor-core path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -397,13 +400,193 @@ def run_ours(args, w):
     return 0
 
 
+# ------------------------------------------------------------------------------------------------
+DECODE_METRIC = "PRISM decode step tokens/s (one token per sequence, all heads) + % of HBM roofline"
+TOKEN_KEYS = ("q", "k", "v", "beta", "alpha", "u", "gamma", "eta")
+
+
+def decode_alg_bytes(w):
+    """Bytes one decode step must move: the fp32 state read and written once per (sequence,
+    head), the token's inputs, the convolution history read and written, the output, and the
+    convolution weights once."""
+    io = 2 if w.dtype == "bf16" else 4
+    per_head = (2 * w.dv * w.dk * 4 + io * (2 * w.dk + w.dv + w.R * w.dk) + 4 * (2 + 2 * w.R)
+                + 2 * 3 * w.dv * io + w.dv * io)
+    return w.B * w.H * per_head + w.H * 4 * w.dv * io
+
+
+def decode_inputs(w, seed=0):
+    import torch
+    from ssm_sequence_layer_gb300.inputs import make_inputs
+    inp = make_inputs(w.B, w.H, 1, w.dk, w.dv, w.L, dtype=w.dtype, seed=seed)
+    tok = {k: (v[:, :, 0].contiguous() if k in TOKEN_KEYS else v) for k, v in inp.items()}
+    g = torch.Generator().manual_seed(seed + 1)
+    S = torch.randn(w.B, w.H, w.dv, w.dk, generator=g) * 0.3
+    hist = torch.randn(w.B, w.H, 3, w.dv, generator=g).to(tok["v"].dtype)
+    return inp, tok, S, hist
+
+
+def decode_oracle_sample(w, inp, S, hist, seconds_target, nthreads, reps=None):
+    """The oracle's step (T = 1 from S_init and v_hist) over all B*H heads, repeated for about
+    `seconds_target` seconds (or `reps` times).  Returns (tokens/s, repetitions, seconds)."""
+    from oracle import prism_oracle
+    a = {k: (v.double().numpy() if hasattr(v, "double") else v) for k, v in inp.items()}
+    S64, h64 = S.double().numpy(), hist.double().numpy()
+
+    def once():
+        prism_oracle.forward(a["q"], a["k"], a["v"], a["beta"], a["alpha"], a["u"], a["gamma"], a["eta"],
+                             a["conv_w"], a["L"], S_init=S64, v_hist=h64, want_state=True, nthreads=nthreads)
+
+    if reps is None:
+        t0 = time.perf_counter()
+        once()
+        dt1 = time.perf_counter() - t0
+        reps = max(1, int(seconds_target / max(dt1, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        once()
+    dt = time.perf_counter() - t0
+    return w.B * reps / dt, reps, dt
+
+
+def run_decode(args, w):
+    import torch
+
+    from ssm_sequence_layer_gb300 import binding as Bd
+    from ssm_sequence_layer_gb300 import build as cuda_build
+
+    world, rank, local = dist_setup(args)
+    if rank == 0:
+        cuda_build.build()
+    barrier(world)
+    steps, warm = args.steps, max(args.warmup, 3)
+    inp_cpu, tok_cpu, S_cpu, hist_cpu = decode_inputs(w)
+    tok = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in tok_cpu.items()}
+    S, hist = S_cpu.cuda(), hist_cpu.cuda()
+    out = torch.empty(w.B, w.H, w.dv, dtype=tok["v"].dtype, device="cuda")
+    stream = torch.cuda.current_stream()
+    plan = Bd.Plan(w.B, w.H, 1, w.dk, w.dv, w.L, io=w.dtype)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for _ in range(warm):
+        flush.zero_()
+        plan.decode_step(tok, hist, S, out, stream)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):  # one kernel per step: the step events time the decode kernel itself
+        flush.zero_()
+        ev[i][0].record(stream)
+        plan.decode_step(tok, hist, S, out, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    plan.last_device_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_local = sum(step_ms) / steps
+    ms = max_over_ranks(ms_local, world)
+    value = w.B * world / (ms / 1e3)
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    alg = decode_alg_bytes(w)
+    achieved = alg / (ms_local / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": traffic_from_profiles("decode", w.name),
+                "alg_bytes_per_launch": alg, "kernel_ms": ms_local, "peak_source": f"{peak_kind} hbm_gbs"}
+
+    e2e = None
+    if not args.no_e2e:  # the token's inputs from pinned host memory, the output back; the state stays resident
+        host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in tok_cpu.items()}
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for k, v in host.items() if torch.is_tensor(v) and k != "conv_w"
+                  and (w.L > 1 or k not in ("u", "gamma", "eta")))
+        dtok = {k: (torch.empty_like(v, device="cuda") if torch.is_tensor(v) else v) for k, v in host.items()}
+        e2e_ms = []
+        for i in range(max(3, min(steps, 20)) + 2):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k, v in host.items():
+                if torch.is_tensor(v) and k != "conv_w":
+                    dtok[k].copy_(v, non_blocking=True)
+            plan.decode_step(dtok, hist, S, out, stream)
+            hout.copy_(out, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                e2e_ms.append(a.elapsed_time(b))
+        e2e_ms_mean = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+        e2e = {"value": w.B * world / (e2e_ms_mean / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": hout.numel() * hout.element_size(), "ms_per_step": e2e_ms_mean}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = max(1, min(len(os.sched_getaffinity(0)), w.B * w.H))
+        v, reps, dt = decode_oracle_sample(w, inp_cpu, S_cpu, hist_cpu, args.cpu_seconds, nthreads)
+        cpu = {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+               "sample": f"fp64 oracle, one token for all {w.B * w.H} (sequence, head) pairs, {reps} times ({dt:.1f} s)"}
+    plan.close()
+    if rank == 0:
+        line = {
+            "metric": DECODE_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "dk", "dv", "L")},
+                       "io": w.dtype, "state": "fp32, resident", "l2": "flushed by a 512 MiB write before every timed step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": steps, "clocks": clocks,
+            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
-    from ssm_sequence_layer_gb300.inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    from ssm_sequence_layer_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
+    if args.mode == "decode":
+        w = DECODE_WORKLOADS[args.workload or "decode_lm130m"]
+        if args.impl == "reference":
+            return run_decode_reference(args, w)
+        return run_decode(args, w)
+    w = WORKLOADS[args.workload or "seqrec_16k"]
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
+
+
+def run_decode_reference(args, w):
+    """The oracle as the reference arm of the decode step: each step is the oracle's step over
+    all (sequence, head) pairs on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    inp, _, S, hist = decode_inputs(w)
+    nthreads = max(1, min(len(os.sched_getaffinity(0)), w.B * w.H))
+    if args.warmup > 0:
+        decode_oracle_sample(w, inp, S, hist, 0.0, nthreads, reps=args.warmup)
+    _, _, dt = decode_oracle_sample(w, inp, S, hist, 0.0, nthreads, reps=args.steps)
+    value = w.B * args.steps / dt
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "dk", "dv", "L")}, "io": w.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                         "sample": f"oracle step over all {w.B * w.H} (sequence, head) pairs"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 if __name__ == "__main__":

@@ -128,6 +128,54 @@ PRISM_API prism_status prism_forward_host(prism_plan_t plan, const void *q, cons
                                 const float *gamma, const float *eta, const void *conv_w, int L,
                                 void *out, struct CUstream_st *stream);
 
+/*
+ * prism_forward_state -- prism_forward for one part of a sequence that is evaluated over
+ * consecutive calls (a prefill in pieces, streaming input, a prefill followed by
+ * prism_decode_step).  The recurrence above starts from S_0 = S_init, and the anchor's window
+ * reaches back into the previous call: for t - j < 0, v_{t-j} comes from v_hist.  A sequence
+ * split into calls this way gives the outputs and final state of one call over the whole
+ * sequence, up to floating-point rounding.  (The state is the recurrent state of the layer's
+ * RNN form, notes on PRISM, section 2.2; the window is the causal four-tap anchor of
+ * section 2.3.)
+ *
+ * Arguments after conv_w (device pointers, each may be NULL, each 16-byte aligned):
+ *   v_hist      [B,H,3,dv]  io dtype  v_{-3}, v_{-2}, v_{-1}, oldest first; NULL = zeros
+ *   S_init      [B,H,dv,dk] float32   the state before the first token; NULL = zero state
+ *   S_final     [B,H,dv,dk] float32   receives the state after the last token; may be S_init
+ *   v_hist_out  [B,H,3,dv]  io dtype  receives the last three tokens of [v_hist; v], the next
+ *                                      call's v_hist; may be v_hist
+ * Apart from those two pairs, no buffer may overlap another.  The state is carried in fp32;
+ * on the tensor-core path the part of the outputs that S_init contributes goes through fp16
+ * operands, like the state at every segment boundary.  Otherwise as prism_forward.
+ */
+PRISM_API prism_status prism_forward_state(prism_plan_t plan, const void *q, const void *k, const void *v,
+                                 const float *beta, const float *alpha, const void *u,
+                                 const float *gamma, const float *eta, const void *conv_w, int L,
+                                 const void *v_hist, const float *S_init, void *out, float *S_final,
+                                 void *v_hist_out, struct CUstream_st *stream);
+
+/*
+ * prism_decode_step -- one token for each of the plan's B x H sequences: the recurrent form
+ * of the layer (notes on PRISM, section 2.2), for serving after a prefill.  It reads and
+ * updates the state and the convolution history in place and writes o = S q after the update.
+ *   q, k        [B,H,dk]     io dtype        v [B,H,dv]  io dtype     u [B,H,R,dk] io dtype
+ *   beta, alpha [B,H]        float32         gamma, eta [B,H,R] float32
+ *   conv_w      [H,4,dv]     io dtype
+ *   v_hist      [B,H,3,dv]   io dtype: v_{-3}, v_{-2}, v_{-1}; on return shifted by one
+ *                            token, with v as the newest
+ *   S           [B,H,dv,dk]  float32: the state; on return the state after the token
+ *   out         [B,H,dv]     the plan's output dtype
+ * The step equals prism_forward_state with T = 1, S_final = S_init = S and v_hist_out =
+ * v_hist.  The plan's T is not used, so the plan of a prefill can be reused.  Pointers are
+ * device pointers, 16-byte aligned (gates: 4 bytes), not overlapping.  L must equal the
+ * plan's L; with L = 1, u, gamma and eta are not read.  Returns once the step is enqueued
+ * on `stream`.
+ */
+PRISM_API prism_status prism_decode_step(prism_plan_t plan, const void *q, const void *k, const void *v,
+                               const float *beta, const float *alpha, const void *u,
+                               const float *gamma, const float *eta, const void *conv_w, int L,
+                               void *v_hist, float *S, void *out, struct CUstream_st *stream);
+
 /* Free the plan and its workspace.  NULL is accepted. */
 PRISM_API prism_status prism_plan_destroy(prism_plan_t plan);
 

@@ -2,8 +2,8 @@
 
 Argument marshalling only: every step of the forward runs in the CUDA library
 ``libprism_gb300.so``.  The functions keep the C names.  Tensors are passed as
-``torch.Tensor`` (device memory for ``prism_forward``, host memory for
-``prism_forward_host``) or as raw integer addresses.  There is no fallback: if
+``torch.Tensor`` (device memory for ``prism_forward``, ``prism_forward_state`` and
+``prism_decode_step``, host memory for ``prism_forward_host``) or as raw integer addresses.  There is no fallback: if
 the library is missing, the first call raises.
 """
 from __future__ import annotations
@@ -35,7 +35,7 @@ PRISM_OPT_OUT_DTYPE = 4
 EXPORTED = ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
             "prism_plan_destroy", "prism_workspace_bytes", "prism_plan_last_device_status",
             "prism_status_string", "prism_last_error_message", "prism_version", "prism_plan_kernel_times",
-            "prism_forward_noalloc")
+            "prism_forward_noalloc", "prism_forward_state", "prism_decode_step")
 
 
 class prism_kernel_time(ctypes.Structure):
@@ -83,9 +83,12 @@ def lib():
             L.prism_forward_noalloc.argtypes = [i] * 6 + [vp, vp, vp, f, f, vp, f, f, vp, vp, vp,
                                                           ctypes.POINTER(ctypes.c_int)]
             L.prism_forward_noalloc.restype = ctypes.c_int
+            L.prism_forward_state.argtypes = fwd[:11] + [vp, f, vp, f, vp, vp]
+            L.prism_decode_step.argtypes = fwd[:11] + [vp, f, vp, vp]
             L.prism_plan_kernel_times.restype = ctypes.c_int
             for name in ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
-                         "prism_plan_destroy", "prism_plan_last_device_status"):
+                         "prism_plan_destroy", "prism_plan_last_device_status", "prism_forward_state",
+                         "prism_decode_step"):
                 getattr(L, name).restype = ctypes.c_int
             _LIB = L
     return _LIB
@@ -168,6 +171,20 @@ def prism_forward_host(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, out
                                            _stream(stream)))
 
 
+def prism_forward_state(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, v_hist, S_init, out, S_final,
+                        v_hist_out, stream=None):
+    return _check(lib().prism_forward_state(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha),
+                                            _addr(u), _addr(gamma), _addr(eta), _addr(conv_w), int(L),
+                                            _addr(v_hist), _addr(S_init), _addr(out), _addr(S_final),
+                                            _addr(v_hist_out), _stream(stream)))
+
+
+def prism_decode_step(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, v_hist, S, out, stream=None):
+    return _check(lib().prism_decode_step(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha),
+                                          _addr(u), _addr(gamma), _addr(eta), _addr(conv_w), int(L),
+                                          _addr(v_hist), _addr(S), _addr(out), _stream(stream)))
+
+
 def prism_forward_noalloc(B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, conv_w, out, stream=None,
                           wait=True):
     """The allocation-free forward (see include/prism.h).  With wait=True the call waits for
@@ -224,6 +241,37 @@ class Plan:
         if out is None:
             out = torch.empty(inp["v"].shape, dtype=self._out_torch_dtype(), device=inp["v"].device)
         prism_forward(self.handle, *ts, out, stream)
+        return out
+
+    @staticmethod
+    def _check_device(ts, what):
+        for t in ts:
+            if t is not None and (not t.is_cuda or not t.is_contiguous()):
+                raise ValueError(f"{what} takes contiguous CUDA tensors")
+
+    def forward_state(self, inp, v_hist=None, S_init=None, S_final=None, v_hist_out=None, out=None, stream=None):
+        """One part of a sequence evaluated over consecutive calls (see prism_forward_state):
+        v_hist [B,H,3,dv] and S_init [B,H,dv,dk] (fp32) carry the sequence in, S_final and
+        v_hist_out carry it out (each may be None; S_final may be S_init, v_hist_out v_hist)."""
+        import torch
+        ts = self._tensors(inp)
+        self._check_device(ts[:-1] + (v_hist, S_init, S_final, v_hist_out), "prism_forward_state")
+        if out is None:
+            out = torch.empty(inp["v"].shape, dtype=self._out_torch_dtype(), device=inp["v"].device)
+        prism_forward_state(self.handle, *ts, v_hist, S_init, out, S_final, v_hist_out, stream)
+        return out
+
+    def decode_step(self, inp, v_hist, S, out=None, stream=None):
+        """One token per sequence (see prism_decode_step): q, k [B,H,dk], v [B,H,dv], u [B,H,R,dk],
+        beta, alpha [B,H], gamma, eta [B,H,R] (a T axis of length 1 is accepted too); v_hist and
+        S are updated in place."""
+        import torch
+        ts = self._tensors(inp)
+        self._check_device(ts[:-1] + (v_hist, S), "prism_decode_step")
+        if out is None:
+            B, H = self.shape[:2]
+            out = torch.empty((B, H, self.shape[4]), dtype=self._out_torch_dtype(), device=inp["v"].device)
+        prism_decode_step(self.handle, *ts, v_hist, S, out, stream)
         return out
 
     def _out_torch_dtype(self):

@@ -146,6 +146,36 @@ prism_status ensure_workspace(prism_plan_s *p, int path)
     return PRISM_OK;
 }
 
+prism_status check_plan_device(const prism_plan_s *p)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != p->device)
+        return fail(PRISM_ERR_INVALID_ARG, "current device %d differs from the plan's device %d", dev, p->device);
+    return PRISM_OK;
+}
+
+// The launch sequence of a validated forward on the plan's path.
+prism_status run_forward(prism_plan_s *p, const prism::ForwardArgs &a, struct CUstream_st *stream)
+{
+    prism_status st = check_plan_device(p);
+    if (st != PRISM_OK) return st;
+    const int path = resolve_path(p);
+    if (path == 2 && !prism::tc_supported(p->shape, p->io))
+        return fail(PRISM_ERR_UNSUPPORTED, "the tensor-core path takes bf16 io, dk = dv = 64 and L <= 4");
+    if ((st = ensure_workspace(p, path)) != PRISM_OK) return st;
+    p->timer.on = p->opt_timing != 0;
+    p->timer.reset((cudaStream_t)stream);
+    cudaError_t e;
+    if (path == 2)
+        e = prism::tc_forward(p->shape, a, p->out_dtype == PRISM_F32, p->tcw, p->d_status, p->opt_wait_ns, p->timer);
+    else
+        e = prism::simt_forward(p->shape, p->io, p->out_dtype, a, p->simt, p->d_status, p->timer);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return PRISM_OK;
+}
+
 }  // namespace
 
 void prism_set_error_message(const char *msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
@@ -259,22 +289,54 @@ prism_status prism_forward(prism_plan_t p, const void *q, const void *k, const v
 {
     prism_status st = check_forward_args(p, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, out);
     if (st != PRISM_OK) return st;
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev != p->device)
-        return fail(PRISM_ERR_INVALID_ARG, "current device %d differs from the plan's device %d", dev, p->device);
-    const int path = resolve_path(p);
-    if (path == 2 && !prism::tc_supported(p->shape, p->io))
-        return fail(PRISM_ERR_UNSUPPORTED, "the tensor-core path takes bf16 io, dk = dv = 64 and L <= 4");
-    if ((st = ensure_workspace(p, path)) != PRISM_OK) return st;
+    return run_forward(p, prism::ForwardArgs{q, k, v, u, conv_w, beta, alpha, gamma, eta, out}, stream);
+}
+
+prism_status prism_forward_state(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,
+                                 const float *alpha, const void *u, const float *gamma, const float *eta,
+                                 const void *conv_w, int L, const void *v_hist, const float *S_init, void *out,
+                                 float *S_final, void *v_hist_out, struct CUstream_st *stream)
+{
+    prism_status st = check_forward_args(p, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, out);
+    if (st != PRISM_OK) return st;
+    const void *sp[] = {v_hist, S_init, S_final, v_hist_out};
+    const char *sn[] = {"v_hist", "S_init", "S_final", "v_hist_out"};
+    for (int i = 0; i < 4; ++i)
+        if (sp[i] && !aligned(sp[i], 16)) return fail(PRISM_ERR_MISALIGNED, "%s is not 16-byte aligned", sn[i]);
     prism::ForwardArgs a{q, k, v, u, conv_w, beta, alpha, gamma, eta, out};
+    a.v_hist = v_hist;
+    a.S_init = S_init;
+    a.S_final = S_final;
+    a.v_hist_out = v_hist_out;
+    return run_forward(p, a, stream);
+}
+
+prism_status prism_decode_step(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,
+                               const float *alpha, const void *u, const float *gamma, const float *eta,
+                               const void *conv_w, int L, void *v_hist, float *S, void *out,
+                               struct CUstream_st *stream)
+{
+    if (!p) return fail(PRISM_ERR_INVALID_ARG, "plan is NULL");
+    if (L != p->shape.L) return fail(PRISM_ERR_INVALID_ARG, "L=%d differs from the plan's L=%d", L, p->shape.L);
+    if (!q || !k || !v || !beta || !alpha || !conv_w || !v_hist || !S || !out)
+        return fail(PRISM_ERR_INVALID_ARG, "q, k, v, beta, alpha, conv_w, v_hist, S and out must not be NULL");
+    const bool lvl = p->shape.R > 0;
+    if (lvl && (!u || !gamma || !eta))
+        return fail(PRISM_ERR_INVALID_ARG, "u, gamma and eta must not be NULL when L > 1");
+    const void *ap[] = {q, k, v, conv_w, v_hist, S, out, lvl ? u : nullptr};
+    const char *an[] = {"q", "k", "v", "conv_w", "v_hist", "S", "out", "u"};
+    for (int i = 0; i < 8; ++i)
+        if (ap[i] && !aligned(ap[i], 16)) return fail(PRISM_ERR_MISALIGNED, "%s is not 16-byte aligned", an[i]);
+    const void *fp[] = {beta, alpha, lvl ? gamma : nullptr, lvl ? eta : nullptr};
+    const char *fn[] = {"beta", "alpha", "gamma", "eta"};
+    for (int i = 0; i < 4; ++i)
+        if (fp[i] && !aligned(fp[i], 4)) return fail(PRISM_ERR_MISALIGNED, "%s is not 4-byte aligned", fn[i]);
+    prism_status st = check_plan_device(p);
+    if (st != PRISM_OK) return st;
+    prism::DecodeArgs a{q, k, v, u, conv_w, beta, alpha, gamma, eta, v_hist, S, out};
     p->timer.on = p->opt_timing != 0;
     p->timer.reset((cudaStream_t)stream);
-    if (path == 2)
-        e = prism::tc_forward(p->shape, a, p->out_dtype == PRISM_F32, p->tcw, p->d_status, p->opt_wait_ns, p->timer);
-    else
-        e = prism::simt_forward(p->shape, p->io, p->out_dtype, a, p->simt, p->d_status, p->timer);
+    const cudaError_t e = prism::decode_step(p->shape, p->io, p->out_dtype, a, p->timer);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return PRISM_OK;
 }

@@ -20,11 +20,18 @@ enum DeviceStatus : int {
     kDevTimeout = 2,  // a bounded wait expired
 };
 
-// Pointers of one forward call (device memory, layouts as in prism.h).
+// Pointers of one forward call (device memory, layouts as in prism.h).  The last four carry a
+// sequence across calls and may be null: v_hist [BH][3][dv] (v_{-3}, v_{-2}, v_{-1}, io dtype),
+// S_init / S_final [BH][dv][dk] fp32, v_hist_out [BH][3][dv] (the last three tokens of
+// [v_hist; v]).
 struct ForwardArgs {
     const void *q, *k, *v, *u, *conv_w;
     const float *beta, *alpha, *gamma, *eta;
     void *out;
+    const void *v_hist = nullptr;
+    const float *S_init = nullptr;
+    float *S_final = nullptr;
+    void *v_hist_out = nullptr;
 };
 
 // Problem shape shared by all kernels.
@@ -71,8 +78,8 @@ struct KernelTimer {
 struct TcWorkspace {
     float *zsum;             // [BH][P][128][64]  segment maps Z = [N; M]
     __half *sstart;          // [BH][P][64][64]   state entering each segment (fp16, fix-up operand)
-    void *stash_o;           // [BH][NC][64][64]  o0 per chunk (segments >= 1), fp32 or fp16
-    __half *stash_q;         // [BH][NC][64][64]  Qhat per chunk (segments >= 1)
+    void *stash_o;           // [BH][NC][64][64]  o0 per chunk (tracked segments), fp32 or fp16
+    __half *stash_q;         // [BH][NC][64][64]  Qhat per chunk (tracked segments)
     int P;                   // segments per sequence
 };
 
@@ -83,6 +90,20 @@ void tc_carve(const Shape &s, int P, void *base, TcWorkspace *w);
 cudaError_t tc_prepare();
 cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const TcWorkspace &w, int *d_status,
                        long long wait_ns, KernelTimer &tm);
+
+// v_hist_out = the last three tokens of [v_hist; v] (kernel in prism_state.cu); safe in place
+cudaError_t launch_history(const Shape &s, prism_dtype io, const void *v_hist, const void *v, void *v_hist_out,
+                           KernelTimer &tm);
+
+// One recurrent step for every (batch, head) (layouts as in prism.h, prism_decode_step).
+struct DecodeArgs {
+    const void *q, *k, *v, *u, *conv_w;
+    const float *beta, *alpha, *gamma, *eta;
+    void *v_hist;
+    float *S;
+    void *out;
+};
+cudaError_t decode_step(const Shape &s, prism_dtype io, prism_dtype out, const DecodeArgs &a, KernelTimer &tm);
 
 size_t simt_workspace_bytes(const Shape &s);
 void simt_carve(const Shape &s, void *base, SimtWorkspace *w);

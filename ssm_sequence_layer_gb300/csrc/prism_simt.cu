@@ -33,8 +33,11 @@ __device__ __forceinline__ void stf(__nv_bfloat16 *p, float x) { *p = __float2bf
 
 // ---------------------------------------------------------------------------------------------
 // Step a1: anchor, gain, residual and the closed-form residual chain -> X [BH][T][R][dv].
+// v_hist [BH][3][dv] (v_{-3}, v_{-2}, v_{-1}) supplies the window before the first token; null
+// means zeros.
 template <typename io_t>
-__global__ void __launch_bounds__(NT) prep_kernel(const io_t *__restrict__ v, const io_t *__restrict__ conv_w,
+__global__ void __launch_bounds__(NT) prep_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
+                                                  const io_t *__restrict__ conv_w,
                                                   const float *__restrict__ gamma,
                                                   const float *__restrict__ eta, float *__restrict__ X,
                                                   int H, int T, int dv, int R)
@@ -48,7 +51,10 @@ __global__ void __launch_bounds__(NT) prep_kernel(const io_t *__restrict__ v, co
     float a = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        if (t - j >= 0) a = fmaf(ldf(conv_w + ((size_t)h * 4 + j) * dv + c), ldf(vb + (size_t)(t - j) * dv + c), a);
+        if (t - j >= 0)
+            a = fmaf(ldf(conv_w + ((size_t)h * 4 + j) * dv + c), ldf(vb + (size_t)(t - j) * dv + c), a);
+        else if (v_hist)
+            a = fmaf(ldf(conv_w + ((size_t)h * 4 + j) * dv + c), ldf(v_hist + ((size_t)bh * 3 + 3 + t - j) * dv + c), a);
     const float Phi = 0.5f * erfcf(-a * 0.70710678118654752f);
     const float phi = 0.39894228040143268f * expf(-0.5f * a * a);
     const float g = fmaf(a, phi, Phi);
@@ -245,12 +251,15 @@ __global__ void __launch_bounds__(NT) wy_kernel(const io_t *__restrict__ k, cons
 }
 
 // ---------------------------------------------------------------------------------------------
-// Step a6: inter-chunk state passing, sequential over chunks, VB value rows per block.
+// Step a6: inter-chunk state passing, sequential over chunks, VB value rows per block, from
+// S_init (or 0); S_final, if given, receives the state after the last token.  Each block reads
+// and writes only its own rows, so S_final may be S_init.
 template <typename io_t>
 __global__ void __launch_bounds__(NT) state_kernel(const io_t *__restrict__ k, const io_t *__restrict__ u,
                                                    const float *__restrict__ X, const float *__restrict__ lam_ws,
                                                    const float *__restrict__ W_ws, const float *__restrict__ Up_ws,
                                                    float *__restrict__ S0_ws, float *__restrict__ Vt_ws,
+                                                   const float *S_init, float *S_final,
                                                    int T, int dk, int dv, int R, int NC)
 {
     extern __shared__ float smem[];
@@ -262,7 +271,10 @@ __global__ void __launch_bounds__(NT) state_kernel(const io_t *__restrict__ k, c
     float *Vs = Ks + C * ldk;   // C x ldb
     float *lam = Vs + C * ldb;  // C
 
-    for (int e = tid; e < VB * ldk; e += NT) S[e] = 0.f;
+    for (int e = tid; e < VB * dk; e += NT) {
+        const int r = e / dk, m = e % dk;
+        S[r * ldk + m] = S_init ? S_init[((size_t)bh * dv + r0 + r) * dk + m] : 0.f;
+    }
     for (int c = 0; c < NC; ++c) {
         const int t0 = c * C;
         const int n = min(C, T - t0);
@@ -317,6 +329,13 @@ __global__ void __launch_bounds__(NT) state_kernel(const io_t *__restrict__ k, c
                 for (int i = 0; i < C; ++i) s = fmaf(Vs[i * ldb + r], Ks[i * ldk + m], s);
                 S[r * ldk + m] = s;
             }
+        }
+    }
+    if (S_final) {
+        __syncthreads();
+        for (int e = tid; e < VB * dk; e += NT) {
+            const int r = e / dk, m = e % dk;
+            S_final[((size_t)bh * dv + r0 + r) * dk + m] = S[r * ldk + m];
         }
     }
 }
@@ -451,7 +470,8 @@ static cudaError_t forward_t(const Shape &s, const ForwardArgs &a, const SimtWor
         const long long elems = (long long)s.T * s.dv;
         dim3 grid((unsigned)((elems + NT - 1) / NT), s.BH);
         tm.begin("simt_prep");
-        prep_kernel<io_t><<<grid, NT, 0, st>>>(v, cw, a.gamma, a.eta, w.X, s.H, s.T, s.dv, s.R);
+        prep_kernel<io_t><<<grid, NT, 0, st>>>(v, (const io_t *)a.v_hist, cw, a.gamma, a.eta, w.X, s.H, s.T, s.dv,
+                                               s.R);
         tm.end();
     }
     tm.begin("simt_chunk_solve");
@@ -462,8 +482,9 @@ static cudaError_t forward_t(const Shape &s, const ForwardArgs &a, const SimtWor
                                                          s.dv, s.R, s.NC);
     tm.end();
     tm.begin("simt_state");
-    state_kernel<io_t><<<dim3(s.BH, s.dv / VB), NT, sm.state, st>>>(k, u, w.X, w.lam, w.W, w.Up, w.S0, w.Vt, s.T,
-                                                                    s.dk, s.dv, s.R, s.NC);
+    state_kernel<io_t><<<dim3(s.BH, s.dv / VB), NT, sm.state, st>>>(k, u, w.X, w.lam, w.W, w.Up, w.S0, w.Vt,
+                                                                    a.S_init, a.S_final, s.T, s.dk, s.dv, s.R,
+                                                                    s.NC);
     tm.end();
     tm.begin("simt_out");
     out_kernel<io_t, out_t><<<dim3(s.NC, s.BH), NT, sm.out, st>>>(q, k, u, w.X, w.lam, w.S0, w.Vt, out, s.T, s.dk, s.dv,
@@ -516,11 +537,15 @@ cudaError_t simt_forward(const Shape &s, prism_dtype io, prism_dtype out, const 
                          int *d_status, KernelTimer &timer)
 {
     (void)d_status;
+    cudaError_t e;
     if (io == PRISM_BF16)
-        return out == PRISM_F32 ? simt::forward_t<__nv_bfloat16, float>(s, a, w, timer)
-                                : simt::forward_t<__nv_bfloat16, __nv_bfloat16>(s, a, w, timer);
-    return out == PRISM_F32 ? simt::forward_t<float, float>(s, a, w, timer)
-                            : simt::forward_t<float, __nv_bfloat16>(s, a, w, timer);
+        e = out == PRISM_F32 ? simt::forward_t<__nv_bfloat16, float>(s, a, w, timer)
+                             : simt::forward_t<__nv_bfloat16, __nv_bfloat16>(s, a, w, timer);
+    else
+        e = out == PRISM_F32 ? simt::forward_t<float, float>(s, a, w, timer)
+                             : simt::forward_t<float, __nv_bfloat16>(s, a, w, timer);
+    if (e == cudaSuccess && a.v_hist_out) e = launch_history(s, io, a.v_hist, a.v, a.v_hist_out, timer);
+    return e;
 }
 
 }  // namespace prism

@@ -8,11 +8,13 @@
 //            factors and the chunk's state map S -> S M_c + N_c, and carries the augmented state
 //            Z = [N; M] (the segment's map S_start -> S_start M + N) through the segment.  The
 //            output of a chunk is o = o0 + Qhat S_start^T: o0 and Qhat are exact given Z, so the
-//            first segment of a sequence (S_start = 0) writes o directly and the others stash
-//            (o0, Qhat) for the fix-up.
-//   combine  per sequence, S_start of segment p from the maps of segments 0..p-1 (associative
-//            combine of the input-only affine maps, notes on PRISM section 2.1).
-//   fixup    o = o0 + Qhat S_start^T for the chunks of segments >= 1.
+//            first segment of a sequence that starts from S = 0 writes o directly and the others
+//            stash (o0, Qhat) for the fix-up.  A sequence continued from an earlier call starts
+//            from S_init, with the anchor's left context v_{-3..-1} in place of the zero halo.
+//   combine  per sequence, S_start of segment p from S_init (or 0) and the maps of segments
+//            0..p-1 (associative combine of the input-only affine maps, notes on PRISM
+//            section 2.1); optionally the state after the last token.
+//   fixup    o = o0 + Qhat S_start^T for the chunks of the stashing segments.
 //
 // Chunk algebra (local index i, j; lambda_i = sum_{m<=i} ln alpha_m; lc = lambda_{C-1};
 // rowf_i = e^{lambda_i - lc} >= 1, colf_j = e^{lc - lambda_j} <= 1, Gamma_i = e^{lambda_i}):
@@ -116,9 +118,11 @@ struct SegParams {
     float *zsum;            // [BH][P][128][64]
     void *stash_o;          // [BH][NC][64][64]  o0 (token-major; fp32 for fp32 output, else fp16)
     __half *stash_q;        // [BH][NC][64][64]  Qhat (token-major)
+    const __nv_bfloat16 *v_hist;  // [BH][3][64] v_{-3..-1} of the sequence, or null (zeros)
     int *status;
     int H, T, R, NC, P;
     int out_f32;
+    int has_init;           // the sequence starts from a given state: segment 0 is tracked too
     unsigned long long wait_ns;  // bound of every wait on an mbarrier
 };
 
@@ -303,6 +307,9 @@ __global__ void __launch_bounds__(NT, 1)
     const int R = p.R;
     const int c_begin = (int)(((long long)seg * p.NC) / p.P);
     const int c_end = (int)(((long long)(seg + 1) * p.NC) / p.P);
+    // a tracked segment carries M (the map's linear part) and stashes o0/Qhat for the fix-up;
+    // only the first segment of a sequence that starts from S = 0 can write o directly
+    const bool tracked = seg > 0 || p.has_init;
 
     float *sc = reinterpret_cast<float *>(sm + OFF_SC);
     // per-token scalars, one set per chunk parity (the next chunk's set is filled while the
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(NT, 1)
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_u);
     }
-    // zero tile, bf16 identity, and Z = [0; I] (segments >= 1) or 0 (segment 0)
+    // zero tile, bf16 identity, and Z = [0; I] (tracked segments) or 0
     for (int e = tid; e < (int)(TILE / 16); e += NT) reinterpret_cast<uint4 *>(sm + OFF_ZERO)[e] = make_uint4(0, 0, 0, 0);
     {
         const int i = tid >> 3, g = tid & 7;  // row i, 16-byte group g (8 columns)
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     for (int e = tid; e < 128 * 64; e += NT) {
         const int r = e >> 6, m = e & 63;
-        const float z = (seg > 0 && r >= 64 && (r - 64) == m) ? 1.f : 0.f;
+        const float z = (tracked && r >= 64 && (r - 64) == m) ? 1.f : 0.f;
         *reinterpret_cast<__half *>(sm + OFF_ZA + sw128(r, m)) = __float2half_rn(z);
     }
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 512);
@@ -490,6 +497,14 @@ __global__ void __launch_bounds__(NT, 1)
             fill_scalars(set);
             if (c + 1 < c_end) load_gates(c + 1);
             if (!wait_one(mb_v[stage], ph_v[stage], 4u << stage)) break;
+            if (seg == 0 && p.v_hist != nullptr) {  // the convolution's left context replaces the zero halo
+                if (tid < 24) {  // 3 rows (tokens -3..-1) x 8 groups of 16 bytes
+                    const uint4 hv = reinterpret_cast<const uint4 *>(p.v_hist + (size_t)bh * 3 * D)[tid];
+                    *reinterpret_cast<uint4 *>(sm + (stage ? OFF_V1 : OFF_V0) + (5 + (tid >> 3)) * 128 + (tid & 7) * 16) = hv;
+                    fence_async_smem();  // the stage is refilled by TMA later
+                }
+                __syncthreads();
+            }
             prep(c, stage);
             fence_async_smem();
         }
@@ -953,7 +968,7 @@ __global__ void __launch_bounds__(NT, 1)
             if (row < 64) {
 #pragma unroll
                 for (int q = 0; q < CW; ++q) so[(j0 + q) * 64 + row] = o[q] + s_rowf[j0 + q] * ol[q];
-            } else if (seg > 0) {
+            } else if (tracked) {
 #pragma unroll
                 for (int q = 0; q < CW; ++q) sq[(j0 + q) * 64 + row - 64] = __float2half_rn(o[q]);
             }
@@ -970,7 +985,7 @@ __global__ void __launch_bounds__(NT, 1)
                 const float4 v = *reinterpret_cast<const float4 *>(so + i * 64 + c4);
                 finite = finite && isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w);
                 const size_t o = (tok0 + i) * D + c4;
-                if (seg == 0) {
+                if (!tracked) {
                     if (p.out_f32) {
                         *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o) = v;
                     } else {
@@ -993,7 +1008,7 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             PHASE_MARK(18);
-            if (seg > 0) {
+            if (tracked) {
                 const uint4 *sq = reinterpret_cast<const uint4 *>(sm + OFF_E + 2 * TILE);
                 uint4 *dq = reinterpret_cast<uint4 *>(p.stash_q + ((size_t)bh * p.NC + c) * 4096);
                 for (int e = tid; e < 512; e += NT) dq[e] = sq[e];
@@ -1027,8 +1042,9 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} in fp32, 8 value rows per block, written
-// out as fp16 (the fix-up's MMA operand).  The maps stream through a ring of CB_STAGES
+// combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} in fp32 from S_start[0] = S_init (or 0),
+// 8 value rows per block, written out as fp16 (the fix-up's MMA operand); with S_final the map of
+// the last segment is applied too and the result written out in fp32.  The maps stream through a ring of CB_STAGES
 // shared-memory stages filled by bulk copies (16 KB of M and this block's 2 KB of N per
 // segment), so the serial chain never waits on global memory latency.  Each step's 8x64x64
 // product is split over the sum index: thread (kq, rg, lane) accumulates rows 4 rg .. 4 rg + 3,
@@ -1043,7 +1059,8 @@ constexpr int CB_STAGE_FLOATS = 64 * 64 + CB_ROWS * 64;
 constexpr size_t CB_SMEM = (size_t)CB_STAGES * CB_STAGE_FLOATS * 4 + 128;
 
 __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__restrict__ zsum, __half *__restrict__ sstart,
-                                                             int P, int *status, unsigned long long wait_ns)
+                                                             int P, const float *S_init, float *S_final, int *status,
+                                                             unsigned long long wait_ns)
 {
     extern __shared__ __align__(128) float ring[];  // [CB_STAGES][M 64x64 | N 8x64]
     __shared__ __align__(8) uint64_t mb[CB_STAGES];
@@ -1055,10 +1072,14 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
     const int rr = tid >> 5;  // the row this thread reduces (columns c2, c2 + 1)
     prism::tc::grid_dependency_wait();  // the segment maps of the segment kernel
     prism::tc::allow_dependent_launch();
-    *reinterpret_cast<__half2 *>(sstart + ((size_t)bh * P * 64 + r0 + rr) * 64 + c2) = __floats2half2_rn(0.f, 0.f);
-    *reinterpret_cast<float2 *>(&S[0][rr][c2]) = make_float2(0.f, 0.f);
-    if (P < 2) return;
-    const int nmaps = P - 1;  // maps of segments 0..P-2 are used
+    // S_init and S_final may be one buffer: each thread reads its two entries here and writes the
+    // same two at the end
+    const float2 s0 = S_init ? *reinterpret_cast<const float2 *>(S_init + ((size_t)bh * 64 + r0 + rr) * 64 + c2)
+                             : make_float2(0.f, 0.f);
+    *reinterpret_cast<__half2 *>(sstart + ((size_t)bh * P * 64 + r0 + rr) * 64 + c2) = __floats2half2_rn(s0.x, s0.y);
+    *reinterpret_cast<float2 *>(&S[0][rr][c2]) = s0;
+    const int nmaps = S_final ? P : P - 1;  // maps of segments 0..P-2 (and P-1 for S_final)
+    if (nmaps == 0) return;
     auto issue = [&](int sp) {
         const int st = sp % CB_STAGES;
         const uint32_t m = prism::tc::smem_u32(&mb[st]);
@@ -1140,8 +1161,11 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
             o.y += v.y;
         }
         *reinterpret_cast<float2 *>(&S[buf ^ 1][rr][c2]) = o;
-        *reinterpret_cast<__half2 *>(sstart + (((size_t)bh * P + k + 1) * 64 + r0 + rr) * 64 + c2) =
-            __floats2half2_rn(o.x, o.y);
+        if (k + 1 < P)
+            *reinterpret_cast<__half2 *>(sstart + (((size_t)bh * P + k + 1) * 64 + r0 + rr) * 64 + c2) =
+                __floats2half2_rn(o.x, o.y);
+        else  // k + 1 == P: the state after the last token (S_final was asked for)
+            *reinterpret_cast<float2 *>(S_final + ((size_t)bh * 64 + r0 + rr) * 64 + c2) = o;
     }
 #ifdef PRISM_PHASE_TIMERS
     if (trace) {  // combine tracing: block (0, 0), thread 0: map waits and the whole chain
@@ -1158,7 +1182,7 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
                                        1000000000ull);
 }
 
-// fixup: o = o0 + Qhat S_start^T for the chunks of segments >= 1, one CTA of 4 warps per chunk
+// fixup: o = o0 + Qhat S_start^T for the chunks of tracked segments, one CTA of 4 warps per chunk
 // (many chunks in flight per SM).  Qhat, S_start (fp16) and o0 are copied into padded
 // shared-memory rows with 16-byte cp.async (coalesced, no register staging); the 64x64x64
 // product runs on mma.sync m16n8k16 (fp16 in, fp32 accumulate) with A = Qhat [i][m],
@@ -1182,7 +1206,7 @@ constexpr int FX_LDF = 72;  // row stride (floats) of the fp32 o0 tile
 
 __global__ void __launch_bounds__(128) fixup_kernel(const void *__restrict__ stash_o, const __half *__restrict__ stash_q,
                                                     const __half *__restrict__ sstart, void *__restrict__ out,
-                                                    int out_f32, int T, int NC, int P)
+                                                    int out_f32, int T, int NC, int P, int has_init)
 {
     __shared__ __align__(16) __half Qs[64 * FX_LDH];             // Qhat [i][m]
     __shared__ __align__(16) __half Ss[64 * FX_LDH];             // S_start [c][m]
@@ -1194,7 +1218,7 @@ __global__ void __launch_bounds__(128) fixup_kernel(const void *__restrict__ sta
     while (seg > 0 && ((long long)seg * NC) / P > c) --seg;
     grid_dependency_wait();  // the stash of the segment kernel and S_start of the combine
     allow_dependent_launch();
-    if (seg == 0) return;
+    if (seg == 0 && !has_init) return;  // written directly by the segment kernel
     const size_t chunk = (size_t)bh * NC + c;
     const int t0 = c * 64, n = min(64, T - t0);
     {
@@ -1402,6 +1426,8 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
     p.zsum = w.zsum;
     p.stash_o = w.stash_o;
     p.stash_q = w.stash_q;
+    p.v_hist = (const __nv_bfloat16 *)a.v_hist;
+    p.has_init = a.S_init != nullptr;
     p.status = d_status;
     p.H = s.H;
     p.T = s.T;
@@ -1426,22 +1452,29 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
     cudaError_t e = cudaLaunchKernelEx(&cfg, segment_kernel, mq, mk, mv, mu, p);
     tm.end();
     if (e != cudaSuccess) return e;
-    if (w.P > 1) {
+    if (w.P > 1 || a.S_init || a.S_final) {
         tm.begin("tc_combine");
         cfg.gridDim = dim3(s.BH, 64 / CB_ROWS);
         cfg.blockDim = dim3(CB_THREADS);
         cfg.dynamicSmemBytes = CB_SMEM;
-        e = cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)w.zsum, w.sstart, (int)w.P, d_status,
-                               (unsigned long long)p.wait_ns);
+        e = cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)w.zsum, w.sstart, (int)w.P, a.S_init, a.S_final,
+                               d_status, (unsigned long long)p.wait_ns);
         tm.end();
         if (e != cudaSuccess) return e;
+    }
+    if (w.P > 1 || a.S_init) {
         tm.begin("tc_fixup");
         cfg.gridDim = dim3(s.NC, s.BH);
         cfg.blockDim = dim3(128);
         cfg.dynamicSmemBytes = 0;
         e = cudaLaunchKernelEx(&cfg, fixup_kernel, (const void *)w.stash_o, (const __half *)w.stash_q,
-                               (const __half *)w.sstart, a.out, (int)p.out_f32, (int)s.T, (int)s.NC, (int)w.P);
+                               (const __half *)w.sstart, a.out, (int)p.out_f32, (int)s.T, (int)s.NC, (int)w.P,
+                               p.has_init);
         tm.end();
+        if (e != cudaSuccess) return e;
+    }
+    if (a.v_hist_out) {  // a plain launch: it runs after every kernel above has finished reading v_hist
+        e = launch_history(s, PRISM_BF16, a.v_hist, a.v, a.v_hist_out, tm);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

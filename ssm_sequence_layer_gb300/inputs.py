@@ -21,8 +21,9 @@ eta draws.
 The five named workloads reproduce the shapes the method is measured on: a tiny
 fp32 case, a GDN-degenerate (L = 1) case, the 130M-parameter language-model
 layer shape (2K tokens, 6 heads of 128), the 16K-token sequential-recommendation
-shape (4 heads of 64) and a 64K-token long-memory stress case.  No dataset item
-is used: the values are synthetic.
+shape (4 heads of 64) and a 64K-token long-memory stress case.  The decode
+workloads take one token per sequence with those head shapes over a serving batch.
+No dataset item is used: the values are synthetic.
 """
 from __future__ import annotations
 
@@ -63,6 +64,14 @@ WORKLOADS = {
     "long_64k": Workload("long_64k", 1, 16, 65536, 128, 128, 8, "bf16", 64.0),
 }
 HEADLINE = "seqrec_16k"
+
+# One recurrent step (one token per sequence) over a serving batch: the head shapes of the
+# language-model layer and of the recommendation shape, with as many sequences as make the
+# fp32 state (B H dv dk 4 bytes) larger than the 129 MB L2, so that a step streams it from HBM.
+DECODE_WORKLOADS = {
+    "decode_lm130m": Workload("decode_lm130m", 512, 6, 1, 128, 128, 4, "bf16"),
+    "decode_seqrec": Workload("decode_seqrec", 2048, 4, 1, 64, 64, 4, "bf16"),
+}
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
 
