@@ -8,7 +8,8 @@ bf16 io), plus the achieved fraction of the roofline of the binding resource.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step is one prism_forward over the whole synthetic batch (inputs resident in
-HBM).  L2 is flushed (a 512 MiB write) before every timed step and the step is
+HBM).  L2 is flushed (a 512 MiB write, then a 512 MiB read, so that no dirty line of
+the flush is written back inside the timed region) before every timed step and the step is
 timed alone with CUDA events on the launch stream.  N > 1 runs one independent
 replica per GPU (the path has no exchange step), launched by torchrun; rank 0
 prints one JSON line with the max-over-ranks time.
@@ -180,6 +181,26 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------------
+class L2Flush:
+    """Evicts L2 (129 MB on GB300) between timed steps: a 512 MiB write, then a 512 MiB read of
+    another buffer, so that the lines the write leaves dirty are written back before the timed
+    region starts rather than inside it."""
+
+    DESCRIPTION = "flushed before every timed step: 512 MiB written, then 512 MiB of another buffer read"
+
+    def __init__(self):
+        import torch
+        n = 512 * 1024 * 1024 // 4
+        self.w = torch.empty(n, dtype=torch.float32, device="cuda")
+        self.r = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
+
+
 def dist_setup(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -287,10 +308,10 @@ def run_ours(args, w):
     out = torch.empty_like(dev["v"])
     stream = torch.cuda.current_stream()
     plan = Bd.Plan.for_inputs(dev, path=args.path if args.path else None)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
 
     for _ in range(warm):
-        flush.zero_()
+        flush()
         plan.forward(dev, out, stream)
     torch.cuda.synchronize()
     plan.last_device_status()
@@ -302,7 +323,7 @@ def run_ours(args, w):
     barrier(world)
     torch.cuda.synchronize()
     for i in range(steps):  # the timed steps: no per-kernel events inside the forward
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         plan.forward(dev, out, stream)
         ev[i][1].record(stream)
@@ -317,7 +338,7 @@ def run_ours(args, w):
     per_kernel = {}
     launches = 0
     for i in range(steps):
-        flush.zero_()
+        flush()
         plan.forward(dev, out, stream)
         torch.cuda.synchronize()
         kt = plan.kernel_times()
@@ -362,7 +383,7 @@ def run_ours(args, w):
             plan.forward_host(host, hout, stream)
         e2e_ms = []
         for _ in range(max(3, min(steps, 20))):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             plan.forward_host(host, hout, stream)
@@ -387,7 +408,7 @@ def run_ours(args, w):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")},
-                       "io": w.dtype, "l2": "flushed by a 512 MiB write before every timed step",
+                       "io": w.dtype, "l2": L2Flush.DESCRIPTION,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline, "path_roofline": path_roofline, "kernels": kernels,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
@@ -466,9 +487,9 @@ def run_decode(args, w):
     out = torch.empty(w.B, w.H, w.dv, dtype=tok["v"].dtype, device="cuda")
     stream = torch.cuda.current_stream()
     plan = Bd.Plan(w.B, w.H, 1, w.dk, w.dv, w.L, io=w.dtype)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
     for _ in range(warm):
-        flush.zero_()
+        flush()
         plan.decode_step(tok, hist, S, out, stream)
     torch.cuda.synchronize()
 
@@ -479,7 +500,7 @@ def run_decode(args, w):
     barrier(world)
     torch.cuda.synchronize()
     for i in range(steps):  # one kernel per step: the step events time the decode kernel itself
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         plan.decode_step(tok, hist, S, out, stream)
         ev[i][1].record(stream)
@@ -508,7 +529,7 @@ def run_decode(args, w):
         dtok = {k: (torch.empty_like(v, device="cuda") if torch.is_tensor(v) else v) for k, v in host.items()}
         e2e_ms = []
         for i in range(max(3, min(steps, 20)) + 2):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for k, v in host.items():
@@ -537,7 +558,7 @@ def run_decode(args, w):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "dk", "dv", "L")},
-                       "io": w.dtype, "state": "fp32, resident", "l2": "flushed by a 512 MiB write before every timed step",
+                       "io": w.dtype, "state": "fp32, resident", "l2": L2Flush.DESCRIPTION,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": steps, "clocks": clocks,
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),

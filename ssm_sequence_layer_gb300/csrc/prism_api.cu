@@ -336,7 +336,8 @@ prism_status prism_decode_step(prism_plan_t p, const void *q, const void *k, con
     prism::DecodeArgs a{q, k, v, u, conv_w, beta, alpha, gamma, eta, v_hist, S, out};
     p->timer.on = p->opt_timing != 0;
     p->timer.reset((cudaStream_t)stream);
-    const cudaError_t e = prism::decode_step(p->shape, p->io, p->out_dtype, a, p->timer);
+    const cudaError_t e =
+        prism::decode_step(p->shape, p->io, p->out_dtype, a, p->sm_count, p->d_status, p->opt_wait_ns, p->timer);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return PRISM_OK;
 }

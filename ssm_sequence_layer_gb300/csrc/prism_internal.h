@@ -103,7 +103,8 @@ struct DecodeArgs {
     float *S;
     void *out;
 };
-cudaError_t decode_step(const Shape &s, prism_dtype io, prism_dtype out, const DecodeArgs &a, KernelTimer &tm);
+cudaError_t decode_step(const Shape &s, prism_dtype io, prism_dtype out, const DecodeArgs &a, int sm_count,
+                        int *d_status, long long wait_ns, KernelTimer &tm);
 
 size_t simt_workspace_bytes(const Shape &s);
 void simt_carve(const Shape &s, void *base, SimtWorkspace *w);
