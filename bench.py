@@ -106,26 +106,37 @@ def kernel_alg_bytes(name, w):
     return table.get(name, q + k + v + u + gates + out)
 
 
+# the source files each kernel is built from (its own translation unit and the headers it uses)
+KERNEL_SOURCES = {
+    "tc_": ("prism_tc.cu", "tc_ptx.h", "prism_internal.h"),
+    "decode": ("prism_state.cu", "tc_ptx.h", "prism_internal.h"),
+    "simt_": ("prism_simt.cu", "prism_internal.h"),
+}
+
+
 def traffic_from_profiles(kernel, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
-    kernel source (the summary records the source digest); else None."""
+    source of that kernel (the summary records the digest of the kernel's source files);
+    else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != source_digest():
+    if not m or not s or s.group(1) != source_digest(kernel):
         return None
     return float(m.group(1))
 
 
-def source_digest():
-    h = hashlib.sha256()
+def source_digest(kernel):
+    files = next((f for prefix, f in KERNEL_SOURCES.items() if kernel.startswith(prefix)), None)
     csrc = os.path.join(ROOT, "ssm_sequence_layer_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".h")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    if files is None:
+        files = sorted(fn for fn in os.listdir(csrc) if fn.endswith((".cu", ".h")))
+    h = hashlib.sha256()
+    for fn in files:
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
