@@ -30,6 +30,13 @@
  *             standard GDN write, article part 03 item four)
  *   readout   o_t = S_t q_t  (post-update state)
  *
+ * Non-linear residual variant (optional input p_gain, notes section 2.3: a gain vector
+ * p_{t,l} predicted from the anchor replaces GELU'(h), and each level takes a non-linear
+ * step off the residual, "greedy residual subtraction"):
+ *   delta_{t,l} = GELU(p_{t,l} (.) r_{t,l}),  r_{t,l+1} = r_{t,l} - delta_{t,l},
+ *   injection factor of level l: gamma_{t,l} delta_{t,l}      (eta is not read)
+ * Everything else (anchor, r_{t,1} = e_t, transition, GDN write, readout) is unchanged.
+ *
  * Storage (row-major, contiguous), R = L - 1:
  *   q, k   [B,H,T,dk]      v, out [B,H,T,dv]      u [B,H,T,R,dk]
  *   beta, alpha [B,H,T]    gamma, eta [B,H,T,R]   conv_w [H,4,dv] (tap j
@@ -41,6 +48,7 @@
  *   X_out   [B,H,T,R,dv]  injection factors x_{t,l} = gamma_{t,l} g_t (.) r_{t,l}
  *   h_out, g_out, e_out [B,H,T,dv]  anchor, gain and residual
  *   S_init  [B,H,dv,dk]   optional initial state (NULL means S_0 = 0)
+ *   p_gain  [B,H,T,R,dv]  optional gains of the non-linear variant (slot l-1: level l)
  *   v_hist  [B,H,3,dv]    optional left context of the convolution: slot j holds
  *                         v_{j-3} (oldest first), the last three tokens before this
  *                         call's first one (NULL means zeros).  With S_init it lets
@@ -57,7 +65,7 @@
 
 typedef struct {
     int B, H, T, dk, dv, L;
-    const double *q, *k, *v, *beta, *alpha, *u, *gamma, *eta, *conv_w, *v_hist, *S_init;
+    const double *q, *k, *v, *beta, *alpha, *u, *gamma, *eta, *p_gain, *conv_w, *v_hist, *S_init;
     double *out, *S_final, *X_out, *h_out, *g_out, *e_out;
     int nthreads;
     int thread_id;
@@ -75,7 +83,8 @@ static void run_head(const oracle_args *a, int b, int h)
     const double *alpha = a->alpha + bh * T;
     const double *u = R > 0 ? a->u + bh * T * R * dk : NULL;
     const double *gamma = R > 0 ? a->gamma + bh * T * R : NULL;
-    const double *eta = R > 0 ? a->eta + bh * T * R : NULL;
+    const double *eta = (R > 0 && a->eta) ? a->eta + bh * T * R : NULL;
+    const double *pg = (R > 0 && a->p_gain) ? a->p_gain + bh * T * R * dv : NULL;
     const double *w = a->conv_w + (size_t)h * 4 * dv;
     const double *vh = a->v_hist ? a->v_hist + bh * 3 * dv : NULL;
     double *out = a->out + bh * T * dv;
@@ -130,12 +139,19 @@ static void run_head(const oracle_args *a, int b, int h)
         for (int l = 1; l <= R; ++l) {
             const double gm = gamma[(size_t)t * R + (l - 1)];
             const double *ul = u + ((size_t)t * R + (l - 1)) * dk;
+            const double *pl = pg ? pg + ((size_t)t * R + (l - 1)) * dv : NULL;
             for (int i = 0; i < dv; ++i) {
                 double x = gm * g[i] * r[i];
+                if (pl) { /* non-linear variant: delta = GELU(p r), r <- r - delta */
+                    const double z = pl[i] * r[i];
+                    const double delta = z * 0.5 * (1.0 + erf(z * inv_sqrt2));
+                    x = gm * delta;
+                    r[i] -= delta;
+                }
                 if (a->X_out) a->X_out[((bh * T + t) * R + (l - 1)) * dv + i] = x;
                 for (int j = 0; j < dk; ++j) S[(size_t)i * dk + j] += x * ul[j];
             }
-            if (l < R) {
+            if (!pl && l < R) {
                 const double et = eta[(size_t)t * R + (l - 1)];
                 for (int i = 0; i < dv; ++i) r[i] *= (1.0 - et * g[i]);
             }
@@ -166,19 +182,20 @@ int prism_oracle_forward_f64(int B, int H, int T, int dk, int dv, int L,
                              const double *q, const double *k, const double *v,
                              const double *beta, const double *alpha,
                              const double *u, const double *gamma, const double *eta,
-                             const double *conv_w, const double *v_hist, const double *S_init,
+                             const double *p_gain, const double *conv_w, const double *v_hist,
+                             const double *S_init,
                              double *out, double *S_final, double *X_out,
                              double *h_out, double *g_out, double *e_out, int nthreads)
 {
     if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0 || L < 1) return -1;
     if (!q || !k || !v || !beta || !alpha || !conv_w || !out) return -2;
-    if (L > 1 && (!u || !gamma || !eta)) return -3;
+    if (L > 1 && (!u || !gamma || (!eta && !p_gain))) return -3;
     const int units = B * H;
     if (units == 0) return 0;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > units) nthreads = units;
 
-    oracle_args base = {B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, conv_w, v_hist, S_init,
+    oracle_args base = {B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, p_gain, conv_w, v_hist, S_init,
                         out, S_final, X_out, h_out, g_out, e_out, nthreads, 0};
     if (nthreads == 1) {
         worker(&base);

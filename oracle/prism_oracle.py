@@ -43,7 +43,7 @@ def _open(path):
     lib = ctypes.CDLL(path)
     dp = ctypes.POINTER(ctypes.c_double)
     lib.prism_oracle_forward_f64.restype = ctypes.c_int
-    lib.prism_oracle_forward_f64.argtypes = [ctypes.c_int] * 6 + [dp] * 11 + [dp] * 6 + [ctypes.c_int]
+    lib.prism_oracle_forward_f64.argtypes = [ctypes.c_int] * 6 + [dp] * 12 + [dp] * 6 + [ctypes.c_int]
     return lib
 
 
@@ -69,17 +69,18 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def forward(q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None, v_hist=None,
+def forward(q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None, v_hist=None, p_gain=None,
             want_state=False, want_x=False, want_hge=False, nthreads=None):
     """Run the oracle.  Arrays follow the layouts in ``prism_oracle.c``; ``S_init``
     [B,H,dv,dk] and ``v_hist`` [B,H,3,dv] (v_{-3}, v_{-2}, v_{-1}) carry a sequence over
-    from a previous call.
+    from a previous call.  ``p_gain`` [B,H,T,R,dv] selects the non-linear residual variant
+    (``eta`` is then not read and may be None).
 
     Returns a dict with ``out`` [B,H,T,dv] and, on request, ``S_final``
     [B,H,dv,dk], ``X`` [B,H,T,R,dv] and ``h``/``g``/``e`` [B,H,T,dv], all fp64.
     """
     return _forward(_load(), q, k, v, beta, alpha, u, gamma, eta, conv_w, L, S_init=S_init, v_hist=v_hist,
-                    want_state=want_state, want_x=want_x, want_hge=want_hge, nthreads=nthreads)
+                    p_gain=p_gain, want_state=want_state, want_x=want_x, want_hge=want_hge, nthreads=nthreads)
 
 
 class OracleLib:
@@ -93,7 +94,7 @@ class OracleLib:
         return _forward(self._lib, *args, **kw)
 
 
-def _forward(lib, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None, v_hist=None,
+def _forward(lib, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None, v_hist=None, p_gain=None,
              want_state=False, want_x=False, want_hge=False, nthreads=None):
     q, k, v = _f64(q), _f64(k), _f64(v)
     beta, alpha, conv_w = _f64(beta), _f64(alpha), _f64(conv_w)
@@ -101,10 +102,12 @@ def _forward(lib, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None
     dv = v.shape[-1]
     R = L - 1
     if R > 0:
-        u, gamma, eta = _f64(u), _f64(gamma), _f64(eta)
-        assert u.shape == (B, H, T, R, dk) and gamma.shape == (B, H, T, R) and eta.shape == (B, H, T, R)
+        u, gamma, eta, p_gain = _f64(u), _f64(gamma), _f64(eta), _f64(p_gain)
+        assert u.shape == (B, H, T, R, dk) and gamma.shape == (B, H, T, R)
+        assert (eta is None and p_gain is not None) or eta.shape == (B, H, T, R)
+        assert p_gain is None or p_gain.shape == (B, H, T, R, dv)
     else:
-        u = gamma = eta = None
+        u = gamma = eta = p_gain = None
     assert k.shape == (B, H, T, dk) and v.shape == (B, H, T, dv)
     assert beta.shape == (B, H, T) and alpha.shape == (B, H, T) and conv_w.shape == (H, 4, dv)
     S_init = _f64(S_init)
@@ -123,7 +126,7 @@ def _forward(lib, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, *, S_init=None
         nthreads = len(os.sched_getaffinity(0))
     rc = lib.prism_oracle_forward_f64(
         B, H, T, dk, dv, L, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(u),
-        _ptr(gamma), _ptr(eta), _ptr(conv_w), _ptr(v_hist), _ptr(S_init), _ptr(out), _ptr(S_final), _ptr(X),
+        _ptr(gamma), _ptr(eta), _ptr(p_gain), _ptr(conv_w), _ptr(v_hist), _ptr(S_init), _ptr(out), _ptr(S_final), _ptr(X),
         _ptr(hh), _ptr(gg), _ptr(ee), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")

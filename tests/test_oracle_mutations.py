@@ -37,6 +37,11 @@ MUTATIONS = [
     ("history in reverse order", "vh[(size_t)(3 + t - j) * dv + c]", "vh[(size_t)(j - t - 1) * dv + c]"),
     ("history ignored", "else if (vh) acc +=", "else if (0) acc +="),
     ("initial state ignored", "    if (a->S_init)\n", "    if (0)\n"),
+    ("non-linear step adds", "r[i] -= delta;", "r[i] += delta;"),
+    ("non-linear step with Phi", "const double delta = z * 0.5 * (1.0 + erf(z * inv_sqrt2));",
+     "const double delta = 0.5 * (1.0 + erf(z * inv_sqrt2));"),
+    ("gain slot shifted", "pg + ((size_t)t * R + (l - 1)) * dv", "pg + ((size_t)t * R + (R - l)) * dv"),
+    ("non-linear factor without gamma", "x = gm * delta;", "x = delta;"),
     ("readout dropped", "        /* readout from the post-update state */",
      "        /* readout from the post-update state */\n        if (0)"),
 ]
@@ -58,6 +63,10 @@ def _pin_suite(mod):
         ("zeroconv", lambda: pins.test_zero_conv_gives_half_gain(mod)),
         ("inert", lambda: pins.test_history_equals_prepended_inert_tokens(mod)),
         ("split", lambda: pins.test_split_calls_with_history_and_state(mod, (2, 3, 29))),
+        ("nl_zero", lambda: pins.test_nonlinear_zero_gain_is_gdn(mod)),
+        ("nl_small", lambda: pins.test_nonlinear_small_signal_limit_is_the_linear_chain(mod)),
+        ("nl_sat", lambda: pins.test_nonlinear_saturation_leaves_nothing_for_later_levels(mod)),
+        ("nl_gelu", lambda: pins.test_nonlinear_chain_against_library_gelu(mod)),
     ]
     for name, fn in cases:
         try:

@@ -318,6 +318,68 @@ def test_split_calls_with_history_and_state(oracle_mod, cuts):
     np.testing.assert_allclose(S, full["S_final"], rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------------------------------------
+# the non-linear residual variant (notes section 2.3): delta = GELU(p r), r <- r - delta
+def nonlinear_inputs(T=20, dk=6, dv=5, L=4, seed=18, p_scale=1.0):
+    inp = f64_inputs(B=1, H=2, T=T, dk=dk, dv=dv, L=L, seed=seed)
+    rng = np.random.default_rng(seed)
+    inp["p_gain"] = p_scale / (1.0 + np.exp(-rng.standard_normal((1, 2, T, L - 1, dv))))
+    return inp
+
+
+def test_nonlinear_zero_gain_is_gdn(oracle_mod):
+    """p = 0: GELU(0) = 0, so no level writes and the output is the L = 1 (GDN) output."""
+    inp = nonlinear_inputs()
+    inp["p_gain"] = np.zeros_like(inp["p_gain"])
+    res = run(oracle_mod, inp, p_gain=inp["p_gain"], want_x=True)
+    gdn = run(oracle_mod, dict(inp, L=1, u=None, gamma=None, eta=None))
+    assert np.all(res["X"] == 0.0)
+    np.testing.assert_array_equal(res["out"], gdn["out"])
+
+
+def test_nonlinear_small_signal_limit_is_the_linear_chain(oracle_mod):
+    """GELU(z) = z/2 + O(z^2): for tiny residuals, p = 2 g and eta = 1 turn the non-linear
+    chain into the linear one (x_l = gamma g r_l, r_{l+1} = r_l (1 - g)), which the closed-form
+    pin above fixes independently."""
+    inp = nonlinear_inputs(L=5)
+    inp["v"] = inp["v"] * 1e-7
+    lin = dict(inp, eta=np.ones_like(inp["eta"]))
+    ref = run(oracle_mod, lin, want_x=True, want_hge=True)
+    g = ref["g"]
+    p = np.repeat(2.0 * g[:, :, :, None, :], 4, axis=3)
+    res = run(oracle_mod, inp, p_gain=p, want_x=True)
+    scale = np.max(np.abs(ref["X"]))
+    assert scale > 0
+    assert np.max(np.abs(res["X"] - ref["X"])) <= 1e-5 * scale
+
+
+def test_nonlinear_saturation_leaves_nothing_for_later_levels(oracle_mod):
+    """p = 1 and a large positive residual: GELU(r) = r up to r Phi(-r), so the first level
+    takes the whole residual and the later levels see (almost) zero."""
+    inp = nonlinear_inputs(L=3)
+    inp["v"] = np.full_like(inp["v"], 20.0)
+    inp["conv_w"] = np.zeros_like(inp["conv_w"])  # h = 0, so e = v
+    p = np.ones_like(inp["p_gain"])
+    res = run(oracle_mod, inp, p_gain=p, want_x=True)
+    X = res["X"]
+    np.testing.assert_allclose(X[:, :, :, 0, :], np.broadcast_to(inp["gamma"][:, :, :, 0, None] * 20.0, X.shape[:3] + X.shape[4:]),
+                               rtol=1e-12)
+    assert np.max(np.abs(X[:, :, :, 1, :])) < 1e-60
+
+
+def test_nonlinear_chain_against_library_gelu(oracle_mod):
+    """Each level's factor from scipy's normal CDF, level by level, slot l - 1 for level l."""
+    inp = nonlinear_inputs(L=4, p_scale=3.0)
+    res = run(oracle_mod, inp, p_gain=inp["p_gain"], want_x=True, want_hge=True)
+    r = inp["v"] - gelu_lib(res["h"])
+    for l in range(3):
+        z = inp["p_gain"][:, :, :, l, :] * r
+        d = gelu_lib(z)
+        np.testing.assert_allclose(res["X"][:, :, :, l, :], inp["gamma"][:, :, :, l, None] * d, rtol=1e-12, atol=1e-15)
+        assert d.shape == res["X"][:, :, :, l, :].shape
+        r = r - d
+
+
 def test_state_stays_bounded_long_memory(oracle_mod):
     """beta in (0,1), ||k|| = 1, alpha < 1: the transition is a contraction, so
     ||S_t|| <= max_t ||B_t|| / (1 - max alpha) (notes, section 2.2 stability remark)."""
