@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "PRISM layer fwd tokens/s on 1 GB300 (T=16K) + % of HBM/tensor roofline"
+NONLINEAR_METRIC = "PRISM layer fwd tokens/s, non-linear residual variant + % of HBM roofline"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bit masks
@@ -47,9 +48,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="default seqrec_16k (forward) or decode_lm130m (decode)")
-    ap.add_argument("--mode", choices=["forward", "decode"], default="forward",
+    ap.add_argument("--mode", choices=["forward", "decode", "nonlinear"], default="forward",
                     help="forward: prism_forward over whole sequences (the headline); decode: one "
-                         "prism_decode_step (one token per sequence) over a serving batch")
+                         "prism_decode_step (one token per sequence) over a serving batch; nonlinear: "
+                         "prism_forward_nonlinear (the non-linear residual variant) over whole sequences")
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 portable fp32 kernels, 2 tensor-core path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -68,8 +70,10 @@ def load_peaks():
 
 # ------------------------------------------------------------------------------------------------
 # algorithmic work of the path, per (token, head)
-def alg_bytes_per_token_head(w):
+def alg_bytes_per_token_head(w, nonlinear=False):
     io = 2 if w.dtype == "bf16" else 4
+    if nonlinear:  # gains p (R dv, io dtype) in place of eta
+        return io * (2 * w.dk + 2 * w.dv + w.R * w.dk + w.R * w.dv) + 4 * (2 + w.R)
     return io * (2 * w.dk + 2 * w.dv + w.R * w.dk) + 4 * (2 + 2 * w.R)
 
 
@@ -78,7 +82,7 @@ def alg_flops_per_token_head(w):
     return 2 * w.dk * w.dv * (w.L + 3)
 
 
-def kernel_alg_bytes(name, w):
+def kernel_alg_bytes(name, w, nonlinear=False):
     """Bytes a kernel must move at minimum (each of its inputs read once, each output written
     once), for one launch over the whole workload."""
     io = 2 if w.dtype == "bf16" else 4
@@ -96,13 +100,16 @@ def kernel_alg_bytes(name, w):
     W = th * w.dk * 4
     Up = Vt = th * w.dv * 4
     S0 = chunks * w.dv * w.dk * 4
+    p_or_eta = th * R * w.dv * io if nonlinear else th * 4 * R
     table = {
-        "simt_prep": v + th * 4 * 2 * R + X,
+        "simt_prep": v + th * 4 * R + p_or_eta + X,
         "simt_chunk_solve": k + th * 8 + lam + Tm,
         "simt_wy": k + v + th * 4 + u + X + lam + Tm + W + Up,
         "simt_state": k + u + X + lam + W + Up + S0 + Vt,
         "simt_out": q + k + u + X + lam + S0 + Vt + out,
     }
+    if nonlinear:
+        gates = th * 4 * (2 + R) + th * R * w.dv * io
     return table.get(name, q + k + v + u + gates + out)
 
 
@@ -236,7 +243,7 @@ def max_over_ranks(x, world):
     return _max(x, world, device="cuda")
 
 
-def oracle_sample(w, inp, seconds_target, nthreads):
+def oracle_sample(w, inp, seconds_target, nthreads, p_gain=None):
     """Time the oracle on the first Ts tokens of every sequence, Ts sized so the run takes
     about `seconds_target` seconds.  Returns (tokens/s, Ts, seconds)."""
     from oracle import prism_oracle
@@ -245,7 +252,8 @@ def oracle_sample(w, inp, seconds_target, nthreads):
         sub = {k: (v[:, :, :Ts] if hasattr(v, "shape") and k != "conv_w" else v) for k, v in inp.items()}
         t0 = time.perf_counter()
         prism_oracle.forward(sub["q"], sub["k"], sub["v"], sub["beta"], sub["alpha"], sub["u"], sub["gamma"],
-                             sub["eta"], sub["conv_w"], sub["L"], nthreads=nthreads)
+                             sub["eta"], sub["conv_w"], sub["L"], nthreads=nthreads,
+                             p_gain=None if p_gain is None else p_gain[:, :, :Ts])
         return time.perf_counter() - t0
 
     Ts = min(w.T, 256)
@@ -307,7 +315,7 @@ def run_ours(args, w):
 
     from ssm_sequence_layer_gb300 import binding as Bd
     from ssm_sequence_layer_gb300 import build as cuda_build
-    from ssm_sequence_layer_gb300.inputs import make_workload_inputs
+    from ssm_sequence_layer_gb300.inputs import make_gain, make_workload_inputs
 
     world, rank, local = dist_setup(args)
     if rank == 0:
@@ -320,10 +328,19 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
     plan = Bd.Plan.for_inputs(dev, path=args.path if args.path else None)
     flush = L2Flush()
+    nonlinear = args.mode == "nonlinear"
+    p_cpu = make_gain(w.B, w.H, w.T, w.L, w.dv, dtype=w.dtype, seed=0) if nonlinear else None
+    p_dev = p_cpu.cuda() if nonlinear else None
+
+    def forward(inputs, p):
+        if nonlinear:
+            plan.forward_nonlinear(inputs, p, out=out, stream=stream)
+        else:
+            plan.forward(inputs, out, stream)
 
     for _ in range(warm):
         flush()
-        plan.forward(dev, out, stream)
+        forward(dev, p_dev)
     torch.cuda.synchronize()
     plan.last_device_status()
 
@@ -336,7 +353,7 @@ def run_ours(args, w):
     for i in range(steps):  # the timed steps: no per-kernel events inside the forward
         flush()
         ev[i][0].record(stream)
-        plan.forward(dev, out, stream)
+        forward(dev, p_dev)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -350,7 +367,7 @@ def run_ours(args, w):
     launches = 0
     for i in range(steps):
         flush()
-        plan.forward(dev, out, stream)
+        forward(dev, p_dev)
         torch.cuda.synchronize()
         kt = plan.kernel_times()
         launches += len(kt)
@@ -368,10 +385,10 @@ def run_ours(args, w):
     tot = {n: sum(v) for n, v in per_kernel.items()}
     dom = max(tot, key=tot.get)
     dom_ms = tot[dom] / len(per_kernel[dom])
-    dom_bytes = kernel_alg_bytes(dom, w)
+    dom_bytes = kernel_alg_bytes(dom, w, nonlinear)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     hbm = float(peaks["hbm_gbs"])
-    path_bytes = alg_bytes_per_token_head(w) * w.B * w.H * w.T
+    path_bytes = alg_bytes_per_token_head(w, nonlinear) * w.B * w.H * w.T
     path_achieved = path_bytes / (ms_local / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": traffic_from_profiles(dom, w.name),
@@ -384,7 +401,35 @@ def run_ours(args, w):
 
     # end to end through the host entry point (pinned host buffers, copies inside the timed region)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and nonlinear:  # no host entry point: the inputs copied in, the output back
+        host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in inp_cpu.items() if k != "eta"}
+        host_p = p_cpu.pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = host_p.numel() * host_p.element_size() + sum(v.numel() * v.element_size() for v in host.values()
+                                                            if torch.is_tensor(v))
+        d2h = hout.numel() * hout.element_size()
+        dbuf = {k: (torch.empty_like(v, device="cuda") if torch.is_tensor(v) else v) for k, v in host.items()}
+        dbuf["eta"] = None
+        dp = torch.empty_like(host_p, device="cuda")
+        e2e_ms = []
+        for i in range(max(3, min(steps, 20)) + 2):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k, v in host.items():
+                if torch.is_tensor(v):
+                    dbuf[k].copy_(v, non_blocking=True)
+            dp.copy_(host_p, non_blocking=True)
+            forward(dbuf, dp)
+            hout.copy_(out, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                e2e_ms.append(a.elapsed_time(b))
+        e2e_ms_mean = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+        e2e = {"value": tokens_per_step * world / (e2e_ms_mean / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_mean}
+    elif not args.no_e2e:
         host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in inp_cpu.items()}
         hout = torch.empty_like(host["v"]).pin_memory()
         h2d = sum(v.numel() * v.element_size() for k, v in host.items()
@@ -408,14 +453,16 @@ def run_ours(args, w):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = cpu_threads(w)
-        v, Ts, dt = oracle_sample(w, inp_cpu, args.cpu_seconds, nthreads)
+        v, Ts, dt = oracle_sample(w, inp_cpu, args.cpu_seconds, nthreads,
+                                  p_gain=p_cpu.double().numpy() if nonlinear else None)
         cpu = {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
                "sample": f"fp64 oracle over the first {Ts} tokens of all {w.B * w.H} sequences ({dt:.1f} s)"}
     plan.close()
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warm,
+            "metric": NONLINEAR_METRIC if nonlinear else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": warm,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")},
@@ -589,6 +636,11 @@ def main():
         if args.impl == "reference":
             return run_decode_reference(args, w)
         return run_decode(args, w)
+    if args.mode == "nonlinear":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the forward and the decode step"}))
+            return 0
+        return run_ours(args, WORKLOADS[args.workload or "lm130m_layer"])
     w = WORKLOADS[args.workload or "seqrec_16k"]
     if args.impl == "reference":
         return run_reference(args, w)

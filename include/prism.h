@@ -176,6 +176,27 @@ PRISM_API prism_status prism_decode_step(prism_plan_t plan, const void *q, const
                                const float *gamma, const float *eta, const void *conv_w, int L,
                                void *v_hist, float *S, void *out, struct CUstream_st *stream);
 
+/*
+ * prism_forward_nonlinear -- the non-linear residual variant of the write path (notes on
+ * PRISM, section 2.3, "greedy residual subtraction"): a gain vector p_{t,l}, predicted from
+ * the anchor outside this library like the directions u_{t,l}, replaces GELU'(h_t), and each
+ * level takes a non-linear step off the residual:
+ *   r_{t,1} = e_t = v_t - GELU(h_t)
+ *   delta_{t,l} = GELU(p_{t,l} (.) r_{t,l}),   r_{t,l+1} = r_{t,l} - delta_{t,l}
+ *   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *         + sum_{l=1..R} gamma_{t,l} delta_{t,l} u_{t,l}^T,      o_t = S_t q_t
+ * Only the token-local injection factors differ from prism_forward.  Arguments as
+ * prism_forward_state, with p_gain [B,H,T,R,dv] in the io dtype (16-byte aligned; slot l-1
+ * holds level l) in place of eta, which this variant does not have.  With L = 1 it equals
+ * prism_forward_state.  The chain has no closed form, so it runs on the portable fp32
+ * kernels whatever the shape (PRISM_OPT_PATH = 2 returns PRISM_ERR_UNSUPPORTED).
+ */
+PRISM_API prism_status prism_forward_nonlinear(prism_plan_t plan, const void *q, const void *k, const void *v,
+                                     const float *beta, const float *alpha, const void *u,
+                                     const float *gamma, const void *p_gain, const void *conv_w, int L,
+                                     const void *v_hist, const float *S_init, void *out, float *S_final,
+                                     void *v_hist_out, struct CUstream_st *stream);
+
 /* Free the plan and its workspace.  NULL is accepted. */
 PRISM_API prism_status prism_plan_destroy(prism_plan_t plan);
 

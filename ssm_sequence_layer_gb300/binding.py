@@ -35,7 +35,7 @@ PRISM_OPT_OUT_DTYPE = 4
 EXPORTED = ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
             "prism_plan_destroy", "prism_workspace_bytes", "prism_plan_last_device_status",
             "prism_status_string", "prism_last_error_message", "prism_version", "prism_plan_kernel_times",
-            "prism_forward_noalloc", "prism_forward_state", "prism_decode_step")
+            "prism_forward_noalloc", "prism_forward_state", "prism_decode_step", "prism_forward_nonlinear")
 
 
 class prism_kernel_time(ctypes.Structure):
@@ -85,10 +85,11 @@ def lib():
             L.prism_forward_noalloc.restype = ctypes.c_int
             L.prism_forward_state.argtypes = fwd[:11] + [vp, f, vp, f, vp, vp]
             L.prism_decode_step.argtypes = fwd[:11] + [vp, f, vp, vp]
+            L.prism_forward_nonlinear.argtypes = fwd[:11] + [vp, f, vp, f, vp, vp]
             L.prism_plan_kernel_times.restype = ctypes.c_int
             for name in ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
                          "prism_plan_destroy", "prism_plan_last_device_status", "prism_forward_state",
-                         "prism_decode_step"):
+                         "prism_decode_step", "prism_forward_nonlinear"):
                 getattr(L, name).restype = ctypes.c_int
             _LIB = L
     return _LIB
@@ -179,6 +180,14 @@ def prism_forward_state(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, v_
                                             _addr(v_hist_out), _stream(stream)))
 
 
+def prism_forward_nonlinear(plan, q, k, v, beta, alpha, u, gamma, p_gain, conv_w, L, v_hist, S_init, out, S_final,
+                            v_hist_out, stream=None):
+    return _check(lib().prism_forward_nonlinear(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha),
+                                                _addr(u), _addr(gamma), _addr(p_gain), _addr(conv_w), int(L),
+                                                _addr(v_hist), _addr(S_init), _addr(out), _addr(S_final),
+                                                _addr(v_hist_out), _stream(stream)))
+
+
 def prism_decode_step(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, v_hist, S, out, stream=None):
     return _check(lib().prism_decode_step(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha),
                                           _addr(u), _addr(gamma), _addr(eta), _addr(conv_w), int(L),
@@ -259,6 +268,21 @@ class Plan:
         if out is None:
             out = torch.empty(inp["v"].shape, dtype=self._out_torch_dtype(), device=inp["v"].device)
         prism_forward_state(self.handle, *ts, v_hist, S_init, out, S_final, v_hist_out, stream)
+        return out
+
+    def forward_nonlinear(self, inp, p_gain, v_hist=None, S_init=None, S_final=None, v_hist_out=None, out=None,
+                          stream=None):
+        """The non-linear residual variant (see prism_forward_nonlinear): p_gain [B,H,T,R,dv] in
+        the io dtype takes the place of eta; the state arguments are those of forward_state."""
+        import torch
+        q, k, v, beta, alpha, u, gamma, _eta, conv_w, L = self._tensors(inp)
+        lv = L > 1
+        self._check_device((q, k, v, beta, alpha, u, gamma, conv_w, p_gain if lv else None, v_hist, S_init,
+                            S_final, v_hist_out), "prism_forward_nonlinear")
+        if out is None:
+            out = torch.empty(inp["v"].shape, dtype=self._out_torch_dtype(), device=inp["v"].device)
+        prism_forward_nonlinear(self.handle, q, k, v, beta, alpha, u, gamma, p_gain if lv else None, conv_w, L,
+                                v_hist, S_init, out, S_final, v_hist_out, stream)
         return out
 
     def decode_step(self, inp, v_hist, S, out=None, stream=None):

@@ -161,7 +161,12 @@ prism_status run_forward(prism_plan_s *p, const prism::ForwardArgs &a, struct CU
 {
     prism_status st = check_plan_device(p);
     if (st != PRISM_OK) return st;
-    const int path = resolve_path(p);
+    int path = resolve_path(p);
+    if (a.p_gain) {  // the non-linear residual chain runs on the portable kernels only
+        if (p->opt_path == 2)
+            return fail(PRISM_ERR_UNSUPPORTED, "the non-linear residual variant has no tensor-core path");
+        path = 1;
+    }
     if (path == 2 && !prism::tc_supported(p->shape, p->io))
         return fail(PRISM_ERR_UNSUPPORTED, "the tensor-core path takes bf16 io, dk = dv = 64 and L <= 4");
     if ((st = ensure_workspace(p, path)) != PRISM_OK) return st;
@@ -308,6 +313,32 @@ prism_status prism_forward_state(prism_plan_t p, const void *q, const void *k, c
     a.S_init = S_init;
     a.S_final = S_final;
     a.v_hist_out = v_hist_out;
+    return run_forward(p, a, stream);
+}
+
+prism_status prism_forward_nonlinear(prism_plan_t p, const void *q, const void *k, const void *v,
+                                     const float *beta, const float *alpha, const void *u, const float *gamma,
+                                     const void *p_gain, const void *conv_w, int L, const void *v_hist,
+                                     const float *S_init, void *out, float *S_final, void *v_hist_out,
+                                     struct CUstream_st *stream)
+{
+    if (!p) return fail(PRISM_ERR_INVALID_ARG, "plan is NULL");
+    const bool lvl = p->shape.R > 0;
+    if (lvl && !p_gain) return fail(PRISM_ERR_INVALID_ARG, "p_gain must not be NULL when L > 1");
+    // eta is not part of this variant: validate the rest as prism_forward does (gamma stands in
+    // for eta's null check)
+    prism_status st = check_forward_args(p, q, k, v, beta, alpha, u, gamma, lvl ? gamma : nullptr, conv_w, L, out);
+    if (st != PRISM_OK) return st;
+    const void *sp[] = {v_hist, S_init, S_final, v_hist_out, lvl ? p_gain : nullptr};
+    const char *sn[] = {"v_hist", "S_init", "S_final", "v_hist_out", "p_gain"};
+    for (int i = 0; i < 5; ++i)
+        if (sp[i] && !aligned(sp[i], 16)) return fail(PRISM_ERR_MISALIGNED, "%s is not 16-byte aligned", sn[i]);
+    prism::ForwardArgs a{q, k, v, u, conv_w, beta, alpha, gamma, nullptr, out};
+    a.v_hist = v_hist;
+    a.S_init = S_init;
+    a.S_final = S_final;
+    a.v_hist_out = v_hist_out;
+    a.p_gain = lvl ? p_gain : nullptr;
     return run_forward(p, a, stream);
 }
 

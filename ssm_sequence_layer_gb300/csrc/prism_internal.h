@@ -20,10 +20,11 @@ enum DeviceStatus : int {
     kDevTimeout = 2,  // a bounded wait expired
 };
 
-// Pointers of one forward call (device memory, layouts as in prism.h).  The last four carry a
-// sequence across calls and may be null: v_hist [BH][3][dv] (v_{-3}, v_{-2}, v_{-1}, io dtype),
-// S_init / S_final [BH][dv][dk] fp32, v_hist_out [BH][3][dv] (the last three tokens of
-// [v_hist; v]).
+// Pointers of one forward call (device memory, layouts as in prism.h).  v_hist .. v_hist_out
+// carry a sequence across calls and may be null: v_hist [BH][3][dv] (v_{-3}, v_{-2}, v_{-1}, io
+// dtype), S_init / S_final [BH][dv][dk] fp32, v_hist_out [BH][3][dv] (the last three tokens of
+// [v_hist; v]).  p_gain [BH][T][R][dv] (io dtype), when set, selects the non-linear residual
+// variant (portable path only; eta is then not read).
 struct ForwardArgs {
     const void *q, *k, *v, *u, *conv_w;
     const float *beta, *alpha, *gamma, *eta;
@@ -32,6 +33,7 @@ struct ForwardArgs {
     const float *S_init = nullptr;
     float *S_final = nullptr;
     void *v_hist_out = nullptr;
+    const void *p_gain = nullptr;
 };
 
 // Problem shape shared by all kernels.

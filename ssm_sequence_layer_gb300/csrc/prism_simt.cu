@@ -34,10 +34,13 @@ __device__ __forceinline__ void stf(__nv_bfloat16 *p, float x) { *p = __float2bf
 // ---------------------------------------------------------------------------------------------
 // Step a1: anchor, gain, residual and the closed-form residual chain -> X [BH][T][R][dv].
 // v_hist [BH][3][dv] (v_{-3}, v_{-2}, v_{-1}) supplies the window before the first token; null
-// means zeros.
+// means zeros.  With p_gain [BH][T][R][dv] the chain is the non-linear residual variant of the
+// notes on PRISM (section 2.3): delta_l = GELU(p_l r_l), x_l = gamma_l delta_l,
+// r_{l+1} = r_l - delta_l (eta is not read).
 template <typename io_t>
 __global__ void __launch_bounds__(NT) prep_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
                                                   const io_t *__restrict__ conv_w,
+                                                  const io_t *__restrict__ p_gain,
                                                   const float *__restrict__ gamma,
                                                   const float *__restrict__ eta, float *__restrict__ X,
                                                   int H, int T, int dv, int R)
@@ -62,6 +65,16 @@ __global__ void __launch_bounds__(NT) prep_kernel(const io_t *__restrict__ v, co
     const float *gm = gamma + ((size_t)bh * T + t) * R;
     const float *et = eta + ((size_t)bh * T + t) * R;
     float *xo = X + ((size_t)bh * T + t) * R * dv + c;
+    if (p_gain) {
+        const io_t *pg = p_gain + ((size_t)bh * T + t) * R * dv + c;
+        for (int l = 0; l < R; ++l) {
+            const float z = ldf(pg + (size_t)l * dv) * r;
+            const float d = z * (0.5f * erfcf(-z * 0.70710678118654752f));
+            xo[(size_t)l * dv] = gm[l] * d;
+            r -= d;
+        }
+        return;
+    }
     for (int l = 0; l < R; ++l) {
         xo[(size_t)l * dv] = gm[l] * g * r;
         if (l + 1 < R) r *= (1.f - et[l] * g);
@@ -470,8 +483,8 @@ static cudaError_t forward_t(const Shape &s, const ForwardArgs &a, const SimtWor
         const long long elems = (long long)s.T * s.dv;
         dim3 grid((unsigned)((elems + NT - 1) / NT), s.BH);
         tm.begin("simt_prep");
-        prep_kernel<io_t><<<grid, NT, 0, st>>>(v, (const io_t *)a.v_hist, cw, a.gamma, a.eta, w.X, s.H, s.T, s.dv,
-                                               s.R);
+        prep_kernel<io_t><<<grid, NT, 0, st>>>(v, (const io_t *)a.v_hist, cw, (const io_t *)a.p_gain, a.gamma, a.eta,
+                                               w.X, s.H, s.T, s.dv, s.R);
         tm.end();
     }
     tm.begin("simt_chunk_solve");

@@ -117,6 +117,16 @@ def make_workload_inputs(w: Workload | str, seed=0, **overrides):
     return make_inputs(**kw)
 
 
+def make_gain(B, H, T, L, dv, dtype="bf16", seed=0):
+    """Gains p [B,H,T,L-1,dv] of the non-linear residual variant: sigmoid(N(0, 1)), the range
+    of the gain GELU'(h) they stand in for, drawn from a generator of their own (seed + 7919)
+    so that the other inputs of a seed are unchanged; cast to the io dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 7919)
+    p = torch.sigmoid(torch.randn(B, H, T, max(L - 1, 0), dv, generator=g, dtype=torch.float32))
+    return p.to(TORCH_DTYPE[dtype])
+
+
 def select_heads(inp: dict, pairs):
     """Slice an input set down to the listed (b, h) pairs as a [1, len(pairs)] batch.
 
