@@ -362,19 +362,40 @@ __global__ void __launch_bounds__(NT) wy_kernel(const io_t *__restrict__ k, cons
 // and writes only its own rows, so S_final may be S_init.
 //
 // The block's VB x DK slice of S stays in registers: thread (rg, cg) holds rows RPT rg ..
-// RPT rg + RPT - 1 and columns 4 cg .. 4 cg + 3.  Per chunk, V~ = U' - W S0^T is formed in 2 x 2
-// tiles (token pair x row pair) from shared copies of W and S0, then S <- Gamma_C S0 +
-// (decayed V~)^T K and S += (decayed X_l)^T U_l, each an outer-product sweep over the chunk's
-// tokens reading one float4 of K (or U_l) and RPT decayed values per token.
+// RPT rg + RPT - 1 and columns 4 cg .. 4 cg + 3.  A chunk is a sequence of phases: the key phase
+// (V~ = U' - W S0^T in 2 x 2 tiles from shared copies of W and S0, then S <- Gamma_C S0 +
+// (decayed V~)^T K) and one phase per level (S += (decayed X_l)^T U_l), each an outer-product
+// sweep over the chunk's tokens.  The operands of the next phase (K or U_l, and U' or X_l) are
+// loaded into registers before the current sweep and parked in shared memory after it, so their
+// latency overlaps the sweep; only W is loaded at the phase that uses it.
 template <int DK>
 struct StateTile {
     static constexpr int LD = DK + 4;     // row stride (floats) of the shared tiles: 16-byte rows
     static constexpr int CG = DK / 4;     // column groups of 4
     static constexpr int RG = NT / CG;    // row groups
     static constexpr int RPT = VB / RG;   // rows per thread
-    static_assert(RPT * RG == VB && RPT >= 1, "row split");
-    static constexpr size_t SMEM = sizeof(float) * (2 * C * LD + VB * LD + C * VB + C);
+    static constexpr int PB = C * CG / NT;  // float4 groups of a [C x DK] tile per thread
+    static_assert(RPT * RG == VB && RPT >= 1 && PB * NT == C * CG && C * VB == 4 * NT, "splits");
+    static constexpr size_t SMEM = sizeof(float) * (2 * C * LD + VB * LD + 2 * C * VB + C);
 };
+
+template <typename io_t>
+struct Raw4;  // 4 io values as loaded from global memory
+template <>
+struct Raw4<float> {
+    using type = float4;
+};
+template <>
+struct Raw4<__nv_bfloat16> {
+    using type = uint2;
+};
+__device__ __forceinline__ float4 raw_to_f4(float4 r) { return r; }
+__device__ __forceinline__ float4 raw_to_f4(uint2 w)
+{
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
 
 template <typename io_t, int DK>
 __global__ void __launch_bounds__(NT) state_kernel(const io_t *__restrict__ k, const io_t *__restrict__ u,
@@ -384,22 +405,58 @@ __global__ void __launch_bounds__(NT) state_kernel(const io_t *__restrict__ k, c
                                                    const float *S_init, float *S_final, int T, int dv, int R, int NC)
 {
     using TL = StateTile<DK>;
-    constexpr int LD = TL::LD, CG = TL::CG, RPT = TL::RPT;
+    using raw_t = typename Raw4<io_t>::type;
+    constexpr int LD = TL::LD, CG = TL::CG, RPT = TL::RPT, PB = TL::PB;
     extern __shared__ __align__(16) float smem[];
     float *Ws = smem;             // C x LD   W of the chunk
     float *Ks = Ws + C * LD;      // C x LD   K, then U_l
     float *Ss = Ks + C * LD;      // VB x LD  S at the chunk start
     float *Vs = Ss + VB * LD;     // C x VB   decayed V~, then decayed X_l
-    float *lam = Vs + C * VB;     // C
+    float *Ups = Vs + C * VB;     // C x VB   U' of the block's rows
+    float *lam = Ups + C * VB;    // C
     const int bh = blockIdx.x, r0 = blockIdx.y * VB, tid = threadIdx.x;
     const int cg = tid % CG, rg = tid / CG;
     const int ip = tid >> 3, rp = tid & 7;  // V~ tile: tokens 2 ip, 2 ip + 1; rows 2 rp, 2 rp + 1
+    const int xi = tid >> 2, xq = tid & 3;  // this thread's float4 of a [C x VB] tile: row xi, columns 4 xq
 
     float4 s[RPT];
 #pragma unroll
     for (int r = 0; r < RPT; ++r)
         s[r] = S_init ? ld4(S_init + ((size_t)bh * dv + r0 + rg * RPT + r) * DK + 4 * cg) : make_float4(0.f, 0.f, 0.f, 0.f);
 
+    // operands of one phase in registers: ph = c (1 + R) + 1 + l, l = -1 for the key phase
+    raw_t pb[PB];
+    float4 px;
+    float pl = 0.f;
+    auto prefetch = [&](int ph) {
+        const int c = ph / (1 + R), l = ph % (1 + R) - 1;
+        if (c >= NC) return;
+        const int t0 = c * C, n = min(C, T - t0);
+        const io_t *src = (l < 0) ? k + ((size_t)bh * T + t0) * DK : u + (((size_t)bh * T + t0) * R + l) * DK;
+        const size_t stride = (l < 0) ? DK : (size_t)R * DK;
+#pragma unroll
+        for (int q = 0; q < PB; ++q) {
+            const int e = tid + q * NT, i = e / CG, m4 = e % CG;
+            if (i < n)
+                pb[q] = *reinterpret_cast<const raw_t *>(src + (size_t)i * stride + 4 * m4);
+            else
+                pb[q] = raw_t{};
+        }
+        if (l < 0) {
+            px = ld4(Up_ws + ((size_t)bh * NC * C + t0 + xi) * dv + r0 + 4 * xq);
+            if (tid < C) pl = lam_ws[(size_t)bh * T + t0 + min(tid, n - 1)];
+        } else {
+            px = (xi < n) ? ld4(X + (((size_t)bh * T + t0 + xi) * R + l) * dv + r0 + 4 * xq)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    auto park_b = [&]() {
+#pragma unroll
+        for (int q = 0; q < PB; ++q) {
+            const int e = tid + q * NT, i = e / CG, m4 = e % CG;
+            *reinterpret_cast<float4 *>(Ks + i * LD + 4 * m4) = raw_to_f4(pb[q]);
+        }
+    };
     // S += V^T B over the chunk's tokens (V in Vs, B in Ks)
     auto sweep = [&]() {
 #pragma unroll 4
@@ -415,19 +472,16 @@ __global__ void __launch_bounds__(NT) state_kernel(const io_t *__restrict__ k, c
             }
         }
     };
-    // rows i < n of an io-dtype [.. x DK] operand into Ks (zeros below)
-    auto load_b = [&](const io_t *src, size_t stride, int n) {
-        for (int e = tid; e < C * CG; e += NT) {
-            const int i = e / CG, m4 = e % CG;
-            const float4 v = (i < n) ? ld4(src + (size_t)i * stride + 4 * m4) : make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4 *>(Ks + i * LD + 4 * m4) = v;
-        }
-    };
 
+    prefetch(0);
+    int ph = 0;
     for (int c = 0; c < NC; ++c) {
         const int t0 = c * C;
         const int n = min(C, T - t0);
-        __syncthreads();  // the previous chunk's readers of the shared tiles are done
+        __syncthreads();  // the previous sweep is done: the shared tiles are free
+        park_b();
+        *reinterpret_cast<float4 *>(Ups + xi * VB + 4 * xq) = px;
+        if (tid < C) lam[tid] = pl;
         float *s0 = S0_ws + ((size_t)bh * NC + c) * dv * DK;
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
@@ -436,13 +490,13 @@ __global__ void __launch_bounds__(NT) state_kernel(const io_t *__restrict__ k, c
             *reinterpret_cast<float4 *>(Ss + row * LD + 4 * cg) = s[r];
         }
         const float *wb = W_ws + ((size_t)bh * NC * C + t0) * DK;
-        for (int e = tid; e < C * CG; e += NT) {
-            const int i = e / CG, m4 = e % CG;
+#pragma unroll
+        for (int q = 0; q < PB; ++q) {
+            const int e = tid + q * NT, i = e / CG, m4 = e % CG;
             *reinterpret_cast<float4 *>(Ws + i * LD + 4 * m4) = ld4(wb + (size_t)i * DK + 4 * m4);
         }
-        load_b(k + ((size_t)bh * T + t0) * DK, DK, n);
-        if (tid < C) lam[tid] = lam_ws[(size_t)bh * T + t0 + min(tid, n - 1)];
         __syncthreads();
+        prefetch(++ph);  // the first level (or the next chunk's key phase)
         const float lam_last = lam[C - 1];
         {  // V~ = U' - W S0^T, and its decayed copy for the state update
             float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
@@ -460,10 +514,9 @@ __global__ void __launch_bounds__(NT) state_kernel(const io_t *__restrict__ k, c
 #pragma unroll
             for (int di = 0; di < 2; ++di) {
                 const int i = 2 * ip + di;
-                const size_t o = ((size_t)bh * NC * C + t0 + i) * dv + r0 + 2 * rp;
-                const float2 up = *reinterpret_cast<const float2 *>(Up_ws + o);
+                const float2 up = *reinterpret_cast<const float2 *>(Ups + i * VB + 2 * rp);
                 const float2 vt = make_float2(up.x - acc[di][0], up.y - acc[di][1]);
-                *reinterpret_cast<float2 *>(Vt_ws + o) = vt;
+                *reinterpret_cast<float2 *>(Vt_ws + ((size_t)bh * NC * C + t0 + i) * dv + r0 + 2 * rp) = vt;
                 const float f = (i < n) ? expf(lam_last - lam[i]) : 0.f;
                 Vs[i * VB + 2 * rp] = vt.x * f;
                 Vs[i * VB + 2 * rp + 1] = vt.y * f;
@@ -481,12 +534,13 @@ __global__ void __launch_bounds__(NT) state_kernel(const io_t *__restrict__ k, c
         sweep();
         for (int l = 0; l < R; ++l) {
             __syncthreads();
-            load_b(u + (((size_t)bh * T + t0) * R + l) * DK, (size_t)R * DK, n);
-            for (int e = tid; e < C * VB; e += NT) {
-                const int i = e / VB, r = e % VB;
-                Vs[e] = (i < n) ? X[(((size_t)bh * T + t0 + i) * R + l) * dv + r0 + r] * expf(lam_last - lam[i]) : 0.f;
+            park_b();
+            {
+                const float f = (xi < n) ? expf(lam_last - lam[xi]) : 0.f;
+                *reinterpret_cast<float4 *>(Vs + xi * VB + 4 * xq) = make_float4(px.x * f, px.y * f, px.z * f, px.w * f);
             }
             __syncthreads();
+            prefetch(++ph);
             sweep();
         }
     }
