@@ -375,6 +375,36 @@ def run_ours(args, w):
             per_kernel.setdefault(name, []).append(ms)
     plan.set_option(Bd.PRISM_OPT_TIMING, 0)
     plan.last_device_status()
+
+    # the same forward replayed from a CUDA graph (L2 flushed before each replay, outside the
+    # graph), and back-to-back forwards with a warm L2 -- reported beside the main figure
+    graph_ms = None
+    if not nonlinear:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.forward(dev, out, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        gms = []
+        for i in range(steps + 3):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                gms.append(a.elapsed_time(b))
+        plan.last_device_status()
+        graph_ms = {"mean": sum(gms) / len(gms), "median": statistics.median(gms)}
+        del g
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    forward(dev, p_dev)
+    a.record(stream)
+    for _ in range(steps):
+        forward(dev, p_dev)
+    b.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = a.elapsed_time(b) / steps
     ms_local = sum(step_ms) / steps
     ms = max_over_ranks(ms_local, world)
     tokens_per_step = w.B * w.T
@@ -471,6 +501,7 @@ def run_ours(args, w):
             "roofline": roofline, "path_roofline": path_roofline, "kernels": kernels,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+            "graph_ms_per_step": graph_ms, "warm_l2_ms_per_step": warm_ms,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

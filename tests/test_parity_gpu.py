@@ -196,6 +196,25 @@ def test_bf16_output_is_the_rounded_fp32_output(path, segments):
     assert torch.equal(o16, o32.to(torch.bfloat16))
 
 
+@pytest.mark.parametrize("path", [1, 2])
+def test_forward_replays_from_a_cuda_graph(path):
+    """The forward is capturable (no allocation, synchronisation or host read inside): a graph
+    replay writes bit for bit the output of a direct call."""
+    inp = make_inputs(1, 2, 600, 64, 64, 3, dtype="bf16", seed=33)
+    d = to_device(inp)
+    with B.Plan.for_inputs(d, path=path) as p:
+        ref = p.forward(d)
+        out = torch.zeros_like(ref)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            p.forward(d, out, torch.cuda.current_stream())
+        g.replay()
+        torch.cuda.synchronize()
+        p.last_device_status()
+    assert torch.equal(out, ref)
+
+
 def test_host_entry_point_matches_device_entry_point():
     inp = make_inputs(1, 2, 200, 64, 64, 3, dtype="bf16", seed=12)
     d = to_device(inp)
