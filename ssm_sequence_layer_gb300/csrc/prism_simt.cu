@@ -737,27 +737,18 @@ __global__ void __launch_bounds__(NT) out_kernel(const io_t *__restrict__ q, con
 }
 
 // ---------------------------------------------------------------------------------------------
-struct Smem {
-    size_t solve, wy, state, out;
-};
-
-static Smem smem_bytes(int dk, int dv)
-{
-    const size_t ldk = dk + 1, ldv = dv + 1, ldc = C + 1;
-    Smem s;
-    s.solve = sizeof(float) * (C * ldk + 2 * C * ldc + 2 * C);
-    s.wy = sizeof(float) * (C * ldc + 2 * C * ldk + C * ldv + C * ldc + 2 * C);
-    s.state = dk == 64 ? StateTile<64>::SMEM : StateTile<128>::SMEM;
-    s.out = sizeof(float) * (2 * C * ldk + C * ldc + (dv * ldk > C * ldv ? dv * ldk : C * ldv) + C);
-    return s;
-}
+// dynamic shared memory of the chunk-solve kernel (the product kernels size theirs with their
+// tile structs)
+static size_t solve_smem_bytes(int dk) { return sizeof(float) * (C * (dk + 1) + 2 * C * (C + 1) + 2 * C); }
 
 template <typename io_t>
 static cudaError_t prepare_t(int dk, int dv)
 {
-    const Smem s = smem_bytes(dk, dv);
+    (void)dv;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(chunk_solve_kernel<io_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s.solve))) return e;
+    if ((e = cudaFuncSetAttribute(chunk_solve_kernel<io_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)solve_smem_bytes(dk))))
+        return e;
 #define PRISM_WY_ATTR(DK_, DV_)                                                                                   \
     if ((e = cudaFuncSetAttribute(wy_kernel<io_t, DK_, DV_>, cudaFuncAttributeMaxDynamicSharedMemorySize,              \
                                   (int)WyTile<DK_, DV_>::SMEM)))                                                       \
@@ -792,7 +783,6 @@ template <typename io_t, typename out_t>
 static cudaError_t forward_t(const Shape &s, const ForwardArgs &a, const SimtWorkspace &w, KernelTimer &tm)
 {
     cudaStream_t st = tm.stream;
-    const Smem sm = smem_bytes(s.dk, s.dv);
     const io_t *q = (const io_t *)a.q, *k = (const io_t *)a.k, *v = (const io_t *)a.v;
     const io_t *u = (const io_t *)a.u, *cw = (const io_t *)a.conv_w;
     out_t *out = (out_t *)a.out;
@@ -805,7 +795,7 @@ static cudaError_t forward_t(const Shape &s, const ForwardArgs &a, const SimtWor
         tm.end();
     }
     tm.begin("simt_chunk_solve");
-    chunk_solve_kernel<io_t><<<dim3(s.NC, s.BH), NT, sm.solve, st>>>(k, a.beta, a.alpha, w.lam, w.Tm, s.T, s.dk, s.NC);
+    chunk_solve_kernel<io_t><<<dim3(s.NC, s.BH), NT, solve_smem_bytes(s.dk), st>>>(k, a.beta, a.alpha, w.lam, w.Tm, s.T, s.dk, s.NC);
     tm.end();
     tm.begin("simt_wy");
     {
