@@ -48,10 +48,11 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="default seqrec_16k (forward) or decode_lm130m (decode)")
-    ap.add_argument("--mode", choices=["forward", "decode", "nonlinear"], default="forward",
+    ap.add_argument("--mode", choices=["forward", "decode", "nonlinear", "project"], default="forward",
                     help="forward: prism_forward over whole sequences (the headline); decode: one "
                          "prism_decode_step (one token per sequence) over a serving batch; nonlinear: "
-                         "prism_forward_nonlinear (the non-linear residual variant) over whole sequences")
+                         "prism_forward_nonlinear (the non-linear residual variant) over whole sequences; "
+                         "project: prism_project (the block's input projections)")
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 portable fp32 kernels, 2 tensor-core path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -115,6 +116,7 @@ def kernel_alg_bytes(name, w, nonlinear=False):
 
 # the source files each kernel is built from (its own translation unit and the headers it uses)
 KERNEL_SOURCES = {
+    "project": ("prism_project.cu", "prism_project.h", "tc_ptx.h", "prism_internal.h"),
     "tc_": ("prism_tc.cu", "tc_ptx.h", "prism_internal.h"),
     "decode": ("prism_state.cu", "tc_ptx.h", "prism_internal.h"),
     "simt_": ("prism_simt.cu", "prism_internal.h"),
@@ -659,6 +661,102 @@ def run_decode(args, w):
     return 0
 
 
+PROJECT_METRIC = "PRISM input projections tokens/s (ShortConv + basis/gain/gate GEMM) + % of roofline"
+
+
+def run_project(args, name):
+    import torch
+
+    from ssm_sequence_layer_gb300 import binding as Bd
+    from ssm_sequence_layer_gb300 import build as cuda_build
+    from ssm_sequence_layer_gb300.inputs import PROJECTION_WORKLOADS, make_projection_inputs
+
+    world, rank, local = dist_setup(args)
+    if rank == 0:
+        cuda_build.build()
+    barrier(world)
+    cfg = PROJECTION_WORKLOADS[name]
+    B_, T, D, H, R, dk, dv = (cfg[k] for k in ("B", "T", "D", "H", "R", "dk", "dv"))
+    N = H * R * (dk + dv + 1)
+    steps, warm = args.steps, max(args.warmup, 3)
+    pi = make_projection_inputs(B_, T, D, H, R, dk, dv, seed=0)
+    X, cw, W = pi["X"].cuda(), pi["conv_x"].cuda(), pi["W"].cuda()
+    plan = Bd.Plan(B_, H, T, dk, dv, R + 1, io="bf16")
+    out = (torch.empty(B_, H, T, R, dk, dtype=torch.bfloat16, device="cuda"),
+           torch.empty(B_, H, T, R, dv, dtype=torch.bfloat16, device="cuda"),
+           torch.empty(B_, H, T, R, dtype=torch.float32, device="cuda"))
+    stream = torch.cuda.current_stream()
+    flush = L2Flush()
+    for _ in range(warm):
+        flush()
+        plan.project(X, cw, W, out, stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        plan.project(X, cw, W, out, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    plan.last_device_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_local = sum(step_ms) / steps
+    ms = max_over_ranks(ms_local, world)
+    tokens = B_ * T
+    value = tokens * world / (ms / 1e3)
+    peaks, peak_kind = load_peaks()
+    flops = 2.0 * tokens * D * N
+    alg_bytes = 2 * tokens * D + 2 * N * D + 8 * D + tokens * H * R * (2 * dk + 2 * dv + 4)
+    t_hbm = alg_bytes / (float(peaks["hbm_gbs"]) * 1e9)
+    t_tc = flops / (float(peaks["bf16_tflops"]) * 1e12)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    if bound == "tensor":
+        ach = flops / (ms_local / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                "frac": ach / float(peaks["bf16_tflops"]), "peak_source": f"{peak_kind} bf16_tflops"}
+    else:
+        ach = alg_bytes / (ms_local / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "frac": ach / float(peaks["hbm_gbs"]), "peak_source": f"{peak_kind} hbm_gbs"}
+    roof.update(kernel="project", traffic=traffic_from_profiles("project", name), alg_bytes_per_launch=alg_bytes,
+                alg_flops_per_launch=flops, kernel_ms=ms_local,
+                hbm_frac=alg_bytes / (ms_local / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+                tensor_frac=flops / (ms_local / 1e3) / 1e12 / float(peaks["bf16_tflops"]))
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import prism_projection
+        Ts = min(T, 512)
+        sub = pi["X"][:, :Ts]
+        t0 = time.perf_counter()
+        prism_projection.project(sub, pi["conv_x"], pi["W"], H, R, dk, dv)
+        dt = time.perf_counter() - t0
+        cpu = {"value": B_ * Ts / dt, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"numpy fp64 oracle over the first {Ts} tokens of all {B_} sequences ({dt:.2f} s)"}
+    plan.close()
+    if rank == 0:
+        line = {
+            "metric": PROJECT_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": name, **cfg, "N": N, "l2": L2Flush.DESCRIPTION,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": None, "gpu_launches": steps, "clocks": clocks,
+            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     from ssm_sequence_layer_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
@@ -667,6 +765,11 @@ def main():
         if args.impl == "reference":
             return run_decode_reference(args, w)
         return run_decode(args, w)
+    if args.mode == "project":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the forward and the decode step"}))
+            return 0
+        return run_project(args, args.workload or "project_lm130m")
     if args.mode == "nonlinear":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the forward and the decode step"}))

@@ -197,6 +197,32 @@ PRISM_API prism_status prism_forward_nonlinear(prism_plan_t plan, const void *q,
                                      const void *v_hist, const float *S_init, void *out, float *S_final,
                                      void *v_hist_out, struct CUstream_st *stream);
 
+/*
+ * prism_project -- the block's input projections that produce the recurrence's directions,
+ * gains and step gates from the layer input (notes on PRISM, section 2.3, "Input-Anchored
+ * Simulation": a short causal convolution over the input gives the anchor; per refinement
+ * level, projections of the anchor give the basis k^(l), the gain p^(l) and the gate
+ * beta^(l)).  Per batch b and token t:
+ *   a_t = sum_{j=0..3} conv_x[j] (.) X_{t-j}     (depthwise, zero before t = 0)
+ *   y   = W a_t                                  W [N,D], N = H R dk + H R dv + H R
+ *   u_{t,l}     (head h) = the dk entries of basis row block (h, l) of y, divided by their norm
+ *                          (0 if the norm is 0)
+ *   p_{t,l}     (head h) = the dv entries of gain row block (h, l) of y
+ *   gamma_{t,l} (head h) = sigmoid(gate row (h, l) of y)
+ * The rows of W are ordered: the basis rows (h, l, c) for c < dk, then the gain rows (h, l, c)
+ * for c < dv, then the H R gate rows (h, l).  The outputs are the u, p (prism_forward_nonlinear's
+ * gains) and gamma inputs of the recurrence.
+ *   X [B,T,D] bf16, conv_x [4,D] bf16, W [N,D] bf16 (inputs)
+ *   u [B,H,T,R,dk] bf16, p [B,H,T,R,dv] bf16, gamma [B,H,T,R] float32 (outputs)
+ * Sizes B, H, T, dk, dv and R = L - 1 (at least 1) come from the plan, which must have bf16
+ * io; D is a multiple of 64.  All pointers are device pointers, 16-byte aligned (gamma: 4).
+ * The anchor enters the tensor cores rounded to bf16; products accumulate in fp32.  Returns
+ * once the work is enqueued on `stream`; an expired device-side wait is reported by
+ * prism_plan_last_device_status.
+ */
+PRISM_API prism_status prism_project(prism_plan_t plan, int D, const void *X, const void *conv_x, const void *W,
+                                     void *u, void *p, float *gamma, struct CUstream_st *stream);
+
 /* Free the plan and its workspace.  NULL is accepted. */
 PRISM_API prism_status prism_plan_destroy(prism_plan_t plan);
 

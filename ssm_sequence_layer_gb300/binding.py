@@ -35,7 +35,8 @@ PRISM_OPT_OUT_DTYPE = 4
 EXPORTED = ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
             "prism_plan_destroy", "prism_workspace_bytes", "prism_plan_last_device_status",
             "prism_status_string", "prism_last_error_message", "prism_version", "prism_plan_kernel_times",
-            "prism_forward_noalloc", "prism_forward_state", "prism_decode_step", "prism_forward_nonlinear")
+            "prism_forward_noalloc", "prism_forward_state", "prism_decode_step", "prism_forward_nonlinear",
+            "prism_project")
 
 
 class prism_kernel_time(ctypes.Structure):
@@ -86,10 +87,11 @@ def lib():
             L.prism_forward_state.argtypes = fwd[:11] + [vp, f, vp, f, vp, vp]
             L.prism_decode_step.argtypes = fwd[:11] + [vp, f, vp, vp]
             L.prism_forward_nonlinear.argtypes = fwd[:11] + [vp, f, vp, f, vp, vp]
+            L.prism_project.argtypes = [vp, i, vp, vp, vp, vp, vp, f, vp]
             L.prism_plan_kernel_times.restype = ctypes.c_int
             for name in ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
                          "prism_plan_destroy", "prism_plan_last_device_status", "prism_forward_state",
-                         "prism_decode_step", "prism_forward_nonlinear"):
+                         "prism_decode_step", "prism_forward_nonlinear", "prism_project"):
                 getattr(L, name).restype = ctypes.c_int
             _LIB = L
     return _LIB
@@ -188,6 +190,11 @@ def prism_forward_nonlinear(plan, q, k, v, beta, alpha, u, gamma, p_gain, conv_w
                                                 _addr(v_hist_out), _stream(stream)))
 
 
+def prism_project(plan, D, X, conv_x, W, u, p, gamma, stream=None):
+    return _check(lib().prism_project(plan, int(D), _addr(X), _addr(conv_x), _addr(W), _addr(u), _addr(p),
+                                      _addr(gamma), _stream(stream)))
+
+
 def prism_decode_step(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, v_hist, S, out, stream=None):
     return _check(lib().prism_decode_step(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha),
                                           _addr(u), _addr(gamma), _addr(eta), _addr(conv_w), int(L),
@@ -284,6 +291,22 @@ class Plan:
         prism_forward_nonlinear(self.handle, q, k, v, beta, alpha, u, gamma, p_gain if lv else None, conv_w, L,
                                 v_hist, S_init, out, S_final, v_hist_out, stream)
         return out
+
+    def project(self, X, conv_x, W, out=None, stream=None):
+        """The block's input projections (see prism_project): X [B,T,D], conv_x [4,D], W [N,D],
+        bf16 CUDA tensors; returns (u, p, gamma), allocated unless `out` gives them."""
+        import torch
+        self._check_device((X, conv_x, W), "prism_project")
+        B, H, T, dk, dv, L = self.shape
+        R = L - 1
+        if out is None:
+            dev = X.device
+            out = (torch.empty(B, H, T, R, dk, dtype=torch.bfloat16, device=dev),
+                   torch.empty(B, H, T, R, dv, dtype=torch.bfloat16, device=dev),
+                   torch.empty(B, H, T, R, dtype=torch.float32, device=dev))
+        u, p, gamma = out
+        prism_project(self.handle, X.shape[-1], X, conv_x, W, u, p, gamma, stream)
+        return u, p, gamma
 
     def decode_step(self, inp, v_hist, S, out=None, stream=None):
         """One token per sequence (see prism_decode_step): q, k [B,H,dk], v [B,H,dv], u [B,H,R,dk],

@@ -6,6 +6,7 @@
 #include <new>
 
 #include "prism_internal.h"
+#include "prism_project.h"
 
 namespace {
 
@@ -228,6 +229,7 @@ prism_status prism_plan(int B, int H, int T, int dk, int dv, int L, prism_dtype 
 
     cudaError_t e = prism::simt_prepare(s, io);
     if (e == cudaSuccess && prism::tc_supported(s, io)) e = prism::tc_prepare();
+    if (e == cudaSuccess && io == PRISM_BF16) e = prism::project_prepare();
     if (e != cudaSuccess) {
         delete p;
         return cuda_fail(e, "kernel attribute setup");
@@ -340,6 +342,31 @@ prism_status prism_forward_nonlinear(prism_plan_t p, const void *q, const void *
     a.v_hist_out = v_hist_out;
     a.p_gain = lvl ? p_gain : nullptr;
     return run_forward(p, a, stream);
+}
+
+prism_status prism_project(prism_plan_t p, int D, const void *X, const void *conv_x, const void *W, void *u,
+                           void *pg, float *gamma, struct CUstream_st *stream)
+{
+    if (!p) return fail(PRISM_ERR_INVALID_ARG, "plan is NULL");
+    if (p->io != PRISM_BF16) return fail(PRISM_ERR_UNSUPPORTED, "prism_project takes a bf16 plan");
+    if (p->shape.R < 1) return fail(PRISM_ERR_INVALID_ARG, "prism_project needs L >= 2 (at least one level)");
+    if (D < 64 || D % 64 != 0 || D > 65536)
+        return fail(PRISM_ERR_UNSUPPORTED, "D must be a multiple of 64 in [64, 65536] (got %d)", D);
+    if (!X || !conv_x || !W || !u || !pg || !gamma)
+        return fail(PRISM_ERR_INVALID_ARG, "X, conv_x, W, u, p and gamma must not be NULL");
+    const void *ap[] = {X, conv_x, W, u, pg};
+    const char *an[] = {"X", "conv_x", "W", "u", "p"};
+    for (int i = 0; i < 5; ++i)
+        if (!aligned(ap[i], 16)) return fail(PRISM_ERR_MISALIGNED, "%s is not 16-byte aligned", an[i]);
+    if (!aligned(gamma, 4)) return fail(PRISM_ERR_MISALIGNED, "gamma is not 4-byte aligned");
+    prism_status st = check_plan_device(p);
+    if (st != PRISM_OK) return st;
+    prism::ProjectArgs a{X, conv_x, W, u, pg, gamma};
+    p->timer.on = p->opt_timing != 0;
+    p->timer.reset((cudaStream_t)stream);
+    const cudaError_t e = prism::project_forward(p->shape, D, a, p->d_status, p->opt_wait_ns, p->timer);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return PRISM_OK;
 }
 
 prism_status prism_decode_step(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,

@@ -127,6 +127,27 @@ def make_gain(B, H, T, L, dv, dtype="bf16", seed=0):
     return p.to(TORCH_DTYPE[dtype])
 
 
+# The block's input projections: the layer input X [B,T,D] with D = H dk (the model width of the
+# head shapes above), feeding R = L - 1 levels.
+PROJECTION_WORKLOADS = {
+    "project_seqrec": dict(B=2, T=16384, D=256, H=4, R=3, dk=64, dv=64),
+    "project_lm130m": dict(B=8, T=2048, D=768, H=6, R=3, dk=128, dv=128),
+}
+
+
+def make_projection_inputs(B, T, D, H, R, dk, dv, seed=0):
+    """X ~ N(0, 1) [B,T,D], conv_x ~ N(0, 1/4) [4,D], W ~ N(0, 1/D) [N,D] with
+    N = H R (dk + dv + 1), drawn in that order from one generator, cast to bf16."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    N = H * R * (dk + dv + 1)
+    X = torch.randn(B, T, D, generator=g)
+    conv_x = torch.randn(4, D, generator=g) * 0.5
+    W = torch.randn(N, D, generator=g) / D ** 0.5
+    return {"X": X.to(torch.bfloat16), "conv_x": conv_x.to(torch.bfloat16), "W": W.to(torch.bfloat16),
+            "B": B, "T": T, "D": D, "H": H, "R": R, "dk": dk, "dv": dv}
+
+
 def select_heads(inp: dict, pairs):
     """Slice an input set down to the listed (b, h) pairs as a [1, len(pairs)] batch.
 

@@ -104,6 +104,8 @@ def test_null_plan_handling(lib):
     assert rc == B.PRISM_ERR_INVALID_ARG
     rc = lib.prism_decode_step(None, 16, 16, 16, 16, 16, None, None, None, 16, 1, 16, 16, 16, None)
     assert rc == B.PRISM_ERR_INVALID_ARG
+    rc = lib.prism_project(None, 64, 16, 16, 16, 16, 16, 16, None)
+    assert rc == B.PRISM_ERR_INVALID_ARG
     rc = lib.prism_forward_nonlinear(None, 16, 16, 16, 16, 16, None, None, None, 16, 1, None, None, 16, None,
                                      None, None)
     assert rc == B.PRISM_ERR_INVALID_ARG
