@@ -216,8 +216,10 @@ PRISM_API prism_status prism_forward_nonlinear(prism_plan_t plan, const void *q,
  *   u [B,H,T,R,dk] bf16, p [B,H,T,R,dv] bf16, gamma [B,H,T,R] float32 (outputs)
  * Sizes B, H, T, dk, dv and R = L - 1 (at least 1) come from the plan, which must have bf16
  * io; D is a multiple of 64.  All pointers are device pointers, 16-byte aligned (gamma: 4).
- * The anchor enters the tensor cores rounded to bf16; products accumulate in fp32.  Returns
- * once the work is enqueued on `stream`; an expired device-side wait is reported by
+ * The anchor enters the tensor cores rounded to bf16; products accumulate in fp32.  It is
+ * formed once into a scratch buffer owned by the plan (B T D 2 bytes, allocated by the first
+ * call that needs it, so make that call before capturing a stream).  Returns once the work is
+ * enqueued on `stream`; an expired device-side wait is reported by
  * prism_plan_last_device_status.
  */
 PRISM_API prism_status prism_project(prism_plan_t plan, int D, const void *X, const void *conv_x, const void *W,

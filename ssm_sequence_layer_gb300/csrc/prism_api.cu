@@ -361,7 +361,17 @@ prism_status prism_project(prism_plan_t p, int D, const void *X, const void *con
     if (!aligned(gamma, 4)) return fail(PRISM_ERR_MISALIGNED, "gamma is not 4-byte aligned");
     prism_status st = check_plan_device(p);
     if (st != PRISM_OK) return st;
-    prism::ProjectArgs a{X, conv_x, W, u, pg, gamma};
+    // the anchor a = ShortConv(X) goes through the plan's staging buffer (B T D bf16)
+    const size_t abytes = (size_t)p->shape.B * p->shape.T * D * 2;
+    if (p->stage_bytes < abytes) {
+        if (p->stage) cudaFree(p->stage);
+        p->stage = nullptr;
+        p->stage_bytes = 0;
+        cudaError_t e = cudaMalloc(&p->stage, abytes);
+        if (e != cudaSuccess) return cuda_fail(e, "anchor buffer allocation");
+        p->stage_bytes = abytes;
+    }
+    prism::ProjectArgs a{X, conv_x, W, u, pg, gamma, p->stage};
     p->timer.on = p->opt_timing != 0;
     p->timer.reset((cudaStream_t)stream);
     const cudaError_t e = prism::project_forward(p->shape, D, a, p->d_status, p->opt_wait_ns, p->timer);

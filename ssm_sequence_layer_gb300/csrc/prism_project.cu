@@ -11,14 +11,16 @@
 //   gamma_{t,l} (h) = sigmoid(column (h, l) of the gates)   -> gamma [B,H,T,R]     fp32
 // which are the directions, gains and step gates the recurrence takes.
 //
-// One CTA computes a 128-token x 128-column tile of Y: per 64-wide slice of D, TMA brings the
-// slice of X (with an 8-token halo, zero-filled before the sequence start) and of W; the threads
-// form the anchor slice in shared memory (bf16, 128-byte swizzled: the tensor core's A operand);
-// one thread issues four tcgen05.mma (M = 128, N = 128, K = 16) into a 128-column fp32
-// accumulator in tensor memory.  Two stages: the next slice's copies overlap the current
-// slice's convolution and products.  The epilogue (warps 0-3, one token row each) normalises
-// the basis columns, applies the gate's logistic and scatters the results into the head-major
-// layouts of the recurrence.  Every wait is bounded; an expired one is recorded in the status
+// Two kernels.  anchor_kernel forms a = ShortConv(X) once, in bf16 (the tensor core's operand
+// type), 8 channels per thread with 16-byte loads.  project_kernel computes a 128-token x
+// 128-column tile of Y = a W^T: per 64-wide slice of D, TMA brings the slices of a and W
+// (128-byte swizzled) into a ring of STAGES stages and one thread issues four tcgen05.mma
+// (M = 128, N = 128, K = 16) into a 128-column fp32 accumulator in tensor memory.  The epilogue
+// (each warp a 32-token lane quarter and one 64-column half) normalises the basis columns,
+// applies the gate's logistic and scatters the results into the head-major layouts of the
+// recurrence.  (Forming the anchor inside the product kernel repeats the convolution for every
+// one of the N / 128 column tiles; measured, that made the product kernel instruction- and
+// latency-bound.)  Every wait is bounded; an expired one is recorded in the status
 // word and the CTA drains its copies and products before it releases tensor memory.
 #include <cudaTypedefs.h>
 
@@ -30,18 +32,14 @@ namespace proj {
 
 using namespace prism::tc;
 
-constexpr int PM = 128, PN = 128, PK = 64, THREADS = 256, STAGES = 2;
-constexpr int XROWS = PM + 8;                    // 8-token halo (the window needs 3)
-constexpr uint32_t TILE = PM * PK * 2;           // 16 KB: a 128 x 64 bf16 operand tile
-constexpr uint32_t XBYTES = XROWS * PK * 2;      // 17 KB: the X slice, unswizzled rows of 128 B
-constexpr uint32_t OFF_A = 0;                    // [STAGES] anchor tiles (SW128)
+constexpr int PM = 128, PN = 128, PK = 64, THREADS = 256, STAGES = 3;
+constexpr uint32_t TILE = PM * PK * 2;             // 16 KB: a 128 x 64 bf16 operand tile
+constexpr uint32_t OFF_A = 0;                      // [STAGES] anchor tiles (SW128, by TMA)
 constexpr uint32_t OFF_B = OFF_A + STAGES * TILE;  // [STAGES] W tiles (SW128, by TMA)
-constexpr uint32_t OFF_X = OFF_B + STAGES * TILE;  // [STAGES] X slices (by TMA)
-constexpr uint32_t SMEM = OFF_X + STAGES * XBYTES + 1024;  // + alignment slack
-static_assert(OFF_B % 1024 == 0 && OFF_X % 1024 == 0 && XBYTES % 128 == 0, "layout");
+constexpr uint32_t SMEM = OFF_B + STAGES * TILE + 1024;  // + alignment slack: two CTAs per SM
+static_assert(OFF_B % 1024 == 0 && 2 * SMEM <= 232448, "layout");
 
 struct ProjParams {
-    const __nv_bfloat16 *conv;  // [4][D]
     __nv_bfloat16 *u, *p;
     float *gamma;
     int *status;
@@ -61,13 +59,43 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// a[b][t][d] = sum_j conv[j][d] X[b][t - j][d] (zero before t = 0), 8 channels per thread
+__global__ void __launch_bounds__(256) anchor_kernel(const __nv_bfloat16 *__restrict__ X,
+                                                     const __nv_bfloat16 *__restrict__ conv,
+                                                     __nv_bfloat16 *__restrict__ a, int T, int D, long long n8)
+{
+    const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= n8) return;
+    const int d8 = (int)(e % (D / 8)) * 8;
+    const long long row = e / (D / 8);  // b T + t
+    const int t = (int)(row % T);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (t - j < 0) break;
+        const uint4 xv = *reinterpret_cast<const uint4 *>(X + (row - j) * D + d8);
+        const uint4 wv = *reinterpret_cast<const uint4 *>(conv + (size_t)j * D + d8);
+        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+        const __nv_bfloat162 *w2 = reinterpret_cast<const __nv_bfloat162 *>(&wv);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 xf = __bfloat1622float2(x2[q]), wf = __bfloat1622float2(w2[q]);
+            acc[2 * q] = fmaf(wf.x, xf.x, acc[2 * q]);
+            acc[2 * q + 1] = fmaf(wf.y, xf.y, acc[2 * q + 1]);
+        }
+    }
+    *reinterpret_cast<uint4 *>(a + row * D + d8) =
+        make_uint4(pack_bf2(acc[0], acc[1]), pack_bf2(acc[2], acc[3]), pack_bf2(acc[4], acc[5]), pack_bf2(acc[6], acc[7]));
+}
+
 __global__ void __launch_bounds__(THREADS, 2)
-    project_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, ProjParams p)
+    project_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w, ProjParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint32_t tmem_base_s;
     __shared__ __align__(8) uint64_t full[STAGES], mmad[STAGES];
+    __shared__ float ssx[2][PM];  // sums of squares of the two 64-column halves, per token row
     __shared__ int abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x / p.tiles_t, t0 = (blockIdx.x % p.tiles_t) * PM, n0 = blockIdx.y * PN;
@@ -83,7 +111,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             mbar_init(smem_u32(&mmad[s]), 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_a);
         prefetch_tmap(&tm_w);
     }
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), PN);
@@ -92,13 +120,15 @@ __global__ void __launch_bounds__(THREADS, 2)
     fence_after_sync();
     const uint32_t tmem = tmem_base_s;
 
-    // thread 0's view of the copies and products in flight, for the drain after an expired wait
+    // thread 0's view of the copies and products in flight, for the drain after an expired wait;
+    // products complete in issue order, so waiting for product j waits the barrier phases of the
+    // products not yet seen, in order (each phase exactly once)
     int loads_issued = 0, loads_waited = 0, mmas_issued = 0, mmas_waited = 0;
-    auto issue = [&](int ks) {  // thread 0: the X and W slices of step ks into stage ks % STAGES
+    auto issue = [&](int ks) {  // thread 0: the a and W slices of step ks into stage ks % STAGES
         const int s = ks % STAGES;
         const uint32_t mb = smem_u32(&full[s]);
-        mbar_expect_tx(mb, XBYTES + TILE);
-        tma_load_3d(sbase + OFF_X + s * XBYTES, &tm_x, mb, ks * PK, t0 - 8, b);
+        mbar_expect_tx(mb, 2 * TILE);
+        tma_load_3d(sbase + OFF_A + s * TILE, &tm_a, mb, ks * PK, t0, b);
         asm volatile(
             "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
                 sbase + OFF_B + s * TILE),
@@ -106,58 +136,24 @@ __global__ void __launch_bounds__(THREADS, 2)
             : "memory");
         ++loads_issued;
     };
-    if (tid == 0) issue(0);
-
-    const int cp = tid & 31, rg = tid >> 5;  // convolution: column pair cp, rows rg + 8 r
-    for (int ks = 0; ks < KS; ++ks) {
-        const int s = ks % STAGES;
-        if (tid == 0) {
-            bool ok = true;
-            if (ks + 1 < KS) {
-                // stage s ^ 1 is free once the products of step ks - 1 have read it
-                if (ks >= 1) {
-                    ok = mbar_wait(smem_u32(&mmad[(ks - 1) % STAGES]), (uint32_t)(((ks - 1) / STAGES) & 1), p.wait_ns);
-                    if (ok) ++mmas_waited;
-                }
-                if (ok) issue(ks + 1);
-            }
-            if (ok) {
-                ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((ks / STAGES) & 1), p.wait_ns);
-                if (ok) ++loads_waited;
-            }
-            if (!ok) {
-                abort_s = 1;
-                atomicCAS(p.status, 0, kDevTimeout);
-            }
+    auto wait_mma_upto = [&](int j) -> bool {  // thread 0: products 0..j complete
+        while (mmas_waited <= j) {
+            const int k = mmas_waited;
+            if (!mbar_wait(smem_u32(&mmad[k % STAGES]), (uint32_t)((k / STAGES) & 1), p.wait_ns)) return false;
+            ++mmas_waited;
         }
-        __syncthreads();
-        if (abort_s) break;
-        // the anchor slice: A[i][c] = sum_j w_j[d0 + c] X[t0 + i - j][d0 + c]  (X row i + 8 - j of the slice)
-        {
-            const int d0 = ks * PK;
-            const __nv_bfloat162 *cw = reinterpret_cast<const __nv_bfloat162 *>(p.conv + d0) + cp;
-            const float2 w0 = __bfloat1622float2(cw[0]);
-            const float2 w1 = __bfloat1622float2(cw[p.D / 2]);
-            const float2 w2 = __bfloat1622float2(cw[2 * (p.D / 2)]);
-            const float2 w3 = __bfloat1622float2(cw[3 * (p.D / 2)]);
-            const __nv_bfloat162 *xs = reinterpret_cast<const __nv_bfloat162 *>(sm + OFF_X + s * XBYTES) + cp;
-            uint8_t *A = sm + OFF_A + s * TILE;
-#pragma unroll 4
-            for (int r = 0; r < PM / 8; ++r) {
-                const int i = rg + 8 * r;
-                const float2 x0 = __bfloat1622float2(xs[(i + 8) * 32]);
-                const float2 x1 = __bfloat1622float2(xs[(i + 7) * 32]);
-                const float2 x2 = __bfloat1622float2(xs[(i + 6) * 32]);
-                const float2 x3 = __bfloat1622float2(xs[(i + 5) * 32]);
-                const float a0 = fmaf(w0.x, x0.x, fmaf(w1.x, x1.x, fmaf(w2.x, x2.x, w3.x * x3.x)));
-                const float a1 = fmaf(w0.y, x0.y, fmaf(w1.y, x1.y, fmaf(w2.y, x2.y, w3.y * x3.y)));
-                *reinterpret_cast<uint32_t *>(A + sw128(i, 2 * cp)) = pack_bf2(a0, a1);
-            }
-        }
-        fence_async_smem();  // the anchor tile is read by the tensor core (async proxy)
-        fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
+        return true;
+    };
+    // the main loop runs on thread 0 alone: wait for a stage, issue its products, refill the stage
+    // the previous step's products have released
+    if (tid == 0) {
+        bool ok = true;
+        for (int k = 0; k < STAGES && k < KS; ++k) issue(k);
+        for (int ks = 0; ks < KS && ok; ++ks) {
+            const int s = ks % STAGES;
+            ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((ks / STAGES) & 1), p.wait_ns);
+            if (!ok) break;
+            ++loads_waited;
             fence_after_sync();
 #pragma unroll
             for (int j = 0; j < PK / 16; ++j)
@@ -165,50 +161,54 @@ __global__ void __launch_bounds__(THREADS, 2)
                         (ks > 0 || j > 0) ? 1u : 0u);
             mma_commit(smem_u32(&mmad[s]));
             ++mmas_issued;
+            if (ks >= 1 && ks - 1 + STAGES < KS) {  // stage of step ks - 1 -> step ks - 1 + STAGES
+                ok = wait_mma_upto(ks - 1);
+                if (ok) issue(ks - 1 + STAGES);
+            }
         }
-    }
-    // all products done (thread 0 waits for the last one), then the epilogue
-    if (tid == 0 && !abort_s && mmas_issued > 0) {
-        const int last = mmas_issued - 1;
-        if (mbar_wait(smem_u32(&mmad[last % STAGES]), (uint32_t)((last / STAGES) & 1), p.wait_ns))
-            mmas_waited = mmas_issued;
-        else {
+        if (!ok) {
             abort_s = 1;
             atomicCAS(p.status, 0, kDevTimeout);
         }
     }
+    // all products done (thread 0 waits for the last one), then the epilogue
+    if (tid == 0 && !abort_s && mmas_issued > 0 && !wait_mma_upto(mmas_issued - 1)) {
+        abort_s = 1;
+        atomicCAS(p.status, 0, kDevTimeout);
+    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (!abort_s && warp < 4) {
-        const int i = warp * 32 + lane, t = t0 + i;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    if (!abort_s) {
+        const int q = warp & 3, hf = warp >> 2;  // TMEM lane quarter (32 token rows), 64-column half
+        const int i = q * 32 + lane, t = t0 + i;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const int NU = p.H * p.R * p.dk, NP = p.H * p.R * p.dv;
         const bool live = t < p.T;
-        // sum of squares of each basis group in this tile (at most PN / 64 groups, 64-column aligned)
-        float ss[PN / 64] = {0.f, 0.f};
-        if (n0 < NU) {
+        const int nh = n0 + 64 * hf;  // first column of this half
+        float sq = 0.f;  // sum of squares of this half (used when it holds basis columns)
+        if (nh < NU) {
 #pragma unroll
-            for (int ch = 0; ch < PN / 32; ++ch) {
+            for (int ch = 0; ch < 2; ++ch) {
                 float v[32];
-                tmem_ld(tmem + lane_off + (uint32_t)(32 * ch), v);
-                float q = 0.f;
+                tmem_ld(tmem + lane_off + (uint32_t)(64 * hf + 32 * ch), v);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) q = fmaf(v[e], v[e], q);
-                ss[ch / 2] += q;
+                for (int e = 0; e < 32; ++e) sq = fmaf(v[e], v[e], sq);
             }
         }
+        ssx[hf][i] = sq;
+        __syncthreads();
+        // a basis group is one half (dk = 64) or the whole tile (dk = 128)
+        const float gsq = (p.dk == 64) ? sq : ssx[0][i] + ssx[1][i];
 #pragma unroll
-        for (int ch = 0; ch < PN / 32; ++ch) {
+        for (int ch = 0; ch < 2; ++ch) {
             float v[32];
-            tmem_ld(tmem + lane_off + (uint32_t)(32 * ch), v);
-            const int n = n0 + 32 * ch;
+            tmem_ld(tmem + lane_off + (uint32_t)(64 * hf + 32 * ch), v);
+            const int n = nh + 32 * ch;
             if (!live || n >= p.N) continue;
             if (n < NU) {  // basis: scale by 1 / ||y|| of its (h, l) group
                 const int g = n / p.dk, c = n % p.dk;
-                // the group's columns in this tile: dk = 64 -> one 64-column half; dk = 128 -> the whole tile
-                float q = (p.dk == 64) ? ss[ch / 2] : ss[0] + ss[1];
-                const float f = q > 0.f ? rsqrtf(q) : 0.f;
+                const float f = gsq > 0.f ? rsqrtf(gsq) : 0.f;
                 __nv_bfloat16 *dst = p.u + ((((size_t)b * p.H + g / p.R) * p.T + t) * p.R + g % p.R) * p.dk + c;
                 uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
@@ -280,12 +280,12 @@ cudaError_t project_forward(const Shape &s, int D, const ProjectArgs &a, int *d_
 {
     using namespace proj;
     const int N = s.H * s.R * (s.dk + s.dv + 1);
-    CUtensorMap mx, mw;
+    CUtensorMap ma, mw;
     {
         cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)s.T, (cuuint64_t)s.B};
         cuuint64_t str[2] = {(cuuint64_t)D * 2, (cuuint64_t)s.T * D * 2};
-        cuuint32_t box[3] = {PK, XROWS, 1};
-        if (!encode_bf16(&mx, a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+        cuuint32_t box[3] = {PK, PM, 1};
+        if (!encode_bf16(&ma, a.anchor, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)N};
@@ -294,7 +294,6 @@ cudaError_t project_forward(const Shape &s, int D, const ProjectArgs &a, int *d_
         if (!encode_bf16(&mw, a.W, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     ProjParams p;
-    p.conv = (const __nv_bfloat16 *)a.conv;
     p.u = (__nv_bfloat16 *)a.u;
     p.p = (__nv_bfloat16 *)a.p;
     p.gamma = a.gamma;
@@ -309,8 +308,16 @@ cudaError_t project_forward(const Shape &s, int D, const ProjectArgs &a, int *d_
     p.N = N;
     p.tiles_t = (s.T + PM - 1) / PM;
     const dim3 grid(s.B * p.tiles_t, (N + PN - 1) / PN);
+    const long long n8 = (long long)s.B * s.T * (D / 8);
+    tm.begin("anchor");
+    anchor_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, tm.stream>>>((const __nv_bfloat16 *)a.X,
+                                                                    (const __nv_bfloat16 *)a.conv,
+                                                                    (__nv_bfloat16 *)a.anchor, s.T, D, n8);
+    tm.end();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     tm.begin("project");
-    project_kernel<<<grid, THREADS, SMEM, tm.stream>>>(mx, mw, p);
+    project_kernel<<<grid, THREADS, SMEM, tm.stream>>>(ma, mw, p);
     tm.end();
     return cudaGetLastError();
 }

@@ -12,6 +12,7 @@ struct ProjectArgs {
     const void *W;     // [N,D] bf16, N = H R (dk + dv + 1)
     void *u, *p;       // [B,H,T,R,dk], [B,H,T,R,dv] bf16
     float *gamma;      // [B,H,T,R]
+    void *anchor;      // [B,T,D] bf16 scratch: the convolved input
 };
 
 cudaError_t project_prepare();
