@@ -32,7 +32,7 @@ namespace proj {
 
 using namespace prism::tc;
 
-constexpr int PM = 128, PN = 128, PK = 64, THREADS = 256, STAGES = 3;
+constexpr int PM = 128, PN = 128, PK = 64, STAGES = 3;
 constexpr uint32_t TILE = PM * PK * 2;             // 16 KB: a 128 x 64 bf16 operand tile
 constexpr uint32_t OFF_A = 0;                      // [STAGES] anchor tiles (SW128, by TMA)
 constexpr uint32_t OFF_B = OFF_A + STAGES * TILE;  // [STAGES] W tiles (SW128, by TMA)
@@ -44,7 +44,7 @@ struct ProjParams {
     float *gamma;
     int *status;
     unsigned long long wait_ns;
-    int T, D, H, R, dk, dv, N, tiles_t;
+    int T, D, H, R, dk, dv, N, tiles_t, tiles_bt;
 };
 
 // K-major 128B-swizzled operand at byte offset off: 16-byte core-matrix rows, 1024-byte 8-row groups
@@ -88,18 +88,27 @@ __global__ void __launch_bounds__(256) anchor_kernel(const __nv_bfloat16 *__rest
         make_uint4(pack_bf2(acc[0], acc[1]), pack_bf2(acc[2], acc[3]), pack_bf2(acc[4], acc[5]), pack_bf2(acc[6], acc[7]));
 }
 
-__global__ void __launch_bounds__(THREADS, 2)
+// Persistent product kernel: a CTA takes tiles round-robin (token-tile major, so CTAs running at
+// the same time share the anchor tile in L2).  Warp 0 (one thread) runs the main loop: TMA into
+// the ring, four MMAs per K-step into one of two accumulators in tensor memory, a commit on the
+// accumulator's "full" barrier after a tile's last step.  Warps 1-4 are the epilogue, one TMEM
+// lane quarter each (token rows), all 128 columns per thread: they wait for an accumulator,
+// drain it and release it on its "empty" barrier, so a tile's epilogue runs under the next
+// tile's products.
+constexpr int PTHREADS = 160;  // warp 0: main loop; warps 1-4: epilogue
+
+__global__ void __launch_bounds__(PTHREADS, 2)
     project_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w, ProjParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint32_t tmem_base_s;
-    __shared__ __align__(8) uint64_t full[STAGES], mmad[STAGES];
-    __shared__ float ssx[2][PM];  // sums of squares of the two 64-column halves, per token row
+    __shared__ __align__(8) uint64_t full[STAGES], mmad[STAGES], acc_full[2], acc_empty[2];
     __shared__ int abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x / p.tiles_t, t0 = (blockIdx.x % p.tiles_t) * PM, n0 = blockIdx.y * PN;
     const int KS = p.D / PK;
+    const int tiles_n = (p.N + PN - 1) / PN, ntiles = p.tiles_bt * tiles_n;
+    const int my_tiles = ntiles > (int)blockIdx.x ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const uint32_t sbase = smem_u32(sm);
     const uint64_t dbase = sdesc(sbase, 0, 0);
     const uint32_t idesc = idesc_bf16(PM, PN, 0, 0);
@@ -110,132 +119,152 @@ __global__ void __launch_bounds__(THREADS, 2)
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&mmad[s]), 1);
         }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&acc_full[s]), 1);
+            mbar_init(smem_u32(&acc_empty[s]), 4);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tm_a);
         prefetch_tmap(&tm_w);
     }
-    if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), PN);
+    if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 2 * PN);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = tmem_base_s;
 
-    // thread 0's view of the copies and products in flight, for the drain after an expired wait;
-    // products complete in issue order, so waiting for product j waits the barrier phases of the
-    // products not yet seen, in order (each phase exactly once)
+    // thread 0's view of the copies and products in flight (for the drain after an expired wait)
     int loads_issued = 0, loads_waited = 0, mmas_issued = 0, mmas_waited = 0;
-    auto issue = [&](int ks) {  // thread 0: the a and W slices of step ks into stage ks % STAGES
-        const int s = ks % STAGES;
-        const uint32_t mb = smem_u32(&full[s]);
-        mbar_expect_tx(mb, 2 * TILE);
-        tma_load_3d(sbase + OFF_A + s * TILE, &tm_a, mb, ks * PK, t0, b);
-        asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-                sbase + OFF_B + s * TILE),
-            "l"((uint64_t)&tm_w), "r"(mb), "r"(ks * PK), "r"(n0)
-            : "memory");
-        ++loads_issued;
-    };
-    auto wait_mma_upto = [&](int j) -> bool {  // thread 0: products 0..j complete
-        while (mmas_waited <= j) {
-            const int k = mmas_waited;
-            if (!mbar_wait(smem_u32(&mmad[k % STAGES]), (uint32_t)((k / STAGES) & 1), p.wait_ns)) return false;
-            ++mmas_waited;
-        }
-        return true;
-    };
-    // the main loop runs on thread 0 alone: wait for a stage, issue its products, refill the stage
-    // the previous step's products have released
     if (tid == 0) {
+        // global step g = tile i * KS + ks; stage g % STAGES
+        const int total = my_tiles * KS;
+        auto tile_of = [&](int i, int &b, int &t0, int &n0) {
+            const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+            const int bt = tile / tiles_n;
+            n0 = (tile % tiles_n) * PN;
+            b = bt / p.tiles_t;
+            t0 = (bt % p.tiles_t) * PM;
+        };
+        auto issue = [&](int g) {
+            int b, t0, n0;
+            tile_of(g / KS, b, t0, n0);
+            const int ks = g % KS, s = g % STAGES;
+            const uint32_t mb = smem_u32(&full[s]);
+            mbar_expect_tx(mb, 2 * TILE);
+            tma_load_3d(sbase + OFF_A + s * TILE, &tm_a, mb, ks * PK, t0, b);
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+                    sbase + OFF_B + s * TILE),
+                "l"((uint64_t)&tm_w), "r"(mb), "r"(ks * PK), "r"(n0)
+                : "memory");
+            ++loads_issued;
+        };
+        auto wait_mma_upto = [&](int j) -> bool {  // products 0..j complete (each phase waited once, in order)
+            while (mmas_waited <= j) {
+                const int k = mmas_waited;
+                if (!mbar_wait(smem_u32(&mmad[k % STAGES]), (uint32_t)((k / STAGES) & 1), p.wait_ns)) return false;
+                ++mmas_waited;
+            }
+            return true;
+        };
         bool ok = true;
-        for (int k = 0; k < STAGES && k < KS; ++k) issue(k);
-        for (int ks = 0; ks < KS && ok; ++ks) {
-            const int s = ks % STAGES;
-            ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((ks / STAGES) & 1), p.wait_ns);
+        for (int g = 0; g < STAGES && g < total; ++g) issue(g);
+        for (int g = 0; g < total && ok; ++g) {
+            const int i = g / KS, ks = g % KS, s = g % STAGES, buf = i & 1;
+            if (ks == 0 && i >= 2) {  // the accumulator's previous tile (i - 2) has been drained
+                ok = mbar_wait(smem_u32(&acc_empty[buf]), (uint32_t)(((i - 2) / 2) & 1), p.wait_ns);
+                if (!ok) break;
+            }
+            ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((g / STAGES) & 1), p.wait_ns);
             if (!ok) break;
             ++loads_waited;
             fence_after_sync();
 #pragma unroll
             for (int j = 0; j < PK / 16; ++j)
-                mma_f16(tmem, op_desc(dbase, OFF_A + s * TILE + j * 32), op_desc(dbase, OFF_B + s * TILE + j * 32), idesc,
-                        (ks > 0 || j > 0) ? 1u : 0u);
+                mma_f16(tmem + buf * PN, op_desc(dbase, OFF_A + s * TILE + j * 32), op_desc(dbase, OFF_B + s * TILE + j * 32),
+                        idesc, (ks > 0 || j > 0) ? 1u : 0u);
             mma_commit(smem_u32(&mmad[s]));
+            if (ks == KS - 1) mma_commit(smem_u32(&acc_full[buf]));  // the tile's products are in the accumulator
             ++mmas_issued;
-            if (ks >= 1 && ks - 1 + STAGES < KS) {  // stage of step ks - 1 -> step ks - 1 + STAGES
-                ok = wait_mma_upto(ks - 1);
-                if (ok) issue(ks - 1 + STAGES);
+            if (g >= 1 && g - 1 + STAGES < total) {  // stage of step g - 1 -> step g - 1 + STAGES
+                ok = wait_mma_upto(g - 1);
+                if (ok) issue(g - 1 + STAGES);
             }
         }
         if (!ok) {
             abort_s = 1;
             atomicCAS(p.status, 0, kDevTimeout);
         }
-    }
-    // all products done (thread 0 waits for the last one), then the epilogue
-    if (tid == 0 && !abort_s && mmas_issued > 0 && !wait_mma_upto(mmas_issued - 1)) {
-        abort_s = 1;
-        atomicCAS(p.status, 0, kDevTimeout);
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (!abort_s) {
-        const int q = warp & 3, hf = warp >> 2;  // TMEM lane quarter (32 token rows), 64-column half
-        const int i = q * 32 + lane, t = t0 + i;
+    } else if (warp >= 1) {  // epilogue warps 1-4: lane quarter q = warp & 3
+        const int q = warp & 3;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const int NU = p.H * p.R * p.dk, NP = p.H * p.R * p.dv;
-        const bool live = t < p.T;
-        const int nh = n0 + 64 * hf;  // first column of this half
-        float sq = 0.f;  // sum of squares of this half (used when it holds basis columns)
-        if (nh < NU) {
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                float v[32];
-                tmem_ld(tmem + lane_off + (uint32_t)(64 * hf + 32 * ch), v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) sq = fmaf(v[e], v[e], sq);
+        for (int i = 0; i < my_tiles; ++i) {
+            const int buf = i & 1;
+            const bool done = mbar_wait(smem_u32(&acc_full[buf]), (uint32_t)((i / 2) & 1), p.wait_ns);
+            if (!__all_sync(0xffffffffu, done)) {
+                if (lane == 0) atomicCAS(p.status, 0, kDevTimeout);
+                break;
             }
-        }
-        ssx[hf][i] = sq;
-        __syncthreads();
-        // a basis group is one half (dk = 64) or the whole tile (dk = 128)
-        const float gsq = (p.dk == 64) ? sq : ssx[0][i] + ssx[1][i];
+            fence_after_sync();
+            const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+            const int bt = tile / tiles_n, n0 = (tile % tiles_n) * PN;
+            const int b = bt / p.tiles_t, t = (bt % p.tiles_t) * PM + q * 32 + lane;
+            const bool live = t < p.T;
+            const uint32_t acc = tmem + buf * PN + lane_off;
+            float sq[2] = {0.f, 0.f};  // sums of squares of the two 64-column halves
+            if (n0 < NU) {
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-            float v[32];
-            tmem_ld(tmem + lane_off + (uint32_t)(64 * hf + 32 * ch), v);
-            const int n = nh + 32 * ch;
-            if (!live || n >= p.N) continue;
-            if (n < NU) {  // basis: scale by 1 / ||y|| of its (h, l) group
-                const int g = n / p.dk, c = n % p.dk;
-                const float f = gsq > 0.f ? rsqrtf(gsq) : 0.f;
-                __nv_bfloat16 *dst = p.u + ((((size_t)b * p.H + g / p.R) * p.T + t) * p.R + g % p.R) * p.dk + c;
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                for (int ch = 0; ch < PN / 32; ++ch) {
+                    float v[32];
+                    tmem_ld(acc + (uint32_t)(32 * ch), v);
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    d4[e] = make_uint4(pack_bf2(v[8 * e] * f, v[8 * e + 1] * f), pack_bf2(v[8 * e + 2] * f, v[8 * e + 3] * f),
-                                       pack_bf2(v[8 * e + 4] * f, v[8 * e + 5] * f), pack_bf2(v[8 * e + 6] * f, v[8 * e + 7] * f));
-            } else if (n < NU + NP) {  // gain
-                const int m = n - NU, g = m / p.dv, c = m % p.dv;
-                __nv_bfloat16 *dst = p.p + ((((size_t)b * p.H + g / p.R) * p.T + t) * p.R + g % p.R) * p.dv + c;
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                    for (int e = 0; e < 32; ++e) sq[ch >> 1] = fmaf(v[e], v[e], sq[ch >> 1]);
+                }
+            }
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    d4[e] = make_uint4(pack_bf2(v[8 * e], v[8 * e + 1]), pack_bf2(v[8 * e + 2], v[8 * e + 3]),
-                                       pack_bf2(v[8 * e + 4], v[8 * e + 5]), pack_bf2(v[8 * e + 6], v[8 * e + 7]));
-            } else {  // gates: logistic, one column each
+            for (int ch = 0; ch < PN / 32; ++ch) {
+                float v[32];
+                tmem_ld(acc + (uint32_t)(32 * ch), v);
+                const int n = n0 + 32 * ch;
+                if (!live || n >= p.N) continue;
+                if (n < NU) {  // basis: a group is one 64-column half (dk = 64) or the whole tile (dk = 128)
+                    const int g = n / p.dk, c = n % p.dk;
+                    const float gsq = (p.dk == 64) ? sq[ch >> 1] : sq[0] + sq[1];
+                    const float f = gsq > 0.f ? rsqrtf(gsq) : 0.f;
+                    __nv_bfloat16 *dst = p.u + ((((size_t)b * p.H + g / p.R) * p.T + t) * p.R + g % p.R) * p.dk + c;
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int m = n + e - NU - NP;
-                    if (n + e < p.N) {
-                        const int h = m / p.R, l = m % p.R;
-                        p.gamma[(((size_t)b * p.H + h) * p.T + t) * p.R + l] = 1.f / (1.f + __expf(-v[e]));
+                    for (int e = 0; e < 4; ++e)
+                        d4[e] = make_uint4(pack_bf2(v[8 * e] * f, v[8 * e + 1] * f), pack_bf2(v[8 * e + 2] * f, v[8 * e + 3] * f),
+                                           pack_bf2(v[8 * e + 4] * f, v[8 * e + 5] * f),
+                                           pack_bf2(v[8 * e + 6] * f, v[8 * e + 7] * f));
+                } else if (n < NU + NP) {  // gain
+                    const int m = n - NU, g = m / p.dv, c = m % p.dv;
+                    __nv_bfloat16 *dst = p.p + ((((size_t)b * p.H + g / p.R) * p.T + t) * p.R + g % p.R) * p.dv + c;
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        d4[e] = make_uint4(pack_bf2(v[8 * e], v[8 * e + 1]), pack_bf2(v[8 * e + 2], v[8 * e + 3]),
+                                           pack_bf2(v[8 * e + 4], v[8 * e + 5]), pack_bf2(v[8 * e + 6], v[8 * e + 7]));
+                } else {  // gates: logistic, one column each
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int m = n + e - NU - NP;
+                        if (n + e < p.N) {
+                            const int h = m / p.R, l = m % p.R;
+                            p.gamma[(((size_t)b * p.H + h) * p.T + t) * p.R + l] = 1.f / (1.f + __expf(-v[e]));
+                        }
                     }
                 }
             }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));  // this quarter is done with the accumulator
         }
     }
     // drain: after an expired wait, the copies and products in flight land before the CTA exits
+    __syncthreads();
     if (tid == 0 && abort_s) {
         for (int k = mmas_waited; k < mmas_issued; ++k)
             (void)mbar_wait(smem_u32(&mmad[k % STAGES]), (uint32_t)((k / STAGES) & 1), 1000000000ull);
@@ -244,7 +273,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, PN);
+    if (warp == 0) tmem_dealloc(tmem, 2 * PN);
 }
 
 }  // namespace proj
@@ -307,7 +336,16 @@ cudaError_t project_forward(const Shape &s, int D, const ProjectArgs &a, int *d_
     p.dv = s.dv;
     p.N = N;
     p.tiles_t = (s.T + PM - 1) / PM;
-    const dim3 grid(s.B * p.tiles_t, (N + PN - 1) / PN);
+    p.tiles_bt = s.B * p.tiles_t;
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    const int ntiles = p.tiles_bt * ((N + PN - 1) / PN);
+    const dim3 grid(ntiles < 2 * sms ? ntiles : 2 * sms);
     const long long n8 = (long long)s.B * s.T * (D / 8);
     tm.begin("anchor");
     anchor_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, tm.stream>>>((const __nv_bfloat16 *)a.X,
@@ -317,7 +355,7 @@ cudaError_t project_forward(const Shape &s, int D, const ProjectArgs &a, int *d_
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     tm.begin("project");
-    project_kernel<<<grid, THREADS, SMEM, tm.stream>>>(ma, mw, p);
+    project_kernel<<<grid, PTHREADS, SMEM, tm.stream>>>(ma, mw, p);
     tm.end();
     return cudaGetLastError();
 }
