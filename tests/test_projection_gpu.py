@@ -1,7 +1,9 @@
 """GPU parity of the block's input projections (prism_project) against the fp64 oracle
 (oracle/prism_projection.py) on the same bf16 inputs.  Bars: max |x - x_ref| / rms(x_ref) <= 2e-2
-for the basis and gain outputs (bf16 operands and outputs, fp32 accumulation), max |gamma -
-gamma_ref| <= 2e-3 for the gates (a logistic, so absolute)."""
+for the basis and gain outputs (bf16 operands and outputs, fp32 accumulation); max |gamma -
+gamma_ref| <= 5e-3 for the gates, derived from the arithmetic: the anchor enters the tensor
+cores rounded to bf16 (relative 2^-9 per entry), which moves a logit z by up to about
+2^-9 |z| with |z| <= ~8 on these inputs, and the logistic's slope is at most 1/4."""
 import numpy as np
 import pytest
 import torch
@@ -43,7 +45,7 @@ def test_projection_matches_oracle(B_, T, D, H, R, dk, dv):
     ru, rp, rg = PP.project(pi["X"], pi["conv_x"], pi["W"], H, R, dk, dv)
     assert rel_err(u.double().cpu().numpy(), ru) <= TOL["bf16"]
     assert rel_err(p.double().cpu().numpy(), rp) <= TOL["bf16"]
-    assert np.max(np.abs(g.double().cpu().numpy() - rg)) <= 2e-3
+    assert np.max(np.abs(g.double().cpu().numpy() - rg)) <= 5e-3
     un = torch.linalg.vector_norm(u.float(), dim=-1)
     assert torch.all((un - 1).abs() < 1e-2)
 
