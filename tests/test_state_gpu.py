@@ -180,6 +180,41 @@ def test_decode_step_equals_one_token_forward():
     assert torch.equal(h_a, h_b)
 
 
+def test_decode_steps_replay_from_a_cuda_graph():
+    """A serving loop captures the decode step once and replays it: each replay advances the
+    state and the history in place exactly as a direct call does."""
+    inp = make_inputs(4, 2, 6, 64, 64, 4, dtype="bf16", seed=86)
+    d = to_device(inp)
+    S0 = init_state(4, 2, 64, 64, seed=87).cuda()
+    h0 = torch.zeros(4, 2, 3, 64, dtype=torch.bfloat16, device="cuda")
+    with B.Plan(4, 2, 1, 64, 64, 4, io="bf16", out="f32") as p:
+        # direct calls on tokens 0..5
+        S_a, h_a, outs_a = S0.clone(), h0.clone(), []
+        for t in range(6):
+            outs_a.append(p.decode_step(token(d, t), h_a, S_a).clone())
+        # the same steps from one captured graph: the token's inputs are copied into fixed buffers
+        S_b, h_b = S0.clone(), h0.clone()
+        tok = {kk: (vv.clone() if torch.is_tensor(vv) else vv) for kk, vv in token(d, 0).items()}
+        out = torch.empty(4, 2, 64, device="cuda")
+        p.decode_step(tok, h_b.clone(), S_b.clone(), out)  # first call outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            p.decode_step(tok, h_b, S_b, out, torch.cuda.current_stream())
+        outs_b = []
+        for t in range(6):
+            for kk, vv in token(d, t).items():
+                if torch.is_tensor(vv) and kk != "conv_w":
+                    tok[kk].copy_(vv)
+            g.replay()
+            outs_b.append(out.clone())
+        torch.cuda.synchronize()
+        p.last_device_status()
+    for a, b in zip(outs_a, outs_b):
+        assert torch.equal(a, b)
+    assert torch.equal(S_a, S_b) and torch.equal(h_a, h_b)
+
+
 def test_decode_zero_write_gates_keep_decayed_state():
     """beta = gamma = 0: the step only decays the state, S <- alpha S, and reads it out."""
     inp = make_inputs(2, 2, 1, 64, 64, 3, dtype="f32", seed=83)
