@@ -160,3 +160,14 @@ def select_heads(inp: dict, pairs):
         out[name] = inp[name][bs, hs].unsqueeze(0)
     out["conv_w"] = inp["conv_w"][hs]
     return out
+
+
+def make_cotangents(B, H, T, dk, dv, seed=0, with_state=False):
+    """Cotangents for the backward pass: dout ~ N(0, 1) [B,H,T,dv] (float32) and, with
+    ``with_state``, dS_final ~ N(0, 1) [B,H,dv,dk] (float32), drawn in that order from a
+    generator of their own (seed + 104729) so that the forward inputs of a seed are unchanged."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 104729)
+    dout = torch.randn(B, H, T, dv, generator=g, dtype=torch.float32)
+    dS_final = torch.randn(B, H, dv, dk, generator=g, dtype=torch.float32) if with_state else None
+    return dout, dS_final
