@@ -17,6 +17,7 @@ prints one JSON line with the max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -48,12 +49,15 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="default seqrec_16k (forward) or decode_lm130m (decode)")
-    ap.add_argument("--mode", choices=["forward", "decode", "nonlinear", "project"], default="forward",
+    ap.add_argument("--mode", choices=["forward", "decode", "nonlinear", "project", "backward"], default="forward",
                     help="forward: prism_forward over whole sequences (the headline); decode: one "
                          "prism_decode_step (one token per sequence) over a serving batch; nonlinear: "
                          "prism_forward_nonlinear (the non-linear residual variant) over whole sequences; "
-                         "project: prism_project (the block's input projections)")
+                         "project: prism_project (the block's input projections); backward: prism_backward "
+                         "(the cotangents of every input) over whole sequences")
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 portable fp32 kernels, 2 tensor-core path")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override the workload's T (a smaller case of the same shape, e.g. for a profiler)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU-baseline sample")
@@ -120,6 +124,7 @@ KERNEL_SOURCES = {
     "tc_": ("prism_tc.cu", "tc_ptx.h", "prism_internal.h"),
     "decode": ("prism_state.cu", "tc_ptx.h", "prism_internal.h"),
     "simt_": ("prism_simt.cu", "prism_internal.h"),
+    "bwd_": ("prism_backward.cu", "prism_internal.h"),
 }
 
 
@@ -757,6 +762,232 @@ def run_project(args, name):
     return 0
 
 
+BACKWARD_METRIC = "PRISM layer bwd tokens/s (all input cotangents, T=16K) + % of HBM roofline"
+BWD_KEYS = ("q", "k", "v", "beta", "alpha", "u", "gamma", "eta", "conv_w")
+
+
+def backward_kernel_bytes(name, w):
+    """Bytes a backward kernel must move at minimum for one launch over the workload: each of
+    its inputs read once and each of its outputs written once, the per-token states S_{t-1} and
+    cotangents dS_t of the design included (fp32, dv dk floats per token each)."""
+    io = 2 if w.dtype == "bf16" else 4
+    th = w.B * w.H * w.T
+    R = w.R
+    qk = th * w.dk * io
+    v = th * w.dv * io
+    u = th * R * w.dk * io
+    gates2 = th * 8
+    X = dX = th * R * w.dv * 4
+    state = th * w.dv * w.dk * 4
+    per_row = th * w.dv * 4  # z, dout, dh or a dv-sized fp32 cotangent
+    ntile = -(-w.T // 64)
+    table = {
+        "bwd_factors": v + th * 8 * R + X,
+        # both halves of the scan launch: S_{t-1} forward, dS_t (with z, dx) in reverse
+        "bwd_scan": (qk + v + u + gates2 + X + state) + (2 * qk + u + gates2 + per_row + state + per_row + dX),
+        "bwd_token_grad": 2 * qk + v + u + gates2 + X + 2 * state + 2 * per_row + 2 * th * w.dk * 4 + per_row
+        + th * R * w.dk * 4 + th * 8,
+        "bwd_chain_grad": v + th * 8 * R + dX + 2 * per_row + per_row + th * 8 * R,
+        "bwd_conv_grad": v + 3 * per_row + w.B * w.H * ntile * 4 * w.dv * 4,
+        "bwd_conv_reduce": w.B * w.H * ntile * 4 * w.dv * 4 + w.H * 4 * w.dv * 4,
+    }
+    return table[name]
+
+
+def backward_path_bytes(w):
+    """The pass's own minimum: the inputs and dout read once, every cotangent written once."""
+    io = 2 if w.dtype == "bf16" else 4
+    th = w.B * w.H * w.T
+    R = w.R
+    ins = th * (2 * w.dk + w.dv + R * w.dk) * io + th * 4 * (2 + 2 * R) + th * w.dv * 4
+    outs = th * 4 * (2 * w.dk + w.dv + 2 + R * w.dk + 2 * R)
+    return ins + outs
+
+
+def backward_oracle_step(sub, dout, nthreads):
+    from oracle import prism_backward
+    prism_backward.backward(sub["q"], sub["k"], sub["v"], sub["beta"], sub["alpha"], sub["u"], sub["gamma"],
+                            sub["eta"], sub["conv_w"], sub["L"], dout, nthreads=nthreads)
+
+
+def backward_sample(inp, dout, Ts):
+    sub = {k: (v[:, :, :Ts].contiguous() if hasattr(v, "shape") and k != "conv_w" else v) for k, v in inp.items()}
+    sub = {k: (v.double().numpy() if hasattr(v, "double") else v) for k, v in sub.items()}
+    return sub, dout[:, :, :Ts].double().numpy()
+
+
+def run_backward(args, w):
+    import torch
+
+    from ssm_sequence_layer_gb300 import binding as Bd
+    from ssm_sequence_layer_gb300 import build as cuda_build
+    from ssm_sequence_layer_gb300.inputs import make_cotangents, make_workload_inputs
+
+    world, rank, local = dist_setup(args)
+    if rank == 0:
+        cuda_build.build()
+    barrier(world)
+    steps, warm = args.steps, max(args.warmup, 3)
+    inp_cpu = make_workload_inputs(w, seed=0)
+    dout_cpu, _ = make_cotangents(w.B, w.H, w.T, w.dk, w.dv, seed=0)
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp_cpu.items()}
+    dout = dout_cpu.cuda()
+    stream = torch.cuda.current_stream()
+    plan = Bd.Plan.for_inputs(dev)
+    flush = L2Flush()
+    grads = plan.backward(dev, dout, stream=stream)
+    for _ in range(warm):
+        flush()
+        plan.backward(dev, dout, grads=grads, stream=stream)
+    torch.cuda.synchronize()
+    plan.last_device_status()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        plan.backward(dev, dout, grads=grads, stream=stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    plan.last_device_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    plan.set_option(Bd.PRISM_OPT_TIMING, 1)
+    per_kernel, launches = {}, 0
+    for _ in range(steps):
+        flush()
+        plan.backward(dev, dout, grads=grads, stream=stream)
+        torch.cuda.synchronize()
+        kt = plan.kernel_times()
+        launches += len(kt)
+        for name, ms in kt:
+            per_kernel.setdefault(name, []).append(ms)
+    plan.set_option(Bd.PRISM_OPT_TIMING, 0)
+    plan.last_device_status()
+    ms_local = sum(step_ms) / steps
+    ms = max_over_ranks(ms_local, world)
+    tokens = w.B * w.T
+    value = tokens * world / (ms / 1e3)
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tot = {n: sum(v) for n, v in per_kernel.items()}
+    dom = max(tot, key=tot.get)
+    dom_ms = tot[dom] / len(per_kernel[dom])
+    dom_bytes = backward_kernel_bytes(dom, w)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": traffic_from_profiles(dom, w.name),
+                "alg_bytes_per_launch": dom_bytes, "kernel_ms": dom_ms, "peak_source": f"{peak_kind} hbm_gbs"}
+    kernels = {n: {"ms_mean": tot[n] / len(per_kernel[n]), "share": tot[n] / sum(tot.values()),
+                   "hbm_frac": backward_kernel_bytes(n, w) / (tot[n] / len(per_kernel[n]) / 1e3) / 1e9 / hbm}
+               for n in tot}
+    pb = backward_path_bytes(w)
+    path_roofline = {"achieved": pb / (ms_local / 1e3) / 1e9, "unit": "GB/s",
+                     "frac": pb / (ms_local / 1e3) / 1e9 / hbm, "alg_bytes_per_step": pb}
+
+    e2e = None
+    if not args.no_e2e:  # inputs and dout copied in from pinned host memory, every cotangent copied back
+        host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in inp_cpu.items()}
+        hdout = dout_cpu.pin_memory()
+        hgrads = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()}
+        used = [k for k in BWD_KEYS if w.L > 1 or k not in ("u", "gamma", "eta")]
+        h2d = hdout.numel() * 4 + sum(host[k].numel() * host[k].element_size() for k in used)
+        d2h = sum(v.numel() * v.element_size() for k, v in hgrads.items()
+                  if w.L > 1 or k not in ("du", "dgamma", "deta"))
+        dbuf = {k: (torch.empty_like(v, device="cuda") if torch.is_tensor(v) else v) for k, v in host.items()}
+        ddout = torch.empty_like(hdout, device="cuda")
+        e2e_ms = []
+        for i in range(max(3, min(steps, 10)) + 2):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k in used:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            ddout.copy_(hdout, non_blocking=True)
+            plan.backward(dbuf, ddout, grads=grads, stream=stream)
+            for k, v in hgrads.items():
+                v.copy_(grads[k], non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                e2e_ms.append(a.elapsed_time(b))
+        e2e_mean = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+        e2e = {"value": tokens * world / (e2e_mean / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = cpu_threads(w)
+        Ts = min(w.T, 256)
+        sub, sd = backward_sample(inp_cpu, dout_cpu, Ts)
+        t0 = time.perf_counter()
+        backward_oracle_step(sub, sd, nthreads)
+        dt = time.perf_counter() - t0
+        Ts = int(min(w.T, max(Ts, Ts * args.cpu_seconds / max(dt, 1e-3))))
+        sub, sd = backward_sample(inp_cpu, dout_cpu, Ts)
+        t0 = time.perf_counter()
+        backward_oracle_step(sub, sd, nthreads)
+        dt = time.perf_counter() - t0
+        cpu = {"value": w.B * Ts / dt, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+               "sample": f"fp64 backward oracle over the first {Ts} tokens of all {w.B * w.H} sequences ({dt:.1f} s)"}
+    plan.close()
+    if rank == 0:
+        line = {
+            "metric": BACKWARD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")},
+                       "io": w.dtype, "l2": L2Flush.DESCRIPTION,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roofline, "path_roofline": path_roofline, "kernels": kernels, "cpu_baseline": cpu,
+            "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_backward_reference(args, w):
+    """The backward oracle as the reference arm: each step is the oracle's backward over the
+    first Ts tokens of every sequence of the workload, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    from ssm_sequence_layer_gb300.inputs import make_cotangents, make_workload_inputs
+    inp = make_workload_inputs(w)
+    dout, _ = make_cotangents(w.B, w.H, w.T, w.dk, w.dv, seed=0)
+    nthreads = cpu_threads(w)
+    Ts = min(w.T, 512)
+    sub, sd = backward_sample(inp, dout, Ts)
+    for _ in range(max(args.warmup, 0)):
+        backward_oracle_step(sub, sd, nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        backward_oracle_step(sub, sd, nthreads)
+    dt = time.perf_counter() - t0
+    value = w.B * Ts * args.steps / dt
+    line = {
+        "impl": "reference", "metric": BACKWARD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")}, "io": w.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                         "sample": f"backward oracle over the first {Ts} tokens of all {w.B * w.H} sequences per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     from ssm_sequence_layer_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
@@ -770,6 +1001,13 @@ def main():
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the forward and the decode step"}))
             return 0
         return run_project(args, args.workload or "project_lm130m")
+    if args.mode == "backward":
+        w = WORKLOADS[args.workload or "seqrec_16k"]
+        if args.seq_len:
+            w = dataclasses.replace(w, T=args.seq_len, name=f"{w.name}_T{args.seq_len}")
+        if args.impl == "reference":
+            return run_backward_reference(args, w)
+        return run_backward(args, w)
     if args.mode == "nonlinear":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the forward and the decode step"}))

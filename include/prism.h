@@ -225,6 +225,42 @@ PRISM_API prism_status prism_forward_nonlinear(prism_plan_t plan, const void *q,
 PRISM_API prism_status prism_project(prism_plan_t plan, int D, const void *X, const void *conv_x, const void *W,
                                      void *u, void *p, float *gamma, struct CUstream_st *stream);
 
+/*
+ * prism_backward -- the cotangents of every input of prism_forward_state (the linear residual
+ * chain), given dout = dLoss/d out and optionally dS_final = dLoss/d S_final: reverse-mode
+ * differentiation of the definition at the top of this file, token by token backwards.
+ * With P = S_{t-1}, y = P k_t and dS_t the cotangent of S_t (dout_t q_t^T included), z = dS_t k_t:
+ *   dS_{t-1} = alpha_t (dS_t - beta_t z k_t^T)
+ *   dq_t = S_t^T dout_t      dk_t = dS_t^T (beta_t v_t - alpha_t beta_t y) - alpha_t beta_t P^T z
+ *   dalpha_t = <dS_t, P> - beta_t y.z      dbeta_t = v_t.z - alpha_t y.z
+ *   du_{t,l} = dS_t^T x_{t,l}              dx_{t,l} = dS_t u_{t,l}   (x = the injection factors)
+ * and through the residual chain, the gain (GELU''), the residual and the convolution to dv,
+ * dgamma, deta and dconv_w.
+ * Inputs: q .. L, v_hist and S_init exactly as prism_forward_state (v_hist, S_init may be NULL);
+ *   dout      [B,H,T,dv]  float32
+ *   dS_final  [B,H,dv,dk] float32 or NULL (zero)
+ * Outputs (float32, each with its input's layout, overwritten):
+ *   dq, dk [B,H,T,dk]  dv [B,H,T,dv]  dbeta, dalpha [B,H,T]  du [B,H,T,R,dk]  dgamma, deta [B,H,T,R]
+ *   (deta[..., R-1] = 0: that gain is never read)  dconv_w [H,4,dv] (summed over the batch)
+ *   dv_hist   [B,H,3,dv]  or NULL: the cotangent of the three history slots (also when v_hist is
+ *                         NULL, i.e. with respect to the zeros that stand in for them)
+ *   dS_init   [B,H,dv,dk] or NULL: the cotangent of the initial state
+ * With L = 1, u, gamma, eta, du, dgamma and deta are not touched (dconv_w and dv_hist are 0).
+ * dout, dS_final, dq, dk, dv, du, dv_hist and dS_init start on 16-byte boundaries; dbeta,
+ * dalpha, dgamma, deta and dconv_w on 4.  No output overlaps another buffer.
+ * The pass computes in fp32 from the io values.  It keeps S_{t-1} and dS_t of every token in
+ * a workspace owned by the plan (2 B H T dv dk floats plus small per-token buffers, reported by
+ * prism_workspace_bytes), allocated by the first call, so make that call before capturing a
+ * stream.  Returns once the work is enqueued on `stream`.
+ */
+PRISM_API prism_status prism_backward(prism_plan_t plan, const void *q, const void *k, const void *v,
+                                      const float *beta, const float *alpha, const void *u, const float *gamma,
+                                      const float *eta, const void *conv_w, int L, const void *v_hist,
+                                      const float *S_init, const float *dout, const float *dS_final, float *dq,
+                                      float *dk, float *dv, float *dbeta, float *dalpha, float *du, float *dgamma,
+                                      float *deta, float *dconv_w, float *dv_hist, float *dS_init,
+                                      struct CUstream_st *stream);
+
 /* Free the plan and its workspace.  NULL is accepted. */
 PRISM_API prism_status prism_plan_destroy(prism_plan_t plan);
 

@@ -36,7 +36,7 @@ EXPORTED = ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forwa
             "prism_plan_destroy", "prism_workspace_bytes", "prism_plan_last_device_status",
             "prism_status_string", "prism_last_error_message", "prism_version", "prism_plan_kernel_times",
             "prism_forward_noalloc", "prism_forward_state", "prism_decode_step", "prism_forward_nonlinear",
-            "prism_project")
+            "prism_project", "prism_backward")
 
 
 class prism_kernel_time(ctypes.Structure):
@@ -88,10 +88,11 @@ def lib():
             L.prism_decode_step.argtypes = fwd[:11] + [vp, f, vp, vp]
             L.prism_forward_nonlinear.argtypes = fwd[:11] + [vp, f, vp, f, vp, vp]
             L.prism_project.argtypes = [vp, i, vp, vp, vp, vp, vp, f, vp]
+            L.prism_backward.argtypes = fwd[:11] + [vp, f, f, f] + [f] * 11 + [vp]
             L.prism_plan_kernel_times.restype = ctypes.c_int
             for name in ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
                          "prism_plan_destroy", "prism_plan_last_device_status", "prism_forward_state",
-                         "prism_decode_step", "prism_forward_nonlinear", "prism_project"):
+                         "prism_decode_step", "prism_forward_nonlinear", "prism_project", "prism_backward"):
                 getattr(L, name).restype = ctypes.c_int
             _LIB = L
     return _LIB
@@ -199,6 +200,15 @@ def prism_decode_step(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, v_hi
     return _check(lib().prism_decode_step(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha),
                                           _addr(u), _addr(gamma), _addr(eta), _addr(conv_w), int(L),
                                           _addr(v_hist), _addr(S), _addr(out), _stream(stream)))
+
+
+def prism_backward(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, v_hist, S_init, dout, dS_final, dq, dk, dv,
+                   dbeta, dalpha, du, dgamma, deta, dconv_w, dv_hist, dS_init, stream=None):
+    return _check(lib().prism_backward(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha), _addr(u),
+                                       _addr(gamma), _addr(eta), _addr(conv_w), int(L), _addr(v_hist),
+                                       _addr(S_init), _addr(dout), _addr(dS_final), _addr(dq), _addr(dk), _addr(dv),
+                                       _addr(dbeta), _addr(dalpha), _addr(du), _addr(dgamma), _addr(deta),
+                                       _addr(dconv_w), _addr(dv_hist), _addr(dS_init), _stream(stream)))
 
 
 def prism_forward_noalloc(B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, conv_w, out, stream=None,
@@ -320,6 +330,35 @@ class Plan:
             out = torch.empty((B, H, self.shape[4]), dtype=self._out_torch_dtype(), device=inp["v"].device)
         prism_decode_step(self.handle, *ts, v_hist, S, out, stream)
         return out
+
+    def backward(self, inp, dout, dS_final=None, v_hist=None, S_init=None, want_dv_hist=False,
+                 want_dS_init=False, grads=None, stream=None):
+        """Cotangents of the inputs (see prism_backward): dout [B,H,T,dv] and dS_final
+        [B,H,dv,dk] are float32 CUDA tensors (dS_final may be None).  Returns a dict of float32
+        tensors dq, dk, dv, dbeta, dalpha, du, dgamma, deta, dconv_w (plus dv_hist and dS_init on
+        request), allocated unless `grads` holds them."""
+        import torch
+        ts = self._tensors(inp)
+        self._check_device(ts[:-1] + (dout, dS_final, v_hist, S_init), "prism_backward")
+        B, H, T, dk, dv, L = self.shape
+        R = L - 1
+        if grads is None:
+            dev = inp["v"].device
+            e = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=dev)  # noqa: E731
+            grads = {"dq": e(B, H, T, dk), "dk": e(B, H, T, dk), "dv": e(B, H, T, dv), "dbeta": e(B, H, T),
+                     "dalpha": e(B, H, T), "du": e(B, H, T, R, dk), "dgamma": e(B, H, T, R),
+                     "deta": e(B, H, T, R), "dconv_w": e(H, 4, dv)}
+            if want_dv_hist:
+                grads["dv_hist"] = e(B, H, 3, dv)
+            if want_dS_init:
+                grads["dS_init"] = e(B, H, dv, dk)
+        g = grads
+        lv = R > 0
+        self._check_device(tuple(g.values()), "prism_backward")
+        prism_backward(self.handle, *ts, v_hist, S_init, dout, dS_final, g["dq"], g["dk"], g["dv"], g["dbeta"],
+                       g["dalpha"], g["du"] if lv else None, g["dgamma"] if lv else None, g["deta"] if lv else None,
+                       g["dconv_w"], g.get("dv_hist"), g.get("dS_init"), stream)
+        return g
 
     def _out_torch_dtype(self):
         import torch

@@ -112,6 +112,9 @@ void free_workspaces(prism_plan_s *p)
     if (p->ws_simt) cudaFree(p->ws_simt);
     if (p->ws_tc) cudaFree(p->ws_tc);
     if (p->d_status) cudaFree(p->d_status);
+    if (p->ws_bwd) cudaFree(p->ws_bwd);
+    p->ws_bwd = nullptr;
+    p->ws_bwd_bytes = 0;
     p->ws_simt = p->ws_tc = nullptr;
     p->d_status = nullptr;
 }
@@ -230,6 +233,7 @@ prism_status prism_plan(int B, int H, int T, int dk, int dv, int L, prism_dtype 
     cudaError_t e = prism::simt_prepare(s, io);
     if (e == cudaSuccess && prism::tc_supported(s, io)) e = prism::tc_prepare();
     if (e == cudaSuccess && io == PRISM_BF16) e = prism::project_prepare();
+    if (e == cudaSuccess) e = prism::backward_prepare();
     if (e != cudaSuccess) {
         delete p;
         return cuda_fail(e, "kernel attribute setup");
@@ -410,6 +414,51 @@ prism_status prism_decode_step(prism_plan_t p, const void *q, const void *k, con
     return PRISM_OK;
 }
 
+prism_status prism_backward(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,
+                            const float *alpha, const void *u, const float *gamma, const float *eta,
+                            const void *conv_w, int L, const void *v_hist, const float *S_init, const float *dout,
+                            const float *dS_final, float *dq, float *dk, float *dv, float *dbeta, float *dalpha,
+                            float *du, float *dgamma, float *deta, float *dconv_w, float *dv_hist, float *dS_init,
+                            struct CUstream_st *stream)
+{
+    if (!p) return fail(PRISM_ERR_INVALID_ARG, "plan is NULL");
+    // the forward's checks stand for the inputs; dout takes the place of out
+    prism_status st = check_forward_args(p, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, dout);
+    if (st != PRISM_OK) return st;
+    const bool lvl = p->shape.R > 0;
+    if (!dq || !dk || !dv || !dbeta || !dalpha || !dconv_w)
+        return fail(PRISM_ERR_INVALID_ARG, "dq, dk, dv, dbeta, dalpha and dconv_w must not be NULL");
+    if (lvl && (!du || !dgamma || !deta))
+        return fail(PRISM_ERR_INVALID_ARG, "du, dgamma and deta must not be NULL when L > 1");
+    const void *ap[] = {v_hist, S_init, dS_final, dv_hist, dS_init, dout, dq, dk, dv, lvl ? du : nullptr};
+    const char *an[] = {"v_hist", "S_init", "dS_final", "dv_hist", "dS_init", "dout", "dq", "dk", "dv", "du"};
+    for (int i = 0; i < 10; ++i)
+        if (ap[i] && !aligned(ap[i], 16)) return fail(PRISM_ERR_MISALIGNED, "%s is not 16-byte aligned", an[i]);
+    const void *fp[] = {dbeta, dalpha, dconv_w, lvl ? dgamma : nullptr, lvl ? deta : nullptr};
+    const char *fn[] = {"dbeta", "dalpha", "dconv_w", "dgamma", "deta"};
+    for (int i = 0; i < 5; ++i)
+        if (fp[i] && !aligned(fp[i], 4)) return fail(PRISM_ERR_MISALIGNED, "%s is not 4-byte aligned", fn[i]);
+    if ((st = check_plan_device(p)) != PRISM_OK) return st;
+    if (!p->ws_bwd) {
+        const size_t bytes = prism::backward_workspace_bytes(p->shape);
+        cudaError_t e = cudaMalloc(&p->ws_bwd, bytes);
+        if (e != cudaSuccess) {
+            p->ws_bwd = nullptr;
+            return cuda_fail(e, "backward workspace allocation");
+        }
+        p->ws_bwd_bytes = bytes;
+    }
+    prism::BackwardArgs a{q, k, v, lvl ? u : nullptr, conv_w, v_hist, beta, alpha, lvl ? gamma : nullptr,
+                          lvl ? eta : nullptr, S_init, dout, dS_final, dq, dk, dv, dbeta, dalpha,
+                          lvl ? du : nullptr, lvl ? dgamma : nullptr, lvl ? deta : nullptr, dconv_w, dv_hist,
+                          dS_init};
+    p->timer.on = p->opt_timing != 0;
+    p->timer.reset((cudaStream_t)stream);
+    const cudaError_t e = prism::backward(p->shape, p->io, a, p->ws_bwd, p->timer);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return PRISM_OK;
+}
+
 prism_status prism_forward_host(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,
                                 const float *alpha, const void *u, const float *gamma, const float *eta,
                                 const void *conv_w, int L, void *out, struct CUstream_st *stream)
@@ -465,7 +514,7 @@ prism_status prism_plan_destroy(prism_plan_t p)
     return PRISM_OK;
 }
 
-size_t prism_workspace_bytes(prism_plan_t p) { return p ? p->ws_simt_bytes + p->ws_tc_bytes : 0; }
+size_t prism_workspace_bytes(prism_plan_t p) { return p ? p->ws_simt_bytes + p->ws_tc_bytes + p->ws_bwd_bytes : 0; }
 
 int prism_plan_kernel_times(prism_plan_t p, prism_kernel_time *out, int max)
 {

@@ -1,0 +1,693 @@
+// Backward pass of the PRISM memory recurrence (portable fp32 kernels, no tensor cores).
+//
+// The recurrence S_t = S_{t-1} A_t + B_t with A_t = alpha_t (I - beta_t k_t k_t^T) acts on each
+// row of S on its own (row i of S_t depends only on row i of S_{t-1}; notes on PRISM, section
+// 2.2), and so does its transpose, the carry of the state cotangent
+//   dS_{t-1} = alpha_t (dS_t - beta_t (dS_t k_t) k_t^T),   dS_t += dout_t q_t^T first.
+// So the two sequential scans run eight lanes per state row, token by token, with the row in
+// registers and one dot product on the dependency chain per token.  They do not
+// depend on each other and run side by side in one launch (scan_kernel):
+//   forward half   S_{t-1} for every t -> workspace (forward order)
+//   reverse half   dS_t for every t -> workspace, z_t = dS_t k_t, dx_{t,l} = dS_t u_{t,l}
+//                  (reverse order)
+// Everything that needs sums over the rows is then token-parallel:
+//   token_grad   dq, dk, du, dalpha, dbeta and the write's share of dv, from S_{t-1}, dS_t
+//   chain_grad   the residual chain and gain backwards: dgamma, deta, dh and e's share of dv
+//   conv_grad    the short convolution backwards: v's share, dv_hist, per-tile dconv_w sums
+//   conv_reduce  dconv_w = the sum of the tiles over the batch
+// The formulas (reverse-mode differentiation of the sequential definition), with P = S_{t-1},
+// y = P k_t, z = dS_t k_t:
+//   dq_t = S_t^T dout_t = alpha P^T dout - alpha beta k (y . dout) + beta k (v . dout)
+//          + sum_l u_l (x_l . dout)
+//   dk_t = dS_t^T (beta v - alpha beta y) - alpha beta P^T z
+//   dalpha_t = <dS_t, P> - beta y . z,   dbeta_t = v . z - alpha y . z
+//   dv_t += beta z,   du_{t,l} = dS_t^T x_{t,l}
+// and per channel, levels l = R .. 1 (the cotangent of r_{t,R+1} is zero):
+//   dr_l = gamma_l g dx_l + (1 - eta_l g) dr_{l+1},   dg += gamma_l r_l dx_l - eta_l r_l dr_{l+1}
+//   dgamma_l = sum_c g r_l dx_l,   deta_l = -sum_c g r_l dr_{l+1}
+//   dv_t += dr_1,   dh_t = -g dr_1 + phi(h) (2 - h^2) dg
+// then dv_{t-j} += w_j dh_t and dw_j += dh_t v_{t-j} over the window.
+#include "prism_internal.h"
+
+namespace prism {
+namespace bwd {
+
+constexpr int NT = 256;    // threads of the token-parallel kernels
+constexpr int CT = 64;     // tokens per block of the convolution kernel
+constexpr int RMAX = 15;   // largest R = L - 1
+
+__device__ __forceinline__ float ldf(const float *p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Anchor h, its normal cdf Phi and density phi for channel c of token t of sequence bh.
+template <typename io_t>
+__device__ __forceinline__ void anchor_at(const io_t *v, const io_t *v_hist, const io_t *conv_w, int bh, int h, int t,
+                                          int T, int dv, int c, float &a, float &Phi, float &phi)
+{
+    const io_t *vb = v + (size_t)bh * T * dv;
+    a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float w = ldf(conv_w + ((size_t)h * 4 + j) * dv + c);
+        if (t - j >= 0)
+            a = fmaf(w, ldf(vb + (size_t)(t - j) * dv + c), a);
+        else if (v_hist)
+            a = fmaf(w, ldf(v_hist + ((size_t)bh * 3 + 3 + t - j) * dv + c), a);
+    }
+    Phi = 0.5f * erfcf(-a * 0.70710678118654752f);
+    phi = 0.39894228040143268f * expf(-0.5f * a * a);
+}
+
+// Injection factors x_{t,l} = gamma_l g r_l -> X [BH][T][R][dv].
+template <typename io_t>
+__global__ void __launch_bounds__(NT) factors_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
+                                                     const io_t *__restrict__ conv_w, const float *__restrict__ gamma,
+                                                     const float *__restrict__ eta, float *__restrict__ X, int H,
+                                                     int T, int dv, int R)
+{
+    const int bh = blockIdx.y;
+    const long long idx = (long long)blockIdx.x * NT + threadIdx.x;
+    if (idx >= (long long)T * dv) return;
+    const int t = (int)(idx / dv), c = (int)(idx % dv);
+    float a, Phi, phi;
+    anchor_at(v, v_hist, conv_w, bh, bh % H, t, T, dv, c, a, Phi, phi);
+    const float g = fmaf(a, phi, Phi);
+    float r = ldf(v + ((size_t)bh * T + t) * dv + c) - a * Phi;
+    const size_t tok = (size_t)bh * T + t;
+    for (int l = 0; l < R; ++l) {
+        X[(tok * R + l) * dv + c] = gamma[tok * R + l] * g * r;
+        r *= 1.f - eta[tok * R + l] * g;
+    }
+}
+
+// The two sequential scans.  A block of SCAN_WARPS warps owns ROWS = 4 SCAN_WARPS state rows of
+// one sequence: each row is spread over 8 lanes (LPR), each lane holding DK / 8 consecutive
+// columns, so a row's dot product ends in a 3-step shuffle tree.  The per-token inputs of a
+// chunk of `ct` tokens are staged in shared memory by cp.async, in two buffers: the copies of
+// the next chunk are in flight while the warps walk the current one, so only the dot product
+// and the row update remain on the per-token dependency chain.
+constexpr int LPR = 8;                      // lanes per state row
+constexpr int SCAN_WARPS = 4;
+constexpr int ROWS = SCAN_WARPS * 32 / LPR;  // state rows per scan block (16)
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Sum over the 8 lanes of a row (lanes 8r .. 8r + 7).
+__device__ __forceinline__ float row_sum(float x)
+{
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x;
+}
+
+// N consecutive values from a 16-byte aligned address (shared or global) as floats.
+template <int N>
+__device__ __forceinline__ void load_vec(const float *p, float (&o)[N])
+{
+#pragma unroll
+    for (int e = 0; e < N; e += 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(p + e);
+        o[e] = t.x;
+        o[e + 1] = t.y;
+        o[e + 2] = t.z;
+        o[e + 3] = t.w;
+    }
+}
+template <int N>
+__device__ __forceinline__ void load_vec(const __nv_bfloat16 *p, float (&o)[N])
+{
+#pragma unroll
+    for (int e = 0; e < N; e += 8) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(p + e);
+        const uint32_t wds[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wds[h]));
+            o[e + 2 * h] = f.x;
+            o[e + 2 * h + 1] = f.y;
+        }
+    }
+}
+template <int N>
+__device__ __forceinline__ void store_vec(float *p, const float (&o)[N])
+{
+#pragma unroll
+    for (int e = 0; e < N; e += 4) *reinterpret_cast<float4 *>(p + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+}
+
+// Byte offsets of one stage buffer of `ct` tokens (each part a multiple of 16 bytes).
+struct StageLayout {
+    int q, k, u, row, x, gate, bytes;
+};
+__host__ __device__ inline int align16(int n) { return (n + 15) & ~15; }
+__host__ __device__ inline StageLayout stage_layout(int ct, int dk, int R, int io_bytes)
+{
+    StageLayout s;
+    s.q = 0;                                        // q [ct][dk] io (reverse half)
+    s.k = s.q + align16(ct * dk * io_bytes);        // k [ct][dk] io
+    s.u = s.k + align16(ct * dk * io_bytes);        // u [ct][R][dk] io
+    s.row = s.u + align16(ct * R * dk * io_bytes);  // v (io) or dout (fp32) of the ROWS rows, 64 B a token
+    s.x = s.row + ct * ROWS * 4;                    // x [ct][R][ROWS] fp32 (forward half)
+    s.gate = s.x + ct * R * ROWS * 4;               // alpha [ct], beta [ct] fp32
+    s.bytes = s.gate + align16(2 * ct * 4);
+    return s;
+}
+
+// Queue the copies of tokens [t0, t0 + n) of sequence bh for rows i0 .. i0 + ROWS - 1.
+template <typename io_t, int DK>
+__device__ __forceinline__ void stage_issue(char *buf, const StageLayout &L, bool reverse, const io_t *q,
+                                            const io_t *k, const io_t *u, const io_t *v, const float *dout,
+                                            const float *X, const float *alpha, const float *beta, int bh, int T,
+                                            int t0, int n, int dv, int R, int i0)
+{
+    const int tid = threadIdx.x, nth = SCAN_WARPS * 32;
+    const size_t tok0 = (size_t)bh * T + t0;
+    constexpr int PER16 = 16 / sizeof(io_t);
+    const int nk = n * DK / PER16;  // 16-byte pieces of k (and q)
+    for (int p = tid; p < nk; p += nth) {
+        cp16(buf + L.k + p * 16, k + tok0 * DK + (size_t)p * PER16);
+        if (reverse) cp16(buf + L.q + p * 16, q + tok0 * DK + (size_t)p * PER16);
+    }
+    const int nu = n * R * DK / PER16;
+    for (int p = tid; p < nu; p += nth) cp16(buf + L.u + p * 16, u + tok0 * R * DK + (size_t)p * PER16);
+    // the rows' entries of v (ROWS io values) or of dout (ROWS floats): 16-byte pieces
+    const int row_pieces = reverse ? ROWS * 4 / 16 : ROWS * (int)sizeof(io_t) / 16;
+    for (int p = tid; p < n * row_pieces; p += nth) {
+        const int tt = p / row_pieces, pc = p % row_pieces;
+        if (reverse) cp16(buf + L.row + tt * ROWS * 4 + pc * 16, dout + (tok0 + tt) * dv + i0 + pc * 4);
+        else cp16(buf + L.row + tt * ROWS * 4 + pc * 16, v + (tok0 + tt) * dv + i0 + pc * PER16);
+    }
+    for (int p = tid; p < n; p += nth) {
+        cp4(buf + L.gate + p * 4, alpha + tok0 + p);
+        cp4(buf + L.gate + (n + p) * 4, beta + tok0 + p);
+    }
+    if (!reverse)
+        for (int p = tid; p < n * R * (ROWS / 4); p += nth) {
+            const int tl = p / (ROWS / 4), pc = p % (ROWS / 4);  // (token, level) pair and its piece
+            cp16(buf + L.x + tl * ROWS * 4 + pc * 16, X + ((tok0 + tl / R) * R + tl % R) * dv + i0 + pc * 4);
+        }
+}
+
+// blockIdx.z = 0: S_{t-1} of every token (forward order) -> Sp.
+// blockIdx.z = 1: dS_t of every token (reverse order) -> Gs, with z_t = dS_t k_t -> Z and
+//                 dx_{t,l} = dS_t u_{t,l} -> dX; the last cotangent -> dS_init.
+template <typename io_t, int DK>
+__global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(
+    const io_t *__restrict__ q, const io_t *__restrict__ k, const io_t *__restrict__ v, const io_t *__restrict__ u,
+    const float *__restrict__ beta, const float *__restrict__ alpha, const float *__restrict__ X,
+    const float *__restrict__ S_init, const float *__restrict__ dout, const float *__restrict__ dS_final,
+    float *__restrict__ Sp, float *__restrict__ Gs, float *__restrict__ Z, float *__restrict__ dX,
+    float *__restrict__ dS_init, int T, int dv, int R, int ct)
+{
+    constexpr int NPL = DK / LPR;  // columns per lane
+    extern __shared__ __align__(16) char stage[];
+    const bool rev = blockIdx.z == 1;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int rw = w * (32 / LPR) + lane / LPR;  // row within the block
+    const int col = (lane % LPR) * NPL;          // first column of this lane
+    const bool lead = (lane % LPR) == 0;
+    const int bh = blockIdx.y, i0 = blockIdx.x * ROWS, i = i0 + rw;  // grid.x = dv / ROWS
+    const size_t DD = (size_t)dv * DK;
+    const StageLayout L = stage_layout(ct, DK, R, sizeof(io_t));
+    const int nch = (T + ct - 1) / ct;
+    float S[NPL];
+    const float *S0 = rev ? dS_final : S_init;
+    if (S0) load_vec(S0 + bh * DD + (size_t)i * DK + col, S);
+    else
+#pragma unroll
+        for (int e = 0; e < NPL; ++e) S[e] = 0.f;
+
+    auto issue = [&](int c) {
+        const int t0 = (rev ? nch - 1 - c : c) * ct;
+        stage_issue<io_t, DK>(stage + (c & 1) * L.bytes, L, rev, q, k, u, v, dout, X, alpha, beta, bh, T, t0,
+                              min(ct, T - t0), dv, R, i0);
+        cp_commit();
+    };
+    issue(0);
+    for (int c = 0; c < nch; ++c) {
+        if (c + 1 < nch) {
+            issue(c + 1);
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
+        __syncthreads();
+        const char *b = stage + (c & 1) * L.bytes;
+        const int t0 = (rev ? nch - 1 - c : c) * ct, n = min(ct, T - t0);
+        const io_t *kS = reinterpret_cast<const io_t *>(b + L.k);
+        const io_t *uS = reinterpret_cast<const io_t *>(b + L.u);
+        const float *aS = reinterpret_cast<const float *>(b + L.gate), *bS = aS + n;
+        if (!rev) {
+            const io_t *vS = reinterpret_cast<const io_t *>(b + L.row);
+            const float *xS = reinterpret_cast<const float *>(b + L.x);
+            for (int tt = 0; tt < n; ++tt) {
+                const size_t tok = (size_t)bh * T + t0 + tt;
+                float kk[NPL];
+                load_vec(kS + tt * DK + col, kk);
+                store_vec(Sp + tok * DD + (size_t)i * DK + col, S);
+                float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < NPL; e += 2) {
+                    y0 = fmaf(S[e], kk[e], y0);
+                    y1 = fmaf(S[e + 1], kk[e + 1], y1);
+                }
+                const float y = row_sum(y0 + y1);
+                const float al = aS[tt], be = bS[tt];
+                const float vi = ldf(vS + tt * (ROWS * 4 / sizeof(io_t)) + rw);
+#pragma unroll
+                for (int e = 0; e < NPL; ++e) S[e] = fmaf(al, fmaf(-be * y, kk[e], S[e]), be * vi * kk[e]);
+                for (int l = 0; l < R; ++l) {
+                    const float xl = xS[(tt * R + l) * ROWS + rw];
+                    float ul[NPL];
+                    load_vec(uS + (tt * R + l) * DK + col, ul);
+#pragma unroll
+                    for (int e = 0; e < NPL; ++e) S[e] = fmaf(xl, ul[e], S[e]);
+                }
+            }
+        } else {
+            const io_t *qS = reinterpret_cast<const io_t *>(b + L.q);
+            const float *dS = reinterpret_cast<const float *>(b + L.row);
+            for (int tt = n - 1; tt >= 0; --tt) {
+                const size_t tok = (size_t)bh * T + t0 + tt;
+                const float di = dS[tt * ROWS + rw];
+                float kk[NPL], qq[NPL];
+                load_vec(kS + tt * DK + col, kk);
+                load_vec(qS + tt * DK + col, qq);
+                float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < NPL; ++e) S[e] = fmaf(di, qq[e], S[e]);
+                store_vec(Gs + tok * DD + (size_t)i * DK + col, S);
+#pragma unroll
+                for (int e = 0; e < NPL; e += 2) {
+                    z0 = fmaf(S[e], kk[e], z0);
+                    z1 = fmaf(S[e + 1], kk[e + 1], z1);
+                }
+                const float z = row_sum(z0 + z1);
+                for (int l = 0; l < R; ++l) {
+                    float ul[NPL];
+                    load_vec(uS + (tt * R + l) * DK + col, ul);
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < NPL; e += 2) {
+                        s0 = fmaf(S[e], ul[e], s0);
+                        s1 = fmaf(S[e + 1], ul[e + 1], s1);
+                    }
+                    const float s = row_sum(s0 + s1);
+                    if (lead) dX[(tok * R + l) * dv + i] = s;
+                }
+                if (lead) Z[tok * dv + i] = z;
+                const float al = aS[tt], be = bS[tt];
+#pragma unroll
+                for (int e = 0; e < NPL; ++e) S[e] = al * fmaf(-be * z, kk[e], S[e]);
+            }
+        }
+        __syncthreads();  // the buffer is refilled by the copies issued in the next iteration
+    }
+    if (rev && dS_init) store_vec(dS_init + bh * DD + (size_t)i * DK + col, S);
+}
+
+// Tokens per stage buffer: the largest power of two up to 32 whose two buffers fit in kScanSmem.
+constexpr int kScanSmem = 96 * 1024;
+inline int scan_chunk(int dk, int R, int io_bytes)
+{
+    int ct = 32;
+    while (ct > 1 && 2 * stage_layout(ct, dk, R, io_bytes).bytes > kScanSmem) ct >>= 1;
+    return ct;
+}
+
+// Shared-memory floats of token_grad_kernel.
+__host__ __device__ constexpr size_t token_grad_smem_floats(int dk, int dv, int R)
+{
+    return (size_t)dv * dk + dk + 4 * (size_t)dv + (size_t)R * dv + (size_t)(NT / dk) * (3 + R) * dk +
+           (NT / 32) * (4 + R) + NT / 32 + 4 + R;
+}
+
+// Per token: dq, dk, du, dalpha, dbeta and dv <- beta z (the later kernels add to dv).
+template <typename io_t, int DK>
+__global__ void __launch_bounds__(NT) token_grad_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
+                                                        const io_t *__restrict__ v, const io_t *__restrict__ u,
+                                                        const float *__restrict__ beta,
+                                                        const float *__restrict__ alpha,
+                                                        const float *__restrict__ X, const float *__restrict__ Sp,
+                                                        const float *__restrict__ Gs, const float *__restrict__ Z,
+                                                        const float *__restrict__ dout, float *__restrict__ dq,
+                                                        float *__restrict__ dk, float *__restrict__ dv_out,
+                                                        float *__restrict__ dbeta, float *__restrict__ dalpha,
+                                                        float *__restrict__ du, long long ntok, int dv, int R)
+{
+    constexpr int NG = NT / DK;  // row groups of the column sums
+    const int NS = 4 + R;        // per-token scalars: y.dout, v.dout, y.z, v.z, x_l.dout
+    extern __shared__ float sm[];
+    float *Ps = sm;                         // [dv][DK]  S_{t-1}
+    float *ks = Ps + (size_t)dv * DK;       // [DK]
+    float *ys = ks + DK;                    // [dv]  y = S_{t-1} k
+    float *ws = ys + dv;                    // [dv]  beta v - alpha beta y
+    float *ds = ws + dv;                    // [dv]  dout_t
+    float *zs = ds + dv;                    // [dv]  z
+    float *xs = zs + dv;                    // [R][dv]
+    float *cs = xs + (size_t)R * dv;        // [NG][3 + R][DK]
+    float *red = cs + (size_t)NG * (3 + R) * DK;  // [NT/32][NS]
+    float *redp = red + (NT / 32) * NS;     // [NT/32]  <dS_t, S_{t-1}> per warp
+    float *scal = redp + NT / 32;           // [NS]
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    for (long long tok = blockIdx.x; tok < ntok; tok += gridDim.x) {
+        const float al = alpha[tok], be = beta[tok];
+        const float4 *P4 = reinterpret_cast<const float4 *>(Sp + (size_t)tok * dv * DK);
+        for (int n = tid; n < dv * DK / 4; n += NT) reinterpret_cast<float4 *>(Ps)[n] = P4[n];
+        for (int j = tid; j < DK; j += NT) ks[j] = ldf(k + (size_t)tok * DK + j);
+        if (tid < dv) {
+            ds[tid] = dout[(size_t)tok * dv + tid];
+            zs[tid] = Z[(size_t)tok * dv + tid];
+            for (int l = 0; l < R; ++l) xs[l * dv + tid] = X[((size_t)tok * R + l) * dv + tid];
+        }
+        __syncthreads();
+        for (int i = wid; i < dv; i += NT / 32) {
+            float s = 0.f;
+            for (int j = lane; j < DK; j += 32) s = fmaf(Ps[i * DK + j], ks[j], s);
+            s = warp_sum(s);
+            if (lane == 0) ys[i] = s;
+        }
+        __syncthreads();
+        if (tid < dv) {  // dv is a multiple of 32: whole warps
+            const float yi = ys[tid], vi = ldf(v + (size_t)tok * dv + tid), di = ds[tid], zi = zs[tid];
+            ws[tid] = be * vi - al * be * yi;
+            dv_out[(size_t)tok * dv + tid] = be * zi;
+            float part[4] = {yi * di, vi * di, yi * zi, vi * zi};
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const float r = warp_sum(part[s]);
+                if (lane == 0) red[wid * NS + s] = r;
+            }
+            for (int l = 0; l < R; ++l) {
+                const float r = warp_sum(xs[l * dv + tid] * di);
+                if (lane == 0) red[wid * NS + 4 + l] = r;
+            }
+        }
+        __syncthreads();
+        if (tid < NS) {
+            float s = 0.f;
+            for (int w = 0; w < dv / 32; ++w) s += red[w * NS + tid];
+            scal[tid] = s;
+        }
+        // column sums over the rows of group g
+        {
+            const int g = tid / DK, j = tid % DK;
+            float a = 0.f, c = 0.f, b = 0.f, dsp = 0.f, dul[RMAX];
+#pragma unroll
+            for (int l = 0; l < RMAX; ++l) dul[l] = 0.f;
+            const float *G = Gs + (size_t)tok * dv * DK;
+            for (int i = g; i < dv; i += NG) {
+                const float p = Ps[i * DK + j], gg = G[(size_t)i * DK + j];
+                a = fmaf(p, ds[i], a);
+                c = fmaf(p, zs[i], c);
+                b = fmaf(gg, ws[i], b);
+                dsp = fmaf(gg, p, dsp);
+#pragma unroll
+                for (int l = 0; l < RMAX; ++l)
+                    if (l < R) dul[l] = fmaf(gg, xs[l * dv + i], dul[l]);
+            }
+            float *cg = cs + (size_t)g * (3 + R) * DK;
+            cg[j] = a;
+            cg[DK + j] = c;
+            cg[2 * DK + j] = b;
+#pragma unroll
+            for (int l = 0; l < RMAX; ++l)
+                if (l < R) cg[(3 + l) * DK + j] = dul[l];
+            dsp = warp_sum(dsp);
+            if (lane == 0) redp[wid] = dsp;
+        }
+        __syncthreads();
+        if (tid < DK) {
+            const int j = tid;
+            float A = 0.f, Cc = 0.f, Bb = 0.f;
+            for (int g = 0; g < NG; ++g) {
+                const float *cg = cs + (size_t)g * (3 + R) * DK;
+                A += cg[j];
+                Cc += cg[DK + j];
+                Bb += cg[2 * DK + j];
+            }
+            const float kj = ks[j];
+            float dqj = al * A - al * be * kj * scal[0] + be * kj * scal[1];
+            for (int l = 0; l < R; ++l) {
+                float Ul = 0.f;
+                for (int g = 0; g < NG; ++g) Ul += cs[((size_t)g * (3 + R) + 3 + l) * DK + j];
+                du[((size_t)tok * R + l) * DK + j] = Ul;
+                dqj = fmaf(ldf(u + ((size_t)tok * R + l) * DK + j), scal[4 + l], dqj);
+            }
+            dq[(size_t)tok * DK + j] = dqj;
+            dk[(size_t)tok * DK + j] = Bb - al * be * Cc;
+        }
+        if (tid == 0) {
+            float s = 0.f;
+            for (int w = 0; w < NT / 32; ++w) s += redp[w];
+            dalpha[tok] = s - be * scal[2];
+            dbeta[tok] = scal[3] - al * scal[2];
+        }
+        __syncthreads();  // the shared buffers are reused by the next token
+    }
+}
+
+// The residual chain and the gain backwards, one block of NT threads over NT / dv tokens.
+template <typename io_t>
+__global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
+                                                        const io_t *__restrict__ conv_w,
+                                                        const float *__restrict__ gamma,
+                                                        const float *__restrict__ eta, const float *__restrict__ dX,
+                                                        float *__restrict__ dH, float *__restrict__ dv_out,
+                                                        float *__restrict__ dgamma, float *__restrict__ deta,
+                                                        long long ntok, int H, int T, int dv, int R)
+{
+    __shared__ float red[NT / 32][2 * RMAX];
+    const int tpb = NT / dv;
+    const int slot = threadIdx.x / dv, c = threadIdx.x % dv;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, wpt = dv / 32;  // warps per token
+    for (long long base = (long long)blockIdx.x * tpb; base < ntok; base += (long long)gridDim.x * tpb) {
+        const long long tok = base + slot;
+        const bool live = tok < ntok;  // uniform over a warp (dv is a multiple of 32)
+        float dgam[RMAX], det[RMAX];
+#pragma unroll
+        for (int l = 0; l < RMAX; ++l) dgam[l] = det[l] = 0.f;
+        if (live) {
+            const int bh = (int)(tok / T), t = (int)(tok % T);
+            float a, Phi, phi;
+            anchor_at(v, v_hist, conv_w, bh, bh % H, t, T, dv, c, a, Phi, phi);
+            const float g = fmaf(a, phi, Phi);
+            float rl[RMAX];
+            float r = ldf(v + (size_t)tok * dv + c) - a * Phi;
+#pragma unroll
+            for (int l = 0; l < RMAX; ++l)
+                if (l < R) {
+                    rl[l] = r;
+                    r *= 1.f - eta[(size_t)tok * R + l] * g;
+                }
+            float drn = 0.f, dg = 0.f;
+#pragma unroll
+            for (int l = RMAX - 1; l >= 0; --l)
+                if (l < R) {
+                    const float gm = gamma[(size_t)tok * R + l], et = eta[(size_t)tok * R + l];
+                    const float dx = dX[((size_t)tok * R + l) * dv + c];
+                    dgam[l] = g * rl[l] * dx;
+                    det[l] = -g * rl[l] * drn;
+                    dg += gm * rl[l] * dx - et * rl[l] * drn;
+                    drn = gm * g * dx + (1.f - et * g) * drn;
+                }
+            dv_out[(size_t)tok * dv + c] += drn;
+            dH[(size_t)tok * dv + c] = -g * drn + phi * (2.f - a * a) * dg;
+        }
+#pragma unroll
+        for (int l = 0; l < RMAX; ++l)
+            if (l < R) {
+                const float s1 = warp_sum(dgam[l]), s2 = warp_sum(det[l]);
+                if (lane == 0) {
+                    red[wid][2 * l] = s1;
+                    red[wid][2 * l + 1] = s2;
+                }
+            }
+        __syncthreads();
+        if (live && c < 2 * R) {
+            float s = 0.f;
+            for (int w = 0; w < wpt; ++w) s += red[slot * wpt + w][c];
+            const int l = c >> 1;
+            if (c & 1) deta[(size_t)tok * R + l] = s;
+            else dgamma[(size_t)tok * R + l] = s;
+        }
+        __syncthreads();
+    }
+}
+
+// The convolution backwards over tiles of CT tokens: v's share of dv, dv_hist (first tile)
+// and the tile's sums for dconv_w -> dWp [BH][ntile][4][dv].
+template <typename io_t>
+__global__ void conv_grad_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
+                                 const io_t *__restrict__ conv_w, const float *__restrict__ dH,
+                                 float *__restrict__ dv_out, float *__restrict__ dv_hist, float *__restrict__ dWp,
+                                 int H, int T, int dv, int ntile)
+{
+    const int c = threadIdx.x, bh = blockIdx.y, tile = blockIdx.x, h = bh % H;  // blockDim.x = dv
+    const int t0 = tile * CT, t1 = min(T, t0 + CT);
+    float w[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = ldf(conv_w + ((size_t)h * 4 + j) * dv + c);
+    const size_t base = (size_t)bh * T;
+    for (int t = t0; t < t1; ++t) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (t + j < T) s = fmaf(w[j], dH[(base + t + j) * dv + c], s);
+        dv_out[(base + t) * dv + c] += s;
+        const float d = dH[(base + t) * dv + c];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int src = t - j;
+            const float vv = src >= 0 ? ldf(v + (base + src) * dv + c)
+                                      : (v_hist ? ldf(v_hist + ((size_t)bh * 3 + 3 + src) * dv + c) : 0.f);
+            acc[j] = fmaf(d, vv, acc[j]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dWp[(((size_t)bh * ntile + tile) * 4 + j) * dv + c] = acc[j];
+    if (tile == 0 && dv_hist) {
+        // slot s holds v_{s-3}, which enters h_t through tap j = t - s + 3 for t in [0, s]
+        for (int s = 0; s < 3; ++s) {
+            float g = 0.f;
+            for (int t = 0; t <= s && t < T; ++t) g = fmaf(w[t - s + 3], dH[(base + t) * dv + c], g);
+            dv_hist[((size_t)bh * 3 + s) * dv + c] = g;
+        }
+    }
+}
+
+// dconv_w[h][j][c] = sum over the batch and the tiles of dWp.
+__global__ void conv_reduce_kernel(const float *__restrict__ dWp, float *__restrict__ dconv_w, int B, int H, int dv,
+                                   int ntile)
+{
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= H * 4 * dv) return;
+    const int h = idx / (4 * dv), jc = idx % (4 * dv);
+    float s = 0.f;
+    for (int b = 0; b < B; ++b)
+        for (int tile = 0; tile < ntile; ++tile) s += dWp[(((size_t)b * H + h) * ntile + tile) * 4 * dv + jc];
+    dconv_w[idx] = s;
+}
+
+struct Carve {
+    float *X, *Sp, *Gs, *Z, *dX, *dH, *dWp;
+};
+
+size_t carve(const Shape &s, void *base, Carve *out)
+{
+    Carve scratch{};
+    Carve *w = out ? out : &scratch;
+    const size_t th = (size_t)s.BH * s.T;
+    const int ntile = (s.T + CT - 1) / CT;
+    const size_t n[7] = {th * s.R * s.dv, th * s.dv * s.dk, th * s.dv * s.dk, th * s.dv, th * s.R * s.dv,
+                         th * s.dv, (size_t)s.BH * ntile * 4 * s.dv};
+    float **dst[7] = {&w->X, &w->Sp, &w->Gs, &w->Z, &w->dX, &w->dH, &w->dWp};
+    size_t off = 0;
+    for (int i = 0; i < 7; ++i) {
+        if (base) *dst[i] = reinterpret_cast<float *>(static_cast<char *>(base) + off);
+        off += (n[i] * sizeof(float) + 255) & ~(size_t)255;
+    }
+    return off;
+}
+
+template <typename io_t, int DK>
+cudaError_t launch(const Shape &s, const BackwardArgs &a, void *ws, KernelTimer &tm)
+{
+    Carve w{};
+    carve(s, ws, &w);
+    cudaStream_t st = tm.stream;
+    const io_t *q = static_cast<const io_t *>(a.q), *k = static_cast<const io_t *>(a.k);
+    const io_t *v = static_cast<const io_t *>(a.v), *u = static_cast<const io_t *>(a.u);
+    const io_t *cw = static_cast<const io_t *>(a.conv_w), *vh = static_cast<const io_t *>(a.v_hist);
+    const long long ntok = (long long)s.BH * s.T;
+    const int ntile = (s.T + CT - 1) / CT;
+    if (s.R > 0) {
+        tm.begin("bwd_factors");
+        factors_kernel<io_t><<<dim3((unsigned)(((long long)s.T * s.dv + NT - 1) / NT), s.BH), NT, 0, st>>>(
+            v, vh, cw, a.gamma, a.eta, w.X, s.H, s.T, s.dv, s.R);
+        tm.end();
+    }
+    const int ct = scan_chunk(DK, s.R, sizeof(io_t));
+    const size_t scan_smem = 2 * (size_t)stage_layout(ct, DK, s.R, sizeof(io_t)).bytes;
+    tm.begin("bwd_scan");
+    scan_kernel<io_t, DK><<<dim3(s.dv / ROWS, s.BH, 2), SCAN_WARPS * 32, scan_smem, st>>>(
+        q, k, v, u, a.beta, a.alpha, w.X, a.S_init, a.dout, a.dS_final, w.Sp, w.Gs, w.Z, w.dX, a.dS_init, s.T, s.dv,
+        s.R, ct);
+    tm.end();
+    const size_t smem = token_grad_smem_floats(DK, s.dv, s.R) * sizeof(float);
+    const long long tg_grid = ntok < (1LL << 30) ? ntok : (1LL << 30);
+    tm.begin("bwd_token_grad");
+    token_grad_kernel<io_t, DK><<<(unsigned)tg_grid, NT, smem, st>>>(q, k, v, u, a.beta, a.alpha, w.X, w.Sp, w.Gs,
+                                                                     w.Z, a.dout, a.dq, a.dk, a.dv, a.dbeta,
+                                                                     a.dalpha, a.du, ntok, s.dv, s.R);
+    tm.end();
+    const int tpb = NT / s.dv;
+    long long cg_grid = (ntok + tpb - 1) / tpb;
+    if (cg_grid > (1LL << 30)) cg_grid = 1LL << 30;
+    tm.begin("bwd_chain_grad");
+    chain_grad_kernel<io_t><<<(unsigned)cg_grid, NT, 0, st>>>(v, vh, cw, a.gamma, a.eta, w.dX, w.dH, a.dv, a.dgamma,
+                                                              a.deta, ntok, s.H, s.T, s.dv, s.R);
+    tm.end();
+    tm.begin("bwd_conv_grad");
+    conv_grad_kernel<io_t><<<dim3(ntile, s.BH), s.dv, 0, st>>>(v, vh, cw, w.dH, a.dv, a.dv_hist, w.dWp, s.H, s.T,
+                                                               s.dv, ntile);
+    tm.end();
+    tm.begin("bwd_conv_reduce");
+    conv_reduce_kernel<<<(s.H * 4 * s.dv + NT - 1) / NT, NT, 0, st>>>(w.dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
+    tm.end();
+    return cudaGetLastError();
+}
+
+template <typename io_t, int DK>
+cudaError_t set_smem()
+{
+    const size_t most = token_grad_smem_floats(DK, 128, RMAX) * sizeof(float);
+    cudaError_t e =
+        cudaFuncSetAttribute(token_grad_kernel<io_t, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(scan_kernel<io_t, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+}
+
+}  // namespace bwd
+
+size_t backward_workspace_bytes(const Shape &s) { return bwd::carve(s, nullptr, nullptr); }
+
+cudaError_t backward_prepare()
+{
+    cudaError_t e;
+    if ((e = bwd::set_smem<float, 64>()) != cudaSuccess) return e;
+    if ((e = bwd::set_smem<float, 128>()) != cudaSuccess) return e;
+    if ((e = bwd::set_smem<__nv_bfloat16, 64>()) != cudaSuccess) return e;
+    return bwd::set_smem<__nv_bfloat16, 128>();
+}
+
+cudaError_t backward(const Shape &s, prism_dtype io, const BackwardArgs &a, void *ws, KernelTimer &tm)
+{
+    if (io == PRISM_BF16)
+        return s.dk == 64 ? bwd::launch<__nv_bfloat16, 64>(s, a, ws, tm) : bwd::launch<__nv_bfloat16, 128>(s, a, ws, tm);
+    return s.dk == 64 ? bwd::launch<float, 64>(s, a, ws, tm) : bwd::launch<float, 128>(s, a, ws, tm);
+}
+
+}  // namespace prism

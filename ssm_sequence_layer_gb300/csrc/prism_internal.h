@@ -108,6 +108,18 @@ struct DecodeArgs {
 cudaError_t decode_step(const Shape &s, prism_dtype io, prism_dtype out, const DecodeArgs &a, int sm_count,
                         int *d_status, long long wait_ns, KernelTimer &tm);
 
+// Pointers of one backward call (layouts as in prism.h, prism_backward).  v_hist, S_init,
+// dS_final, dv_hist and dS_init may be null; u, gamma, eta, du, dgamma and deta are not read or
+// written when R = 0.
+struct BackwardArgs {
+    const void *q, *k, *v, *u, *conv_w, *v_hist;
+    const float *beta, *alpha, *gamma, *eta, *S_init, *dout, *dS_final;
+    float *dq, *dk, *dv, *dbeta, *dalpha, *du, *dgamma, *deta, *dconv_w, *dv_hist, *dS_init;
+};
+size_t backward_workspace_bytes(const Shape &s);
+cudaError_t backward_prepare();
+cudaError_t backward(const Shape &s, prism_dtype io, const BackwardArgs &a, void *ws, KernelTimer &tm);
+
 size_t simt_workspace_bytes(const Shape &s);
 void simt_carve(const Shape &s, void *base, SimtWorkspace *w);
 cudaError_t simt_prepare(const Shape &s, prism_dtype io);
@@ -138,6 +150,9 @@ struct prism_plan_s {
     void *ws_tc;
     size_t ws_tc_bytes;
     prism::TcWorkspace tcw;
+    // workspace of the backward pass (owned, allocated by the first prism_backward)
+    void *ws_bwd;
+    size_t ws_bwd_bytes;
     // device staging buffers for prism_forward_host (owned, allocated on first use)
     void *stage;
     size_t stage_bytes;
