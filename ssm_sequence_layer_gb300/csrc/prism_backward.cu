@@ -210,10 +210,89 @@ __device__ __forceinline__ void stage_issue(char *buf, const StageLayout &L, boo
         }
 }
 
+// NPL io values as raw 16-byte words (read from shared memory ahead of their use).
+template <typename io_t, int N>
+struct Raw {
+    static constexpr int W = N * (int)sizeof(io_t) / 16;
+    uint4 w[W];
+};
+template <typename io_t, int N>
+__device__ __forceinline__ void load_raw(const io_t *p, Raw<io_t, N> &r)
+{
+#pragma unroll
+    for (int j = 0; j < Raw<io_t, N>::W; ++j) r.w[j] = reinterpret_cast<const uint4 *>(p)[j];
+}
+template <int N>
+__device__ __forceinline__ void unpack(const Raw<float, N> &r, float (&o)[N])
+{
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j) {
+        o[4 * j] = __uint_as_float(r.w[j].x);
+        o[4 * j + 1] = __uint_as_float(r.w[j].y);
+        o[4 * j + 2] = __uint_as_float(r.w[j].z);
+        o[4 * j + 3] = __uint_as_float(r.w[j].w);
+    }
+}
+template <int N>
+__device__ __forceinline__ void unpack(const Raw<__nv_bfloat16, N> &r, float (&o)[N])
+{
+    // a 32-bit word holds two consecutive bf16 values, the first in its low half
+#pragma unroll
+    for (int j = 0; j < N / 8; ++j) {
+        const uint32_t wd[4] = {r.w[j].x, r.w[j].y, r.w[j].z, r.w[j].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            o[8 * j + 2 * h] = __uint_as_float(wd[h] << 16);
+            o[8 * j + 2 * h + 1] = __uint_as_float(wd[h] & 0xffff0000u);
+        }
+    }
+}
+
+// One token's inputs for a lane of the forward half and of the reverse half.
+template <typename io_t, int N, int RT>
+struct FwdTok {
+    Raw<io_t, N> k, u[RT > 0 ? RT : 1];
+    float x[RT > 0 ? RT : 1], a, b, v;
+};
+template <typename io_t, int N, int RT>
+struct RevTok {
+    Raw<io_t, N> k, q, u[RT > 0 ? RT : 1];
+    float d, a, b;
+};
+template <typename io_t, int N, int RT>
+__device__ __forceinline__ void fetch_fwd(FwdTok<io_t, N, RT> &f, const io_t *kS, const io_t *uS, const float *xS,
+                                          const io_t *vS, const float *aS, const float *bS, int tt, int dk, int col,
+                                          int rw)
+{
+    load_raw(kS + tt * dk + col, f.k);
+#pragma unroll
+    for (int l = 0; l < RT; ++l) {
+        load_raw(uS + (tt * RT + l) * dk + col, f.u[l]);
+        f.x[l] = xS[(tt * RT + l) * ROWS + rw];
+    }
+    f.a = aS[tt];
+    f.b = bS[tt];
+    f.v = ldf(vS + tt * (ROWS * 4 / (int)sizeof(io_t)) + rw);
+}
+template <typename io_t, int N, int RT>
+__device__ __forceinline__ void fetch_rev(RevTok<io_t, N, RT> &f, const io_t *kS, const io_t *qS, const io_t *uS,
+                                          const float *dS, const float *aS, const float *bS, int tt, int dk, int col,
+                                          int rw)
+{
+    load_raw(kS + tt * dk + col, f.k);
+    load_raw(qS + tt * dk + col, f.q);
+#pragma unroll
+    for (int l = 0; l < RT; ++l) load_raw(uS + (tt * RT + l) * dk + col, f.u[l]);
+    f.d = dS[tt * ROWS + rw];
+    f.a = aS[tt];
+    f.b = bS[tt];
+}
+
 // blockIdx.z = 0: S_{t-1} of every token (forward order) -> Sp.
 // blockIdx.z = 1: dS_t of every token (reverse order) -> Gs, with z_t = dS_t k_t -> Z and
 //                 dx_{t,l} = dS_t u_{t,l} -> dX; the last cotangent -> dS_init.
-template <typename io_t, int DK>
+// RT >= 0: R = RT levels, known at compile time; RT = -1: any R.
+template <typename io_t, int DK, int RT>
 __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(
     const io_t *__restrict__ q, const io_t *__restrict__ k, const io_t *__restrict__ v, const io_t *__restrict__ u,
     const float *__restrict__ beta, const float *__restrict__ alpha, const float *__restrict__ X,
@@ -259,7 +338,85 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(
         const io_t *kS = reinterpret_cast<const io_t *>(b + L.k);
         const io_t *uS = reinterpret_cast<const io_t *>(b + L.u);
         const float *aS = reinterpret_cast<const float *>(b + L.gate), *bS = aS + n;
-        if (!rev) {
+        if constexpr (RT >= 0) {
+            // the level count is known: each token's shared-memory inputs are read one token
+            // ahead into registers, and the rank-R injection is formed off the chain
+            if (!rev) {
+                const io_t *vS = reinterpret_cast<const io_t *>(b + L.row);
+                const float *xS = reinterpret_cast<const float *>(b + L.x);
+                FwdTok<io_t, NPL, RT> cur, nxt;
+                fetch_fwd(cur, kS, uS, xS, vS, aS, bS, 0, DK, col, rw);
+                for (int tt = 0; tt < n; ++tt) {
+                    fetch_fwd(nxt, kS, uS, xS, vS, aS, bS, min(tt + 1, n - 1), DK, col, rw);
+                    const size_t tok = (size_t)bh * T + t0 + tt;
+                    float kk[NPL];
+                    unpack(cur.k, kk);
+                    store_vec(Sp + tok * DD + (size_t)i * DK + col, S);
+                    float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < NPL; e += 2) {
+                        y0 = fmaf(S[e], kk[e], y0);
+                        y1 = fmaf(S[e + 1], kk[e + 1], y1);
+                    }
+                    const float y = row_sum(y0 + y1);
+                    float wv[NPL];  // beta v k + sum_l x_l u_l: does not depend on S
+                    const float bv = cur.b * cur.v;
+#pragma unroll
+                    for (int e = 0; e < NPL; ++e) wv[e] = bv * kk[e];
+#pragma unroll
+                    for (int l = 0; l < RT; ++l) {
+                        float ul[NPL];
+                        unpack(cur.u[l], ul);
+#pragma unroll
+                        for (int e = 0; e < NPL; ++e) wv[e] = fmaf(cur.x[l], ul[e], wv[e]);
+                    }
+                    const float c = -cur.b * y;
+#pragma unroll
+                    for (int e = 0; e < NPL; ++e) S[e] = fmaf(cur.a, fmaf(c, kk[e], S[e]), wv[e]);
+                    cur = nxt;
+                }
+            } else {
+                const io_t *qS = reinterpret_cast<const io_t *>(b + L.q);
+                const float *dS = reinterpret_cast<const float *>(b + L.row);
+                RevTok<io_t, NPL, RT> cur, nxt;
+                fetch_rev(cur, kS, qS, uS, dS, aS, bS, n - 1, DK, col, rw);
+                for (int tt = n - 1; tt >= 0; --tt) {
+                    fetch_rev(nxt, kS, qS, uS, dS, aS, bS, max(tt - 1, 0), DK, col, rw);
+                    const size_t tok = (size_t)bh * T + t0 + tt;
+                    float kk[NPL], qq[NPL];
+                    unpack(cur.k, kk);
+                    unpack(cur.q, qq);
+#pragma unroll
+                    for (int e = 0; e < NPL; ++e) S[e] = fmaf(cur.d, qq[e], S[e]);
+                    store_vec(Gs + tok * DD + (size_t)i * DK + col, S);
+                    float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < NPL; e += 2) {
+                        z0 = fmaf(S[e], kk[e], z0);
+                        z1 = fmaf(S[e + 1], kk[e + 1], z1);
+                    }
+                    const float z = row_sum(z0 + z1);
+#pragma unroll
+                    for (int l = 0; l < RT; ++l) {
+                        float ul[NPL];
+                        unpack(cur.u[l], ul);
+                        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                        for (int e = 0; e < NPL; e += 2) {
+                            s0 = fmaf(S[e], ul[e], s0);
+                            s1 = fmaf(S[e + 1], ul[e + 1], s1);
+                        }
+                        const float s = row_sum(s0 + s1);
+                        if (lead) dX[(tok * RT + l) * dv + i] = s;
+                    }
+                    if (lead) Z[tok * dv + i] = z;
+                    const float c = -cur.b * z;
+#pragma unroll
+                    for (int e = 0; e < NPL; ++e) S[e] = cur.a * fmaf(c, kk[e], S[e]);
+                    cur = nxt;
+                }
+            }
+        } else if (!rev) {
             const io_t *vS = reinterpret_cast<const io_t *>(b + L.row);
             const float *xS = reinterpret_cast<const float *>(b + L.x);
             for (int tt = 0; tt < n; ++tt) {
@@ -632,9 +789,18 @@ cudaError_t launch(const Shape &s, const BackwardArgs &a, void *ws, KernelTimer 
     const int ct = scan_chunk(DK, s.R, sizeof(io_t));
     const size_t scan_smem = 2 * (size_t)stage_layout(ct, DK, s.R, sizeof(io_t)).bytes;
     tm.begin("bwd_scan");
-    scan_kernel<io_t, DK><<<dim3(s.dv / ROWS, s.BH, 2), SCAN_WARPS * 32, scan_smem, st>>>(
-        q, k, v, u, a.beta, a.alpha, w.X, a.S_init, a.dout, a.dS_final, w.Sp, w.Gs, w.Z, w.dX, a.dS_init, s.T, s.dv,
-        s.R, ct);
+    auto kern = scan_kernel<io_t, DK, -1>;
+    switch (s.R) {
+    case 0: kern = scan_kernel<io_t, DK, 0>; break;
+    case 1: kern = scan_kernel<io_t, DK, 1>; break;
+    case 2: kern = scan_kernel<io_t, DK, 2>; break;
+    case 3: kern = scan_kernel<io_t, DK, 3>; break;
+    case 4: kern = scan_kernel<io_t, DK, 4>; break;
+    default: break;
+    }
+    kern<<<dim3(s.dv / ROWS, s.BH, 2), SCAN_WARPS * 32, scan_smem, st>>>(q, k, v, u, a.beta, a.alpha, w.X, a.S_init,
+                                                                        a.dout, a.dS_final, w.Sp, w.Gs, w.Z, w.dX,
+                                                                        a.dS_init, s.T, s.dv, s.R, ct);
     tm.end();
     const size_t smem = token_grad_smem_floats(DK, s.dv, s.R) * sizeof(float);
     const long long tg_grid = ntok < (1LL << 30) ? ntok : (1LL << 30);
@@ -667,7 +833,13 @@ cudaError_t set_smem()
     cudaError_t e =
         cudaFuncSetAttribute(token_grad_kernel<io_t, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(scan_kernel<io_t, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+    using scan_fn = decltype(&scan_kernel<io_t, DK, -1>);
+    const scan_fn kerns[] = {scan_kernel<io_t, DK, -1>, scan_kernel<io_t, DK, 0>, scan_kernel<io_t, DK, 1>,
+                             scan_kernel<io_t, DK, 2>, scan_kernel<io_t, DK, 3>, scan_kernel<io_t, DK, 4>};
+    for (scan_fn kern : kerns)
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem)) != cudaSuccess)
+            return e;
+    return cudaSuccess;
 }
 
 }  // namespace bwd
