@@ -49,9 +49,10 @@
  * Storage: as the forward oracle (q, k [B,H,T,dk]; v, dout [B,H,T,dv];
  * u, du [B,H,T,R,dk]; beta, alpha [B,H,T]; gamma, eta [B,H,T,R]; conv_w
  * [H,4,dv]; S_init, dS_final, dS_init [B,H,dv,dk]; v_hist, dv_hist [B,H,3,dv]).
- * Every gradient has the layout of its input.  deta[..., R-1] is 0 (that gain
- * is never read).  Optional pointers may be NULL: S_init, v_hist (zeros),
- * dS_final (zero), dv_hist, dS_init (not returned).
+ * Every gradient has the layout of its input.  deta[..., R-1] is 0: that gain
+ * is never read (as in the forward), so it may hold anything, NaN included.
+ * Optional pointers may be NULL: S_init, v_hist (zeros), dS_final (zero),
+ * dv_hist, dS_init (not returned).
  *
  * Build: gcc -O2 -fno-fast-math -shared -fPIC prism_oracle_bwd.c -lm -lpthread
  */
@@ -120,7 +121,7 @@ static void run_head(bwd_args *a, int b, int h)
             double r = vt[c] - s * Phi_of(s);
             for (int l = 0; l < R; ++l) {
                 xt[(size_t)l * dv + c] = gamma[(size_t)t * R + l] * g * r;
-                r *= 1.0 - eta[(size_t)t * R + l] * g;
+                if (l + 1 < R) r *= 1.0 - eta[(size_t)t * R + l] * g;
             }
         }
         memcpy(Sprev + (size_t)t * DD, S, sizeof(double) * DD);
@@ -205,11 +206,12 @@ static void run_head(bwd_args *a, int b, int h)
             double r = vt[c] - hc * Ph;
             for (int l = 0; l < R; ++l) {  /* the chain's values r_{t,l} */
                 rs[(size_t)l * dv + c] = r;
-                r *= 1.0 - eta[(size_t)t * R + l] * g;
+                if (l + 1 < R) r *= 1.0 - eta[(size_t)t * R + l] * g;
             }
             double dr_next = 0.0, dg = 0.0;
             for (int l = R - 1; l >= 0; --l) {
-                const double gm = gamma[(size_t)t * R + l], et = eta[(size_t)t * R + l];
+                /* the last level's gain shapes nothing (the cotangent of r_{t,R+1} is zero) */
+                const double gm = gamma[(size_t)t * R + l], et = l + 1 < R ? eta[(size_t)t * R + l] : 0.0;
                 const double rl = rs[(size_t)l * dv + c], dxl = dx[(size_t)l * dv + c];
                 dgamma[(size_t)t * R + l] += g * rl * dxl;
                 deta[(size_t)t * R + l] += -g * rl * dr_next;

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(NT) factors_kernel(const io_t *__restrict__ v,
     const size_t tok = (size_t)bh * T + t;
     for (int l = 0; l < R; ++l) {
         X[(tok * R + l) * dv + c] = gamma[tok * R + l] * g * r;
-        r *= 1.f - eta[tok * R + l] * g;
+        if (l + 1 < R) r *= 1.f - eta[tok * R + l] * g;  // the last gain is never read
     }
 }
 
@@ -657,13 +657,14 @@ __global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__
             for (int l = 0; l < RMAX; ++l)
                 if (l < R) {
                     rl[l] = r;
-                    r *= 1.f - eta[(size_t)tok * R + l] * g;
+                    if (l + 1 < R) r *= 1.f - eta[(size_t)tok * R + l] * g;
                 }
             float drn = 0.f, dg = 0.f;
 #pragma unroll
             for (int l = RMAX - 1; l >= 0; --l)
                 if (l < R) {
-                    const float gm = gamma[(size_t)tok * R + l], et = eta[(size_t)tok * R + l];
+                    // the last level's gain shapes nothing (the cotangent of r_{t,R+1} is zero)
+                    const float gm = gamma[(size_t)tok * R + l], et = l + 1 < R ? eta[(size_t)tok * R + l] : 0.f;
                     const float dx = dX[((size_t)tok * R + l) * dv + c];
                     dgam[l] = g * rl[l] * dx;
                     det[l] = -g * rl[l] * drn;

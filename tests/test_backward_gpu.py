@@ -101,6 +101,19 @@ def test_short_sequences_with_history(T):
     compare(got, ref, "f32", list(PER_HEAD) + ["dconv_w", "dv_hist", "dS_init"])
 
 
+def test_unread_gain_slot_is_never_read():
+    """NaN in eta[..., R-1] (a gain the forward never reads) leaves every cotangent finite and
+    equal to the oracle's."""
+    inp = make_inputs(1, 2, 150, 64, 64, 4, dtype="bf16", seed=12)
+    inp["eta"][..., -1] = float("nan")
+    dout, dS_final = make_cotangents(1, 2, 150, 64, 64, seed=12, with_state=True)
+    got = gpu_backward(inp, dout, dS_final)
+    ref = oracle_backward(inp, dout, dS_final)
+    for kk, vv in got.items():
+        assert np.all(np.isfinite(vv)), kk
+    compare(got, ref, "bf16", list(PER_HEAD) + ["dconv_w", "dv_hist", "dS_init"])
+
+
 def test_backward_is_deterministic():
     inp = make_inputs(2, 2, 300, 64, 64, 4, dtype="bf16", seed=9)
     dout, dS_final = make_cotangents(2, 2, 300, 64, 64, seed=9, with_state=True)

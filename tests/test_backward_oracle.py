@@ -103,6 +103,18 @@ def test_every_element_on_a_tiny_case():
             assert abs(gx.reshape(-1)[idx] - fd) <= 1e-7 * (1 + abs(fd)), (name, idx, gx.reshape(-1)[idx], fd)
 
 
+def test_unread_gain_slot_is_never_read():
+    """eta[..., R-1] shapes a residual nothing uses: NaN there changes no cotangent."""
+    x, cot, L = f64_case(L=3)
+    g = grads(x, cot, L)
+    x2 = dict(x)
+    x2["eta"] = x["eta"].copy()
+    x2["eta"][..., L - 2] = np.nan
+    g2 = grads(x2, cot, L)
+    for key in g:
+        assert np.array_equal(g[key], g2[key]), key
+
+
 def test_unread_gain_slot_has_zero_cotangent():
     x, cot, L = f64_case(L=3)
     g = grads(x, cot, L)
