@@ -23,6 +23,9 @@ prism_status fail(prism_status s, const char *fmt, ...)
 
 prism_status cuda_fail(cudaError_t e, const char *what)
 {
+    // reset the runtime's last-error state, so that a recoverable failure (an allocation that did
+    // not fit) is not reported again by the error check after a later call's launches
+    (void)cudaGetLastError();
     return fail(PRISM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
