@@ -43,6 +43,15 @@
  * cotangent of those history slots is returned in dv_hist.
  * dS_init is the state cotangent after token 0 has been processed.
  *
+ * Non-linear residual variant (optional input p_gain [B,H,T,R,dv], notes section
+ * 2.3; eta is then not read): r_{t,1} = e_t, delta_{t,l} = GELU(p_{t,l} (.) r_{t,l}),
+ * x_{t,l} = gamma_{t,l} delta_{t,l}, r_{t,l+1} = r_{t,l} - delta_{t,l}.  Its chain
+ * backwards, l = R .. 1 (the cotangent of r_{t,R+1} is zero), with z = p (.) r_{t,l}:
+ *   ddelta = gamma_{t,l} dx_{t,l} - dr_{t,l+1},   dgamma_{t,l} = sum_c delta dx_{t,l}
+ *   dz = ddelta GELU'(z),   dp_{t,l} = dz (.) r_{t,l},   dr_{t,l} = dr_{t,l+1} + dz (.) p
+ * then dv_t += dr_{t,1} and dh_t = -g dr_{t,1} (the gain GELU'(h) is not used by this
+ * chain); the cotangent of p_gain is returned in dp_gain instead of deta.
+ *
  * The pre-update states S_{t-1} of one (batch, head) are all kept from a first
  * forward pass (T dv dk doubles).
  *
@@ -63,8 +72,8 @@
 
 typedef struct {
     int B, H, T, dk, dv, L;
-    const double *q, *k, *v, *beta, *alpha, *u, *gamma, *eta, *conv_w, *v_hist, *S_init, *dout, *dS_final;
-    double *dq, *dk_, *dv_, *dbeta, *dalpha, *du, *dgamma, *deta, *dconv_part, *dv_hist, *dS_init;
+    const double *q, *k, *v, *beta, *alpha, *u, *gamma, *eta, *p_gain, *conv_w, *v_hist, *S_init, *dout, *dS_final;
+    double *dq, *dk_, *dv_, *dbeta, *dalpha, *du, *dgamma, *deta, *dp_gain, *dconv_part, *dv_hist, *dS_init;
     int nthreads, thread_id, status;
 } bwd_args;
 
@@ -79,7 +88,8 @@ static void run_head(bwd_args *a, int b, int h)
     const double *beta = a->beta + bh * T, *alpha = a->alpha + bh * T;
     const double *u = R > 0 ? a->u + bh * T * R * dk : NULL;
     const double *gamma = R > 0 ? a->gamma + bh * T * R : NULL;
-    const double *eta = R > 0 ? a->eta + bh * T * R : NULL;
+    const double *eta = (R > 0 && a->eta) ? a->eta + bh * T * R : NULL;
+    const double *pg = (R > 0 && a->p_gain) ? a->p_gain + bh * T * R * dv : NULL;
     const double *w = a->conv_w + (size_t)h * 4 * dv;
     const double *vh = a->v_hist ? a->v_hist + bh * 3 * dv : NULL;
     const double *dO = a->dout + bh * T * dv;
@@ -87,7 +97,8 @@ static void run_head(bwd_args *a, int b, int h)
     double *dbeta = a->dbeta + bh * T, *dalpha = a->dalpha + bh * T;
     double *du = R > 0 ? a->du + bh * T * R * dk : NULL;
     double *dgamma = R > 0 ? a->dgamma + bh * T * R : NULL;
-    double *deta = R > 0 ? a->deta + bh * T * R : NULL;
+    double *deta = (R > 0 && !pg) ? a->deta + bh * T * R : NULL;
+    double *dpg = (R > 0 && pg) ? a->dp_gain + bh * T * R * dv : NULL;
     double *dw = a->dconv_part + bh * 4 * dv;
 
     double *Sprev = malloc(sizeof(double) * DD * (size_t)T);  /* S_{t-1} for every t */
@@ -120,6 +131,13 @@ static void run_head(bwd_args *a, int b, int h)
             const double g = Phi_of(s) + s * phi_of(s);
             double r = vt[c] - s * Phi_of(s);
             for (int l = 0; l < R; ++l) {
+                if (pg) {  /* non-linear variant: delta = GELU(p r), r <- r - delta */
+                    const double zz = pg[((size_t)t * R + l) * dv + c] * r;
+                    const double delta = zz * Phi_of(zz);
+                    xt[(size_t)l * dv + c] = gamma[(size_t)t * R + l] * delta;
+                    r -= delta;
+                    continue;
+                }
                 xt[(size_t)l * dv + c] = gamma[(size_t)t * R + l] * g * r;
                 if (l + 1 < R) r *= 1.0 - eta[(size_t)t * R + l] * g;
             }
@@ -197,9 +215,33 @@ static void run_head(bwd_args *a, int b, int h)
         /* residual chain and anchor, channel by channel */
         for (int l = 0; l < R; ++l) {
             dgamma[(size_t)t * R + l] = 0.0;
-            deta[(size_t)t * R + l] = 0.0;
+            if (deta) deta[(size_t)t * R + l] = 0.0;
         }
-        for (int c = 0; c < dv; ++c) {
+        for (int c = 0; pg && c < dv; ++c) {  /* the non-linear chain */
+            const double hc = hh[(size_t)t * dv + c];
+            const double g = Phi_of(hc) + hc * phi_of(hc);
+            double r = vt[c] - hc * Phi_of(hc);
+            for (int l = 0; l < R; ++l) {
+                rs[(size_t)l * dv + c] = r;
+                const double zz = pg[((size_t)t * R + l) * dv + c] * r;
+                r -= zz * Phi_of(zz);
+            }
+            double dr_next = 0.0;  /* nothing reads r_{t,R+1} */
+            for (int l = R - 1; l >= 0; --l) {
+                const double gm = gamma[(size_t)t * R + l], p = pg[((size_t)t * R + l) * dv + c];
+                const double rl = rs[(size_t)l * dv + c], dxl = dx[(size_t)l * dv + c];
+                const double zz = p * rl, delta = zz * Phi_of(zz);
+                /* x_l = gamma delta_l and r_{l+1} = r_l - delta_l */
+                const double ddelta = gm * dxl - dr_next;
+                dgamma[(size_t)t * R + l] += delta * dxl;
+                const double dz = ddelta * (Phi_of(zz) + zz * phi_of(zz));
+                dpg[((size_t)t * R + l) * dv + c] = dz * rl;
+                dr_next = dr_next + dz * p;
+            }
+            dvv[(size_t)t * dv + c] += dr_next;
+            dh[(size_t)t * dv + c] = -g * dr_next;  /* e = v - GELU(h); the gain g is not used */
+        }
+        for (int c = 0; !pg && c < dv; ++c) {
             const double hc = hh[(size_t)t * dv + c];
             const double Ph = Phi_of(hc), ph = phi_of(hc);
             const double g = Ph + hc * ph;
@@ -262,16 +304,17 @@ int prism_oracle_backward_f64(int B, int H, int T, int dk, int dv, int L,
                               const double *q, const double *k, const double *v,
                               const double *beta, const double *alpha,
                               const double *u, const double *gamma, const double *eta,
-                              const double *conv_w, const double *v_hist, const double *S_init,
-                              const double *dout, const double *dS_final,
+                              const double *p_gain, const double *conv_w, const double *v_hist,
+                              const double *S_init, const double *dout, const double *dS_final,
                               double *dq, double *dk_, double *dv_, double *dbeta, double *dalpha,
-                              double *du, double *dgamma, double *deta, double *dconv_w,
+                              double *du, double *dgamma, double *deta, double *dp_gain, double *dconv_w,
                               double *dv_hist, double *dS_init, int nthreads)
 {
     if (B < 0 || H < 0 || T < 1 || dk <= 0 || dv <= 0 || L < 1) return -1;
     if (!q || !k || !v || !beta || !alpha || !conv_w || !dout) return -2;
     if (!dq || !dk_ || !dv_ || !dbeta || !dalpha || !dconv_w) return -2;
-    if (L > 1 && (!u || !gamma || !eta || !du || !dgamma || !deta)) return -3;
+    if (L > 1 && (!u || !gamma || !du || !dgamma)) return -3;
+    if (L > 1 && (p_gain ? !dp_gain : (!eta || !deta))) return -3;
     const int units = B * H;
     if (units == 0) return 0;
     const size_t th = (size_t)units * T;
@@ -282,9 +325,9 @@ int prism_oracle_backward_f64(int B, int H, int T, int dk, int dv, int L,
     if (!part) return -9;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > units) nthreads = units;
-    bwd_args base = {B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, conv_w, v_hist, S_init, dout,
-                     dS_final, dq, dk_, dv_, dbeta, dalpha, du, dgamma, deta, part, dv_hist, dS_init,
-                     nthreads, 0, 0};
+    bwd_args base = {B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, p_gain, conv_w, v_hist, S_init,
+                     dout, dS_final, dq, dk_, dv_, dbeta, dalpha, du, dgamma, deta, dp_gain, part, dv_hist,
+                     dS_init, nthreads, 0, 0};
     pthread_t *th_ids = malloc(sizeof(pthread_t) * nthreads);
     bwd_args *args = malloc(sizeof(bwd_args) * nthreads);
     int status = 0;

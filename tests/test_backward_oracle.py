@@ -18,14 +18,19 @@ import numpy as np
 import pytest
 
 from oracle import prism_backward, prism_oracle
-from ssm_sequence_layer_gb300.inputs import make_cotangents, make_inputs
+from ssm_sequence_layer_gb300.inputs import make_cotangents, make_gain, make_inputs
 
 INPUT_NAMES = ("q", "k", "v", "beta", "alpha", "u", "gamma", "eta", "conv_w")
 
 
-def f64_case(B=1, H=2, T=24, dk=6, dv=5, L=3, seed=3, state=True, hist=True):
+def f64_case(B=1, H=2, T=24, dk=6, dv=5, L=3, seed=3, state=True, hist=True, nonlinear=False):
+    """Inputs of one case; with `nonlinear` the forward is the non-linear residual variant:
+    gains p (make_gain) take the place of eta."""
     inp = make_inputs(B, H, T, dk, dv, L, dtype="f32", seed=seed)
     x = {n: inp[n].double().numpy() for n in INPUT_NAMES}
+    x["p_gain"] = make_gain(B, H, T, L, dv, dtype="f32", seed=seed).double().numpy() if nonlinear else None
+    if nonlinear:
+        x["eta"] = None
     rng = np.random.default_rng(seed + 11)
     x["S_init"] = rng.standard_normal((B, H, dv, dk)) * 0.3 if state else None
     x["v_hist"] = rng.standard_normal((B, H, 3, dv)) if hist else None
@@ -36,7 +41,8 @@ def f64_case(B=1, H=2, T=24, dk=6, dv=5, L=3, seed=3, state=True, hist=True):
 
 def loss(x, cot, L):
     r = prism_oracle.forward(x["q"], x["k"], x["v"], x["beta"], x["alpha"], x["u"], x["gamma"], x["eta"],
-                             x["conv_w"], L, S_init=x["S_init"], v_hist=x["v_hist"], want_state=True, nthreads=1)
+                             x["conv_w"], L, S_init=x["S_init"], v_hist=x["v_hist"], p_gain=x.get("p_gain"),
+                             want_state=True, nthreads=1)
     f = float(np.sum(cot["dout"] * r["out"]))
     if cot["dS_final"] is not None:
         f += float(np.sum(cot["dS_final"] * r["S_final"]))
@@ -46,11 +52,11 @@ def loss(x, cot, L):
 def grads(x, cot, L, mod=prism_backward):
     return mod.backward(x["q"], x["k"], x["v"], x["beta"], x["alpha"], x["u"], x["gamma"], x["eta"], x["conv_w"],
                         L, cot["dout"], S_init=x["S_init"], v_hist=x["v_hist"], dS_final=cot["dS_final"],
-                        want_dv_hist=True, want_dS_init=True, nthreads=1)
+                        p_gain=x.get("p_gain"), want_dv_hist=True, want_dS_init=True, nthreads=1)
 
 
 GRAD_OF = {"q": "dq", "k": "dk", "v": "dv", "beta": "dbeta", "alpha": "dalpha", "u": "du", "gamma": "dgamma",
-           "eta": "deta", "conv_w": "dconv_w", "S_init": "dS_init", "v_hist": "dv_hist"}
+           "eta": "deta", "conv_w": "dconv_w", "S_init": "dS_init", "v_hist": "dv_hist", "p_gain": "dp_gain"}
 
 
 def directional_check(x, cot, L, name, g, eps=1e-5, seed=0):
@@ -68,6 +74,12 @@ def directional_check(x, cot, L, name, g, eps=1e-5, seed=0):
 
 
 ALL = ("q", "k", "v", "beta", "alpha", "u", "gamma", "eta", "conv_w", "S_init", "v_hist")
+
+
+def inputs_of(x):
+    """The differentiable inputs present in a case (eta or p_gain, S_init and v_hist if given)."""
+    names = [n for n in ALL if x.get(n) is not None]
+    return names + (["p_gain"] if x.get("p_gain") is not None else [])
 
 
 @pytest.mark.parametrize("L", [1, 2, 4])
@@ -149,3 +161,31 @@ def test_gradients_are_linear_in_the_cotangents():
     g2 = grads(x, cot2, L)
     for key in g1:
         np.testing.assert_allclose(g2[key], 2.5 * g1[key], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("L", [2, 4])
+def test_nonlinear_variant_directional_derivatives(L):
+    """The non-linear residual variant (gains p in place of eta): every input, p included."""
+    x, cot, L = f64_case(L=L, T=21, B=2, H=2, nonlinear=True)
+    g = grads(x, cot, L)
+    assert "deta" not in g and g["dp_gain"].shape == x["p_gain"].shape
+    for name in inputs_of(x):
+        for seed in (0, 1):
+            err, an, fd = directional_check(x, cot, L, name, g, seed=seed)
+            assert err < 1e-8, f"d/d{name} (non-linear, L={L}): analytic {an!r} vs central difference {fd!r}"
+
+
+def test_nonlinear_variant_every_element_on_a_tiny_case():
+    x, cot, L = f64_case(B=1, H=1, T=6, dk=3, dv=2, L=3, seed=7, nonlinear=True)
+    g = grads(x, cot, L)
+    eps = 1e-6
+    for name in inputs_of(x):
+        gx = g[GRAD_OF[name]].reshape(-1)
+        flat = x[name].reshape(-1)
+        for idx in range(flat.size):
+            a, b = flat.copy(), flat.copy()
+            a[idx] += eps
+            b[idx] -= eps
+            fd = (loss(dict(x, **{name: a.reshape(x[name].shape)}), cot, L)
+                  - loss(dict(x, **{name: b.reshape(x[name].shape)}), cot, L)) / (2 * eps)
+            assert abs(gx[idx] - fd) <= 1e-7 * (1 + abs(fd)), (name, idx, gx[idx], fd)

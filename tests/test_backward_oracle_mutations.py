@@ -31,7 +31,16 @@ MUTATIONS = [
     ("gain cotangent without the chain term", "dg += gm * rl * dxl - et * rl * dr_next;", "dg += gm * rl * dxl;"),
     ("deta sign", "deta[(size_t)t * R + l] += -g * rl * dr_next;", "deta[(size_t)t * R + l] += g * rl * dr_next;"),
     ("gain derivative without the h^2 term", "ph * (2.0 - hc * hc) * dg", "ph * 2.0 * dg"),
-    ("residual derivative with Phi only", "dh[(size_t)t * dv + c] = -g * dr_next", "dh[(size_t)t * dv + c] = -Ph * dr_next"),
+    ("residual derivative with Phi only", "dh[(size_t)t * dv + c] = -g * dr_next + ph",
+     "dh[(size_t)t * dv + c] = -Ph * dr_next + ph"),
+    ("non-linear step cotangent sign", "const double ddelta = gm * dxl - dr_next;",
+     "const double ddelta = gm * dxl + dr_next;"),
+    ("non-linear gain cotangent from the gain", "dpg[((size_t)t * R + l) * dv + c] = dz * rl;",
+     "dpg[((size_t)t * R + l) * dv + c] = dz * p;"),
+    ("non-linear GELU derivative without z phi", "const double dz = ddelta * (Phi_of(zz) + zz * phi_of(zz));",
+     "const double dz = ddelta * Phi_of(zz);"),
+    ("non-linear residual derivative dropped", "dh[(size_t)t * dv + c] = -g * dr_next;  /*",
+     "dh[(size_t)t * dv + c] = 0.0 * dr_next;  /*"),
     ("conv transpose taps reversed", "dvv[(size_t)src * dv + c] += w[j * dv + c] * d;",
      "dvv[(size_t)src * dv + c] += w[(3 - j) * dv + c] * d;"),
     ("conv weight cotangent from the wrong token", "dw[j * dv + c] += v[(size_t)src * dv + c] * d;",
@@ -43,14 +52,15 @@ MUTATIONS = [
 
 
 def _pins_fail(mod):
-    """Directional pins at L = 2 and 3 on the mutated build; True if any fails."""
-    for L in (2, 3):
-        x, cot, L = pins.f64_case(L=L, T=13)
+    """Directional pins at L = 2 and 3 (linear chain) and L = 3 (non-linear chain) on the
+    mutated build; True if any fails."""
+    for L, nonlinear in ((2, False), (3, False), (3, True)):
+        x, cot, L = pins.f64_case(L=L, T=13, nonlinear=nonlinear)
         try:
             g = pins.grads(x, cot, L, mod=mod)
         except (ValueError, OSError):
             return True
-        for name in pins.ALL:
+        for name in pins.inputs_of(x):
             err, _, _ = pins.directional_check(x, cot, L, name, g)
             if not np.isfinite(err) or err > 1e-8:
                 return True
