@@ -17,28 +17,28 @@
 //   fixup    o = o0 + Qhat S_start^T for the chunks of the stashing segments.
 //
 // Chunk algebra (local index i, j; lambda_i = sum_{m<=i} ln alpha_m; lc = lambda_{C-1};
-// rowf_i = e^{lambda_i - lc} >= 1, colf_j = e^{lc - lambda_j} <= 1, Gamma_i = e^{lambda_i}):
-//   A_ij  = beta_i rowf_i colf_j k_i.k_j            (j < i)   -> T = (I + A)^{-1}   (fp32 solve)
-//   PK_l  = k_i.u_{j,l} (j < i);  PQ_l = q_i.u_{j,l}, G = q_i.k_j (j <= i)      (unscaled scores,
-//           computed and stored transposed, [j][i], from Grams with key/direction rows)
-//   Xs_l  = colf_j x_{j,l}                             (x = gamma g (.) r, the prep)
-//   RHS   = diag(beta) V - diag(beta rowf) sum_l PK_l Xs_l
-//   [U'^T; W^T] = [RHS | diag(beta Gamma) K]^T T^T
-//   UWs   = [U'^T; W^T] diag(colf) = [RHS | diag(beta Gamma) K]^T (diag(colf) T)^T   (one MMA)
-//   D4    = (UWs G^T + [Xs^T; 0] PQ^T) diag(rowf) = [O_loc^T ; (G~ W)^T]   (G~ = Q K^T o D)
-//   D5    = UWs K + [Xs^T; 0] U         = [N_c ; W^T K']
-//   Qt    = Q~^T = diag(Gamma) Q^T - (G~ W)^T,   M_c = Gamma_C I - W^T K'
+// D_ij = e^{lambda_i - lambda_j} (j <= i), colf_j = e^{lc - lambda_j} <= 1, Gamma_i = e^{lambda_i}):
+//   A_ij  = beta_i D_ij k_i.k_j                        (j < i)   -> T = (I + A)^{-1}   (fp32 solve)
+//   PK_l  = D_ij k_i.u_{j,l} (j < i);  PQ_l = D_ij q_i.u_{j,l}, G = D_ij q_i.k_j (j <= i)  (decayed
+//           scores, computed and stored transposed, [j][i], from Grams with key/direction rows)
+//   X_l   = x_{j,l}                                    (x = gamma g (.) r, the prep)
+//   K'    = diag(colf) K,  U'_l = diag(colf) U_l       (the state-side key and direction tiles)
+//   RHS   = diag(beta) (V - sum_l PK_l X_l)
+//   [U'^T; W^T] = [RHS | diag(beta Gamma) K]^T T^T  = UW
+//   D4    = UW G^T + [X^T; 0] PQ^T = [O_loc^T ; (G W)^T]
+//   D5    = UW K' + [X^T; 0] U'   = [N_c ; W^T K']
+//   Qt    = Q~^T = diag(Gamma) Q^T - (G W)^T,   M_c = Gamma_C I - W^T K'
 //   Z    <- Z M_c + [N_c; 0],   [o0^T ; Qhat^T] = Z Qt + [O_loc^T ; 0]   (Z before the update)
-// The decay factors of every masked product multiply to e^{lambda_i - lambda_j} <= 1; a
-// chunk whose total decay exceeds 80 nats (rowf would leave fp32 range) sets the status word.
+// Every decay that a product needs is applied in fp32 before an operand is rounded: D_ij on the
+// score tiles (as e^{lambda_i - lc} e^{lc - lambda_j} while the chunk's total decay is within fp32
+// range, else one exponential per element), colf on the state side.  No fp16 operand carries a
+// factor that a later step multiplies back up, so an operand that underflows only drops a
+// contribution below fp16's range, however strong the decay.
 // All matrix products above run on tcgen05.mma (fp16 operands in 128B-swizzled shared memory,
 // fp32 accumulators in tensor memory); operands come from TMA or from the epilogues.  The Gram
-// runs on the bf16 input tiles; K and U are then converted to fp16 in place (exact for
-// unit-scale rows) for the state-side products: fp16's 10-bit
-// mantissa keeps the computed operands (scores, Xs, T, U'/W, Q~, M_c, Z) 8x closer to fp32
-// than bf16 would, at the same tensor-core rate.  Row factors >= 1 (e^{lambda_i - lc},
-// beta_i) are kept out of the operands and applied to the accumulators in the epilogues, so
-// every fp16 operand stays of order one.
+// runs on the bf16 input tiles; K and U are then converted to fp16 in place, scaled by colf, for
+// the state-side products: fp16's 10-bit mantissa keeps the computed operands (scores, X, T,
+// U'/W, Q~, M_c, Z) 8x closer to fp32 than bf16 would, at the same tensor-core rate.
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -83,12 +83,12 @@ constexpr uint32_t OFF_K = OFF_Q + TILE;          // the tile below Q is the fir
 constexpr uint32_t OFF_U = OFF_K + TILE;
 constexpr uint32_t OFF_E = OFF_U + RMAX * TILE;   // [PK0|PQ0^T|PK1|PQ1^T|PK2|PQ2^T|G^T]; later Qt, Mc
 constexpr uint32_t OFF_G = OFF_E + 6 * TILE;
-constexpr uint32_t OFF_AKK = OFF_E + 7 * TILE;    // A (fp32, row stride LDA); later UWs
+constexpr uint32_t OFF_AKK = OFF_E + 7 * TILE;    // A (fp32, row stride LDA); later UW
 constexpr uint32_t LDA = 68;    // row stride (floats) of A and T32 (float4 rows, conflict-free fragments)
 constexpr uint32_t OFF_T32 = OFF_AKK + 64 * LDA * 4;
 constexpr uint32_t OFF_TB = OFF_T32 + 64 * LDA * 4;  // bf16 identity (written once): B of the Q^T copy
 constexpr uint32_t OFF_TF = OFF_E + 2 * TILE;        // T (fp16), over PK_1^T (free once MX completed)
-constexpr uint32_t OFF_XS = OFF_TB + TILE;            // Xs0..Xs2
+constexpr uint32_t OFF_XS = OFF_TB + TILE;            // X0..X2
 constexpr uint32_t OFF_ZERO = OFF_XS + RMAX * TILE;   // zero tile
 constexpr uint32_t OFF_ZA = OFF_ZERO + TILE;          // Z (128 rows, bf16, K-major)
 constexpr uint32_t OFF_BGK = OFF_ZA + 2 * TILE;       // diag(beta Gamma) K (fp16 tile)
@@ -127,6 +127,12 @@ struct SegParams {
 };
 
 __device__ __forceinline__ void set_status(int *st, int code) { atomicCAS(st, 0, code); }
+
+// compile-time flag for code paths chosen by a uniform runtime branch
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
 
 __device__ __forceinline__ uint32_t pack2(float a, float b)
 {
@@ -225,23 +231,26 @@ __device__ __forceinline__ void frag_c_store(const Frag &f, float *M, int ld, in
     p[8 * ld + 1] = sgn * c[3];
 }
 
-// in-place bf16 -> fp16 conversion of `bytes` bytes of tiles (layout unchanged)
-__device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes, int t, int nthreads)
+// in-place bf16 -> fp16 conversion of `bytes` bytes of [64][64] tiles (layout unchanged), each
+// row r of every tile scaled by scale[r] (a 16-byte group never leaves its row under the swizzle)
+__device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes, int t, int nthreads,
+                                                  const float *scale)
 {
     for (uint32_t e = t; e < bytes / 16; e += nthreads) {
         uint4 w = reinterpret_cast<uint4 *>(base)[e];
+        const float sc = scale[(e >> 3) & 63];
         uint32_t *pw = &w.x;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&pw[q]);
             const float2 f = __bfloat1622float2(b);
-            pw[q] = pack2(f.x, f.y);
+            pw[q] = pack2(sc * f.x, sc * f.y);
         }
         reinterpret_cast<uint4 *>(base)[e] = w;
     }
 }
 
-// prep of one chunk (P1): anchor, gain and residual chain -> Xs tiles, two channels x 4 tokens per
+// prep of one chunk (P1): anchor, gain and residual chain -> X tiles, two channels x 4 tokens per
 // thread, from V stage `stg` and the chunk's per-token scalars `pset`.  Kept out of line: the
 // segment kernel calls it at two places, and one copy of its code keeps the loop body smaller.
 __device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __nv_bfloat162 *cw2, int stg, int R)
@@ -251,7 +260,7 @@ __device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __
     const float2 w1 = __bfloat1622float2(cw2[1 * (D / 2)]);
     const float2 w2 = __bfloat1622float2(cw2[2 * (D / 2)]);
     const float2 w3 = __bfloat1622float2(cw2[3 * (D / 2)]);
-    const float *p_colf = pset + 192, *p_gc = pset + 384, *p_eta = pset + 384 + 64 * RMAX;
+    const float *p_gc = pset + 384, *p_eta = pset + 384 + 64 * RMAX;
     const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stg ? OFF_V1 : OFF_V0));
     const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
     constexpr int TPT = 64 / (NT / 32);     // tokens per thread
@@ -262,11 +271,10 @@ __device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __
         const float2 v1 = __bfloat1622float2(vb[(i + 7) * 32 + cp]);
         const float2 v2 = __bfloat1622float2(vb[(i + 6) * 32 + cp]);
         const float2 v3 = __bfloat1622float2(vb[(i + 5) * 32 + cp]);
-        const float cf = p_colf[i];
         float gcl[RMAX], etl[RMAX];
 #pragma unroll
         for (int l = 0; l < RMAX; ++l) {
-            gcl[l] = p_gc[i * RMAX + l] * cf;
+            gcl[l] = p_gc[i * RMAX + l];
             etl[l] = p_eta[i * RMAX + l];
         }
         const float a0 = fmaf(w0.x, v0.x, fmaf(w1.x, v1.x, fmaf(w2.x, v2.x, w3.x * v3.x)));
@@ -463,7 +471,6 @@ __global__ void __launch_bounds__(NT, 1)
             set[256 + i1] = __expf(l1);
             set[320 + i0] = pf_b0 * __expf(l0);
             set[320 + i1] = pf_b1 * __expf(l1);
-            if (lane == 31 && -lcw > 80.f) set_status(p.status, kDevBounds);  // beyond the factorised range
         }
         if (gt >= 0 && gt < 64 * RMAX) {
             set[384 + gt] = pf_gam;
@@ -471,7 +478,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
     };
 
-    // prep of chunk cc (P1): anchor, gain and residual chain -> Xs tiles, two channels x 4 tokens
+    // prep of chunk cc (P1): anchor, gain and residual chain -> X tiles, two channels x 4 tokens
     // per thread, from the V stage stg and the chunk's per-token scalars.  It runs in the
     // previous chunk's tail, while that chunk's last MMAs are in flight.
     auto prep = [&](int cc, int stg) { prep_chunk(sm, sc + (cc & 1) * SC_SET, cw2, stg, R); };
@@ -558,63 +565,98 @@ __global__ void __launch_bounds__(NT, 1)
         fence_after_sync();
 
         PHASE_MARK(2);
-        // ---- E1: masks and decay factors -> A (fp32), PK_l^T, PQ_l^T, G^T (fp16 tiles) ----------
+        // ---- E1: masks and decays -> A (fp32), PK_l^T, PQ_l^T, G^T (fp16 tiles) --------------------
         // TMEM lanes 0..63 hold key rows k_j, 64..127 direction rows u_{j,0} (D1) and u_{j,1},
-        // u_{j,2} (D1'); column block 0/2 holds the query side q_i, 1/3 the key side k_i.
+        // u_{j,2} (D1'); column block 0/2 holds the query side q_i, 1/3 the key side k_i.  Each
+        // kept element takes its pair decay D_ij = e^{lambda_i - lambda_j} in fp32: the product
+        // rowf_i colf_j while the chunk's total decay keeps both factors in fp32 range (the usual
+        // case), else one exponential per element.
         {
             const int r = row & 63;
             const bool upper = row >= 64;
             const int nblk = R >= 2 ? 4 : 2;
             const bool skip = upper && R == 0;  // u_0 rows do not exist
-            const float rf = s_rowf[r];
+            const float lr = s_lam[r];
+            const float rf_r = s_rowf[r], cf_r = s_colf[r];
             const float br = s_beta[r];
             const int j0 = sub * CW;
+            // one copy of the epilogue per decay form (a uniform branch: no per-element select)
+            auto e1 = [&](auto form) {
+                constexpr bool kFactored = decltype(form)::value;
+                // decay of row token r (a key / direction token j) to column token i = j0 + q, i >= r
+                float dq[CW];
+                if constexpr (kFactored) {
 #pragma unroll
-            for (int b2 = 0; b2 < 4; b2 += 2) {  // two 64-column blocks per TMEM wait
-                if (b2 >= nblk || skip) break;
-                if (b2 == 2 && upper && R < 3) break;  // u_2 rows do not exist
-                uint32_t rr[2][CW];
+                    for (int g = 0; g < CW / 4; ++g) {
+                        const float4 f = reinterpret_cast<const float4 *>(s_rowf + j0)[g];
+                        dq[4 * g + 0] = f.x * cf_r;
+                        dq[4 * g + 1] = f.y * cf_r;
+                        dq[4 * g + 2] = f.z * cf_r;
+                        dq[4 * g + 3] = f.w * cf_r;
+                    }
+                } else {
 #pragma unroll
-                for (int u = 0; u < 2; ++u)
-                    tmem_ld_nowait(tmem + TM_D1 + ((uint32_t)(quad * 32) << 16) + (uint32_t)((b2 + u) * 64 + j0), rr[u]);
-                tmem_wait_ld();
-                const int l = b2 ? (upper ? 2 : 1) : 0;  // direction level of an upper / D1' row
-                const bool keyrow = b2 == 0 && !upper;
+                    for (int q = 0; q < CW; ++q) dq[q] = __expf(fminf(s_lam[j0 + q] - lr, 0.f));
+                }
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    float v[CW];
-                    u2f(rr[u], v);
-                    if (u == 0) {  // query side: G^T (key rows) or PQ_l^T, kept where i >= j
+                for (int b2 = 0; b2 < 4; b2 += 2) {  // two 64-column blocks per TMEM wait
+                    if (b2 >= nblk || skip) break;
+                    if (b2 == 2 && upper && R < 3) break;  // u_2 rows do not exist
+                    uint32_t rr[2][CW];
 #pragma unroll
-                        for (int q = 0; q < CW; ++q) v[q] = (j0 + q >= r) ? v[q] : 0.f;
-                        st_row(sm + (keyrow ? OFF_G : OFF_E + (2 * l + 1) * TILE), r, j0, v);
-                    } else if (keyrow) {  // A_ij = beta_i rowf_i colf_j k_i.k_j (j < i), from k_j.k_i
-                        float4 *A4 = reinterpret_cast<float4 *>(sm + OFF_AKK + (r * LDA + j0) * 4);
-                        const float4 *cf4 = reinterpret_cast<const float4 *>(s_colf + j0);
-                        const float brf = br * rf;
+                    for (int u = 0; u < 2; ++u)
+                        tmem_ld_nowait(tmem + TM_D1 + ((uint32_t)(quad * 32) << 16) + (uint32_t)((b2 + u) * 64 + j0),
+                                       rr[u]);
+                    tmem_wait_ld();
+                    const int l = b2 ? (upper ? 2 : 1) : 0;  // direction level of an upper / D1' row
+                    const bool keyrow = b2 == 0 && !upper;
 #pragma unroll
-                        for (int g = 0; g < CW / 4; ++g) {
-                            const float4 cf = cf4[g];
-                            const int j = j0 + 4 * g;
-                            A4[g] = make_float4(j + 0 < r ? v[4 * g + 0] * brf * cf.x : 0.f,
-                                                j + 1 < r ? v[4 * g + 1] * brf * cf.y : 0.f,
-                                                j + 2 < r ? v[4 * g + 2] * brf * cf.z : 0.f,
-                                                j + 3 < r ? v[4 * g + 3] * brf * cf.w : 0.f);
+                    for (int u = 0; u < 2; ++u) {
+                        float v[CW];
+                        u2f(rr[u], v);
+                        if (u == 0) {  // query side: G^T (key rows) or PQ_l^T, kept where i >= j
+#pragma unroll
+                            for (int q = 0; q < CW; ++q) v[q] = (j0 + q >= r) ? v[q] * dq[q] : 0.f;
+                            st_row(sm + (keyrow ? OFF_G : OFF_E + (2 * l + 1) * TILE), r, j0, v);
+                        } else if (keyrow) {  // A_ij = beta_i D_ij k_i.k_j (j < i), row i = r, from k_j.k_i
+                            float4 *A4 = reinterpret_cast<float4 *>(sm + OFF_AKK + (r * LDA + j0) * 4);
+#pragma unroll
+                            for (int g = 0; g < CW / 4; ++g) {
+                                float d[4];
+                                if constexpr (kFactored) {
+                                    const float4 cf = reinterpret_cast<const float4 *>(s_colf + j0)[g];
+                                    const float b = br * rf_r;
+                                    d[0] = b * cf.x;
+                                    d[1] = b * cf.y;
+                                    d[2] = b * cf.z;
+                                    d[3] = b * cf.w;
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) d[e] = br * __expf(fminf(lr - s_lam[j0 + 4 * g + e], 0.f));
+                                }
+                                const int j = j0 + 4 * g;
+                                A4[g] = make_float4(j + 0 < r ? v[4 * g + 0] * d[0] : 0.f, j + 1 < r ? v[4 * g + 1] * d[1] : 0.f,
+                                                    j + 2 < r ? v[4 * g + 2] * d[2] : 0.f, j + 3 < r ? v[4 * g + 3] * d[3] : 0.f);
+                            }
+                        } else {  // PK_l^T, kept where i > j
+#pragma unroll
+                            for (int q = 0; q < CW; ++q) v[q] = (j0 + q > r) ? v[q] * dq[q] : 0.f;
+                            st_row(sm + OFF_E + 2 * l * TILE, r, j0, v);
                         }
-                    } else {  // PK_l^T, kept where i > j
-#pragma unroll
-                        for (int q = 0; q < CW; ++q) v[q] = (j0 + q > r) ? v[q] : 0.f;
-                        st_row(sm + OFF_E + 2 * l * TILE, r, j0, v);
                     }
                 }
-            }
+            };
+            if (-lc <= 80.f)
+                e1(BoolTag<true>{});
+            else
+                e1(BoolTag<false>{});
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
 
         PHASE_MARK(3);
-        // ---- P3: MX = sum_l PK_l Xs_l on the tensor core.  Meanwhile the warps of TMEM lane
+        // ---- P3: MX = sum_l PK_l X_l on the tensor core.  Meanwhile the warps of TMEM lane
         // quarters 2-3 solve T = (I + A)^{-1}, and those of quarters 0-1 (thread 0 among them)
         // wait for MX, form the RHS (E2) and convert K and U to fp16.  The two groups of 256
         // threads sync on named barriers 1 and 2 and meet again at the CTA barrier before P4.
@@ -746,17 +788,15 @@ __global__ void __launch_bounds__(NT, 1)
                     set_status(p.status, kDevTimeout);
                 }
                 named_bar(1, NT / 2);
-                // T is stored as diag(colf) T (row i scaled by colf_i = e^{lc - lambda_i}), so that
-                // MMA3 yields [U'^T; W^T] diag(colf) = UWs directly
-                for (int e = stid; e < 64 * 8; e += NT / 2) {  // (fp16, [i][j], zero above the diagonal)
+                // T as an fp16 operand ([i][j], zero above the diagonal)
+                for (int e = stid; e < 64 * 8; e += NT / 2) {
                     const int i = e >> 3, g = e & 7;
-                    const float cfi = s_colf[i];
                     const float4 lo = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g);
                     const float4 hi = *reinterpret_cast<const float4 *>(T32 + i * LDA + 8 * g + 4);
                     const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
                     float m[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) m[q] = (8 * g + q <= i) ? v[q] * cfi : 0.f;
+                    for (int q = 0; q < 8; ++q) m[q] = (8 * g + q <= i) ? v[q] : 0.f;
                     uint4 w;
                     w.x = pack2(m[0], m[1]);
                     w.y = pack2(m[2], m[3]);
@@ -784,7 +824,7 @@ __global__ void __launch_bounds__(NT, 1)
             PHASE_MARK(4);
             if (abort_s == 0) {
                 fence_after_sync();
-                // ---- E2: RHS = diag(beta) V - MX (diag(beta Gamma) K was formed during the prep) -----
+                // ---- E2: RHS = diag(beta) (V - MX) (diag(beta Gamma) K was formed during the prep) ---
                 // (lanes 0..63 hold the MX rows)
                 const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + (stage ? OFF_V1 : OFF_V0));
                 const int i = row, j0 = sub * CW;
@@ -795,13 +835,14 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                     for (int q = 0; q < CW; ++q) v[q] = 0.f;  // no levels: M X = 0 (D2 is never written)
                 }
-                const float bi = s_beta[i], brf = s_beta[i] * s_rowf[i];
+                const float bi = s_beta[i];
 #pragma unroll
-                for (int q = 0; q < CW; ++q) v[q] = bi * __bfloat162float(vb[(i + 8) * 64 + j0 + q]) - brf * v[q];
+                for (int q = 0; q < CW; ++q) v[q] = bi * (__bfloat162float(vb[(i + 8) * 64 + j0 + q]) - v[q]);
                 st_row(sm + OFF_E, i, j0, v);  // RHS tile, over PK_0^T (MX, its reader, is complete)
                 PHASE_MARK(12);
-                // K and U to fp16 in place for the state-side products (the Gram has read them)
-                tiles_bf16_to_f16(sm + OFF_K, (1 + R) * TILE, (warp >> 2) * 64 + (warp & 1) * 32 + lane, NT / 2);
+                // K' = diag(colf) K and U'_l = diag(colf) U_l in fp16, in place, for the state-side
+                // products (the Gram has read K and U)
+                tiles_bf16_to_f16(sm + OFF_K, (1 + R) * TILE, (warp >> 2) * 64 + (warp & 1) * 32 + lane, NT / 2, s_colf);
                 PHASE_MARK(13);
             }
         }
@@ -828,7 +869,7 @@ __global__ void __launch_bounds__(NT, 1)
         fence_after_sync();
 
         PHASE_MARK(6);
-        // ---- E3: UWs = [U'^T; W^T] diag(e^{lc - lambda_j}) (the scaling rode on T) -> fp16 --------
+        // ---- E3: UW = [U'^T; W^T] -> fp16 --------------------------------------------------------
         {
             const int j0 = sub * CW;
             float v[CW];
@@ -841,7 +882,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (abort_s) break;
 
         PHASE_MARK(7);
-        // ---- P5: [D5 | D4] = UWs [K | G^T] + sum_l [Xs_l^T; 0] [U_l | PQ_l^T]  (N = 128) ----------
+        // ---- P5: [D5 | D4] = UW [K' | G^T] + sum_l [X_l^T; 0] [U'_l | PQ_l^T]  (N = 128) ----------
         if (tid == 0) {
             fence_after_sync();
             const uint32_t idk = idesc_f16(128, 128, 0, 1), idx = idesc_f16(128, 128, 1, 1);
@@ -874,7 +915,7 @@ __global__ void __launch_bounds__(NT, 1)
             pending |= 2u;
         }
         PHASE_MARK(8);
-        // ---- E4: Qt = diag(Gamma) Q^T - (G~W)^T ;  Mc = Gamma_C I - W^T K' -------------------------
+        // ---- E4: Qt = diag(Gamma) Q^T - (G W)^T ;  Mc = Gamma_C I - W^T K' --------------------------
         if (quad >= 2) {
             const int m = row - 64, j0 = sub * CW;
             float v[CW], v5[CW];
@@ -887,7 +928,7 @@ __global__ void __launch_bounds__(NT, 1)
                 u2f(r4, v);
                 u2f(r5, v5);
 #pragma unroll
-                for (int q = 0; q < CW; ++q) v[q] = s_gam[j0 + q] * __uint_as_float(rq[q]) - s_rowf[j0 + q] * v[q];
+                for (int q = 0; q < CW; ++q) v[q] = s_gam[j0 + q] * __uint_as_float(rq[q]) - v[q];
             }
             st_row(sm + OFF_E, m, j0, v);  // Qt [m][i]
 #pragma unroll
@@ -921,7 +962,7 @@ __global__ void __launch_bounds__(NT, 1)
             mma_commit(mb_mma);
             pending |= 1u;
         }
-        if (c + 1 < c_end) {  // the next chunk's prep while MMA6 runs (Xs of this chunk is dead)
+        if (c + 1 < c_end) {  // the next chunk's prep while MMA6 runs (X of this chunk is dead)
             prep(c + 1, stage ^ 1);
             fence_async_smem();
         }
@@ -967,7 +1008,7 @@ __global__ void __launch_bounds__(NT, 1)
             __half *sq = reinterpret_cast<__half *>(sm + OFF_E + 2 * TILE);   // [64][64] fp16
             if (row < 64) {
 #pragma unroll
-                for (int q = 0; q < CW; ++q) so[(j0 + q) * 64 + row] = o[q] + s_rowf[j0 + q] * ol[q];
+                for (int q = 0; q < CW; ++q) so[(j0 + q) * 64 + row] = o[q] + ol[q];
             } else if (tracked) {
 #pragma unroll
                 for (int q = 0; q < CW; ++q) sq[(j0 + q) * 64 + row - 64] = __float2half_rn(o[q]);
