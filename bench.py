@@ -252,26 +252,66 @@ def max_over_ranks(x, world):
 
 def oracle_sample(w, inp, seconds_target, nthreads, p_gain=None):
     """Time the oracle on the first Ts tokens of every sequence, Ts sized so the run takes
-    about `seconds_target` seconds.  Returns (tokens/s, Ts, seconds)."""
+    about `seconds_target` seconds.  Returns (tokens/s, Ts, seconds, oracle output [B,H,Ts,dv])."""
     from oracle import prism_oracle
 
     def run(Ts):
         sub = {k: (v[:, :, :Ts] if hasattr(v, "shape") and k != "conv_w" else v) for k, v in inp.items()}
         t0 = time.perf_counter()
-        prism_oracle.forward(sub["q"], sub["k"], sub["v"], sub["beta"], sub["alpha"], sub["u"], sub["gamma"],
-                             sub["eta"], sub["conv_w"], sub["L"], nthreads=nthreads,
-                             p_gain=None if p_gain is None else p_gain[:, :, :Ts])
-        return time.perf_counter() - t0
+        res = prism_oracle.forward(sub["q"], sub["k"], sub["v"], sub["beta"], sub["alpha"], sub["u"], sub["gamma"],
+                                   sub["eta"], sub["conv_w"], sub["L"], nthreads=nthreads,
+                                   p_gain=None if p_gain is None else p_gain[:, :, :Ts])
+        return time.perf_counter() - t0, res["out"]
 
     Ts = min(w.T, 256)
-    dt = run(Ts)
+    dt, _ = run(Ts)
     Ts = int(min(w.T, max(Ts, Ts * seconds_target / max(dt, 1e-3))))
-    dt = run(Ts)
-    return w.B * Ts / dt, Ts, dt
+    dt, ref = run(Ts)
+    return w.B * Ts / dt, Ts, dt, ref
+
+
+def parity_error(out, ref, bf16_out):
+    """max |o - o_ref| / rms(o_ref) over the compared outputs; for a bf16 output each element is
+    first allowed the half-ulp its own rounding to bf16 costs (at the larger of |o| and |o_ref|)."""
+    import numpy as np
+    out = np.asarray(out, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    diff = np.abs(out - ref)
+    if bf16_out:
+        a = np.maximum(np.abs(out), np.abs(ref))
+        half_ulp = np.where(a > 0, np.exp2(np.floor(np.log2(np.maximum(a, 1e-300))) - 8), 0.0)
+        diff = np.maximum(diff - half_ulp, 0.0)
+    return float(np.max(diff) / max(rms, 1e-300))
 
 
 def cpu_threads(w):
     return max(1, min(len(os.sched_getaffinity(0)), w.B * w.H))
+
+
+def cpu_model():
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, which also names Arm cores)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def host_info(nthreads):
+    """Threads the oracle used, the cores this process may run on, and the CPU model."""
+    return {"cores": nthreads, "host_cores": len(os.sched_getaffinity(0)), "cpu_model": cpu_model()}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -309,7 +349,7 @@ def run_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")},
                    "io": w.dtype},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, **host_info(nthreads), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -366,6 +406,7 @@ def run_ours(args, w):
     barrier(world)
     clocks = sampler.stop() if sampler else None
     plan.last_device_status()
+    timed_out = out.detach().cpu()  # the output of the last timed step, checked against the oracle below
     step_ms = [a.elapsed_time(b) for a, b in ev]
     # per-kernel durations: the same number of forwards again, with CUDA events around every
     # kernel launch on the plan's stream (these runs are not part of the step time)
@@ -488,12 +529,22 @@ def run_ours(args, w):
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_mean}
 
     cpu = None
+    parity = parity_detail = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = cpu_threads(w)
-        v, Ts, dt = oracle_sample(w, inp_cpu, args.cpu_seconds, nthreads,
-                                  p_gain=p_cpu.double().numpy() if nonlinear else None)
-        cpu = {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+        v, Ts, dt, ref = oracle_sample(w, inp_cpu, args.cpu_seconds, nthreads,
+                                       p_gain=p_cpu.double().numpy() if nonlinear else None)
+        cpu = {"value": v, "unit": UNIT, **host_info(nthreads), "kind": "oracle",
                "sample": f"fp64 oracle over the first {Ts} tokens of all {w.B * w.H} sequences ({dt:.1f} s)"}
+        # the timed output against the oracle rows the baseline just computed (same inputs)
+        got = timed_out[:, :, :Ts].double().numpy()
+        bf16_out = timed_out.dtype == torch.bfloat16
+        parity = parity_error(got, ref, bf16_out)
+        parity_detail = {"err": parity, "bar": 2e-2 if w.dtype == "bf16" else 1e-4,
+                         "raw_err": parity_error(got, ref, False), "tokens_per_sequence": Ts,
+                         "sequences": w.B * w.H, "output": "bf16" if bf16_out else "f32",
+                         "measure": "max|o - o_ref| / rms(o_ref)" + (" beyond each element's bf16 half-ulp"
+                                                                     if bf16_out else "")}
     plan.close()
 
     if rank == 0:
@@ -506,6 +557,7 @@ def run_ours(args, w):
                        "io": w.dtype, "l2": L2Flush.DESCRIPTION,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline, "path_roofline": path_roofline, "kernels": kernels,
+            "parity": parity, "parity_detail": parity_detail,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
             "graph_ms_per_step": graph_ms, "warm_l2_ms_per_step": warm_ms,
@@ -604,6 +656,7 @@ def run_decode(args, w):
     barrier(world)
     clocks = sampler.stop() if sampler else None
     plan.last_device_status()
+    timed_out = out.detach().cpu()  # the output of the last timed step, checked against the oracle below
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_local = sum(step_ms) / steps
     ms = max_over_ranks(ms_local, world)
@@ -645,7 +698,7 @@ def run_decode(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = max(1, min(len(os.sched_getaffinity(0)), w.B * w.H))
         v, reps, dt = decode_oracle_sample(w, inp_cpu, S_cpu, hist_cpu, args.cpu_seconds, nthreads)
-        cpu = {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+        cpu = {"value": v, "unit": UNIT, **host_info(nthreads), "kind": "oracle",
                "sample": f"fp64 oracle, one token for all {w.B * w.H} (sequence, head) pairs, {reps} times ({dt:.1f} s)"}
     plan.close()
     if rank == 0:
@@ -711,6 +764,7 @@ def run_project(args, name):
     barrier(world)
     clocks = sampler.stop() if sampler else None
     plan.last_device_status()
+    timed_out = out.detach().cpu()  # the output of the last timed step, checked against the oracle below
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_local = sum(step_ms) / steps
     ms = max_over_ranks(ms_local, world)
@@ -742,7 +796,7 @@ def run_project(args, name):
         t0 = time.perf_counter()
         prism_projection.project(sub, pi["conv_x"], pi["W"], H, R, dk, dv)
         dt = time.perf_counter() - t0
-        cpu = {"value": B_ * Ts / dt, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+        cpu = {"value": B_ * Ts / dt, "unit": UNIT, **host_info(len(os.sched_getaffinity(0))), "kind": "oracle",
                "sample": f"numpy fp64 oracle over the first {Ts} tokens of all {B_} sequences ({dt:.2f} s)"}
     plan.close()
     if rank == 0:
@@ -856,6 +910,7 @@ def run_backward(args, w):
     barrier(world)
     clocks = sampler.stop() if sampler else None
     plan.last_device_status()
+    timed_out = out.detach().cpu()  # the output of the last timed step, checked against the oracle below
     step_ms = [a.elapsed_time(b) for a, b in ev]
     plan.set_option(Bd.PRISM_OPT_TIMING, 1)
     per_kernel, launches = {}, 0
@@ -933,7 +988,7 @@ def run_backward(args, w):
         t0 = time.perf_counter()
         backward_oracle_step(sub, sd, nthreads)
         dt = time.perf_counter() - t0
-        cpu = {"value": w.B * Ts / dt, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+        cpu = {"value": w.B * Ts / dt, "unit": UNIT, **host_info(nthreads), "kind": "oracle",
                "sample": f"fp64 backward oracle over the first {Ts} tokens of all {w.B * w.H} sequences ({dt:.1f} s)"}
     plan.close()
     if rank == 0:
@@ -980,7 +1035,7 @@ def run_backward_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")}, "io": w.dtype},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, **host_info(nthreads), "kind": "oracle",
                          "sample": f"backward oracle over the first {Ts} tokens of all {w.B * w.H} sequences per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -1037,7 +1092,7 @@ def run_decode_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "dk", "dv", "L")}, "io": w.dtype},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, **host_info(nthreads), "kind": "oracle",
                          "sample": f"oracle step over all {w.B * w.H} (sequence, head) pairs"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
