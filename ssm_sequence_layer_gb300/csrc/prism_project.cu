@@ -203,7 +203,10 @@ __global__ void __launch_bounds__(PTHREADS, 2)
             const int buf = i & 1;
             const bool done = mbar_wait(smem_u32(&acc_full[buf]), (uint32_t)((i / 2) & 1), p.wait_ns);
             if (!__all_sync(0xffffffffu, done)) {
-                if (lane == 0) atomicCAS(p.status, 0, kDevTimeout);
+                if (lane == 0) {
+                    atomicCAS(p.status, 0, kDevTimeout);
+                    abort_s = 1;  // the products of this tile may still be in flight: drain before the dealloc
+                }
                 break;
             }
             fence_after_sync();

@@ -159,25 +159,29 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-__device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity)
+// One test of the phase: the thread may be suspended up to hint_ns (at most the hardware's own
+// limit) waiting for it, then the result is returned.
+__device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity, uint32_t hint_ns)
 {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(mbar), "r"(parity)
+        : "r"(mbar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
 
 // Wait for the given phase parity, bounded by max_ns of wall time (%globaltimer); false if
-// the bound ran out before the phase completed.
+// the bound ran out before the phase completed.  Each test suspends the thread for at most
+// min(max_ns, 1 ms), so that a short bound is not stretched by the hardware's own suspend limit.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint64_t max_ns)
 {
-    if (mbar_try(mbar, parity)) return true;
+    const uint32_t hint = max_ns < 1000000ull ? (uint32_t)(max_ns > 0 ? max_ns : 1) : 1000000u;
+    if (mbar_try(mbar, parity, hint)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try(mbar, parity)) return true;
+        if (mbar_try(mbar, parity, hint)) return true;
         if (globaltimer_ns() - t0 > max_ns) return false;
     }
 }
