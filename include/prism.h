@@ -304,11 +304,12 @@ PRISM_API const char *prism_last_error_message(void);
  * holds that array until the process exits.
  *
  * Sizes and tensors are those of prism_forward (layouts at the top of this file), with
- * bf16 io and out, dk = dv = 64 and 1 <= L <= 4.  The scratch needs 24 KiB per 64-token
- * chunk of all sequences plus 40 KiB per sequence and segment; the call uses as many
- * segments as prism_forward would, fewer if they do not fit, and returns
- * PRISM_ERR_UNSUPPORTED (with a message) when even one segment per sequence does not fit
- * -- about 170K token-heads.
+ * bf16 io and out, dk = dv = 64 and 1 <= L <= 4.  The call uses prism_forward's automatic
+ * segment count when its scratch fits (24 KiB per 64-token chunk of all sequences plus
+ * 40 KiB per sequence and segment: up to about 170K token-heads); otherwise one segment per
+ * sequence, which needs no per-chunk stash (40 KiB per sequence, any length, slower); and it
+ * returns PRISM_ERR_UNSUPPORTED (with a message) when even that does not fit -- more than
+ * about 1600 sequences (B * H).
  *
  * The first call on each device resolves the array's device address and sets a kernel
  * attribute; make that first call before any stream capture.  All calls share the one

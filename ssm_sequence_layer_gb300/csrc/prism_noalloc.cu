@@ -26,6 +26,9 @@ thread_local char g_noalloc_err[256] = "";
 
 prism_status noalloc_fail(prism_status s, const char *msg)
 {
+    // reset the runtime's last-error state after a failed CUDA call, so that the error is not
+    // reported again by the launch check of a later, unrelated call
+    if (s == PRISM_ERR_CUDA) (void)cudaGetLastError();
     snprintf(g_noalloc_err, sizeof(g_noalloc_err), "prism_forward_noalloc: %s", msg);
     prism_set_error_message(g_noalloc_err);
     return s;
@@ -92,18 +95,29 @@ extern "C" prism_status prism_forward_noalloc(int B, int H, int T, int dk, int d
     prism_status st = setup_device(dev, &scratch, &sms);
     if (st != PRISM_OK) return st;
 
-    // as many segments as the automatic choice, fewer if the scratch would not hold them
+    // The automatic segment count, as prism_forward chooses it, when its scratch fits.  Else one
+    // segment per sequence: a single segment starts from S = 0 and writes its outputs directly, so
+    // it needs no per-chunk stash, only its map and start state (40 KiB per sequence).
     const size_t avail = (size_t)PRISM_NOALLOC_SCRATCH_BYTES - 256;
     int P = prism::tc_segments(s, sms, 0);
-    while (P > 1 && prism::tc_workspace_bytes(s, P) > avail) --P;
-    if (prism::tc_workspace_bytes(s, P) > avail)
+    bool stash = true;
+    if (prism::tc_workspace_bytes(s, P) > avail) {
+        P = 1;
+        stash = false;
+    }
+    const size_t maps_bytes = (size_t)s.BH * (128 * 64 * 4 + 64 * 64 * 2) + 256;
+    if (!stash && maps_bytes > avail)
         return noalloc_fail(PRISM_ERR_UNSUPPORTED,
-                            "problem too large for the fixed scratch (needs 24 KiB per 64-token chunk "
-                            "of all sequences plus 40 KiB per sequence and segment; 64 MiB in total)");
+                            "problem too large for the fixed scratch (one segment per sequence needs 40 KiB "
+                            "per sequence; several need 24 KiB more per 64-token chunk; 64 MiB in total)");
 
     int *d_status = (int *)scratch;
     prism::TcWorkspace w;
     prism::tc_carve(s, P, (char *)scratch + 256, &w);
+    if (!stash) {  // never read or written with one segment and no initial state
+        w.stash_o = nullptr;
+        w.stash_q = nullptr;
+    }
     cudaStream_t cs = (cudaStream_t)stream;
     if (cudaMemsetAsync(d_status, 0, sizeof(int), cs) != cudaSuccess)
         return noalloc_fail(PRISM_ERR_CUDA, "clearing the status word failed");
