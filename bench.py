@@ -107,6 +107,8 @@ def kernel_alg_bytes(name, w, nonlinear=False):
     S0 = chunks * w.dv * w.dk * 4
     p_or_eta = th * R * w.dv * io if nonlinear else th * 4 * R
     table = {
+        "map_chunks": q + k + v + u + gates,      # every input read once (the maps are its own output)
+        "map_scan": out,                          # the outputs written once (the maps are read back)
         "simt_prep": v + th * 4 * R + p_or_eta + X,
         "simt_chunk_solve": k + th * 8 + lam + Tm,
         "simt_wy": k + v + th * 4 + u + X + lam + Tm + W + Up,
@@ -122,6 +124,7 @@ def kernel_alg_bytes(name, w, nonlinear=False):
 KERNEL_SOURCES = {
     "project": ("prism_project.cu", "prism_project.h", "tc_ptx.h", "prism_internal.h"),
     "tc_": ("prism_tc.cu", "tc_ptx.h", "prism_internal.h"),
+    "map_": ("prism_map.cu", "tc_util.h", "tc_ptx.h", "prism_internal.h"),
     "decode": ("prism_state.cu", "tc_ptx.h", "prism_internal.h"),
     "simt_": ("prism_simt.cu", "prism_internal.h"),
     "bwd_": ("prism_backward.cu", "prism_internal.h"),

@@ -102,23 +102,30 @@ void tensor_bytes(const prism_plan_s *p, size_t nb[10])
     nb[9] = th * s.dv * io_size(p->out_dtype);
 }
 
-// 1 = portable fp32 kernels, 2 = tensor-core path
+// 1 = portable fp32 kernels, 2 = tensor-core path (the segment kernels for dk = dv = 64 and
+// L <= 4, the chunk-map kernels for dk = dv = 128 and L <= 16)
+bool tensor_core_shape(const prism_plan_s *p)
+{
+    return prism::tc_supported(p->shape, p->io) || prism::map_supported(p->shape, p->io);
+}
+
 int resolve_path(const prism_plan_s *p)
 {
     if (p->opt_path == 1) return 1;
     if (p->opt_path == 2) return 2;
-    return prism::tc_supported(p->shape, p->io) ? 2 : 1;
+    return tensor_core_shape(p) ? 2 : 1;
 }
 
 void free_workspaces(prism_plan_s *p)
 {
     if (p->ws_simt) cudaFree(p->ws_simt);
     if (p->ws_tc) cudaFree(p->ws_tc);
+    if (p->ws_map) cudaFree(p->ws_map);
     if (p->d_status) cudaFree(p->d_status);
     if (p->ws_bwd) cudaFree(p->ws_bwd);
     p->ws_bwd = nullptr;
     p->ws_bwd_bytes = 0;
-    p->ws_simt = p->ws_tc = nullptr;
+    p->ws_simt = p->ws_tc = p->ws_map = nullptr;
     p->d_status = nullptr;
 }
 
@@ -134,6 +141,17 @@ prism_status ensure_workspace(prism_plan_s *p, int path)
         }
         p->ws_simt_bytes = bytes;
         prism::simt_carve(p->shape, p->ws_simt, &p->simt);
+        return PRISM_OK;
+    }
+    if (!prism::tc_supported(p->shape, p->io)) {  // chunk-map kernels
+        if (p->ws_map) return PRISM_OK;
+        const size_t bytes = prism::map_workspace_bytes(p->shape);
+        if ((e = cudaMalloc(&p->ws_map, bytes)) != cudaSuccess) {
+            p->ws_map = nullptr;
+            return cuda_fail(e, "workspace allocation (chunk-map kernels)");
+        }
+        p->ws_map_bytes = bytes;
+        prism::map_carve(p->shape, p->ws_map, &p->mapw);
         return PRISM_OK;
     }
     const int P = prism::tc_segments(p->shape, p->sm_count, p->opt_segments);
@@ -174,14 +192,18 @@ prism_status run_forward(prism_plan_s *p, const prism::ForwardArgs &a, struct CU
             return fail(PRISM_ERR_UNSUPPORTED, "the non-linear residual variant has no tensor-core path");
         path = 1;
     }
-    if (path == 2 && !prism::tc_supported(p->shape, p->io))
-        return fail(PRISM_ERR_UNSUPPORTED, "the tensor-core path takes bf16 io, dk = dv = 64 and L <= 4");
+    if (path == 2 && !tensor_core_shape(p))
+        return fail(PRISM_ERR_UNSUPPORTED,
+                    "the tensor-core path takes bf16 io with dk = dv = 64 and L <= 4, or dk = dv = 128 and L <= 16");
     if ((st = ensure_workspace(p, path)) != PRISM_OK) return st;
     p->timer.on = p->opt_timing != 0;
     p->timer.reset((cudaStream_t)stream);
     cudaError_t e;
-    if (path == 2)
+    if (path == 2 && prism::tc_supported(p->shape, p->io))
         e = prism::tc_forward(p->shape, a, p->out_dtype == PRISM_F32, p->tcw, p->d_status, p->opt_wait_ns, p->timer);
+    else if (path == 2)
+        e = prism::map_forward(p->shape, a, p->out_dtype == PRISM_F32, p->mapw, p->sm_count, p->d_status,
+                               p->opt_wait_ns, p->timer);
     else
         e = prism::simt_forward(p->shape, p->io, p->out_dtype, a, p->simt, p->d_status, p->timer);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -235,6 +257,7 @@ prism_status prism_plan(int B, int H, int T, int dk, int dv, int L, prism_dtype 
 
     cudaError_t e = prism::simt_prepare(s, io);
     if (e == cudaSuccess && prism::tc_supported(s, io)) e = prism::tc_prepare();
+    if (e == cudaSuccess && prism::map_supported(s, io)) e = prism::map_prepare();
     if (e == cudaSuccess && io == PRISM_BF16) e = prism::project_prepare();
     if (e == cudaSuccess) e = prism::backward_prepare();
     if (e != cudaSuccess) {
@@ -517,7 +540,10 @@ prism_status prism_plan_destroy(prism_plan_t p)
     return PRISM_OK;
 }
 
-size_t prism_workspace_bytes(prism_plan_t p) { return p ? p->ws_simt_bytes + p->ws_tc_bytes + p->ws_bwd_bytes : 0; }
+size_t prism_workspace_bytes(prism_plan_t p)
+{
+    return p ? p->ws_simt_bytes + p->ws_tc_bytes + p->ws_map_bytes + p->ws_bwd_bytes : 0;
+}
 
 int prism_plan_kernel_times(prism_plan_t p, prism_kernel_time *out, int max)
 {

@@ -93,6 +93,21 @@ cudaError_t tc_prepare();
 cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const TcWorkspace &w, int *d_status,
                        long long wait_ns, KernelTimer &tm);
 
+// Workspace of the chunk-map path (dk = dv = 128): the per-chunk maps, fp16, row-major.
+struct MapWorkspace {
+    __half *A;  // [BH*NC][128][128]  A_c (state -> state)
+    __half *Q;  // [BH*NC][64][128]   Q~   (state -> outputs)
+    __half *B;  // [BH*NC][128][128]  B_c (the chunk's own write)
+    __half *O;  // [BH*NC][64][128]   O_loc (the chunk's outputs from a zero state)
+};
+
+bool map_supported(const Shape &s, prism_dtype io);
+size_t map_workspace_bytes(const Shape &s);
+void map_carve(const Shape &s, void *base, MapWorkspace *w);
+cudaError_t map_prepare();
+cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const MapWorkspace &w, int sm_count,
+                        int *d_status, long long wait_ns, KernelTimer &tm);
+
 // v_hist_out = the last three tokens of [v_hist; v] (kernel in prism_state.cu); safe in place
 cudaError_t launch_history(const Shape &s, prism_dtype io, const void *v_hist, const void *v, void *v_hist_out,
                            KernelTimer &tm);
@@ -150,6 +165,9 @@ struct prism_plan_s {
     void *ws_tc;
     size_t ws_tc_bytes;
     prism::TcWorkspace tcw;
+    void *ws_map;
+    size_t ws_map_bytes;
+    prism::MapWorkspace mapw;
     // workspace of the backward pass (owned, allocated by the first prism_backward)
     void *ws_bwd;
     size_t ws_bwd_bytes;

@@ -1,0 +1,968 @@
+// Chunk-map path of the PRISM memory-recurrence forward (sm_103a: tcgen05 + TMA), for
+// dk = dv = 128, 1 <= L <= 16, bf16 io.
+//
+// The recurrence over one 64-token chunk is an affine map of the state entering it (notes on
+// PRISM, section 2.2, the A/B form S_t = S_{t-1} A_t + B_t, composed over the chunk), and the
+// chunk's outputs are affine in that state too:
+//   S_next = S A_c + B_c,      O = O_loc + Q~ S^T.
+// Two kernels:
+//   map   one CTA per SM, looping over chunks (every chunk independent of the others): the prep
+//         (anchor, gain, residual chain), the Gram tiles of every level, the UT solve, the WY
+//         factors, and the four map tensors A_c [dk][dk], B_c [dv][dk], Q~ [C][dk], O_loc [C][dv]
+//         (fp16) written to the plan's workspace.
+//   scan  one CTA per sequence: S <- S A_c + B_c and o = O_loc + Q~ S^T chunk after chunk, the
+//         maps streamed through a two-stage TMA ring, both products on the tensor core.
+//
+// Chunk algebra (local index i, j; lambda_i = sum_{m<=i} ln alpha_m; lc = lambda_{C-1};
+// D_ij = e^{lambda_i - lambda_j} (j <= i); colf_j = e^{lc - lambda_j}; Gamma_i = e^{lambda_i}),
+// with the level key tiles U_{-1} = K, U_l (l < R) and x_{t,l} = gamma_{t,l} g_t (.) r_{t,l}:
+//   Gram of level l:  [Q; K] U_l^T  -> rows i < 64: q_i.u_{j,l}, rows 64 + i: k_i.u_{j,l}
+//   G~ = D o (Q K^T) (j <= i),  A = diag(beta) D o (K K^T) (j < i)  ->  T = (I + A)^{-1}
+//   PQ_l = D o (Q U_l^T) (j <= i),  PK_l = D o (K U_l^T) (j < i)
+//   [O_X ; MX] = sum_l [PQ_l ; PK_l] X_l,    B_X = sum_l X_l^T U'_l   (U'_l = diag(colf) U_l)
+//   RHS = diag(beta) (V - MX),  U' = T RHS,  W = T diag(beta Gamma) K,  K' = diag(colf) K
+//   B_c = B_X + U'^T K',  O_loc = O_X + G~ U',  A_c = Gamma_C I - W^T K',  Q~ = diag(Gamma) Q - G~ W
+// Every decay a product needs is applied in fp32 before an operand is rounded to fp16 (the pair
+// decays on the score tiles, colf on the state-side key tiles), so fp16 underflow only drops
+// contributions below its range, however strong the decay.
+//
+// Products (tcgen05.mma kind::f16, fp32 accumulators in tensor memory): the Grams on the bf16
+// input tiles; everything after them on fp16 operands (10-bit mantissa), the computed operands
+// staying of order one.
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "prism_internal.h"
+#include "tc_ptx.h"
+#include "tc_util.h"
+
+namespace prism {
+namespace mp {
+
+using namespace tc;
+using tcu::dsc;
+using tcu::Flag;
+using tcu::pack_h2;
+using tcu::set_status;
+using tcu::st_row_h;
+
+constexpr int C = kChunk;
+constexpr int D = 128;       // dk = dv
+constexpr int RM = 15;       // levels handled (L <= 16)
+constexpr int RMS = 16;      // row stride of the per-token level scalars
+constexpr int NT = 512;      // threads of the map kernel: 16 warps, 4 per TMEM lane quarter
+constexpr uint32_t PANEL = 8192;  // [64 rows][64 cols] 16-bit SW128
+
+// ---- map kernel: shared memory (bytes from a 1024-aligned base) -------------------------------
+constexpr uint32_t OFF_QK = 0;                     // [Q_p0 | K_p0 | Q_p1 | K_p1] (bf16; K later K' fp16)
+constexpr uint32_t OFF_V = 32768;                  // V rows t0-8 .. t0+63, [72][128] bf16, unswizzled
+constexpr uint32_t VBYTES = 72 * D * 2;
+constexpr uint32_t OFF_G = OFF_V + VBYTES;          // G~ [64][64] fp16 K-major
+constexpr uint32_t OFF_TF = OFF_G + PANEL;          // T  [64][64] fp16 K-major
+constexpr uint32_t OFF_A = OFF_TF + PANEL;          // A   fp32 [64][LDA]
+constexpr uint32_t OFF_T32 = OFF_A + 64 * tcu::LDA * 4;  // T fp32 [64][LDA]
+constexpr uint32_t OFF_LV = OFF_T32 + 64 * tcu::LDA * 4; // two level buffers
+constexpr uint32_t LVB = 3 * 2 * PANEL;             // per level buffer: U (2 panels) | [PQ; PK] | X (2 panels)
+constexpr uint32_t LV_U = 0, LV_PQK = 2 * PANEL, LV_X = 4 * PANEL;
+// after the level loop the level buffers hold RHS, diag(beta Gamma) K, U' and W ([64][128] fp16)
+constexpr uint32_t OFF_RHS = OFF_LV, OFF_BGK = OFF_LV + 2 * PANEL, OFF_UP = OFF_LV + 4 * PANEL,
+                   OFF_W = OFF_LV + 6 * PANEL;
+constexpr uint32_t OFF_SC = OFF_LV + 2 * LVB;       // per-token scalars
+constexpr uint32_t SC_FLOATS = 6 * 64 + 2 * 64 * RMS + tcu::SOLVE_SCRATCH;
+constexpr uint32_t MAP_SMEM = OFF_SC + SC_FLOATS * 4 + 1024;  // + alignment slack
+
+static_assert(OFF_V % 1024 == 0 && OFF_G % 1024 == 0 && OFF_TF % 1024 == 0 && OFF_LV % 1024 == 0 &&
+                  LVB % 1024 == 0 && OFF_SC % 16 == 0,
+              "alignment of the tiles");
+static_assert(OFF_W + 2 * PANEL <= OFF_LV + 2 * LVB, "post-solve tiles fit the level buffers");
+static_assert(MAP_SMEM <= 232448, "shared memory budget");
+
+// tensor memory columns (512 allocated)
+constexpr uint32_t TM_GRAM = 0;     // two 64-column Gram buffers (by level parity)
+constexpr uint32_t TM_OX = 128;     // [O_X ; MX] (rows i < 64: O_loc, rows 64 + i: MX), 128 columns
+constexpr uint32_t TM_BX = 256;     // B_c [c][n]
+constexpr uint32_t TM_UP = 0;       // U' [i][c]       (after the level loop)
+constexpr uint32_t TM_W = 384;      // W  [j][n]
+constexpr uint32_t TM_AC = 0;       // W^T K' [m][n]   (after U' and W are in shared memory)
+constexpr uint32_t TM_QT = 384;     // G~ W   [i][n]
+
+struct MapParams {
+    const float *beta, *alpha, *gamma, *eta;
+    const __nv_bfloat16 *conv_w;
+    const __nv_bfloat16 *v_hist;  // [BH][3][D] v_{-3..-1}, or null
+    __half *mA, *mQ, *mB, *mO;    // [BH*NC][128][128], [BH*NC][64][128], [BH*NC][128][128], [BH*NC][64][128]
+    int *status;
+    int H, T, R, NC, nchunks;
+    unsigned long long wait_ns;
+};
+
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(NT, 1)
+    map_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_u, MapParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint32_t tmem_base_s;
+    __shared__ __align__(8) uint64_t mbar[8];  // 0 Q/K/V, 1-2 U buffers, 3 Gram, 4-5 level products, 6 post products, 7 drain
+    __shared__ int abort_s;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, sub = warp >> 2;
+    const int row = quad * 32 + lane;  // TMEM lane of this thread in epilogues
+    const int R = p.R;
+
+    float *sc = reinterpret_cast<float *>(sm + OFF_SC);
+    float *s_beta = sc, *s_lam = sc + 64, *s_rowf = sc + 128, *s_colf = sc + 192, *s_gam = sc + 256,
+          *s_bg = sc + 320;
+    float *s_gm = sc + 384, *s_et = s_gm + 64 * RMS;  // [64][RMS] gamma, eta
+    float *s_xtmp = s_et + 64 * RMS;
+
+    const uint32_t sbase = smem_u32(sm);
+    const uint64_t dbase = sdesc(sbase, 0, 0);
+    const uint32_t mb_qkv = smem_u32(&mbar[0]), mb_gram = smem_u32(&mbar[3]), mb_post = smem_u32(&mbar[6]);
+    const uint32_t mb_u[2] = {smem_u32(&mbar[1]), smem_u32(&mbar[2])};
+    const uint32_t mb_lvl[2] = {smem_u32(&mbar[4]), smem_u32(&mbar[5])};
+
+    if (tid == 0) {
+        abort_s = 0;
+        for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&mbar[i]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_u);
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_base_s;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    // the maps this kernel writes may still be read by the previous forward's scan kernel
+    grid_dependency_wait();
+    allow_dependent_launch();
+
+    // phases of the barriers (every thread tracks the ones it waits on)
+    uint32_t ph_qkv = 0, ph_gram = 0, ph_post = 0, ph_u[2] = {0, 0}, ph_lvl[2] = {0, 0};
+    // thread 0: the copies it has in flight and the level products it has not waited for
+    bool pend_qkv = false, pend_u[2] = {false, false}, pend_lvl[2] = {false, false};
+    auto expired = [&]() {
+        abort_s = 1;
+        set_status(p.status, kDevTimeout);
+    };
+    // every thread waits on an MMA barrier itself (no CTA barrier needs to follow); after an expiry
+    // the chunk loop ends at the next CTA barrier and the drain waits for the products
+    auto wait_all = [&](uint32_t mb, uint32_t &ph) {
+        if (!mbar_wait(mb, ph, p.wait_ns)) expired();
+        ph ^= 1u;
+    };
+    auto issue_u = [&](int chunk_bh, int t0, int l) {
+        const int b = l & 1;
+        const uint32_t dst = sbase + OFF_LV + b * LVB + LV_U;
+        mbar_expect_tx(mb_u[b], 2 * PANEL);
+        tma_load_4d(dst, &tm_u, mb_u[b], 0, l, t0, chunk_bh);
+        tma_load_4d(dst + PANEL, &tm_u, mb_u[b], 64, l, t0, chunk_bh);
+        pend_u[b] = true;
+    };
+
+    // this thread's prep elements: channels 2 cp, 2 cp + 1 of tokens tg + 8 k
+    const int cp = tid & 63, tg = tid >> 6;
+
+    for (int chunk = blockIdx.x; chunk < p.nchunks && abort_s == 0; chunk += gridDim.x) {
+        const int bh = chunk / p.NC, c = chunk % p.NC, h = bh % p.H;
+        const int t0 = c * C, n = min(C, p.T - t0);
+        const size_t tok0 = (size_t)bh * p.T + t0;
+
+        // ---- loads of this chunk (the previous chunk's readers are done: see the loop's end) ----
+        if (tid == 0) {
+            mbar_expect_tx(mb_qkv, 4 * PANEL + VBYTES);
+            tma_load_3d(sbase + OFF_QK, &tm_q, mb_qkv, 0, t0, bh);
+            tma_load_3d(sbase + OFF_QK + PANEL, &tm_k, mb_qkv, 0, t0, bh);
+            tma_load_3d(sbase + OFF_QK + 2 * PANEL, &tm_q, mb_qkv, 64, t0, bh);
+            tma_load_3d(sbase + OFF_QK + 3 * PANEL, &tm_k, mb_qkv, 64, t0, bh);
+            tma_load_3d(sbase + OFF_V, &tm_v, mb_qkv, 0, t0 - 8, bh);
+            pend_qkv = true;
+            if (R > 0) issue_u(bh, t0, 0);
+            if (R > 1) issue_u(bh, t0, 1);
+        }
+        // ---- per-token scalars: gates, log-decay prefix, decay factors ----------------------------
+        if (warp == 0) {  // inclusive scan of the 64 log-decays, two per lane
+            const int i0 = 2 * lane, i1 = i0 + 1;
+            const float b0 = i0 < n ? p.beta[tok0 + i0] : 0.f, b1 = i1 < n ? p.beta[tok0 + i1] : 0.f;
+            const float la0 = i0 < n ? logf(p.alpha[tok0 + i0]) : 0.f, la1 = i1 < n ? logf(p.alpha[tok0 + i1]) : 0.f;
+            float s = la0 + la1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, s, off);
+                if (lane >= off) s += y;
+            }
+            const float l1 = s, l0 = s - la1;
+            const float lcw = __shfl_sync(0xffffffffu, s, 31);
+            s_beta[i0] = b0;
+            s_beta[i1] = b1;
+            s_lam[i0] = l0;
+            s_lam[i1] = l1;
+            s_rowf[i0] = __expf(l0 - lcw);  // used only while the chunk's decay is within fp32 range
+            s_rowf[i1] = __expf(l1 - lcw);
+            s_colf[i0] = __expf(lcw - l0);
+            s_colf[i1] = __expf(lcw - l1);
+            s_gam[i0] = __expf(l0);
+            s_gam[i1] = __expf(l1);
+            s_bg[i0] = b0 * __expf(l0);
+            s_bg[i1] = b1 * __expf(l1);
+        } else if (R > 0) {  // gamma, eta [i][l] of this chunk
+            for (int e = tid - 32; e < 64 * R; e += NT - 32) {
+                const int i = e / R, l = e % R;
+                const bool valid = i < n;
+                s_gm[i * RMS + l] = valid ? p.gamma[(tok0 + i) * R + l] : 0.f;
+                s_et[i * RMS + l] = valid ? p.eta[(tok0 + i) * R + l] : 0.f;
+            }
+        }
+        // Q, K and V have landed (every thread waits; the history, if any, then replaces the halo)
+        if (tid == 0) {
+            if (mbar_wait(mb_qkv, ph_qkv, p.wait_ns)) pend_qkv = false;
+            else expired();
+        }
+        ph_qkv ^= 1u;
+        __syncthreads();
+        if (abort_s) break;
+        if (c == 0 && p.v_hist != nullptr) {
+            if (tid < 48) {  // rows 5..7 of the tile (tokens -3..-1): 3 x 16 groups of 16 bytes
+                const uint4 hv = reinterpret_cast<const uint4 *>(p.v_hist + (size_t)bh * 3 * D)[tid];
+                *reinterpret_cast<uint4 *>(sm + OFF_V + 5 * D * 2 + tid * 16) = hv;
+                fence_async_smem();  // a later TMA rewrites the tile
+            }
+            __syncthreads();
+        }
+        const float lc = s_lam[63];
+        const bool factored = -lc <= 80.f;  // both decay factors in fp32 range
+
+        // ---- level -1 (the key level): Gram [Q; K] K^T -------------------------------------------
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t ko = (uint32_t)(s >> 2) * 2 * PANEL + (uint32_t)(s & 3) * 32;
+                mma_f16(tmem + TM_GRAM, dsc(dbase, OFF_QK + ko, 16, 1024), dsc(dbase, OFF_QK + PANEL + ko, 16, 1024), id,
+                        s > 0);
+            }
+            mma_commit(mb_gram);
+        }
+        // prep, level-independent part: anchor h, gain g, residual r = v - GELU(h)
+        float g_[8][2], r_[8][2];
+        {
+            const __nv_bfloat162 *cw2 = reinterpret_cast<const __nv_bfloat162 *>(p.conv_w) + (size_t)h * 4 * (D / 2) + cp;
+            const float2 w0 = __bfloat1622float2(cw2[0]), w1 = __bfloat1622float2(cw2[D / 2]);
+            const float2 w2 = __bfloat1622float2(cw2[2 * (D / 2)]), w3 = __bfloat1622float2(cw2[3 * (D / 2)]);
+            const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + OFF_V);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = tg + 8 * k;
+                const float2 v0 = __bfloat1622float2(vb[(i + 8) * (D / 2) + cp]);
+                const float2 v1 = __bfloat1622float2(vb[(i + 7) * (D / 2) + cp]);
+                const float2 v2 = __bfloat1622float2(vb[(i + 6) * (D / 2) + cp]);
+                const float2 v3 = __bfloat1622float2(vb[(i + 5) * (D / 2) + cp]);
+                const float a0 = fmaf(w0.x, v0.x, fmaf(w1.x, v1.x, fmaf(w2.x, v2.x, w3.x * v3.x)));
+                const float a1 = fmaf(w0.y, v0.y, fmaf(w1.y, v1.y, fmaf(w2.y, v2.y, w3.y * v3.y)));
+                float Phi0, Phi1;
+                tcu::gelu_gain(a0, g_[k][0], Phi0);
+                tcu::gelu_gain(a1, g_[k][1], Phi1);
+                r_[k][0] = v0.x - a0 * Phi0;
+                r_[k][1] = v0.y - a1 * Phi1;
+            }
+        }
+        wait_all(mb_gram, ph_gram);
+        fence_after_sync();
+
+        // E1 of one level: the Gram buffer `gb` (64 columns) -> decayed, masked score rows.  Thread
+        // (quad, sub) holds TMEM row `row` (i = row & 63; rows < 64 the query side, j <= i kept;
+        // rows >= 64 the key side, j < i kept) and columns 16 sub .. 16 sub + 15.
+        auto scores = [&](uint32_t gb, float (&v)[16], bool &query, int &i) {
+            const int j0 = sub * 16;
+            i = row & 63;
+            query = row < 64;
+            float dq[16];
+            auto fill = [&](auto form) {
+                if constexpr (decltype(form)::value) {
+                    const float rf = s_rowf[i];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const float4 f = reinterpret_cast<const float4 *>(s_colf + j0)[g];
+                        dq[4 * g + 0] = rf * f.x;
+                        dq[4 * g + 1] = rf * f.y;
+                        dq[4 * g + 2] = rf * f.z;
+                        dq[4 * g + 3] = rf * f.w;
+                    }
+                } else {
+                    const float li = s_lam[i];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) dq[q] = __expf(fminf(li - s_lam[j0 + q], 0.f));
+                }
+            };
+            if (factored)
+                fill(Flag<true>{});
+            else
+                fill(Flag<false>{});
+            tmem_ld(tmem + gb + lane_off + (uint32_t)j0, v);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int j = j0 + q;
+                v[q] = (query ? j <= i : j < i) ? v[q] * dq[q] : 0.f;
+            }
+        };
+        {
+            float v[16];
+            bool query;
+            int i;
+            scores(TM_GRAM, v, query, i);
+            if (query) {
+                st_row_h(sm + OFF_G, i, sub * 16, v);
+            } else {  // A_ij = beta_i D_ij k_i.k_j
+                float4 *A4 = reinterpret_cast<float4 *>(sm + OFF_A + (i * tcu::LDA + sub * 16) * 4);
+                const float b = s_beta[i];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) A4[g] = make_float4(b * v[4 * g], b * v[4 * g + 1], b * v[4 * g + 2], b * v[4 * g + 3]);
+            }
+        }
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- levels 0 .. R-1 -------------------------------------------------------------------------
+        for (int l = 0; l < R; ++l) {
+            const int b = l & 1;
+            const uint32_t lvb = OFF_LV + b * LVB;
+            if (tid == 0) {
+                // the other buffer is free once level l - 1's products have completed: prefetch U_{l+1}
+                if (l >= 1 && l + 1 < R) {
+                    if (mbar_wait(mb_lvl[b ^ 1], ph_lvl[b ^ 1], p.wait_ns)) {
+                        ph_lvl[b ^ 1] ^= 1u;
+                        pend_lvl[b ^ 1] = false;
+                        issue_u(bh, t0, l + 1);
+                    } else {
+                        expired();
+                    }
+                }
+                if (mbar_wait(mb_u[b], ph_u[b], p.wait_ns)) {
+                    ph_u[b] ^= 1u;
+                    pend_u[b] = false;
+                    fence_after_sync();
+                    const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t ko = (uint32_t)(s >> 2) * 2 * PANEL + (uint32_t)(s & 3) * 32;
+                        const uint32_t uo = lvb + LV_U + (uint32_t)(s >> 2) * PANEL + (uint32_t)(s & 3) * 32;
+                        mma_f16(tmem + TM_GRAM + 64 * b, dsc(dbase, OFF_QK + ko, 16, 1024), dsc(dbase, uo, 16, 1024), id,
+                                s > 0);
+                    }
+                    mma_commit(mb_gram);
+                } else {
+                    expired();
+                }
+            }
+            __syncthreads();  // an expiry above is seen by every thread before it waits on the Gram
+            if (abort_s) break;
+            wait_all(mb_gram, ph_gram);
+            fence_after_sync();
+            {  // [PQ_l ; PK_l] rows
+                float v[16];
+                bool query;
+                int i;
+                scores(TM_GRAM + 64 * b, v, query, i);
+                st_row_h(sm + lvb + LV_PQK, row, sub * 16, v);
+            }
+            // U_l -> U'_l = diag(colf) U_l (fp16, in place; the Gram has read it)
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int e = tid + NT * e2;  // 16-byte group: panel e >> 9, row (e & 511) >> 3
+                uint4 w = reinterpret_cast<const uint4 *>(sm + lvb + LV_U)[e];
+                const float sc_j = s_colf[(e & 511) >> 3];
+                uint32_t *pw = &w.x;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pw[q]));
+                    pw[q] = pack_h2(sc_j * f.x, sc_j * f.y);
+                }
+                reinterpret_cast<uint4 *>(sm + lvb + LV_U)[e] = w;
+            }
+            // X_l = gamma_l g r, then r <- r (1 - eta_l g)
+            {
+                uint8_t *xp = sm + lvb + LV_X + (uint32_t)((2 * cp) >> 6) * PANEL;
+                const int col = (2 * cp) & 63;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int i = tg + 8 * k;
+                    const float gm = s_gm[i * RMS + l], et = s_et[i * RMS + l];
+                    *reinterpret_cast<uint32_t *>(xp + sw128(i, col)) =
+                        pack_h2(gm * g_[k][0] * r_[k][0], gm * g_[k][1] * r_[k][1]);
+                    r_[k][0] *= 1.f - et * g_[k][0];
+                    r_[k][1] *= 1.f - et * g_[k][1];
+                }
+            }
+            fence_async_smem();
+            fence_before_sync();
+            __syncthreads();
+            if (tid == 0) {
+                fence_after_sync();
+                // [O_X ; MX] += [PQ_l ; PK_l] X_l   (A K-major, B = X_l [j][c] MN-major)
+                const uint32_t id1 = idesc_f16(128, 128, 0, 1);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(tmem + TM_OX, dsc(dbase, lvb + LV_PQK + s * 32, 16, 1024),
+                            dsc(dbase, lvb + LV_X + s * 2048, PANEL, 1024), id1, (l | s) != 0);
+                // B_X += X_l^T U'_l   (A = X_l [j][c] MN-major, B = U'_l [j][n] MN-major)
+                const uint32_t id2 = idesc_f16(128, 128, 1, 1);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(tmem + TM_BX, dsc(dbase, lvb + LV_X + s * 2048, PANEL, 1024),
+                            dsc(dbase, lvb + LV_U + s * 2048, PANEL, 1024), id2, (l | s) != 0);
+                mma_commit(mb_lvl[b]);
+                pend_lvl[b] = true;
+            }
+        }
+        if (abort_s) break;
+
+        // ---- after the levels: the products of the last ones complete, then the solve (warps 8-15)
+        // beside the RHS, diag(beta Gamma) K and K' (warps 0-7) ---------------------------------------
+        if (tid == 0) {
+            for (int b = 0; b < 2; ++b)
+                if (pend_lvl[b]) {
+                    if (mbar_wait(mb_lvl[b], ph_lvl[b], p.wait_ns)) {
+                        ph_lvl[b] ^= 1u;
+                        pend_lvl[b] = false;
+                    } else {
+                        expired();
+                    }
+                }
+        }
+        fence_before_sync();
+        __syncthreads();
+        if (abort_s) break;
+        fence_after_sync();
+        if (warp >= 8) {
+            tcu::ut_solve(reinterpret_cast<const float *>(sm + OFF_A), reinterpret_cast<float *>(sm + OFF_T32), s_xtmp,
+                          sm + OFF_TF, tid - 256, 1);
+        } else if (quad >= 2) {  // RHS = diag(beta) (V - MX): TMEM rows 64 + i, 64 columns per thread
+            const int i = row - 64, c0 = (warp >> 2) * 64;
+            const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_V) + (size_t)(i + 8) * D;
+            const float bi = s_beta[i];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float mx[32];
+                if (R > 0) {
+                    tmem_ld(tmem + TM_OX + lane_off + (uint32_t)(c0 + 32 * half), mx);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) mx[q] = 0.f;  // no levels: MX = 0 (never written)
+                }
+                float rv[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) rv[q] = bi * (__bfloat162float(vb[c0 + 32 * half + q]) - mx[q]);
+                st_row_h(sm + OFF_RHS + (uint32_t)(c0 >> 6) * PANEL, i, 32 * half, rv);
+            }
+        } else {  // diag(beta Gamma) K and K' = diag(colf) K from the bf16 K panels (warps 0, 1, 4, 5)
+            const int t = (warp >> 2) * 64 + (warp & 1) * 32 + lane;  // 0..127
+            for (int e = t; e < 1024; e += 128) {
+                const int pnl = e >> 9, j = (e & 511) >> 3;
+                uint8_t *kp = sm + OFF_QK + PANEL + (uint32_t)pnl * 2 * PANEL;
+                uint4 w = reinterpret_cast<const uint4 *>(kp)[e & 511];
+                uint4 wb = w;
+                const float bg = s_bg[j], cf = s_colf[j];
+                uint32_t *pw = &w.x, *pb = &wb.x;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pw[q]));
+                    pb[q] = pack_h2(bg * f.x, bg * f.y);
+                    pw[q] = pack_h2(cf * f.x, cf * f.y);
+                }
+                reinterpret_cast<uint4 *>(sm + OFF_BGK + (uint32_t)pnl * PANEL)[e & 511] = wb;
+                reinterpret_cast<uint4 *>(kp)[e & 511] = w;
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- U' = T RHS, W = T diag(beta Gamma) K ------------------------------------------------------
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t id = idesc_f16(128, 128, 0, 1);  // A = T [i][j] K-major (rows 64.. unused)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                mma_f16(tmem + TM_UP, dsc(dbase, OFF_TF + s * 32, 16, 1024), dsc(dbase, OFF_RHS + s * 2048, PANEL, 1024), id,
+                        s > 0);
+                mma_f16(tmem + TM_W, dsc(dbase, OFF_TF + s * 32, 16, 1024), dsc(dbase, OFF_BGK + s * 2048, PANEL, 1024), id,
+                        s > 0);
+            }
+            mma_commit(mb_post);
+        }
+        wait_all(mb_post, ph_post);
+        fence_after_sync();
+        if (quad < 2) {  // rows i < 64: sub 0, 1 -> U' columns, sub 2, 3 -> W columns (64 per thread)
+            const bool isw = sub >= 2;
+            const int c0 = (sub & 1) * 64;
+            const uint32_t src = tmem + (isw ? TM_W : TM_UP) + lane_off + (uint32_t)c0;
+            uint8_t *dst = sm + (isw ? OFF_W : OFF_UP) + (uint32_t)(c0 >> 6) * PANEL;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float v[32];
+                tmem_ld(src + 32 * half, v);
+                st_row_h(dst, row, 32 * half, v);
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (abort_s) break;
+
+        // ---- B_c += U'^T K', O_loc += G~ U', W^T K', G~ W ----------------------------------------------
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t idmm = idesc_f16(128, 128, 1, 1), idkm = idesc_f16(128, 128, 0, 1);
+            const uint32_t kq = OFF_QK + PANEL;  // K' panels at 16 KB stride
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint32_t ks = s * 2048;
+                mma_f16(tmem + TM_BX, dsc(dbase, OFF_UP + ks, PANEL, 1024), dsc(dbase, kq + ks, 2 * PANEL, 1024), idmm,
+                        (R > 0 || s > 0) ? 1u : 0u);
+                mma_f16(tmem + TM_OX, dsc(dbase, OFF_G + s * 32, 16, 1024), dsc(dbase, OFF_UP + ks, PANEL, 1024), idkm,
+                        (R > 0 || s > 0) ? 1u : 0u);
+                mma_f16(tmem + TM_AC, dsc(dbase, OFF_W + ks, PANEL, 1024), dsc(dbase, kq + ks, 2 * PANEL, 1024), idmm, s > 0);
+                mma_f16(tmem + TM_QT, dsc(dbase, OFF_G + s * 32, 16, 1024), dsc(dbase, OFF_W + ks, PANEL, 1024), idkm, s > 0);
+            }
+            mma_commit(mb_post);
+        }
+        wait_all(mb_post, ph_post);
+        fence_after_sync();
+
+        // ---- the map tensors to global memory: thread row = TMEM lane, 32 columns per thread -------
+        {
+            const size_t ch = (size_t)chunk;
+            const int n0 = sub * 32;
+            const float gC = __expf(lc);
+            float v[32];
+            // A_c [m][n] = Gamma_C [m == n] - (W^T K')[m][n]
+            tmem_ld(tmem + TM_AC + lane_off + (uint32_t)n0, v);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = (n0 + q == row ? gC : 0.f) - v[q];
+            {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.mA + (ch * 128 + row) * D + n0);
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    dst[g] = make_uint4(pack_h2(v[8 * g], v[8 * g + 1]), pack_h2(v[8 * g + 2], v[8 * g + 3]),
+                                        pack_h2(v[8 * g + 4], v[8 * g + 5]), pack_h2(v[8 * g + 6], v[8 * g + 7]));
+            }
+            // B_c [c][n]
+            tmem_ld(tmem + TM_BX + lane_off + (uint32_t)n0, v);
+            {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.mB + (ch * 128 + row) * D + n0);
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    dst[g] = make_uint4(pack_h2(v[8 * g], v[8 * g + 1]), pack_h2(v[8 * g + 2], v[8 * g + 3]),
+                                        pack_h2(v[8 * g + 4], v[8 * g + 5]), pack_h2(v[8 * g + 6], v[8 * g + 7]));
+            }
+            if (quad < 2) {
+                // Q~ [i][n] = Gamma_i Q[i][n] - (G~ W)[i][n]
+                tmem_ld(tmem + TM_QT + lane_off + (uint32_t)n0, v);
+                const float gi = s_gam[row];
+                const uint8_t *qp = sm + OFF_QK + (uint32_t)(n0 >> 6) * 2 * PANEL;
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                    v[q] = gi * __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qp + sw128(row, (n0 & 63) + q))) - v[q];
+                uint4 *dq = reinterpret_cast<uint4 *>(p.mQ + (ch * 64 + row) * D + n0);
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    dq[g] = make_uint4(pack_h2(v[8 * g], v[8 * g + 1]), pack_h2(v[8 * g + 2], v[8 * g + 3]),
+                                       pack_h2(v[8 * g + 4], v[8 * g + 5]), pack_h2(v[8 * g + 6], v[8 * g + 7]));
+                // O_loc [i][c]
+                tmem_ld(tmem + TM_OX + lane_off + (uint32_t)n0, v);
+                uint4 *dO = reinterpret_cast<uint4 *>(p.mO + (ch * 64 + row) * D + n0);
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    dO[g] = make_uint4(pack_h2(v[8 * g], v[8 * g + 1]), pack_h2(v[8 * g + 2], v[8 * g + 3]),
+                                       pack_h2(v[8 * g + 4], v[8 * g + 5]), pack_h2(v[8 * g + 6], v[8 * g + 7]));
+            }
+        }
+        fence_before_sync();
+        __syncthreads();  // every read of this chunk's tiles and tensor memory is done
+    }
+
+    // drain: after an expired wait, let every copy and product still in flight land (bounded by one
+    // second each) before the CTA releases its shared and tensor memory.  One more commit arrives
+    // once every product this thread issued has completed.
+    if (tid == 0 && abort_s) {
+        const uint64_t drain_ns = 1000000000ull;
+        if (pend_qkv) (void)mbar_wait(mb_qkv, ph_qkv, drain_ns);
+        for (int b = 0; b < 2; ++b)
+            if (pend_u[b]) (void)mbar_wait(mb_u[b], ph_u[b], drain_ns);
+        const uint32_t mb_drain = smem_u32(&mbar[7]);
+        mma_commit(mb_drain);
+        (void)mbar_wait(mb_drain, 0, drain_ns);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------------------------
+// scan: one CTA per sequence, 8 warps.  Per chunk: D1 = S A_c and D2 = Q~ S^T (S fp16 in shared
+// memory, K-major [c][m]), then S <- D1 + B_c (every thread: one state row, 64 columns) and
+// o = D2 + O_loc for the chunk's tokens (rows i < 64: warps of lane quarters 0-1).  The maps of
+// the next two chunks stream through a two-stage ring of TMA copies.
+constexpr int ST = 256;
+constexpr uint32_t SC_OFF_S = 0;  // S: 2 panels [128 rows][64] fp16 (16 KB each)
+constexpr uint32_t STAGE = 4 * PANEL + 2 * PANEL + 4 * PANEL + 2 * PANEL;  // A_c | Q~ | B_c | O_loc
+constexpr uint32_t SG_A = 0, SG_Q = 4 * PANEL, SG_B = 6 * PANEL, SG_O = 10 * PANEL;
+constexpr uint32_t SC_OFF_ST = 4 * PANEL;
+constexpr uint32_t SCAN_SMEM = SC_OFF_ST + 2 * STAGE + 1024;
+static_assert(SCAN_SMEM <= 232448, "shared memory budget");
+constexpr uint32_t TM_D1 = 0, TM_D2 = 128;
+
+struct ScanParams {
+    const float *S_init;  // [BH][D][D] or null
+    float *S_final;       // [BH][D][D] or null
+    void *out;            // [BH][T][D] bf16, or fp32 with out_f32
+    int *status;
+    int T, NC, out_f32;
+    unsigned long long wait_ns;
+};
+
+__global__ void __launch_bounds__(ST, 1)
+    scan_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_qt,
+                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_o, ScanParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint32_t tmem_base_s;
+    __shared__ __align__(8) uint64_t mbar[4];  // 0, 1: ring stages; 2: products; 3: drain
+    __shared__ int abort_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half (64 columns)
+    const int row = quad * 32 + lane;
+    const int bh = blockIdx.x;
+    const uint32_t sbase = smem_u32(sm);
+    const uint64_t dbase = sdesc(sbase, 0, 0);
+    const uint32_t mb_full[2] = {smem_u32(&mbar[0]), smem_u32(&mbar[1])}, mb_mma = smem_u32(&mbar[2]);
+
+    if (tid == 0) {
+        abort_s = 0;
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&mbar[i]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tm_a);
+        prefetch_tmap(&tm_qt);
+        prefetch_tmap(&tm_b);
+        prefetch_tmap(&tm_o);
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 256);
+    // the initial state (fp16 operand copy): this thread's row, 64 columns
+    {
+        float v[64];
+#pragma unroll
+        for (int q = 0; q < 64; ++q)
+            v[q] = p.S_init ? p.S_init[((size_t)bh * D + row) * D + 64 * half + q] : 0.f;
+        uint8_t *sp = sm + SC_OFF_S + (uint32_t)half * 2 * PANEL;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            float w[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) w[q] = v[32 * g + q];
+            st_row_h(sp, row, 32 * g, w);
+        }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_base_s;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    grid_dependency_wait();  // the maps of the map kernel
+    allow_dependent_launch();
+
+    const int NC = p.NC;
+    const size_t ch0 = (size_t)bh * NC;
+    auto issue = [&](int c) {  // chunk c's maps into stage c & 1
+        const int st = c & 1;
+        const uint32_t base = sbase + SC_OFF_ST + st * STAGE;
+        const int ra = (int)((ch0 + c) * 128), rq = (int)((ch0 + c) * 64);
+        mbar_expect_tx(mb_full[st], STAGE);
+        tma_load_2d(base + SG_A, &tm_a, mb_full[st], 0, ra);
+        tma_load_2d(base + SG_A + 2 * PANEL, &tm_a, mb_full[st], 64, ra);
+        tma_load_2d(base + SG_Q, &tm_qt, mb_full[st], 0, rq);
+        tma_load_2d(base + SG_Q + PANEL, &tm_qt, mb_full[st], 64, rq);
+        tma_load_2d(base + SG_B, &tm_b, mb_full[st], 0, ra);
+        tma_load_2d(base + SG_B + 2 * PANEL, &tm_b, mb_full[st], 64, ra);
+        tma_load_2d(base + SG_O, &tm_o, mb_full[st], 0, rq);
+        tma_load_2d(base + SG_O + PANEL, &tm_o, mb_full[st], 64, rq);
+    };
+    uint32_t ph_full[2] = {0, 0}, ph_mma = 0;
+    int issued = 0, consumed = 0;  // thread 0: chunks whose maps were requested / have landed
+    if (tid == 0) {
+        for (; issued < 2 && issued < NC; ++issued) issue(issued);
+    }
+    bool finite = true;
+    for (int c = 0; c < NC; ++c) {
+        const int st = c & 1;
+        const uint32_t sb = SC_OFF_ST + st * STAGE;
+        if (tid == 0) {
+            if (mbar_wait(mb_full[st], ph_full[st], p.wait_ns)) {
+                ++consumed;
+                fence_after_sync();
+                // D1 = S A_c (A = S [c][m] K-major, B = A_c [m][n] MN-major); D2 = Q~ S^T (A = Q~ [i][n]
+                // K-major, rows 64.. unused; B = S [c][m] as N x K K-major)
+                const uint32_t id1 = idesc_f16(128, 128, 0, 1), id2 = idesc_f16(128, 128, 0, 0);
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t so = SC_OFF_S + (uint32_t)(s >> 2) * 2 * PANEL + (uint32_t)(s & 3) * 32;
+                    mma_f16(tmem + TM_D1, dsc(dbase, so, 16, 1024), dsc(dbase, sb + SG_A + s * 2048, 2 * PANEL, 1024), id1,
+                            s > 0);
+                }
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t so = SC_OFF_S + (uint32_t)(s >> 2) * 2 * PANEL + (uint32_t)(s & 3) * 32;
+                    const uint32_t qo = sb + SG_Q + (uint32_t)(s >> 2) * PANEL + (uint32_t)(s & 3) * 32;
+                    mma_f16(tmem + TM_D2, dsc(dbase, qo, 16, 1024), dsc(dbase, so, 16, 1024), id2, s > 0);
+                }
+                mma_commit(mb_mma);
+            } else {
+                abort_s = 1;
+                set_status(p.status, kDevTimeout);
+            }
+        }
+        __syncthreads();
+        if (abort_s) break;
+        ph_full[st] ^= 1u;
+        if (!mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
+            abort_s = 1;
+            set_status(p.status, kDevTimeout);
+        }
+        ph_mma ^= 1u;
+        fence_after_sync();
+        // S <- S A_c + B_c (this thread: row `row`, columns 64 half .. 64 half + 63)
+        {
+            const uint8_t *bp = sm + sb + SG_B + (uint32_t)half * 2 * PANEL;
+            uint8_t *sp = sm + SC_OFF_S + (uint32_t)half * 2 * PANEL;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                float v[32];
+                tmem_ld(tmem + TM_D1 + lane_off + (uint32_t)(64 * half + 32 * g), v);
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                    v[q] += __half2float(*reinterpret_cast<const __half *>(bp + sw128(row, 32 * g + q)));
+                if (c + 1 == NC && p.S_final) {
+                    float4 *sf = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + row) * D + 64 * half + 32 * g);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) sf[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+                st_row_h(sp, row, 32 * g, v);
+            }
+        }
+        // o = Q~ S^T + O_loc for tokens i = row < n (lane quarters 0-1)
+        if (quad < 2) {
+            const int n = min(C, p.T - c * C);
+            const uint8_t *op = sm + sb + SG_O + (uint32_t)half * PANEL;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                float v[32];
+                tmem_ld(tmem + TM_D2 + lane_off + (uint32_t)(64 * half + 32 * g), v);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    v[q] += __half2float(*reinterpret_cast<const __half *>(op + sw128(row, 32 * g + q)));
+                    finite = finite && isfinite(v[q]);
+                }
+                if (row < n) {
+                    const size_t o = ((size_t)bh * p.T + (size_t)c * C + row) * D + 64 * half + 32 * g;
+                    if (p.out_f32) {
+                        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + o);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+                                w[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                            }
+                            dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            }
+        }
+        fence_async_smem();  // S is the next chunk's MMA operand
+        fence_before_sync();
+        __syncthreads();     // stage st and both accumulators are free
+        if (tid == 0 && issued < NC) issue(issued++);
+    }
+    if (!finite) set_status(p.status, kDevBounds);  // outside the fp16 operand range
+    // drain: copies and products still in flight after an expired wait land before the CTA exits
+    if (tid == 0 && abort_s) {
+        for (int c = consumed; c < issued; ++c)
+            (void)mbar_wait(mb_full[c & 1], (uint32_t)((c >> 1) & 1), 1000000000ull);
+        const uint32_t mb_drain = smem_u32(&mbar[3]);
+        mma_commit(mb_drain);
+        (void)mbar_wait(mb_drain, 0, 1000000000ull);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+}  // namespace mp
+
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    }
+    return fn;
+}
+
+bool encode_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, int rank, const cuuint64_t *dims,
+                const cuuint64_t *strides_bytes, const cuuint32_t *box, CUtensorMapSwizzle sw)
+{
+    auto fn = map_encoder();
+    if (!fn) return false;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, dt, (cuuint32_t)rank, const_cast<void *>(base), dims, strides_bytes, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool map_supported(const Shape &s, prism_dtype io)
+{
+    return io == PRISM_BF16 && s.dk == mp::D && s.dv == mp::D && s.L >= 1 && s.L <= 1 + mp::RM;
+}
+
+size_t map_workspace_bytes(const Shape &s)
+{
+    const size_t chunks = (size_t)s.BH * s.NC;
+    return chunks * (2 * 128 + 2 * 64) * mp::D * 2 + 4 * 256;
+}
+
+void map_carve(const Shape &s, void *base, MapWorkspace *w)
+{
+    const size_t chunks = (size_t)s.BH * s.NC;
+    uintptr_t p = ((uintptr_t)base + 255) & ~(uintptr_t)255;
+    w->A = (__half *)p;
+    p += chunks * 128 * mp::D * 2;
+    w->Q = (__half *)p;
+    p += chunks * 64 * mp::D * 2;
+    w->B = (__half *)p;
+    p += chunks * 128 * mp::D * 2;
+    w->O = (__half *)p;
+}
+
+cudaError_t map_prepare()
+{
+    cudaError_t e = cudaFuncSetAttribute(mp::map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mp::MAP_SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mp::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mp::SCAN_SMEM);
+}
+
+cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const MapWorkspace &w, int sm_count,
+                        int *d_status, long long wait_ns, KernelTimer &tm)
+{
+    using namespace mp;
+    const cuuint64_t BH = s.BH, T = s.T;
+    CUtensorMap mq, mk, mv, mu, ma, mqt, mb, mo;
+    const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)D, T, BH};
+        cuuint64_t str[2] = {(cuuint64_t)D * 2, T * D * 2};
+        cuuint32_t box[3] = {64, 64, 1};
+        if (!encode_map(&mq, BF, a.q, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!encode_map(&mk, BF, a.k, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        cuuint32_t vbox[3] = {(cuuint32_t)D, 72, 1};
+        if (!encode_map(&mv, BF, a.v, 3, dims, str, vbox, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+    }
+    if (s.R > 0) {
+        cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)s.R, T, BH};
+        cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)s.R * D * 2, T * s.R * D * 2};
+        cuuint32_t box[4] = {64, 1, 64, 1};
+        if (!encode_map(&mu, BF, a.u, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    } else {
+        mu = mk;  // never read with L = 1
+    }
+    const cuuint64_t chunks = (cuuint64_t)s.BH * s.NC;
+    {
+        cuuint64_t str[1] = {(cuuint64_t)D * 2};
+        cuuint64_t d128[2] = {(cuuint64_t)D, chunks * 128}, d64[2] = {(cuuint64_t)D, chunks * 64};
+        cuuint32_t b128[2] = {64, 128}, b64[2] = {64, 64};
+        if (!encode_map(&ma, F16, w.A, 2, d128, str, b128, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!encode_map(&mqt, F16, w.Q, 2, d64, str, b64, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!encode_map(&mb, F16, w.B, 2, d128, str, b128, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!encode_map(&mo, F16, w.O, 2, d64, str, b64, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    }
+    const unsigned long long wns = wait_ns > 0 ? (unsigned long long)wait_ns : 100000000ull;
+    MapParams mp_;
+    mp_.beta = a.beta;
+    mp_.alpha = a.alpha;
+    mp_.gamma = a.gamma;
+    mp_.eta = a.eta;
+    mp_.conv_w = (const __nv_bfloat16 *)a.conv_w;
+    mp_.v_hist = (const __nv_bfloat16 *)a.v_hist;
+    mp_.mA = w.A;
+    mp_.mQ = w.Q;
+    mp_.mB = w.B;
+    mp_.mO = w.O;
+    mp_.status = d_status;
+    mp_.H = s.H;
+    mp_.T = s.T;
+    mp_.R = s.R;
+    mp_.NC = s.NC;
+    mp_.nchunks = (int)chunks;
+    mp_.wait_ns = wns;
+    ScanParams sp;
+    sp.S_init = a.S_init;
+    sp.S_final = a.S_final;
+    sp.out = a.out;
+    sp.status = d_status;
+    sp.T = s.T;
+    sp.NC = s.NC;
+    sp.out_f32 = out_f32 ? 1 : 0;
+    sp.wait_ns = wns;
+
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = tm.stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    tm.begin("map_chunks");
+    cfg.gridDim = dim3((unsigned)((int)chunks < sm_count ? (int)chunks : sm_count));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = MAP_SMEM;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, map_kernel, mq, mk, mv, mu, mp_);
+    tm.end();
+    if (e != cudaSuccess) return e;
+    tm.begin("map_scan");
+    cfg.gridDim = dim3((unsigned)s.BH);
+    cfg.blockDim = dim3(ST);
+    cfg.dynamicSmemBytes = SCAN_SMEM;
+    e = cudaLaunchKernelEx(&cfg, scan_kernel, ma, mqt, mb, mo, sp);
+    tm.end();
+    if (e != cudaSuccess) return e;
+    if (a.v_hist_out) {  // a plain launch: it runs after the kernels above have read v_hist
+        e = launch_history(s, PRISM_BF16, a.v_hist, a.v, a.v_hist_out, tm);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace prism

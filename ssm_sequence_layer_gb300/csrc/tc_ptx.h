@@ -231,6 +231,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t mbar, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::
+            "r"(dst),
+        "l"((uint64_t)map), "r"(mbar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 // Untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a multiple of 16),
 // completing on an mbarrier's transaction count.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar)
