@@ -15,9 +15,11 @@
  *   o_t     = S_t q_t,     S_0 = 0,   S_t in R^{dv x dk}
  *
  * With L = 1 this is the gated delta rule (GDN).  The sequence is evaluated in
- * 64-token chunks (a WY/UT form of the products of the rank-1 transitions)
- * with segment-parallel state passing; the result equals the sequential
- * definition up to floating-point rounding.
+ * 64-token chunks (a WY/UT form of the products of the rank-1 transitions);
+ * the state is passed between chunks either segment-parallel (tensor-core
+ * path, dk = dv = 64, L <= 4) or as per-chunk affine maps S -> S A_c + B_c
+ * applied in order (tensor-core path, dk = dv = 128, L <= 16); the result
+ * equals the sequential definition up to floating-point rounding.
  *
  * Tensor layouts (all row-major and contiguous, caller-owned device memory):
  *   q, k    [B,H,T,dk]   io dtype        v, out [B,H,T,dv]   io dtype
@@ -74,8 +76,12 @@ typedef enum prism_dtype {
 } prism_dtype;
 
 typedef enum prism_option {
-    PRISM_OPT_SEGMENTS = 0,  /* segments per sequence for the state passing; 0 = automatic */
-    PRISM_OPT_PATH = 1,      /* 0 = automatic, 1 = portable fp32 kernels, 2 = tensor-core path */
+    PRISM_OPT_SEGMENTS = 0,  /* segments per sequence for the segment-parallel state passing
+                                (dk = dv = 64 tensor-core kernels); 0 = automatic */
+    PRISM_OPT_PATH = 1,      /* 0 = automatic, 1 = portable fp32 kernels, 2 = tensor-core path (bf16 io
+                                with dk = dv = 64 and L <= 4, or dk = dv = 128 and L <= 16; other
+                                shapes return PRISM_ERR_UNSUPPORTED); automatic takes the tensor-core
+                                path wherever it applies */
     PRISM_OPT_WAIT_NS = 2,   /* bound of any device-side wait in ns; 0 = default (100 ms) */
     PRISM_OPT_TIMING = 3,    /* 1 = record CUDA events around each kernel (see prism_plan_kernel_times) */
     PRISM_OPT_OUT_DTYPE = 4  /* prism_dtype of `out`; default = the plan's io dtype.  float32 output
@@ -188,8 +194,9 @@ PRISM_API prism_status prism_decode_step(prism_plan_t plan, const void *q, const
  * Only the token-local injection factors differ from prism_forward.  Arguments as
  * prism_forward_state, with p_gain [B,H,T,R,dv] in the io dtype (16-byte aligned; slot l-1
  * holds level l) in place of eta, which this variant does not have.  With L = 1 it equals
- * prism_forward_state.  The chain has no closed form, so it runs on the portable fp32
- * kernels whatever the shape (PRISM_OPT_PATH = 2 returns PRISM_ERR_UNSUPPORTED).
+ * prism_forward_state.  It runs on the same path as prism_forward for the plan's shape (the
+ * tensor-core kernels for bf16 io with dk = dv = 64 and L <= 4 or dk = dv = 128 and L <= 16,
+ * else the portable fp32 kernels): only their prep, which steps the chain level by level, differs.
  */
 PRISM_API prism_status prism_forward_nonlinear(prism_plan_t plan, const void *q, const void *k, const void *v,
                                      const float *beta, const float *alpha, const void *u,

@@ -186,12 +186,7 @@ prism_status run_forward(prism_plan_s *p, const prism::ForwardArgs &a, struct CU
 {
     prism_status st = check_plan_device(p);
     if (st != PRISM_OK) return st;
-    int path = resolve_path(p);
-    if (a.p_gain) {  // the non-linear residual chain runs on the portable kernels only
-        if (p->opt_path == 2)
-            return fail(PRISM_ERR_UNSUPPORTED, "the non-linear residual variant has no tensor-core path");
-        path = 1;
-    }
+    const int path = resolve_path(p);
     if (path == 2 && !tensor_core_shape(p))
         return fail(PRISM_ERR_UNSUPPORTED,
                     "the tensor-core path takes bf16 io with dk = dv = 64 and L <= 4, or dk = dv = 128 and L <= 16");

@@ -24,7 +24,7 @@ enum DeviceStatus : int {
 // carry a sequence across calls and may be null: v_hist [BH][3][dv] (v_{-3}, v_{-2}, v_{-1}, io
 // dtype), S_init / S_final [BH][dv][dk] fp32, v_hist_out [BH][3][dv] (the last three tokens of
 // [v_hist; v]).  p_gain [BH][T][R][dv] (io dtype), when set, selects the non-linear residual
-// variant (portable path only; eta is then not read).
+// variant (eta is then not read).
 struct ForwardArgs {
     const void *q, *k, *v, *u, *conv_w;
     const float *beta, *alpha, *gamma, *eta;

@@ -15,7 +15,9 @@
 //
 // Chunk algebra (local index i, j; lambda_i = sum_{m<=i} ln alpha_m; lc = lambda_{C-1};
 // D_ij = e^{lambda_i - lambda_j} (j <= i); colf_j = e^{lc - lambda_j}; Gamma_i = e^{lambda_i}),
-// with the level key tiles U_{-1} = K, U_l (l < R) and x_{t,l} = gamma_{t,l} g_t (.) r_{t,l}:
+// with the level key tiles U_{-1} = K, U_l (l < R) and x_{t,l} = gamma_{t,l} g_t (.) r_{t,l} (or, for
+// the non-linear residual chain of the notes' section 2.3, x_{t,l} = gamma_{t,l} GELU(p_{t,l} r_{t,l})
+// with r_{t,l+1} = r_{t,l} - GELU(p_{t,l} r_{t,l})):
 //   Gram of level l:  [Q; K] U_l^T  -> rows i < 64: q_i.u_{j,l}, rows 64 + i: k_i.u_{j,l}
 //   G~ = D o (Q K^T) (j <= i),  A = diag(beta) D o (K K^T) (j < i)  ->  T = (I + A)^{-1}
 //   PQ_l = D o (Q U_l^T) (j <= i),  PK_l = D o (K U_l^T) (j < i)
@@ -36,6 +38,25 @@
 #include "tc_ptx.h"
 #include "tc_util.h"
 
+// Developer tracing: with -DPRISM_PHASE_TIMERS thread 0 of every CTA accumulates clock64() cycles
+// per phase of the chunk loop (slots 0..7: map kernel, 8..15: scan kernel) into
+// prism_map_phase_cycles.
+#ifdef PRISM_PHASE_TIMERS
+__device__ unsigned long long prism_map_phase_cycles[16];
+#define MAP_MARK(k)                                            \
+    do {                                                       \
+        if (threadIdx.x == 0) {                                \
+            const long long now_ = clock64();                  \
+            ph_acc[k] += (unsigned long long)(now_ - ph_last); \
+            ph_last = now_;                                    \
+        }                                                      \
+    } while (0)
+#else
+#define MAP_MARK(k) \
+    do {            \
+    } while (0)
+#endif
+
 namespace prism {
 namespace mp {
 
@@ -54,27 +75,35 @@ constexpr int NT = 512;      // threads of the map kernel: 16 warps, 4 per TMEM 
 constexpr uint32_t PANEL = 8192;  // [64 rows][64 cols] 16-bit SW128
 
 // ---- map kernel: shared memory (bytes from a 1024-aligned base) -------------------------------
-constexpr uint32_t OFF_QK = 0;                     // [Q_p0 | K_p0 | Q_p1 | K_p1] (bf16; K later K' fp16)
-constexpr uint32_t OFF_V = 32768;                  // V rows t0-8 .. t0+63, [72][128] bf16, unswizzled
+// Two regions alternate between chunks: one holds the chunk's [Q_p0 | K_p0 | Q_p1 | K_p1] (bf16; K
+// later K' fp16), the other its A and T (fp32) for the solve; once the solve is done the latter
+// receives the next chunk's Q and K, so their loads run under the rest of the chunk.
+constexpr uint32_t REGION = 34 * 1024;
+constexpr uint32_t OFF_R0 = 0, OFF_R1 = REGION;
+constexpr uint32_t AT_T32 = 64 * tcu::LDA * 4;       // T32 after A within the solve region
+constexpr uint32_t OFF_V = 2 * REGION;               // V rows t0-8 .. t0+63, [72][128] bf16, unswizzled
 constexpr uint32_t VBYTES = 72 * D * 2;
-constexpr uint32_t OFF_G = OFF_V + VBYTES;          // G~ [64][64] fp16 K-major
-constexpr uint32_t OFF_TF = OFF_G + PANEL;          // T  [64][64] fp16 K-major
-constexpr uint32_t OFF_A = OFF_TF + PANEL;          // A   fp32 [64][LDA]
-constexpr uint32_t OFF_T32 = OFF_A + 64 * tcu::LDA * 4;  // T fp32 [64][LDA]
-constexpr uint32_t OFF_LV = OFF_T32 + 64 * tcu::LDA * 4; // two level buffers
-constexpr uint32_t LVB = 3 * 2 * PANEL;             // per level buffer: U (2 panels) | [PQ; PK] | X (2 panels)
+constexpr uint32_t OFF_G = OFF_V + VBYTES;           // G~ [64][64] fp16 K-major
+constexpr uint32_t OFF_TF = OFF_G + PANEL;           // T  [64][64] fp16 K-major
+constexpr uint32_t OFF_LV = OFF_TF + PANEL;          // two level buffers
+constexpr uint32_t LVB = 3 * 2 * PANEL;              // per level buffer: U (2 panels) | [PQ; PK] | X (2 panels)
 constexpr uint32_t LV_U = 0, LV_PQK = 2 * PANEL, LV_X = 4 * PANEL;
-// after the level loop the level buffers hold RHS, diag(beta Gamma) K, U' and W ([64][128] fp16)
+// after the level loop the level buffers hold RHS, diag(beta Gamma) K, U' and W ([64][128] fp16),
+// and at the end of the chunk the map tensors on their way out (A_c, B_c [128][128], Q~, O_loc
+// [64][128], fp16, SW128 panels of 64 columns)
 constexpr uint32_t OFF_RHS = OFF_LV, OFF_BGK = OFF_LV + 2 * PANEL, OFF_UP = OFF_LV + 4 * PANEL,
                    OFF_W = OFF_LV + 6 * PANEL;
-constexpr uint32_t OFF_SC = OFF_LV + 2 * LVB;       // per-token scalars
+constexpr uint32_t OUT_A = OFF_LV, OUT_B = OFF_LV + 4 * PANEL, OUT_Q = OFF_LV + 8 * PANEL, OUT_O = OFF_LV + 10 * PANEL;
+constexpr uint32_t OFF_SC = OFF_LV + 2 * LVB;        // per-token scalars
 constexpr uint32_t SC_FLOATS = 6 * 64 + 2 * 64 * RMS + tcu::SOLVE_SCRATCH;
 constexpr uint32_t MAP_SMEM = OFF_SC + SC_FLOATS * 4 + 1024;  // + alignment slack
 
+static_assert(2 * AT_T32 <= REGION && 4 * PANEL <= REGION, "the alternating regions hold Q/K or A/T");
 static_assert(OFF_V % 1024 == 0 && OFF_G % 1024 == 0 && OFF_TF % 1024 == 0 && OFF_LV % 1024 == 0 &&
-                  LVB % 1024 == 0 && OFF_SC % 16 == 0,
+                  LVB % 1024 == 0 && OFF_SC % 16 == 0 && REGION % 1024 == 0,
               "alignment of the tiles");
-static_assert(OFF_W + 2 * PANEL <= OFF_LV + 2 * LVB, "post-solve tiles fit the level buffers");
+static_assert(OFF_W + 2 * PANEL <= OFF_LV + 2 * LVB && OUT_O + 2 * PANEL <= OFF_LV + 2 * LVB,
+              "post-solve and output tiles fit the level buffers");
 static_assert(MAP_SMEM <= 232448, "shared memory budget");
 
 // tensor memory columns (512 allocated)
@@ -90,6 +119,7 @@ struct MapParams {
     const float *beta, *alpha, *gamma, *eta;
     const __nv_bfloat16 *conv_w;
     const __nv_bfloat16 *v_hist;  // [BH][3][D] v_{-3..-1}, or null
+    const __nv_bfloat16 *p_gain;  // [BH][T][R][D] gains of the non-linear residual chain, or null (linear)
     __half *mA, *mQ, *mB, *mO;    // [BH*NC][128][128], [BH*NC][64][128], [BH*NC][128][128], [BH*NC][64][128]
     int *status;
     int H, T, R, NC, nchunks;
@@ -99,7 +129,9 @@ struct MapParams {
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(NT, 1)
     map_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_u, MapParams p)
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_u,
+               const __grid_constant__ CUtensorMap tm_ma, const __grid_constant__ CUtensorMap tm_mq,
+               const __grid_constant__ CUtensorMap tm_mb, const __grid_constant__ CUtensorMap tm_mo, MapParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -132,6 +164,10 @@ __global__ void __launch_bounds__(NT, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_u);
+        prefetch_tmap(&tm_ma);
+        prefetch_tmap(&tm_mq);
+        prefetch_tmap(&tm_mb);
+        prefetch_tmap(&tm_mo);
     }
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 512);
     fence_before_sync();
@@ -165,24 +201,40 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_4d(dst + PANEL, &tm_u, mb_u[b], 64, l, t0, chunk_bh);
         pend_u[b] = true;
     };
+    // Q, K (into the region `qk`) and V of the chunk with flat index `ch`
+    auto issue_qkv = [&](int ch, uint32_t qk) {
+        const int cbh = ch / p.NC, ct0 = (ch % p.NC) * C;
+        mbar_expect_tx(mb_qkv, 4 * PANEL + VBYTES);
+        tma_load_3d(sbase + qk, &tm_q, mb_qkv, 0, ct0, cbh);
+        tma_load_3d(sbase + qk + PANEL, &tm_k, mb_qkv, 0, ct0, cbh);
+        tma_load_3d(sbase + qk + 2 * PANEL, &tm_q, mb_qkv, 64, ct0, cbh);
+        tma_load_3d(sbase + qk + 3 * PANEL, &tm_k, mb_qkv, 64, ct0, cbh);
+        tma_load_3d(sbase + OFF_V, &tm_v, mb_qkv, 0, ct0 - 8, cbh);
+        pend_qkv = true;
+    };
 
     // this thread's prep elements: channels 2 cp, 2 cp + 1 of tokens tg + 8 k
     const int cp = tid & 63, tg = tid >> 6;
+#ifdef PRISM_PHASE_TIMERS
+    unsigned long long ph_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    long long ph_last = clock64();
+#endif
+    if (tid == 0 && (int)blockIdx.x < p.nchunks) issue_qkv(blockIdx.x, OFF_R0);
 
-    for (int chunk = blockIdx.x; chunk < p.nchunks && abort_s == 0; chunk += gridDim.x) {
+    for (int it = 0;; ++it) {
+        const int chunk = (int)blockIdx.x + it * (int)gridDim.x;
+        if (chunk >= p.nchunks || abort_s) break;
         const int bh = chunk / p.NC, c = chunk % p.NC, h = bh % p.H;
         const int t0 = c * C, n = min(C, p.T - t0);
         const size_t tok0 = (size_t)bh * p.T + t0;
+        const uint32_t QK = (it & 1) ? OFF_R1 : OFF_R0;  // this chunk's Q/K
+        const uint32_t AT = (it & 1) ? OFF_R0 : OFF_R1;  // this chunk's A/T, then the next chunk's Q/K
+        float *const sA = reinterpret_cast<float *>(sm + AT);
+        float *const sT32 = reinterpret_cast<float *>(sm + AT + AT_T32);
 
-        // ---- loads of this chunk (the previous chunk's readers are done: see the loop's end) ----
+        // ---- U_0, U_1 of this chunk (the level buffers held the previous chunk's outgoing maps) ----
         if (tid == 0) {
-            mbar_expect_tx(mb_qkv, 4 * PANEL + VBYTES);
-            tma_load_3d(sbase + OFF_QK, &tm_q, mb_qkv, 0, t0, bh);
-            tma_load_3d(sbase + OFF_QK + PANEL, &tm_k, mb_qkv, 0, t0, bh);
-            tma_load_3d(sbase + OFF_QK + 2 * PANEL, &tm_q, mb_qkv, 64, t0, bh);
-            tma_load_3d(sbase + OFF_QK + 3 * PANEL, &tm_k, mb_qkv, 64, t0, bh);
-            tma_load_3d(sbase + OFF_V, &tm_v, mb_qkv, 0, t0 - 8, bh);
-            pend_qkv = true;
+            bulk_wait_read();
             if (R > 0) issue_u(bh, t0, 0);
             if (R > 1) issue_u(bh, t0, 1);
         }
@@ -216,7 +268,7 @@ __global__ void __launch_bounds__(NT, 1)
                 const int i = e / R, l = e % R;
                 const bool valid = i < n;
                 s_gm[i * RMS + l] = valid ? p.gamma[(tok0 + i) * R + l] : 0.f;
-                s_et[i * RMS + l] = valid ? p.eta[(tok0 + i) * R + l] : 0.f;
+                s_et[i * RMS + l] = (valid && p.eta) ? p.eta[(tok0 + i) * R + l] : 0.f;
             }
         }
         // Q, K and V have landed (every thread waits; the history, if any, then replaces the halo)
@@ -237,6 +289,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         const float lc = s_lam[63];
         const bool factored = -lc <= 80.f;  // both decay factors in fp32 range
+        MAP_MARK(0);
 
         // ---- level -1 (the key level): Gram [Q; K] K^T -------------------------------------------
         if (tid == 0) {
@@ -245,8 +298,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t ko = (uint32_t)(s >> 2) * 2 * PANEL + (uint32_t)(s & 3) * 32;
-                mma_f16(tmem + TM_GRAM, dsc(dbase, OFF_QK + ko, 16, 1024), dsc(dbase, OFF_QK + PANEL + ko, 16, 1024), id,
-                        s > 0);
+                mma_f16(tmem + TM_GRAM, dsc(dbase, QK + ko, 16, 1024), dsc(dbase, QK + PANEL + ko, 16, 1024), id, s > 0);
             }
             mma_commit(mb_gram);
         }
@@ -320,7 +372,7 @@ __global__ void __launch_bounds__(NT, 1)
             if (query) {
                 st_row_h(sm + OFF_G, i, sub * 16, v);
             } else {  // A_ij = beta_i D_ij k_i.k_j
-                float4 *A4 = reinterpret_cast<float4 *>(sm + OFF_A + (i * tcu::LDA + sub * 16) * 4);
+                float4 *A4 = reinterpret_cast<float4 *>(sA + i * tcu::LDA + sub * 16);
                 const float b = s_beta[i];
 #pragma unroll
                 for (int g = 0; g < 4; ++g) A4[g] = make_float4(b * v[4 * g], b * v[4 * g + 1], b * v[4 * g + 2], b * v[4 * g + 3]);
@@ -328,22 +380,25 @@ __global__ void __launch_bounds__(NT, 1)
         }
         fence_before_sync();
         __syncthreads();
+        MAP_MARK(1);
 
         // ---- levels 0 .. R-1 -------------------------------------------------------------------------
         for (int l = 0; l < R; ++l) {
             const int b = l & 1;
             const uint32_t lvb = OFF_LV + b * LVB;
-            if (tid == 0) {
-                // the other buffer is free once level l - 1's products have completed: prefetch U_{l+1}
-                if (l >= 1 && l + 1 < R) {
-                    if (mbar_wait(mb_lvl[b ^ 1], ph_lvl[b ^ 1], p.wait_ns)) {
-                        ph_lvl[b ^ 1] ^= 1u;
-                        pend_lvl[b ^ 1] = false;
-                        issue_u(bh, t0, l + 1);
-                    } else {
-                        expired();
-                    }
+            // the non-linear chain's gains of this level (read early: their latency hides behind the Gram)
+            uint32_t pz[8];
+            if (p.p_gain) {
+                const uint32_t *pg = reinterpret_cast<const uint32_t *>(p.p_gain) + ((tok0 * R + l) * D) / 2 + cp;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int i = tg + 8 * k;
+                    pz[k] = i < n ? pg[(size_t)i * R * (D / 2)] : 0u;
                 }
+            }
+            if (tid == 0) {
+                // the Gram first (it queues behind level l - 1's products), then the prefetch of U_{l+1}
+                // into the other buffer once level l - 1's products have completed
                 if (mbar_wait(mb_u[b], ph_u[b], p.wait_ns)) {
                     ph_u[b] ^= 1u;
                     pend_u[b] = false;
@@ -353,10 +408,19 @@ __global__ void __launch_bounds__(NT, 1)
                     for (int s = 0; s < 8; ++s) {
                         const uint32_t ko = (uint32_t)(s >> 2) * 2 * PANEL + (uint32_t)(s & 3) * 32;
                         const uint32_t uo = lvb + LV_U + (uint32_t)(s >> 2) * PANEL + (uint32_t)(s & 3) * 32;
-                        mma_f16(tmem + TM_GRAM + 64 * b, dsc(dbase, OFF_QK + ko, 16, 1024), dsc(dbase, uo, 16, 1024), id,
+                        mma_f16(tmem + TM_GRAM + 64 * b, dsc(dbase, QK + ko, 16, 1024), dsc(dbase, uo, 16, 1024), id,
                                 s > 0);
                     }
                     mma_commit(mb_gram);
+                    if (l >= 1 && l + 1 < R) {
+                        if (mbar_wait(mb_lvl[b ^ 1], ph_lvl[b ^ 1], p.wait_ns)) {
+                            ph_lvl[b ^ 1] ^= 1u;
+                            pend_lvl[b ^ 1] = false;
+                            issue_u(bh, t0, l + 1);
+                        } else {
+                            expired();
+                        }
+                    }
                 } else {
                     expired();
                 }
@@ -386,18 +450,32 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 reinterpret_cast<uint4 *>(sm + lvb + LV_U)[e] = w;
             }
-            // X_l = gamma_l g r, then r <- r (1 - eta_l g)
+            // X_l = gamma_l g r, then r <- r (1 - eta_l g); or, with gains p, the non-linear chain
+            // delta = GELU(p r), X_l = gamma_l delta, r <- r - delta
             {
                 uint8_t *xp = sm + lvb + LV_X + (uint32_t)((2 * cp) >> 6) * PANEL;
                 const int col = (2 * cp) & 63;
+                if (p.p_gain) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int i = tg + 8 * k;
-                    const float gm = s_gm[i * RMS + l], et = s_et[i * RMS + l];
-                    *reinterpret_cast<uint32_t *>(xp + sw128(i, col)) =
-                        pack_h2(gm * g_[k][0] * r_[k][0], gm * g_[k][1] * r_[k][1]);
-                    r_[k][0] *= 1.f - et * g_[k][0];
-                    r_[k][1] *= 1.f - et * g_[k][1];
+                    for (int k = 0; k < 8; ++k) {
+                        const int i = tg + 8 * k;
+                        const float gm = s_gm[i * RMS + l];
+                        const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pz[k]));
+                        const float d0 = tcu::gelu_value(pf.x * r_[k][0]), d1 = tcu::gelu_value(pf.y * r_[k][1]);
+                        *reinterpret_cast<uint32_t *>(xp + sw128(i, col)) = pack_h2(gm * d0, gm * d1);
+                        r_[k][0] -= d0;
+                        r_[k][1] -= d1;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int i = tg + 8 * k;
+                        const float gm = s_gm[i * RMS + l], et = s_et[i * RMS + l];
+                        *reinterpret_cast<uint32_t *>(xp + sw128(i, col)) =
+                            pack_h2(gm * g_[k][0] * r_[k][0], gm * g_[k][1] * r_[k][1]);
+                        r_[k][0] *= 1.f - et * g_[k][0];
+                        r_[k][1] *= 1.f - et * g_[k][1];
+                    }
                 }
             }
             fence_async_smem();
@@ -422,6 +500,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         if (abort_s) break;
+        MAP_MARK(2);
 
         // ---- after the levels: the products of the last ones complete, then the solve (warps 8-15)
         // beside the RHS, diag(beta Gamma) K and K' (warps 0-7) ---------------------------------------
@@ -441,8 +520,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (abort_s) break;
         fence_after_sync();
         if (warp >= 8) {
-            tcu::ut_solve(reinterpret_cast<const float *>(sm + OFF_A), reinterpret_cast<float *>(sm + OFF_T32), s_xtmp,
-                          sm + OFF_TF, tid - 256, 1);
+            tcu::ut_solve(sA, sT32, s_xtmp, sm + OFF_TF, tid - 256, 1);
         } else if (quad >= 2) {  // RHS = diag(beta) (V - MX): TMEM rows 64 + i, 64 columns per thread
             const int i = row - 64, c0 = (warp >> 2) * 64;
             const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_V) + (size_t)(i + 8) * D;
@@ -465,7 +543,7 @@ __global__ void __launch_bounds__(NT, 1)
             const int t = (warp >> 2) * 64 + (warp & 1) * 32 + lane;  // 0..127
             for (int e = t; e < 1024; e += 128) {
                 const int pnl = e >> 9, j = (e & 511) >> 3;
-                uint8_t *kp = sm + OFF_QK + PANEL + (uint32_t)pnl * 2 * PANEL;
+                uint8_t *kp = sm + QK + PANEL + (uint32_t)pnl * 2 * PANEL;
                 uint4 w = reinterpret_cast<const uint4 *>(kp)[e & 511];
                 uint4 wb = w;
                 const float bg = s_bg[j], cf = s_colf[j];
@@ -483,8 +561,9 @@ __global__ void __launch_bounds__(NT, 1)
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
+        MAP_MARK(3);
 
-        // ---- U' = T RHS, W = T diag(beta Gamma) K ------------------------------------------------------
+        // ---- U' = T RHS, W = T diag(beta Gamma) K; the next chunk's Q, K, V load under the rest ------
         if (tid == 0) {
             fence_after_sync();
             const uint32_t id = idesc_f16(128, 128, 0, 1);  // A = T [i][j] K-major (rows 64.. unused)
@@ -496,6 +575,9 @@ __global__ void __launch_bounds__(NT, 1)
                         s > 0);
             }
             mma_commit(mb_post);
+            // the solve region (A, T) is free and V has been read: prefetch the next chunk's inputs
+            const int next = chunk + (int)gridDim.x;
+            if (next < p.nchunks) issue_qkv(next, AT);
         }
         wait_all(mb_post, ph_post);
         fence_after_sync();
@@ -515,12 +597,13 @@ __global__ void __launch_bounds__(NT, 1)
         fence_before_sync();
         __syncthreads();
         if (abort_s) break;
+        MAP_MARK(4);
 
         // ---- B_c += U'^T K', O_loc += G~ U', W^T K', G~ W ----------------------------------------------
         if (tid == 0) {
             fence_after_sync();
             const uint32_t idmm = idesc_f16(128, 128, 1, 1), idkm = idesc_f16(128, 128, 0, 1);
-            const uint32_t kq = OFF_QK + PANEL;  // K' panels at 16 KB stride
+            const uint32_t kq = QK + PANEL;  // K' panels at 16 KB stride
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint32_t ks = s * 2048;
@@ -535,70 +618,82 @@ __global__ void __launch_bounds__(NT, 1)
         }
         wait_all(mb_post, ph_post);
         fence_after_sync();
+        MAP_MARK(5);
 
-        // ---- the map tensors to global memory: thread row = TMEM lane, 32 columns per thread -------
+        // ---- the map tensors: thread row = TMEM lane, 32 columns per thread, into SW128 panels of
+        // the level buffers (free now), then out by TMA stores --------------------------------------
         {
-            const size_t ch = (size_t)chunk;
             const int n0 = sub * 32;
             const float gC = __expf(lc);
+            const uint32_t pnl = (uint32_t)(n0 >> 6) * 2 * PANEL;  // [128][64] panels of A_c, B_c
             float v[32];
             // A_c [m][n] = Gamma_C [m == n] - (W^T K')[m][n]
             tmem_ld(tmem + TM_AC + lane_off + (uint32_t)n0, v);
 #pragma unroll
             for (int q = 0; q < 32; ++q) v[q] = (n0 + q == row ? gC : 0.f) - v[q];
-            {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.mA + (ch * 128 + row) * D + n0);
-#pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    dst[g] = make_uint4(pack_h2(v[8 * g], v[8 * g + 1]), pack_h2(v[8 * g + 2], v[8 * g + 3]),
-                                        pack_h2(v[8 * g + 4], v[8 * g + 5]), pack_h2(v[8 * g + 6], v[8 * g + 7]));
-            }
+            st_row_h(sm + OUT_A + pnl, row, n0 & 63, v);
             // B_c [c][n]
             tmem_ld(tmem + TM_BX + lane_off + (uint32_t)n0, v);
-            {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.mB + (ch * 128 + row) * D + n0);
-#pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    dst[g] = make_uint4(pack_h2(v[8 * g], v[8 * g + 1]), pack_h2(v[8 * g + 2], v[8 * g + 3]),
-                                        pack_h2(v[8 * g + 4], v[8 * g + 5]), pack_h2(v[8 * g + 6], v[8 * g + 7]));
-            }
+            st_row_h(sm + OUT_B + pnl, row, n0 & 63, v);
             if (quad < 2) {
+                const uint32_t pq = (uint32_t)(n0 >> 6) * PANEL;  // [64][64] panels of Q~, O_loc
                 // Q~ [i][n] = Gamma_i Q[i][n] - (G~ W)[i][n]
                 tmem_ld(tmem + TM_QT + lane_off + (uint32_t)n0, v);
                 const float gi = s_gam[row];
-                const uint8_t *qp = sm + OFF_QK + (uint32_t)(n0 >> 6) * 2 * PANEL;
+                const uint8_t *qp = sm + QK + (uint32_t)(n0 >> 6) * 2 * PANEL;
 #pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    v[q] = gi * __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qp + sw128(row, (n0 & 63) + q))) - v[q];
-                uint4 *dq = reinterpret_cast<uint4 *>(p.mQ + (ch * 64 + row) * D + n0);
+                for (int e = 0; e < 4; ++e) {  // 16-byte groups of 8 bf16 of the swizzled Q row
+                    const uint4 w = *reinterpret_cast<const uint4 *>(qp + sw128(row, (n0 & 63) + 8 * e));
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    dq[g] = make_uint4(pack_h2(v[8 * g], v[8 * g + 1]), pack_h2(v[8 * g + 2], v[8 * g + 3]),
-                                       pack_h2(v[8 * g + 4], v[8 * g + 5]), pack_h2(v[8 * g + 6], v[8 * g + 7]));
+                    for (int h2 = 0; h2 < 4; ++h2) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ww[h2]));
+                        v[8 * e + 2 * h2] = gi * f.x - v[8 * e + 2 * h2];
+                        v[8 * e + 2 * h2 + 1] = gi * f.y - v[8 * e + 2 * h2 + 1];
+                    }
+                }
+                st_row_h(sm + OUT_Q + pq, row, n0 & 63, v);
                 // O_loc [i][c]
                 tmem_ld(tmem + TM_OX + lane_off + (uint32_t)n0, v);
-                uint4 *dO = reinterpret_cast<uint4 *>(p.mO + (ch * 64 + row) * D + n0);
-#pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    dO[g] = make_uint4(pack_h2(v[8 * g], v[8 * g + 1]), pack_h2(v[8 * g + 2], v[8 * g + 3]),
-                                       pack_h2(v[8 * g + 4], v[8 * g + 5]), pack_h2(v[8 * g + 6], v[8 * g + 7]));
+                st_row_h(sm + OUT_O + pq, row, n0 & 63, v);
             }
         }
+        fence_async_smem();
         fence_before_sync();
         __syncthreads();  // every read of this chunk's tiles and tensor memory is done
+        if (tid == 0) {
+            const int ra = chunk * 128, rq = chunk * 64;
+            tma_store_2d(&tm_ma, sbase + OUT_A, 0, ra);
+            tma_store_2d(&tm_ma, sbase + OUT_A + 2 * PANEL, 64, ra);
+            tma_store_2d(&tm_mb, sbase + OUT_B, 0, ra);
+            tma_store_2d(&tm_mb, sbase + OUT_B + 2 * PANEL, 64, ra);
+            tma_store_2d(&tm_mq, sbase + OUT_Q, 0, rq);
+            tma_store_2d(&tm_mq, sbase + OUT_Q + PANEL, 64, rq);
+            tma_store_2d(&tm_mo, sbase + OUT_O, 0, rq);
+            tma_store_2d(&tm_mo, sbase + OUT_O + PANEL, 64, rq);
+            bulk_commit();
+        }
+        MAP_MARK(6);
     }
+#ifdef PRISM_PHASE_TIMERS
+    if (tid == 0)
+        for (int k = 0; k < 8; ++k) atomicAdd(&prism_map_phase_cycles[k], ph_acc[k]);
+#endif
 
     // drain: after an expired wait, let every copy and product still in flight land (bounded by one
     // second each) before the CTA releases its shared and tensor memory.  One more commit arrives
     // once every product this thread issued has completed.
-    if (tid == 0 && abort_s) {
-        const uint64_t drain_ns = 1000000000ull;
-        if (pend_qkv) (void)mbar_wait(mb_qkv, ph_qkv, drain_ns);
-        for (int b = 0; b < 2; ++b)
-            if (pend_u[b]) (void)mbar_wait(mb_u[b], ph_u[b], drain_ns);
-        const uint32_t mb_drain = smem_u32(&mbar[7]);
-        mma_commit(mb_drain);
-        (void)mbar_wait(mb_drain, 0, drain_ns);
+    if (tid == 0) {
+        bulk_wait_all();  // the outgoing maps have been written
+        if (abort_s) {
+            const uint64_t drain_ns = 1000000000ull;
+            if (pend_qkv) (void)mbar_wait(mb_qkv, ph_qkv, drain_ns);
+            for (int b = 0; b < 2; ++b)
+                if (pend_u[b]) (void)mbar_wait(mb_u[b], ph_u[b], drain_ns);
+            const uint32_t mb_drain = smem_u32(&mbar[7]);
+            mma_commit(mb_drain);
+            (void)mbar_wait(mb_drain, 0, drain_ns);
+        }
     }
     fence_before_sync();
     __syncthreads();
@@ -608,20 +703,43 @@ __global__ void __launch_bounds__(NT, 1)
 // ---------------------------------------------------------------------------------------------
 // scan: one CTA per sequence, 8 warps.  Per chunk: D1 = S A_c and D2 = Q~ S^T (S fp16 in shared
 // memory, K-major [c][m]), then S <- D1 + B_c (every thread: one state row, 64 columns) and
-// o = D2 + O_loc for the chunk's tokens (rows i < 64: warps of lane quarters 0-1).  The maps of
-// the next two chunks stream through a two-stage ring of TMA copies.
+// o = D2 + O_loc for the chunk's tokens (rows i < 64: warps of lane quarters 0-1).  A_c, Q~ and B_c
+// of the next two chunks stream through a two-stage ring of TMA copies; a stage is refilled as soon
+// as the products have read it and B_c has been taken into registers.  O_loc is read from global
+// memory into registers at the start of the step; a bf16 output leaves through a shared-memory
+// tile and a TMA store.
+// v[o .. o + 7] += the 8 halves of w
+__device__ __forceinline__ void add_h8(float (&v)[32], int o, const uint4 w)
+{
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h2 = 0; h2 < 4; ++h2) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[h2]));
+        v[o + 2 * h2] += f.x;
+        v[o + 2 * h2 + 1] += f.y;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_b2(float a, float b)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 constexpr int ST = 256;
 constexpr uint32_t SC_OFF_S = 0;  // S: 2 panels [128 rows][64] fp16 (16 KB each)
-constexpr uint32_t STAGE = 4 * PANEL + 2 * PANEL + 4 * PANEL + 2 * PANEL;  // A_c | Q~ | B_c | O_loc
-constexpr uint32_t SG_A = 0, SG_Q = 4 * PANEL, SG_B = 6 * PANEL, SG_O = 10 * PANEL;
+constexpr uint32_t STAGE = 4 * PANEL + 2 * PANEL + 4 * PANEL;  // A_c | Q~ | B_c
+constexpr uint32_t SG_A = 0, SG_Q = 4 * PANEL, SG_B = 6 * PANEL;
 constexpr uint32_t SC_OFF_ST = 4 * PANEL;
-constexpr uint32_t SCAN_SMEM = SC_OFF_ST + 2 * STAGE + 1024;
+constexpr uint32_t SC_OFF_OUT = SC_OFF_ST + 2 * STAGE;  // bf16 output tile: 2 panels [64][64]
+constexpr uint32_t SCAN_SMEM = SC_OFF_OUT + 2 * PANEL + 1024;
 static_assert(SCAN_SMEM <= 232448, "shared memory budget");
 constexpr uint32_t TM_D1 = 0, TM_D2 = 128;
 
 struct ScanParams {
     const float *S_init;  // [BH][D][D] or null
     float *S_final;       // [BH][D][D] or null
+    const __half *mO;     // [BH*NC][64][128] O_loc
     void *out;            // [BH][T][D] bf16, or fp32 with out_f32
     int *status;
     int T, NC, out_f32;
@@ -630,7 +748,7 @@ struct ScanParams {
 
 __global__ void __launch_bounds__(ST, 1)
     scan_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_qt,
-                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_o, ScanParams p)
+                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_out, ScanParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -652,21 +770,18 @@ __global__ void __launch_bounds__(ST, 1)
         prefetch_tmap(&tm_a);
         prefetch_tmap(&tm_qt);
         prefetch_tmap(&tm_b);
-        prefetch_tmap(&tm_o);
+        prefetch_tmap(&tm_out);
     }
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 256);
     // the initial state (fp16 operand copy): this thread's row, 64 columns
     {
-        float v[64];
-#pragma unroll
-        for (int q = 0; q < 64; ++q)
-            v[q] = p.S_init ? p.S_init[((size_t)bh * D + row) * D + 64 * half + q] : 0.f;
         uint8_t *sp = sm + SC_OFF_S + (uint32_t)half * 2 * PANEL;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
             float w[32];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) w[q] = v[32 * g + q];
+            for (int q = 0; q < 32; ++q)
+                w[q] = p.S_init ? p.S_init[((size_t)bh * D + row) * D + 64 * half + 32 * g + q] : 0.f;
             st_row_h(sp, row, 32 * g, w);
         }
     }
@@ -681,7 +796,7 @@ __global__ void __launch_bounds__(ST, 1)
 
     const int NC = p.NC;
     const size_t ch0 = (size_t)bh * NC;
-    auto issue = [&](int c) {  // chunk c's maps into stage c & 1
+    auto issue = [&](int c) {  // chunk c's A_c, Q~, B_c into stage c & 1
         const int st = c & 1;
         const uint32_t base = sbase + SC_OFF_ST + st * STAGE;
         const int ra = (int)((ch0 + c) * 128), rq = (int)((ch0 + c) * 64);
@@ -692,8 +807,6 @@ __global__ void __launch_bounds__(ST, 1)
         tma_load_2d(base + SG_Q + PANEL, &tm_qt, mb_full[st], 64, rq);
         tma_load_2d(base + SG_B, &tm_b, mb_full[st], 0, ra);
         tma_load_2d(base + SG_B + 2 * PANEL, &tm_b, mb_full[st], 64, ra);
-        tma_load_2d(base + SG_O, &tm_o, mb_full[st], 0, rq);
-        tma_load_2d(base + SG_O + PANEL, &tm_o, mb_full[st], 64, rq);
     };
     uint32_t ph_full[2] = {0, 0}, ph_mma = 0;
     int issued = 0, consumed = 0;  // thread 0: chunks whose maps were requested / have landed
@@ -701,7 +814,11 @@ __global__ void __launch_bounds__(ST, 1)
         for (; issued < 2 && issued < NC; ++issued) issue(issued);
     }
     bool finite = true;
-    for (int c = 0; c < NC; ++c) {
+#ifdef PRISM_PHASE_TIMERS
+    unsigned long long ph_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    long long ph_last = clock64();
+#endif
+    for (int c = 0; c < NC && abort_s == 0; ++c) {
         const int st = c & 1;
         const uint32_t sb = SC_OFF_ST + st * STAGE;
         if (tid == 0) {
@@ -729,26 +846,44 @@ __global__ void __launch_bounds__(ST, 1)
                 set_status(p.status, kDevTimeout);
             }
         }
+        // O_loc of this thread's token row (rows i < 64), from global memory while the products run
+        uint4 ol[8];
+        if (quad < 2) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.mO + ((ch0 + c) * 64 + row) * D + 64 * half);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ol[e] = src[e];
+        }
         __syncthreads();
         if (abort_s) break;
+        MAP_MARK(0);
         ph_full[st] ^= 1u;
+        // B_c of this thread's state row into registers, so that the stage can be refilled
+        uint4 bc[8];
+        {
+            const uint8_t *bp = sm + sb + SG_B + (uint32_t)half * 2 * PANEL;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bc[e] = *reinterpret_cast<const uint4 *>(bp + sw128(row, 8 * e));
+        }
         if (!mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
             abort_s = 1;
             set_status(p.status, kDevTimeout);
         }
         ph_mma ^= 1u;
+        if (tid == 0) bulk_wait_read();  // the previous chunk's output tile has been read out
+        fence_before_sync();
+        __syncthreads();  // stage st is consumed: refill it with chunk c + 2
         fence_after_sync();
+        if (tid == 0 && issued < NC && abort_s == 0) issue(issued++);
+        MAP_MARK(1);
         // S <- S A_c + B_c (this thread: row `row`, columns 64 half .. 64 half + 63)
         {
-            const uint8_t *bp = sm + sb + SG_B + (uint32_t)half * 2 * PANEL;
             uint8_t *sp = sm + SC_OFF_S + (uint32_t)half * 2 * PANEL;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 float v[32];
                 tmem_ld(tmem + TM_D1 + lane_off + (uint32_t)(64 * half + 32 * g), v);
 #pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    v[q] += __half2float(*reinterpret_cast<const __half *>(bp + sw128(row, 32 * g + q)));
+                for (int e = 0; e < 4; ++e) add_h8(v, 8 * e, bc[4 * g + e]);
                 if (c + 1 == NC && p.S_final) {
                     float4 *sf = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + row) * D + 64 * half + 32 * g);
 #pragma unroll
@@ -757,54 +892,61 @@ __global__ void __launch_bounds__(ST, 1)
                 st_row_h(sp, row, 32 * g, v);
             }
         }
+        MAP_MARK(2);
         // o = Q~ S^T + O_loc for tokens i = row < n (lane quarters 0-1)
         if (quad < 2) {
             const int n = min(C, p.T - c * C);
-            const uint8_t *op = sm + sb + SG_O + (uint32_t)half * PANEL;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 float v[32];
                 tmem_ld(tmem + TM_D2 + lane_off + (uint32_t)(64 * half + 32 * g), v);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    v[q] += __half2float(*reinterpret_cast<const __half *>(op + sw128(row, 32 * g + q)));
-                    finite = finite && isfinite(v[q]);
-                }
-                if (row < n) {
+                for (int e = 0; e < 4; ++e) add_h8(v, 8 * e, ol[4 * g + e]);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) finite = finite && isfinite(v[q]);
+                if (!p.out_f32) {  // into the output tile (the TMA store drops rows past T)
+                    uint8_t *op = sm + SC_OFF_OUT + (uint32_t)half * PANEL;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4 *>(op + sw128(row, 32 * g + 8 * q)) =
+                            make_uint4(pack_b2(v[8 * q], v[8 * q + 1]), pack_b2(v[8 * q + 2], v[8 * q + 3]),
+                                       pack_b2(v[8 * q + 4], v[8 * q + 5]), pack_b2(v[8 * q + 6], v[8 * q + 7]));
+                } else if (row < n) {
                     const size_t o = ((size_t)bh * p.T + (size_t)c * C + row) * D + 64 * half + 32 * g;
-                    if (p.out_f32) {
-                        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o);
+                    float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + o);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
-                                w[e] = *reinterpret_cast<const uint32_t *>(&b2);
-                            }
-                            dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    }
+                    for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
             }
         }
-        fence_async_smem();  // S is the next chunk's MMA operand
+        MAP_MARK(3);
+        fence_async_smem();  // S is the next chunk's MMA operand; the output tile goes out by TMA
         fence_before_sync();
-        __syncthreads();     // stage st and both accumulators are free
-        if (tid == 0 && issued < NC) issue(issued++);
+        __syncthreads();
+        fence_after_sync();
+        if (tid == 0 && !p.out_f32) {
+            tma_store_3d(&tm_out, sbase + SC_OFF_OUT, 0, c * C, bh);
+            tma_store_3d(&tm_out, sbase + SC_OFF_OUT + PANEL, 64, c * C, bh);
+            bulk_commit();
+        }
+        MAP_MARK(4);
     }
+#ifdef PRISM_PHASE_TIMERS
+    if (tid == 0)
+        for (int k = 0; k < 5; ++k) atomicAdd(&prism_map_phase_cycles[8 + k], ph_acc[k]);
+#endif
     if (!finite) set_status(p.status, kDevBounds);  // outside the fp16 operand range
-    // drain: copies and products still in flight after an expired wait land before the CTA exits
-    if (tid == 0 && abort_s) {
-        for (int c = consumed; c < issued; ++c)
-            (void)mbar_wait(mb_full[c & 1], (uint32_t)((c >> 1) & 1), 1000000000ull);
-        const uint32_t mb_drain = smem_u32(&mbar[3]);
-        mma_commit(mb_drain);
-        (void)mbar_wait(mb_drain, 0, 1000000000ull);
+    // drain: the output stores complete; after an expired wait, copies and products still in flight
+    // land before the CTA exits
+    if (tid == 0) {
+        bulk_wait_all();
+        if (abort_s) {
+            for (int c = consumed; c < issued; ++c)
+                (void)mbar_wait(mb_full[c & 1], (uint32_t)((c >> 1) & 1), 1000000000ull);
+            const uint32_t mb_drain = smem_u32(&mbar[3]);
+            mma_commit(mb_drain);
+            (void)mbar_wait(mb_drain, 0, 1000000000ull);
+        }
     }
     fence_before_sync();
     __syncthreads();
@@ -916,6 +1058,7 @@ cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, cons
     mp_.eta = a.eta;
     mp_.conv_w = (const __nv_bfloat16 *)a.conv_w;
     mp_.v_hist = (const __nv_bfloat16 *)a.v_hist;
+    mp_.p_gain = (const __nv_bfloat16 *)a.p_gain;
     mp_.mA = w.A;
     mp_.mQ = w.Q;
     mp_.mB = w.B;
@@ -927,7 +1070,17 @@ cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, cons
     mp_.NC = s.NC;
     mp_.nchunks = (int)chunks;
     mp_.wait_ns = wns;
+    CUtensorMap mout;
+    if (out_f32) {
+        mout = ma;  // not read: an fp32 output is written directly
+    } else {
+        cuuint64_t dims[3] = {(cuuint64_t)D, T, BH};
+        cuuint64_t str[2] = {(cuuint64_t)D * 2, T * D * 2};
+        cuuint32_t box[3] = {64, 64, 1};
+        if (!encode_map(&mout, BF, a.out, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    }
     ScanParams sp;
+    sp.mO = w.O;
     sp.S_init = a.S_init;
     sp.S_final = a.S_final;
     sp.out = a.out;
@@ -948,14 +1101,14 @@ cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, cons
     cfg.gridDim = dim3((unsigned)((int)chunks < sm_count ? (int)chunks : sm_count));
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = MAP_SMEM;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, map_kernel, mq, mk, mv, mu, mp_);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, map_kernel, mq, mk, mv, mu, ma, mqt, mb, mo, mp_);
     tm.end();
     if (e != cudaSuccess) return e;
     tm.begin("map_scan");
     cfg.gridDim = dim3((unsigned)s.BH);
     cfg.blockDim = dim3(ST);
     cfg.dynamicSmemBytes = SCAN_SMEM;
-    e = cudaLaunchKernelEx(&cfg, scan_kernel, ma, mqt, mb, mo, sp);
+    e = cudaLaunchKernelEx(&cfg, scan_kernel, ma, mqt, mb, mout, sp);
     tm.end();
     if (e != cudaSuccess) return e;
     if (a.v_hist_out) {  // a plain launch: it runs after the kernels above have read v_hist
@@ -966,3 +1119,16 @@ cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, cons
 }
 
 }  // namespace prism
+
+#ifdef PRISM_PHASE_TIMERS
+// developer tracing build only: copy out (and optionally clear) the per-phase cycle totals
+extern "C" __attribute__((visibility("default"))) int prism_debug_map_phase_cycles(unsigned long long *out, int reset)
+{
+    if (cudaMemcpyFromSymbol(out, prism_map_phase_cycles, sizeof(unsigned long long) * 16) != cudaSuccess) return -1;
+    if (reset) {
+        unsigned long long z[16] = {0};
+        if (cudaMemcpyToSymbol(prism_map_phase_cycles, z, sizeof(z)) != cudaSuccess) return -1;
+    }
+    return 0;
+}
+#endif

@@ -119,6 +119,7 @@ struct SegParams {
     void *stash_o;          // [BH][NC][64][64]  o0 (token-major; fp32 for fp32 output, else fp16)
     __half *stash_q;        // [BH][NC][64][64]  Qhat (token-major)
     const __nv_bfloat16 *v_hist;  // [BH][3][64] v_{-3..-1} of the sequence, or null (zeros)
+    const __nv_bfloat16 *p_gain;  // [BH][T][R][64] gains of the non-linear residual chain, or null (linear)
     int *status;
     int H, T, R, NC, P;
     int out_f32;
@@ -183,6 +184,14 @@ __device__ __forceinline__ void gelu_gain(float a, float &g, float &Phi)
     const float erfx = 1.f - poly * t * E;
     Phi = 0.5f + copysignf(0.5f * erfx, a);
     g = fmaf(a, 0.39894228040143268f * E, Phi);
+}
+
+// GELU(z) = z Phi(z), Phi from the same approximation of erf as gelu_gain
+__device__ __forceinline__ float gelu_value(float z)
+{
+    float g, Phi;
+    gelu_gain(z, g, Phi);
+    return z * Phi;
 }
 
 // round to tf32 (the operand format of mma.sync .tf32)
@@ -253,7 +262,8 @@ __device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes,
 // prep of one chunk (P1): anchor, gain and residual chain -> X tiles, two channels x 4 tokens per
 // thread, from V stage `stg` and the chunk's per-token scalars `pset`.  Kept out of line: the
 // segment kernel calls it at two places, and one copy of its code keeps the loop body smaller.
-__device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __nv_bfloat162 *cw2, int stg, int R)
+__device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __nv_bfloat162 *cw2, int stg, int R,
+                                        const uint32_t *pg, int n)
 {
     const int tid = threadIdx.x;
     const float2 w0 = __bfloat1622float2(cw2[0 * (D / 2)]);
@@ -264,6 +274,16 @@ __device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __
     const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(sm + (stg ? OFF_V1 : OFF_V0));
     const int cp = tid & 31, tg = tid >> 5;  // channel pair, token group
     constexpr int TPT = 64 / (NT / 32);     // tokens per thread
+    // the non-linear chain's gains of this thread's tokens, all loads issued before any is used
+    uint32_t pz[TPT][RMAX];
+    if (pg) {
+#pragma unroll
+        for (int k = 0; k < TPT; ++k) {
+            const int i = tg + (NT / 32) * k;
+#pragma unroll
+            for (int l = 0; l < RMAX; ++l) pz[k][l] = (i < n && l < R) ? pg[(size_t)(i * R + l) * (D / 2) + cp] : 0u;
+        }
+    }
 #pragma unroll
     for (int k = 0; k < TPT; ++k) {
         const int i = tg + (NT / 32) * k;
@@ -284,11 +304,24 @@ __device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __
         gelu_gain(a1, g1, Phi1);
         float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
         uint8_t *xs = sm + OFF_XS + sw128(i, 2 * cp);
+        if (pg) {  // non-linear chain: delta = GELU(p r), x = gamma delta, r <- r - delta
 #pragma unroll
-        for (int l = 0; l < RMAX; ++l) {
-            if (l < R) *reinterpret_cast<uint32_t *>(xs + l * TILE) = pack2(gcl[l] * g0 * r0, gcl[l] * g1 * r1);
-            r0 *= 1.f - etl[l] * g0;
-            r1 *= 1.f - etl[l] * g1;
+            for (int l = 0; l < RMAX; ++l) {
+                if (l < R) {
+                    const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pz[k][l]));
+                    const float d0 = gelu_value(pf.x * r0), d1 = gelu_value(pf.y * r1);
+                    *reinterpret_cast<uint32_t *>(xs + l * TILE) = pack2(gcl[l] * d0, gcl[l] * d1);
+                    r0 -= d0;
+                    r1 -= d1;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int l = 0; l < RMAX; ++l) {
+                if (l < R) *reinterpret_cast<uint32_t *>(xs + l * TILE) = pack2(gcl[l] * g0 * r0, gcl[l] * g1 * r1);
+                r0 *= 1.f - etl[l] * g0;
+                r1 *= 1.f - etl[l] * g1;
+            }
         }
     }
 }
@@ -442,7 +475,7 @@ __global__ void __launch_bounds__(NT, 1)
             const int i = gt / RMAX, l = gt % RMAX;
             const bool valid = (i < n) && (l < R);
             pf_gam = valid ? p.gamma[(tok0 + i) * R + l] : 0.f;
-            pf_eta = valid ? p.eta[(tok0 + i) * R + l] : 0.f;
+            pf_eta = (valid && p.eta) ? p.eta[(tok0 + i) * R + l] : 0.f;
         }
     };
     if (c_begin < c_end) load_gates(c_begin);
@@ -481,7 +514,12 @@ __global__ void __launch_bounds__(NT, 1)
     // prep of chunk cc (P1): anchor, gain and residual chain -> X tiles, two channels x 4 tokens
     // per thread, from the V stage stg and the chunk's per-token scalars.  It runs in the
     // previous chunk's tail, while that chunk's last MMAs are in flight.
-    auto prep = [&](int cc, int stg) { prep_chunk(sm, sc + (cc & 1) * SC_SET, cw2, stg, R); };
+    auto prep = [&](int cc, int stg) {
+        const uint32_t *pg = p.p_gain ? reinterpret_cast<const uint32_t *>(p.p_gain) +
+                                            ((size_t)bh * p.T + (size_t)cc * C) * R * (D / 2)
+                                      : nullptr;
+        prep_chunk(sm, sc + (cc & 1) * SC_SET, cw2, stg, R, pg, min(C, p.T - cc * C));
+    };
 
 #ifdef PRISM_PHASE_TIMERS
     // per-phase totals in shared memory (registers would crowd the kernel's own)
@@ -1468,6 +1506,7 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
     p.stash_o = w.stash_o;
     p.stash_q = w.stash_q;
     p.v_hist = (const __nv_bfloat16 *)a.v_hist;
+    p.p_gain = (const __nv_bfloat16 *)a.p_gain;
     p.has_init = a.S_init != nullptr;
     p.status = d_status;
     p.H = s.H;

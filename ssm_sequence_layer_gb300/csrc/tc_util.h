@@ -68,6 +68,20 @@ __device__ __forceinline__ void gelu_gain(float a, float &g, float &Phi)
     g = fmaf(a, 0.39894228040143268f * E, Phi);
 }
 
+// GELU(z) = z Phi(z) (exact-erf form), Phi from the same rational approximation of erf.
+__device__ __forceinline__ float gelu_value(float z)
+{
+    const float x = fabsf(z) * 0.70710678118654752f;
+    const float t = __fdividef(1.f, fmaf(0.3275911f, x, 1.f));
+    const float E = __expf(-0.5f * z * z);
+    float poly = fmaf(t, 1.061405429f, -1.453152027f);
+    poly = fmaf(t, poly, 1.421413741f);
+    poly = fmaf(t, poly, -0.284496736f);
+    poly = fmaf(t, poly, 0.254829592f);
+    const float erfx = 1.f - poly * t * E;
+    return z * (0.5f + copysignf(0.5f * erfx, z));
+}
+
 // barrier over `n` threads (whole warps) of the CTA; ids 1.. (0 is __syncthreads')
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 

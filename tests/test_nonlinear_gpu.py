@@ -88,13 +88,27 @@ def test_nonlinear_split_calls_with_state(oracle_mod):
     assert rel_err(S.double().cpu().numpy(), ref["S_final"]) <= TOL["f32"]
 
 
-def test_nonlinear_variant_refuses_the_tensor_core_path():
+@pytest.mark.parametrize("B_,H,T,d,L", [
+    (1, 2, 300, 64, 4), (2, 1, 1000, 64, 3), (1, 1, 65, 64, 2),       # segment kernels
+    (2, 2, 257, 128, 4), (1, 1, 130, 128, 8), (1, 2, 64, 128, 16),    # chunk-map kernels
+])
+def test_nonlinear_variant_on_the_tensor_core_path(oracle_mod, B_, H, T, d, L):
+    """The variant on the tensor-core kernels (forced, and chosen automatically for bf16): only
+    their prep differs, stepping delta = GELU(p r), r <- r - delta level by level."""
+    inp = make_inputs(B_, H, T, d, d, L, dtype="bf16", seed=110 + L + T)
+    p = make_gain(B_, H, T, L, d, dtype="bf16", seed=110 + L + T)
+    ref = oracle_forward(oracle_mod, inp, p_gain=p.double().numpy())["out"]
+    dd = to_device(inp)
+    for kw in (dict(path=2), {}):
+        with B.Plan.for_inputs(dd, out="f32", **kw) as plan:
+            out = plan.forward_nonlinear(dd, p.cuda())
+            torch.cuda.synchronize()
+            plan.last_device_status()
+        assert rel_err(out.double().cpu().numpy(), ref) <= TOL["bf16"]
+
+
+def test_nonlinear_variant_checks_its_gains():
     inp = to_device(make_inputs(1, 1, 64, 64, 64, 3, dtype="bf16", seed=98))
-    p = make_gain(1, 1, 64, 3, 64, dtype="bf16", seed=98).cuda()
-    with B.Plan.for_inputs(inp, path=2) as plan:
-        with pytest.raises(B.PrismError) as ei:
-            plan.forward_nonlinear(inp, p)
-        assert ei.value.status == B.PRISM_ERR_UNSUPPORTED
     with B.Plan.for_inputs(inp) as plan:
         with pytest.raises(B.PrismError) as ei:
             B.prism_forward_nonlinear(plan.handle, *plan._tensors(inp)[:7], None, inp["conv_w"], 3, None, None,
