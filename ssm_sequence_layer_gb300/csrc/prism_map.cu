@@ -215,6 +215,31 @@ __global__ void __launch_bounds__(NT, 1)
 
     // this thread's prep elements: channels 2 cp, 2 cp + 1 of tokens tg + 8 k
     const int cp = tid & 63, tg = tid >> 6;
+    // gates of one chunk in registers (loaded one chunk ahead, so their latency hides): lanes of
+    // warp 0 hold beta and alpha of tokens 2 lane, 2 lane + 1; the other threads two (gamma, eta)
+    // entries [i][l] each (64 R <= 2 (NT - 32) entries)
+    static_assert(64 * RM <= 2 * (NT - 32), "gate entries per thread");
+    float gv[4];
+    auto load_gates = [&](int ch) {
+        const int cbh = ch / p.NC, ct0 = (ch % p.NC) * C, cn = min(C, p.T - ct0);
+        const size_t ctok = (size_t)cbh * p.T + ct0;
+        if (warp == 0) {
+            const int i0 = 2 * lane, i1 = i0 + 1;
+            gv[0] = i0 < cn ? p.beta[ctok + i0] : 0.f;
+            gv[1] = i1 < cn ? p.beta[ctok + i1] : 0.f;
+            gv[2] = i0 < cn ? p.alpha[ctok + i0] : 1.f;
+            gv[3] = i1 < cn ? p.alpha[ctok + i1] : 1.f;
+        } else if (R > 0) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int e = tid - 32 + k * (NT - 32);
+                const int i = e / R, l = e % R;
+                const bool valid = e < 64 * R && i < cn;
+                gv[2 * k] = valid ? p.gamma[(ctok + i) * R + l] : 0.f;
+                gv[2 * k + 1] = (valid && p.eta) ? p.eta[(ctok + i) * R + l] : 0.f;
+            }
+        }
+    };
 #ifdef PRISM_PHASE_TIMERS
     unsigned long long ph_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     long long ph_last = clock64();
@@ -238,11 +263,12 @@ __global__ void __launch_bounds__(NT, 1)
             if (R > 0) issue_u(bh, t0, 0);
             if (R > 1) issue_u(bh, t0, 1);
         }
-        // ---- per-token scalars: gates, log-decay prefix, decay factors ----------------------------
+        // ---- per-token scalars: gates (loaded during the previous chunk), log-decay prefix, decays --
+        if (it == 0) load_gates(chunk);
         if (warp == 0) {  // inclusive scan of the 64 log-decays, two per lane
             const int i0 = 2 * lane, i1 = i0 + 1;
-            const float b0 = i0 < n ? p.beta[tok0 + i0] : 0.f, b1 = i1 < n ? p.beta[tok0 + i1] : 0.f;
-            const float la0 = i0 < n ? logf(p.alpha[tok0 + i0]) : 0.f, la1 = i1 < n ? logf(p.alpha[tok0 + i1]) : 0.f;
+            const float b0 = gv[0], b1 = gv[1];
+            const float la0 = logf(gv[2]), la1 = logf(gv[3]);
             float s = la0 + la1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -264,11 +290,14 @@ __global__ void __launch_bounds__(NT, 1)
             s_bg[i0] = b0 * __expf(l0);
             s_bg[i1] = b1 * __expf(l1);
         } else if (R > 0) {  // gamma, eta [i][l] of this chunk
-            for (int e = tid - 32; e < 64 * R; e += NT - 32) {
-                const int i = e / R, l = e % R;
-                const bool valid = i < n;
-                s_gm[i * RMS + l] = valid ? p.gamma[(tok0 + i) * R + l] : 0.f;
-                s_et[i * RMS + l] = (valid && p.eta) ? p.eta[(tok0 + i) * R + l] : 0.f;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int e = tid - 32 + k * (NT - 32);
+                if (e < 64 * R) {
+                    const int i = e / R, l = e % R;
+                    s_gm[i * RMS + l] = gv[2 * k];
+                    s_et[i * RMS + l] = gv[2 * k + 1];
+                }
             }
         }
         // Q, K and V have landed (every thread waits; the history, if any, then replaces the halo)
@@ -579,6 +608,10 @@ __global__ void __launch_bounds__(NT, 1)
             const int next = chunk + (int)gridDim.x;
             if (next < p.nchunks) issue_qkv(next, AT);
         }
+        {  // the next chunk's gates, while the products run
+            const int next = chunk + (int)gridDim.x;
+            if (next < p.nchunks) load_gates(next);
+        }
         wait_all(mb_post, ph_post);
         fence_after_sync();
         if (quad < 2) {  // rows i < 64: sub 0, 1 -> U' columns, sub 2, 3 -> W columns (64 per thread)
@@ -701,15 +734,17 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// scan: one CTA per sequence, 8 warps.  Per chunk: D1 = S A_c and D2 = Q~ S^T (S fp16 in shared
-// memory, K-major [c][m]), then S <- D1 + B_c (every thread: one state row, 64 columns) and
-// o = D2 + O_loc for the chunk's tokens (rows i < 64: warps of lane quarters 0-1).  A_c, Q~ and B_c
-// of the next two chunks stream through a two-stage ring of TMA copies; a stage is refilled as soon
-// as the products have read it and B_c has been taken into registers.  O_loc is read from global
-// memory into registers at the start of the step; a bf16 output leaves through a shared-memory
-// tile and a TMA store.
+// scan: two CTAs per sequence, one per half of the value rows (the rows of S evolve independently),
+// 8 warps each.  Per chunk: D1 = S_h A_c and D2 = Q~ S_h^T (S_h, this CTA's 64 state rows, fp16 in
+// shared memory, K-major [c][m]), then S_h <- D1 + B_c (rows c < 64: warps of lane quarters 0-1,
+// 64 columns per thread) and o = D2 + O_loc for the chunk's tokens and this half's 64 channels.
+// A_c, Q~ and this half of B_c stream through a three-stage ring of TMA copies; a stage is refilled
+// as soon as the products have read it and B_c has been taken into registers.  O_loc is read from
+// global memory into registers at the start of the step; a bf16 output leaves through a
+// shared-memory tile and a TMA store.
 // v[o .. o + 7] += the 8 halves of w
-__device__ __forceinline__ void add_h8(float (&v)[32], int o, const uint4 w)
+template <int N>
+__device__ __forceinline__ void add_h8(float (&v)[N], int o, const uint4 w)
 {
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -727,12 +762,13 @@ __device__ __forceinline__ uint32_t pack_b2(float a, float b)
 }
 
 constexpr int ST = 256;
-constexpr uint32_t SC_OFF_S = 0;  // S: 2 panels [128 rows][64] fp16 (16 KB each)
-constexpr uint32_t STAGE = 4 * PANEL + 2 * PANEL + 4 * PANEL;  // A_c | Q~ | B_c
+constexpr int SC_STAGES = 3;
+constexpr uint32_t SC_OFF_S = 0;  // S_h: 2 panels [64 rows][64] fp16 (8 KB each)
+constexpr uint32_t STAGE = 4 * PANEL + 2 * PANEL + 2 * PANEL;  // A_c | Q~ | B_c rows of this half
 constexpr uint32_t SG_A = 0, SG_Q = 4 * PANEL, SG_B = 6 * PANEL;
-constexpr uint32_t SC_OFF_ST = 4 * PANEL;
-constexpr uint32_t SC_OFF_OUT = SC_OFF_ST + 2 * STAGE;  // bf16 output tile: 2 panels [64][64]
-constexpr uint32_t SCAN_SMEM = SC_OFF_OUT + 2 * PANEL + 1024;
+constexpr uint32_t SC_OFF_ST = 2 * PANEL;
+constexpr uint32_t SC_OFF_OUT = SC_OFF_ST + SC_STAGES * STAGE;  // bf16 output tile: [64 tokens][64 channels]
+constexpr uint32_t SCAN_SMEM = SC_OFF_OUT + PANEL + 1024;
 static_assert(SCAN_SMEM <= 232448, "shared memory budget");
 constexpr uint32_t TM_D1 = 0, TM_D2 = 128;
 
@@ -753,19 +789,21 @@ __global__ void __launch_bounds__(ST, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint32_t tmem_base_s;
-    __shared__ __align__(8) uint64_t mbar[4];  // 0, 1: ring stages; 2: products; 3: drain
+    __shared__ __align__(8) uint64_t mbar[SC_STAGES + 2];  // ring stages; products; drain
     __shared__ int abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half (64 columns)
-    const int row = quad * 32 + lane;
-    const int bh = blockIdx.x;
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half of the epilogues
+    const int row = quad * 32 + lane;             // state row / token within this half (< 64: live)
+    const bool live = quad < 2;
+    const int bh = blockIdx.x >> 1, vh = blockIdx.x & 1;  // sequence; half of the value rows
+    const int r0 = 64 * vh;                               // first state row / channel of this half
     const uint32_t sbase = smem_u32(sm);
     const uint64_t dbase = sdesc(sbase, 0, 0);
-    const uint32_t mb_full[2] = {smem_u32(&mbar[0]), smem_u32(&mbar[1])}, mb_mma = smem_u32(&mbar[2]);
+    const uint32_t mb_mma = smem_u32(&mbar[SC_STAGES]);
 
     if (tid == 0) {
         abort_s = 0;
-        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&mbar[i]), 1);
+        for (int i = 0; i < SC_STAGES + 2; ++i) mbar_init(smem_u32(&mbar[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tm_a);
         prefetch_tmap(&tm_qt);
@@ -773,15 +811,15 @@ __global__ void __launch_bounds__(ST, 1)
         prefetch_tmap(&tm_out);
     }
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 256);
-    // the initial state (fp16 operand copy): this thread's row, 64 columns
-    {
-        uint8_t *sp = sm + SC_OFF_S + (uint32_t)half * 2 * PANEL;
+    // the initial state (fp16 operand copy): row `row`, 64 columns of this thread's half
+    if (live) {
+        uint8_t *sp = sm + SC_OFF_S + (uint32_t)half * PANEL;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
             float w[32];
 #pragma unroll
             for (int q = 0; q < 32; ++q)
-                w[q] = p.S_init ? p.S_init[((size_t)bh * D + row) * D + 64 * half + 32 * g + q] : 0.f;
+                w[q] = p.S_init ? p.S_init[((size_t)bh * D + r0 + row) * D + 64 * half + 32 * g + q] : 0.f;
             st_row_h(sp, row, 32 * g, w);
         }
     }
@@ -796,22 +834,22 @@ __global__ void __launch_bounds__(ST, 1)
 
     const int NC = p.NC;
     const size_t ch0 = (size_t)bh * NC;
-    auto issue = [&](int c) {  // chunk c's A_c, Q~, B_c into stage c & 1
-        const int st = c & 1;
-        const uint32_t base = sbase + SC_OFF_ST + st * STAGE;
+    auto issue = [&](int c) {  // chunk c's A_c, Q~ and this half of B_c into stage c % SC_STAGES
+        const int st = c % SC_STAGES;
+        const uint32_t base = sbase + SC_OFF_ST + st * STAGE, mb = smem_u32(&mbar[st]);
         const int ra = (int)((ch0 + c) * 128), rq = (int)((ch0 + c) * 64);
-        mbar_expect_tx(mb_full[st], STAGE);
-        tma_load_2d(base + SG_A, &tm_a, mb_full[st], 0, ra);
-        tma_load_2d(base + SG_A + 2 * PANEL, &tm_a, mb_full[st], 64, ra);
-        tma_load_2d(base + SG_Q, &tm_qt, mb_full[st], 0, rq);
-        tma_load_2d(base + SG_Q + PANEL, &tm_qt, mb_full[st], 64, rq);
-        tma_load_2d(base + SG_B, &tm_b, mb_full[st], 0, ra);
-        tma_load_2d(base + SG_B + 2 * PANEL, &tm_b, mb_full[st], 64, ra);
+        mbar_expect_tx(mb, STAGE);
+        tma_load_2d(base + SG_A, &tm_a, mb, 0, ra);
+        tma_load_2d(base + SG_A + 2 * PANEL, &tm_a, mb, 64, ra);
+        tma_load_2d(base + SG_Q, &tm_qt, mb, 0, rq);
+        tma_load_2d(base + SG_Q + PANEL, &tm_qt, mb, 64, rq);
+        tma_load_2d(base + SG_B, &tm_b, mb, 0, ra + r0);
+        tma_load_2d(base + SG_B + PANEL, &tm_b, mb, 64, ra + r0);
     };
-    uint32_t ph_full[2] = {0, 0}, ph_mma = 0;
+    uint32_t ph_mma = 0;
     int issued = 0, consumed = 0;  // thread 0: chunks whose maps were requested / have landed
     if (tid == 0) {
-        for (; issued < 2 && issued < NC; ++issued) issue(issued);
+        for (; issued < SC_STAGES && issued < NC; ++issued) issue(issued);
     }
     bool finite = true;
 #ifdef PRISM_PHASE_TIMERS
@@ -819,24 +857,24 @@ __global__ void __launch_bounds__(ST, 1)
     long long ph_last = clock64();
 #endif
     for (int c = 0; c < NC && abort_s == 0; ++c) {
-        const int st = c & 1;
+        const int st = c % SC_STAGES;
         const uint32_t sb = SC_OFF_ST + st * STAGE;
         if (tid == 0) {
-            if (mbar_wait(mb_full[st], ph_full[st], p.wait_ns)) {
+            if (mbar_wait(smem_u32(&mbar[st]), (uint32_t)((c / SC_STAGES) & 1), p.wait_ns)) {
                 ++consumed;
                 fence_after_sync();
-                // D1 = S A_c (A = S [c][m] K-major, B = A_c [m][n] MN-major); D2 = Q~ S^T (A = Q~ [i][n]
-                // K-major, rows 64.. unused; B = S [c][m] as N x K K-major)
-                const uint32_t id1 = idesc_f16(128, 128, 0, 1), id2 = idesc_f16(128, 128, 0, 0);
+                // D1 = S_h A_c (A = S_h [c][m] K-major, rows 64.. unused; B = A_c [m][n] MN-major);
+                // D2 = Q~ S_h^T (A = Q~ [i][n] K-major, rows 64.. unused; B = S_h [c][m] as N x K)
+                const uint32_t id1 = idesc_f16(128, 128, 0, 1), id2 = idesc_f16(128, 64, 0, 0);
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
-                    const uint32_t so = SC_OFF_S + (uint32_t)(s >> 2) * 2 * PANEL + (uint32_t)(s & 3) * 32;
+                    const uint32_t so = SC_OFF_S + (uint32_t)(s >> 2) * PANEL + (uint32_t)(s & 3) * 32;
                     mma_f16(tmem + TM_D1, dsc(dbase, so, 16, 1024), dsc(dbase, sb + SG_A + s * 2048, 2 * PANEL, 1024), id1,
                             s > 0);
                 }
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
-                    const uint32_t so = SC_OFF_S + (uint32_t)(s >> 2) * 2 * PANEL + (uint32_t)(s & 3) * 32;
+                    const uint32_t so = SC_OFF_S + (uint32_t)(s >> 2) * PANEL + (uint32_t)(s & 3) * 32;
                     const uint32_t qo = sb + SG_Q + (uint32_t)(s >> 2) * PANEL + (uint32_t)(s & 3) * 32;
                     mma_f16(tmem + TM_D2, dsc(dbase, qo, 16, 1024), dsc(dbase, so, 16, 1024), id2, s > 0);
                 }
@@ -846,21 +884,20 @@ __global__ void __launch_bounds__(ST, 1)
                 set_status(p.status, kDevTimeout);
             }
         }
-        // O_loc of this thread's token row (rows i < 64), from global memory while the products run
-        uint4 ol[8];
-        if (quad < 2) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.mO + ((ch0 + c) * 64 + row) * D + 64 * half);
+        // O_loc of this thread's token row and 32 channels, from global memory while the products run
+        uint4 ol[4];
+        if (live) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.mO + ((ch0 + c) * 64 + row) * D + r0 + 32 * half);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ol[e] = src[e];
+            for (int e = 0; e < 4; ++e) ol[e] = src[e];
         }
         __syncthreads();
         if (abort_s) break;
         MAP_MARK(0);
-        ph_full[st] ^= 1u;
-        // B_c of this thread's state row into registers, so that the stage can be refilled
+        // B_c of this thread's state row (64 columns) into registers, so that the stage can be refilled
         uint4 bc[8];
-        {
-            const uint8_t *bp = sm + sb + SG_B + (uint32_t)half * 2 * PANEL;
+        if (live) {
+            const uint8_t *bp = sm + sb + SG_B + (uint32_t)half * PANEL;
 #pragma unroll
             for (int e = 0; e < 8; ++e) bc[e] = *reinterpret_cast<const uint4 *>(bp + sw128(row, 8 * e));
         }
@@ -871,13 +908,13 @@ __global__ void __launch_bounds__(ST, 1)
         ph_mma ^= 1u;
         if (tid == 0) bulk_wait_read();  // the previous chunk's output tile has been read out
         fence_before_sync();
-        __syncthreads();  // stage st is consumed: refill it with chunk c + 2
+        __syncthreads();  // stage st is consumed: refill it with chunk c + SC_STAGES
         fence_after_sync();
         if (tid == 0 && issued < NC && abort_s == 0) issue(issued++);
         MAP_MARK(1);
-        // S <- S A_c + B_c (this thread: row `row`, columns 64 half .. 64 half + 63)
-        {
-            uint8_t *sp = sm + SC_OFF_S + (uint32_t)half * 2 * PANEL;
+        if (live) {
+            // S_h <- S_h A_c + B_c (row `row`, columns 64 half .. 64 half + 63)
+            uint8_t *sp = sm + SC_OFF_S + (uint32_t)half * PANEL;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 float v[32];
@@ -885,7 +922,7 @@ __global__ void __launch_bounds__(ST, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) add_h8(v, 8 * e, bc[4 * g + e]);
                 if (c + 1 == NC && p.S_final) {
-                    float4 *sf = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + row) * D + 64 * half + 32 * g);
+                    float4 *sf = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + r0 + row) * D + 64 * half + 32 * g);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) sf[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
@@ -893,40 +930,36 @@ __global__ void __launch_bounds__(ST, 1)
             }
         }
         MAP_MARK(2);
-        // o = Q~ S^T + O_loc for tokens i = row < n (lane quarters 0-1)
-        if (quad < 2) {
+        if (live) {
+            // o = Q~ S_h^T + O_loc: token `row`, this half's channels 32 half .. 32 half + 31
             const int n = min(C, p.T - c * C);
+            float v[32];
+            tmem_ld(tmem + TM_D2 + lane_off + (uint32_t)(32 * half), v);
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                float v[32];
-                tmem_ld(tmem + TM_D2 + lane_off + (uint32_t)(64 * half + 32 * g), v);
+            for (int e = 0; e < 4; ++e) add_h8(v, 8 * e, ol[e]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) add_h8(v, 8 * e, ol[4 * g + e]);
+            for (int q = 0; q < 32; ++q) finite = finite && isfinite(v[q]);
+            if (!p.out_f32) {  // into the output tile (the TMA store drops rows past T)
+                uint8_t *op = sm + SC_OFF_OUT;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) finite = finite && isfinite(v[q]);
-                if (!p.out_f32) {  // into the output tile (the TMA store drops rows past T)
-                    uint8_t *op = sm + SC_OFF_OUT + (uint32_t)half * PANEL;
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4 *>(op + sw128(row, 32 * half + 8 * q)) =
+                        make_uint4(pack_b2(v[8 * q], v[8 * q + 1]), pack_b2(v[8 * q + 2], v[8 * q + 3]),
+                                   pack_b2(v[8 * q + 4], v[8 * q + 5]), pack_b2(v[8 * q + 6], v[8 * q + 7]));
+            } else if (row < n) {
+                const size_t o = ((size_t)bh * p.T + (size_t)c * C + row) * D + r0 + 32 * half;
+                float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4 *>(op + sw128(row, 32 * g + 8 * q)) =
-                            make_uint4(pack_b2(v[8 * q], v[8 * q + 1]), pack_b2(v[8 * q + 2], v[8 * q + 3]),
-                                       pack_b2(v[8 * q + 4], v[8 * q + 5]), pack_b2(v[8 * q + 6], v[8 * q + 7]));
-                } else if (row < n) {
-                    const size_t o = ((size_t)bh * p.T + (size_t)c * C + row) * D + 64 * half + 32 * g;
-                    float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                }
+                for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         }
         MAP_MARK(3);
-        fence_async_smem();  // S is the next chunk's MMA operand; the output tile goes out by TMA
+        fence_async_smem();  // S_h is the next chunk's MMA operand; the output tile goes out by TMA
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
         if (tid == 0 && !p.out_f32) {
-            tma_store_3d(&tm_out, sbase + SC_OFF_OUT, 0, c * C, bh);
-            tma_store_3d(&tm_out, sbase + SC_OFF_OUT + PANEL, 64, c * C, bh);
+            tma_store_3d(&tm_out, sbase + SC_OFF_OUT, r0, c * C, bh);
             bulk_commit();
         }
         MAP_MARK(4);
@@ -942,8 +975,8 @@ __global__ void __launch_bounds__(ST, 1)
         bulk_wait_all();
         if (abort_s) {
             for (int c = consumed; c < issued; ++c)
-                (void)mbar_wait(mb_full[c & 1], (uint32_t)((c >> 1) & 1), 1000000000ull);
-            const uint32_t mb_drain = smem_u32(&mbar[3]);
+                (void)mbar_wait(smem_u32(&mbar[c % SC_STAGES]), (uint32_t)((c / SC_STAGES) & 1), 1000000000ull);
+            const uint32_t mb_drain = smem_u32(&mbar[SC_STAGES + 1]);
             mma_commit(mb_drain);
             (void)mbar_wait(mb_drain, 0, 1000000000ull);
         }
@@ -1021,7 +1054,7 @@ cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, cons
 {
     using namespace mp;
     const cuuint64_t BH = s.BH, T = s.T;
-    CUtensorMap mq, mk, mv, mu, ma, mqt, mb, mo;
+    CUtensorMap mq, mk, mv, mu, ma, mqt, mb, mo, mbh;
     const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     {
         cuuint64_t dims[3] = {(cuuint64_t)D, T, BH};
@@ -1048,6 +1081,7 @@ cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, cons
         if (!encode_map(&ma, F16, w.A, 2, d128, str, b128, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
         if (!encode_map(&mqt, F16, w.Q, 2, d64, str, b64, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
         if (!encode_map(&mb, F16, w.B, 2, d128, str, b128, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!encode_map(&mbh, F16, w.B, 2, d128, str, b64, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
         if (!encode_map(&mo, F16, w.O, 2, d64, str, b64, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     const unsigned long long wns = wait_ns > 0 ? (unsigned long long)wait_ns : 100000000ull;
@@ -1105,10 +1139,10 @@ cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, cons
     tm.end();
     if (e != cudaSuccess) return e;
     tm.begin("map_scan");
-    cfg.gridDim = dim3((unsigned)s.BH);
+    cfg.gridDim = dim3((unsigned)(2 * s.BH));
     cfg.blockDim = dim3(ST);
     cfg.dynamicSmemBytes = SCAN_SMEM;
-    e = cudaLaunchKernelEx(&cfg, scan_kernel, ma, mqt, mb, mout, sp);
+    e = cudaLaunchKernelEx(&cfg, scan_kernel, ma, mqt, mbh, mout, sp);
     tm.end();
     if (e != cudaSuccess) return e;
     if (a.v_hist_out) {  // a plain launch: it runs after the kernels above have read v_hist
