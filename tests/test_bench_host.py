@@ -37,7 +37,7 @@ def test_every_backward_kernel_has_algorithmic_bytes():
 def test_every_forward_kernel_has_algorithmic_bytes():
     w = WORKLOADS["seqrec_16k"]
     for n in recorded_names():
-        if n.startswith(("simt_", "tc_")):
+        if n.startswith(("simt_", "tc_", "map_")):
             assert bench.kernel_alg_bytes(n, w) > 0, n
 
 
