@@ -659,7 +659,6 @@ def run_decode(args, w):
     barrier(world)
     clocks = sampler.stop() if sampler else None
     plan.last_device_status()
-    timed_out = out.detach().cpu()  # the output of the last timed step, checked against the oracle below
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_local = sum(step_ms) / steps
     ms = max_over_ranks(ms_local, world)
@@ -767,7 +766,6 @@ def run_project(args, name):
     barrier(world)
     clocks = sampler.stop() if sampler else None
     plan.last_device_status()
-    timed_out = out.detach().cpu()  # the output of the last timed step, checked against the oracle below
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_local = sum(step_ms) / steps
     ms = max_over_ranks(ms_local, world)
@@ -913,7 +911,6 @@ def run_backward(args, w):
     barrier(world)
     clocks = sampler.stop() if sampler else None
     plan.last_device_status()
-    timed_out = out.detach().cpu()  # the output of the last timed step, checked against the oracle below
     step_ms = [a.elapsed_time(b) for a, b in ev]
     plan.set_option(Bd.PRISM_OPT_TIMING, 1)
     per_kernel, launches = {}, 0

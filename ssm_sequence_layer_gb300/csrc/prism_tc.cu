@@ -14,7 +14,7 @@
 //   combine  per sequence, S_start of segment p from S_init (or 0) and the maps of segments
 //            0..p-1 (associative combine of the input-only affine maps, notes on PRISM
 //            section 2.1); optionally the state after the last token.
-//   fixup    o = o0 + Qhat S_start^T for the chunks of the stashing segments.
+//   fixup    o = o0 + Qhat S_start^T for the chunks of the stashing segments (tcgen05, one CTA per chunk pair).
 //
 // Chunk algebra (local index i, j; lambda_i = sum_{m<=i} ln alpha_m; lc = lambda_{C-1};
 // D_ij = e^{lambda_i - lambda_j} (j <= i), colf_j = e^{lc - lambda_j} <= 1, Gamma_i = e^{lambda_i}):
@@ -262,6 +262,7 @@ __device__ __forceinline__ void tiles_bf16_to_f16(uint8_t *base, uint32_t bytes,
 // prep of one chunk (P1): anchor, gain and residual chain -> X tiles, two channels x 4 tokens per
 // thread, from V stage `stg` and the chunk's per-token scalars `pset`.  Kept out of line: the
 // segment kernel calls it at two places, and one copy of its code keeps the loop body smaller.
+template <bool kNonlinear>
 __device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __nv_bfloat162 *cw2, int stg, int R,
                                         const uint32_t *pg, int n)
 {
@@ -276,7 +277,7 @@ __device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __
     constexpr int TPT = 64 / (NT / 32);     // tokens per thread
     // the non-linear chain's gains of this thread's tokens, all loads issued before any is used
     uint32_t pz[TPT][RMAX];
-    if (pg) {
+    if constexpr (kNonlinear) {
 #pragma unroll
         for (int k = 0; k < TPT; ++k) {
             const int i = tg + (NT / 32) * k;
@@ -304,7 +305,7 @@ __device__ __noinline__ void prep_chunk(uint8_t *sm, const float *pset, const __
         gelu_gain(a1, g1, Phi1);
         float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
         uint8_t *xs = sm + OFF_XS + sw128(i, 2 * cp);
-        if (pg) {  // non-linear chain: delta = GELU(p r), x = gamma delta, r <- r - delta
+        if constexpr (kNonlinear) {  // non-linear chain: delta = GELU(p r), x = gamma delta, r <- r - delta
 #pragma unroll
             for (int l = 0; l < RMAX; ++l) {
                 if (l < R) {
@@ -518,7 +519,10 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t *pg = p.p_gain ? reinterpret_cast<const uint32_t *>(p.p_gain) +
                                             ((size_t)bh * p.T + (size_t)cc * C) * R * (D / 2)
                                       : nullptr;
-        prep_chunk(sm, sc + (cc & 1) * SC_SET, cw2, stg, R, pg, min(C, p.T - cc * C));
+        if (pg)
+            prep_chunk<true>(sm, sc + (cc & 1) * SC_SET, cw2, stg, R, pg, min(C, p.T - cc * C));
+        else
+            prep_chunk<false>(sm, sc + (cc & 1) * SC_SET, cw2, stg, R, nullptr, 0);
     };
 
 #ifdef PRISM_PHASE_TIMERS
@@ -1261,139 +1265,168 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
                                        1000000000ull);
 }
 
-// fixup: o = o0 + Qhat S_start^T for the chunks of tracked segments, one CTA of 4 warps per chunk
-// (many chunks in flight per SM).  Qhat, S_start (fp16) and o0 are copied into padded
-// shared-memory rows with 16-byte cp.async (coalesced, no register staging); the 64x64x64
-// product runs on mma.sync m16n8k16 (fp16 in, fp32 accumulate) with A = Qhat [i][m],
-// B[m][c] = S_start[c][m] and C initialised with o0; the result goes back over o0's rows and
-// leaves as coalesced 16-byte stores.  Warp w owns rows 16 w .. 16 w + 15 and all 64 columns.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
+// fixup: o = o0 + Qhat S_start^T for the chunks of tracked segments, on tcgen05: one CTA of 4 warps
+// (one per tensor-memory lane quarter) per pair of consecutive chunks of a segment, several CTAs
+// per SM.  A = [Qhat_c; Qhat_{c+1}] (128 token rows, K-major) and B = S_start (fp16 [c][m]) come by
+// TMA; one product M = 128, N = 64, K = 64; o0 is added in the epilogue (thread = token row) and a
+// bf16 result leaves by TMA stores, an fp32 one by 16-byte stores.
+constexpr int FX_THREADS = 128;
+constexpr uint32_t FX_PANEL = 8192;
+constexpr uint32_t FX_OFF_S = 0;                      // S_start [64][64] fp16
+constexpr uint32_t FX_OFF_Q = FX_PANEL;               // [Qhat_c; Qhat_{c+1}] [128][64] fp16
+constexpr uint32_t FX_OFF_OUT = FX_OFF_Q + 2 * FX_PANEL;  // output tile [128][64] bf16
+constexpr uint32_t FX_SMEM = FX_OFF_OUT + 2 * FX_PANEL + 1024;
 
-__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
-}
+struct FixParams {
+    const void *stash_o;  // [BH][NC][64][64] o0 (fp16, or fp32 with out_f32)
+    void *out;
+    int *status;
+    int T, NC, P, out_f32, has_init;
+    unsigned long long wait_ns;
+};
 
-constexpr int FX_LDH = 72;  // row stride (halves) of the fp16 tiles: conflict-free fragment reads
-constexpr int FX_LDF = 72;  // row stride (floats) of the fp32 o0 tile
-
-__global__ void __launch_bounds__(128) fixup_kernel(const void *__restrict__ stash_o, const __half *__restrict__ stash_q,
-                                                    const __half *__restrict__ sstart, void *__restrict__ out,
-                                                    int out_f32, int T, int NC, int P, int has_init)
+__global__ void __launch_bounds__(FX_THREADS)
+    fixup_kernel(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_qh,
+                 const __grid_constant__ CUtensorMap tm_out, FixParams p)
 {
-    __shared__ __align__(16) __half Qs[64 * FX_LDH];             // Qhat [i][m]
-    __shared__ __align__(16) __half Ss[64 * FX_LDH];             // S_start [c][m]
-    __shared__ __align__(16) float Os[64 * FX_LDF];              // o0 / out [i][c] (fp32, or fp16 in the first half)
-    const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
-    // segment of chunk c: the largest p with begin(p) <= c
-    int seg = (int)(((long long)c * P) / NC);
-    while (seg + 1 < P && ((long long)(seg + 1) * NC) / P <= c) ++seg;
-    while (seg > 0 && ((long long)seg * NC) / P > c) --seg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint32_t tmem_base_s;
+    __shared__ __align__(8) uint64_t mbar[3];  // 0: tiles; 1: product; 2: drain
+    __shared__ int abort_s;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int bh = blockIdx.x / p.P, seg = blockIdx.x % p.P, k = blockIdx.y;  // pair k of the segment
+    const int c_begin = (int)(((long long)seg * p.NC) / p.P), c_end = (int)(((long long)(seg + 1) * p.NC) / p.P);
+    const int c0 = c_begin + 2 * k;
+    if ((seg == 0 && !p.has_init) || c0 >= c_end) {  // segment 0 is written by the segment kernel
+        grid_dependency_wait();
+        allow_dependent_launch();
+        return;
+    }
+    const uint32_t sbase = smem_u32(sm);
+    const uint64_t dbase = sdesc(sbase, 0, 0);
+    const uint32_t mb_t = smem_u32(&mbar[0]), mb_mma = smem_u32(&mbar[1]);
+    if (tid == 0) {
+        abort_s = 0;
+        for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&mbar[i]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 64);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_base_s;
     grid_dependency_wait();  // the stash of the segment kernel and S_start of the combine
     allow_dependent_launch();
-    if (seg == 0 && !has_init) return;  // written directly by the segment kernel
-    const size_t chunk = (size_t)bh * NC + c;
-    const int t0 = c * 64, n = min(64, T - t0);
-    {
-        const __half *gq = stash_q + chunk * 4096;
-        const __half *gs = sstart + ((size_t)bh * P + seg) * 4096;
+
+    const size_t ch0 = (size_t)bh * p.NC;
+    bool loads_pending = false;
+    if (tid == 0) {
+        mbar_expect_tx(mb_t, 3 * FX_PANEL);
+        tma_load_2d(sbase + FX_OFF_S, &tm_s, mb_t, 0, (int)(((size_t)bh * p.P + seg) * 64));
+        tma_load_2d(sbase + FX_OFF_Q, &tm_qh, mb_t, 0, (int)((ch0 + c0) * 64));
+        loads_pending = true;
+    }
+    // o0 of this thread's row while the tiles load
+    const int r = tid, chunk = c0 + (r >> 6), i = r & 63;
+    const bool valid = chunk < c_end && chunk * 64 + i < p.T;
+    float o[64];
+    if (valid) {
+        const size_t base = ((ch0 + chunk) * 64 + i) * 64;
+        if (p.out_f32) {
+            const float4 *src = reinterpret_cast<const float4 *>(p.stash_o) + base / 4;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // 512 16-byte groups per tile: row e >> 3, group e & 7
-            const int e = tid + 128 * k, r = e >> 3, g = (e & 7) * 8;
-            cp_async16(Qs + r * FX_LDH + g, gq + r * 64 + g);
-            cp_async16(Ss + r * FX_LDH + g, gs + r * 64 + g);
-        }
-        if (out_f32) {
-            const float *go = reinterpret_cast<const float *>(stash_o) + chunk * 4096;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int e = tid + 128 * k, r = e >> 4, g = (e & 15) * 4;
-                cp_async16(Os + r * FX_LDF + g, go + r * 64 + g);
+            for (int e = 0; e < 16; ++e) {
+                const float4 v = src[e];
+                o[4 * e] = v.x;
+                o[4 * e + 1] = v.y;
+                o[4 * e + 2] = v.z;
+                o[4 * e + 3] = v.w;
             }
         } else {
-            const __half *go = reinterpret_cast<const __half *>(stash_o) + chunk * 4096;
-            __half *oh = reinterpret_cast<__half *>(Os);
+            const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __half *>(p.stash_o) + base);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int e = tid + 128 * k, r = e >> 3, g = (e & 7) * 8;
-                cp_async16(oh + r * FX_LDH + g, go + r * 64 + g);
+            for (int e = 0; e < 8; ++e) {
+                const uint4 w = src[e];
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[h2]));
+                    o[8 * e + 2 * h2] = f.x;
+                    o[8 * e + 2 * h2 + 1] = f.y;
+                }
             }
         }
-        asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     }
-    __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-    const int i0 = 16 * warp + gq, i1 = i0 + 8;
-    uint32_t a[4][4];
+    if (tid == 0) {
+        if (mbar_wait(mb_t, 0, p.wait_ns)) {
+            loads_pending = false;
+            fence_after_sync();
+            const uint32_t id = idesc_f16(128, 64, 0, 0);
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-        a[ks][0] = *reinterpret_cast<const uint32_t *>(Qs + i0 * FX_LDH + 16 * ks + 2 * tq);
-        a[ks][1] = *reinterpret_cast<const uint32_t *>(Qs + i1 * FX_LDH + 16 * ks + 2 * tq);
-        a[ks][2] = *reinterpret_cast<const uint32_t *>(Qs + i0 * FX_LDH + 16 * ks + 2 * tq + 8);
-        a[ks][3] = *reinterpret_cast<const uint32_t *>(Qs + i1 * FX_LDH + 16 * ks + 2 * tq + 8);
-    }
-    __half *oh = reinterpret_cast<__half *>(Os);
-    float acc[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-        const int cc = 8 * nt + 2 * tq;
-        float2 o0, o1;
-        if (out_f32) {
-            o0 = *reinterpret_cast<const float2 *>(Os + i0 * FX_LDF + cc);
-            o1 = *reinterpret_cast<const float2 *>(Os + i1 * FX_LDF + cc);
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem, dsc(dbase, FX_OFF_Q + s * 32, 16, 1024), dsc(dbase, FX_OFF_S + s * 32, 16, 1024), id, s > 0);
+            mma_commit(mb_mma);
         } else {
-            o0 = __half22float2(*reinterpret_cast<const __half2 *>(oh + i0 * FX_LDH + cc));
-            o1 = __half22float2(*reinterpret_cast<const __half2 *>(oh + i1 * FX_LDH + cc));
-        }
-        acc[nt][0] = o0.x;
-        acc[nt][1] = o0.y;
-        acc[nt][2] = o1.x;
-        acc[nt][3] = o1.y;
-    }
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const int cn = 8 * nt + gq;
-            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(Ss + cn * FX_LDH + 16 * ks + 2 * tq);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(Ss + cn * FX_LDH + 16 * ks + 2 * tq + 8);
-            mma_f16_16816(acc[nt], a[ks], b0, b1);
-        }
-    // the result replaces o0 at the same positions (each position is read and written by one
-    // thread), in the output's element type
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-        const int cc = 8 * nt + 2 * tq;
-        if (out_f32) {
-            *reinterpret_cast<float2 *>(Os + i0 * FX_LDF + cc) = make_float2(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<float2 *>(Os + i1 * FX_LDF + cc) = make_float2(acc[nt][2], acc[nt][3]);
-        } else {
-            *reinterpret_cast<__nv_bfloat162 *>(oh + i0 * FX_LDH + cc) = __floats2bfloat162_rn(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<__nv_bfloat162 *>(oh + i1 * FX_LDH + cc) = __floats2bfloat162_rn(acc[nt][2], acc[nt][3]);
+            abort_s = 1;
+            set_status(p.status, kDevTimeout);
         }
     }
     __syncthreads();
-    if (out_f32) {
-        float *go = reinterpret_cast<float *>(out) + ((size_t)bh * T + t0) * 64;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int e = tid + 128 * k, r = e >> 4, g = (e & 15) * 4;
-            if (r < n) *reinterpret_cast<float4 *>(go + r * 64 + g) = *reinterpret_cast<const float4 *>(Os + r * FX_LDF + g);
+    if (abort_s == 0) {
+        if (!mbar_wait(mb_mma, 0, p.wait_ns)) {
+            abort_s = 1;
+            set_status(p.status, kDevTimeout);
         }
-    } else {
-        __nv_bfloat16 *go = reinterpret_cast<__nv_bfloat16 *>(out) + ((size_t)bh * T + t0) * 64;
+        fence_after_sync();
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int e = tid + 128 * k, r = e >> 3, g = (e & 7) * 8;
-            if (r < n) *reinterpret_cast<uint4 *>(go + r * 64 + g) = *reinterpret_cast<const uint4 *>(oh + r * FX_LDH + g);
+        for (int g = 0; g < 2; ++g) {
+            float v[32];
+            tmem_ld(tmem + lane_off + (uint32_t)(32 * g), v);
+            if (!valid) continue;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] += o[32 * g + q];
+            if (p.out_f32) {
+                float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) +
+                                                         ((size_t)bh * p.T + (size_t)chunk * 64 + i) * 64 + 32 * g);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+                uint8_t *op = sm + FX_OFF_OUT + (uint32_t)(r >> 6) * FX_PANEL;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+                        w[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    *reinterpret_cast<uint4 *>(op + sw128(i, 32 * g + 8 * q)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+        fence_async_smem();
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        if (!p.out_f32 && abort_s == 0) {  // the TMA store drops rows past T
+            tma_store_3d(&tm_out, sbase + FX_OFF_OUT, 0, c0 * 64, bh);
+            if (c0 + 1 < c_end) tma_store_3d(&tm_out, sbase + FX_OFF_OUT + FX_PANEL, 0, (c0 + 1) * 64, bh);
+            bulk_commit();
+        }
+        bulk_wait_all();
+        if (abort_s) {  // drain after an expired wait
+            if (loads_pending) (void)mbar_wait(mb_t, 0, 1000000000ull);
+            const uint32_t mb_drain = smem_u32(&mbar[2]);
+            mma_commit(mb_drain);
+            (void)mbar_wait(mb_drain, 0, 1000000000ull);
         }
     }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
 }  // namespace tc
@@ -1416,12 +1449,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode()
 }
 
 bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides_bytes,
-            const cuuint32_t *box, CUtensorMapSwizzle sw)
+            const cuuint32_t *box, CUtensorMapSwizzle sw,
+            CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
 {
     auto fn = get_encode();
     if (!fn) return false;
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides_bytes, box,
+    return fn(m, dt, (cuuint32_t)rank, const_cast<void *>(base), dims, strides_bytes, box,
               es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1467,6 +1501,8 @@ void tc_carve(const Shape &s, int P, void *base, TcWorkspace *w)
 cudaError_t tc_prepare()
 {
     cudaError_t e = cudaFuncSetAttribute(tc::segment_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tc::fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::FX_SMEM);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(tc::combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::CB_SMEM);
 }
@@ -1544,12 +1580,38 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
     }
     if (w.P > 1 || a.S_init) {
         tm.begin("tc_fixup");
-        cfg.gridDim = dim3(s.NC, s.BH);
-        cfg.blockDim = dim3(128);
-        cfg.dynamicSmemBytes = 0;
-        e = cudaLaunchKernelEx(&cfg, fixup_kernel, (const void *)w.stash_o, (const __half *)w.stash_q,
-                               (const __half *)w.sstart, a.out, (int)p.out_f32, (int)s.T, (int)s.NC, (int)w.P,
-                               p.has_init);
+        CUtensorMap ms, mqh, mo;
+        {
+            cuuint64_t str[1] = {(cuuint64_t)D * 2};
+            cuuint64_t dS[2] = {(cuuint64_t)D, (cuuint64_t)s.BH * w.P * 64}, dQ[2] = {(cuuint64_t)D, (cuuint64_t)s.BH * s.NC * 64};
+            cuuint32_t b64[2] = {64, 64}, b128[2] = {64, 128};
+            if (!encode(&ms, w.sstart, 2, dS, str, b64, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
+                !encode(&mqh, w.stash_q, 2, dQ, str, b128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
+                return cudaErrorInvalidValue;
+            if (out_f32) {
+                mo = mqh;  // not read: an fp32 output is written directly
+            } else {
+                cuuint64_t dims[3] = {(cuuint64_t)D, T, BH};
+                cuuint64_t ostr[2] = {(cuuint64_t)D * 2, T * D * 2};
+                cuuint32_t box[3] = {64, 64, 1};
+                if (!encode(&mo, a.out, 3, dims, ostr, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+            }
+        }
+        FixParams fp;
+        fp.stash_o = w.stash_o;
+        fp.out = a.out;
+        fp.status = d_status;
+        fp.T = s.T;
+        fp.NC = s.NC;
+        fp.P = w.P;
+        fp.out_f32 = p.out_f32;
+        fp.has_init = p.has_init;
+        fp.wait_ns = p.wait_ns;
+        const int max_pairs = (s.NC / w.P + 2) / 2;  // chunk pairs of the longest segment
+        cfg.gridDim = dim3(s.BH * w.P, max_pairs);
+        cfg.blockDim = dim3(FX_THREADS);
+        cfg.dynamicSmemBytes = FX_SMEM;
+        e = cudaLaunchKernelEx(&cfg, fixup_kernel, ms, mqh, mo, fp);
         tm.end();
         if (e != cudaSuccess) return e;
     }
