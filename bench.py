@@ -127,6 +127,9 @@ KERNEL_SOURCES = {
     "map_": ("prism_map.cu", "tc_util.h", "tc_ptx.h", "prism_internal.h"),
     "decode": ("prism_state.cu", "tc_ptx.h", "prism_internal.h"),
     "simt_": ("prism_simt.cu", "prism_internal.h"),
+    "bwd_maps": ("prism_bwd_tc.cu", "tc_util.h", "tc_ptx.h", "prism_internal.h"),
+    "bwd_chunk": ("prism_bwd_tc.cu", "tc_util.h", "tc_ptx.h", "prism_internal.h"),
+    "bwd_grad": ("prism_bwd_tc.cu", "tc_util.h", "tc_ptx.h", "prism_internal.h"),
     "bwd_": ("prism_backward.cu", "prism_internal.h"),
 }
 
@@ -823,8 +826,10 @@ BWD_KEYS = ("q", "k", "v", "beta", "alpha", "u", "gamma", "eta", "conv_w")
 
 def backward_kernel_bytes(name, w):
     """Bytes a backward kernel must move at minimum for one launch over the workload: each of
-    its inputs read once and each of its outputs written once, the per-token states S_{t-1} and
-    cotangents dS_t of the design included (fp32, dv dk floats per token each)."""
+    its inputs read once and each of its outputs written once, the intermediates of the design
+    included (token-serial form: the per-token states S_{t-1} and cotangents dS_t, fp32, dv dk
+    floats per token each; chunked form: four fp32 chunk maps, the chunk states and cotangents,
+    and the fp16 stash of 5 + R tiles per chunk, plus Vt and z)."""
     io = 2 if w.dtype == "bf16" else 4
     th = w.B * w.H * w.T
     R = w.R
@@ -836,7 +841,17 @@ def backward_kernel_bytes(name, w):
     state = th * w.dv * w.dk * 4
     per_row = th * w.dv * 4  # z, dout, dh or a dv-sized fp32 cotangent
     ntile = -(-w.T // 64)
+    chunks = w.B * w.H * ntile
+    dd = w.dk * w.dv * 4
+    tile = 64 * w.dv * 2
+    gates = th * 4 * (2 + 2 * R)
     table = {
+        "bwd_maps": 2 * qk + v + u + gates + per_row + 4 * chunks * dd + chunks * (5 + R) * tile,
+        "bwd_chunk_scan": 4 * chunks * dd + (2 * chunks + w.B * w.H) * dd,
+        "bwd_grad_a": 2 * qk + v + u + gates + per_row + 2 * chunks * dd + chunks * (5 + R) * tile
+        + per_row + dX + th * 8 + 2 * chunks * tile,
+        "bwd_grad_b": 2 * qk + u + gates + per_row + (2 + R) * chunks * tile + 3 * chunks * dd + th * 4
+        + 2 * th * w.dk * 4 + th * R * w.dk * 4 + th * 4,
         "bwd_factors": v + th * 8 * R + X,
         # both halves of the scan launch: S_{t-1} forward, dS_t (with z, dx) in reverse
         "bwd_scan": (qk + v + u + gates2 + X + state) + (2 * qk + u + gates2 + per_row + state + per_row + dX),

@@ -255,10 +255,20 @@ PRISM_API prism_status prism_project(prism_plan_t plan, int D, const void *X, co
  * With L = 1, u, gamma, eta, du, dgamma and deta are not touched (dconv_w and dv_hist are 0).
  * dout, dS_final, dq, dk, dv, du, dv_hist and dS_init start on 16-byte boundaries; dbeta,
  * dalpha, dgamma, deta and dconv_w on 4.  No output overlaps another buffer.
- * The pass computes in fp32 from the io values.  It keeps S_{t-1} and dS_t of every token in
- * a workspace owned by the plan (2 B H T dv dk floats plus small per-token buffers, reported by
- * prism_workspace_bytes), allocated by the first call, so make that call before capturing a
- * stream.  Returns once the work is enqueued on `stream`.
+ * Two forms compute this.
+ *   Chunked (bf16 io, dk = dv = 64, L <= 4; taken unless PRISM_OPT_PATH = 1): the state entering
+ *     every 64-token chunk and the cotangent flowing into every chunk's last state come from
+ *     chunk-level recurrences S_{c+1} = S_c A_c + B_c and G_{c-1} = G_c A_c^T + Bbar_c whose maps
+ *     depend on the chunk's inputs only (notes on PRISM, section 2.1; the transition of section
+ *     2.2 is symmetric, so the cotangent runs through A_c^T); every per-token cotangent of a chunk
+ *     is then a set of chunk-sized products (tcgen05 tensor cores, fp16 operands, fp32
+ *     accumulation), the WY factors of the forward reused.  Workspace: per-chunk maps, states and
+ *     factors, O(B H ceil(T/64) dv dk) -- about 0.5 GB for B H T = 131072 tokens of heads of 64.
+ *   Token-serial (every other shape, and PRISM_OPT_PATH = 1): fp32 from the io values, keeping
+ *     S_{t-1} and dS_t of every token (2 B H T dv dk floats plus per-token buffers).
+ * The workspace is owned by the plan (prism_workspace_bytes reports it) and allocated by the first
+ * call of a form, so make that call before capturing a stream.  Returns once the work is enqueued
+ * on `stream`; a bounded device wait that runs out is reported by prism_plan_last_device_status.
  */
 PRISM_API prism_status prism_backward(prism_plan_t plan, const void *q, const void *k, const void *v,
                                       const float *beta, const float *alpha, const void *u, const float *gamma,

@@ -255,6 +255,7 @@ prism_status prism_plan(int B, int H, int T, int dk, int dv, int L, prism_dtype 
     if (e == cudaSuccess && prism::map_supported(s, io)) e = prism::map_prepare();
     if (e == cudaSuccess && io == PRISM_BF16) e = prism::project_prepare();
     if (e == cudaSuccess) e = prism::backward_prepare();
+    if (e == cudaSuccess) e = prism::backward_tc_prepare();
     if (e != cudaSuccess) {
         delete p;
         return cuda_fail(e, "kernel attribute setup");
@@ -460,8 +461,17 @@ prism_status prism_backward(prism_plan_t p, const void *q, const void *k, const 
     for (int i = 0; i < 5; ++i)
         if (fp[i] && !aligned(fp[i], 4)) return fail(PRISM_ERR_MISALIGNED, "%s is not 4-byte aligned", fn[i]);
     if ((st = check_plan_device(p)) != PRISM_OK) return st;
+    // the chunked tensor-core form wherever it applies, unless the portable kernels are asked for
+    const bool chunked = p->opt_path != 1 && prism::backward_tc_supported(p->shape, p->io);
+    const size_t bytes =
+        chunked ? prism::backward_tc_workspace_bytes(p->shape) : prism::backward_workspace_bytes(p->shape);
+    if (p->ws_bwd && p->ws_bwd_bytes < bytes) {
+        cudaError_t e = cudaFree(p->ws_bwd);
+        p->ws_bwd = nullptr;
+        p->ws_bwd_bytes = 0;
+        if (e != cudaSuccess) return cuda_fail(e, "backward workspace release");
+    }
     if (!p->ws_bwd) {
-        const size_t bytes = prism::backward_workspace_bytes(p->shape);
         cudaError_t e = cudaMalloc(&p->ws_bwd, bytes);
         if (e != cudaSuccess) {
             p->ws_bwd = nullptr;
@@ -475,7 +485,8 @@ prism_status prism_backward(prism_plan_t p, const void *q, const void *k, const 
                           dS_init};
     p->timer.on = p->opt_timing != 0;
     p->timer.reset((cudaStream_t)stream);
-    const cudaError_t e = prism::backward(p->shape, p->io, a, p->ws_bwd, p->timer);
+    const cudaError_t e = chunked ? prism::backward_tc(p->shape, a, p->ws_bwd, p->d_status, p->opt_wait_ns, p->timer)
+                                  : prism::backward(p->shape, p->io, a, p->ws_bwd, p->timer);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return PRISM_OK;
 }

@@ -626,73 +626,108 @@ __global__ void __launch_bounds__(NT) token_grad_kernel(const io_t *__restrict__
     }
 }
 
-// The residual chain and the gain backwards, one block of NT threads over NT / dv tokens.
+// The residual chain and the gain backwards, one warp per token, lane c handling the channel
+// pairs 2 (c + 32 k), k < CPL (CPL = dv / 64); every load of the token is issued before the
+// arithmetic; the per-level sums over channels (dgamma, deta) are warp reductions.
 template <typename io_t>
+__device__ __forceinline__ float2 ld2(const io_t *p);
+template <>
+__device__ __forceinline__ float2 ld2<float>(const float *p)
+{
+    return *reinterpret_cast<const float2 *>(p);
+}
+template <>
+__device__ __forceinline__ float2 ld2<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+}
+
+template <typename io_t, int CPL, int RM>
 __global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
                                                         const io_t *__restrict__ conv_w,
                                                         const float *__restrict__ gamma,
                                                         const float *__restrict__ eta, const float *__restrict__ dX,
                                                         float *__restrict__ dH, float *__restrict__ dv_out,
                                                         float *__restrict__ dgamma, float *__restrict__ deta,
-                                                        long long ntok, int H, int T, int dv, int R)
+                                                        long long ntok, int H, int T, int R)
 {
-    __shared__ float red[NT / 32][2 * RMAX];
-    const int tpb = NT / dv;
-    const int slot = threadIdx.x / dv, c = threadIdx.x % dv;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, wpt = dv / 32;  // warps per token
-    for (long long base = (long long)blockIdx.x * tpb; base < ntok; base += (long long)gridDim.x * tpb) {
-        const long long tok = base + slot;
-        const bool live = tok < ntok;  // uniform over a warp (dv is a multiple of 32)
-        float dgam[RMAX], det[RMAX];
+    constexpr int dv = 64 * CPL;
+    const int lane = threadIdx.x & 31;
+    const long long tok = (long long)blockIdx.x * (NT / 32) + (threadIdx.x >> 5);
+    if (tok >= ntok) return;
+    const int bh = (int)(tok / T), t = (int)(tok % T), h = bh % H;
+    float gm[RM], et[RM];
 #pragma unroll
-        for (int l = 0; l < RMAX; ++l) dgam[l] = det[l] = 0.f;
-        if (live) {
-            const int bh = (int)(tok / T), t = (int)(tok % T);
-            float a, Phi, phi;
-            anchor_at(v, v_hist, conv_w, bh, bh % H, t, T, dv, c, a, Phi, phi);
+    for (int l = 0; l < RM; ++l) {
+        // the last level's gain shapes nothing (the cotangent of r_{t,R+1} is zero)
+        gm[l] = l < R ? gamma[(size_t)tok * R + l] : 0.f;
+        et[l] = l + 1 < R ? eta[(size_t)tok * R + l] : 0.f;
+    }
+    float2 vv[CPL][4], w[CPL][4], dxv[CPL][RM];
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        const int c = 2 * (lane + 32 * k);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            w[k][j] = ld2(conv_w + ((size_t)h * 4 + j) * dv + c);
+            vv[k][j] = make_float2(0.f, 0.f);
+            if (t - j >= 0) vv[k][j] = ld2(v + ((size_t)bh * T + t - j) * dv + c);
+            else if (v_hist) vv[k][j] = ld2(v_hist + ((size_t)bh * 3 + 3 + t - j) * dv + c);
+        }
+#pragma unroll
+        for (int l = 0; l < RM; ++l)
+            if (l < R) dxv[k][l] = *reinterpret_cast<const float2 *>(dX + ((size_t)tok * R + l) * dv + c);
+    }
+    float dgam[RM], det[RM];
+#pragma unroll
+    for (int l = 0; l < RM; ++l) dgam[l] = det[l] = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        const int c = 2 * (lane + 32 * k);
+        float drn2[2], dh2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float a = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a = fmaf(e ? w[k][j].y : w[k][j].x, e ? vv[k][j].y : vv[k][j].x, a);
+            const float Phi = 0.5f * erfcf(-a * 0.70710678118654752f);
+            const float phi = 0.39894228040143268f * expf(-0.5f * a * a);
             const float g = fmaf(a, phi, Phi);
-            float rl[RMAX];
-            float r = ldf(v + (size_t)tok * dv + c) - a * Phi;
+            float rl[RM];
+            float r = (e ? vv[k][0].y : vv[k][0].x) - a * Phi;
 #pragma unroll
-            for (int l = 0; l < RMAX; ++l)
+            for (int l = 0; l < RM; ++l)
                 if (l < R) {
                     rl[l] = r;
-                    if (l + 1 < R) r *= 1.f - eta[(size_t)tok * R + l] * g;
+                    r *= 1.f - et[l] * g;
                 }
             float drn = 0.f, dg = 0.f;
 #pragma unroll
-            for (int l = RMAX - 1; l >= 0; --l)
+            for (int l = RM - 1; l >= 0; --l)
                 if (l < R) {
-                    // the last level's gain shapes nothing (the cotangent of r_{t,R+1} is zero)
-                    const float gm = gamma[(size_t)tok * R + l], et = l + 1 < R ? eta[(size_t)tok * R + l] : 0.f;
-                    const float dx = dX[((size_t)tok * R + l) * dv + c];
-                    dgam[l] = g * rl[l] * dx;
-                    det[l] = -g * rl[l] * drn;
-                    dg += gm * rl[l] * dx - et * rl[l] * drn;
-                    drn = gm * g * dx + (1.f - et * g) * drn;
+                    const float dx = e ? dxv[k][l].y : dxv[k][l].x;
+                    dgam[l] = fmaf(g * rl[l], dx, dgam[l]);
+                    det[l] = fmaf(-g * rl[l], drn, det[l]);
+                    dg += gm[l] * rl[l] * dx - et[l] * rl[l] * drn;
+                    drn = gm[l] * g * dx + (1.f - et[l] * g) * drn;
                 }
-            dv_out[(size_t)tok * dv + c] += drn;
-            dH[(size_t)tok * dv + c] = -g * drn + phi * (2.f - a * a) * dg;
+            drn2[e] = drn;
+            dh2[e] = -g * drn + phi * (2.f - a * a) * dg;
         }
-#pragma unroll
-        for (int l = 0; l < RMAX; ++l)
-            if (l < R) {
-                const float s1 = warp_sum(dgam[l]), s2 = warp_sum(det[l]);
-                if (lane == 0) {
-                    red[wid][2 * l] = s1;
-                    red[wid][2 * l + 1] = s2;
-                }
-            }
-        __syncthreads();
-        if (live && c < 2 * R) {
-            float s = 0.f;
-            for (int w = 0; w < wpt; ++w) s += red[slot * wpt + w][c];
-            const int l = c >> 1;
-            if (c & 1) deta[(size_t)tok * R + l] = s;
-            else dgamma[(size_t)tok * R + l] = s;
-        }
-        __syncthreads();
+        float2 *dvp = reinterpret_cast<float2 *>(dv_out + (size_t)tok * dv + c);
+        const float2 old = *dvp;
+        *dvp = make_float2(old.x + drn2[0], old.y + drn2[1]);
+        *reinterpret_cast<float2 *>(dH + (size_t)tok * dv + c) = make_float2(dh2[0], dh2[1]);
     }
+#pragma unroll
+    for (int l = 0; l < RM; ++l)
+        if (l < R) {
+            const float s1 = warp_sum(dgam[l]), s2 = warp_sum(det[l]);
+            if (lane == 0) {
+                dgamma[(size_t)tok * R + l] = s1;
+                deta[(size_t)tok * R + l] = s2;
+            }
+        }
 }
 
 // The convolution backwards over tiles of CT tokens: v's share of dv, dv_hist (first tile)
@@ -770,6 +805,35 @@ size_t carve(const Shape &s, void *base, Carve *out)
     return off;
 }
 
+// The token-local tail of the backward, given dX (the cotangents of the injection factors) and dv
+// holding beta z: the residual chain and gain backwards (dv, dgamma, deta, dH), then the
+// convolution backwards (v's share of dv, dv_hist, dconv_w).
+template <typename io_t>
+cudaError_t token_local(const Shape &s, const BackwardArgs &a, float *dX, float *dH, float *dWp, KernelTimer &tm)
+{
+    cudaStream_t st = tm.stream;
+    const io_t *v = static_cast<const io_t *>(a.v);
+    const io_t *cw = static_cast<const io_t *>(a.conv_w), *vh = static_cast<const io_t *>(a.v_hist);
+    const long long ntok = (long long)s.BH * s.T;
+    const int ntile = (s.T + CT - 1) / CT;
+    const long long cg_grid = (ntok + NT / 32 - 1) / (NT / 32);  // one warp per token
+    tm.begin("bwd_chain_grad");
+    // the level arrays sized for L <= 4 or for the largest L (registers)
+    auto kern = s.dv == 64 ? (s.R <= 3 ? chain_grad_kernel<io_t, 1, 3> : chain_grad_kernel<io_t, 1, RMAX>)
+                           : (s.R <= 3 ? chain_grad_kernel<io_t, 2, 3> : chain_grad_kernel<io_t, 2, RMAX>);
+    kern<<<(unsigned)cg_grid, NT, 0, st>>>(v, vh, cw, a.gamma, a.eta, dX, dH, a.dv, a.dgamma, a.deta, ntok, s.H, s.T,
+                                           s.R);
+    tm.end();
+    tm.begin("bwd_conv_grad");
+    conv_grad_kernel<io_t><<<dim3(ntile, s.BH), s.dv, 0, st>>>(v, vh, cw, dH, a.dv, a.dv_hist, dWp, s.H, s.T, s.dv,
+                                                               ntile);
+    tm.end();
+    tm.begin("bwd_conv_reduce");
+    conv_reduce_kernel<<<(s.H * 4 * s.dv + NT - 1) / NT, NT, 0, st>>>(dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
+    tm.end();
+    return cudaGetLastError();
+}
+
 template <typename io_t, int DK>
 cudaError_t launch(const Shape &s, const BackwardArgs &a, void *ws, KernelTimer &tm)
 {
@@ -780,7 +844,6 @@ cudaError_t launch(const Shape &s, const BackwardArgs &a, void *ws, KernelTimer 
     const io_t *v = static_cast<const io_t *>(a.v), *u = static_cast<const io_t *>(a.u);
     const io_t *cw = static_cast<const io_t *>(a.conv_w), *vh = static_cast<const io_t *>(a.v_hist);
     const long long ntok = (long long)s.BH * s.T;
-    const int ntile = (s.T + CT - 1) / CT;
     if (s.R > 0) {
         tm.begin("bwd_factors");
         factors_kernel<io_t><<<dim3((unsigned)(((long long)s.T * s.dv + NT - 1) / NT), s.BH), NT, 0, st>>>(
@@ -810,21 +873,7 @@ cudaError_t launch(const Shape &s, const BackwardArgs &a, void *ws, KernelTimer 
                                                                      w.Z, a.dout, a.dq, a.dk, a.dv, a.dbeta,
                                                                      a.dalpha, a.du, ntok, s.dv, s.R);
     tm.end();
-    const int tpb = NT / s.dv;
-    long long cg_grid = (ntok + tpb - 1) / tpb;
-    if (cg_grid > (1LL << 30)) cg_grid = 1LL << 30;
-    tm.begin("bwd_chain_grad");
-    chain_grad_kernel<io_t><<<(unsigned)cg_grid, NT, 0, st>>>(v, vh, cw, a.gamma, a.eta, w.dX, w.dH, a.dv, a.dgamma,
-                                                              a.deta, ntok, s.H, s.T, s.dv, s.R);
-    tm.end();
-    tm.begin("bwd_conv_grad");
-    conv_grad_kernel<io_t><<<dim3(ntile, s.BH), s.dv, 0, st>>>(v, vh, cw, w.dH, a.dv, a.dv_hist, w.dWp, s.H, s.T,
-                                                               s.dv, ntile);
-    tm.end();
-    tm.begin("bwd_conv_reduce");
-    conv_reduce_kernel<<<(s.H * 4 * s.dv + NT - 1) / NT, NT, 0, st>>>(w.dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
-    tm.end();
-    return cudaGetLastError();
+    return token_local<io_t>(s, a, w.dX, w.dH, w.dWp, tm);
 }
 
 template <typename io_t, int DK>
@@ -861,6 +910,15 @@ cudaError_t backward(const Shape &s, prism_dtype io, const BackwardArgs &a, void
     if (io == PRISM_BF16)
         return s.dk == 64 ? bwd::launch<__nv_bfloat16, 64>(s, a, ws, tm) : bwd::launch<__nv_bfloat16, 128>(s, a, ws, tm);
     return s.dk == 64 ? bwd::launch<float, 64>(s, a, ws, tm) : bwd::launch<float, 128>(s, a, ws, tm);
+}
+
+int backward_conv_tiles(int T) { return (T + bwd::CT - 1) / bwd::CT; }
+
+cudaError_t backward_token_local(const Shape &s, prism_dtype io, const BackwardArgs &a, float *dX, float *dH,
+                                 float *dWp, KernelTimer &tm)
+{
+    return io == PRISM_BF16 ? bwd::token_local<__nv_bfloat16>(s, a, dX, dH, dWp, tm)
+                            : bwd::token_local<float>(s, a, dX, dH, dWp, tm);
 }
 
 }  // namespace prism

@@ -131,9 +131,22 @@ struct BackwardArgs {
     const float *beta, *alpha, *gamma, *eta, *S_init, *dout, *dS_final;
     float *dq, *dk, *dv, *dbeta, *dalpha, *du, *dgamma, *deta, *dconv_w, *dv_hist, *dS_init;
 };
+// token-serial backward (every shape): per-token states and cotangents in the workspace
 size_t backward_workspace_bytes(const Shape &s);
 cudaError_t backward_prepare();
 cudaError_t backward(const Shape &s, prism_dtype io, const BackwardArgs &a, void *ws, KernelTimer &tm);
+// the token-local tail shared by both backward forms (prism_backward.cu): chain, gain and convolution
+// backwards from dX [BH T][R][dv] and dv = beta z; dH [BH T][dv] and dWp are scratch
+int backward_conv_tiles(int T);
+cudaError_t backward_token_local(const Shape &s, prism_dtype io, const BackwardArgs &a, float *dX, float *dH,
+                                 float *dWp, KernelTimer &tm);
+// chunked backward on the tensor cores (prism_bwd_tc.cu; bf16 io, dk = dv = 64, L <= 4): per-chunk
+// maps, a chunk-level scan of the states and cotangents, per-chunk cotangent products
+bool backward_tc_supported(const Shape &s, prism_dtype io);
+size_t backward_tc_workspace_bytes(const Shape &s);
+cudaError_t backward_tc_prepare();
+cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_status, long long wait_ns,
+                        KernelTimer &tm);
 
 size_t simt_workspace_bytes(const Shape &s);
 void simt_carve(const Shape &s, void *base, SimtWorkspace *w);

@@ -1,6 +1,7 @@
-"""GPU parity of prism_backward against the fp64 backward oracle on the same seeded inputs.
+"""GPU parity of prism_backward's token-serial form (PRISM_OPT_PATH = 1, every shape) against the
+fp64 backward oracle on the same seeded inputs.
 
-The backward computes in fp32 from the io values, which the oracle receives exactly (bf16
+The token-serial form computes in fp32 from the io values, which the oracle receives exactly (bf16
 inputs are widened to fp64).  So no bf16 rounding happens inside, and the bars are those of
 fp32 arithmetic: max |g - g_ref| / rms(g_ref) <= 1e-4 per cotangent tensor for float32 io (the
 forward's own fp32 bar) and <= 1e-3 for bfloat16 io, whose workloads here run 16K-token chains.
@@ -38,9 +39,9 @@ def side_inputs(B_, H, dk, dv, seed, io):
     return S0, vh
 
 
-def gpu_backward(inp, dout, dS_final=None, v_hist=None, S_init=None):
+def gpu_backward(inp, dout, dS_final=None, v_hist=None, S_init=None, path=1):
     d = to_device(inp)
-    with B.Plan.for_inputs(d) as p:
+    with B.Plan.for_inputs(d, path=path) as p:
         g = p.backward(d, dout.cuda(), dS_final=None if dS_final is None else dS_final.cuda(),
                        v_hist=None if v_hist is None else v_hist.cuda(),
                        S_init=None if S_init is None else S_init.cuda(), want_dv_hist=True, want_dS_init=True)
@@ -127,7 +128,7 @@ def test_backward_reuses_its_workspace_and_rejects_bad_arguments():
     inp = make_inputs(1, 2, 64, 64, 64, 3, dtype="bf16", seed=4)
     d = to_device(inp)
     dout, _ = make_cotangents(1, 2, 64, 64, 64, seed=4)
-    with B.Plan.for_inputs(d) as p:
+    with B.Plan.for_inputs(d, path=1) as p:
         g1 = p.backward(d, dout.cuda())
         ws = p.workspace_bytes()
         g2 = p.backward(d, dout.cuda())

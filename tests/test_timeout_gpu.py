@@ -119,3 +119,22 @@ def test_decode_wait_expires_and_the_plan_recovers():
         o_b = fresh.decode_step(tok, h_b, S_b)
         assert _status(fresh) == B.PRISM_OK
     assert torch.equal(o_a, o_b) and torch.equal(S_a, S_b) and torch.equal(h_a, h_b)
+
+
+def test_chunked_backward_wait_expires_and_the_plan_recovers():
+    """Chunked backward: the TMA and bulk-copy loads and the product completions of its three
+    tensor-core kernels (a few thousand chunk CTAs, so that some product wait is still pending
+    when its 1 ns bound is checked)."""
+    from ssm_sequence_layer_gb300.inputs import make_cotangents
+    d = _dev(make_inputs(2, 4, 8192, 64, 64, 4, dtype="bf16", seed=905))
+    dout, _ = make_cotangents(2, 4, 8192, 64, 64, seed=905)
+    dout = dout.cuda()
+    with B.Plan.for_inputs(d) as plan:
+        _expire(plan, lambda: plan.backward(d, dout))
+        again = plan.backward(d, dout)
+        assert _status(plan) == B.PRISM_OK
+    with B.Plan.for_inputs(d) as fresh:
+        ref = fresh.backward(d, dout)
+        assert _status(fresh) == B.PRISM_OK
+    for kk in ref:
+        assert torch.equal(again[kk], ref[kk]), kk
