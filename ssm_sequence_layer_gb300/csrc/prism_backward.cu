@@ -772,16 +772,25 @@ __global__ void conv_grad_kernel(const io_t *__restrict__ v, const io_t *__restr
 }
 
 // dconv_w[h][j][c] = sum over the batch and the tiles of dWp.
-__global__ void conv_reduce_kernel(const float *__restrict__ dWp, float *__restrict__ dconv_w, int B, int H, int dv,
-                                   int ntile)
+__global__ void __launch_bounds__(NT) conv_reduce_kernel(const float *__restrict__ dWp, float *__restrict__ dconv_w,
+                                                         int B, int H, int dv, int ntile)
 {
-    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= H * 4 * dv) return;
-    const int h = idx / (4 * dv), jc = idx % (4 * dv);
+    // block: 64 consecutive (h, j, c) outputs x 4 groups of the (b, tile) terms, fixed order
+    __shared__ float part[4][64];
+    const int o = blockIdx.x * 64 + (threadIdx.x & 63), grp = threadIdx.x >> 6;
+    const int nout = H * 4 * dv;
     float s = 0.f;
-    for (int b = 0; b < B; ++b)
-        for (int tile = 0; tile < ntile; ++tile) s += dWp[(((size_t)b * H + h) * ntile + tile) * 4 * dv + jc];
-    dconv_w[idx] = s;
+    if (o < nout) {
+        const int h = o / (4 * dv), jc = o % (4 * dv);
+        const int nterm = B * ntile;
+        for (int e = grp; e < nterm; e += 4) {
+            const int b = e / ntile, tile = e % ntile;
+            s += dWp[(((size_t)b * H + h) * ntile + tile) * 4 * dv + jc];
+        }
+    }
+    part[grp][threadIdx.x & 63] = s;
+    __syncthreads();
+    if (grp == 0 && o < nout) dconv_w[o] = (part[0][threadIdx.x] + part[1][threadIdx.x]) + (part[2][threadIdx.x] + part[3][threadIdx.x]);
 }
 
 struct Carve {
@@ -829,7 +838,7 @@ cudaError_t token_local(const Shape &s, const BackwardArgs &a, float *dX, float 
                                                                ntile);
     tm.end();
     tm.begin("bwd_conv_reduce");
-    conv_reduce_kernel<<<(s.H * 4 * s.dv + NT - 1) / NT, NT, 0, st>>>(dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
+    conv_reduce_kernel<<<(s.H * 4 * s.dv + 63) / 64, NT, 0, st>>>(dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
     tm.end();
     return cudaGetLastError();
 }

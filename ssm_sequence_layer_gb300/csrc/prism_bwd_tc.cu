@@ -603,16 +603,16 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // =====================================================================================================
-// scan: grid (64 / 8 row blocks, BH, 2 directions), 256 threads; warp r owns row r of the block,
-// lane (cg, h) columns 4 cg .. 4 cg + 3 and half h of the sum over m (the two halves meet by one
-// shuffle).  Forward: S_{c+1} = S_c A_c + B_c from S_init (or 0), storing S_c for c = 0 .. NC.
-// Reverse: G_{c-1} = G_c A_c^T + Bbar_c from dS_final (or 0), storing G_c for c = NC-1 .. 0, the
-// last value being dS_init.  The map and the block's rows of B of the next steps stream through a
-// four-stage ring of bulk copies (one thread issues them; every thread waits on the stage's
-// mbarrier, bounded); the state rows are double-buffered, so one CTA barrier per step suffices.
-constexpr int SC_ROWS = 8, SC_STAGES = 8;
+// scan: grid (64 / 8 row blocks, BH, 2 directions), 256 threads.  Forward: S_{c+1} = S_c A_c + B_c
+// from S_init (or 0), storing S_c for c = 0 .. NC.  Reverse: G_{c-1} = G_c A_c^T + Bbar_c from
+// dS_final (or 0), storing G_c for c = NC-1 .. 0, the last value being dS_init.  Thread (q, c)
+// forms the partial sums over m in [16 q, 16 q + 16) of all 8 rows of column c, so each map element
+// is read from shared memory once per step and used for the 8 rows from a register; the four
+// partials meet through shared memory.  The maps stream through a ring of bulk copies (one thread
+// issues them; every thread waits on the stage's mbarrier, bounded).
+constexpr int SC_ROWS = 8, SC_STAGES = 4;
 constexpr int SC_STAGE_FLOATS = D * D + SC_ROWS * D;
-constexpr size_t SCAN_SMEM = (size_t)(SC_STAGES * SC_STAGE_FLOATS + 2 * SC_ROWS * D) * 4 + 128;
+constexpr size_t SCAN_SMEM = (size_t)(SC_STAGES * SC_STAGE_FLOATS + SC_ROWS * D + 4 * SC_ROWS * D) * 4 + 128;
 
 __global__ void __launch_bounds__(NT) scan_kernel(const float *__restrict__ mapA, const float *__restrict__ mapAT,
                                                   const float *__restrict__ mapB, const float *__restrict__ mapBb,
@@ -622,10 +622,12 @@ __global__ void __launch_bounds__(NT) scan_kernel(const float *__restrict__ mapA
                                                   unsigned long long wait_ns)
 {
     extern __shared__ __align__(128) float ssm[];
-    float *st = ssm + SC_STAGES * SC_STAGE_FLOATS;  // the state rows, [2][8][64]
+    float *st = ssm + SC_STAGES * SC_STAGE_FLOATS;  // the state rows [8][64]
+    float *red = st + SC_ROWS * D;                  // partial sums [4][8][64]
     __shared__ __align__(8) uint64_t mbar[SC_STAGES];
     __shared__ int abort_s;
-    const int tid = threadIdx.x, r = tid >> 5, lane = tid & 31, cg = lane >> 1, hm = lane & 1;
+    const int tid = threadIdx.x, col = tid & 63, qm = tid >> 6;  // partial-sum role
+    const int orow = tid >> 5, oc = 2 * (tid & 31);               // output role: row, column pair
     const int rb = blockIdx.x * SC_ROWS, bh = blockIdx.y;
     const bool rev = blockIdx.z == 1;
     const float *M = rev ? mapAT : mapA, *Bv = rev ? mapBb : mapB;
@@ -637,9 +639,9 @@ __global__ void __launch_bounds__(NT) scan_kernel(const float *__restrict__ mapA
     }
     grid_dependency_wait();
     allow_dependent_launch();
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (init) s = *reinterpret_cast<const float4 *>(init + ((size_t)bh * D + rb + r) * D + 4 * cg);
-    if (hm == 0) reinterpret_cast<float4 *>(st + r * D)[cg] = s;
+    float2 s = make_float2(0.f, 0.f);
+    if (init) s = *reinterpret_cast<const float2 *>(init + ((size_t)bh * D + rb + orow) * D + oc);
+    reinterpret_cast<float2 *>(st + orow * D)[tid & 31] = s;
     int issued = 0;  // thread 0: stages issued so far
     auto stage_in = [&](int k) {
         const int cc = rev ? NC - 1 - k : k;
@@ -658,42 +660,40 @@ __global__ void __launch_bounds__(NT) scan_kernel(const float *__restrict__ mapA
     for (; k < NC; ++k) {
         const int cc = rev ? NC - 1 - k : k;
         float *out = rev ? Gst + ((size_t)bh * NC + cc) * D * D : Sst + ((size_t)bh * (NC + 1) + cc) * D * D;
-        if (hm == 0) reinterpret_cast<float4 *>(out + (size_t)(rb + r) * D)[cg] = s;
-        if (!mbar_wait_spin(smem_u32(&mbar[k % SC_STAGES]), (uint32_t)(k / SC_STAGES) & 1u, wait_ns)) {
+        *reinterpret_cast<float2 *>(out + (size_t)(rb + orow) * D + oc) = s;
+        if (!mbar_wait(smem_u32(&mbar[k % SC_STAGES]), (uint32_t)(k / SC_STAGES) & 1u, wait_ns)) {
             abort_s = 1;
             set_status(status, kDevTimeout);
         }
         const float *mm = ssm + (k % SC_STAGES) * SC_STAGE_FLOATS;
-        const float *cur = st + (k & 1) * SC_ROWS * D;
-        float4 acc = hm == 0 ? reinterpret_cast<const float4 *>(mm + D * D + r * D)[cg] : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 *sr = reinterpret_cast<const float4 *>(cur + r * D + hm * 32);
-        const float *mh = mm + hm * 32 * D;
+        float part[SC_ROWS];
 #pragma unroll
-        for (int m4 = 0; m4 < 8; ++m4) {
-            const float4 a = sr[m4];
-            const float av[4] = {a.x, a.y, a.z, a.w};
+        for (int r = 0; r < SC_ROWS; ++r) part[r] = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 w = reinterpret_cast<const float4 *>(mh + (4 * m4 + q) * D)[cg];
-                float4 &t = (q & 1) ? acc2 : acc;
-                t.x = fmaf(av[q], w.x, t.x);
-                t.y = fmaf(av[q], w.y, t.y);
-                t.z = fmaf(av[q], w.z, t.z);
-                t.w = fmaf(av[q], w.w, t.w);
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const int m0 = 16 * qm + 4 * m4;
+            float w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = mm[(m0 + q) * D + col];
+#pragma unroll
+            for (int r = 0; r < SC_ROWS; ++r) {
+                const float4 a = *reinterpret_cast<const float4 *>(st + r * D + m0);
+                part[r] = fmaf(a.x, w[0], fmaf(a.y, w[1], fmaf(a.z, w[2], fmaf(a.w, w[3], part[r]))));
             }
         }
-        acc.x += acc2.x;
-        acc.y += acc2.y;
-        acc.z += acc2.z;
-        acc.w += acc2.w;
-        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
-        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
-        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 1);
-        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 1);
-        if (hm == 0) reinterpret_cast<float4 *>(st + ((k + 1) & 1) * SC_ROWS * D + r * D)[cg] = acc;
+#pragma unroll
+        for (int r = 0; r < SC_ROWS; ++r) red[(qm * SC_ROWS + r) * D + col] = part[r];
+        __syncthreads();  // partials complete; the state rows of step k are no longer read
+        float2 acc = *reinterpret_cast<const float2 *>(mm + D * D + orow * D + oc);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 pq = *reinterpret_cast<const float2 *>(red + (q * SC_ROWS + orow) * D + oc);
+            acc.x += pq.x;
+            acc.y += pq.y;
+        }
+        *reinterpret_cast<float2 *>(st + orow * D + oc) = acc;
         s = acc;
-        __syncthreads();  // stage k % 4 and the state rows of step k are no longer read
+        __syncthreads();  // the new state is written; stage k % SC_STAGES and the partials are free
         if (abort_s) break;
         if (tid == 0 && k + SC_STAGES < NC) stage_in(k + SC_STAGES);
     }
@@ -705,10 +705,8 @@ __global__ void __launch_bounds__(NT) scan_kernel(const float *__restrict__ mapA
                 (void)mbar_wait(smem_u32(&mbar[j % SC_STAGES]), (uint32_t)(j / SC_STAGES) & 1u, 1000000000ull);
         return;
     }
-    if (hm == 0) {
-        if (!rev) reinterpret_cast<float4 *>(Sst + ((size_t)bh * (NC + 1) + NC) * D * D + (size_t)(rb + r) * D)[cg] = s;
-        else if (dS_init) reinterpret_cast<float4 *>(dS_init + ((size_t)bh * D + rb + r) * D)[cg] = s;
-    }
+    if (!rev) *reinterpret_cast<float2 *>(Sst + ((size_t)bh * (NC + 1) + NC) * D * D + (size_t)(rb + orow) * D + oc) = s;
+    else if (dS_init) *reinterpret_cast<float2 *>(dS_init + ((size_t)bh * D + rb + orow) * D + oc) = s;
 }
 
 // =====================================================================================================
