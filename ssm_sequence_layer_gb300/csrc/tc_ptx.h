@@ -186,32 +186,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint64
     }
 }
 
-// Non-blocking test of the phase (no suspension).
-__device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// The same bounded wait as mbar_wait by polling without suspension: for short waits on a chain
-// of dependent steps, where a suspended thread would resume later than the phase completes.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t mbar, uint32_t parity, uint64_t max_ns)
-{
-    if (mbar_test(mbar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_test(mbar, parity)) return true;
-        if (globaltimer_ns() - t0 > max_ns) return false;
-    }
-}
-
 // ---- TMA ----------------------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t mbar, int c0, int c1, int c2)
 {
