@@ -56,7 +56,9 @@ using tcu::st_row_h;
 constexpr int C = kChunk;
 constexpr int D = 64;                 // dk = dv
 constexpr int RMAX = 3;               // levels handled (L <= 4)
-constexpr int NT = 256;               // threads: 8 warps, two per TMEM lane quarter
+constexpr int NT = 512;               // threads of the per-chunk kernels: 16 warps, four per TMEM lane quarter
+constexpr int CW = 64 / (NT / 128);   // columns of a 64-column accumulator block each thread handles
+constexpr int SCAN_NT = 256;          // threads of the scan
 constexpr uint32_t PANEL = 8192;      // [64 rows][64 cols] 16-bit SW128
 constexpr int STASH = 8;              // stash panels per chunk (maps kernel): U', W, Wbar, Z0, E0, X_0..X_2
 enum { ST_UP = 0, ST_W = 1, ST_WB = 2, ST_Z0 = 3, ST_E0 = 4, ST_X = 5 };
@@ -65,7 +67,7 @@ constexpr int VZ = 2;                 // per chunk (grad_a): Vt, Z
 // per-token scalars (floats from the scalar region): beta, lambda, Gamma, colf, beta Gamma, gamma, eta
 constexpr int SC_BETA = 0, SC_LAM = 64, SC_GAM = 128, SC_COLF = 192, SC_BG = 256, SC_GM = 320,
               SC_ET = 320 + 64 * RMAX, SC_HALO = 320 + 128 * RMAX, SC_RED = SC_HALO + 3 * D;
-constexpr int SC_FLOATS = SC_RED + 10 * 64 + 32;  // + per-token partial sums (fixed slots, summed in a fixed order)
+constexpr int SC_FLOATS = SC_RED + 20 * 64 + 32;  // + per-token partial sums (fixed slots, summed in a fixed order)
 
 struct Params {
     const __nv_bfloat16 *v;          // [BH][T][64]
@@ -100,11 +102,12 @@ __device__ __forceinline__ void mma_k64(uint32_t d, uint64_t a, bool a_mn, uint6
                 (acc || s > 0) ? 1u : 0u);
 }
 
-// 32 halves of row `row`, columns col0 .. col0 + 31, of an SW128 panel image (shared or global)
-__device__ __forceinline__ void ld_row_h(const uint8_t *panel, int row, int col0, float (&v)[32])
+// N halves of row `row`, columns col0 .. col0 + N - 1, of an SW128 panel image (shared or global)
+template <int N>
+__device__ __forceinline__ void ld_row_h(const uint8_t *panel, int row, int col0, float (&v)[N])
 {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < N / 8; ++g) {
         const uint4 w = *reinterpret_cast<const uint4 *>(panel + sw128(row, col0 + 8 * g));
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -116,17 +119,19 @@ __device__ __forceinline__ void ld_row_h(const uint8_t *panel, int row, int col0
     }
 }
 
-// the raw 16-byte groups of the same row segment (issued early, converted later by h8x4_to_f)
-__device__ __forceinline__ void ld_row_raw(const uint8_t *panel, int row, int col0, uint4 (&w)[4])
+// the raw 16-byte groups of the same row segment (issued early, converted later by h8_to_f)
+template <int G>
+__device__ __forceinline__ void ld_row_raw(const uint8_t *panel, int row, int col0, uint4 (&w)[G])
 {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) w[g] = *reinterpret_cast<const uint4 *>(panel + sw128(row, col0 + 8 * g));
+    for (int g = 0; g < G; ++g) w[g] = *reinterpret_cast<const uint4 *>(panel + sw128(row, col0 + 8 * g));
 }
 
-__device__ __forceinline__ void h8x4_to_f(const uint4 (&w)[4], float (&v)[32])
+template <int G>
+__device__ __forceinline__ void h8_to_f(const uint4 (&w)[G], float (&v)[8 * G])
 {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < G; ++g) {
         const uint32_t ww[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -138,10 +143,11 @@ __device__ __forceinline__ void h8x4_to_f(const uint4 (&w)[4], float (&v)[32])
 }
 
 // the same from a bf16 panel (TMA image)
-__device__ __forceinline__ void ld_row_b(const uint8_t *panel, int row, int col0, float (&v)[32])
+template <int N>
+__device__ __forceinline__ void ld_row_b(const uint8_t *panel, int row, int col0, float (&v)[N])
 {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < N / 8; ++g) {
         const uint4 w = *reinterpret_cast<const uint4 *>(panel + sw128(row, col0 + 8 * g));
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -260,13 +266,14 @@ __device__ __forceinline__ void load_scalars(float *sc, const Params &p, size_t 
     }
 }
 
-// decayed, masked scores of row i, columns j0 .. j0 + 31: v[q] *= D_{i, j} for j <= i (incl) or
+// decayed, masked scores of row i, columns j0 .. j0 + N - 1: v[q] *= D_{i, j} for j <= i (incl) or
 // j < i; 0 elsewhere
-__device__ __forceinline__ void decay_row(float (&v)[32], const float *lam, int i, int j0, bool incl)
+template <int N>
+__device__ __forceinline__ void decay_row(float (&v)[N], const float *lam, int i, int j0, bool incl)
 {
     const float li = lam[i];
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
+    for (int q = 0; q < N; ++q) {
         const int j = j0 + q;
         const bool keep = incl ? j <= i : j < i;
         v[q] = keep ? v[q] * __expf(fminf(li - lam[j], 0.f)) : 0.f;
@@ -274,21 +281,23 @@ __device__ __forceinline__ void decay_row(float (&v)[32], const float *lam, int 
 }
 
 // the transposed mask: v[q] (row m, column j = j0 + q) *= D_{j, m} for j >= m (incl) or j > m
-__device__ __forceinline__ void decay_col(float (&v)[32], const float *lam, int m, int j0, bool incl)
+template <int N>
+__device__ __forceinline__ void decay_col(float (&v)[N], const float *lam, int m, int j0, bool incl)
 {
     const float lm = lam[m];
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
+    for (int q = 0; q < N; ++q) {
         const int j = j0 + q;
         const bool keep = incl ? j >= m : j > m;
         v[q] = keep ? v[q] * __expf(fminf(lam[j] - lm, 0.f)) : 0.f;
     }
 }
 
-__device__ __forceinline__ void st_row_f(float *dst, const float (&v)[32])
+template <int N>
+__device__ __forceinline__ void st_row_f(float *dst, const float (&v)[N])
 {
 #pragma unroll
-    for (int g = 0; g < 8; ++g)
+    for (int g = 0; g < N / 4; ++g)
         reinterpret_cast<float4 *>(dst)[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
 }
 
@@ -396,7 +405,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (abort_s) break;
         // ---- prep: x_{i,l} = gamma_il g_i r_il (two channels, eight tokens per thread) -> X_l -----------
         if (R > 0) {
-            const int cp = tid & 31, tg = tid >> 5;
+            const int cp = tid & 31, tg = tid >> 5;  // channel pair; tokens tg + 16 k
             const __nv_bfloat162 *cw = reinterpret_cast<const __nv_bfloat162 *>(p.conv_w) + (size_t)h * 4 * (D / 2) + cp;
             float2 w[4];
 #pragma unroll
@@ -407,8 +416,8 @@ __global__ void __launch_bounds__(NT, 1)
                 return make_float2(sc[SC_HALO + (3 + i) * D + 2 * cp], sc[SC_HALO + (3 + i) * D + 2 * cp + 1]);
             };
 #pragma unroll 2
-            for (int k = 0; k < 8; ++k) {
-                const int i = tg + 8 * k;
+            for (int k = 0; k < 64 / (NT / 32); ++k) {
+                const int i = tg + (NT / 32) * k;
                 const float2 v0 = vat(i), v1 = vat(i - 1), v2 = vat(i - 2), v3 = vat(i - 3);
                 const float a0 = fmaf(w[0].x, v0.x, fmaf(w[1].x, v1.x, fmaf(w[2].x, v2.x, w[3].x * v3.x)));
                 const float a1 = fmaf(w[0].y, v0.y, fmaf(w[1].y, v1.y, fmaf(w[2].y, v2.y, w[3].y * v3.y)));
@@ -433,8 +442,8 @@ __global__ void __launch_bounds__(NT, 1)
         // the solve); Mku_l = (K U_l^T) o D (j < i) --------------------------------------------------------
         float *sA = reinterpret_cast<float *>(P(F)), *sT32 = sA + 64 * tcu::LDA, *sX = sT32 + 64 * tcu::LDA;
         {
-            const int j0 = 32 * sub;
-            float v[32];
+            const int j0 = CW * sub;
+            float v[CW];
             if (row < 64) {
                 tmem_ld(tmem + TM_G1 + lane_off + (uint32_t)j0, v);
                 decay_row(v, s_lam, row, j0, true);
@@ -445,7 +454,7 @@ __global__ void __launch_bounds__(NT, 1)
                 decay_row(v, s_lam, i, j0, false);
                 const float b = s_beta[i];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] *= b;
+                for (int q = 0; q < CW; ++q) v[q] *= b;
                 st_row_f(sA + i * tcu::LDA + j0, v);
                 for (int l = 0; l < R; ++l) {
                     tmem_ld(tmem + TM_G1 + 64 * (l + 1) + lane_off + (uint32_t)j0, v);
@@ -467,30 +476,30 @@ __global__ void __launch_bounds__(NT, 1)
                     idesc_f16(128, 64, 1, 1), false);
             mma_commit(smem_u32(&mbar[2]));
         }
-        tcu::ut_solve(sA, sT32, sX, P(TF), tid, 1);
+        if (tid < tcu::SOLVE_THREADS) tcu::ut_solve(sA, sT32, sX, P(TF), tid, 1);
         fence_async_smem();
         wait_all(2, 0);
         fence_after_sync();
         __syncthreads();  // the solve region is free from here on
         // ---- E0 = V - Mku X, beta E0, Y (rows < 64); the scaled key and query copies (rows >= 64) ------
         {
-            const int c0 = 32 * sub;
-            float v[32], e[32];
+            const int c0 = CW * sub;
+            float v[CW], e[CW];
             if (row < 64) {
                 const int i = row;
                 if (R > 0) {
                     tmem_ld(tmem + TM_E + lane_off + (uint32_t)c0, e);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) e[q] = 0.f;
+                    for (int q = 0; q < CW; ++q) e[q] = 0.f;
                 }
                 ld_row_b(P(V), i, c0, v);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] -= e[q];
+                for (int q = 0; q < CW; ++q) v[q] -= e[q];
                 st_row_h(stash + ST_E0 * PANEL, i, c0, v);
                 const float b = s_beta[i];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] *= b;
+                for (int q = 0; q < CW; ++q) v[q] *= b;
                 st_row_h(P(BE), i, c0, v);
                 tmem_ld(tmem + TM_Y + lane_off + (uint32_t)c0, v);
                 st_row_h(P(Y), i, c0, v);
@@ -499,23 +508,23 @@ __global__ void __launch_bounds__(NT, 1)
                 ld_row_b(P(K), i, c0, v);
                 const float bg = s_bg[i], cf = s_colf[i];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) e[q] = bg * v[q];
+                for (int q = 0; q < CW; ++q) e[q] = bg * v[q];
                 st_row_h(P(BGK), i, c0, e);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) e[q] = -e[q];
+                for (int q = 0; q < CW; ++q) e[q] = -e[q];
                 st_row_h(P(NBGK), i, c0, e);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) e[q] = cf * v[q];
+                for (int q = 0; q < CW; ++q) e[q] = cf * v[q];
                 st_row_h(P(CK), i, c0, e);
                 ld_row_b(P(Q), i, c0, v);
                 const float gi = s_gam[i];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] *= gi;
+                for (int q = 0; q < CW; ++q) v[q] *= gi;
                 st_row_h(P(PK), i, c0, v);
                 for (int l = 0; l < R; ++l) {
                     ld_row_b(P(U0 + l), i, c0, v);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] *= cf;
+                    for (int q = 0; q < CW; ++q) v[q] *= cf;
                     st_row_h(P(MKU0 + l), i, c0, v);
                 }
             }
@@ -535,8 +544,8 @@ __global__ void __launch_bounds__(NT, 1)
         wait_all(3, 0);
         fence_after_sync();
         if (row < 64) {
-            const int i = row, c0 = 32 * sub;
-            float v[32];
+            const int i = row, c0 = CW * sub;
+            float v[CW];
             tmem_ld(tmem + TM_WY + lane_off + (uint32_t)c0, v);
             st_row_h(P(UP), i, c0, v);
             st_row_h(stash + ST_UP * PANEL, i, c0, v);
@@ -570,17 +579,17 @@ __global__ void __launch_bounds__(NT, 1)
         wait_all(4, 0);
         fence_after_sync();
         {
-            const int n0 = 32 * sub;
+            const int n0 = CW * sub;
             const size_t mo = (size_t)chunk * D * D;
-            float v[32];
+            float v[CW];
             tmem_ld(tmem + TM_MAP + lane_off + (uint32_t)n0, v);
             if (row < 64) {  // A_c [m][n] = Gamma_63 [m == n] - (W^T colf K)[m][n], and its transpose
                 const float g63 = s_gam[63];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] = (n0 + q == row ? g63 : 0.f) - v[q];
+                for (int q = 0; q < CW; ++q) v[q] = (n0 + q == row ? g63 : 0.f) - v[q];
                 st_row_f(p.mapA + mo + (size_t)row * D + n0, v);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) p.mapAT[mo + (size_t)(n0 + q) * D + row] = v[q];
+                for (int q = 0; q < CW; ++q) p.mapAT[mo + (size_t)(n0 + q) * D + row] = v[q];
             } else {
                 st_row_f(p.mapB + mo + (size_t)(row - 64) * D + n0, v);
                 tmem_ld(tmem + TM_BAR + lane_off + (uint32_t)n0, v);
@@ -614,7 +623,7 @@ constexpr int SC_ROWS = 8, SC_STAGES = 4;
 constexpr int SC_STAGE_FLOATS = D * D + SC_ROWS * D;
 constexpr size_t SCAN_SMEM = (size_t)(SC_STAGES * SC_STAGE_FLOATS + SC_ROWS * D + 4 * SC_ROWS * D) * 4 + 128;
 
-__global__ void __launch_bounds__(NT) scan_kernel(const float *__restrict__ mapA, const float *__restrict__ mapAT,
+__global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__ mapA, const float *__restrict__ mapAT,
                                                   const float *__restrict__ mapB, const float *__restrict__ mapBb,
                                                   const float *__restrict__ S_init, const float *__restrict__ dS_final,
                                                   float *__restrict__ Sst, float *__restrict__ Gst,
@@ -742,8 +751,8 @@ __global__ void __launch_bounds__(NT, 1)
     float *sc = reinterpret_cast<float *>(sm + SC_OFF);
     const float *s_beta = sc + SC_BETA, *s_lam = sc + SC_LAM, *s_gam = sc + SC_GAM, *s_colf = sc + SC_COLF;
     // per-token partial sums, one slot per source so that the totals do not depend on timing:
-    // sigma [8][64] (slots 0-1: beta v.z by column half; 2 + 2 l + half: x_l.dx_l), dbeta [2][64]
-    float *s_sig = sc + SC_RED, *s_db = sc + SC_RED + 8 * 64;
+    // sigma [16][64] (slots 0-3: beta v.z by column part; 4 + 4 l + part: x_l.dx_l), dbeta [4][64]
+    float *s_sig = sc + SC_RED, *s_db = sc + SC_RED + 16 * 64;
     auto P = [&](int idx) { return sm + (uint32_t)idx * PANEL; };
     const uint32_t sbase = smem_u32(sm);
     const uint64_t dbase = sdesc(sbase, 0, 0);
@@ -785,14 +794,14 @@ __global__ void __launch_bounds__(NT, 1)
         else expired();
     }
     load_scalars(sc, p, tok0, n, tid);
-    for (int e = tid; e < 10 * 64; e += NT) sc[SC_RED + e] = 0.f;
+    for (int e = tid; e < 20 * 64; e += NT) sc[SC_RED + e] = 0.f;
     f32_to_panel(P(S0), p.Sst + ((size_t)bh * (p.NC + 1) + c) * D * D, D, tid);
     f32_to_panel(P(GB), p.Gst + ((size_t)bh * p.NC + c) * D * D, D, tid);
     f32_to_panel(P(DO), p.dout + tok0 * D, n, tid);
     for (int e = tid; e < 512; e += NT) reinterpret_cast<uint4 *>(P(ZERO))[e] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
-    float z[32];  // rows < 64: this thread's 32 columns of z_i (kept for dbeta)
+    float z[CW];  // rows < 64: this thread's columns of z_i (kept for dbeta)
     do {
         if (abort_s) break;
         // ---- the input tiles to fp16 in place; colf U_l copies ----------------------------------------------
@@ -813,15 +822,15 @@ __global__ void __launch_bounds__(NT, 1)
             mma_commit(smem_u32(&mbar[1]));
         }
         // this thread's rows of the stash and of v, loaded while the products run
-        uint4 pre[3][4];
+        uint4 pre[3][CW / 8];
         {
-            const int j0 = 32 * sub, i = row & 63;
+            const int j0 = CW * sub, i = row & 63;
             if (row < 64) {
                 ld_row_raw(stash + ST_E0 * PANEL, i, j0, pre[0]);
                 ld_row_raw(stash + ST_Z0 * PANEL, i, j0, pre[1]);
                 if (i < n) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) pre[2][g] = reinterpret_cast<const uint4 *>(p.v + (tok0 + i) * D + j0)[g];
+                    for (int g = 0; g < CW / 8; ++g) pre[2][g] = reinterpret_cast<const uint4 *>(p.v + (tok0 + i) * D + j0)[g];
                 }
             } else {
                 ld_row_raw(stash + ST_UP * PANEL, i, j0, pre[0]);
@@ -830,8 +839,8 @@ __global__ void __launch_bounds__(NT, 1)
         wait_all(1, 0);
         fence_after_sync();
         {
-            const int j0 = 32 * sub;
-            float v[32], s2[32];
+            const int j0 = CW * sub;
+            float v[CW], s2[CW];
             if (row < 64) {
                 const int i = row;
                 // P_l = (Q U_l^T) o D (j <= i)
@@ -842,31 +851,31 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 // E = E0 - Gamma_i (K S^T)_i  (fp32)
                 tmem_ld(tmem + TM_D1 + lane_off + (uint32_t)j0, v);
-                h8x4_to_f(pre[0], s2);
+                h8_to_f(pre[0], s2);
                 const float gi = s_gam[i];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) s2[q] -= gi * v[q];
+                for (int q = 0; q < CW; ++q) s2[q] -= gi * v[q];
                 st_row_f(reinterpret_cast<float *>(P(E32)) + i * D + j0, s2);
                 // z = Z0 + (Wbar G^T)_i;  -beta z;  dv = beta z;  sigma += beta v.z
                 tmem_ld(tmem + TM_D2 + lane_off + (uint32_t)j0, v);
-                h8x4_to_f(pre[1], s2);
+                h8_to_f(pre[1], s2);
                 const float b = s_beta[i];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
+                for (int q = 0; q < CW; ++q) {
                     z[q] = s2[q] + v[q];
                     v[q] = -b * z[q];
                 }
                 st_row_h(P(NBZ), i, j0, v);
                 st_row_h(vz + PANEL, i, j0, z);
                 if (i < n) {
-                    float dvv[32];
+                    float dvv[CW];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) dvv[q] = b * z[q];
+                    for (int q = 0; q < CW; ++q) dvv[q] = b * z[q];
                     st_row_f(p.dv + (tok0 + i) * D + j0, dvv);
                     const __nv_bfloat162 *vr = reinterpret_cast<const __nv_bfloat162 *>(pre[2]);
                     float part = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
+                    for (int q = 0; q < CW / 2; ++q) {
                         const float2 f = __bfloat1622float2(vr[q]);
                         part = fmaf(f.x, z[2 * q], fmaf(f.y, z[2 * q + 1], part));
                     }
@@ -885,9 +894,9 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 // Vt = U' - (W S^T)_i
                 tmem_ld(tmem + TM_D1 + lane_off + (uint32_t)j0, v);
-                h8x4_to_f(pre[0], s2);
+                h8_to_f(pre[0], s2);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) s2[q] -= v[q];
+                for (int q = 0; q < CW; ++q) s2[q] -= v[q];
                 st_row_h(P(VT), i, j0, s2);
                 st_row_h(vz, i, j0, s2);
             }
@@ -915,9 +924,9 @@ __global__ void __launch_bounds__(NT, 1)
                     idesc_f16(128, 64, 0, 1), false);
             mma_commit(smem_u32(&mbar[2]));
         }
-        uint4 prx[2][4];  // the X rows this thread's dX rows pair with (rows < 64: X_1; else X_0, X_2)
+        uint4 prx[2][CW / 8];  // the X rows this thread's dX rows pair with (rows < 64: X_1; else X_0, X_2)
         {
-            const int j0 = 32 * sub, i = row & 63;
+            const int j0 = CW * sub, i = row & 63;
             if (row < 64) {
                 if (R >= 2) ld_row_raw(stash + (ST_X + 1) * PANEL, i, j0, prx[0]);
             } else {
@@ -928,17 +937,17 @@ __global__ void __launch_bounds__(NT, 1)
         wait_all(2, 0);
         fence_after_sync();
         {
-            const int j0 = 32 * sub;
-            float v[32], x[32];
-            auto dx_out = [&](uint32_t col, int l, int i, const uint4 (&xr)[4]) {  // dX_l row i -> global, sigma += x.dx
+            const int j0 = CW * sub;
+            float v[CW], x[CW];
+            auto dx_out = [&](uint32_t col, int l, int i, const uint4 (&xr)[CW / 8]) {  // dX_l row i -> global, sigma += x.dx
                 tmem_ld(tmem + col + lane_off + (uint32_t)j0, v);
                 if (i < n) {
                     st_row_f(p.dX + ((tok0 + i) * R + l) * D + j0, v);
-                    h8x4_to_f(xr, x);
+                    h8_to_f(xr, x);
                     float part = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) part = fmaf(x[q], v[q], part);
-                    s_sig[(2 + 2 * l + sub) * 64 + i] = part;
+                    for (int q = 0; q < CW; ++q) part = fmaf(x[q], v[q], part);
+                    s_sig[(4 + 4 * l + sub) * 64 + i] = part;
                 }
             };
             if (row < 64) {
@@ -949,7 +958,7 @@ __global__ void __launch_bounds__(NT, 1)
                 const float *Er = reinterpret_cast<const float *>(P(E32)) + i * D + j0;
                 float part = 0.f;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) part = fmaf(z[q], Er[q] - v[q], part);
+                for (int q = 0; q < CW; ++q) part = fmaf(z[q], Er[q] - v[q], part);
                 s_db[sub * 64 + i] = part;
             } else {
                 const int i = row - 64;
@@ -959,10 +968,10 @@ __global__ void __launch_bounds__(NT, 1)
         }
         __syncthreads();
         if (tid < n) {
-            p.dbeta[tok0 + tid] = s_db[tid] + s_db[64 + tid];
+            p.dbeta[tok0 + tid] = (s_db[tid] + s_db[64 + tid]) + (s_db[128 + tid] + s_db[192 + tid]);
             float sg = 0.f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) sg += s_sig[k * 64 + tid];
+            for (int k = 0; k < 16; ++k) sg += s_sig[k * 64 + tid];
             p.sigma[tok0 + tid] = sg;
         }
     } while (0);
@@ -1010,7 +1019,7 @@ __global__ void __launch_bounds__(NT, 1)
     const size_t tok0 = (size_t)bh * p.T + t0;
     float *sc = reinterpret_cast<float *>(sm + SC_OFF);
     const float *s_beta = sc + SC_BETA, *s_lam = sc + SC_LAM, *s_gam = sc + SC_GAM, *s_colf = sc + SC_COLF;
-    float *s_qdq = sc + SC_RED, *s_Fw = sc + SC_RED + 128;  // q.dq [2][64] by column half; <G, S'> per warp
+    float *s_qdq = sc + SC_RED, *s_Fw = sc + SC_RED + 4 * 64;  // q.dq [4][64] by column part; <G, S'> per warp
     auto P = [&](int idx) { return sm + (uint32_t)idx * PANEL; };
     const uint32_t sbase = smem_u32(sm);
     const uint64_t dbase = sdesc(sbase, 0, 0);
@@ -1055,7 +1064,7 @@ __global__ void __launch_bounds__(NT, 1)
         else expired();
     }
     load_scalars(sc, p, tok0, n, tid);
-    if (tid < 128) s_qdq[tid] = 0.f;
+    if (tid < 4 * 64) s_qdq[tid] = 0.f;
     f32_to_panel(P(S0), Sc, D, tid);
     f32_to_panel(P(GB), Gc, D, tid);
     f32_to_panel(P(DO), p.dout + tok0 * D, n, tid);
@@ -1063,7 +1072,7 @@ __global__ void __launch_bounds__(NT, 1)
         const float4 *g4 = reinterpret_cast<const float4 *>(Gc), *s4 = reinterpret_cast<const float4 *>(Sc + D * D);
         float part = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < D * D / 4 / NT; ++q) {
             const float4 a = g4[tid + NT * q], b = s4[tid + NT * q];
             part = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, part))));
         }
@@ -1090,20 +1099,19 @@ __global__ void __launch_bounds__(NT, 1)
         wait_all(1, 0);
         fence_after_sync();
         // J_b[m][j] = (w_m . dout_j) D_{j,m} (j >= m), H_b[m][j] = (w_m . z_j) D_{j,m} (j > m); thread
-        // (quad, sub): row `row` of group `sub` (block b = 2 sub + row / 64)
+        // (quad, sub): row `row` of group sub & 1 (block b = 2 (sub & 1) + row / 64), the 32 columns
+        // of half sub >> 1
         {
-            const int g = sub, b = 2 * g + (row >> 6), m = row & 63;
+            const int g = sub & 1, h2 = sub >> 1, b = 2 * g + (row >> 6), m = row & 63;
             if ((g == 0 || R >= 2) && b <= R) {
                 float v[32];
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const uint32_t col = TM_C + 128 * g + (uint32_t)(h2 * 32);
-                    tmem_ld(tmem + col + lane_off, v);
-                    decay_col(v, s_lam, m, 32 * h2, true);
-                    st_row_h(P(J0 + b), m, 32 * h2, v);
-                    tmem_ld(tmem + col + 64 + lane_off, v);
-                    decay_col(v, s_lam, m, 32 * h2, false);
-                    st_row_h(P(H0 + b), m, 32 * h2, v);
-                }
+                const uint32_t col = TM_C + 128 * g + (uint32_t)(h2 * 32);
+                tmem_ld(tmem + col + lane_off, v);
+                decay_col(v, s_lam, m, 32 * h2, true);
+                st_row_h(P(J0 + b), m, 32 * h2, v);
+                tmem_ld(tmem + col + 64 + lane_off, v);
+                decay_col(v, s_lam, m, 32 * h2, false);
+                st_row_h(P(H0 + b), m, 32 * h2, v);
             }
         }
         // the operands of the next products, scaled in place (the Grams have read them)
@@ -1134,8 +1142,8 @@ __global__ void __launch_bounds__(NT, 1)
         fence_after_sync();
         float *dkw = reinterpret_cast<float *>(P(DKW));
         {
-            const int n0 = 32 * sub;
-            float v[32];
+            const int n0 = CW * sub;
+            float v[CW];
             if (row < 64) {
                 const int i = row;
                 tmem_ld(tmem + TM_D + lane_off + (uint32_t)n0, v);  // the write part of dk
@@ -1147,11 +1155,11 @@ __global__ void __launch_bounds__(NT, 1)
                 tmem_ld(tmem + TM_E + lane_off + (uint32_t)n0, v);  // dq
                 if (i < n) {
                     st_row_f(p.dq + (tok0 + i) * D + n0, v);
-                    float qv[32];
+                    float qv[CW];
                     ld_row_h(P(Q), i, n0, qv);
                     float part = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) part = fmaf(qv[q], v[q], part);
+                    for (int q = 0; q < CW; ++q) part = fmaf(qv[q], v[q], part);
                     s_qdq[sub * 64 + i] = part;
                 }
             } else {
@@ -1168,22 +1176,26 @@ __global__ void __launch_bounds__(NT, 1)
         }
         __syncthreads();
         if (row >= 64) {  // dk = (dKw)_0 - beta (Gamma Z S + H^T Kw)
-            const int i = row - 64, n0 = 32 * sub;
-            float v[32];
+            const int i = row - 64, n0 = CW * sub;
+            float v[CW];
             tmem_ld(tmem + TM_E + lane_off + (uint32_t)n0, v);
             if (i < n) {
                 const float b = s_beta[i];
                 const float *w = dkw + i * D + n0;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] = w[q] - b * v[q];
+                for (int q = 0; q < CW; ++q) v[q] = w[q] - b * v[q];
                 st_row_f(p.dk + (tok0 + i) * D + n0, v);
             }
         }
         // alpha_i dalpha_i = F0 + sum_{j >= i} (q_j.dq_j - sigma_j)
         if (warp == 0) {
             const int i0 = 2 * lane, i1 = i0 + 1;
-            const float a0 = i0 < n ? s_qdq[i0] + s_qdq[64 + i0] - p.sigma[tok0 + i0] : 0.f;
-            const float a1 = i1 < n ? s_qdq[i1] + s_qdq[64 + i1] - p.sigma[tok0 + i1] : 0.f;
+            const float a0 = i0 < n ? (s_qdq[i0] + s_qdq[64 + i0]) + (s_qdq[128 + i0] + s_qdq[192 + i0]) -
+                                          p.sigma[tok0 + i0]
+                                    : 0.f;
+            const float a1 = i1 < n ? (s_qdq[i1] + s_qdq[64 + i1]) + (s_qdq[128 + i1] + s_qdq[192 + i1]) -
+                                          p.sigma[tok0 + i1]
+                                    : 0.f;
             float x = a0 + a1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -1371,6 +1383,7 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     cfg.numAttrs = 1;
     tm.begin("bwd_chunk_scan");
     cfg.gridDim = dim3(D / SC_ROWS, s.BH, 2);
+    cfg.blockDim = dim3(SCAN_NT);
     cfg.dynamicSmemBytes = SCAN_SMEM;
     e = cudaLaunchKernelEx(&cfg, scan_kernel, (const float *)w.mapA, (const float *)w.mapAT, (const float *)w.mapB,
                            (const float *)w.mapBb, a.S_init, a.dS_final, w.Sst, w.Gst, a.dS_init, s.NC, d_status,
@@ -1379,6 +1392,7 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     if (e != cudaSuccess) return e;
     tm.begin("bwd_grad_a");
     cfg.gridDim = dim3(nchunks);
+    cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = ga::SMEM;
     e = cudaLaunchKernelEx(&cfg, grad_a_kernel, mq, mk_, mu, p);
     tm.end();
