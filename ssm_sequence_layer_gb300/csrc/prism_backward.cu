@@ -744,20 +744,29 @@ __global__ void conv_grad_kernel(const io_t *__restrict__ v, const io_t *__restr
 #pragma unroll
     for (int j = 0; j < 4; ++j) w[j] = ldf(conv_w + ((size_t)h * 4 + j) * dv + c);
     const size_t base = (size_t)bh * T;
+    // sliding windows in registers: hw[j] = dH[t + j] (0 past the end), vw[j] = v[t - j] (history or
+    // 0 before the start), so each token's dH and v are loaded once
+    auto vat = [&](int src) -> float {
+        if (src >= 0) return ldf(v + (base + src) * dv + c);
+        return v_hist ? ldf(v_hist + ((size_t)bh * 3 + 3 + src) * dv + c) : 0.f;
+    };
+    float hw[4], vw[4];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) hw[j] = t0 + j < T ? dH[(base + t0 + j) * dv + c] : 0.f;
+#pragma unroll
+    for (int j = 1; j < 4; ++j) vw[j] = vat(t0 - j);
+#pragma unroll 4
     for (int t = t0; t < t1; ++t) {
-        float s = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (t + j < T) s = fmaf(w[j], dH[(base + t + j) * dv + c], s);
+        hw[3] = t + 3 < T ? dH[(base + t + 3) * dv + c] : 0.f;
+        vw[0] = ldf(v + (base + t) * dv + c);
+        const float s = fmaf(w[0], hw[0], fmaf(w[1], hw[1], fmaf(w[2], hw[2], w[3] * hw[3])));
         dv_out[(base + t) * dv + c] += s;
-        const float d = dH[(base + t) * dv + c];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int src = t - j;
-            const float vv = src >= 0 ? ldf(v + (base + src) * dv + c)
-                                      : (v_hist ? ldf(v_hist + ((size_t)bh * 3 + 3 + src) * dv + c) : 0.f);
-            acc[j] = fmaf(d, vv, acc[j]);
-        }
+        for (int j = 0; j < 4; ++j) acc[j] = fmaf(hw[0], vw[j], acc[j]);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) hw[j] = hw[j + 1];
+#pragma unroll
+        for (int j = 3; j > 0; --j) vw[j] = vw[j - 1];
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) dWp[(((size_t)bh * ntile + tile) * 4 + j) * dv + c] = acc[j];

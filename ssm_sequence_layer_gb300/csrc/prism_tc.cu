@@ -1184,7 +1184,8 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
     unsigned long long t_wait = 0, t_comp = 0, t_barb = 0;
     const long long t_begin = clock64();
 #endif
-    for (int k = 0; k < nmaps; ++k) {
+    int k = 0;
+    for (; k < nmaps; ++k) {
         const int st = k % CB_STAGES, buf = k & 1;
 #ifdef PRISM_PHASE_TIMERS
         const long long tw0 = clock64();
@@ -1258,10 +1259,11 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
         atomicAdd(&prism_tc_phase_cycles[23], t_barb);
     }
 #endif
-    // after an expired wait: let the copies still in flight land before the block exits
+    // after an expired wait at step k: the stages k .. issued-1 may still be in flight (each the
+    // next phase of its slot; earlier ones were consumed); let them land before the block exits
     if (tid == 0 && abort_s)
-        for (int k = 0; k < issued; ++k)
-            (void)prism::tc::mbar_wait(prism::tc::smem_u32(&mb[k % CB_STAGES]), (uint32_t)((k / CB_STAGES) & 1),
+        for (int j = k; j < issued; ++j)
+            (void)prism::tc::mbar_wait(prism::tc::smem_u32(&mb[j % CB_STAGES]), (uint32_t)((j / CB_STAGES) & 1),
                                        1000000000ull);
 }
 
