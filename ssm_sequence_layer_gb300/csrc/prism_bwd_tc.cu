@@ -612,14 +612,17 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // =====================================================================================================
-// scan: grid (64 / 8 row blocks, BH, 2 directions), 256 threads.  Forward: S_{c+1} = S_c A_c + B_c
+// scan: grid (64 / SC_ROWS row blocks, BH, 2 directions), 256 threads.  Forward: S_{c+1} = S_c A_c + B_c
 // from S_init (or 0), storing S_c for c = 0 .. NC.  Reverse: G_{c-1} = G_c A_c^T + Bbar_c from
 // dS_final (or 0), storing G_c for c = NC-1 .. 0, the last value being dS_init.  Thread (q, c)
-// forms the partial sums over m in [16 q, 16 q + 16) of all 8 rows of column c, so each map element
-// is read from shared memory once per step and used for the 8 rows from a register; the four
-// partials meet through shared memory.  The maps stream through a ring of bulk copies (one thread
+// forms the partial sums over m in [16 q, 16 q + 16) of all the block's rows of column c, so each
+// map element is read from shared memory once per step and used for every row from a register; the
+// four partials meet through shared memory.  Four rows a block: two blocks share an SM, which hides
+// the step's latencies better than one block of eight rows.  The maps stream through a ring of bulk copies (one thread
 // issues them; every thread waits on the stage's mbarrier, bounded).
-constexpr int SC_ROWS = 8, SC_STAGES = 4;
+constexpr int SC_ROWS = 4, SC_STAGES = 4;
+constexpr int SC_OUTS = SC_ROWS * D / SCAN_NT;  // outputs a thread forms in the reduction (consecutive columns)
+static_assert(SC_OUTS >= 1 && SC_OUTS <= 4, "scan layout");
 constexpr int SC_STAGE_FLOATS = D * D + SC_ROWS * D;
 constexpr size_t SCAN_SMEM = (size_t)(SC_STAGES * SC_STAGE_FLOATS + SC_ROWS * D + 4 * SC_ROWS * D) * 4 + 128;
 
@@ -631,12 +634,12 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__
                                                   unsigned long long wait_ns)
 {
     extern __shared__ __align__(128) float ssm[];
-    float *st = ssm + SC_STAGES * SC_STAGE_FLOATS;  // the state rows [8][64]
-    float *red = st + SC_ROWS * D;                  // partial sums [4][8][64]
+    float *st = ssm + SC_STAGES * SC_STAGE_FLOATS;  // the state rows [SC_ROWS][64]
+    float *red = st + SC_ROWS * D;                  // partial sums [4][SC_ROWS][64]
     __shared__ __align__(8) uint64_t mbar[SC_STAGES];
     __shared__ int abort_s;
     const int tid = threadIdx.x, col = tid & 63, qm = tid >> 6;  // partial-sum role
-    const int orow = tid >> 5, oc = 2 * (tid & 31);               // output role: row, column pair
+    const int orow = tid / (D / SC_OUTS), oc = (tid % (D / SC_OUTS)) * SC_OUTS;  // output role
     const int rb = blockIdx.x * SC_ROWS, bh = blockIdx.y;
     const bool rev = blockIdx.z == 1;
     const float *M = rev ? mapAT : mapA, *Bv = rev ? mapBb : mapB;
@@ -648,9 +651,11 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__
     }
     grid_dependency_wait();
     allow_dependent_launch();
-    float2 s = make_float2(0.f, 0.f);
-    if (init) s = *reinterpret_cast<const float2 *>(init + ((size_t)bh * D + rb + orow) * D + oc);
-    reinterpret_cast<float2 *>(st + orow * D)[tid & 31] = s;
+    float s[SC_OUTS];
+#pragma unroll
+    for (int e = 0; e < SC_OUTS; ++e) s[e] = init ? init[((size_t)bh * D + rb + orow) * D + oc + e] : 0.f;
+#pragma unroll
+    for (int e = 0; e < SC_OUTS; ++e) st[orow * D + oc + e] = s[e];
     int issued = 0;  // thread 0: stages issued so far
     auto stage_in = [&](int k) {
         const int cc = rev ? NC - 1 - k : k;
@@ -669,7 +674,8 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__
     for (; k < NC; ++k) {
         const int cc = rev ? NC - 1 - k : k;
         float *out = rev ? Gst + ((size_t)bh * NC + cc) * D * D : Sst + ((size_t)bh * (NC + 1) + cc) * D * D;
-        *reinterpret_cast<float2 *>(out + (size_t)(rb + orow) * D + oc) = s;
+#pragma unroll
+        for (int e = 0; e < SC_OUTS; ++e) out[(size_t)(rb + orow) * D + oc + e] = s[e];
         if (!mbar_wait(smem_u32(&mbar[k % SC_STAGES]), (uint32_t)(k / SC_STAGES) & 1u, wait_ns)) {
             abort_s = 1;
             set_status(status, kDevTimeout);
@@ -693,18 +699,20 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__
 #pragma unroll
         for (int r = 0; r < SC_ROWS; ++r) red[(qm * SC_ROWS + r) * D + col] = part[r];
         __syncthreads();  // partials complete; the state rows of step k are no longer read
-        float2 acc = *reinterpret_cast<const float2 *>(mm + D * D + orow * D + oc);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 pq = *reinterpret_cast<const float2 *>(red + (q * SC_ROWS + orow) * D + oc);
-            acc.x += pq.x;
-            acc.y += pq.y;
+        for (int e = 0; e < SC_OUTS; ++e) {
+            float acc = mm[D * D + orow * D + oc + e];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc += red[(q * SC_ROWS + orow) * D + oc + e];
+            st[orow * D + oc + e] = acc;
+            s[e] = acc;
         }
-        *reinterpret_cast<float2 *>(st + orow * D + oc) = acc;
-        s = acc;
         __syncthreads();  // the new state is written; stage k % SC_STAGES and the partials are free
         if (abort_s) break;
-        if (tid == 0 && k + SC_STAGES < NC) stage_in(k + SC_STAGES);
+        if (tid == 0 && k + SC_STAGES < NC) {
+            fence_async_smem();  // the threads' reads of this stage precede the copy that refills it
+            stage_in(k + SC_STAGES);
+        }
     }
     if (abort_s) {
         // after an expired wait at step k, the stages k .. issued-1 may still be in flight (each
@@ -714,8 +722,11 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__
                 (void)mbar_wait(smem_u32(&mbar[j % SC_STAGES]), (uint32_t)(j / SC_STAGES) & 1u, 1000000000ull);
         return;
     }
-    if (!rev) *reinterpret_cast<float2 *>(Sst + ((size_t)bh * (NC + 1) + NC) * D * D + (size_t)(rb + orow) * D + oc) = s;
-    else if (dS_init) *reinterpret_cast<float2 *>(dS_init + ((size_t)bh * D + rb + orow) * D + oc) = s;
+#pragma unroll
+    for (int e = 0; e < SC_OUTS; ++e) {
+        if (!rev) Sst[((size_t)bh * (NC + 1) + NC) * D * D + (size_t)(rb + orow) * D + oc + e] = s[e];
+        else if (dS_init) dS_init[((size_t)bh * D + rb + orow) * D + oc + e] = s[e];
+    }
 }
 
 // =====================================================================================================

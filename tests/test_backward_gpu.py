@@ -145,17 +145,27 @@ def test_backward_reuses_its_workspace_and_rejects_bad_arguments():
                              g1["dalpha"], g1["du"], g1["dgamma"], g1["deta"], g1["dconv_w"], None, None)
 
 
-@pytest.mark.parametrize("name", ["seqrec_16k"])
+@pytest.mark.parametrize("name", ["seqrec_16k", "long_64k"])
 def test_full_size_sampled_sequences(name):
-    """The whole workload on the GPU in one call; two of its sequences through the oracle."""
+    """The whole workload on the GPU in one call; two of its sequences through the oracle.  The
+    64K-token stress shape (16 heads of 128, L = 8) is the largest: its per-token states and
+    cotangents take 2 B H T dv dk 4 bytes = 137 GB of the device's memory."""
     w = WORKLOADS[name]
     inp = make_workload_inputs(w, seed=0)
     dout, _ = make_cotangents(w.B, w.H, w.T, w.dk, w.dv, seed=0)
-    got = gpu_backward(inp, dout)
     pairs = [(0, 1), (w.B - 1, w.H - 1)]
-    for b, h in pairs:
+    d = to_device(inp)
+    with B.Plan.for_inputs(d, path=1) as p:
+        g = p.backward(d, dout.cuda())
+        torch.cuda.synchronize()
+        p.last_device_status()
+        got = {kk: [vv[b:b + 1, h:h + 1].double().cpu().numpy() for b, h in pairs] for kk, vv in g.items()
+               if kk in PER_HEAD}
+    del d, g
+    torch.cuda.empty_cache()
+    for n_, (b, h) in enumerate(pairs):
         one = {kk: (vv[b:b + 1, h:h + 1].contiguous() if kk not in ("L", "conv_w") else vv) for kk, vv in inp.items()}
         one["conv_w"] = inp["conv_w"][h:h + 1].contiguous()
         ref = oracle_backward(one, dout[b:b + 1, h:h + 1])
-        mine = {kk: got[kk][b:b + 1, h:h + 1] for kk in PER_HEAD}
+        mine = {kk: got[kk][n_] for kk in PER_HEAD}
         compare(mine, ref, w.dtype, PER_HEAD)
