@@ -107,8 +107,11 @@ def test_map_path_replays_from_a_cuda_graph():
 
 def test_map_path_wait_expires_and_the_plan_recovers():
     """A 1 ns bound on every wait of the map and scan kernels: PRISM_ERR_TIMEOUT comes back, and
-    with the default bound the same plan reproduces a fresh plan's output bit for bit."""
-    d = to_device(make_inputs(2, 2, 700, 128, 128, 4, dtype="bf16", seed=570))
+    with the default bound the same plan reproduces a fresh plan's output bit for bit.  Sixteen
+    sequences of 8192 tokens: a thousand chunks through the map kernel and a hundred and
+    twenty-eight ring steps per scan block, so that some wait is still pending when its 1 ns bound
+    is checked."""
+    d = to_device(make_inputs(2, 8, 8192, 128, 128, 4, dtype="bf16", seed=570))
     flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
     with B.Plan.for_inputs(d, path=2) as plan:
         plan.set_option(B.PRISM_OPT_WAIT_NS, 1)
