@@ -903,7 +903,7 @@ def run_backward(args, w):
     dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp_cpu.items()}
     dout = dout_cpu.cuda()
     stream = torch.cuda.current_stream()
-    plan = Bd.Plan.for_inputs(dev)
+    plan = Bd.Plan.for_inputs(dev, path=args.path or None)  # --path 1: the token-serial form
     flush = L2Flush()
     grads = plan.backward(dev, dout, stream=stream)
     for _ in range(warm):
@@ -1007,12 +1007,14 @@ def run_backward(args, w):
                "sample": f"fp64 backward oracle over the first {Ts} tokens of all {w.B * w.H} sequences ({dt:.1f} s)"}
     plan.close()
     if rank == 0:
+        chunked = "bwd_maps" in per_kernel  # which form the library took (the kernels it launched)
         line = {
             "metric": BACKWARD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
             "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            # the chunked form's products take fp16 operands (fp32 accumulation); the token-serial form is fp32
+            "dtype": "f16" if chunked else "f32", "data": "synthetic",
             "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")},
-                       "io": w.dtype, "l2": L2Flush.DESCRIPTION,
+                       "io": w.dtype, "form": "chunked" if chunked else "token-serial", "l2": L2Flush.DESCRIPTION,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline, "path_roofline": path_roofline, "kernels": kernels, "cpu_baseline": cpu,
             "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
