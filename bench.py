@@ -829,7 +829,7 @@ def backward_kernel_bytes(name, w):
     its inputs read once and each of its outputs written once, the intermediates of the design
     included (token-serial form: the per-token states S_{t-1} and cotangents dS_t, fp32, dv dk
     floats per token each; chunked form: four fp32 chunk maps, the chunk states and cotangents,
-    and the fp16 stash of 5 + R tiles per chunk, plus Vt and z)."""
+    and the fp16 stash of 5 + R tiles per chunk)."""
     io = 2 if w.dtype == "bf16" else 4
     th = w.B * w.H * w.T
     R = w.R
@@ -848,10 +848,9 @@ def backward_kernel_bytes(name, w):
     table = {
         "bwd_maps": 2 * qk + v + u + gates + per_row + 4 * chunks * dd + chunks * (5 + R) * tile,
         "bwd_chunk_scan": 4 * chunks * dd + (2 * chunks + w.B * w.H) * dd,
-        "bwd_grad_a": 2 * qk + v + u + gates + per_row + 2 * chunks * dd + chunks * (5 + R) * tile
-        + per_row + dX + th * 8 + 2 * chunks * tile,
-        "bwd_grad_b": 2 * qk + u + gates + per_row + (2 + R) * chunks * tile + 3 * chunks * dd + th * 4
-        + 2 * th * w.dk * 4 + th * R * w.dk * 4 + th * 4,
+        # the chunk's inputs, dout, S_c, S_{c+1}, G_c, the stash read; dv, dX, dbeta, dq, dk, du, dalpha written
+        "bwd_grad": 2 * qk + v + u + gates + per_row + 3 * chunks * dd + chunks * (5 + R) * tile
+        + per_row + dX + th * 4 + 2 * th * w.dk * 4 + th * R * w.dk * 4 + th * 4,
         "bwd_factors": v + th * 8 * R + X,
         # both halves of the scan launch: S_{t-1} forward, dS_t (with z, dx) in reverse
         "bwd_scan": (qk + v + u + gates2 + X + state) + (2 * qk + u + gates2 + per_row + state + per_row + dX),

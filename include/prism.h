@@ -264,6 +264,10 @@ PRISM_API prism_status prism_project(prism_plan_t plan, int D, const void *X, co
  *     is then a set of chunk-sized products (tcgen05 tensor cores, fp16 operands, fp32
  *     accumulation), the WY factors of the forward reused.  Workspace: per-chunk maps, states and
  *     factors, O(B H ceil(T/64) dv dk) -- about 0.5 GB for B H T = 131072 tokens of heads of 64.
+ *     dalpha_t comes from alpha_t dalpha_t = <G, S'> + a suffix sum over the chunk of per-token
+ *     terms of order one, which cancels down to order alpha_t: its rounding error grows like
+ *     1 / alpha_t (within 1e-2 of rms for alpha_t >= 0.5; use PRISM_OPT_PATH = 1, the
+ *     token-serial form, where gates far below that matter).
  *   Token-serial (every other shape, and PRISM_OPT_PATH = 1): fp32 from the io values, keeping
  *     S_{t-1} and dS_t of every token (2 B H T dv dk floats plus per-token buffers).
  * The workspace is owned by the plan (prism_workspace_bytes reports it) and allocated by the first

@@ -13,12 +13,12 @@
 //          gradient kernels reuse go to a per-chunk stash (fp16 tiles in their shared-memory image).
 //   scan   per sequence, direction and 16 state rows: S_c for every chunk (forward) and G_c
 //          (reverse), fp32 SIMT (rows of the state evolve independently).
-//   grad_a one CTA per chunk: the delta-rule values Vt = U' - W S_c^T, z = G_t k_t (Z = Z0 + Wbar
-//          G_c^T), the cotangents of the injection factors dX_l, dbeta, dv = beta z and the
-//          per-token sum sigma_t = beta_t v_t.z_t + sum_l x_tl.dx_tl.
-//   grad_b one CTA per chunk: the masked Grams J = (Vw dO^T) o Dbar, H = (Vw Z^T) o Dbar, the key
-//          side dk, du, the query side dq and dalpha (alpha_t dalpha_t = <G_c, S_{c+1}> + the
-//          suffix sum over the chunk of q.dq - sigma).
+//   grad   one CTA per chunk, two halves on one set of tiles: the delta-rule values Vt = U' - W
+//          S_c^T, z = G_t k_t (Z = Z0 + Wbar G_c^T), the cotangents of the injection factors dX_l,
+//          dbeta, dv = beta z and the per-token sum sigma_t = beta_t v_t.z_t + sum_l x_tl.dx_tl;
+//          then the masked Grams J = (Vw dO^T) o Dbar, H = (Vw Z^T) o Dbar, the key side dk, du,
+//          the query side dq and dalpha (alpha_t dalpha_t = <G_c, S_{c+1}> + the suffix sum over
+//          the chunk of q.dq - sigma).
 // The token-local chain, gain and convolution backwards then run as in the token-serial pass.
 //
 // Chunk algebra (local index i, j; lambda_i = sum_{m<=i} ln alpha_m; D_ij = e^{lambda_i - lambda_j};
@@ -62,12 +62,11 @@ constexpr int SCAN_NT = 256;          // threads of the scan
 constexpr uint32_t PANEL = 8192;      // [64 rows][64 cols] 16-bit SW128
 constexpr int STASH = 8;              // stash panels per chunk (maps kernel): U', W, Wbar, Z0, E0, X_0..X_2
 enum { ST_UP = 0, ST_W = 1, ST_WB = 2, ST_Z0 = 3, ST_E0 = 4, ST_X = 5 };
-constexpr int VZ = 2;                 // per chunk (grad_a): Vt, Z
 
 // per-token scalars (floats from the scalar region): beta, lambda, Gamma, colf, beta Gamma, gamma, eta
 constexpr int SC_BETA = 0, SC_LAM = 64, SC_GAM = 128, SC_COLF = 192, SC_BG = 256, SC_GM = 320,
               SC_ET = 320 + 64 * RMAX, SC_HALO = 320 + 128 * RMAX, SC_RED = SC_HALO + 3 * D;
-constexpr int SC_FLOATS = SC_RED + 20 * 64 + 32;  // + per-token partial sums (fixed slots, summed in a fixed order)
+constexpr int SC_FLOATS = SC_RED + 24 * 64 + 32;  // + per-token partial sums (fixed slots, summed in a fixed order)
 
 struct Params {
     const __nv_bfloat16 *v;          // [BH][T][64]
@@ -77,12 +76,10 @@ struct Params {
     const float *dout;               // [BH][T][64]
     float *mapA, *mapAT, *mapB, *mapBb;  // [chunks][64][64]
     __half *stash;                   // [chunks][STASH][4096]
-    __half *vz;                      // [chunks][VZ][4096]
     const float *Sst;                // [BH][NC + 1][64][64]  state entering each chunk (and the final one)
     const float *Gst;                // [BH][NC][64][64]      cotangent flowing into each chunk's last state
     float *dq, *dk, *dv, *dbeta, *dalpha, *du;
     float *dX;                       // [BH T][R][64]
-    float *sigma;                    // [BH T]
     int *status;
     int H, T, R, NC;
     unsigned long long wait_ns;
@@ -730,28 +727,43 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__
 }
 
 // =====================================================================================================
-// grad_a: shared-memory panels
-namespace ga {
+// grad: the cotangents of one chunk, one CTA per chunk.  Two halves on one set of tiles:
+//   values   [K; W] S^T -> E and Vt;  [Wbar; colf U_0] G^T -> z, then + [0; P_0^T] dO - [0; Mku_0^T]
+//            beta Z -> dX_0 (likewise dX_1, dX_2);  Akk Vt -> dbeta;  dv = beta z;
+//            sigma_t = beta_t v_t.z_t + sum_l x_tl.dx_tl
+//   keys     [Vt; X_0] [dO | Z]^T, [X_1; X_2] [dO | Z]^T -> J, H;  [colf Vt; colf X_0] G + [J_0; J_1] Q
+//            - [H_0; H_1] beta K -> dk's write part and du_0 (likewise du_1, du_2);
+//            [Gamma dO; Gamma Z] S + sum_b [J_b^T; H_b^T] Kw_b -> dq and dk's state part; dalpha.
+// Vt, Z, X and dO stay in shared memory between the halves; E stays in the registers of the
+// threads (rows < 64) that form dbeta.  Shared-memory panels (index x PANEL from a 1024-aligned
+// base); the second half's tiles take the first half's dead ones.
+namespace gk {
 enum {
-    Q = 0, K = 1, W = 2, U0 = 3, WB = 6, CU0 = 7, S0 = 10, GB = 11, DO = 12, ZERO = 13, P0 = 14, AKK = 17,
-    MKU0 = 18, NPANELS = 21,
-    VT = 0, NBZ = 3, E32 = 4  // after the first products: Vt in Q's place, -beta Z in U_0's, E (fp32) in U_1, U_2's
+    Q = 0, K = 1, W = 2, U0 = 3, VT = 6, X0 = 7, DO = 10, Z = 11, S0 = 12, GB = 13, WB = 14, CU0 = 15, ZERO = 18,
+    P0 = 19, AKK = 22, MKU0 = 23, NPANELS = 26,
+    NBK = 2,    // -beta K, in W's place (W is read by the first products only)
+    J0 = 14,    // J_0..J_3 over Wbar and colf U_l
+    H0 = 18,    // H_0..H_3 over the zero tile and P_l (H_b = J_b + 4 panels)
+    DKW = 22    // dk's write part, fp32 [64][64], over Akk and Mku_0
 };
 constexpr uint32_t SC_OFF = NPANELS * PANEL;
 constexpr uint32_t SMEM = SC_OFF + SC_FLOATS * 4 + 1024;
 static_assert(SMEM <= 232448, "shared memory budget");
+static_assert(H0 - J0 == 4 && X0 == VT + 1 && Z == DO + 1 && W == K + 1 && CU0 == WB + 1, "stacked operands");
+// tensor memory columns (512): first half, then the second half over the dead first-half columns
 constexpr uint32_t TM_G1 = 0, TM_D1 = 256, TM_D2 = 320, TM_D3 = 384, TM_DF = 448;
-}  // namespace ga
+constexpr uint32_t TM_C = 0, TM_D = 256, TM_E = 384;
+}  // namespace gk
 
 __global__ void __launch_bounds__(NT, 1)
-    grad_a_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_u, Params p)
+    grad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_u, Params p)
 {
-    using namespace ga;
+    using namespace gk;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint32_t tmem_base_s;
-    __shared__ __align__(8) uint64_t mbar[4];  // 0 loads, 1 first products, 2 second products, 3 drain
+    __shared__ __align__(8) uint64_t mbar[6];  // 0 loads, 1-4 products, 5 drain
     __shared__ int abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, sub = warp >> 2;
     const int row = quad * 32 + lane;
@@ -761,18 +773,20 @@ __global__ void __launch_bounds__(NT, 1)
     const size_t tok0 = (size_t)bh * p.T + t0;
     float *sc = reinterpret_cast<float *>(sm + SC_OFF);
     const float *s_beta = sc + SC_BETA, *s_lam = sc + SC_LAM, *s_gam = sc + SC_GAM, *s_colf = sc + SC_COLF;
-    // per-token partial sums, one slot per source so that the totals do not depend on timing:
-    // sigma [16][64] (slots 0-3: beta v.z by column part; 4 + 4 l + part: x_l.dx_l), dbeta [4][64]
-    float *s_sig = sc + SC_RED, *s_db = sc + SC_RED + 16 * 64;
+    // per-token partial sums in fixed slots (summed in a fixed order, so the pass is deterministic):
+    // sigma [16][64] (slots 0-3: beta v.z by column part; 4 + 4 l + part: x_l.dx_l), dbeta [4][64],
+    // q.dq [4][64]; <G, S'> per warp [16]
+    float *s_sig = sc + SC_RED, *s_db = s_sig + 16 * 64, *s_qdq = s_db + 4 * 64, *s_Fw = s_qdq + 4 * 64;
     auto P = [&](int idx) { return sm + (uint32_t)idx * PANEL; };
     const uint32_t sbase = smem_u32(sm);
     const uint64_t dbase = sdesc(sbase, 0, 0);
     const uint8_t *stash = reinterpret_cast<const uint8_t *>(p.stash) + (size_t)chunk * STASH * PANEL;
-    uint8_t *vz = reinterpret_cast<uint8_t *>(p.vz) + (size_t)chunk * VZ * PANEL;
+    const float *Gc = p.Gst + ((size_t)bh * p.NC + c) * D * D;
+    const float *Sc = p.Sst + ((size_t)bh * (p.NC + 1) + c) * D * D;
 
     if (tid == 0) {
         abort_s = 0;
-        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&mbar[i]), 1);
+        for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&mbar[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 512);
@@ -785,12 +799,13 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t mb_ld = smem_u32(&mbar[0]);
     bool pend_ld = false;
     if (tid == 0) {
-        mbar_expect_tx(mb_ld, (uint32_t)(4 + R) * PANEL);
+        mbar_expect_tx(mb_ld, (uint32_t)(4 + 2 * R) * PANEL);
         tma_load_3d(sbase + Q * PANEL, &tm_q, mb_ld, 0, t0, bh);
         tma_load_3d(sbase + K * PANEL, &tm_k, mb_ld, 0, t0, bh);
         for (int l = 0; l < R; ++l) tma_load_4d(sbase + (U0 + l) * PANEL, &tm_u, mb_ld, 0, l, t0, bh);
         bulk_load(sbase + W * PANEL, stash + ST_W * PANEL, PANEL, mb_ld);
         bulk_load(sbase + WB * PANEL, stash + ST_WB * PANEL, PANEL, mb_ld);
+        for (int l = 0; l < R; ++l) bulk_load(sbase + (X0 + l) * PANEL, stash + (ST_X + l) * PANEL, PANEL, mb_ld);
         pend_ld = true;
     }
     auto expired = [&]() {
@@ -805,14 +820,26 @@ __global__ void __launch_bounds__(NT, 1)
         else expired();
     }
     load_scalars(sc, p, tok0, n, tid);
-    for (int e = tid; e < 20 * 64; e += NT) sc[SC_RED + e] = 0.f;
-    f32_to_panel(P(S0), p.Sst + ((size_t)bh * (p.NC + 1) + c) * D * D, D, tid);
-    f32_to_panel(P(GB), p.Gst + ((size_t)bh * p.NC + c) * D * D, D, tid);
+    for (int e = tid; e < 24 * 64; e += NT) s_sig[e] = 0.f;  // sigma, dbeta, q.dq slots
+    f32_to_panel(P(S0), Sc, D, tid);
+    f32_to_panel(P(GB), Gc, D, tid);
     f32_to_panel(P(DO), p.dout + tok0 * D, n, tid);
     for (int e = tid; e < 512; e += NT) reinterpret_cast<uint4 *>(P(ZERO))[e] = make_uint4(0, 0, 0, 0);
+    {  // F0 = <G_c, S_{c+1}> (for dalpha), partial per warp
+        const float4 *g4 = reinterpret_cast<const float4 *>(Gc), *s4 = reinterpret_cast<const float4 *>(Sc + D * D);
+        float part = 0.f;
+#pragma unroll
+        for (int q = 0; q < D * D / 4 / NT; ++q) {
+            const float4 a = g4[tid + NT * q], b = s4[tid + NT * q];
+            part = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, part))));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) s_Fw[warp] = part;
+    }
     __syncthreads();
 
-    float z[CW];  // rows < 64: this thread's columns of z_i (kept for dbeta)
+    float z[CW], Ev[CW];  // rows < 64: this thread's columns of z_i and of E_i (kept for dbeta)
     do {
         if (abort_s) break;
         // ---- the input tiles to fp16 in place; colf U_l copies ----------------------------------------------
@@ -821,7 +848,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int l = 0; l < R; ++l) panel_to_f16(P(U0 + l), P(CU0 + l), s_colf, 1.f, tid);
         fence_async_smem();
         __syncthreads();
-        // ---- Grams [Q; K] [K | U_l]^T;  [K; W] S^T;  [Wbar; colf U_0] G^T;  [colf U_1; colf U_2] G^T -------
+        // ---- values: Grams [Q; K] [K | U_l]^T;  [K; W] S^T;  [Wbar; colf U_0] G^T;  [colf U_1; colf U_2] G^T ----
         if (tid == 0) {
             const uint32_t id = idesc_f16(128, 64, 0, 0);
             for (int b = 0; b <= R; ++b)
@@ -860,24 +887,19 @@ __global__ void __launch_bounds__(NT, 1)
                     decay_row(v, s_lam, i, j0, true);
                     st_row_h(P(P0 + l), i, j0, v);
                 }
-                // E = E0 - Gamma_i (K S^T)_i  (fp32)
+                // E = E0 - Gamma_i (K S^T)_i  (fp32, kept in registers for dbeta)
                 tmem_ld(tmem + TM_D1 + lane_off + (uint32_t)j0, v);
-                h8_to_f(pre[0], s2);
+                h8_to_f(pre[0], Ev);
                 const float gi = s_gam[i];
 #pragma unroll
-                for (int q = 0; q < CW; ++q) s2[q] -= gi * v[q];
-                st_row_f(reinterpret_cast<float *>(P(E32)) + i * D + j0, s2);
-                // z = Z0 + (Wbar G^T)_i;  -beta z;  dv = beta z;  sigma += beta v.z
+                for (int q = 0; q < CW; ++q) Ev[q] -= gi * v[q];
+                // z = Z0 + (Wbar G^T)_i;  Z (fp16);  dv = beta z;  sigma += beta v.z
                 tmem_ld(tmem + TM_D2 + lane_off + (uint32_t)j0, v);
                 h8_to_f(pre[1], s2);
                 const float b = s_beta[i];
 #pragma unroll
-                for (int q = 0; q < CW; ++q) {
-                    z[q] = s2[q] + v[q];
-                    v[q] = -b * z[q];
-                }
-                st_row_h(P(NBZ), i, j0, v);
-                st_row_h(vz + PANEL, i, j0, z);
+                for (int q = 0; q < CW; ++q) z[q] = s2[q] + v[q];
+                st_row_h(P(Z), i, j0, z);
                 if (i < n) {
                     float dvv[CW];
 #pragma unroll
@@ -894,13 +916,16 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             } else {
                 const int i = row - 64;
-                // Akk = (K K^T) o D (j < i);  Mku_l = (K U_l^T) o D (j < i)
+                const float nb = -s_beta[i];
+                // Akk = (K K^T) o D (j < i);  -beta_i Mku_l = -beta_i (K U_l^T) o D (j < i)
                 tmem_ld(tmem + TM_G1 + lane_off + (uint32_t)j0, v);
                 decay_row(v, s_lam, i, j0, false);
                 st_row_h(P(AKK), i, j0, v);
                 for (int l = 0; l < R; ++l) {
                     tmem_ld(tmem + TM_G1 + 64 * (l + 1) + lane_off + (uint32_t)j0, v);
                     decay_row(v, s_lam, i, j0, false);
+#pragma unroll
+                    for (int q = 0; q < CW; ++q) v[q] *= nb;
                     st_row_h(P(MKU0 + l), i, j0, v);
                 }
                 // Vt = U' - (W S^T)_i
@@ -909,52 +934,46 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int q = 0; q < CW; ++q) s2[q] -= v[q];
                 st_row_h(P(VT), i, j0, s2);
-                st_row_h(vz, i, j0, s2);
+                // -beta K (for the keys half), in W's place: the products that read W are complete
+                ld_row_h(P(K), i, j0, s2);
+#pragma unroll
+                for (int q = 0; q < CW; ++q) s2[q] *= nb;
+                st_row_h(P(NBK), i, j0, s2);
             }
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
-        // ---- dX_l += P_l^T dO - Mku_l^T (beta Z);  Akk Vt ----------------------------------------------------
+        // ---- dX_l += P_l^T dO + (-beta Mku_l)^T Z;  Akk Vt ---------------------------------------------------
         if (tid == 0) {
             fence_after_sync();
             const uint32_t id = idesc_f16(128, 64, 1, 1);
             if (R >= 1) {
                 mma_k64(tmem + TM_D2, mn(dbase, ZERO * PANEL, (P0 - ZERO) * PANEL), true, mn(dbase, DO * PANEL, PANEL),
                         true, id, true);
-                mma_k64(tmem + TM_D2, mn(dbase, ZERO * PANEL, (MKU0 - ZERO) * PANEL), true, mn(dbase, NBZ * PANEL, PANEL),
+                mma_k64(tmem + TM_D2, mn(dbase, ZERO * PANEL, (MKU0 - ZERO) * PANEL), true, mn(dbase, Z * PANEL, PANEL),
                         true, id, true);
             }
             if (R >= 2) {
                 mma_k64(tmem + TM_D3, mn(dbase, (P0 + 1) * PANEL, PANEL), true, mn(dbase, DO * PANEL, PANEL), true, id,
                         true);
-                mma_k64(tmem + TM_D3, mn(dbase, (MKU0 + 1) * PANEL, PANEL), true, mn(dbase, NBZ * PANEL, PANEL), true,
-                        id, true);
+                mma_k64(tmem + TM_D3, mn(dbase, (MKU0 + 1) * PANEL, PANEL), true, mn(dbase, Z * PANEL, PANEL), true, id,
+                        true);
             }
             mma_k64(tmem + TM_DF, km(dbase, AKK * PANEL), false, mn(dbase, VT * PANEL, PANEL), true,
                     idesc_f16(128, 64, 0, 1), false);
             mma_commit(smem_u32(&mbar[2]));
-        }
-        uint4 prx[2][CW / 8];  // the X rows this thread's dX rows pair with (rows < 64: X_1; else X_0, X_2)
-        {
-            const int j0 = CW * sub, i = row & 63;
-            if (row < 64) {
-                if (R >= 2) ld_row_raw(stash + (ST_X + 1) * PANEL, i, j0, prx[0]);
-            } else {
-                if (R >= 1) ld_row_raw(stash + ST_X * PANEL, i, j0, prx[0]);
-                if (R >= 3) ld_row_raw(stash + (ST_X + 2) * PANEL, i, j0, prx[1]);
-            }
         }
         wait_all(2, 0);
         fence_after_sync();
         {
             const int j0 = CW * sub;
             float v[CW], x[CW];
-            auto dx_out = [&](uint32_t col, int l, int i, const uint4 (&xr)[CW / 8]) {  // dX_l row i -> global, sigma += x.dx
+            auto dx_out = [&](uint32_t col, int l, int i) {  // dX_l row i -> global, sigma += x.dx
                 tmem_ld(tmem + col + lane_off + (uint32_t)j0, v);
                 if (i < n) {
                     st_row_f(p.dX + ((tok0 + i) * R + l) * D + j0, v);
-                    h8_to_f(xr, x);
+                    ld_row_h(P(X0 + l), i, j0, x);
                     float part = 0.f;
 #pragma unroll
                     for (int q = 0; q < CW; ++q) part = fmaf(x[q], v[q], part);
@@ -963,151 +982,31 @@ __global__ void __launch_bounds__(NT, 1)
             };
             if (row < 64) {
                 const int i = row;
-                if (R >= 2) dx_out(TM_D3, 1, i, prx[0]);
+                if (R >= 2) dx_out(TM_D3, 1, i);
                 // dbeta_i = sum_c z_ic (E_ic - (Akk Vt)_ic)
                 tmem_ld(tmem + TM_DF + lane_off + (uint32_t)j0, v);
-                const float *Er = reinterpret_cast<const float *>(P(E32)) + i * D + j0;
                 float part = 0.f;
 #pragma unroll
-                for (int q = 0; q < CW; ++q) part = fmaf(z[q], Er[q] - v[q], part);
+                for (int q = 0; q < CW; ++q) part = fmaf(z[q], Ev[q] - v[q], part);
                 s_db[sub * 64 + i] = part;
             } else {
                 const int i = row - 64;
-                if (R >= 1) dx_out(TM_D2, 0, i, prx[0]);
-                if (R >= 3) dx_out(TM_D3, 2, i, prx[1]);
+                if (R >= 1) dx_out(TM_D2, 0, i);
+                if (R >= 3) dx_out(TM_D3, 2, i);
             }
         }
+        fence_before_sync();
         __syncthreads();
-        if (tid < n) {
-            p.dbeta[tok0 + tid] = (s_db[tid] + s_db[64 + tid]) + (s_db[128 + tid] + s_db[192 + tid]);
-            float sg = 0.f;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) sg += s_sig[k * 64 + tid];
-            p.sigma[tok0 + tid] = sg;
-        }
-    } while (0);
-
-    if (tid == 0 && abort_s) {
-        const uint64_t drain_ns = 1000000000ull;
-        if (pend_ld) (void)mbar_wait(mb_ld, 0, drain_ns);
-        const uint32_t mb_drain = smem_u32(&mbar[3]);
-        mma_commit(mb_drain);
-        (void)mbar_wait(mb_drain, 0, drain_ns);
-    }
-    fence_before_sync();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
-}
-
-// =====================================================================================================
-// grad_b: shared-memory panels
-namespace gb {
-enum {
-    Q = 0, K = 1, U0 = 2, VT = 5, X0 = 6, DO = 9, Z = 10, S0 = 11, GB = 12, NBK = 13, J0 = 14, H0 = 18, DKW = 22,
-    NPANELS = 24
-};
-constexpr uint32_t SC_OFF = NPANELS * PANEL;
-constexpr uint32_t SMEM = SC_OFF + SC_FLOATS * 4 + 1024;
-static_assert(SMEM <= 232448, "shared memory budget");
-constexpr uint32_t TM_C = 0, TM_D = 256, TM_E = 384;
-}  // namespace gb
-
-__global__ void __launch_bounds__(NT, 1)
-    grad_b_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_u, Params p)
-{
-    using namespace gb;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ uint32_t tmem_base_s;
-    __shared__ __align__(8) uint64_t mbar[4];  // 0 loads, 1 Grams, 2 products, 3 drain
-    __shared__ int abort_s;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, sub = warp >> 2;
-    const int row = quad * 32 + lane;
-    const int R = p.R;
-    const int chunk = blockIdx.x, bh = chunk / p.NC, c = chunk % p.NC;
-    const int t0 = c * C, n = min(C, p.T - t0);
-    const size_t tok0 = (size_t)bh * p.T + t0;
-    float *sc = reinterpret_cast<float *>(sm + SC_OFF);
-    const float *s_beta = sc + SC_BETA, *s_lam = sc + SC_LAM, *s_gam = sc + SC_GAM, *s_colf = sc + SC_COLF;
-    float *s_qdq = sc + SC_RED, *s_Fw = sc + SC_RED + 4 * 64;  // q.dq [4][64] by column part; <G, S'> per warp
-    auto P = [&](int idx) { return sm + (uint32_t)idx * PANEL; };
-    const uint32_t sbase = smem_u32(sm);
-    const uint64_t dbase = sdesc(sbase, 0, 0);
-    const uint8_t *stash = reinterpret_cast<const uint8_t *>(p.stash) + (size_t)chunk * STASH * PANEL;
-    const uint8_t *vz = reinterpret_cast<const uint8_t *>(p.vz) + (size_t)chunk * VZ * PANEL;
-    const float *Gc = p.Gst + ((size_t)bh * p.NC + c) * D * D;
-    const float *Sc = p.Sst + ((size_t)bh * (p.NC + 1) + c) * D * D;
-
-    if (tid == 0) {
-        abort_s = 0;
-        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&mbar[i]), 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 512);
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tmem = tmem_base_s, lane_off = (uint32_t)(quad * 32) << 16;
-    grid_dependency_wait();  // grad_a's values, z and sigma
-    allow_dependent_launch();
-    const uint32_t mb_ld = smem_u32(&mbar[0]);
-    bool pend_ld = false;
-    if (tid == 0) {
-        mbar_expect_tx(mb_ld, (uint32_t)(4 + 2 * R) * PANEL);
-        tma_load_3d(sbase + Q * PANEL, &tm_q, mb_ld, 0, t0, bh);
-        tma_load_3d(sbase + K * PANEL, &tm_k, mb_ld, 0, t0, bh);
-        for (int l = 0; l < R; ++l) tma_load_4d(sbase + (U0 + l) * PANEL, &tm_u, mb_ld, 0, l, t0, bh);
-        bulk_load(sbase + VT * PANEL, vz, PANEL, mb_ld);
-        bulk_load(sbase + Z * PANEL, vz + PANEL, PANEL, mb_ld);
-        for (int l = 0; l < R; ++l) bulk_load(sbase + (X0 + l) * PANEL, stash + (ST_X + l) * PANEL, PANEL, mb_ld);
-        pend_ld = true;
-    }
-    auto expired = [&]() {
-        abort_s = 1;
-        set_status(p.status, kDevTimeout);
-    };
-    auto wait_all = [&](int b, uint32_t ph) {
-        if (!mbar_wait(smem_u32(&mbar[b]), ph, p.wait_ns)) expired();
-    };
-    if (tid == 0) {  // thread 0 waits for the tiles at once; the others stage
-        if (mbar_wait(mb_ld, 0, p.wait_ns)) pend_ld = false;
-        else expired();
-    }
-    load_scalars(sc, p, tok0, n, tid);
-    if (tid < 4 * 64) s_qdq[tid] = 0.f;
-    f32_to_panel(P(S0), Sc, D, tid);
-    f32_to_panel(P(GB), Gc, D, tid);
-    f32_to_panel(P(DO), p.dout + tok0 * D, n, tid);
-    {  // F0 = <G_c, S_{c+1}>
-        const float4 *g4 = reinterpret_cast<const float4 *>(Gc), *s4 = reinterpret_cast<const float4 *>(Sc + D * D);
-        float part = 0.f;
-#pragma unroll
-        for (int q = 0; q < D * D / 4 / NT; ++q) {
-            const float4 a = g4[tid + NT * q], b = s4[tid + NT * q];
-            part = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, part))));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (lane == 0) s_Fw[warp] = part;
-    }
-    __syncthreads();
-
-    do {
-        if (abort_s) break;
-        panel_to_f16(P(Q), nullptr, nullptr, 1.f, tid);
-        panel_to_f16(P(K), P(NBK), s_beta, -1.f, tid);
-        for (int l = 0; l < R; ++l) panel_to_f16(P(U0 + l), nullptr, nullptr, 1.f, tid);
-        fence_async_smem();
-        __syncthreads();
-        // ---- [Vt; X_0] [dO | Z]^T and [X_1; X_2] [dO | Z]^T ---------------------------------------------------
+        if (tid < n) p.dbeta[tok0 + tid] = (s_db[tid] + s_db[64 + tid]) + (s_db[128 + tid] + s_db[192 + tid]);
+        // ---- keys: [Vt; X_0] [dO | Z]^T and [X_1; X_2] [dO | Z]^T -------------------------------------------
         if (tid == 0) {
+            fence_after_sync();
             const uint32_t id = idesc_f16(128, 128, 0, 0);
             mma_k64(tmem + TM_C, km(dbase, VT * PANEL), false, km(dbase, DO * PANEL), false, id, false);
             if (R >= 2) mma_k64(tmem + TM_C + 128, km(dbase, (X0 + 1) * PANEL), false, km(dbase, DO * PANEL), false, id, false);
-            mma_commit(smem_u32(&mbar[1]));
+            mma_commit(smem_u32(&mbar[3]));
         }
-        wait_all(1, 0);
+        wait_all(3, 0);
         fence_after_sync();
         // J_b[m][j] = (w_m . dout_j) D_{j,m} (j >= m), H_b[m][j] = (w_m . z_j) D_{j,m} (j > m); thread
         // (quad, sub): row `row` of group sub & 1 (block b = 2 (sub & 1) + row / 64), the 32 columns
@@ -1147,9 +1046,9 @@ __global__ void __launch_bounds__(NT, 1)
             for (int b = 0; b <= R; ++b)
                 mma_k64(tmem + TM_E, mn(dbase, (J0 + b) * PANEL, (H0 - J0) * PANEL), true,
                         mn(dbase, (b == 0 ? K : U0 + b - 1) * PANEL, PANEL), true, idesc_f16(128, 64, 1, 1), true);
-            mma_commit(smem_u32(&mbar[2]));
+            mma_commit(smem_u32(&mbar[4]));
         }
-        wait_all(2, 0);
+        wait_all(4, 0);
         fence_after_sync();
         float *dkw = reinterpret_cast<float *>(P(DKW));
         {
@@ -1200,13 +1099,15 @@ __global__ void __launch_bounds__(NT, 1)
         }
         // alpha_i dalpha_i = F0 + sum_{j >= i} (q_j.dq_j - sigma_j)
         if (warp == 0) {
+            auto term = [&](int i) {
+                float sg = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) sg += s_sig[k * 64 + i];
+                return (s_qdq[i] + s_qdq[64 + i]) + (s_qdq[128 + i] + s_qdq[192 + i]) - sg;
+            };
             const int i0 = 2 * lane, i1 = i0 + 1;
-            const float a0 = i0 < n ? (s_qdq[i0] + s_qdq[64 + i0]) + (s_qdq[128 + i0] + s_qdq[192 + i0]) -
-                                          p.sigma[tok0 + i0]
-                                    : 0.f;
-            const float a1 = i1 < n ? (s_qdq[i1] + s_qdq[64 + i1]) + (s_qdq[128 + i1] + s_qdq[192 + i1]) -
-                                          p.sigma[tok0 + i1]
-                                    : 0.f;
+            const float a0 = i0 < n ? term(i0) : 0.f;
+            const float a1 = i1 < n ? term(i1) : 0.f;
             float x = a0 + a1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -1221,10 +1122,11 @@ __global__ void __launch_bounds__(NT, 1)
         }
     } while (0);
 
+    // drain (after an expired wait): let the copies and products in flight land, bounded
     if (tid == 0 && abort_s) {
         const uint64_t drain_ns = 1000000000ull;
         if (pend_ld) (void)mbar_wait(mb_ld, 0, drain_ns);
-        const uint32_t mb_drain = smem_u32(&mbar[3]);
+        const uint32_t mb_drain = smem_u32(&mbar[5]);
         mma_commit(mb_drain);
         (void)mbar_wait(mb_drain, 0, drain_ns);
     }
@@ -1264,11 +1166,10 @@ bool bt_encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dim
 }
 
 // workspace of the chunked backward: maps (4 x fp32 64 x 64 per chunk), the stash (8 fp16 panels per
-// chunk), Vt and Z (2 panels per chunk), the chunk states and cotangents, dX, sigma, and the
-// convolution scratch of the token-local kernels
+// chunk), the chunk states and cotangents, dX, and the convolution scratch of the token-local kernels
 struct BtCarve {
-    float *mapA, *mapAT, *mapB, *mapBb, *Sst, *Gst, *dX, *sigma, *dH, *dWp;
-    __half *stash, *vz;
+    float *mapA, *mapAT, *mapB, *mapBb, *Sst, *Gst, *dX, *dH, *dWp;
+    __half *stash;
 };
 
 size_t bt_carve(const Shape &s, void *base, BtCarve *out)
@@ -1277,16 +1178,14 @@ size_t bt_carve(const Shape &s, void *base, BtCarve *out)
     BtCarve *w = out ? out : &scratch;
     const size_t chunks = (size_t)s.BH * s.NC, dd = (size_t)s.dk * s.dv, th = (size_t)s.BH * s.T;
     const int ntile = backward_conv_tiles(s.T);
-    const size_t bytes[12] = {chunks * dd * 4, chunks * dd * 4, chunks * dd * 4, chunks * dd * 4,
+    const size_t bytes[10] = {chunks * dd * 4, chunks * dd * 4, chunks * dd * 4, chunks * dd * 4,
                               (size_t)s.BH * (s.NC + 1) * dd * 4, chunks * dd * 4,
-                              th * (size_t)(s.R > 0 ? s.R : 1) * s.dv * 4, th * 4, th * s.dv * 4,
-                              (size_t)s.BH * ntile * 4 * s.dv * 4, chunks * bt::STASH * bt::PANEL,
-                              chunks * bt::VZ * bt::PANEL};
-    void **dst[12] = {(void **)&w->mapA, (void **)&w->mapAT, (void **)&w->mapB, (void **)&w->mapBb, (void **)&w->Sst,
-                      (void **)&w->Gst, (void **)&w->dX, (void **)&w->sigma, (void **)&w->dH, (void **)&w->dWp,
-                      (void **)&w->stash, (void **)&w->vz};
+                              th * (size_t)(s.R > 0 ? s.R : 1) * s.dv * 4, th * s.dv * 4,
+                              (size_t)s.BH * ntile * 4 * s.dv * 4, chunks * bt::STASH * bt::PANEL};
+    void **dst[10] = {(void **)&w->mapA, (void **)&w->mapAT, (void **)&w->mapB, (void **)&w->mapBb, (void **)&w->Sst,
+                      (void **)&w->Gst, (void **)&w->dX, (void **)&w->dH, (void **)&w->dWp, (void **)&w->stash};
     size_t off = 0;
-    for (int i = 0; i < 12; ++i) {
+    for (int i = 0; i < 10; ++i) {
         if (base) *dst[i] = static_cast<char *>(base) + off;
         off += (bytes[i] + 1023) & ~(size_t)1023;
     }
@@ -1311,10 +1210,7 @@ cudaError_t backward_tc_prepare()
     if ((e = cudaFuncSetAttribute(bt::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bt::SCAN_SMEM)) !=
         cudaSuccess)
         return e;
-    if ((e = cudaFuncSetAttribute(bt::grad_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bt::ga::SMEM)) !=
-        cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(bt::grad_b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bt::gb::SMEM);
+    return cudaFuncSetAttribute(bt::grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bt::gk::SMEM);
 }
 
 cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_status, long long wait_ns,
@@ -1355,7 +1251,6 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     p.mapB = w.mapB;
     p.mapBb = w.mapBb;
     p.stash = w.stash;
-    p.vz = w.vz;
     p.Sst = w.Sst;
     p.Gst = w.Gst;
     p.dq = a.dq;
@@ -1365,7 +1260,6 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     p.dalpha = a.dalpha;
     p.du = a.du;
     p.dX = w.dX;
-    p.sigma = w.sigma;
     p.status = d_status;
     p.H = s.H;
     p.T = s.T;
@@ -1401,16 +1295,11 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
                            p.wait_ns);
     tm.end();
     if (e != cudaSuccess) return e;
-    tm.begin("bwd_grad_a");
+    tm.begin("bwd_grad");
     cfg.gridDim = dim3(nchunks);
     cfg.blockDim = dim3(NT);
-    cfg.dynamicSmemBytes = ga::SMEM;
-    e = cudaLaunchKernelEx(&cfg, grad_a_kernel, mq, mk_, mu, p);
-    tm.end();
-    if (e != cudaSuccess) return e;
-    tm.begin("bwd_grad_b");
-    cfg.dynamicSmemBytes = gb::SMEM;
-    e = cudaLaunchKernelEx(&cfg, grad_b_kernel, mq, mk_, mu, p);
+    cfg.dynamicSmemBytes = gk::SMEM;
+    e = cudaLaunchKernelEx(&cfg, grad_kernel, mq, mk_, mu, p);
     tm.end();
     if (e != cudaSuccess) return e;
     return backward_token_local(s, PRISM_BF16, a, w.dX, w.dH, w.dWp, tm);

@@ -139,3 +139,31 @@ def test_portable_and_chunked_forms_agree():
     ts, ws_ts = gpu_backward(inp, dout, dS_final, path=1)
     assert ws_tc != ws_ts
     compare(tc, ts, list(PER_HEAD) + ["dconv_w", "dv_hist", "dS_init"])
+
+
+@pytest.mark.parametrize("alpha_div", [4.0, 1.0, 0.25])
+def test_chunked_backward_under_strong_decay(alpha_div):
+    """Gates alpha = exp(-softplus(N(0, 1)) / alpha_div) below the workloads' (alpha_div = 4: alpha
+    from ~0.3; 1: median ~0.5; 0.25: median ~0.06, a chunk decaying by e^-200 and more): the pair
+    decays underflow inside a chunk and every cotangent but dalpha meets the bar.  dalpha comes from
+    alpha_t dalpha_t = <G, S'> + a suffix sum of per-token terms of order one that cancels down to
+    order alpha_t, so its rounding error grows like 1 / alpha_t; it meets the bar on the tokens
+    with alpha_t >= 0.5 (the workloads' gates are >= 0.73)."""
+    inp = make_inputs(1, 2, 300, 64, 64, 4, dtype="bf16", seed=44, alpha_div=alpha_div)
+    dout, dS_final = make_cotangents(1, 2, 300, 64, 64, seed=44, with_state=True)
+    S0, vh = side_inputs(1, 2, 64, 300)
+    got, _ = gpu_backward(inp, dout, dS_final, vh, S0)
+    ref = oracle_backward(inp, dout, dS_final, vh, S0)
+    for kk, vv in got.items():
+        assert np.all(np.isfinite(vv)), kk
+    keys = [kk for kk in list(PER_HEAD) + ["dconv_w", "dv_hist", "dS_init"] if kk != "dalpha"]
+    compare(got, ref, keys)
+    alpha = inp["alpha"].double().numpy()
+    for lo in (0.9, 0.5, 0.25, 0.1, 0.0):
+        sel = alpha >= lo
+        if sel.any():
+            print(f"dalpha on alpha >= {lo}: {sel.mean():.2f} of tokens, err {rel_err(got['dalpha'][sel], ref['dalpha'][sel]):.2e}")
+    sel = alpha >= 0.5
+    if sel.any():
+        e = rel_err(got["dalpha"][sel], ref["dalpha"][sel])
+        assert e <= TC_BAR, e
