@@ -249,3 +249,92 @@ def test_chunk_maps_reproduce_the_forward_final_state():
                                inp["eta"], inp["conv_w"], inp["L"], S_init=S_init[None, None], v_hist=vh[None, None],
                                want_state=True, nthreads=1)
     np.testing.assert_allclose(got["S_final"], np.asarray(ref["S_final"])[0, 0], rtol=1e-10, atol=1e-12)
+
+
+def exact_dalpha(q, k, v, u, beta, alpha, X, dO, pc, S0, G, Vt, Z):
+    """alpha_t dalpha_t = <G_t, alpha_t S_{t-1}> - beta_t z_t . yhat_t from the chunk's quantities with
+    no cancellation: every term carries a decay that spans token t.  With writes w = (tau_w,
+    omega_w, kappa_w) (Vt_tau k_tau^T and x_tau,l u_tau,l^T), Gamma_t = e^{lambda_t}, n the chunk's
+    last token:
+      T1 = Gamma_n <G, S0>                       T2_t = sum_{tau_w < t} colf_tau omega_w . G kappa_w
+      T3_t = sum_{j >= t} Gamma_j dout_j . S0 q_j
+      T4_t = sum_{j >= t > tau_w} D_{j,tau_w} (dout_j . omega_w)(q_j . kappa_w)
+      T5_t = -sum_{j > t} Gamma_j beta_j z_j . S0 k_j
+      T6_t = -sum_{j > t > tau_w} D_{j,tau_w} beta_j (z_j . omega_w)(k_j . kappa_w)
+      yhat_t = alpha_t S_{t-1} k_t = v_t - Vt_t / beta_t ... formed as Gamma_t S0 k_t + sum_{tau_w < t}
+               D_{t,tau_w} (kappa_w . k_t) omega_w (no division)."""
+    n = pc["n"]
+    pad = C - n
+    P2 = lambda a: np.concatenate([a, np.zeros((pad,) + a.shape[1:])]) if pad else a
+    q, k, v, u, X, dO = P2(q), P2(k), P2(v), P2(u), P2(X), P2(dO)
+    beta = np.concatenate([beta, np.zeros(pad)])
+    alpha_p = np.concatenate([alpha, np.ones(pad)])
+    R = u.shape[1]
+    lam = np.cumsum(np.log(alpha_p))
+    Gam = np.exp(lam)
+    colf = np.exp(lam[-1] - lam)
+    Dm = np.exp(lam[:, None] - lam[None, :])
+    Vw = [Vt] + [X[:, l] for l in range(R)]
+    Kw = [k] + [u[:, l] for l in range(R)]
+    a = sum(np.sum(Vw[b] * (Kw[b] @ G.T), axis=1) for b in range(R + 1))   # omega_w . G kappa_w per token
+    bq = np.sum(dO * (q @ S0.T), axis=1)                                   # dout_j . S0 q_j
+    dz = np.sum(Z * (k @ S0.T), axis=1)                                    # z_j . S0 k_j
+    T1 = Gam[-1] * np.sum(G * S0)
+    idx = np.arange(C)
+    T2 = np.array([np.sum(colf[:t] * a[:t]) for t in range(C)])
+    T3 = np.array([np.sum(Gam[t:] * bq[t:]) for t in range(C)])
+    T5 = -np.array([np.sum((Gam * beta * dz)[t + 1:]) for t in range(C)])
+    T4 = np.zeros(C)
+    T6 = np.zeros(C)
+    for b in range(R + 1):
+        Cm = (dO @ Vw[b].T) * (q @ Kw[b].T) * np.where(idx[:, None] > idx[None, :], Dm, 0.0)   # [j][tau]
+        Em = (Z @ Vw[b].T) * (k @ Kw[b].T) * beta[:, None] * np.where(idx[:, None] > idx[None, :], Dm, 0.0)
+        for t in range(C):
+            T4[t] += np.sum(Cm[t:, :t])
+            T6[t] -= np.sum(Em[t + 1:, :t])
+    yhat = Gam[:, None] * (k @ S0.T) + sum(((k @ Kw[b].T) * np.where(idx[:, None] > idx[None, :], Dm, 0.0)) @ Vw[b]
+                                            for b in range(R + 1))
+    num = T1 + T2 + T3 + T4 + T5 + T6 - beta * np.sum(Z * yhat, axis=1)
+    return (num / alpha_p)[:n]
+
+
+@pytest.mark.parametrize("alpha_div", [16.0, 0.25])
+def test_exact_dalpha_from_the_chunk_terms(alpha_div):
+    """The cancellation-free dalpha agrees with the oracle, including gates far below one where the
+    suffix-sum identity loses its precision."""
+    T, L = 200, 4
+    inp = make_inputs(1, 1, T, 16, 12, L, dtype="f32", seed=5, alpha_div=alpha_div)
+    x = {nm: inp[nm].double().numpy()[0, 0] for nm in ("q", "k", "v", "beta", "alpha", "u", "gamma", "eta")}
+    x["conv_w"] = inp["conv_w"].double().numpy()[0]
+    dout, dS_final = make_cotangents(1, 1, T, 16, 12, seed=5, with_state=True)
+    dout, dS_final = dout.double().numpy()[0, 0], dS_final.double().numpy()[0, 0]
+    g = np.random.default_rng(5)
+    S_init, vh = 0.3 * g.standard_normal((12, 16)), g.standard_normal((3, 12))
+    X = factors_with_history(x["v"], vh, x["conv_w"], x["gamma"], x["eta"])
+    NC = (T + C - 1) // C
+    sl = [slice(c * C, min(T, c * C + C)) for c in range(NC)]
+    pcs = [chunk_pieces(x["q"][s], x["k"][s], x["v"][s], x["u"][s], x["beta"][s], x["alpha"][s], X[s], dout[s])
+           for s in sl]
+    S = [S_init]
+    for c in range(NC):
+        S.append(S[-1] @ pcs[c]["A"] + pcs[c]["B"])
+    Gs = [None] * NC
+    gg = dS_final
+    for c in range(NC - 1, -1, -1):
+        Gs[c] = gg
+        gg = gg @ pcs[c]["A"].T + pcs[c]["Bbar"]
+    got = []
+    for c, s in enumerate(sl):
+        pc = pcs[c]
+        n = pc["n"]
+        pad = C - n
+        P2 = lambda a: np.concatenate([a, np.zeros((pad,) + a.shape[1:])]) if pad else a
+        Vt = pc["Up"] - pc["W"] @ S[c].T
+        Z = pc["Z0"] + pc["Wbar"] @ Gs[c].T
+        got.append(exact_dalpha(x["q"][s], x["k"][s], x["v"][s], x["u"][s], x["beta"][s], x["alpha"][s], X[s],
+                                dout[s], pc, S[c], Gs[c], Vt, Z))
+    got = np.concatenate(got)
+    ref = prism_backward.backward(inp["q"], inp["k"], inp["v"], inp["beta"], inp["alpha"], inp["u"], inp["gamma"],
+                                  inp["eta"], inp["conv_w"], inp["L"], dout[None, None], S_init=S_init[None, None],
+                                  v_hist=vh[None, None], dS_final=dS_final[None, None], nthreads=1)
+    np.testing.assert_allclose(got, ref["dalpha"][0, 0], rtol=1e-8, atol=1e-10)
