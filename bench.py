@@ -56,6 +56,8 @@ def parse_args():
                          "project: prism_project (the block's input projections); backward: prism_backward "
                          "(the cotangents of every input) over whole sequences")
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 portable fp32 kernels, 2 tensor-core path")
+    ap.add_argument("--nonlinear", action="store_true",
+                    help="backward mode: prism_backward_nonlinear (the non-linear residual chain's cotangents)")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="override the workload's T (a smaller case of the same shape, e.g. for a profiler)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -824,12 +826,13 @@ BACKWARD_METRIC = "PRISM layer bwd tokens/s (all input cotangents, T=16K) + % of
 BWD_KEYS = ("q", "k", "v", "beta", "alpha", "u", "gamma", "eta", "conv_w")
 
 
-def backward_kernel_bytes(name, w):
+def backward_kernel_bytes(name, w, nl=False):
     """Bytes a backward kernel must move at minimum for one launch over the workload: each of
     its inputs read once and each of its outputs written once, the intermediates of the design
     included (token-serial form: the per-token states S_{t-1} and cotangents dS_t, fp32, dv dk
     floats per token each; chunked form: four fp32 chunk maps, the chunk states and cotangents,
-    and the fp16 stash of 5 + R tiles per chunk)."""
+    and the fp16 stash of 5 + R tiles per chunk).  With ``nl`` (the non-linear chain) the gains p
+    [R dv] per token, in the io dtype, take the place of eta, and dp (fp32) that of deta."""
     io = 2 if w.dtype == "bf16" else 4
     th = w.B * w.H * w.T
     R = w.R
@@ -844,39 +847,46 @@ def backward_kernel_bytes(name, w):
     chunks = w.B * w.H * ntile
     dd = w.dk * w.dv * 4
     tile = 64 * w.dv * 2
-    gates = th * 4 * (2 + 2 * R)
+    gates = th * 4 * (2 + (1 if nl else 2) * R)
+    pg = th * R * w.dv * io if nl else 0    # the gains read
+    dpg = th * R * w.dv * 4 if nl else 0    # their cotangent written
+    eta_rw = 0 if nl else th * 4 * R        # eta read or deta written
     table = {
-        "bwd_maps": 2 * qk + v + u + gates + per_row + 4 * chunks * dd + chunks * (5 + R) * tile,
+        "bwd_maps": 2 * qk + v + u + gates + pg + per_row + 4 * chunks * dd + chunks * (5 + R) * tile,
         "bwd_chunk_scan": 4 * chunks * dd + (2 * chunks + w.B * w.H) * dd,
         # the chunk's inputs, dout, S_c, S_{c+1}, G_c, the stash read; dv, dX, dbeta, dq, dk, du, dalpha written
         "bwd_grad": 2 * qk + v + u + gates + per_row + 3 * chunks * dd + chunks * (5 + R) * tile
         + per_row + dX + th * 4 + 2 * th * w.dk * 4 + th * R * w.dk * 4 + th * 4,
-        "bwd_factors": v + th * 8 * R + X,
+        "bwd_factors": v + th * 4 * R + eta_rw + pg + X,
         # both halves of the scan launch: S_{t-1} forward, dS_t (with z, dx) in reverse
         "bwd_scan": (qk + v + u + gates2 + X + state) + (2 * qk + u + gates2 + per_row + state + per_row + dX),
         "bwd_token_grad": 2 * qk + v + u + gates2 + X + 2 * state + 2 * per_row + 2 * th * w.dk * 4 + per_row
         + th * R * w.dk * 4 + th * 8,
-        "bwd_chain_grad": v + th * 8 * R + dX + 2 * per_row + per_row + th * 8 * R,
+        "bwd_chain_grad": v + th * 4 * R + eta_rw + pg + dX + 2 * per_row + per_row + th * 4 * R + eta_rw + dpg,
         "bwd_conv_grad": v + 3 * per_row + w.B * w.H * ntile * 4 * w.dv * 4,
         "bwd_conv_reduce": w.B * w.H * ntile * 4 * w.dv * 4 + w.H * 4 * w.dv * 4,
     }
     return table[name]
 
 
-def backward_path_bytes(w):
-    """The pass's own minimum: the inputs and dout read once, every cotangent written once."""
+def backward_path_bytes(w, nl=False):
+    """The pass's own minimum: the inputs and dout read once, every cotangent written once (with
+    ``nl``, the gains p and their cotangent in place of eta and deta)."""
     io = 2 if w.dtype == "bf16" else 4
     th = w.B * w.H * w.T
     R = w.R
     ins = th * (2 * w.dk + w.dv + R * w.dk) * io + th * 4 * (2 + 2 * R) + th * w.dv * 4
     outs = th * 4 * (2 * w.dk + w.dv + 2 + R * w.dk + 2 * R)
+    if nl:
+        ins += th * R * w.dv * io - th * 4 * R
+        outs += th * R * w.dv * 4 - th * 4 * R
     return ins + outs
 
 
 def backward_oracle_step(sub, dout, nthreads):
     from oracle import prism_backward
     prism_backward.backward(sub["q"], sub["k"], sub["v"], sub["beta"], sub["alpha"], sub["u"], sub["gamma"],
-                            sub["eta"], sub["conv_w"], sub["L"], dout, nthreads=nthreads)
+                            sub["eta"], sub["conv_w"], sub["L"], dout, p_gain=sub.get("p_gain"), nthreads=nthreads)
 
 
 def backward_sample(inp, dout, Ts):
@@ -890,24 +900,31 @@ def run_backward(args, w):
 
     from ssm_sequence_layer_gb300 import binding as Bd
     from ssm_sequence_layer_gb300 import build as cuda_build
-    from ssm_sequence_layer_gb300.inputs import make_cotangents, make_workload_inputs
+    from ssm_sequence_layer_gb300.inputs import make_cotangents, make_gain, make_workload_inputs
 
     world, rank, local = dist_setup(args)
     if rank == 0:
         cuda_build.build()
     barrier(world)
     steps, warm = args.steps, max(args.warmup, 3)
+    nl = args.nonlinear and w.L > 1
     inp_cpu = make_workload_inputs(w, seed=0)
+    if nl:  # the non-linear residual chain: gains p in place of eta
+        inp_cpu["p_gain"] = make_gain(w.B, w.H, w.T, w.L, w.dv, dtype=w.dtype, seed=0)
     dout_cpu, _ = make_cotangents(w.B, w.H, w.T, w.dk, w.dv, seed=0)
     dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp_cpu.items()}
     dout = dout_cpu.cuda()
     stream = torch.cuda.current_stream()
     plan = Bd.Plan.for_inputs(dev, path=args.path or None)  # --path 1: the token-serial form
     flush = L2Flush()
-    grads = plan.backward(dev, dout, stream=stream)
+
+    def step(d, dz, g=None):
+        return plan.backward(d, dz, grads=g, stream=stream, p_gain=d["p_gain"] if nl else None)
+
+    grads = step(dev, dout)
     for _ in range(warm):
         flush()
-        plan.backward(dev, dout, grads=grads, stream=stream)
+        step(dev, dout, grads)
     torch.cuda.synchronize()
     plan.last_device_status()
     sampler = ClockSampler(local) if rank == 0 else None
@@ -919,7 +936,7 @@ def run_backward(args, w):
     for i in range(steps):
         flush()
         ev[i][0].record(stream)
-        plan.backward(dev, dout, grads=grads, stream=stream)
+        step(dev, dout, grads)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -930,7 +947,7 @@ def run_backward(args, w):
     per_kernel, launches = {}, 0
     for _ in range(steps):
         flush()
-        plan.backward(dev, dout, grads=grads, stream=stream)
+        step(dev, dout, grads)
         torch.cuda.synchronize()
         kt = plan.kernel_times()
         launches += len(kt)
@@ -947,15 +964,15 @@ def run_backward(args, w):
     tot = {n: sum(v) for n, v in per_kernel.items()}
     dom = max(tot, key=tot.get)
     dom_ms = tot[dom] / len(per_kernel[dom])
-    dom_bytes = backward_kernel_bytes(dom, w)
+    dom_bytes = backward_kernel_bytes(dom, w, nl)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": traffic_from_profiles(dom, w.name),
                 "alg_bytes_per_launch": dom_bytes, "kernel_ms": dom_ms, "peak_source": f"{peak_kind} hbm_gbs"}
     kernels = {n: {"ms_mean": tot[n] / len(per_kernel[n]), "share": tot[n] / sum(tot.values()),
-                   "hbm_frac": backward_kernel_bytes(n, w) / (tot[n] / len(per_kernel[n]) / 1e3) / 1e9 / hbm}
+                   "hbm_frac": backward_kernel_bytes(n, w, nl) / (tot[n] / len(per_kernel[n]) / 1e3) / 1e9 / hbm}
                for n in tot}
-    pb = backward_path_bytes(w)
+    pb = backward_path_bytes(w, nl)
     path_roofline = {"achieved": pb / (ms_local / 1e3) / 1e9, "unit": "GB/s",
                      "frac": pb / (ms_local / 1e3) / 1e9 / hbm, "alg_bytes_per_step": pb}
 
@@ -964,7 +981,8 @@ def run_backward(args, w):
         host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in inp_cpu.items()}
         hdout = dout_cpu.pin_memory()
         hgrads = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()}
-        used = [k for k in BWD_KEYS if w.L > 1 or k not in ("u", "gamma", "eta")]
+        used = [k for k in BWD_KEYS + (("p_gain",) if nl else ())
+                if (w.L > 1 or k not in ("u", "gamma", "eta")) and not (nl and k == "eta")]
         h2d = hdout.numel() * 4 + sum(host[k].numel() * host[k].element_size() for k in used)
         d2h = sum(v.numel() * v.element_size() for k, v in hgrads.items()
                   if w.L > 1 or k not in ("du", "dgamma", "deta"))
@@ -978,7 +996,7 @@ def run_backward(args, w):
             for k in used:
                 dbuf[k].copy_(host[k], non_blocking=True)
             ddout.copy_(hdout, non_blocking=True)
-            plan.backward(dbuf, ddout, grads=grads, stream=stream)
+            step(dbuf, ddout, grads)
             for k, v in hgrads.items():
                 v.copy_(grads[k], non_blocking=True)
             b.record(stream)
@@ -1013,7 +1031,8 @@ def run_backward(args, w):
             # the chunked form's products take fp16 operands (fp32 accumulation); the token-serial form is fp32
             "dtype": "f16" if chunked else "f32", "data": "synthetic",
             "config": {"workload": w.name, **{k: getattr(w, k) for k in ("B", "H", "T", "dk", "dv", "L")},
-                       "io": w.dtype, "form": "chunked" if chunked else "token-serial", "l2": L2Flush.DESCRIPTION,
+                       "io": w.dtype, "form": "chunked" if chunked else "token-serial",
+                       "chain": "non-linear" if nl else "linear", "l2": L2Flush.DESCRIPTION,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline, "path_roofline": path_roofline, "kernels": kernels, "cpu_baseline": cpu,
             "e2e": e2e, "gpu_launches": launches, "clocks": clocks,

@@ -282,6 +282,27 @@ PRISM_API prism_status prism_backward(prism_plan_t plan, const void *q, const vo
                                       float *deta, float *dconv_w, float *dv_hist, float *dS_init,
                                       struct CUstream_st *stream);
 
+/*
+ * prism_backward_nonlinear -- the cotangents of every input of prism_forward_nonlinear (the
+ * non-linear residual chain of section 2.3 of the notes on PRISM): arguments, layouts, forms and
+ * workspace as prism_backward, with the gains p_gain [B,H,T,R,dv] (io dtype, 16-byte aligned) in
+ * place of eta and their cotangent dp_gain [B,H,T,R,dv] (float32, 16-byte aligned, overwritten)
+ * in place of deta.  Only the token-local chain differs from the linear one; with z = p_{t,l} (.)
+ * r_{t,l} and the cotangent of r_{t,R+1} zero, for l = R .. 1:
+ *   ddelta = gamma_{t,l} dx_{t,l} - dr_{t,l+1}      dgamma_{t,l} = sum_c GELU(z) dx_{t,l}
+ *   dz = ddelta (.) GELU'(z)    dp_{t,l} = dz (.) r_{t,l}    dr_{t,l} = dr_{t,l+1} + dz (.) p_{t,l}
+ * then dv_t gains dr_{t,1} and the anchor's cotangent is -GELU'(h_t) (.) dr_{t,1}.  With L = 1,
+ * p_gain and dp_gain are not touched (and may be NULL); the call equals prism_backward's.
+ */
+PRISM_API prism_status prism_backward_nonlinear(prism_plan_t plan, const void *q, const void *k, const void *v,
+                                                const float *beta, const float *alpha, const void *u,
+                                                const float *gamma, const void *p_gain, const void *conv_w, int L,
+                                                const void *v_hist, const float *S_init, const float *dout,
+                                                const float *dS_final, float *dq, float *dk, float *dv, float *dbeta,
+                                                float *dalpha, float *du, float *dgamma, float *dp_gain,
+                                                float *dconv_w, float *dv_hist, float *dS_init,
+                                                struct CUstream_st *stream);
+
 /* Free the plan and its workspace.  NULL is accepted. */
 PRISM_API prism_status prism_plan_destroy(prism_plan_t plan);
 

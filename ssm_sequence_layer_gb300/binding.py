@@ -36,7 +36,7 @@ EXPORTED = ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forwa
             "prism_plan_destroy", "prism_workspace_bytes", "prism_plan_last_device_status",
             "prism_status_string", "prism_last_error_message", "prism_version", "prism_plan_kernel_times",
             "prism_forward_noalloc", "prism_forward_state", "prism_decode_step", "prism_forward_nonlinear",
-            "prism_project", "prism_backward")
+            "prism_project", "prism_backward", "prism_backward_nonlinear")
 
 
 class prism_kernel_time(ctypes.Structure):
@@ -89,10 +89,12 @@ def lib():
             L.prism_forward_nonlinear.argtypes = fwd[:11] + [vp, f, vp, f, vp, vp]
             L.prism_project.argtypes = [vp, i, vp, vp, vp, vp, vp, f, vp]
             L.prism_backward.argtypes = fwd[:11] + [vp, f, f, f] + [f] * 11 + [vp]
+            L.prism_backward_nonlinear.argtypes = L.prism_backward.argtypes
             L.prism_plan_kernel_times.restype = ctypes.c_int
             for name in ("prism_plan", "prism_plan_set_option", "prism_forward", "prism_forward_host",
                          "prism_plan_destroy", "prism_plan_last_device_status", "prism_forward_state",
-                         "prism_decode_step", "prism_forward_nonlinear", "prism_project", "prism_backward"):
+                         "prism_decode_step", "prism_forward_nonlinear", "prism_project", "prism_backward",
+                         "prism_backward_nonlinear"):
                 getattr(L, name).restype = ctypes.c_int
             _LIB = L
     return _LIB
@@ -209,6 +211,16 @@ def prism_backward(plan, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, v_hist,
                                        _addr(S_init), _addr(dout), _addr(dS_final), _addr(dq), _addr(dk), _addr(dv),
                                        _addr(dbeta), _addr(dalpha), _addr(du), _addr(dgamma), _addr(deta),
                                        _addr(dconv_w), _addr(dv_hist), _addr(dS_init), _stream(stream)))
+
+
+def prism_backward_nonlinear(plan, q, k, v, beta, alpha, u, gamma, p_gain, conv_w, L, v_hist, S_init, dout, dS_final,
+                             dq, dk, dv, dbeta, dalpha, du, dgamma, dp_gain, dconv_w, dv_hist, dS_init, stream=None):
+    return _check(lib().prism_backward_nonlinear(plan, _addr(q), _addr(k), _addr(v), _addr(beta), _addr(alpha),
+                                                 _addr(u), _addr(gamma), _addr(p_gain), _addr(conv_w), int(L),
+                                                 _addr(v_hist), _addr(S_init), _addr(dout), _addr(dS_final),
+                                                 _addr(dq), _addr(dk), _addr(dv), _addr(dbeta), _addr(dalpha),
+                                                 _addr(du), _addr(dgamma), _addr(dp_gain), _addr(dconv_w),
+                                                 _addr(dv_hist), _addr(dS_init), _stream(stream)))
 
 
 def prism_forward_noalloc(B, H, T, dk, dv, L, q, k, v, beta, alpha, u, gamma, eta, conv_w, out, stream=None,
@@ -332,22 +344,28 @@ class Plan:
         return out
 
     def backward(self, inp, dout, dS_final=None, v_hist=None, S_init=None, want_dv_hist=False,
-                 want_dS_init=False, grads=None, stream=None):
+                 want_dS_init=False, grads=None, stream=None, p_gain=None):
         """Cotangents of the inputs (see prism_backward): dout [B,H,T,dv] and dS_final
         [B,H,dv,dk] are float32 CUDA tensors (dS_final may be None).  Returns a dict of float32
         tensors dq, dk, dv, dbeta, dalpha, du, dgamma, deta, dconv_w (plus dv_hist and dS_init on
-        request), allocated unless `grads` holds them."""
+        request), allocated unless `grads` holds them.  With p_gain [B,H,T,R,dv] (io dtype) the
+        forward is the non-linear residual variant (see prism_backward_nonlinear): eta is not read
+        and dp_gain [B,H,T,R,dv] takes the place of deta."""
         import torch
         ts = self._tensors(inp)
-        self._check_device(ts[:-1] + (dout, dS_final, v_hist, S_init), "prism_backward")
         B, H, T, dk, dv, L = self.shape
         R = L - 1
+        nl = p_gain is not None
+        if nl:
+            ts = ts[:7] + (None,) + ts[8:]
+        self._check_device(ts[:-1] + (dout, dS_final, v_hist, S_init, p_gain if R > 0 else None), "prism_backward")
         if grads is None:
             dev = inp["v"].device
             e = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=dev)  # noqa: E731
             grads = {"dq": e(B, H, T, dk), "dk": e(B, H, T, dk), "dv": e(B, H, T, dv), "dbeta": e(B, H, T),
                      "dalpha": e(B, H, T), "du": e(B, H, T, R, dk), "dgamma": e(B, H, T, R),
-                     "deta": e(B, H, T, R), "dconv_w": e(H, 4, dv)}
+                     ("dp_gain" if nl else "deta"): e(B, H, T, R, dv) if nl else e(B, H, T, R),
+                     "dconv_w": e(H, 4, dv)}
             if want_dv_hist:
                 grads["dv_hist"] = e(B, H, 3, dv)
             if want_dS_init:
@@ -355,6 +373,14 @@ class Plan:
         g = grads
         lv = R > 0
         self._check_device(tuple(g.values()), "prism_backward")
+        if nl:
+            q, k, v, beta, alpha, u, gamma, _eta, conv_w, L = ts
+            prism_backward_nonlinear(self.handle, q, k, v, beta, alpha, u, gamma, p_gain if lv else None, conv_w, L,
+                                     v_hist, S_init, dout, dS_final, g["dq"], g["dk"], g["dv"], g["dbeta"],
+                                     g["dalpha"], g["du"] if lv else None, g["dgamma"] if lv else None,
+                                     g["dp_gain"] if lv else None, g["dconv_w"], g.get("dv_hist"), g.get("dS_init"),
+                                     stream)
+            return g
         prism_backward(self.handle, *ts, v_hist, S_init, dout, dS_final, g["dq"], g["dk"], g["dv"], g["dbeta"],
                        g["dalpha"], g["du"] if lv else None, g["dgamma"] if lv else None, g["deta"] if lv else None,
                        g["dconv_w"], g.get("dv_hist"), g.get("dS_init"), stream)

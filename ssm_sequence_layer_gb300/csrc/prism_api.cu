@@ -436,27 +436,36 @@ prism_status prism_decode_step(prism_plan_t p, const void *q, const void *k, con
     return PRISM_OK;
 }
 
-prism_status prism_backward(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,
-                            const float *alpha, const void *u, const float *gamma, const float *eta,
-                            const void *conv_w, int L, const void *v_hist, const float *S_init, const float *dout,
-                            const float *dS_final, float *dq, float *dk, float *dv, float *dbeta, float *dalpha,
-                            float *du, float *dgamma, float *deta, float *dconv_w, float *dv_hist, float *dS_init,
-                            struct CUstream_st *stream)
+// Both chains' backward.  The linear chain passes eta and deta; the non-linear one p_gain and
+// dp_gain (eta and deta null).
+static prism_status run_backward(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,
+                                 const float *alpha, const void *u, const float *gamma, const float *eta,
+                                 const void *p_gain, const void *conv_w, int L, const void *v_hist,
+                                 const float *S_init, const float *dout, const float *dS_final, float *dq, float *dk,
+                                 float *dv, float *dbeta, float *dalpha, float *du, float *dgamma, float *deta,
+                                 float *dp_gain, float *dconv_w, float *dv_hist, float *dS_init,
+                                 struct CUstream_st *stream)
 {
     if (!p) return fail(PRISM_ERR_INVALID_ARG, "plan is NULL");
-    // the forward's checks stand for the inputs; dout takes the place of out
-    prism_status st = check_forward_args(p, q, k, v, beta, alpha, u, gamma, eta, conv_w, L, dout);
+    const bool lvl = p->shape.R > 0, nonlinear = p_gain != nullptr || dp_gain != nullptr;
+    if (nonlinear && lvl && (!p_gain || !dp_gain))
+        return fail(PRISM_ERR_INVALID_ARG, "p_gain and dp_gain must not be NULL when L > 1");
+    // the forward's checks stand for the inputs; dout takes the place of out (gamma stands in
+    // for eta's null check in the non-linear chain, which has no eta)
+    prism_status st = check_forward_args(p, q, k, v, beta, alpha, u, gamma, nonlinear && lvl ? gamma : eta, conv_w,
+                                         L, dout);
     if (st != PRISM_OK) return st;
-    const bool lvl = p->shape.R > 0;
     if (!dq || !dk || !dv || !dbeta || !dalpha || !dconv_w)
         return fail(PRISM_ERR_INVALID_ARG, "dq, dk, dv, dbeta, dalpha and dconv_w must not be NULL");
-    if (lvl && (!du || !dgamma || !deta))
+    if (lvl && (!du || !dgamma || (!nonlinear && !deta)))
         return fail(PRISM_ERR_INVALID_ARG, "du, dgamma and deta must not be NULL when L > 1");
-    const void *ap[] = {v_hist, S_init, dS_final, dv_hist, dS_init, dout, dq, dk, dv, lvl ? du : nullptr};
-    const char *an[] = {"v_hist", "S_init", "dS_final", "dv_hist", "dS_init", "dout", "dq", "dk", "dv", "du"};
-    for (int i = 0; i < 10; ++i)
+    const void *ap[] = {v_hist, S_init, dS_final, dv_hist, dS_init, dout, dq, dk, dv, lvl ? du : nullptr,
+                        lvl ? p_gain : nullptr, lvl ? dp_gain : nullptr};
+    const char *an[] = {"v_hist", "S_init", "dS_final", "dv_hist", "dS_init", "dout", "dq", "dk", "dv", "du",
+                        "p_gain", "dp_gain"};
+    for (int i = 0; i < 12; ++i)
         if (ap[i] && !aligned(ap[i], 16)) return fail(PRISM_ERR_MISALIGNED, "%s is not 16-byte aligned", an[i]);
-    const void *fp[] = {dbeta, dalpha, dconv_w, lvl ? dgamma : nullptr, lvl ? deta : nullptr};
+    const void *fp[] = {dbeta, dalpha, dconv_w, lvl ? dgamma : nullptr, lvl && !nonlinear ? deta : nullptr};
     const char *fn[] = {"dbeta", "dalpha", "dconv_w", "dgamma", "deta"};
     for (int i = 0; i < 5; ++i)
         if (fp[i] && !aligned(fp[i], 4)) return fail(PRISM_ERR_MISALIGNED, "%s is not 4-byte aligned", fn[i]);
@@ -480,15 +489,43 @@ prism_status prism_backward(prism_plan_t p, const void *q, const void *k, const 
         p->ws_bwd_bytes = bytes;
     }
     prism::BackwardArgs a{q, k, v, lvl ? u : nullptr, conv_w, v_hist, beta, alpha, lvl ? gamma : nullptr,
-                          lvl ? eta : nullptr, S_init, dout, dS_final, dq, dk, dv, dbeta, dalpha,
-                          lvl ? du : nullptr, lvl ? dgamma : nullptr, lvl ? deta : nullptr, dconv_w, dv_hist,
-                          dS_init};
+                          lvl && !nonlinear ? eta : nullptr, S_init, dout, dS_final, dq, dk, dv, dbeta, dalpha,
+                          lvl ? du : nullptr, lvl ? dgamma : nullptr, lvl && !nonlinear ? deta : nullptr, dconv_w,
+                          dv_hist, dS_init};
+    a.p_gain = lvl ? p_gain : nullptr;
+    a.dp_gain = lvl ? dp_gain : nullptr;
     p->timer.on = p->opt_timing != 0;
     p->timer.reset((cudaStream_t)stream);
     const cudaError_t e = chunked ? prism::backward_tc(p->shape, a, p->ws_bwd, p->d_status, p->opt_wait_ns, p->timer)
                                   : prism::backward(p->shape, p->io, a, p->ws_bwd, p->timer);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return PRISM_OK;
+}
+
+prism_status prism_backward(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,
+                            const float *alpha, const void *u, const float *gamma, const float *eta,
+                            const void *conv_w, int L, const void *v_hist, const float *S_init, const float *dout,
+                            const float *dS_final, float *dq, float *dk, float *dv, float *dbeta, float *dalpha,
+                            float *du, float *dgamma, float *deta, float *dconv_w, float *dv_hist, float *dS_init,
+                            struct CUstream_st *stream)
+{
+    return run_backward(p, q, k, v, beta, alpha, u, gamma, eta, nullptr, conv_w, L, v_hist, S_init, dout, dS_final,
+                        dq, dk, dv, dbeta, dalpha, du, dgamma, deta, nullptr, dconv_w, dv_hist, dS_init, stream);
+}
+
+prism_status prism_backward_nonlinear(prism_plan_t p, const void *q, const void *k, const void *v,
+                                      const float *beta, const float *alpha, const void *u, const float *gamma,
+                                      const void *p_gain, const void *conv_w, int L, const void *v_hist,
+                                      const float *S_init, const float *dout, const float *dS_final, float *dq,
+                                      float *dk, float *dv, float *dbeta, float *dalpha, float *du, float *dgamma,
+                                      float *dp_gain, float *dconv_w, float *dv_hist, float *dS_init,
+                                      struct CUstream_st *stream)
+{
+    if (p && p->shape.R > 0 && (!p_gain || !dp_gain))
+        return fail(PRISM_ERR_INVALID_ARG, "p_gain and dp_gain must not be NULL when L > 1");
+    return run_backward(p, q, k, v, beta, alpha, u, gamma, nullptr, p_gain, conv_w, L, v_hist, S_init, dout,
+                        dS_final, dq, dk, dv, dbeta, dalpha, du, dgamma, nullptr, dp_gain, dconv_w, dv_hist, dS_init,
+                        stream);
 }
 
 prism_status prism_forward_host(prism_plan_t p, const void *q, const void *k, const void *v, const float *beta,

@@ -65,12 +65,13 @@ __device__ __forceinline__ void anchor_at(const io_t *v, const io_t *v_hist, con
     phi = 0.39894228040143268f * expf(-0.5f * a * a);
 }
 
-// Injection factors x_{t,l} = gamma_l g r_l -> X [BH][T][R][dv].
+// Injection factors x_{t,l} = gamma_l g r_l -> X [BH][T][R][dv]; with gains p_gain (the non-linear
+// chain) x_{t,l} = gamma_l GELU(p_l r_l) and r_{l+1} = r_l - GELU(p_l r_l) instead.
 template <typename io_t>
 __global__ void __launch_bounds__(NT) factors_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
                                                      const io_t *__restrict__ conv_w, const float *__restrict__ gamma,
-                                                     const float *__restrict__ eta, float *__restrict__ X, int H,
-                                                     int T, int dv, int R)
+                                                     const float *__restrict__ eta, const io_t *__restrict__ p_gain,
+                                                     float *__restrict__ X, int H, int T, int dv, int R)
 {
     const int bh = blockIdx.y;
     const long long idx = (long long)blockIdx.x * NT + threadIdx.x;
@@ -81,6 +82,15 @@ __global__ void __launch_bounds__(NT) factors_kernel(const io_t *__restrict__ v,
     const float g = fmaf(a, phi, Phi);
     float r = ldf(v + ((size_t)bh * T + t) * dv + c) - a * Phi;
     const size_t tok = (size_t)bh * T + t;
+    if (p_gain) {
+        for (int l = 0; l < R; ++l) {
+            const float z = ldf(p_gain + (tok * R + l) * dv + c) * r;
+            const float delta = z * (0.5f * erfcf(-z * 0.70710678118654752f));
+            X[(tok * R + l) * dv + c] = gamma[tok * R + l] * delta;
+            r -= delta;
+        }
+        return;
+    }
     for (int l = 0; l < R; ++l) {
         X[(tok * R + l) * dv + c] = gamma[tok * R + l] * g * r;
         if (l + 1 < R) r *= 1.f - eta[tok * R + l] * g;  // the last gain is never read
@@ -730,6 +740,106 @@ __global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__
         }
 }
 
+// The non-linear chain backwards (gains p in place of eta), laid out as chain_grad_kernel: per
+// channel, the residuals r_l are stepped forwards again (r_{l+1} = r_l - GELU(p_l r_l)), then with
+// z = p_l r_l, for l = R .. 1 and the cotangent of r_{R+1} zero:
+//   ddelta = gamma_l dx_l - dr_{l+1},  dgamma_l += GELU(z) dx_l,  dz = ddelta GELU'(z),
+//   dp_l = dz r_l,  dr_l = dr_{l+1} + dz p_l;  then dv += dr_1 and dh = -GELU'(h) dr_1.
+template <typename io_t, int CPL, int RM>
+__global__ void __launch_bounds__(NT) chain_grad_nl_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
+                                                           const io_t *__restrict__ conv_w,
+                                                           const float *__restrict__ gamma,
+                                                           const io_t *__restrict__ p_gain,
+                                                           const float *__restrict__ dX, float *__restrict__ dH,
+                                                           float *__restrict__ dv_out, float *__restrict__ dgamma,
+                                                           float *__restrict__ dp_gain, long long ntok, int H, int T,
+                                                           int R)
+{
+    constexpr int dv = 64 * CPL;
+    const int lane = threadIdx.x & 31;
+    const long long tok = (long long)blockIdx.x * (NT / 32) + (threadIdx.x >> 5);
+    if (tok >= ntok) return;
+    const int bh = (int)(tok / T), t = (int)(tok % T), h = bh % H;
+    float gm[RM];
+#pragma unroll
+    for (int l = 0; l < RM; ++l) gm[l] = l < R ? gamma[(size_t)tok * R + l] : 0.f;
+    float2 vv[CPL][4], w[CPL][4], dxv[CPL][RM], pv[CPL][RM];
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        const int c = 2 * (lane + 32 * k);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            w[k][j] = ld2(conv_w + ((size_t)h * 4 + j) * dv + c);
+            vv[k][j] = make_float2(0.f, 0.f);
+            if (t - j >= 0) vv[k][j] = ld2(v + ((size_t)bh * T + t - j) * dv + c);
+            else if (v_hist) vv[k][j] = ld2(v_hist + ((size_t)bh * 3 + 3 + t - j) * dv + c);
+        }
+#pragma unroll
+        for (int l = 0; l < RM; ++l)
+            if (l < R) {
+                dxv[k][l] = *reinterpret_cast<const float2 *>(dX + ((size_t)tok * R + l) * dv + c);
+                pv[k][l] = ld2(p_gain + ((size_t)tok * R + l) * dv + c);
+            }
+    }
+    float dgam[RM];
+#pragma unroll
+    for (int l = 0; l < RM; ++l) dgam[l] = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        const int c = 2 * (lane + 32 * k);
+        float drn2[2], dh2[2], dp2[RM][2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float a = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a = fmaf(e ? w[k][j].y : w[k][j].x, e ? vv[k][j].y : vv[k][j].x, a);
+            const float Phi = 0.5f * erfcf(-a * 0.70710678118654752f);
+            const float phi = 0.39894228040143268f * expf(-0.5f * a * a);
+            const float g = fmaf(a, phi, Phi);
+            float rl[RM], Pzl[RM];  // r_l and Phi(p_l r_l), kept from the forward steps
+            float r = (e ? vv[k][0].y : vv[k][0].x) - a * Phi;
+#pragma unroll
+            for (int l = 0; l < RM; ++l)
+                if (l < R) {
+                    rl[l] = r;
+                    const float z = (e ? pv[k][l].y : pv[k][l].x) * r;
+                    Pzl[l] = 0.5f * erfcf(-z * 0.70710678118654752f);
+                    r -= z * Pzl[l];
+                }
+            float drn = 0.f;
+#pragma unroll
+            for (int l = RM - 1; l >= 0; --l)
+                if (l < R) {
+                    const float pl = e ? pv[k][l].y : pv[k][l].x, dx = e ? dxv[k][l].y : dxv[k][l].x;
+                    const float z = pl * rl[l];
+                    const float Pz = Pzl[l];
+                    const float pz = 0.39894228040143268f * expf(-0.5f * z * z);
+                    const float ddelta = gm[l] * dx - drn;
+                    dgam[l] = fmaf(z * Pz, dx, dgam[l]);
+                    const float dz = ddelta * fmaf(z, pz, Pz);
+                    dp2[l][e] = dz * rl[l];
+                    drn = fmaf(dz, pl, drn);
+                }
+            drn2[e] = drn;
+            dh2[e] = -g * drn;
+        }
+        float2 *dvp = reinterpret_cast<float2 *>(dv_out + (size_t)tok * dv + c);
+        const float2 old = *dvp;
+        *dvp = make_float2(old.x + drn2[0], old.y + drn2[1]);
+        *reinterpret_cast<float2 *>(dH + (size_t)tok * dv + c) = make_float2(dh2[0], dh2[1]);
+#pragma unroll
+        for (int l = 0; l < RM; ++l)
+            if (l < R)
+                *reinterpret_cast<float2 *>(dp_gain + ((size_t)tok * R + l) * dv + c) = make_float2(dp2[l][0], dp2[l][1]);
+    }
+#pragma unroll
+    for (int l = 0; l < RM; ++l)
+        if (l < R) {
+            const float s1 = warp_sum(dgam[l]);
+            if (lane == 0) dgamma[(size_t)tok * R + l] = s1;
+        }
+}
+
 // The convolution backwards over tiles of CT tokens: v's share of dv, dv_hist (first tile)
 // and the tile's sums for dconv_w -> dWp [BH][ntile][4][dv].
 template <typename io_t>
@@ -837,10 +947,17 @@ cudaError_t token_local(const Shape &s, const BackwardArgs &a, float *dX, float 
     const long long cg_grid = (ntok + NT / 32 - 1) / (NT / 32);  // one warp per token
     tm.begin("bwd_chain_grad");
     // the level arrays sized for L <= 4 or for the largest L (registers)
-    auto kern = s.dv == 64 ? (s.R <= 3 ? chain_grad_kernel<io_t, 1, 3> : chain_grad_kernel<io_t, 1, RMAX>)
-                           : (s.R <= 3 ? chain_grad_kernel<io_t, 2, 3> : chain_grad_kernel<io_t, 2, RMAX>);
-    kern<<<(unsigned)cg_grid, NT, 0, st>>>(v, vh, cw, a.gamma, a.eta, dX, dH, a.dv, a.dgamma, a.deta, ntok, s.H, s.T,
-                                           s.R);
+    if (a.p_gain) {
+        auto kern = s.dv == 64 ? (s.R <= 3 ? chain_grad_nl_kernel<io_t, 1, 3> : chain_grad_nl_kernel<io_t, 1, RMAX>)
+                               : (s.R <= 3 ? chain_grad_nl_kernel<io_t, 2, 3> : chain_grad_nl_kernel<io_t, 2, RMAX>);
+        kern<<<(unsigned)cg_grid, NT, 0, st>>>(v, vh, cw, a.gamma, static_cast<const io_t *>(a.p_gain), dX, dH, a.dv,
+                                               a.dgamma, a.dp_gain, ntok, s.H, s.T, s.R);
+    } else {
+        auto kern = s.dv == 64 ? (s.R <= 3 ? chain_grad_kernel<io_t, 1, 3> : chain_grad_kernel<io_t, 1, RMAX>)
+                               : (s.R <= 3 ? chain_grad_kernel<io_t, 2, 3> : chain_grad_kernel<io_t, 2, RMAX>);
+        kern<<<(unsigned)cg_grid, NT, 0, st>>>(v, vh, cw, a.gamma, a.eta, dX, dH, a.dv, a.dgamma, a.deta, ntok, s.H,
+                                               s.T, s.R);
+    }
     tm.end();
     tm.begin("bwd_conv_grad");
     conv_grad_kernel<io_t><<<dim3(ntile, s.BH), s.dv, 0, st>>>(v, vh, cw, dH, a.dv, a.dv_hist, dWp, s.H, s.T, s.dv,
@@ -865,7 +982,7 @@ cudaError_t launch(const Shape &s, const BackwardArgs &a, void *ws, KernelTimer 
     if (s.R > 0) {
         tm.begin("bwd_factors");
         factors_kernel<io_t><<<dim3((unsigned)(((long long)s.T * s.dv + NT - 1) / NT), s.BH), NT, 0, st>>>(
-            v, vh, cw, a.gamma, a.eta, w.X, s.H, s.T, s.dv, s.R);
+            v, vh, cw, a.gamma, a.eta, static_cast<const io_t *>(a.p_gain), w.X, s.H, s.T, s.dv, s.R);
         tm.end();
     }
     const int ct = scan_chunk(DK, s.R, sizeof(io_t));

@@ -73,6 +73,7 @@ struct Params {
     const __nv_bfloat16 *conv_w;     // [H][4][64]
     const __nv_bfloat16 *v_hist;     // [BH][3][64] or null
     const float *beta, *alpha, *gamma, *eta;
+    const __nv_bfloat16 *p_gain;     // [BH][T][R][64] (the non-linear chain) or null
     const float *dout;               // [BH][T][64]
     float *mapA, *mapAT, *mapB, *mapBb;  // [chunks][64][64]
     __half *stash;                   // [chunks][STASH][4096]
@@ -258,7 +259,7 @@ __device__ __forceinline__ void load_scalars(float *sc, const Params &p, size_t 
             const int i = e / RMAX, l = e % RMAX;
             const bool ok = i < n && l < R;
             sc[SC_GM + e] = ok ? p.gamma[(tok0 + i) * R + l] : 0.f;
-            sc[SC_ET + e] = (ok && l + 1 < R) ? p.eta[(tok0 + i) * R + l] : 0.f;
+            sc[SC_ET + e] = (ok && l + 1 < R && p.eta) ? p.eta[(tok0 + i) * R + l] : 0.f;
         }
     }
 }
@@ -400,7 +401,8 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid != 0) wait_all(0, 0);  // V has landed
         __syncthreads();
         if (abort_s) break;
-        // ---- prep: x_{i,l} = gamma_il g_i r_il (two channels, eight tokens per thread) -> X_l -----------
+        // ---- prep: x_{i,l} = gamma_il g_i r_il (two channels, eight tokens per thread) -> X_l; the
+        // non-linear chain x_{i,l} = gamma_il GELU(p_il r_il), r_{i,l+1} = r_il - GELU(p_il r_il) ------
         if (R > 0) {
             const int cp = tid & 31, tg = tid >> 5;  // channel pair; tokens tg + 16 k
             const __nv_bfloat162 *cw = reinterpret_cast<const __nv_bfloat162 *>(p.conv_w) + (size_t)h * 4 * (D / 2) + cp;
@@ -422,13 +424,35 @@ __global__ void __launch_bounds__(NT, 1)
                 tcu::gelu_gain(a0, g0, Phi0);
                 tcu::gelu_gain(a1, g1, Phi1);
                 float r0 = v0.x - a0 * Phi0, r1 = v0.y - a1 * Phi1;
-                for (int l = 0; l < R; ++l) {
+                // the gains of every level loaded before the first is used (tokens past the end: 0,
+                // so delta = 0)
+                float2 pv[RMAX];
+                if (p.p_gain) {
+                    const __nv_bfloat162 *pg = reinterpret_cast<const __nv_bfloat162 *>(p.p_gain + (tok0 + i) * R * D) + cp;
+#pragma unroll
+                    for (int l = 0; l < RMAX; ++l)
+                        pv[l] = (i < n && l < R) ? __bfloat1622float2(pg[l * (D / 2)]) : make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int l = 0; l < RMAX; ++l) {
+                    if (l >= R) break;
                     const float gm = sc[SC_GM + i * RMAX + l], et = sc[SC_ET + i * RMAX + l];
-                    const uint32_t xv = pack_h2(gm * g0 * r0, gm * g1 * r1);
+                    float x0, x1;
+                    if (p.p_gain) {
+                        const float d0 = tcu::gelu_value(pv[l].x * r0), d1 = tcu::gelu_value(pv[l].y * r1);
+                        x0 = gm * d0;
+                        x1 = gm * d1;
+                        r0 -= d0;
+                        r1 -= d1;
+                    } else {
+                        x0 = gm * g0 * r0;
+                        x1 = gm * g1 * r1;
+                        r0 *= 1.f - et * g0;
+                        r1 *= 1.f - et * g1;
+                    }
+                    const uint32_t xv = pack_h2(x0, x1);
                     *reinterpret_cast<uint32_t *>(P(X0 + l) + sw128(i, 2 * cp)) = xv;
                     *reinterpret_cast<uint32_t *>(stash + (ST_X + l) * PANEL + sw128(i, 2 * cp)) = xv;
-                    r0 *= 1.f - et * g0;
-                    r1 *= 1.f - et * g1;
                 }
             }
             fence_async_smem();
@@ -1245,6 +1269,7 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     p.alpha = a.alpha;
     p.gamma = a.gamma;
     p.eta = a.eta;
+    p.p_gain = static_cast<const __nv_bfloat16 *>(a.p_gain);
     p.dout = a.dout;
     p.mapA = w.mapA;
     p.mapAT = w.mapAT;

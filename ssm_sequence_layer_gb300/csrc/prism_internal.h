@@ -130,6 +130,10 @@ struct BackwardArgs {
     const void *q, *k, *v, *u, *conv_w, *v_hist;
     const float *beta, *alpha, *gamma, *eta, *S_init, *dout, *dS_final;
     float *dq, *dk, *dv, *dbeta, *dalpha, *du, *dgamma, *deta, *dconv_w, *dv_hist, *dS_init;
+    // the non-linear residual chain: gains [BH T][R][dv] in the io dtype in place of eta, and
+    // their cotangent (fp32, same layout) in place of deta; null for the linear chain
+    const void *p_gain = nullptr;
+    float *dp_gain = nullptr;
 };
 // token-serial backward (every shape): per-token states and cotangents in the workspace
 size_t backward_workspace_bytes(const Shape &s);

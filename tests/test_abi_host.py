@@ -112,6 +112,9 @@ def test_null_plan_handling(lib):
     rc = lib.prism_backward(None, 16, 16, 16, 16, 16, None, None, None, 16, 1, None, None, 16, None,
                             16, 16, 16, 16, 16, None, None, None, 16, None, None, None)
     assert rc == B.PRISM_ERR_INVALID_ARG
+    rc = lib.prism_backward_nonlinear(None, 16, 16, 16, 16, 16, None, None, None, 16, 1, None, None, 16, None,
+                                      16, 16, 16, 16, 16, None, None, None, 16, None, None, None)
+    assert rc == B.PRISM_ERR_INVALID_ARG
 
 
 def test_binding_raises_with_message(lib):

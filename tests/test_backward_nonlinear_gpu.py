@@ -1,0 +1,199 @@
+"""GPU parity of prism_backward_nonlinear (the cotangents of the non-linear residual variant,
+delta = GELU(p r), r <- r - delta; notes on PRISM, section 2.3) against the fp64 backward oracle
+with the same gains, in both backward forms.
+
+Only the token-local chain differs from the linear backward, so the bars are those of the linear
+chain's tests: max |g - g_ref| / rms(g_ref) per cotangent tensor <= 1e-2 for the chunked
+tensor-core form (fp16 operands, three dependent rounded products at most), <= 1e-4 (float32 io)
+and <= 1e-3 (bfloat16 io) for the token-serial fp32 form.  dp_gain takes the place of deta.
+
+Two of the chunked form's cotangents are per-element products of a cotangent and a forward value:
+dp_{t,l} = dz (.) r_{t,l} and du_{t,l} = dS_t^T x_{t,l}, with x = gamma GELU(p r) quadratic near 0.
+Their error is the factor's error (the other cotangents' size) times the other factor, so its
+largest element scales with the product of both factors' peak-to-rms ratios (about 4 each over
+the 16K-token sequences) rather than one: their max error is held to twice the bar, 2e-2 of rms.
+Every tensor of the chunked form also meets rms |g - g_ref| / rms(g_ref) <= 1e-3, two rounding
+steps of 2^-11 (measured: 3e-4 to 5e-4, as for the linear chain; dalpha 1.2e-3 is held to its
+max bar only, its rounding error grows like 1 / alpha); a dropped or mis-signed term moves a
+tensor's rms error to O(1).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import prism_backward
+from ssm_sequence_layer_gb300 import binding as B
+from ssm_sequence_layer_gb300 import build
+from ssm_sequence_layer_gb300.inputs import WORKLOADS, make_cotangents, make_gain, make_inputs, make_workload_inputs
+from tests.gpu_util import rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+TC_BAR = 1e-2
+SERIAL_BAR = {"f32": 1e-4, "bf16": 1e-3}
+PER_HEAD = ("dq", "dk", "dv", "dbeta", "dalpha", "du", "dgamma", "dp_gain")
+ALL = PER_HEAD + ("dconv_w", "dv_hist", "dS_init")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def side_inputs(B_, H, dk, dv, seed, io):
+    g = torch.Generator().manual_seed(seed + 31)
+    S0 = torch.randn(B_, H, dv, dk, generator=g) * 0.3
+    vh = torch.randn(B_, H, 3, dv, generator=g).to(torch.bfloat16 if io == "bf16" else torch.float32)
+    return S0, vh
+
+
+def gpu_backward(inp, p, dout, dS_final=None, v_hist=None, S_init=None, path=None):
+    d = to_device(inp)
+    with B.Plan.for_inputs(d, path=path) as plan:
+        g = plan.backward(d, dout.cuda(), dS_final=None if dS_final is None else dS_final.cuda(),
+                          v_hist=None if v_hist is None else v_hist.cuda(),
+                          S_init=None if S_init is None else S_init.cuda(), want_dv_hist=True, want_dS_init=True,
+                          p_gain=p.cuda())
+        torch.cuda.synchronize()
+        plan.last_device_status()
+    return {kk: vv.double().cpu().numpy() for kk, vv in g.items()}
+
+
+def oracle_backward(inp, p, dout, dS_final=None, v_hist=None, S_init=None):
+    return prism_backward.backward(inp["q"], inp["k"], inp["v"], inp["beta"], inp["alpha"], inp["u"], inp["gamma"],
+                                   None, inp["conv_w"], inp["L"], dout, S_init=S_init, v_hist=v_hist,
+                                   dS_final=dS_final, p_gain=p if inp["L"] > 1 else None, want_dv_hist=True,
+                                   want_dS_init=True)
+
+
+PRODUCTS = ("dp_gain", "du")  # per-element products of a cotangent and a forward value
+
+
+def rms_err(a, b):
+    return float(np.sqrt(np.mean((a - b) ** 2)) / max(np.sqrt(np.mean(b ** 2)), 1e-30))
+
+
+def compare(got, ref, keys, bar, chunked=False):
+    errs = {kk: rel_err(got[kk], ref[kk]) for kk in keys if ref[kk].size}
+    print("non-linear backward parity: " + ", ".join(f"{kk} {e:.2e}" for kk, e in errs.items()))
+    lim = {kk: (2 * bar if chunked and kk in PRODUCTS else bar) for kk in errs}
+    bad = {kk: e for kk, e in errs.items() if not e <= lim[kk]}
+    assert not bad, f"cotangents over the bar {bar}: {bad} (all: {errs})"
+    if chunked:
+        rms = {kk: rms_err(got[kk], ref[kk]) for kk in errs if kk != "dalpha"}
+        print("  rms: " + ", ".join(f"{kk} {e:.2e}" for kk, e in rms.items()))
+        bad = {kk: e for kk, e in rms.items() if not e <= 1e-3}
+        assert not bad, f"rms errors over 1e-3: {bad}"
+
+
+CHUNKED = [
+    # B, H, T, L, state (S_init, v_hist, dS_final)
+    (1, 2, 200, 3, True),
+    (2, 1, 130, 4, True),
+    (1, 1, 64, 2, False),
+    (1, 1, 5, 4, True),
+]
+
+
+@pytest.mark.parametrize("case", CHUNKED, ids=[f"B{c[0]}H{c[1]}T{c[2]}L{c[3]}{'-state' if c[4] else ''}"
+                                               for c in CHUNKED])
+def test_chunked_form_matches_oracle(case):
+    B_, H, T, L, state = case
+    seed = 300 + T + L
+    inp = make_inputs(B_, H, T, 64, 64, L, dtype="bf16", seed=seed)
+    p = make_gain(B_, H, T, L, 64, dtype="bf16", seed=seed)
+    dout, dS_final = make_cotangents(B_, H, T, 64, 64, seed=seed, with_state=state)
+    S0, vh = side_inputs(B_, H, 64, 64, seed, "bf16") if state else (None, None)
+    got = gpu_backward(inp, p, dout, dS_final, vh, S0)
+    compare(got, oracle_backward(inp, p, dout, dS_final, vh, S0), ALL, TC_BAR, chunked=True)
+
+
+SERIAL = [
+    # B, H, T, dk, dv, L, io, state
+    (1, 2, 200, 64, 64, 3, "f32", True),
+    (2, 1, 130, 128, 128, 8, "bf16", True),
+    (1, 1, 97, 64, 128, 16, "f32", False),
+    (1, 2, 150, 128, 64, 4, "bf16", False),
+]
+
+
+@pytest.mark.parametrize("case", SERIAL, ids=[f"B{c[0]}H{c[1]}T{c[2]}dk{c[3]}dv{c[4]}L{c[5]}{c[6]}" for c in SERIAL])
+def test_token_serial_form_matches_oracle(case):
+    B_, H, T, dk, dv, L, io, state = case
+    seed = 400 + T + L
+    inp = make_inputs(B_, H, T, dk, dv, L, dtype=io, seed=seed)
+    p = make_gain(B_, H, T, L, dv, dtype=io, seed=seed)
+    dout, dS_final = make_cotangents(B_, H, T, dk, dv, seed=seed, with_state=state)
+    S0, vh = side_inputs(B_, H, dk, dv, seed, io) if state else (None, None)
+    got = gpu_backward(inp, p, dout, dS_final, vh, S0, path=1)
+    compare(got, oracle_backward(inp, p, dout, dS_final, vh, S0), ALL, SERIAL_BAR[io])
+
+
+def test_forms_agree_and_differ_from_linear_chain():
+    inp = make_inputs(1, 2, 257, 64, 64, 4, dtype="bf16", seed=41)
+    p = make_gain(1, 2, 257, 4, 64, dtype="bf16", seed=41)
+    dout, dS_final = make_cotangents(1, 2, 257, 64, 64, seed=41, with_state=True)
+    tc = gpu_backward(inp, p, dout, dS_final)
+    ts = gpu_backward(inp, p, dout, dS_final, path=1)
+    compare(tc, ts, ALL, TC_BAR, chunked=True)
+    d = to_device(inp)
+    with B.Plan.for_inputs(d) as plan:
+        lin = plan.backward(d, dout.cuda(), dS_final=dS_final.cuda())
+        torch.cuda.synchronize()
+    assert rel_err(tc["dv"], lin["dv"].double().cpu().numpy()) > 5e-2
+
+
+def test_single_level_equals_linear_backward():
+    """With L = 1 there is no chain: the call is prism_backward's, bit for bit."""
+    inp = make_inputs(1, 2, 150, 64, 64, 1, dtype="bf16", seed=42)
+    p = make_gain(1, 2, 150, 1, 64, dtype="bf16", seed=42)
+    dout, _ = make_cotangents(1, 2, 150, 64, 64, seed=42)
+    nl = gpu_backward(inp, p, dout)
+    d = to_device(inp)
+    with B.Plan.for_inputs(d) as plan:
+        lin = plan.backward(d, dout.cuda(), want_dv_hist=True, want_dS_init=True)
+        torch.cuda.synchronize()
+    for kk in ("dq", "dk", "dv", "dbeta", "dalpha", "dconv_w", "dv_hist", "dS_init"):
+        assert np.array_equal(nl[kk], lin[kk].double().cpu().numpy()), kk
+
+
+def test_full_size_sampled_sequences():
+    """The 16K-token recommendation workload in one call on the chunked form; two of its
+    sequences through the oracle."""
+    w = WORKLOADS["seqrec_16k"]
+    inp = make_workload_inputs(w, seed=0)
+    p = make_gain(w.B, w.H, w.T, w.L, w.dv, dtype="bf16", seed=0)
+    dout, _ = make_cotangents(w.B, w.H, w.T, w.dk, w.dv, seed=0)
+    got = gpu_backward(inp, p, dout)
+    for b, h in [(0, 1), (w.B - 1, w.H - 1)]:
+        one = {kk: (vv[b:b + 1, h:h + 1].contiguous() if kk not in ("L", "conv_w") else vv) for kk, vv in inp.items()}
+        one["conv_w"] = inp["conv_w"][h:h + 1].contiguous()
+        ref = oracle_backward(one, p[b:b + 1, h:h + 1].contiguous(), dout[b:b + 1, h:h + 1])
+        mine = {kk: got[kk][b:b + 1, h:h + 1] for kk in PER_HEAD}
+        compare(mine, ref, PER_HEAD, TC_BAR, chunked=True)
+
+
+def test_argument_errors():
+    inp = make_inputs(1, 1, 70, 64, 64, 3, dtype="bf16", seed=43)
+    d = to_device(inp)
+    dout, _ = make_cotangents(1, 1, 70, 64, 64, seed=43)
+    dout = dout.cuda()
+    with B.Plan.for_inputs(d) as plan:
+        e = lambda *s: torch.zeros(*s, device="cuda")  # noqa: E731
+        g = [e(1, 1, 70, 64), e(1, 1, 70, 64), e(1, 1, 70, 64), e(1, 1, 70), e(1, 1, 70), e(1, 1, 70, 2, 64),
+             e(1, 1, 70, 2), e(1, 1, 70, 2, 64), e(1, 4, 64)]
+        args = (d["q"], d["k"], d["v"], d["beta"], d["alpha"], d["u"], d["gamma"])
+        with pytest.raises(B.PrismError) as ei:  # no gains
+            B.prism_backward_nonlinear(plan.handle, *args, None, d["conv_w"], 3, None, None, dout, None, *g[:7],
+                                       g[7], g[8], None, None)
+        assert ei.value.status == B.PRISM_ERR_INVALID_ARG
+        p = make_gain(1, 1, 70, 3, 64, dtype="bf16", seed=43).cuda()
+        with pytest.raises(B.PrismError) as ei:  # no dp_gain
+            B.prism_backward_nonlinear(plan.handle, *args, p, d["conv_w"], 3, None, None, dout, None, *g[:7], None,
+                                       g[8], None, None)
+        assert ei.value.status == B.PRISM_ERR_INVALID_ARG
+        with pytest.raises(B.PrismError) as ei:  # misaligned gains
+            B.prism_backward_nonlinear(plan.handle, *args, p.view(-1)[1:], d["conv_w"], 3, None, None, dout, None,
+                                       *g[:7], g[7], g[8], None, None)
+        assert ei.value.status == B.PRISM_ERR_MISALIGNED
