@@ -132,7 +132,7 @@ KERNEL_SOURCES = {
     "bwd_maps": ("prism_bwd_tc.cu", "tc_util.h", "tc_ptx.h", "prism_internal.h"),
     "bwd_chunk": ("prism_bwd_tc.cu", "tc_util.h", "tc_ptx.h", "prism_internal.h"),
     "bwd_grad": ("prism_bwd_tc.cu", "tc_util.h", "tc_ptx.h", "prism_internal.h"),
-    "bwd_": ("prism_backward.cu", "prism_internal.h"),
+    "bwd_": ("prism_backward.cu", "tc_util.h", "tc_ptx.h", "prism_internal.h"),
 }
 
 

@@ -28,6 +28,7 @@
 //   dv_t += dr_1,   dh_t = -g dr_1 + phi(h) (2 - h^2) dg
 // then dv_{t-j} += w_j dh_t and dw_j += dh_t v_{t-j} over the window.
 #include "prism_internal.h"
+#include "tc_util.h"
 
 namespace prism {
 namespace bwd {
@@ -673,7 +674,7 @@ __global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__
         gm[l] = l < R ? gamma[(size_t)tok * R + l] : 0.f;
         et[l] = l + 1 < R ? eta[(size_t)tok * R + l] : 0.f;
     }
-    float2 vv[CPL][4], w[CPL][4], dxv[CPL][RM];
+    float2 vv[CPL][4], w[CPL][4], dxv[CPL][RM], dvo[CPL];  // dvo: dv (beta z) as the kernel found it
 #pragma unroll
     for (int k = 0; k < CPL; ++k) {
         const int c = 2 * (lane + 32 * k);
@@ -687,6 +688,7 @@ __global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__
 #pragma unroll
         for (int l = 0; l < RM; ++l)
             if (l < R) dxv[k][l] = *reinterpret_cast<const float2 *>(dX + ((size_t)tok * R + l) * dv + c);
+        dvo[k] = *reinterpret_cast<const float2 *>(dv_out + (size_t)tok * dv + c);
     }
     float dgam[RM], det[RM];
 #pragma unroll
@@ -700,8 +702,8 @@ __global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__
             float a = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) a = fmaf(e ? w[k][j].y : w[k][j].x, e ? vv[k][j].y : vv[k][j].x, a);
-            const float Phi = 0.5f * erfcf(-a * 0.70710678118654752f);
-            const float phi = 0.39894228040143268f * expf(-0.5f * a * a);
+            float Phi, phi;
+            tcu::gauss_parts(a, Phi, phi);
             const float g = fmaf(a, phi, Phi);
             float rl[RM];
             float r = (e ? vv[k][0].y : vv[k][0].x) - a * Phi;
@@ -724,9 +726,7 @@ __global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__
             drn2[e] = drn;
             dh2[e] = -g * drn + phi * (2.f - a * a) * dg;
         }
-        float2 *dvp = reinterpret_cast<float2 *>(dv_out + (size_t)tok * dv + c);
-        const float2 old = *dvp;
-        *dvp = make_float2(old.x + drn2[0], old.y + drn2[1]);
+        *reinterpret_cast<float2 *>(dv_out + (size_t)tok * dv + c) = make_float2(dvo[k].x + drn2[0], dvo[k].y + drn2[1]);
         *reinterpret_cast<float2 *>(dH + (size_t)tok * dv + c) = make_float2(dh2[0], dh2[1]);
     }
 #pragma unroll
@@ -763,7 +763,7 @@ __global__ void __launch_bounds__(NT) chain_grad_nl_kernel(const io_t *__restric
     float gm[RM];
 #pragma unroll
     for (int l = 0; l < RM; ++l) gm[l] = l < R ? gamma[(size_t)tok * R + l] : 0.f;
-    float2 vv[CPL][4], w[CPL][4], dxv[CPL][RM], pv[CPL][RM];
+    float2 vv[CPL][4], w[CPL][4], dxv[CPL][RM], pv[CPL][RM], dvo[CPL];
 #pragma unroll
     for (int k = 0; k < CPL; ++k) {
         const int c = 2 * (lane + 32 * k);
@@ -780,6 +780,7 @@ __global__ void __launch_bounds__(NT) chain_grad_nl_kernel(const io_t *__restric
                 dxv[k][l] = *reinterpret_cast<const float2 *>(dX + ((size_t)tok * R + l) * dv + c);
                 pv[k][l] = ld2(p_gain + ((size_t)tok * R + l) * dv + c);
             }
+        dvo[k] = *reinterpret_cast<const float2 *>(dv_out + (size_t)tok * dv + c);
     }
     float dgam[RM];
 #pragma unroll
@@ -793,18 +794,16 @@ __global__ void __launch_bounds__(NT) chain_grad_nl_kernel(const io_t *__restric
             float a = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) a = fmaf(e ? w[k][j].y : w[k][j].x, e ? vv[k][j].y : vv[k][j].x, a);
-            const float Phi = 0.5f * erfcf(-a * 0.70710678118654752f);
-            const float phi = 0.39894228040143268f * expf(-0.5f * a * a);
+            float Phi, phi;
+            tcu::gauss_parts(a, Phi, phi);
             const float g = fmaf(a, phi, Phi);
-            float rl[RM], Pzl[RM];  // r_l and Phi(p_l r_l), kept from the forward steps
+            float rl[RM];  // r_l, kept from the forward steps
             float r = (e ? vv[k][0].y : vv[k][0].x) - a * Phi;
 #pragma unroll
             for (int l = 0; l < RM; ++l)
                 if (l < R) {
                     rl[l] = r;
-                    const float z = (e ? pv[k][l].y : pv[k][l].x) * r;
-                    Pzl[l] = 0.5f * erfcf(-z * 0.70710678118654752f);
-                    r -= z * Pzl[l];
+                    r -= tcu::gelu_value((e ? pv[k][l].y : pv[k][l].x) * r);
                 }
             float drn = 0.f;
 #pragma unroll
@@ -812,8 +811,8 @@ __global__ void __launch_bounds__(NT) chain_grad_nl_kernel(const io_t *__restric
                 if (l < R) {
                     const float pl = e ? pv[k][l].y : pv[k][l].x, dx = e ? dxv[k][l].y : dxv[k][l].x;
                     const float z = pl * rl[l];
-                    const float Pz = Pzl[l];
-                    const float pz = 0.39894228040143268f * expf(-0.5f * z * z);
+                    float Pz, pz;
+                    tcu::gauss_parts(z, Pz, pz);
                     const float ddelta = gm[l] * dx - drn;
                     dgam[l] = fmaf(z * Pz, dx, dgam[l]);
                     const float dz = ddelta * fmaf(z, pz, Pz);
@@ -823,9 +822,7 @@ __global__ void __launch_bounds__(NT) chain_grad_nl_kernel(const io_t *__restric
             drn2[e] = drn;
             dh2[e] = -g * drn;
         }
-        float2 *dvp = reinterpret_cast<float2 *>(dv_out + (size_t)tok * dv + c);
-        const float2 old = *dvp;
-        *dvp = make_float2(old.x + drn2[0], old.y + drn2[1]);
+        *reinterpret_cast<float2 *>(dv_out + (size_t)tok * dv + c) = make_float2(dvo[k].x + drn2[0], dvo[k].y + drn2[1]);
         *reinterpret_cast<float2 *>(dH + (size_t)tok * dv + c) = make_float2(dh2[0], dh2[1]);
 #pragma unroll
         for (int l = 0; l < RM; ++l)
@@ -841,75 +838,96 @@ __global__ void __launch_bounds__(NT) chain_grad_nl_kernel(const io_t *__restric
 }
 
 // The convolution backwards over tiles of CT tokens: v's share of dv, dv_hist (first tile)
-// and the tile's sums for dconv_w -> dWp [BH][ntile][4][dv].
+// and the tile's sums for dconv_w -> dWp [BH][ntile][4][dv].  Thread (c, sub) walks the CSUB
+// tokens of sub-tile sub for channel c (blockDim = dv x CT / CSUB); the sub-tiles' sums meet in
+// shared memory in a fixed order.
+constexpr int CSUB = 16;
 template <typename io_t>
-__global__ void conv_grad_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
-                                 const io_t *__restrict__ conv_w, const float *__restrict__ dH,
-                                 float *__restrict__ dv_out, float *__restrict__ dv_hist, float *__restrict__ dWp,
-                                 int H, int T, int dv, int ntile)
+__global__ void __launch_bounds__(512) conv_grad_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
+                                                        const io_t *__restrict__ conv_w, const float *__restrict__ dH,
+                                                        float *__restrict__ dv_out, float *__restrict__ dv_hist,
+                                                        float *__restrict__ dWp, int H, int T, int dv, int ntile)
 {
-    const int c = threadIdx.x, bh = blockIdx.y, tile = blockIdx.x, h = bh % H;  // blockDim.x = dv
-    const int t0 = tile * CT, t1 = min(T, t0 + CT);
+    __shared__ float part[CT / CSUB][4][128];
+    const int c = threadIdx.x % dv, sub = threadIdx.x / dv, bh = blockIdx.y, tile = blockIdx.x, h = bh % H;
+    const int t0 = tile * CT + sub * CSUB, t1 = min(T, t0 + CSUB);
     float w[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 4; ++j) w[j] = ldf(conv_w + ((size_t)h * 4 + j) * dv + c);
     const size_t base = (size_t)bh * T;
-    // sliding windows in registers: hw[j] = dH[t + j] (0 past the end), vw[j] = v[t - j] (history or
-    // 0 before the start), so each token's dH and v are loaded once
     auto vat = [&](int src) -> float {
         if (src >= 0) return ldf(v + (base + src) * dv + c);
         return v_hist ? ldf(v_hist + ((size_t)bh * 3 + 3 + src) * dv + c) : 0.f;
     };
-    float hw[4], vw[4];
+    // the sub-tile's dH[t0 .. t0 + CSUB + 2], v[t0 - 3 .. t0 + CSUB - 1] and dv, all loaded before
+    // the arithmetic (0 past the end; history or 0 before the start)
+    float hs[CSUB + 3], vs[CSUB + 3], dvs[CSUB];
 #pragma unroll
-    for (int j = 0; j < 3; ++j) hw[j] = t0 + j < T ? dH[(base + t0 + j) * dv + c] : 0.f;
-#pragma unroll
-    for (int j = 1; j < 4; ++j) vw[j] = vat(t0 - j);
-#pragma unroll 4
-    for (int t = t0; t < t1; ++t) {
-        hw[3] = t + 3 < T ? dH[(base + t + 3) * dv + c] : 0.f;
-        vw[0] = ldf(v + (base + t) * dv + c);
-        const float s = fmaf(w[0], hw[0], fmaf(w[1], hw[1], fmaf(w[2], hw[2], w[3] * hw[3])));
-        dv_out[(base + t) * dv + c] += s;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j] = fmaf(hw[0], vw[j], acc[j]);
-#pragma unroll
-        for (int j = 0; j < 3; ++j) hw[j] = hw[j + 1];
-#pragma unroll
-        for (int j = 3; j > 0; --j) vw[j] = vw[j - 1];
+    for (int i = 0; i < CSUB + 3; ++i) {
+        const int t = t0 + i;
+        hs[i] = t < T ? dH[(base + t) * dv + c] : 0.f;
+        vs[i] = (t0 < T && t - 3 < T) ? vat(t - 3) : 0.f;
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) dWp[(((size_t)bh * ntile + tile) * 4 + j) * dv + c] = acc[j];
-    if (tile == 0 && dv_hist) {
-        // slot s holds v_{s-3}, which enters h_t through tap j = t - s + 3 for t in [0, s]
-        for (int s = 0; s < 3; ++s) {
-            float g = 0.f;
-            for (int t = 0; t <= s && t < T; ++t) g = fmaf(w[t - s + 3], dH[(base + t) * dv + c], g);
-            dv_hist[((size_t)bh * 3 + s) * dv + c] = g;
+    for (int i = 0; i < CSUB; ++i) dvs[i] = t0 + i < T ? dv_out[(base + t0 + i) * dv + c] : 0.f;
+#pragma unroll
+    for (int i = 0; i < CSUB; ++i) {
+        if (t0 + i >= t1) break;
+        // token t = t0 + i: dv_t += sum_j w_j dH_{t+j};  dw_j += dH_t v_{t-j}
+        const float s = fmaf(w[0], hs[i], fmaf(w[1], hs[i + 1], fmaf(w[2], hs[i + 2], w[3] * hs[i + 3])));
+        dv_out[(base + t0 + i) * dv + c] = dvs[i] + s;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j] = fmaf(hs[i], vs[i + 3 - j], acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) part[sub][j][c] = acc[j];
+    __syncthreads();
+    if (sub == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float sum = part[0][j][c];
+#pragma unroll
+            for (int q = 1; q < CT / CSUB; ++q) sum += part[q][j][c];
+            dWp[(((size_t)bh * ntile + tile) * 4 + j) * dv + c] = sum;
+        }
+        if (tile == 0 && dv_hist) {
+            // slot s holds v_{s-3}, which enters h_t through tap j = t - s + 3 for t in [0, s]
+            for (int s = 0; s < 3; ++s) {
+                float g = 0.f;
+                for (int t = 0; t <= s && t < T; ++t) g = fmaf(w[t - s + 3], dH[(base + t) * dv + c], g);
+                dv_hist[((size_t)bh * 3 + s) * dv + c] = g;
+            }
         }
     }
 }
 
-// dconv_w[h][j][c] = sum over the batch and the tiles of dWp.
-__global__ void __launch_bounds__(NT) conv_reduce_kernel(const float *__restrict__ dWp, float *__restrict__ dconv_w,
-                                                         int B, int H, int dv, int ntile)
+// dconv_w[h][j][c] = sum over the batch and the tiles of dWp: a block takes 32 consecutive
+// (h, j, c) outputs; its 32 warps take the (b, tile) terms e = warp, warp + 32, ... (lane =
+// output), and the 32 partial sums meet in shared memory in a fixed order.
+__global__ void __launch_bounds__(1024) conv_reduce_kernel(const float *__restrict__ dWp, float *__restrict__ dconv_w,
+                                                           int B, int H, int dv, int ntile)
 {
-    // block: 64 consecutive (h, j, c) outputs x 4 groups of the (b, tile) terms, fixed order
-    __shared__ float part[4][64];
-    const int o = blockIdx.x * 64 + (threadIdx.x & 63), grp = threadIdx.x >> 6;
-    const int nout = H * 4 * dv;
+    __shared__ float part[32][33];
+    const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+    const int o = blockIdx.x * 32 + lane, nout = H * 4 * dv;
     float s = 0.f;
     if (o < nout) {
         const int h = o / (4 * dv), jc = o % (4 * dv);
         const int nterm = B * ntile;
-        for (int e = grp; e < nterm; e += 4) {
+#pragma unroll 4
+        for (int e = wp; e < nterm; e += 32) {
             const int b = e / ntile, tile = e % ntile;
             s += dWp[(((size_t)b * H + h) * ntile + tile) * 4 * dv + jc];
         }
     }
-    part[grp][threadIdx.x & 63] = s;
+    part[wp][lane] = s;
     __syncthreads();
-    if (grp == 0 && o < nout) dconv_w[o] = (part[0][threadIdx.x] + part[1][threadIdx.x]) + (part[2][threadIdx.x] + part[3][threadIdx.x]);
+    if (wp == 0) {
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) sum += part[q][lane];
+        if (o < nout) dconv_w[o] = sum;
+    }
 }
 
 struct Carve {
@@ -960,11 +978,11 @@ cudaError_t token_local(const Shape &s, const BackwardArgs &a, float *dX, float 
     }
     tm.end();
     tm.begin("bwd_conv_grad");
-    conv_grad_kernel<io_t><<<dim3(ntile, s.BH), s.dv, 0, st>>>(v, vh, cw, dH, a.dv, a.dv_hist, dWp, s.H, s.T, s.dv,
-                                                               ntile);
+    conv_grad_kernel<io_t><<<dim3(ntile, s.BH), s.dv * (CT / CSUB), 0, st>>>(v, vh, cw, dH, a.dv, a.dv_hist, dWp,
+                                                                             s.H, s.T, s.dv, ntile);
     tm.end();
     tm.begin("bwd_conv_reduce");
-    conv_reduce_kernel<<<(s.H * 4 * s.dv + 63) / 64, NT, 0, st>>>(dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
+    conv_reduce_kernel<<<(s.H * 4 * s.dv + 31) / 32, 1024, 0, st>>>(dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
     tm.end();
     return cudaGetLastError();
 }

@@ -51,10 +51,10 @@ __device__ __forceinline__ uint64_t dsc(uint64_t base, uint32_t off, uint32_t lb
     return base + (uint64_t)(off >> 4) + ((uint64_t)(lbo >> 4) << 16) + ((uint64_t)(sbo >> 4) << 32);
 }
 
-// Gain g = GELU'(a) = Phi(a) + a phi(a) and Phi(a), for the exact-erf GELU.  Phi uses the
-// rational approximation of erf from Abramowitz & Stegun, Handbook of Mathematical Functions,
-// formula 7.1.26 (|error| <= 1.5e-7), which shares the Gaussian factor e^{-a^2/2} with phi.
-__device__ __forceinline__ void gelu_gain(float a, float &g, float &Phi)
+// The normal cdf Phi(a) and density phi(a) = e^{-a^2/2} / sqrt(2 pi).  Phi uses the rational
+// approximation of erf from Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26 (|error| <= 1.5e-7), which shares the Gaussian factor e^{-a^2/2} with phi.
+__device__ __forceinline__ void gauss_parts(float a, float &Phi, float &phi)
 {
     const float x = fabsf(a) * 0.70710678118654752f;
     const float t = __fdividef(1.f, fmaf(0.3275911f, x, 1.f));
@@ -65,21 +65,23 @@ __device__ __forceinline__ void gelu_gain(float a, float &g, float &Phi)
     poly = fmaf(t, poly, 0.254829592f);
     const float erfx = 1.f - poly * t * E;
     Phi = 0.5f + copysignf(0.5f * erfx, a);
-    g = fmaf(a, 0.39894228040143268f * E, Phi);
+    phi = 0.39894228040143268f * E;
 }
 
-// GELU(z) = z Phi(z) (exact-erf form), Phi from the same rational approximation of erf.
+// Gain g = GELU'(a) = Phi(a) + a phi(a) and Phi(a), for the exact-erf GELU.
+__device__ __forceinline__ void gelu_gain(float a, float &g, float &Phi)
+{
+    float phi;
+    gauss_parts(a, Phi, phi);
+    g = fmaf(a, phi, Phi);
+}
+
+// GELU(z) = z Phi(z) (exact-erf form).
 __device__ __forceinline__ float gelu_value(float z)
 {
-    const float x = fabsf(z) * 0.70710678118654752f;
-    const float t = __fdividef(1.f, fmaf(0.3275911f, x, 1.f));
-    const float E = __expf(-0.5f * z * z);
-    float poly = fmaf(t, 1.061405429f, -1.453152027f);
-    poly = fmaf(t, poly, 1.421413741f);
-    poly = fmaf(t, poly, -0.284496736f);
-    poly = fmaf(t, poly, 0.254829592f);
-    const float erfx = 1.f - poly * t * E;
-    return z * (0.5f + copysignf(0.5f * erfx, z));
+    float Phi, phi;
+    gauss_parts(z, Phi, phi);
+    return z * Phi;
 }
 
 // barrier over `n` threads (whole warps) of the CTA; ids 1.. (0 is __syncthreads')
