@@ -157,25 +157,6 @@ __device__ __forceinline__ void ld_row_b(const uint8_t *panel, int row, int col0
     }
 }
 
-// fp32 [rows][64] row-major (global) -> fp16 SW128 panel; rows >= nrows (or all, for src == null) zero
-__device__ __forceinline__ void f32_to_panel(uint8_t *panel, const float *src, int nrows, int tid)
-{
-    for (int e = tid; e < 512; e += NT) {
-        const int r = e >> 3, g = e & 7;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-        if (src && r < nrows) {
-            a = *reinterpret_cast<const float4 *>(src + r * D + 8 * g);
-            b = *reinterpret_cast<const float4 *>(src + r * D + 8 * g + 4);
-        }
-        uint4 w;
-        w.x = pack_h2(a.x, a.y);
-        w.y = pack_h2(a.z, a.w);
-        w.z = pack_h2(b.x, b.y);
-        w.w = pack_h2(b.z, b.w);
-        *reinterpret_cast<uint4 *>(panel + sw128(r, 8 * g)) = w;
-    }
-}
-
 // a bf16 panel (as TMA wrote it) -> fp16 in place; with `copy`, also a copy whose row r is scaled
 // by scale[r] (a 16-byte granule at physical offset 128 r + 16 g belongs to row r, whatever column
 // group the swizzle put there)
@@ -369,21 +350,38 @@ __global__ void __launch_bounds__(NT, 1)
     auto wait_all = [&](int b, uint32_t ph) {
         if (!mbar_wait(smem_u32(&mbar[b]), ph, p.wait_ns)) expired();
     };
+    // this thread's dout granules (row tid / 8; 0 past the end) and halo value, loaded before
+    // anything else so that their loads are in flight together: the three tokens before the chunk
+    // are history or earlier tokens of the sequence (zero before it)
+    static_assert(NT == 64 * 8 && 3 * D <= NT, "one row granule pair and one halo value per thread");
+    const int cr = tid >> 3, cg = tid & 7;
+    float4 d0 = make_float4(0.f, 0.f, 0.f, 0.f), d1 = d0;
+    if (cr < n) {
+        const float4 *d4 = reinterpret_cast<const float4 *>(p.dout + (tok0 + cr) * D + 8 * cg);
+        d0 = d4[0];
+        d1 = d4[1];
+    }
+    float hx = 0.f;
+    if (tid < 3 * D) {
+        const int j = tid / D, ch = tid % D, t = t0 - 3 + j;
+        if (t >= 0) hx = __bfloat162float(p.v[((size_t)bh * p.T + t) * D + ch]);
+        else if (p.v_hist) hx = __bfloat162float(p.v_hist[((size_t)bh * 3 + (3 + t)) * D + ch]);
+    }
     // thread 0 waits for the tiles at once (the first product needs them); the others stage
     if (tid == 0) {
         if (mbar_wait(mb_ld, 0, p.wait_ns)) pend_ld = false;
         else expired();
     }
     load_scalars(sc, p, tok0, n, tid);
-    // the three tokens before the chunk (history or earlier tokens of the sequence; zero before it)
-    for (int e = tid; e < 3 * D; e += NT) {
-        const int j = e / D, ch = e % D, t = t0 - 3 + j;
-        float x = 0.f;
-        if (t >= 0) x = __bfloat162float(p.v[((size_t)bh * p.T + t) * D + ch]);
-        else if (p.v_hist) x = __bfloat162float(p.v_hist[((size_t)bh * 3 + (3 + t)) * D + ch]);
-        sc[SC_HALO + e] = x;
+    if (tid < 3 * D) sc[SC_HALO + tid] = hx;
+    {
+        uint4 w;
+        w.x = pack_h2(d0.x, d0.y);
+        w.y = pack_h2(d0.z, d0.w);
+        w.z = pack_h2(d1.x, d1.y);
+        w.w = pack_h2(d1.z, d1.w);
+        *reinterpret_cast<uint4 *>(P(DO) + sw128(cr, 8 * cg)) = w;
     }
-    f32_to_panel(P(DO), p.dout + tok0 * D, n, tid);
     for (int e = tid; e < 512; e += NT) reinterpret_cast<uint4 *>(P(ZERO))[e] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
@@ -839,22 +837,53 @@ __global__ void __launch_bounds__(NT, 1)
     auto wait_all = [&](int b, uint32_t ph) {
         if (!mbar_wait(smem_u32(&mbar[b]), ph, p.wait_ns)) expired();
     };
+    // the chunk's fp32 operands into registers before anything else: S_c, G_c, dout (0 past the
+    // end) and S_{c+1}, granules 2 cg, 2 cg + 1 of row cr, so that their loads are in flight together
+    static_assert(NT == 64 * 8, "one row granule pair per thread");
+    const int cr = tid >> 3, cg = tid & 7;
+    float4 fv[8];
+    {
+        const float4 *s4 = reinterpret_cast<const float4 *>(Sc + cr * D + 8 * cg);
+        const float4 *g4 = reinterpret_cast<const float4 *>(Gc + cr * D + 8 * cg);
+        const float4 *n4 = reinterpret_cast<const float4 *>(Sc + D * D + cr * D + 8 * cg);
+        fv[0] = s4[0];
+        fv[1] = s4[1];
+        fv[2] = g4[0];
+        fv[3] = g4[1];
+        fv[6] = n4[0];
+        fv[7] = n4[1];
+        fv[4] = fv[5] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (cr < n) {
+            const float4 *d4 = reinterpret_cast<const float4 *>(p.dout + (tok0 + cr) * D + 8 * cg);
+            fv[4] = d4[0];
+            fv[5] = d4[1];
+        }
+    }
     if (tid == 0) {  // thread 0 waits for the tiles at once; the others stage
         if (mbar_wait(mb_ld, 0, p.wait_ns)) pend_ld = false;
         else expired();
     }
     load_scalars(sc, p, tok0, n, tid);
     for (int e = tid; e < 24 * 64; e += NT) s_sig[e] = 0.f;  // sigma, dbeta, q.dq slots
-    f32_to_panel(P(S0), Sc, D, tid);
-    f32_to_panel(P(GB), Gc, D, tid);
-    f32_to_panel(P(DO), p.dout + tok0 * D, n, tid);
+    {
+        auto put = [&](int panel, const float4 &a, const float4 &b) {
+            uint4 w;
+            w.x = pack_h2(a.x, a.y);
+            w.y = pack_h2(a.z, a.w);
+            w.z = pack_h2(b.x, b.y);
+            w.w = pack_h2(b.z, b.w);
+            *reinterpret_cast<uint4 *>(P(panel) + sw128(cr, 8 * cg)) = w;
+        };
+        put(S0, fv[0], fv[1]);
+        put(GB, fv[2], fv[3]);
+        put(DO, fv[4], fv[5]);
+    }
     for (int e = tid; e < 512; e += NT) reinterpret_cast<uint4 *>(P(ZERO))[e] = make_uint4(0, 0, 0, 0);
     {  // F0 = <G_c, S_{c+1}> (for dalpha), partial per warp
-        const float4 *g4 = reinterpret_cast<const float4 *>(Gc), *s4 = reinterpret_cast<const float4 *>(Sc + D * D);
         float part = 0.f;
 #pragma unroll
-        for (int q = 0; q < D * D / 4 / NT; ++q) {
-            const float4 a = g4[tid + NT * q], b = s4[tid + NT * q];
+        for (int q = 0; q < 2; ++q) {
+            const float4 a = fv[2 + q], b = fv[6 + q];
             part = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, part))));
         }
 #pragma unroll
