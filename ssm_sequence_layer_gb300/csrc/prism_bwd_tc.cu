@@ -87,6 +87,21 @@ struct Params {
 };
 
 // ---- small helpers ---------------------------------------------------------------------------------
+// barrier over `n` threads (whole warps; id >= 1)
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// barrier over `n` threads (whole warps; id >= 1) that returns whether any of them passed `flag`
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool flag)
+{
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(any)
+        : "r"((uint32_t)flag), "r"(id), "r"(n)
+        : "memory");
+    return any != 0;
+}
+
 __device__ __forceinline__ uint64_t km(uint64_t dbase, uint32_t off) { return dsc(dbase, off, 16, 1024); }
 __device__ __forceinline__ uint64_t mn(uint64_t dbase, uint32_t off, uint32_t lbo) { return dsc(dbase, off, lbo, 1024); }
 
@@ -631,32 +646,34 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // =====================================================================================================
-// scan: grid (64 / SC_ROWS row blocks, BH, 2 directions), 256 threads.  Forward: S_{c+1} = S_c A_c + B_c
+// scan: grid (64 / SC_ROWS row blocks, BH, 2 directions), 256 + 32 threads.  Forward: S_{c+1} = S_c A_c + B_c
 // from S_init (or 0), storing S_c for c = 0 .. NC.  Reverse: G_{c-1} = G_c A_c^T + Bbar_c from
 // dS_final (or 0), storing G_c for c = NC-1 .. 0, the last value being dS_init.  Thread (q, c)
 // forms the partial sums over m in [16 q, 16 q + 16) of all the block's rows of column c, so each
 // map element is read from shared memory once per step and used for every row from a register; the
 // four partials meet through shared memory.  Four rows a block: two blocks share an SM, which hides
-// the step's latencies better than one block of eight rows.  The maps stream through a ring of bulk copies (one thread
-// issues them; every thread waits on the stage's mbarrier, bounded).
+// the step's latencies better than one block of eight rows.  The maps stream through a ring of bulk
+// copies issued by one lane of a producer warp, off the steps' critical path: every consumer waits
+// on the stage's `full` mbarrier, each consumer warp arrives on its `empty` mbarrier once it has
+// read the stage, and the producer waits for that before refilling it (every wait bounded).
 constexpr int SC_ROWS = 4, SC_STAGES = 4;
 constexpr int SC_OUTS = SC_ROWS * D / SCAN_NT;  // outputs a thread forms in the reduction (consecutive columns)
 static_assert(SC_OUTS >= 1 && SC_OUTS <= 4, "scan layout");
 constexpr int SC_STAGE_FLOATS = D * D + SC_ROWS * D;
 constexpr size_t SCAN_SMEM = (size_t)(SC_STAGES * SC_STAGE_FLOATS + SC_ROWS * D + 4 * SC_ROWS * D) * 4 + 128;
+static_assert(SC_OUTS * SCAN_NT == SC_ROWS * D && SCAN_NT % 64 == 0, "the consumers' roles");
 
-__global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__ mapA, const float *__restrict__ mapAT,
-                                                  const float *__restrict__ mapB, const float *__restrict__ mapBb,
-                                                  const float *__restrict__ S_init, const float *__restrict__ dS_final,
-                                                  float *__restrict__ Sst, float *__restrict__ Gst,
-                                                  float *__restrict__ dS_init, int NC, int *status,
-                                                  unsigned long long wait_ns)
+__global__ void __launch_bounds__(SCAN_NT + 32) scan_kernel(const float *__restrict__ mapA, const float *__restrict__ mapAT,
+                                                       const float *__restrict__ mapB, const float *__restrict__ mapBb,
+                                                       const float *__restrict__ S_init, const float *__restrict__ dS_final,
+                                                       float *__restrict__ Sst, float *__restrict__ Gst,
+                                                       float *__restrict__ dS_init, int NC, int *status,
+                                                       unsigned long long wait_ns)
 {
     extern __shared__ __align__(128) float ssm[];
     float *st = ssm + SC_STAGES * SC_STAGE_FLOATS;  // the state rows [SC_ROWS][64]
     float *red = st + SC_ROWS * D;                  // partial sums [4][SC_ROWS][64]
-    __shared__ __align__(8) uint64_t mbar[SC_STAGES];
-    __shared__ int abort_s;
+    __shared__ __align__(8) uint64_t full[SC_STAGES], empty[SC_STAGES];
     const int tid = threadIdx.x, col = tid & 63, qm = tid >> 6;  // partial-sum role
     const int orow = tid / (D / SC_OUTS), oc = (tid % (D / SC_OUTS)) * SC_OUTS;  // output role
     const int rb = blockIdx.x * SC_ROWS, bh = blockIdx.y;
@@ -664,42 +681,65 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__
     const float *M = rev ? mapAT : mapA, *Bv = rev ? mapBb : mapB;
     const float *init = rev ? dS_final : S_init;
     if (tid == 0) {
-        abort_s = 0;
-        for (int i = 0; i < SC_STAGES; ++i) mbar_init(smem_u32(&mbar[i]), 1);
+        for (int i = 0; i < SC_STAGES; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), SCAN_NT / 32);  // one arrival per consumer warp
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     grid_dependency_wait();
     allow_dependent_launch();
     float s[SC_OUTS];
+    if (tid < SCAN_NT) {
 #pragma unroll
-    for (int e = 0; e < SC_OUTS; ++e) s[e] = init ? init[((size_t)bh * D + rb + orow) * D + oc + e] : 0.f;
+        for (int e = 0; e < SC_OUTS; ++e) s[e] = init ? init[((size_t)bh * D + rb + orow) * D + oc + e] : 0.f;
 #pragma unroll
-    for (int e = 0; e < SC_OUTS; ++e) st[orow * D + oc + e] = s[e];
-    int issued = 0;  // thread 0: stages issued so far
-    auto stage_in = [&](int k) {
-        const int cc = rev ? NC - 1 - k : k;
-        const size_t mo = ((size_t)bh * NC + cc) * D * D;
-        const uint32_t mb = smem_u32(&mbar[k % SC_STAGES]);
-        const uint32_t dst = smem_u32(ssm + (k % SC_STAGES) * SC_STAGE_FLOATS);
-        mbar_expect_tx(mb, SC_STAGE_FLOATS * 4);
-        bulk_load(dst, M + mo, D * D * 4, mb);
-        bulk_load(dst + D * D * 4, Bv + mo + (size_t)rb * D, SC_ROWS * D * 4, mb);
-        issued = k + 1;
-    };
+        for (int e = 0; e < SC_OUTS; ++e) st[orow * D + oc + e] = s[e];
+    }
     __syncthreads();
-    if (tid == 0)
-        for (int k = 0; k < SC_STAGES && k < NC; ++k) stage_in(k);
-    int k = 0;
-    for (; k < NC; ++k) {
+
+    if (tid >= SCAN_NT) {  // ---- producer: one lane of the last warp streams the maps -------------------
+        if (tid == SCAN_NT) {
+            int issued = 0;
+            for (int k = 0; k < NC; ++k) {
+                const int slot = k % SC_STAGES;
+                if (k >= SC_STAGES &&
+                    !mbar_wait(smem_u32(&empty[slot]), (uint32_t)(k / SC_STAGES - 1) & 1u, wait_ns)) {
+                    set_status(status, kDevTimeout);
+                    break;
+                }
+                const int cc = rev ? NC - 1 - k : k;
+                const size_t mo = ((size_t)bh * NC + cc) * D * D;
+                const uint32_t mb = smem_u32(&full[slot]);
+                const uint32_t dst = smem_u32(ssm + slot * SC_STAGE_FLOATS);
+                mbar_expect_tx(mb, SC_STAGE_FLOATS * 4);
+                bulk_load(dst, M + mo, D * D * 4, mb);
+                bulk_load(dst + D * D * 4, Bv + mo + (size_t)rb * D, SC_ROWS * D * 4, mb);
+                issued = k + 1;
+            }
+            // every copy issued lands before the CTA exits (bounded): only the last SC_STAGES
+            // stages can still be in flight
+            for (int j = max(0, issued - SC_STAGES); j < issued; ++j)
+                (void)mbar_wait(smem_u32(&full[j % SC_STAGES]), (uint32_t)(j / SC_STAGES) & 1u, 1000000000ull);
+        }
+        return;
+    }
+
+    // ---- consumers (the first SCAN_NT threads); their barriers leave the producer warp out.  An
+    // expired wait is recorded per thread and OR-reduced at the step's last barrier, so every
+    // consumer leaves the loop at the same step.
+    bool expired = false, stop = false;
+    for (int k = 0; k < NC; ++k) {
         const int cc = rev ? NC - 1 - k : k;
         float *out = rev ? Gst + ((size_t)bh * NC + cc) * D * D : Sst + ((size_t)bh * (NC + 1) + cc) * D * D;
 #pragma unroll
         for (int e = 0; e < SC_OUTS; ++e) out[(size_t)(rb + orow) * D + oc + e] = s[e];
-        if (!mbar_wait(smem_u32(&mbar[k % SC_STAGES]), (uint32_t)(k / SC_STAGES) & 1u, wait_ns)) {
-            abort_s = 1;
+        const int slot = k % SC_STAGES;
+        if (!mbar_wait(smem_u32(&full[slot]), (uint32_t)(k / SC_STAGES) & 1u, wait_ns)) {
+            expired = true;
             set_status(status, kDevTimeout);
         }
-        const float *mm = ssm + (k % SC_STAGES) * SC_STAGE_FLOATS;
+        const float *mm = ssm + slot * SC_STAGE_FLOATS;
         float part[SC_ROWS];
 #pragma unroll
         for (int r = 0; r < SC_ROWS; ++r) part[r] = 0.f;
@@ -717,30 +757,24 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float *__restrict__
         }
 #pragma unroll
         for (int r = 0; r < SC_ROWS; ++r) red[(qm * SC_ROWS + r) * D + col] = part[r];
-        __syncthreads();  // partials complete; the state rows of step k are no longer read
+        named_bar(1, SCAN_NT);  // partials complete; the state rows of step k are no longer read
+        float bv[SC_OUTS];
+#pragma unroll
+        for (int e = 0; e < SC_OUTS; ++e) bv[e] = mm[D * D + orow * D + oc + e];
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(smem_u32(&empty[slot]));  // this warp is done with the stage
 #pragma unroll
         for (int e = 0; e < SC_OUTS; ++e) {
-            float acc = mm[D * D + orow * D + oc + e];
+            float acc = bv[e];
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc += red[(q * SC_ROWS + orow) * D + oc + e];
             st[orow * D + oc + e] = acc;
             s[e] = acc;
         }
-        __syncthreads();  // the new state is written; stage k % SC_STAGES and the partials are free
-        if (abort_s) break;
-        if (tid == 0 && k + SC_STAGES < NC) {
-            fence_async_smem();  // the threads' reads of this stage precede the copy that refills it
-            stage_in(k + SC_STAGES);
-        }
+        // the new state is written and the partials are free; leave together after an expired wait
+        if ((stop = named_bar_or(1, SCAN_NT, expired))) break;
     }
-    if (abort_s) {
-        // after an expired wait at step k, the stages k .. issued-1 may still be in flight (each
-        // the next phase of its slot): let them land before the CTA exits, bounded
-        if (tid == 0)
-            for (int j = k; j < issued; ++j)
-                (void)mbar_wait(smem_u32(&mbar[j % SC_STAGES]), (uint32_t)(j / SC_STAGES) & 1u, 1000000000ull);
-        return;
-    }
+    if (stop) return;
 #pragma unroll
     for (int e = 0; e < SC_OUTS; ++e) {
         if (!rev) Sst[((size_t)bh * (NC + 1) + NC) * D * D + (size_t)(rb + orow) * D + oc + e] = s[e];
@@ -1342,7 +1376,7 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     cfg.numAttrs = 1;
     tm.begin("bwd_chunk_scan");
     cfg.gridDim = dim3(D / SC_ROWS, s.BH, 2);
-    cfg.blockDim = dim3(SCAN_NT);
+    cfg.blockDim = dim3(SCAN_NT + 32);
     cfg.dynamicSmemBytes = SCAN_SMEM;
     e = cudaLaunchKernelEx(&cfg, scan_kernel, (const float *)w.mapA, (const float *)w.mapAT, (const float *)w.mapB,
                            (const float *)w.mapBb, a.S_init, a.dS_final, w.Sst, w.Gst, a.dS_init, s.NC, d_status,
