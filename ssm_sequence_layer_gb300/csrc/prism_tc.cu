@@ -448,6 +448,23 @@ __global__ void __launch_bounds__(NT, 1)
         }
     };
 
+    // the Gram tiles D1 = [K; U_0] [Q; K]^T and D1' = [U_1; U_2] [Q; K]^T on the bf16 input tiles
+    // (exact values), committed to the MMA barrier (thread 0)
+    auto issue_gram = [&]() {
+        const uint32_t id = idesc_bf16(128, 128, 0, 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+            mma_f16(tmem + TM_D1, dsc(dbase, OFF_K + s * 32, 16, 1024), dsc(dbase, OFF_Q + s * 32, 16, 1024), id,
+                    s > 0);
+        if (R >= 2)
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + TM_D1 + 128, dsc(dbase, OFF_U + TILE + s * 32, 16, 1024),
+                        dsc(dbase, OFF_Q + s * 32, 16, 1024), id, s > 0);
+        mma_commit(mb_mma);
+        pending |= 1u;
+    };
+
     if (tid == 0 && c_begin < c_end) {
         issue_v(c_begin, 0);
         issue_qku(c_begin);
@@ -563,22 +580,16 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- P2: Gram tiles  D1 = [K; U_0] [Q; K]^T,  D1' = [U_1; U_2] [Q; K]^T ------------------
         // (rows are key/direction tokens j, columns query/key tokens i: the score tiles come out
         // transposed, [j][i], which is the operand form the later products read)
-        if (!wait_one(mb_qku, ph_qku, 2u)) break;
+        // The first chunk of the segment waits for its tiles and issues its Gram here; every later
+        // chunk's Gram was issued at the end of the chunk before it, under that chunk's output
+        // stores, so only its completion is waited for.
+        if (c == c_begin && !wait_one(mb_qku, ph_qku, 2u)) break;
         if (tid == 0 && c + 1 < c_end) issue_v(c + 1, stage ^ 1);
-        if (tid == 0) {  // the input tiles are still bf16 here (exact values); the Gram runs on them
-            fence_after_sync();
-            const uint32_t id = idesc_bf16(128, 128, 0, 0);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_D1, dsc(dbase, OFF_K + s * 32, 16, 1024), dsc(dbase, OFF_Q + s * 32, 16, 1024),
-                        id, s > 0);
-            if (R >= 2)
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_f16(tmem + TM_D1 + 128, dsc(dbase, OFF_U + TILE + s * 32, 16, 1024),
-                            dsc(dbase, OFF_Q + s * 32, 16, 1024), id, s > 0);
-            mma_commit(mb_mma);
-            pending |= 1u;
+        if (tid == 0) {
+            if (c == c_begin) {
+                fence_after_sync();
+                issue_gram();
+            }
             if (mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
                 pending &= ~1u;
             } else {
@@ -1057,8 +1068,23 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         PHASE_MARK(16);
+        fence_before_sync();  // the tensor-memory reads of this chunk precede the next chunk's Gram
         __syncthreads();
         PHASE_MARK(17);
+        // the next chunk's Gram, under this chunk's output stores: its tiles were requested during
+        // this chunk (Q after the Q^T copy, K and U after the state-side products), and tensor
+        // memory columns 0..255 are free (D7 and D6 were read above)
+        if (tid == 0 && c + 1 < c_end && abort_s == 0) {
+            if (mbar_wait(mb_qku, ph_qku, p.wait_ns)) {
+                ph_qku ^= 1u;
+                pending &= ~2u;
+                fence_after_sync();
+                issue_gram();
+            } else {
+                abort_s = 1;
+                set_status(p.status, kDevTimeout);
+            }
+        }
         {
             const float *so = reinterpret_cast<const float *>(sm + OFF_E);
             bool finite = true;
