@@ -150,19 +150,37 @@ __device__ __forceinline__ void ut_solve(const float *A, float *T32, float *x, u
     if (st < 64) {  // diagonal 16x16 blocks, one column per thread
         const int o = 16 * (st >> 4), cc = st & 15;
         float t[16];
+        // the block's row r of A as four 16-byte loads, the next row's in flight while a row is
+        // summed; T's column is stored after the whole column (a store between the rows would keep
+        // every later row's loads of A, which it may alias, behind it)
+        auto arow = [&](int r, float (&a)[16]) {
+            const float4 *src = reinterpret_cast<const float4 *>(A + (o + r) * LDA + o);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 f = src[g];
+                a[4 * g] = f.x;
+                a[4 * g + 1] = f.y;
+                a[4 * g + 2] = f.z;
+                a[4 * g + 3] = f.w;
+            }
+        };
+        float ar[2][16];  // row 0 reads none of A
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
+            if (r + 1 < 16) arow(r + 1, ar[(r + 1) & 1]);
+            const float *a = ar[r & 1];
             // t[j] = 0 for j < cc, so the sum may run over all j < r
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
             for (int j = 0; j + 1 < r; j += 2) {
-                s0 = fmaf(A[(o + r) * LDA + o + j], t[j], s0);
-                s1 = fmaf(A[(o + r) * LDA + o + j + 1], t[j + 1], s1);
+                s0 = fmaf(a[j], t[j], s0);
+                s1 = fmaf(a[j + 1], t[j + 1], s1);
             }
-            if (r & 1) s0 = fmaf(A[(o + r) * LDA + o + r - 1], t[r - 1], s0);
+            if (r & 1) s0 = fmaf(a[r - 1], t[r - 1], s0);
             t[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -(s0 + s1));
-            T32[(o + r) * LDA + o + cc] = t[r];
         }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) T32[(o + r) * LDA + o + cc] = t[r];
     }
     named_bar(bar, SOLVE_THREADS);
     if (sw < 4) {
