@@ -811,48 +811,37 @@ __global__ void __launch_bounds__(NT, 1)
                     frag_c_store(fr, T32, LDA, ri, cj + 8 * nt, y, -1.f);
                 }
                 named_bar(1, NT / 2);
-                if (sw < 4) {
+                {
                     // 32 -> 64: T[32:64][0:32] = -T[32:64][32:64] A[32:64][0:32] T[0:32][0:32]; solver
-                    // warp sw owns the 8-column tile 8 sw of the 32x32 block (both 16-row halves)
-                    const int n0 = 8 * sw;
-                    float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    // warp sw owns the 16-row half mt = sw / 4 of the 8-column tile nt = sw % 4 (n0 = 8 nt):
+                    // its rows of X = A_lo T_lo, then (once all of X is in) its rows of -T_hi X
+                    const int nt = sw & 3, mt = sw >> 2, n0 = 8 * nt;
+                    float x[4] = {0.f, 0.f, 0.f, 0.f};
                     // T_lo[k][n] = 0 for k < 16 <= n: block (0,1) of T32 is never written, so skip it
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {                 // X = A_lo T_lo
                         if (n0 >= 16 && ks < 2) continue;
-                        uint32_t b0, b1;
+                        uint32_t a[4], b0, b1;
                         frag_b(fr, T32, LDA, 8 * ks, n0, b0, b1);
-#pragma unroll
-                        for (int mt = 0; mt < 2; ++mt) {
-                            uint32_t a[4];
-                            frag_a(fr, A, LDA, 32 + 16 * mt, 8 * ks, a);
-                            mma_tf32(x[mt], a[0], a[1], a[2], a[3], b0, b1);
-                        }
+                        frag_a(fr, A, LDA, 32 + 16 * mt, 8 * ks, a);
+                        mma_tf32(x, a[0], a[1], a[2], a[3], b0, b1);
                     }
-                    float *X = s_xtmp + sw * 256;                     // 32 x 8
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        X[(16 * mt + fr.gq) * 8 + 2 * fr.tq] = x[mt][0];
-                        X[(16 * mt + fr.gq) * 8 + 2 * fr.tq + 1] = x[mt][1];
-                        X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq] = x[mt][2];
-                        X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq + 1] = x[mt][3];
-                    }
-                    __syncwarp();
-                    float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    float *X = s_xtmp + nt * 256;                     // 32 x 8
+                    X[(16 * mt + fr.gq) * 8 + 2 * fr.tq] = x[0];
+                    X[(16 * mt + fr.gq) * 8 + 2 * fr.tq + 1] = x[1];
+                    X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq] = x[2];
+                    X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq + 1] = x[3];
+                    named_bar(1, NT / 2);  // both halves of every X tile are in
+                    float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {                 // T_lower = -T_hi X
-                        uint32_t b0, b1;
+                        if (mt == 0 && ks >= 2) continue;  // T_hi[0:16][16:32] = 0 (block (2,3) is never written)
+                        uint32_t a[4], b0, b1;
                         frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
-#pragma unroll
-                        for (int mt = 0; mt < 2; ++mt) {
-                            if (mt == 0 && ks >= 2) continue;  // T_hi[0:16][16:32] = 0 (block (2,3) is never written)
-                            uint32_t a[4];
-                            frag_a(fr, T32, LDA, 32 + 16 * mt, 32 + 8 * ks, a);
-                            mma_tf32(y[mt], a[0], a[1], a[2], a[3], b0, b1);
-                        }
+                        frag_a(fr, T32, LDA, 32 + 16 * mt, 32 + 8 * ks, a);
+                        mma_tf32(y, a[0], a[1], a[2], a[3], b0, b1);
                     }
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) frag_c_store(fr, T32, LDA, 32 + 16 * mt, n0, y[mt], -1.f);
+                    frag_c_store(fr, T32, LDA, 32 + 16 * mt, n0, y, -1.f);
                 }
                 if (tid == 64 && !mbar_wait(mb_mma, ph_mma, p.wait_ns)) {  // MX has read PK_1^T (T's slot)
                     abort_s = 1;
