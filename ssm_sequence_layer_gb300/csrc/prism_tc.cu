@@ -194,42 +194,35 @@ __device__ __forceinline__ float gelu_value(float z)
     return z * Phi;
 }
 
-// round to tf32 (the operand format of mma.sync .tf32)
-__device__ __forceinline__ uint32_t to_tf32(float x)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// D += A B for one m16n8k8 tile (A 16x8 row-major, B 8x8 column-major, tf32 in, fp32 accumulate)
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// m16n8k8 tf32 fragments of fp32 matrices in shared memory (row-major, row stride ld):
-// A: 16 rows from r0, 8 columns from k0; B: 8 rows (k) from k0, 8 columns (n) from n0.
+// The lane's fragment coordinates of a warp-level m16n8 MMA: row group gq = lane / 4, column
+// pair index tq = lane % 4.
 struct Frag {
     int gq, tq;  // lane / 4, lane % 4
 };
-__device__ __forceinline__ void frag_a(const Frag &f, const float *M, int ld, int r0, int k0, uint32_t (&a)[4])
+// m16n8k16 fp16 fragments of fp32 matrices in shared memory (row-major, row stride ld; A: 16 rows
+// from r0, 16 columns from k0; B: 16 rows (k) from k0, 8 columns (n) from n0), rounded to fp16
+// (T enters the tensor-core products as fp16 anyway, and fp16 keeps tf32's 10 mantissa bits), and
+// D += A B with fp32 accumulation.  The C fragment: rows gq and gq + 8, columns 2 tq, 2 tq + 1.
+__device__ __forceinline__ void frag_a16(const Frag &f, const float *M, int ld, int r0, int k0, uint32_t (&a)[4])
 {
-    const float *p = M + (r0 + f.gq) * ld + k0 + f.tq;
-    a[0] = to_tf32(p[0]);
-    a[1] = to_tf32(p[8 * ld]);
-    a[2] = to_tf32(p[4]);
-    a[3] = to_tf32(p[8 * ld + 4]);
+    const float *p = M + (r0 + f.gq) * ld + k0 + 2 * f.tq;
+    a[0] = pack2(p[0], p[1]);
+    a[1] = pack2(p[8 * ld], p[8 * ld + 1]);
+    a[2] = pack2(p[8], p[9]);
+    a[3] = pack2(p[8 * ld + 8], p[8 * ld + 9]);
 }
-__device__ __forceinline__ void frag_b(const Frag &f, const float *M, int ld, int k0, int n0, uint32_t &b0, uint32_t &b1)
+__device__ __forceinline__ void frag_b16(const Frag &f, const float *M, int ld, int k0, int n0, uint32_t &b0, uint32_t &b1)
 {
-    const float *p = M + (k0 + f.tq) * ld + n0 + f.gq;
-    b0 = to_tf32(p[0]);
-    b1 = to_tf32(p[4 * ld]);
+    const float *p = M + (k0 + 2 * f.tq) * ld + n0 + f.gq;
+    b0 = pack2(p[0], p[ld]);
+    b1 = pack2(p[8 * ld], p[9 * ld]);
+}
+__device__ __forceinline__ void mma_h16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ void frag_c_store(const Frag &f, float *M, int ld, int r0, int n0, const float (&c)[4], float sgn)
 {
@@ -787,12 +780,11 @@ __global__ void __launch_bounds__(NT, 1)
                     const int pb = sw >> 1, nt = sw & 1;         // block pair (0: rows 16.., 1: rows 48..)
                     const int ri = 16 + 32 * pb, cj = 32 * pb;        // block (ri, cj) below the diagonal
                     float x[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {                 // X = A[ri][cj] T[cj][cj] (cols 8 nt..)
+                    {                                                 // X = A[ri][cj] T[cj][cj] (cols 8 nt..)
                         uint32_t a[4], b0, b1;
-                        frag_a(fr, A, LDA, ri, cj + 8 * ks, a);
-                        frag_b(fr, T32, LDA, cj + 8 * ks, cj + 8 * nt, b0, b1);
-                        mma_tf32(x, a[0], a[1], a[2], a[3], b0, b1);
+                        frag_a16(fr, A, LDA, ri, cj, a);
+                        frag_b16(fr, T32, LDA, cj, cj + 8 * nt, b0, b1);
+                        mma_h16(x, a, b0, b1);
                     }
                     float *X = s_xtmp + sw * 128;                     // 16 x 8
                     X[fr.gq * 8 + 2 * fr.tq] = x[0];
@@ -801,12 +793,11 @@ __global__ void __launch_bounds__(NT, 1)
                     X[(fr.gq + 8) * 8 + 2 * fr.tq + 1] = x[3];
                     __syncwarp();
                     float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {                 // T[ri][cj] = -T[ri][ri] X
+                    {                                                 // T[ri][cj] = -T[ri][ri] X
                         uint32_t a[4], b0, b1;
-                        frag_a(fr, T32, LDA, ri, ri + 8 * ks, a);
-                        frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
-                        mma_tf32(y, a[0], a[1], a[2], a[3], b0, b1);
+                        frag_a16(fr, T32, LDA, ri, ri, a);
+                        frag_b16(fr, X, 8, 0, 0, b0, b1);
+                        mma_h16(y, a, b0, b1);
                     }
                     frag_c_store(fr, T32, LDA, ri, cj + 8 * nt, y, -1.f);
                 }
@@ -819,12 +810,12 @@ __global__ void __launch_bounds__(NT, 1)
                     float x[4] = {0.f, 0.f, 0.f, 0.f};
                     // T_lo[k][n] = 0 for k < 16 <= n: block (0,1) of T32 is never written, so skip it
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {                 // X = A_lo T_lo
-                        if (n0 >= 16 && ks < 2) continue;
+                    for (int ks = 0; ks < 2; ++ks) {                 // X = A_lo T_lo, 16 of k a step
+                        if (n0 >= 16 && ks == 0) continue;
                         uint32_t a[4], b0, b1;
-                        frag_b(fr, T32, LDA, 8 * ks, n0, b0, b1);
-                        frag_a(fr, A, LDA, 32 + 16 * mt, 8 * ks, a);
-                        mma_tf32(x, a[0], a[1], a[2], a[3], b0, b1);
+                        frag_b16(fr, T32, LDA, 16 * ks, n0, b0, b1);
+                        frag_a16(fr, A, LDA, 32 + 16 * mt, 16 * ks, a);
+                        mma_h16(x, a, b0, b1);
                     }
                     float *X = s_xtmp + nt * 256;                     // 32 x 8
                     X[(16 * mt + fr.gq) * 8 + 2 * fr.tq] = x[0];
@@ -834,12 +825,12 @@ __global__ void __launch_bounds__(NT, 1)
                     named_bar(1, NT / 2);  // both halves of every X tile are in
                     float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {                 // T_lower = -T_hi X
-                        if (mt == 0 && ks >= 2) continue;  // T_hi[0:16][16:32] = 0 (block (2,3) is never written)
+                    for (int ks = 0; ks < 2; ++ks) {                 // T_lower = -T_hi X, 16 of k a step
+                        if (mt == 0 && ks == 1) continue;  // T_hi[0:16][16:32] = 0 (block (2,3) is never written)
                         uint32_t a[4], b0, b1;
-                        frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
-                        frag_a(fr, T32, LDA, 32 + 16 * mt, 32 + 8 * ks, a);
-                        mma_tf32(y, a[0], a[1], a[2], a[3], b0, b1);
+                        frag_b16(fr, X, 8, 16 * ks, 0, b0, b1);
+                        frag_a16(fr, T32, LDA, 32 + 16 * mt, 32 + 16 * ks, a);
+                        mma_h16(y, a, b0, b1);
                     }
                     frag_c_store(fr, T32, LDA, 32 + 16 * mt, n0, y, -1.f);
                 }

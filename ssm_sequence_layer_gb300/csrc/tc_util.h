@@ -1,6 +1,6 @@
 // Device helpers shared by the tensor-core kernels of the chunk-map path: fp16 packing into
 // 128B-swizzled tiles, shared-memory descriptors relative to a 1024-aligned base, the exact-erf
-// GELU gain, warp-level tf32 MMA fragments and the UT solve of one 64-token chunk.
+// GELU gain, warp-level fp16 MMA fragments and the UT solve of one 64-token chunk.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -87,41 +87,35 @@ __device__ __forceinline__ float gelu_value(float z)
 // barrier over `n` threads (whole warps) of the CTA; ids 1.. (0 is __syncthreads')
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
-// ---- warp-level tf32 MMA (the 64x64 triangular solve's block products) ----------------------
-__device__ __forceinline__ uint32_t to_tf32(float x)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// D += A B for one m16n8k8 tile (A 16x8 row-major, B 8x8 column-major, tf32 in, fp32 accumulate)
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// fragments of fp32 matrices in shared memory (row-major, row stride ld): A 16 rows from r0, 8
-// columns from k0; B 8 rows (k) from k0, 8 columns (n) from n0; C 16 x 8 at (r0, n0)
+// ---- warp-level fp16 MMA (the 64x64 triangular solve's block products) ----------------------
+// m16n8k16 fragments of fp32 matrices in shared memory (row-major, row stride ld; A: 16 rows from
+// r0, 16 columns from k0; B: 16 rows (k) from k0, 8 columns (n) from n0), rounded to fp16 (T
+// enters the tensor-core products as fp16 anyway, and fp16 keeps tf32's 10 mantissa bits); the
+// C fragment: rows gq and gq + 8, columns 2 tq, 2 tq + 1 of a 16 x 8 tile.
 struct Frag {
     int gq, tq;  // lane / 4, lane % 4
 };
 __device__ __forceinline__ void frag_a(const Frag &f, const float *M, int ld, int r0, int k0, uint32_t (&a)[4])
 {
-    const float *p = M + (r0 + f.gq) * ld + k0 + f.tq;
-    a[0] = to_tf32(p[0]);
-    a[1] = to_tf32(p[8 * ld]);
-    a[2] = to_tf32(p[4]);
-    a[3] = to_tf32(p[8 * ld + 4]);
+    const float *p = M + (r0 + f.gq) * ld + k0 + 2 * f.tq;
+    a[0] = pack_h2(p[0], p[1]);
+    a[1] = pack_h2(p[8 * ld], p[8 * ld + 1]);
+    a[2] = pack_h2(p[8], p[9]);
+    a[3] = pack_h2(p[8 * ld + 8], p[8 * ld + 9]);
 }
 __device__ __forceinline__ void frag_b(const Frag &f, const float *M, int ld, int k0, int n0, uint32_t &b0, uint32_t &b1)
 {
-    const float *p = M + (k0 + f.tq) * ld + n0 + f.gq;
-    b0 = to_tf32(p[0]);
-    b1 = to_tf32(p[4 * ld]);
+    const float *p = M + (k0 + 2 * f.tq) * ld + n0 + f.gq;
+    b0 = pack_h2(p[0], p[ld]);
+    b1 = pack_h2(p[8 * ld], p[9 * ld]);
+}
+// D += A B for one m16n8k16 tile (fp16 in, fp32 accumulate)
+__device__ __forceinline__ void mma_h16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ void frag_c_store(const Frag &f, float *M, int ld, int r0, int n0, const float (&c)[4], float sgn)
 {
@@ -139,7 +133,7 @@ constexpr int SOLVE_SCRATCH = 4 * 256;
 // T = (I + A)^{-1} for a strictly lower-triangular 64x64 A (fp32, row stride LDA), by 16x16
 // blocks: the diagonal blocks by forward substitution, then the blocks below them,
 // T[bi][bj] = -T[bi][bi] sum_k A[bi][k] T[k][bj], in two merge levels (16 -> 32 -> 64) on warp
-// tf32 MMAs.  Writes T (fp32, T32) and its fp16 copy into the [64][64] SW128 panel `tf` ([i][j],
+// fp16 MMAs (m16n8k16, fp32 accumulation).  Writes T (fp32, T32) and its fp16 copy into the [64][64] SW128 panel `tf` ([i][j],
 // zero above the diagonal).  Run by SOLVE_THREADS threads (whole warps, st = 0..255) that sync on
 // named barrier `bar`; `x` is SOLVE_SCRATCH floats of scratch.  Blocks (0,1) and (2,3) of T32 stay
 // unwritten and are never read.
@@ -189,12 +183,11 @@ __device__ __forceinline__ void ut_solve(const float *A, float *T32, float *x, u
         const int pb = sw >> 1, nt = sw & 1;
         const int ri = 16 + 32 * pb, cj = 32 * pb;
         float xa[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
+        {
             uint32_t a[4], b0, b1;
-            frag_a(fr, A, LDA, ri, cj + 8 * ks, a);
-            frag_b(fr, T32, LDA, cj + 8 * ks, cj + 8 * nt, b0, b1);
-            mma_tf32(xa, a, b0, b1);
+            frag_a(fr, A, LDA, ri, cj, a);
+            frag_b(fr, T32, LDA, cj, cj + 8 * nt, b0, b1);
+            mma_h16(xa, a, b0, b1);
         }
         float *X = x + sw * 128;  // 16 x 8
         X[fr.gq * 8 + 2 * fr.tq] = xa[0];
@@ -203,57 +196,45 @@ __device__ __forceinline__ void ut_solve(const float *A, float *T32, float *x, u
         X[(fr.gq + 8) * 8 + 2 * fr.tq + 1] = xa[3];
         __syncwarp();
         float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
+        {
             uint32_t a[4], b0, b1;
-            frag_a(fr, T32, LDA, ri, ri + 8 * ks, a);
-            frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
-            mma_tf32(y, a, b0, b1);
+            frag_a(fr, T32, LDA, ri, ri, a);
+            frag_b(fr, X, 8, 0, 0, b0, b1);
+            mma_h16(y, a, b0, b1);
         }
         frag_c_store(fr, T32, LDA, ri, cj + 8 * nt, y, -1.f);
     }
     named_bar(bar, SOLVE_THREADS);
-    if (sw < 4) {
+    {
         // 32 -> 64: T[32:64][0:32] = -T[32:64][32:64] A[32:64][0:32] T[0:32][0:32]; warp sw owns the
-        // 8-column tile 8 sw of the 32x32 block (both 16-row halves)
-        const int n0 = 8 * sw;
-        float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // 16-row half mt = sw / 4 of the 8-column tile nt = sw % 4 (n0 = 8 nt): its rows of
+        // X = A_lo T_lo, then (once all of X is in) its rows of -T_hi X
+        const int nt = sw & 3, mt = sw >> 2, n0 = 8 * nt;
+        float xa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            if (n0 >= 16 && ks < 2) continue;  // T_lo[k][n] = 0 for k < 16 <= n
-            uint32_t b0, b1;
-            frag_b(fr, T32, LDA, 8 * ks, n0, b0, b1);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                uint32_t a[4];
-                frag_a(fr, A, LDA, 32 + 16 * mt, 8 * ks, a);
-                mma_tf32(xa[mt], a, b0, b1);
-            }
+        for (int ks = 0; ks < 2; ++ks) {
+            if (n0 >= 16 && ks == 0) continue;  // T_lo[k][n] = 0 for k < 16 <= n
+            uint32_t a[4], b0, b1;
+            frag_b(fr, T32, LDA, 16 * ks, n0, b0, b1);
+            frag_a(fr, A, LDA, 32 + 16 * mt, 16 * ks, a);
+            mma_h16(xa, a, b0, b1);
         }
-        float *X = x + sw * 256;  // 32 x 8
+        float *X = x + nt * 256;  // 32 x 8
+        X[(16 * mt + fr.gq) * 8 + 2 * fr.tq] = xa[0];
+        X[(16 * mt + fr.gq) * 8 + 2 * fr.tq + 1] = xa[1];
+        X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq] = xa[2];
+        X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq + 1] = xa[3];
+        named_bar(bar, SOLVE_THREADS);  // both halves of every X tile are in
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            X[(16 * mt + fr.gq) * 8 + 2 * fr.tq] = xa[mt][0];
-            X[(16 * mt + fr.gq) * 8 + 2 * fr.tq + 1] = xa[mt][1];
-            X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq] = xa[mt][2];
-            X[(16 * mt + fr.gq + 8) * 8 + 2 * fr.tq + 1] = xa[mt][3];
+        for (int ks = 0; ks < 2; ++ks) {
+            if (mt == 0 && ks == 1) continue;  // T_hi[0:16][16:32] = 0
+            uint32_t a[4], b0, b1;
+            frag_b(fr, X, 8, 16 * ks, 0, b0, b1);
+            frag_a(fr, T32, LDA, 32 + 16 * mt, 32 + 16 * ks, a);
+            mma_h16(y, a, b0, b1);
         }
-        __syncwarp();
-        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t b0, b1;
-            frag_b(fr, X, 8, 8 * ks, 0, b0, b1);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                if (mt == 0 && ks >= 2) continue;  // T_hi[0:16][16:32] = 0
-                uint32_t a[4];
-                frag_a(fr, T32, LDA, 32 + 16 * mt, 32 + 8 * ks, a);
-                mma_tf32(y[mt], a, b0, b1);
-            }
-        }
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) frag_c_store(fr, T32, LDA, 32 + 16 * mt, n0, y[mt], -1.f);
+        frag_c_store(fr, T32, LDA, 32 + 16 * mt, n0, y, -1.f);
     }
     named_bar(bar, SOLVE_THREADS);
     for (int e = st; e < 64 * 8; e += SOLVE_THREADS) {  // fp16 copy, zero above the diagonal
