@@ -399,7 +399,6 @@ __global__ void __launch_bounds__(NT, 1)
     const uint64_t l2ef = l2_evict_first_policy();
     uint32_t ph_mma = 0, ph_qku = 0, ph_v[2] = {0, 0};
     uint32_t pending = 0;  // issuer's view (thread 0): 1 MMA, 2 Q/K/U load, 4/8 V loads in flight
-    bool qku_unarmed = false;  // thread 0: the next chunk's Q load is in flight, its phase's arrival not yet made
     const uint32_t qku_bytes = (2 + R) * TILE;
 
     auto issue_qku = [&](int c) {
@@ -716,14 +715,6 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int s = 0; s < 4; ++s)
                     mma_f16(tmem + TM_D2, dsc(dbase, OFF_E + l * 2 * TILE + s * 2048, TILE, 1024),
                              dsc(dbase, OFF_XS + l * TILE + s * 2048, TILE, 1024), id, (l | s) != 0);
-            // [Y; Q^T] I -> Q^T in lanes 64..127 (exact: bf16 times one), so that E4 needs no Q
-            // tile and Q's buffer can take the next chunk's tile right after this.  The first
-            // atom Y is the tile below Q (V data); lanes 0..63 of these columns are never read.
-            const uint32_t idq = idesc_bf16(128, 64, 1, 0);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_QT, dsc(dbase, OFF_Q - TILE + s * 2048, TILE, 1024),
-                        dsc(dbase, OFF_TB + s * 32, 16, 1024), idq, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
         }
@@ -860,12 +851,6 @@ __global__ void __launch_bounds__(NT, 1)
             if (tid == 0) {
                 if (mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
                     pending &= ~1u;
-                    if (c + 1 < c_end) {  // Q was last read by the copy above: reload it now
-                        mbar_add_tx(mb_qku, TILE);
-                        tma_load_3d_hint(sbase + OFF_Q, &tm_q, mb_qku, 0, (c + 1) * C, bh, l2ef);
-                        pending |= 2u;
-                        qku_unarmed = true;
-                    }
                 } else {
                     abort_s = 1;
                     set_status(p.status, kDevTimeout);
@@ -915,6 +900,16 @@ __global__ void __launch_bounds__(NT, 1)
                          id, s > 0);
             mma_commit(mb_mma);
             pending |= 1u;
+            // [Y; Q^T] I -> Q^T in lanes 64..127 (exact: bf16 times one), so that E4 needs no Q tile
+            // and Q's buffer can take the next chunk's tile after P5.  The first atom Y is the tile
+            // below Q (V data); lanes 0..63 of these columns are never read.  Issued here, behind
+            // P4 and outside P3 (where MX and the solve's warp MMAs share the tensor pipe); P5's
+            // commit covers it.
+            const uint32_t idq = idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + TM_QT, dsc(dbase, OFF_Q - TILE + s * 2048, TILE, 1024),
+                        dsc(dbase, OFF_TB + s * 32, 16, 1024), idq, s > 0);
         }
         wait_mma();
         fence_after_sync();
@@ -958,13 +953,9 @@ __global__ void __launch_bounds__(NT, 1)
         wait_mma();
         fence_after_sync();
 
-        if (tid == 0 && c + 1 < c_end && abort_s == 0) {  // K and U of this chunk are no longer read: their
-            mbar_expect_tx(mb_qku, (1 + R) * TILE);             // reload completes the phase
-            qku_unarmed = false;
-            tma_load_3d_hint(sbase + OFF_K, &tm_k, mb_qku, 0, (c + 1) * C, bh, l2ef);
-            for (int l = 0; l < R; ++l) tma_load_4d_hint(sbase + OFF_U + l * TILE, &tm_u, mb_qku, 0, l, (c + 1) * C, bh, l2ef);
-            pending |= 2u;
-        }
+        // the next chunk's Q, K and U: this chunk's Q was last read by the Q^T copy (complete with P5),
+        // K and U by P5
+        if (tid == 0 && c + 1 < c_end && abort_s == 0) issue_qku(c + 1);
         PHASE_MARK(8);
         // ---- E4: Qt = diag(Gamma) Q^T - (G W)^T ;  Mc = Gamma_C I - W^T K' --------------------------
         if (quad >= 2) {
@@ -1138,7 +1129,6 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid == 0 && pending) {
         const uint64_t drain_ns = 1000000000ull;
         if (pending & 1u) (void)mbar_wait(mb_mma, ph_mma, drain_ns);
-        if (qku_unarmed) mbar_arrive(mb_qku);  // the phase's arrival, so that it completes when Q lands
         if (pending & 2u) (void)mbar_wait(mb_qku, ph_qku, drain_ns);
         if (pending & 4u) (void)mbar_wait(mb_v[0], ph_v[0], drain_ns);
         if (pending & 8u) (void)mbar_wait(mb_v[1], ph_v[1], drain_ns);
