@@ -262,9 +262,24 @@ __device__ __forceinline__ void load_scalars(float *sc, const Params &p, size_t 
 
 // decayed, masked scores of row i, columns j0 .. j0 + N - 1: v[q] *= D_{i, j} for j <= i (incl) or
 // j < i; 0 elsewhere
+// The pair decay D_{i,j} = e^{lambda_i - lambda_j} of the kept elements: while the chunk's total
+// decay keeps the per-token factors in fp32 range (-lambda_63 <= 80, the usual case) as a product
+// of two factors from the scalar region (Gamma = e^lambda, colf = e^{lambda_63 - lambda}), else one
+// exponential per element.  `lam` is the scalar region's lambda row.
 template <int N>
 __device__ __forceinline__ void decay_row(float (&v)[N], const float *lam, int i, int j0, bool incl)
 {
+    const float *gam = lam + (SC_GAM - SC_LAM), *colf = lam + (SC_COLF - SC_LAM);
+    if (-lam[63] <= 80.f) {
+        const float ri = gam[i] / gam[63];  // e^{lambda_i - lambda_63}
+#pragma unroll
+        for (int q = 0; q < N; ++q) {
+            const int j = j0 + q;
+            const bool keep = incl ? j <= i : j < i;
+            v[q] = keep ? v[q] * (ri * colf[j]) : 0.f;
+        }
+        return;
+    }
     const float li = lam[i];
 #pragma unroll
     for (int q = 0; q < N; ++q) {
@@ -278,6 +293,17 @@ __device__ __forceinline__ void decay_row(float (&v)[N], const float *lam, int i
 template <int N>
 __device__ __forceinline__ void decay_col(float (&v)[N], const float *lam, int m, int j0, bool incl)
 {
+    const float *gam = lam + (SC_GAM - SC_LAM), *colf = lam + (SC_COLF - SC_LAM);
+    if (-lam[63] <= 80.f) {
+        const float cm = colf[m] / gam[63];  // e^{-lambda_m}
+#pragma unroll
+        for (int q = 0; q < N; ++q) {
+            const int j = j0 + q;
+            const bool keep = incl ? j >= m : j > m;
+            v[q] = keep ? v[q] * (gam[j] * cm) : 0.f;
+        }
+        return;
+    }
     const float lm = lam[m];
 #pragma unroll
     for (int q = 0; q < N; ++q) {
