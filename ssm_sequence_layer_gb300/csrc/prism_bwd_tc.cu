@@ -321,6 +321,40 @@ __device__ __forceinline__ void st_row_f(float *dst, const float (&v)[N])
         reinterpret_cast<float4 *>(dst)[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
 }
 
+// An fp32 [64][64] output tile staged for TMA stores: two panels (columns 0-31 and 32-63), each 64
+// rows of 128 B in the 128B-swizzled layout of the fp32 output tensor maps' boxes.  A row's 16
+// columns from n0 (a multiple of 16) are four 16-byte granules; the rows of a warp hit distinct
+// banks.
+__device__ __forceinline__ uint32_t tile_f_off(int row, int col)
+{
+    return (uint32_t)(col >> 5) * PANEL + sw128(row, 2 * (col & 31));
+}
+__device__ __forceinline__ void st_tile_f(uint8_t *tile, int row, int n0, const float (&v)[16])
+{
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+        *reinterpret_cast<float4 *>(tile + tile_f_off(row, n0 + 4 * g)) =
+            make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+}
+__device__ __forceinline__ void ld_tile_f(const uint8_t *tile, int row, int n0, float (&v)[16])
+{
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const float4 f = *reinterpret_cast<const float4 *>(tile + tile_f_off(row, n0 + 4 * g));
+        v[4 * g] = f.x;
+        v[4 * g + 1] = f.y;
+        v[4 * g + 2] = f.z;
+        v[4 * g + 3] = f.w;
+    }
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     (uint64_t)map),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 // =====================================================================================================
 // maps kernel: shared-memory panels (index x PANEL from a 1024-aligned base)
 namespace mk {
@@ -826,12 +860,15 @@ enum {
     NBK = 2,    // -beta K, in W's place (W is read by the first products only)
     J0 = 14,    // J_0..J_3 over Wbar and colf U_l
     H0 = 18,    // H_0..H_3 over the zero tile and P_l (H_b = J_b + 4 panels)
-    DKW = 22    // dk's write part, fp32 [64][64], over Akk and Mku_0
+    DKW = 22,   // dk's write part, then dk, fp32 [64][64] staged for its TMA store, over Akk and Mku_0
+    DQS = 6,    // dq, staged (fp32, two panels) over Vt and X_0 once the last products have read them
+    DUS = 8     // du_0 .. du_2, staged at DUS + 2 l (X_1 .. GB)
 };
 constexpr uint32_t SC_OFF = NPANELS * PANEL;
 constexpr uint32_t SMEM = SC_OFF + SC_FLOATS * 4 + 1024;
 static_assert(SMEM <= 232448, "shared memory budget");
 static_assert(H0 - J0 == 4 && X0 == VT + 1 && Z == DO + 1 && W == K + 1 && CU0 == WB + 1, "stacked operands");
+static_assert(DQS + 2 <= DUS && DUS + 2 * RMAX <= J0 && DQS > Q, "output staging over tiles the last products read");
 // tensor memory columns (512): first half, then the second half over the dead first-half columns
 constexpr uint32_t TM_G1 = 0, TM_D1 = 256, TM_D2 = 320, TM_D3 = 384, TM_DF = 448;
 constexpr uint32_t TM_C = 0, TM_D = 256, TM_E = 384;
@@ -839,7 +876,8 @@ constexpr uint32_t TM_C = 0, TM_D = 256, TM_E = 384;
 
 __global__ void __launch_bounds__(NT, 1)
     grad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_u, Params p)
+                const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dq,
+                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_du, Params p)
 {
     using namespace gk;
     extern __shared__ uint8_t smem_raw[];
@@ -1163,21 +1201,22 @@ __global__ void __launch_bounds__(NT, 1)
         }
         wait_all(4, 0);
         fence_after_sync();
-        float *dkw = reinterpret_cast<float *>(P(DKW));
+        // the outputs go out by TMA stores of fp32 tiles staged in the tiles the products have read
+        // (rows past the sequence's end are clipped by the tensor maps)
         {
             const int n0 = CW * sub;
             float v[CW];
             if (row < 64) {
                 const int i = row;
                 tmem_ld(tmem + TM_D + lane_off + (uint32_t)n0, v);  // the write part of dk
-                st_row_f(dkw + i * D + n0, v);
+                st_tile_f(P(DKW), i, n0, v);
                 if (R >= 2) {
                     tmem_ld(tmem + TM_D + 64 + lane_off + (uint32_t)n0, v);
-                    if (i < n) st_row_f(p.du + ((tok0 + i) * R + 1) * D + n0, v);
+                    st_tile_f(P(DUS + 2), i, n0, v);
                 }
                 tmem_ld(tmem + TM_E + lane_off + (uint32_t)n0, v);  // dq
+                st_tile_f(P(DQS), i, n0, v);
                 if (i < n) {
-                    st_row_f(p.dq + (tok0 + i) * D + n0, v);
                     float qv[CW];
                     ld_row_h(P(Q), i, n0, qv);
                     float part = 0.f;
@@ -1189,26 +1228,38 @@ __global__ void __launch_bounds__(NT, 1)
                 const int i = row - 64;
                 if (R >= 1) {
                     tmem_ld(tmem + TM_D + lane_off + (uint32_t)n0, v);
-                    if (i < n) st_row_f(p.du + ((tok0 + i) * R + 0) * D + n0, v);
+                    st_tile_f(P(DUS), i, n0, v);
                 }
                 if (R >= 3) {
                     tmem_ld(tmem + TM_D + 64 + lane_off + (uint32_t)n0, v);
-                    if (i < n) st_row_f(p.du + ((tok0 + i) * R + 2) * D + n0, v);
+                    st_tile_f(P(DUS + 4), i, n0, v);
                 }
             }
         }
+        fence_async_smem();
         __syncthreads();
-        if (row >= 64) {  // dk = (dKw)_0 - beta (Gamma Z S + H^T Kw)
-            const int i = row - 64, n0 = CW * sub;
-            float v[CW];
-            tmem_ld(tmem + TM_E + lane_off + (uint32_t)n0, v);
-            if (i < n) {
-                const float b = s_beta[i];
-                const float *w = dkw + i * D + n0;
-#pragma unroll
-                for (int q = 0; q < CW; ++q) v[q] = w[q] - b * v[q];
-                st_row_f(p.dk + (tok0 + i) * D + n0, v);
+        if (tid == 0) {
+            for (int h = 0; h < 2; ++h) {
+                tma_store_3d(&tm_dq, sbase + (DQS + h) * PANEL, 32 * h, t0, bh);
+                for (int l = 0; l < R; ++l) tma_store_4d(&tm_du, sbase + (DUS + 2 * l + h) * PANEL, 32 * h, l, t0, bh);
             }
+            bulk_commit();
+        }
+        if (row >= 64) {  // dk = (dKw)_0 - beta (Gamma Z S + H^T Kw), in place
+            const int i = row - 64, n0 = CW * sub;
+            float v[CW], w[CW];
+            tmem_ld(tmem + TM_E + lane_off + (uint32_t)n0, v);
+            ld_tile_f(P(DKW), i, n0, w);
+            const float b = s_beta[i];
+#pragma unroll
+            for (int q = 0; q < CW; ++q) v[q] = w[q] - b * v[q];
+            st_tile_f(P(DKW), i, n0, v);
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            for (int h = 0; h < 2; ++h) tma_store_3d(&tm_dk, sbase + (DKW + h) * PANEL, 32 * h, t0, bh);
+            bulk_commit();
         }
         // alpha_i dalpha_i = F0 + sum_{j >= i} (q_j.dq_j - sigma_j)
         if (warp == 0) {
@@ -1243,6 +1294,7 @@ __global__ void __launch_bounds__(NT, 1)
         mma_commit(mb_drain);
         (void)mbar_wait(mb_drain, 0, drain_ns);
     }
+    if (tid == 0) bulk_wait_read();  // the output stores have read their tiles
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
@@ -1268,12 +1320,12 @@ PFN_cuTensorMapEncodeTiled_v12000 bt_encoder()
 }
 
 bool bt_encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides_bytes,
-               const cuuint32_t *box)
+               const cuuint32_t *box, CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
 {
     auto fn = bt_encoder();
     if (!fn) return false;
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides_bytes, box,
+    return fn(m, type, (cuuint32_t)rank, const_cast<void *>(base), dims, strides_bytes, box,
               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1350,6 +1402,24 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     } else {
         mu = mk_;  // never read with L = 1
     }
+    // the fp32 outputs the gradient kernel writes by TMA stores: 32-column boxes of one chunk
+    CUtensorMap mdq, mdk, mdu;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)s.T, (cuuint64_t)s.BH};
+        const cuuint64_t str[2] = {(cuuint64_t)D * 4, (cuuint64_t)s.T * D * 4};
+        const cuuint32_t box[3] = {32, 64, 1};
+        if (!bt_encode(&mdq, a.dq, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
+            !bt_encode(&mdk, a.dk, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+            return cudaErrorInvalidValue;
+    }
+    if (s.R > 0) {
+        const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)s.R, (cuuint64_t)s.T, (cuuint64_t)s.BH};
+        const cuuint64_t str[3] = {(cuuint64_t)D * 4, (cuuint64_t)s.R * D * 4, (cuuint64_t)s.T * s.R * D * 4};
+        const cuuint32_t box[4] = {32, 1, 64, 1};
+        if (!bt_encode(&mdu, a.du, 4, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return cudaErrorInvalidValue;
+    } else {
+        mdu = mdq;  // never written with L = 1
+    }
     Params p{};
     p.v = (const __nv_bfloat16 *)a.v;
     p.conv_w = (const __nv_bfloat16 *)a.conv_w;
@@ -1413,7 +1483,7 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     cfg.gridDim = dim3(nchunks);
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = gk::SMEM;
-    e = cudaLaunchKernelEx(&cfg, grad_kernel, mq, mk_, mu, p);
+    e = cudaLaunchKernelEx(&cfg, grad_kernel, mq, mk_, mu, mdq, mdk, mdu, p);
     tm.end();
     if (e != cudaSuccess) return e;
     return backward_token_local(s, PRISM_BF16, a, w.dX, w.dH, w.dWp, tm);
