@@ -862,13 +862,19 @@ enum {
     H0 = 18,    // H_0..H_3 over the zero tile and P_l (H_b = J_b + 4 panels)
     DKW = 22,   // dk's write part, then dk, fp32 [64][64] staged for its TMA store, over Akk and Mku_0
     DQS = 6,    // dq, staged (fp32, two panels) over Vt and X_0 once the last products have read them
-    DUS = 8     // du_0 .. du_2, staged at DUS + 2 l (X_1 .. GB)
+    DUS = 8,    // du_0 .. du_2, staged at DUS + 2 l (X_1 .. GB)
+    DVS = 14,   // dv, staged over Wbar and colf U_0 (read by the first products only)
+    DXS = 22    // dX_0, dX_1 over Akk and Mku (read by the second products); dX_2 at DXS2
 };
+constexpr int DXS2 = 16;  // over colf U_1, U_2
+__host__ __device__ constexpr int dx_stage(int l) { return l < 2 ? DXS + 2 * l : DXS2; }
 constexpr uint32_t SC_OFF = NPANELS * PANEL;
 constexpr uint32_t SMEM = SC_OFF + SC_FLOATS * 4 + 1024;
 static_assert(SMEM <= 232448, "shared memory budget");
 static_assert(H0 - J0 == 4 && X0 == VT + 1 && Z == DO + 1 && W == K + 1 && CU0 == WB + 1, "stacked operands");
 static_assert(DQS + 2 <= DUS && DUS + 2 * RMAX <= J0 && DQS > Q, "output staging over tiles the last products read");
+static_assert(DVS == WB && DVS + 2 == DXS2 && DXS2 + 2 == ZERO && DXS == AKK && DXS + 4 == NPANELS && RMAX <= 3,
+              "dv and dX staging over tiles dead after the first / second products");
 // tensor memory columns (512): first half, then the second half over the dead first-half columns
 constexpr uint32_t TM_G1 = 0, TM_D1 = 256, TM_D2 = 320, TM_D3 = 384, TM_DF = 448;
 constexpr uint32_t TM_C = 0, TM_D = 256, TM_E = 384;
@@ -877,7 +883,8 @@ constexpr uint32_t TM_C = 0, TM_D = 256, TM_E = 384;
 __global__ void __launch_bounds__(NT, 1)
     grad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dq,
-                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_du, Params p)
+                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_du,
+                const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dx, Params p)
 {
     using namespace gk;
     extern __shared__ uint8_t smem_raw[];
@@ -1051,11 +1058,13 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int q = 0; q < CW; ++q) z[q] = s2[q] + v[q];
                 st_row_h(P(Z), i, j0, z);
-                if (i < n) {
+                {
                     float dvv[CW];
 #pragma unroll
                     for (int q = 0; q < CW; ++q) dvv[q] = b * z[q];
-                    st_row_f(p.dv + (tok0 + i) * D + j0, dvv);
+                    st_tile_f(P(DVS), i, j0, dvv);
+                }
+                if (i < n) {
                     const __nv_bfloat162 *vr = reinterpret_cast<const __nv_bfloat162 *>(pre[2]);
                     float part = 0.f;
 #pragma unroll
@@ -1114,16 +1123,18 @@ __global__ void __launch_bounds__(NT, 1)
             mma_k64(tmem + TM_DF, km(dbase, AKK * PANEL), false, mn(dbase, VT * PANEL, PANEL), true,
                     idesc_f16(128, 64, 0, 1), false);
             mma_commit(smem_u32(&mbar[2]));
+            for (int h = 0; h < 2; ++h) tma_store_3d(&tm_dv, sbase + (DVS + h) * PANEL, 32 * h, t0, bh);
+            bulk_commit();
         }
         wait_all(2, 0);
         fence_after_sync();
         {
             const int j0 = CW * sub;
             float v[CW], x[CW];
-            auto dx_out = [&](uint32_t col, int l, int i) {  // dX_l row i -> global, sigma += x.dx
+            auto dx_out = [&](uint32_t col, int l, int i) {  // dX_l row i -> staged, sigma += x.dx
                 tmem_ld(tmem + col + lane_off + (uint32_t)j0, v);
+                st_tile_f(P(dx_stage(l)), i, j0, v);
                 if (i < n) {
-                    st_row_f(p.dX + ((tok0 + i) * R + l) * D + j0, v);
                     ld_row_h(P(X0 + l), i, j0, x);
                     float part = 0.f;
 #pragma unroll
@@ -1146,6 +1157,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (R >= 3) dx_out(TM_D3, 2, i);
             }
         }
+        fence_async_smem();
         fence_before_sync();
         __syncthreads();
         if (tid < n) p.dbeta[tok0 + tid] = (s_db[tid] + s_db[64 + tid]) + (s_db[128 + tid] + s_db[192 + tid]);
@@ -1155,6 +1167,12 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t id = idesc_f16(128, 128, 0, 0);
             mma_k64(tmem + TM_C, km(dbase, VT * PANEL), false, km(dbase, DO * PANEL), false, id, false);
             if (R >= 2) mma_k64(tmem + TM_C + 128, km(dbase, (X0 + 1) * PANEL), false, km(dbase, DO * PANEL), false, id, false);
+            for (int h = 0; h < 2; ++h)
+                for (int l = 0; l < R; ++l) tma_store_4d(&tm_dx, sbase + (dx_stage(l) + h) * PANEL, 32 * h, l, t0, bh);
+            bulk_commit();
+            // J and H (next) take the dv and dX staging tiles: their stores must have read them
+            // before the products' completion releases the epilogue
+            bulk_wait_read();
             mma_commit(smem_u32(&mbar[3]));
         }
         wait_all(3, 0);
@@ -1403,22 +1421,25 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
         mu = mk_;  // never read with L = 1
     }
     // the fp32 outputs the gradient kernel writes by TMA stores: 32-column boxes of one chunk
-    CUtensorMap mdq, mdk, mdu;
+    CUtensorMap mdq, mdk, mdu, mdv, mdx;
     {
         const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)s.T, (cuuint64_t)s.BH};
         const cuuint64_t str[2] = {(cuuint64_t)D * 4, (cuuint64_t)s.T * D * 4};
         const cuuint32_t box[3] = {32, 64, 1};
         if (!bt_encode(&mdq, a.dq, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
-            !bt_encode(&mdk, a.dk, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+            !bt_encode(&mdk, a.dk, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
+            !bt_encode(&mdv, a.dv, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
             return cudaErrorInvalidValue;
     }
     if (s.R > 0) {
         const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)s.R, (cuuint64_t)s.T, (cuuint64_t)s.BH};
         const cuuint64_t str[3] = {(cuuint64_t)D * 4, (cuuint64_t)s.R * D * 4, (cuuint64_t)s.T * s.R * D * 4};
         const cuuint32_t box[4] = {32, 1, 64, 1};
-        if (!bt_encode(&mdu, a.du, 4, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return cudaErrorInvalidValue;
+        if (!bt_encode(&mdu, a.du, 4, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
+            !bt_encode(&mdx, w.dX, 4, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+            return cudaErrorInvalidValue;
     } else {
-        mdu = mdq;  // never written with L = 1
+        mdu = mdx = mdq;  // never written with L = 1
     }
     Params p{};
     p.v = (const __nv_bfloat16 *)a.v;
@@ -1483,7 +1504,7 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     cfg.gridDim = dim3(nchunks);
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = gk::SMEM;
-    e = cudaLaunchKernelEx(&cfg, grad_kernel, mq, mk_, mu, mdq, mdk, mdu, p);
+    e = cudaLaunchKernelEx(&cfg, grad_kernel, mq, mk_, mu, mdq, mdk, mdu, mdv, mdx, p);
     tm.end();
     if (e != cudaSuccess) return e;
     return backward_token_local(s, PRISM_BF16, a, w.dX, w.dH, w.dWp, tm);
