@@ -355,18 +355,31 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t sr
                  : "memory");
 }
 
+// untiled bulk copy shared -> global (bulk-group completion); both addresses 16-byte aligned, bytes
+// a multiple of 16
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
 // =====================================================================================================
 // maps kernel: shared-memory panels (index x PANEL from a 1024-aligned base)
 namespace mk {
 enum {
     Q = 0, K = 1, U0 = 2, V = 5, ZERO = 6, X0 = 7, DO = 10, Z0 = 11, MKU0 = 12, PK = 15, TF = 16, W = 17, UP = 18,
     F = 19,  // solve region (A, T fp32 + scratch), then:
-    BE = 19, BGK = 20, Y = 21, CK = 22, NBGK = 23, NPANELS = 24
+    BE = 19, BGK = 20, Y = 21, CK = 22, NBGK = 23, NPANELS = 24,
+    // the fp32 maps staged for their TMA stores once the last products have read these tiles (none
+    // of them is the source of a stash copy): A_c, A_c^T, B_c, Bbar_c
+    MA = 12, MAT = 14, MB = 19, MBB = 21
 };
 // later tenants: colf U_l in MKU0 + l (after the E product), Gamma Q in PK (after the Y product)
 constexpr uint32_t SC_OFF = NPANELS * PANEL;
 constexpr uint32_t SMEM = SC_OFF + SC_FLOATS * 4 + 1024;
 static_assert(2 * 64 * tcu::LDA * 4 + tcu::SOLVE_SCRATCH * 4 <= 5 * PANEL, "solve region");
+static_assert(MA == MKU0 && MAT == MKU0 + 2 && MAT + 1 == PK && MB == BE && MBB == Y && MBB + 1 == CK,
+              "map staging over tiles the last products read");
 static_assert(SMEM <= 232448, "shared memory budget");
 // tensor memory columns (512)
 constexpr uint32_t TM_G1 = 0, TM_E = 256, TM_Y = 320, TM_WY = 384, TM_ZW = 0, TM_MAP = 128, TM_BAR = 192;
@@ -374,7 +387,9 @@ constexpr uint32_t TM_G1 = 0, TM_E = 256, TM_Y = 320, TM_WY = 384, TM_ZW = 0, TM
 
 __global__ void __launch_bounds__(NT, 1)
     maps_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_u, Params p)
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_u,
+                const __grid_constant__ CUtensorMap tm_ma, const __grid_constant__ CUtensorMap tm_mat,
+                const __grid_constant__ CUtensorMap tm_mb, const __grid_constant__ CUtensorMap tm_mbb, Params p)
 {
     using namespace mk;
     extern __shared__ uint8_t smem_raw[];
@@ -525,7 +540,6 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                     const uint32_t xv = pack_h2(x0, x1);
                     *reinterpret_cast<uint32_t *>(P(X0 + l) + sw128(i, 2 * cp)) = xv;
-                    *reinterpret_cast<uint32_t *>(stash + (ST_X + l) * PANEL + sw128(i, 2 * cp)) = xv;
                 }
             }
             fence_async_smem();
@@ -569,6 +583,8 @@ __global__ void __launch_bounds__(NT, 1)
             mma_k64(tmem + TM_Y, mn(dbase, PK * PANEL, PANEL), true, mn(dbase, DO * PANEL, PANEL), true,
                     idesc_f16(128, 64, 1, 1), false);
             mma_commit(smem_u32(&mbar[2]));
+            for (int l = 0; l < R; ++l) bulk_store(stash + (ST_X + l) * PANEL, sbase + (X0 + l) * PANEL, PANEL);
+            bulk_commit();
         }
         if (tid < tcu::SOLVE_THREADS) tcu::ut_solve(sA, sT32, sX, P(TF), tid, 1);
         fence_async_smem();
@@ -590,7 +606,7 @@ __global__ void __launch_bounds__(NT, 1)
                 ld_row_b(P(V), i, c0, v);
 #pragma unroll
                 for (int q = 0; q < CW; ++q) v[q] -= e[q];
-                st_row_h(stash + ST_E0 * PANEL, i, c0, v);
+                st_row_h(P(V), i, c0, v);  // E0 in place of the values (their last reader), for the stash
                 const float b = s_beta[i];
 #pragma unroll
                 for (int q = 0; q < CW; ++q) v[q] *= b;
@@ -634,6 +650,8 @@ __global__ void __launch_bounds__(NT, 1)
             mma_k64(tmem + TM_ZW, mn(dbase, TF * PANEL, PANEL), true, mn(dbase, Y * PANEL, PANEL), true,
                     idesc_f16(128, 128, 1, 1), false);
             mma_commit(smem_u32(&mbar[3]));
+            bulk_store(stash + ST_E0 * PANEL, sbase + V * PANEL, PANEL);
+            bulk_commit();
         }
         wait_all(3, 0);
         fence_after_sync();
@@ -642,15 +660,12 @@ __global__ void __launch_bounds__(NT, 1)
             float v[CW];
             tmem_ld(tmem + TM_WY + lane_off + (uint32_t)c0, v);
             st_row_h(P(UP), i, c0, v);
-            st_row_h(stash + ST_UP * PANEL, i, c0, v);
             tmem_ld(tmem + TM_WY + 64 + lane_off + (uint32_t)c0, v);
             st_row_h(P(W), i, c0, v);
-            st_row_h(stash + ST_W * PANEL, i, c0, v);
             tmem_ld(tmem + TM_ZW + lane_off + (uint32_t)c0, v);
             st_row_h(P(Z0), i, c0, v);
-            st_row_h(stash + ST_Z0 * PANEL, i, c0, v);
             tmem_ld(tmem + TM_ZW + 64 + lane_off + (uint32_t)c0, v);
-            st_row_h(stash + ST_WB * PANEL, i, c0, v);
+            st_row_h(P(TF), i, c0, v);  // Wbar, for the stash only, over T (read by the products above)
         }
         fence_async_smem();
         fence_before_sync();
@@ -669,26 +684,42 @@ __global__ void __launch_bounds__(NT, 1)
             mma_k64(tmem + TM_BAR, mn(dbase, ZERO * PANEL, (Z0 - ZERO) * PANEL), true, mn(dbase, NBGK * PANEL, PANEL),
                     true, id, true);
             mma_commit(smem_u32(&mbar[4]));
+            bulk_store(stash + ST_UP * PANEL, sbase + UP * PANEL, PANEL);
+            bulk_store(stash + ST_W * PANEL, sbase + W * PANEL, PANEL);
+            bulk_store(stash + ST_Z0 * PANEL, sbase + Z0 * PANEL, PANEL);
+            bulk_store(stash + ST_WB * PANEL, sbase + TF * PANEL, PANEL);
+            bulk_commit();
         }
         wait_all(4, 0);
         fence_after_sync();
         {
             const int n0 = CW * sub;
-            const size_t mo = (size_t)chunk * D * D;
             float v[CW];
             tmem_ld(tmem + TM_MAP + lane_off + (uint32_t)n0, v);
             if (row < 64) {  // A_c [m][n] = Gamma_63 [m == n] - (W^T colf K)[m][n], and its transpose
                 const float g63 = s_gam[63];
 #pragma unroll
                 for (int q = 0; q < CW; ++q) v[q] = (n0 + q == row ? g63 : 0.f) - v[q];
-                st_row_f(p.mapA + mo + (size_t)row * D + n0, v);
+                st_tile_f(P(MA), row, n0, v);
 #pragma unroll
-                for (int q = 0; q < CW; ++q) p.mapAT[mo + (size_t)(n0 + q) * D + row] = v[q];
+                for (int q = 0; q < CW; ++q) *reinterpret_cast<float *>(P(MAT) + tile_f_off(n0 + q, row)) = v[q];
             } else {
-                st_row_f(p.mapB + mo + (size_t)(row - 64) * D + n0, v);
+                st_tile_f(P(MB), row - 64, n0, v);
                 tmem_ld(tmem + TM_BAR + lane_off + (uint32_t)n0, v);
-                st_row_f(p.mapBb + mo + (size_t)(row - 64) * D + n0, v);
+                st_tile_f(P(MBB), row - 64, n0, v);
             }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            for (int h2 = 0; h2 < 2; ++h2) {
+                tma_store_2d(&tm_ma, sbase + (MA + h2) * PANEL, 32 * h2, chunk * 64);
+                tma_store_2d(&tm_mat, sbase + (MAT + h2) * PANEL, 32 * h2, chunk * 64);
+                tma_store_2d(&tm_mb, sbase + (MB + h2) * PANEL, 32 * h2, chunk * 64);
+                tma_store_2d(&tm_mbb, sbase + (MBB + h2) * PANEL, 32 * h2, chunk * 64);
+            }
+            bulk_commit();
         }
     } while (0);
 
@@ -700,6 +731,7 @@ __global__ void __launch_bounds__(NT, 1)
         mma_commit(mb_drain);
         (void)mbar_wait(mb_drain, 0, drain_ns);
     }
+    if (tid == 0) bulk_wait_read();  // the stash and map stores have read their tiles
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
@@ -1441,6 +1473,18 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     } else {
         mdu = mdx = mdq;  // never written with L = 1
     }
+    // the maps kernel's fp32 chunk maps, [chunks x 64][64]
+    CUtensorMap mma_, mmat, mmb, mmbb;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)s.BH * s.NC * 64};
+        const cuuint64_t str[1] = {(cuuint64_t)D * 4};
+        const cuuint32_t box[2] = {32, 64};
+        if (!bt_encode(&mma_, w.mapA, 2, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
+            !bt_encode(&mmat, w.mapAT, 2, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
+            !bt_encode(&mmb, w.mapB, 2, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
+            !bt_encode(&mmbb, w.mapBb, 2, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+            return cudaErrorInvalidValue;
+    }
     Params p{};
     p.v = (const __nv_bfloat16 *)a.v;
     p.conv_w = (const __nv_bfloat16 *)a.conv_w;
@@ -1487,7 +1531,7 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = mk::SMEM;
     cfg.numAttrs = 0;  // the previous kernel on the stream may be anything
-    e = cudaLaunchKernelEx(&cfg, maps_kernel, mq, mk_, mv, mu, p);
+    e = cudaLaunchKernelEx(&cfg, maps_kernel, mq, mk_, mv, mu, mma_, mmat, mmb, mmbb, p);
     tm.end();
     if (e != cudaSuccess) return e;
     cfg.numAttrs = 1;
