@@ -873,6 +873,9 @@ def backward_kernel_bytes(name, w, nl=False):
         + th * R * w.dk * 4 + th * 8,
         "bwd_chain_grad": v + th * 4 * R + eta_rw + pg + dX + 2 * per_row + per_row + th * 4 * R + eta_rw + dpg,
         "bwd_conv_grad": v + 3 * per_row + w.B * w.H * ntile * 4 * w.dv * 4,
+        # the fused tail (bf16, dv = 64): the chain's reads and dv once read and once written; dH stays on chip
+        "bwd_tail": v + th * 4 * R + eta_rw + pg + dX + 2 * per_row + th * 4 * R + eta_rw + dpg
+        + w.B * w.H * ntile * 4 * w.dv * 4,
         "bwd_conv_reduce": w.B * w.H * ntile * 4 * w.dv * 4 + w.H * 4 * w.dv * 4,
     }
     return table[name]

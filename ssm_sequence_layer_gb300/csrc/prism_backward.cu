@@ -27,6 +27,8 @@
 //   dgamma_l = sum_c g r_l dx_l,   deta_l = -sum_c g r_l dr_{l+1}
 //   dv_t += dr_1,   dh_t = -g dr_1 + phi(h) (2 - h^2) dg
 // then dv_{t-j} += w_j dh_t and dw_j += dh_t v_{t-j} over the window.
+#include <type_traits>
+
 #include "prism_internal.h"
 #include "tc_util.h"
 
@@ -653,6 +655,72 @@ __device__ __forceinline__ float2 ld2<__nv_bfloat16>(const __nv_bfloat16 *p)
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
 }
 
+// One channel of one token, linear chain: from the anchor a = h_t, v_t and the level cotangents
+// dx_l, the chain's share of dv (drn, the cotangent of r_1) and dh; dgam and det gather the
+// channel's terms of dgamma and deta.
+template <int RM>
+__device__ __forceinline__ void chain_lin_channel(float a, float v0, const float (&gm)[RM], const float (&et)[RM],
+                                                  const float (&dx)[RM], int R, float (&dgam)[RM], float (&det)[RM],
+                                                  float &drn_out, float &dh_out)
+{
+    float Phi, phi;
+    tcu::gauss_parts(a, Phi, phi);
+    const float g = fmaf(a, phi, Phi);
+    float rl[RM];
+    float r = v0 - a * Phi;
+#pragma unroll
+    for (int l = 0; l < RM; ++l)
+        if (l < R) {
+            rl[l] = r;
+            r *= 1.f - et[l] * g;
+        }
+    float drn = 0.f, dg = 0.f;
+#pragma unroll
+    for (int l = RM - 1; l >= 0; --l)
+        if (l < R) {
+            dgam[l] = fmaf(g * rl[l], dx[l], dgam[l]);
+            det[l] = fmaf(-g * rl[l], drn, det[l]);
+            dg += gm[l] * rl[l] * dx[l] - et[l] * rl[l] * drn;
+            drn = gm[l] * g * dx[l] + (1.f - et[l] * g) * drn;
+        }
+    drn_out = drn;
+    dh_out = -g * drn + phi * (2.f - a * a) * dg;
+}
+
+// The same for the non-linear chain (gains pl in place of eta): dp receives the gains' cotangents.
+template <int RM>
+__device__ __forceinline__ void chain_nl_channel(float a, float v0, const float (&gm)[RM], const float (&pl)[RM],
+                                                 const float (&dx)[RM], int R, float (&dgam)[RM], float (&dp)[RM],
+                                                 float &drn_out, float &dh_out)
+{
+    float Phi, phi;
+    tcu::gauss_parts(a, Phi, phi);
+    const float g = fmaf(a, phi, Phi);
+    float rl[RM];  // r_l, kept from the forward steps
+    float r = v0 - a * Phi;
+#pragma unroll
+    for (int l = 0; l < RM; ++l)
+        if (l < R) {
+            rl[l] = r;
+            r -= tcu::gelu_value(pl[l] * r);
+        }
+    float drn = 0.f;
+#pragma unroll
+    for (int l = RM - 1; l >= 0; --l)
+        if (l < R) {
+            const float z = pl[l] * rl[l];
+            float Pz, pz;
+            tcu::gauss_parts(z, Pz, pz);
+            const float ddelta = gm[l] * dx[l] - drn;
+            dgam[l] = fmaf(z * Pz, dx[l], dgam[l]);
+            const float dz = ddelta * fmaf(z, pz, Pz);
+            dp[l] = dz * rl[l];
+            drn = fmaf(dz, pl[l], drn);
+        }
+    drn_out = drn;
+    dh_out = -g * drn;
+}
+
 template <typename io_t, int CPL, int RM>
 __global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__ v, const io_t *__restrict__ v_hist,
                                                         const io_t *__restrict__ conv_w,
@@ -702,29 +770,10 @@ __global__ void __launch_bounds__(NT) chain_grad_kernel(const io_t *__restrict__
             float a = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) a = fmaf(e ? w[k][j].y : w[k][j].x, e ? vv[k][j].y : vv[k][j].x, a);
-            float Phi, phi;
-            tcu::gauss_parts(a, Phi, phi);
-            const float g = fmaf(a, phi, Phi);
-            float rl[RM];
-            float r = (e ? vv[k][0].y : vv[k][0].x) - a * Phi;
+            float dx[RM];
 #pragma unroll
-            for (int l = 0; l < RM; ++l)
-                if (l < R) {
-                    rl[l] = r;
-                    r *= 1.f - et[l] * g;
-                }
-            float drn = 0.f, dg = 0.f;
-#pragma unroll
-            for (int l = RM - 1; l >= 0; --l)
-                if (l < R) {
-                    const float dx = e ? dxv[k][l].y : dxv[k][l].x;
-                    dgam[l] = fmaf(g * rl[l], dx, dgam[l]);
-                    det[l] = fmaf(-g * rl[l], drn, det[l]);
-                    dg += gm[l] * rl[l] * dx - et[l] * rl[l] * drn;
-                    drn = gm[l] * g * dx + (1.f - et[l] * g) * drn;
-                }
-            drn2[e] = drn;
-            dh2[e] = -g * drn + phi * (2.f - a * a) * dg;
+            for (int l = 0; l < RM; ++l) dx[l] = e ? dxv[k][l].y : dxv[k][l].x;
+            chain_lin_channel<RM>(a, e ? vv[k][0].y : vv[k][0].x, gm, et, dx, R, dgam, det, drn2[e], dh2[e]);
         }
         *reinterpret_cast<float2 *>(dv_out + (size_t)tok * dv + c) = make_float2(dvo[k].x + drn2[0], dvo[k].y + drn2[1]);
         *reinterpret_cast<float2 *>(dH + (size_t)tok * dv + c) = make_float2(dh2[0], dh2[1]);
@@ -794,33 +843,15 @@ __global__ void __launch_bounds__(NT) chain_grad_nl_kernel(const io_t *__restric
             float a = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) a = fmaf(e ? w[k][j].y : w[k][j].x, e ? vv[k][j].y : vv[k][j].x, a);
-            float Phi, phi;
-            tcu::gauss_parts(a, Phi, phi);
-            const float g = fmaf(a, phi, Phi);
-            float rl[RM];  // r_l, kept from the forward steps
-            float r = (e ? vv[k][0].y : vv[k][0].x) - a * Phi;
+            float dx[RM], pl[RM], dp[RM];
 #pragma unroll
-            for (int l = 0; l < RM; ++l)
-                if (l < R) {
-                    rl[l] = r;
-                    r -= tcu::gelu_value((e ? pv[k][l].y : pv[k][l].x) * r);
-                }
-            float drn = 0.f;
+            for (int l = 0; l < RM; ++l) {
+                dx[l] = e ? dxv[k][l].y : dxv[k][l].x;
+                pl[l] = e ? pv[k][l].y : pv[k][l].x;
+            }
+            chain_nl_channel<RM>(a, e ? vv[k][0].y : vv[k][0].x, gm, pl, dx, R, dgam, dp, drn2[e], dh2[e]);
 #pragma unroll
-            for (int l = RM - 1; l >= 0; --l)
-                if (l < R) {
-                    const float pl = e ? pv[k][l].y : pv[k][l].x, dx = e ? dxv[k][l].y : dxv[k][l].x;
-                    const float z = pl * rl[l];
-                    float Pz, pz;
-                    tcu::gauss_parts(z, Pz, pz);
-                    const float ddelta = gm[l] * dx - drn;
-                    dgam[l] = fmaf(z * Pz, dx, dgam[l]);
-                    const float dz = ddelta * fmaf(z, pz, Pz);
-                    dp2[l][e] = dz * rl[l];
-                    drn = fmaf(dz, pl, drn);
-                }
-            drn2[e] = drn;
-            dh2[e] = -g * drn;
+            for (int l = 0; l < RM; ++l) dp2[l][e] = dp[l];
         }
         *reinterpret_cast<float2 *>(dv_out + (size_t)tok * dv + c) = make_float2(dvo[k].x + drn2[0], dvo[k].y + drn2[1]);
         *reinterpret_cast<float2 *>(dH + (size_t)tok * dv + c) = make_float2(dh2[0], dh2[1]);
@@ -901,6 +932,157 @@ __global__ void __launch_bounds__(512) conv_grad_kernel(const io_t *__restrict__
     }
 }
 
+// The token-local tail in one pass for bf16 io and dv = 64: a block takes a tile of CT tokens.
+// Its eight warps run the chain and gain backwards (as chain_grad_kernel / chain_grad_nl_kernel,
+// lane c the channel pair 2c, 2c + 1) for the tile's tokens and the three after it, whose dH the
+// transposed convolution needs; dH, the chain's share of dv and the tile's v stay in shared memory.
+// Then thread (c, sub) takes channel c of sub-tile sub (CSUB tokens) through the convolution
+// backwards as conv_grad_kernel does, in the same order of operations, and writes dv once.
+constexpr int TAIL_NT = 256;
+template <int RM, bool NL>
+__global__ void __launch_bounds__(TAIL_NT) tail_kernel(const __nv_bfloat16 *__restrict__ v,
+                                                       const __nv_bfloat16 *__restrict__ v_hist,
+                                                       const __nv_bfloat16 *__restrict__ conv_w,
+                                                       const float *__restrict__ gamma, const float *__restrict__ eta,
+                                                       const __nv_bfloat16 *__restrict__ p_gain,
+                                                       const float *__restrict__ dX, float *__restrict__ dv_out,
+                                                       float *__restrict__ dgamma, float *__restrict__ deta,
+                                                       float *__restrict__ dp_gain, float *__restrict__ dv_hist,
+                                                       float *__restrict__ dWp, int H, int T, int R, int ntile)
+{
+    constexpr int D = 64, NTOK = CT + 3;
+    static_assert(TAIL_NT == D * (CT / CSUB), "one thread per channel and sub-tile");
+    __shared__ float dHs[NTOK][D];             // dH of tokens t0 .. t0 + CT + 2 (0 past the end)
+    __shared__ float dvs[CT][D];               // dv with the chain's share
+    __shared__ __nv_bfloat16 vs[CT + 3][D];    // v of tokens t0 - 3 .. t0 + CT - 1 (history or 0 before)
+    __shared__ float part[CT / CSUB][4][D];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, tile = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int t0 = tile * CT;
+    const size_t base = (size_t)bh * T;
+    auto vpair = [&](int t, int c) -> __nv_bfloat162 {  // v_t, channels c, c + 1 (history before 0)
+        if (t >= 0) return *reinterpret_cast<const __nv_bfloat162 *>(v + (base + t) * D + c);
+        if (v_hist) return *reinterpret_cast<const __nv_bfloat162 *>(v_hist + ((size_t)bh * 3 + 3 + t) * D + c);
+        return __floats2bfloat162_rn(0.f, 0.f);
+    };
+    {
+        const int c = 2 * lane;
+        float2 w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = ld2(conv_w + ((size_t)h * 4 + j) * D + c);
+        if (warp == 0) {
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {  // the three tokens before the tile
+                const int t = t0 - 3 + j;
+                *reinterpret_cast<__nv_bfloat162 *>(&vs[j][c]) = t < T ? vpair(t, c) : __floats2bfloat162_rn(0.f, 0.f);
+            }
+        }
+#pragma unroll 2
+        for (int tau = warp; tau < NTOK; tau += TAIL_NT / 32) {
+            const int t = t0 + tau;
+            float2 dh = make_float2(0.f, 0.f);
+            if (t < T) {
+                const size_t tok = base + t;
+                float gm[RM], et[RM];
+                float2 vv[4], dxv[RM], pv[RM], dvo = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int l = 0; l < RM; ++l) {
+                    gm[l] = l < R ? gamma[tok * R + l] : 0.f;
+                    et[l] = (!NL && l + 1 < R) ? eta[tok * R + l] : 0.f;
+                    dxv[l] = l < R ? *reinterpret_cast<const float2 *>(dX + (tok * R + l) * D + c) : make_float2(0.f, 0.f);
+                    pv[l] = (NL && l < R) ? ld2(p_gain + (tok * R + l) * D + c) : make_float2(0.f, 0.f);
+                }
+                __nv_bfloat162 v0 = vpair(t, c);
+                vv[0] = __bfloat1622float2(v0);
+#pragma unroll
+                for (int j = 1; j < 4; ++j) vv[j] = __bfloat1622float2(vpair(t - j, c));
+                if (tau < CT) dvo = *reinterpret_cast<const float2 *>(dv_out + tok * D + c);
+                float dgam[RM], det[RM], drn2[2], dh2[2], dp2[RM][2];
+#pragma unroll
+                for (int l = 0; l < RM; ++l) dgam[l] = det[l] = 0.f;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a = fmaf(e ? w[j].y : w[j].x, e ? vv[j].y : vv[j].x, a);
+                    float dx[RM];
+#pragma unroll
+                    for (int l = 0; l < RM; ++l) dx[l] = e ? dxv[l].y : dxv[l].x;
+                    if constexpr (NL) {
+                        float pl[RM], dp[RM];
+#pragma unroll
+                        for (int l = 0; l < RM; ++l) pl[l] = e ? pv[l].y : pv[l].x;
+                        chain_nl_channel<RM>(a, e ? vv[0].y : vv[0].x, gm, pl, dx, R, dgam, dp, drn2[e], dh2[e]);
+#pragma unroll
+                        for (int l = 0; l < RM; ++l) dp2[l][e] = dp[l];
+                    } else {
+                        chain_lin_channel<RM>(a, e ? vv[0].y : vv[0].x, gm, et, dx, R, dgam, det, drn2[e], dh2[e]);
+                    }
+                }
+                dh = make_float2(dh2[0], dh2[1]);
+                if (tau < CT) {  // the tile's own tokens: dv's chain share, the gains' cotangents
+                    *reinterpret_cast<float2 *>(&dvs[tau][c]) = make_float2(dvo.x + drn2[0], dvo.y + drn2[1]);
+                    *reinterpret_cast<__nv_bfloat162 *>(&vs[tau + 3][c]) = v0;
+                    if constexpr (NL) {
+#pragma unroll
+                        for (int l = 0; l < RM; ++l)
+                            if (l < R)
+                                *reinterpret_cast<float2 *>(dp_gain + (tok * R + l) * D + c) = make_float2(dp2[l][0], dp2[l][1]);
+                    }
+#pragma unroll
+                    for (int l = 0; l < RM; ++l)
+                        if (l < R) {
+                            const float s1 = warp_sum(dgam[l]);
+                            if (lane == 0) dgamma[tok * R + l] = s1;
+                            if constexpr (!NL) {
+                                const float s2 = warp_sum(det[l]);
+                                if (lane == 0) deta[tok * R + l] = s2;
+                            }
+                        }
+                }
+            } else if (tau < CT) {
+                *reinterpret_cast<__nv_bfloat162 *>(&vs[tau + 3][c]) = __floats2bfloat162_rn(0.f, 0.f);
+            }
+            *reinterpret_cast<float2 *>(&dHs[tau][c]) = dh;
+        }
+    }
+    __syncthreads();
+    // the convolution backwards: thread (c, sub), tokens t0 + CSUB sub ..
+    const int c = tid % D, sub = tid / D, i0 = sub * CSUB;
+    float w[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = __bfloat162float(conv_w[((size_t)h * 4 + j) * D + c]);
+#pragma unroll
+    for (int i = 0; i < CSUB; ++i) {
+        const int tau = i0 + i;
+        if (t0 + tau >= T) break;
+        // token t: dv_t += sum_j w_j dH_{t+j};  dw_j += dH_t v_{t-j}
+        const float s = fmaf(w[0], dHs[tau][c], fmaf(w[1], dHs[tau + 1][c], fmaf(w[2], dHs[tau + 2][c], w[3] * dHs[tau + 3][c])));
+        dv_out[(base + t0 + tau) * D + c] = dvs[tau][c] + s;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j] = fmaf(dHs[tau][c], __bfloat162float(vs[tau + 3 - j][c]), acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) part[sub][j][c] = acc[j];
+    __syncthreads();
+    if (sub == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float sum = part[0][j][c];
+#pragma unroll
+            for (int q = 1; q < CT / CSUB; ++q) sum += part[q][j][c];
+            dWp[(((size_t)bh * ntile + tile) * 4 + j) * D + c] = sum;
+        }
+        if (tile == 0 && dv_hist) {
+            // slot s holds v_{s-3}, which enters h_t through tap j = t - s + 3 for t in [0, s]
+            for (int s = 0; s < 3; ++s) {
+                float g = 0.f;
+                for (int t = 0; t <= s && t < T; ++t) g = fmaf(w[t - s + 3], dHs[t][c], g);
+                dv_hist[((size_t)bh * 3 + s) * D + c] = g;
+            }
+        }
+    }
+}
+
 // dconv_w[h][j][c] = sum over the batch and the tiles of dWp: a block takes 32 consecutive
 // (h, j, c) outputs; its 32 warps take the (b, tile) terms e = warp, warp + 32, ... (lane =
 // output), and the 32 partial sums meet in shared memory in a fixed order.
@@ -963,6 +1145,27 @@ cudaError_t token_local(const Shape &s, const BackwardArgs &a, float *dX, float 
     const long long ntok = (long long)s.BH * s.T;
     const int ntile = (s.T + CT - 1) / CT;
     const long long cg_grid = (ntok + NT / 32 - 1) / (NT / 32);  // one warp per token
+    if constexpr (std::is_same<io_t, __nv_bfloat16>::value) {
+        if (s.dv == 64) {  // the fused tail: dH and the chain's share of dv stay on chip
+            tm.begin("bwd_tail");
+            const dim3 grid((unsigned)ntile, (unsigned)s.BH);
+            if (a.p_gain) {
+                auto kern = s.R <= 3 ? tail_kernel<3, true> : tail_kernel<RMAX, true>;
+                kern<<<grid, TAIL_NT, 0, st>>>(v, vh, cw, a.gamma, nullptr, static_cast<const io_t *>(a.p_gain), dX,
+                                               a.dv, a.dgamma, nullptr, a.dp_gain, a.dv_hist, dWp, s.H, s.T, s.R,
+                                               ntile);
+            } else {
+                auto kern = s.R <= 3 ? tail_kernel<3, false> : tail_kernel<RMAX, false>;
+                kern<<<grid, TAIL_NT, 0, st>>>(v, vh, cw, a.gamma, a.eta, nullptr, dX, a.dv, a.dgamma, a.deta,
+                                               nullptr, a.dv_hist, dWp, s.H, s.T, s.R, ntile);
+            }
+            tm.end();
+            tm.begin("bwd_conv_reduce");
+            conv_reduce_kernel<<<(s.H * 4 * s.dv + 31) / 32, 1024, 0, st>>>(dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
+            tm.end();
+            return cudaGetLastError();
+        }
+    }
     tm.begin("bwd_chain_grad");
     // the level arrays sized for L <= 4 or for the largest L (registers)
     if (a.p_gain) {
