@@ -753,6 +753,12 @@ constexpr int SC_OUTS = SC_ROWS * D / SCAN_NT;  // outputs a thread forms in the
 static_assert(SC_OUTS >= 1 && SC_OUTS <= 4, "scan layout");
 constexpr int SC_STAGE_FLOATS = D * D + SC_ROWS * D;
 constexpr size_t SCAN_SMEM = (size_t)(SC_STAGES * SC_STAGE_FLOATS + SC_ROWS * D + 4 * SC_ROWS * D) * 4 + 128;
+// The shared memory the scan's launch requests: more than the scan uses, so that at most two of its
+// blocks fit an SM.  Launched while the maps kernel drains (programmatic dependent launch), the
+// blocks are placed on SMs as they free up; with room for three, the first SMs freed took three
+// and the steps of their chains ran slower (0.78 against 0.72 ms per backward pass at 16K tokens).
+constexpr size_t SCAN_SMEM_LAUNCH = 100 * 1024;
+static_assert(SCAN_SMEM <= SCAN_SMEM_LAUNCH && 3 * (SCAN_SMEM_LAUNCH + 1024) > 228 * 1024, "two scan blocks per SM");
 static_assert(SC_OUTS * SCAN_NT == SC_ROWS * D && SCAN_NT % 64 == 0, "the consumers' roles");
 
 __global__ void __launch_bounds__(SCAN_NT + 32) scan_kernel(const float *__restrict__ mapA, const float *__restrict__ mapAT,
@@ -1422,7 +1428,7 @@ cudaError_t backward_tc_prepare()
     if ((e = cudaFuncSetAttribute(bt::maps_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bt::mk::SMEM)) !=
         cudaSuccess)
         return e;
-    if ((e = cudaFuncSetAttribute(bt::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bt::SCAN_SMEM)) !=
+    if ((e = cudaFuncSetAttribute(bt::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bt::SCAN_SMEM_LAUNCH)) !=
         cudaSuccess)
         return e;
     return cudaFuncSetAttribute(bt::grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bt::gk::SMEM);
@@ -1538,7 +1544,7 @@ cudaError_t backward_tc(const Shape &s, const BackwardArgs &a, void *ws, int *d_
     tm.begin("bwd_chunk_scan");
     cfg.gridDim = dim3(D / SC_ROWS, s.BH, 2);
     cfg.blockDim = dim3(SCAN_NT + 32);
-    cfg.dynamicSmemBytes = SCAN_SMEM;
+    cfg.dynamicSmemBytes = SCAN_SMEM_LAUNCH;
     e = cudaLaunchKernelEx(&cfg, scan_kernel, (const float *)w.mapA, (const float *)w.mapAT, (const float *)w.mapB,
                            (const float *)w.mapBb, a.S_init, a.dS_final, w.Sst, w.Gst, a.dS_init, s.NC, d_status,
                            p.wait_ns);

@@ -1154,6 +1154,11 @@ constexpr int CB_KQ = 4;                       // parts of the sum index
 constexpr int CB_THREADS = CB_KQ * 2 * 32;     // x 2 row groups x 32 column pairs
 constexpr int CB_STAGE_FLOATS = 64 * 64 + CB_ROWS * 64;
 constexpr size_t CB_SMEM = (size_t)CB_STAGES * CB_STAGE_FLOATS * 4 + 128;
+// The launch requests more shared memory than the combine uses, so that one of its blocks fits an
+// SM: launched while the segment kernel drains, its blocks are placed on SMs as they free up, and
+// packed three to an SM their chains ran slower (0.165 against 0.160 ms per forward at 16K tokens).
+constexpr size_t CB_SMEM_LAUNCH = 120 * 1024;
+static_assert(CB_SMEM <= CB_SMEM_LAUNCH && 2 * (CB_SMEM_LAUNCH + 1024) > 228 * 1024, "one combine block per SM");
 
 __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__restrict__ zsum, __half *__restrict__ sstart,
                                                              int P, const float *S_init, float *S_final, int *status,
@@ -1520,7 +1525,7 @@ cudaError_t tc_prepare()
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(tc::fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::FX_SMEM);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(tc::combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::CB_SMEM);
+    return cudaFuncSetAttribute(tc::combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::CB_SMEM_LAUNCH);
 }
 
 cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const TcWorkspace &w, int *d_status,
@@ -1588,7 +1593,7 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
         tm.begin("tc_combine");
         cfg.gridDim = dim3(s.BH, 64 / CB_ROWS);
         cfg.blockDim = dim3(CB_THREADS);
-        cfg.dynamicSmemBytes = CB_SMEM;
+        cfg.dynamicSmemBytes = CB_SMEM_LAUNCH;
         e = cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)w.zsum, w.sstart, (int)w.P, a.S_init, a.S_final,
                                d_status, (unsigned long long)p.wait_ns);
         tm.end();
