@@ -1140,18 +1140,20 @@ __global__ void __launch_bounds__(NT, 1)
 
 // ---------------------------------------------------------------------------------------------
 // combine: S_start[p] = S_start[p-1] M_{p-1} + N_{p-1} in fp32 from S_start[0] = S_init (or 0),
-// 8 value rows per block, written out as fp16 (the fix-up's MMA operand); with S_final the map of
-// the last segment is applied too and the result written out in fp32.  The maps stream through a ring of CB_STAGES
-// shared-memory stages filled by bulk copies (16 KB of M and this block's 2 KB of N per
-// segment), so the serial chain never waits on global memory latency.  Each step's 8x64x64
-// product is split over the sum index: thread (kq, rg, lane) accumulates rows 4 rg .. 4 rg + 3,
-// columns 2 lane, 2 lane + 1 over m in [16 kq, 16 kq + 16); the four partial sums meet in shared
-// memory.  The running rows are double-buffered, so two barriers per segment order the row
-// exchange, the partial sums and the reuse of a ring stage.
-constexpr int CB_ROWS = 8;
+// 4 value rows per block (16 blocks a sequence: a short product per step, one block per SM), written
+// out as fp16 (the fix-up's MMA operand); with S_final the map of the last segment is applied too
+// and the result written out in fp32.  The maps stream through a ring of CB_STAGES shared-memory
+// stages filled by bulk copies (16 KB of M and this block's 1 KB of N per segment), so the serial
+// chain never waits on global memory latency.  Each step's 4x64x64 product is split over the sum
+// index: thread (kq, rg, lane) accumulates rows 2 rg, 2 rg + 1, columns 2 lane, 2 lane + 1 over m
+// in [16 kq, 16 kq + 16); the four partial sums meet in shared memory, thread (row, column) adding
+// them.  The running rows are double-buffered, so two barriers per segment order the row exchange,
+// the partial sums and the reuse of a ring stage.
+constexpr int CB_ROWS = 4;
 constexpr int CB_STAGES = 4;
 constexpr int CB_KQ = 4;                       // parts of the sum index
-constexpr int CB_THREADS = CB_KQ * 2 * 32;     // x 2 row groups x 32 column pairs
+constexpr int CB_THREADS = CB_KQ * 2 * 32;     // x 2 row groups (2 rows each) x 32 column pairs
+static_assert(CB_THREADS == CB_ROWS * 64, "one output of the step per thread in the reduction");
 constexpr int CB_STAGE_FLOATS = 64 * 64 + CB_ROWS * 64;
 constexpr size_t CB_SMEM = (size_t)CB_STAGES * CB_STAGE_FLOATS * 4 + 128;
 // The launch requests more shared memory than the combine uses, so that one of its blocks fits an
@@ -1171,15 +1173,14 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
     __shared__ int abort_s;
     const int bh = blockIdx.x, r0 = blockIdx.y * CB_ROWS, tid = threadIdx.x;
     const int kq = tid >> 6, rg = (tid >> 5) & 1, l = tid & 31, c2 = 2 * l;
-    const int rr = tid >> 5;  // the row this thread reduces (columns c2, c2 + 1)
+    const int rr = tid >> 6, cc = tid & 63;  // the entry this thread reduces
     prism::tc::grid_dependency_wait();  // the segment maps of the segment kernel
     prism::tc::allow_dependent_launch();
-    // S_init and S_final may be one buffer: each thread reads its two entries here and writes the
-    // same two at the end
-    const float2 s0 = S_init ? *reinterpret_cast<const float2 *>(S_init + ((size_t)bh * 64 + r0 + rr) * 64 + c2)
-                             : make_float2(0.f, 0.f);
-    *reinterpret_cast<__half2 *>(sstart + ((size_t)bh * P * 64 + r0 + rr) * 64 + c2) = __floats2half2_rn(s0.x, s0.y);
-    *reinterpret_cast<float2 *>(&S[0][rr][c2]) = s0;
+    // S_init and S_final may be one buffer: each thread reads its entry here and writes the same
+    // one at the end
+    const float s0 = S_init ? S_init[((size_t)bh * 64 + r0 + rr) * 64 + cc] : 0.f;
+    sstart[((size_t)bh * P * 64 + r0 + rr) * 64 + cc] = __float2half_rn(s0);
+    S[0][rr][cc] = s0;
     const int nmaps = S_final ? P : P - 1;  // maps of segments 0..P-2 (and P-1 for S_final)
     if (nmaps == 0) return;
     auto issue = [&](int sp) {
@@ -1226,17 +1227,20 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
 #ifdef PRISM_PHASE_TIMERS
         const long long tc0 = clock64();
 #endif
-        float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        constexpr int RPT = CB_ROWS / 2;  // rows of a thread's partial sums
+        float acc[RPT][2];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) acc[r][0] = acc[r][1] = 0.f;
 #pragma unroll
         for (int m = 16 * kq; m < 16 * kq + 16; m += 4) {
-            float4 sv[4];
+            float4 sv[RPT];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) sv[r] = *reinterpret_cast<const float4 *>(&S[buf][4 * rg + r][m]);
+            for (int r = 0; r < RPT; ++r) sv[r] = *reinterpret_cast<const float4 *>(&S[buf][RPT * rg + r][m]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float2 mv = *reinterpret_cast<const float2 *>(M + (m + q) * 64 + c2);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
+                for (int r = 0; r < RPT; ++r) {
                     const float sq = q == 0 ? sv[r].x : q == 1 ? sv[r].y : q == 2 ? sv[r].z : sv[r].w;
                     acc[r][0] = fmaf(sq, mv.x, acc[r][0]);
                     acc[r][1] = fmaf(sq, mv.y, acc[r][1]);
@@ -1244,8 +1248,8 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
             }
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-            *reinterpret_cast<float2 *>(&part[kq][4 * rg + r][c2]) = make_float2(acc[r][0], acc[r][1]);
+        for (int r = 0; r < RPT; ++r)
+            *reinterpret_cast<float2 *>(&part[kq][RPT * rg + r][c2]) = make_float2(acc[r][0], acc[r][1]);
 #ifdef PRISM_PHASE_TIMERS
         const long long tc1 = clock64();
 #endif
@@ -1256,19 +1260,14 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const float *__rest
             t_barb += clock64() - tc1;
         }
 #endif
-        float2 o = *reinterpret_cast<const float2 *>(M + 64 * 64 + rr * 64 + c2);  // N_p
+        float o = M[64 * 64 + rr * 64 + cc];  // N_p
 #pragma unroll
-        for (int q = 0; q < CB_KQ; ++q) {
-            const float2 v = *reinterpret_cast<const float2 *>(&part[q][rr][c2]);
-            o.x += v.x;
-            o.y += v.y;
-        }
-        *reinterpret_cast<float2 *>(&S[buf ^ 1][rr][c2]) = o;
+        for (int q = 0; q < CB_KQ; ++q) o += part[q][rr][cc];
+        S[buf ^ 1][rr][cc] = o;
         if (k + 1 < P)
-            *reinterpret_cast<__half2 *>(sstart + (((size_t)bh * P + k + 1) * 64 + r0 + rr) * 64 + c2) =
-                __floats2half2_rn(o.x, o.y);
+            sstart[(((size_t)bh * P + k + 1) * 64 + r0 + rr) * 64 + cc] = __float2half_rn(o);
         else  // k + 1 == P: the state after the last token (S_final was asked for)
-            *reinterpret_cast<float2 *>(S_final + ((size_t)bh * 64 + r0 + rr) * 64 + c2) = o;
+            S_final[((size_t)bh * 64 + r0 + rr) * 64 + cc] = o;
     }
 #ifdef PRISM_PHASE_TIMERS
     if (trace) {  // combine tracing: block (0, 0), thread 0: map waits and the whole chain
