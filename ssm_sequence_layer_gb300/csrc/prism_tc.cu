@@ -1295,7 +1295,8 @@ constexpr uint32_t FX_PANEL = 8192;
 constexpr uint32_t FX_OFF_S = 0;                      // S_start [64][64] fp16
 constexpr uint32_t FX_OFF_Q = FX_PANEL;               // [Qhat_c; Qhat_{c+1}] [128][64] fp16
 constexpr uint32_t FX_OFF_OUT = FX_OFF_Q + 2 * FX_PANEL;  // output tile [128][64] bf16
-constexpr uint32_t FX_SMEM = FX_OFF_OUT + 2 * FX_PANEL + 1024;
+constexpr uint32_t FX_OFF_O0 = FX_OFF_OUT + 2 * FX_PANEL;  // [o0_c; o0_{c+1}] [128][64] fp16 (bf16 output)
+constexpr uint32_t FX_SMEM = FX_OFF_O0 + 2 * FX_PANEL + 1024;
 
 struct FixParams {
     const void *stash_o;  // [BH][NC][64][64] o0 (fp16, or fp32 with out_f32)
@@ -1307,7 +1308,7 @@ struct FixParams {
 
 __global__ void __launch_bounds__(FX_THREADS)
     fixup_kernel(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_qh,
-                 const __grid_constant__ CUtensorMap tm_out, FixParams p)
+                 const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_o0, FixParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1342,15 +1343,16 @@ __global__ void __launch_bounds__(FX_THREADS)
     const size_t ch0 = (size_t)bh * p.NC;
     bool loads_pending = false;
     if (tid == 0) {
-        mbar_expect_tx(mb_t, 3 * FX_PANEL);
+        mbar_expect_tx(mb_t, (p.out_f32 ? 3 : 5) * FX_PANEL);
         tma_load_2d(sbase + FX_OFF_S, &tm_s, mb_t, 0, (int)(((size_t)bh * p.P + seg) * 64));
         tma_load_2d(sbase + FX_OFF_Q, &tm_qh, mb_t, 0, (int)((ch0 + c0) * 64));
+        if (!p.out_f32) tma_load_2d(sbase + FX_OFF_O0, &tm_o0, mb_t, 0, (int)((ch0 + c0) * 64));
         loads_pending = true;
     }
     // o0 of this thread's row while the tiles load
     const int r = tid, chunk = c0 + (r >> 6), i = r & 63;
     const bool valid = chunk < c_end && chunk * 64 + i < p.T;
-    float o[64];
+    float o[64];  // an fp32 o0 row (fp32 output); the fp16 one comes with the tiles
     if (valid) {
         const size_t base = ((ch0 + chunk) * 64 + i) * 64;
         if (p.out_f32) {
@@ -1362,19 +1364,6 @@ __global__ void __launch_bounds__(FX_THREADS)
                 o[4 * e + 1] = v.y;
                 o[4 * e + 2] = v.z;
                 o[4 * e + 3] = v.w;
-            }
-        } else {
-            const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __half *>(p.stash_o) + base);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint4 w = src[e];
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[h2]));
-                    o[8 * e + 2 * h2] = f.x;
-                    o[8 * e + 2 * h2 + 1] = f.y;
-                }
             }
         }
     }
@@ -1405,8 +1394,22 @@ __global__ void __launch_bounds__(FX_THREADS)
             float v[32];
             tmem_ld(tmem + lane_off + (uint32_t)(32 * g), v);
             if (!valid) continue;
+            if (p.out_f32) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] += o[32 * g + q];
+                for (int q = 0; q < 32; ++q) v[q] += o[32 * g + q];
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {  // o0 row r of the staged pair, 8 columns a 16-byte granule
+                    const uint4 w = *reinterpret_cast<const uint4 *>(sm + FX_OFF_O0 + sw128(r, 32 * g + 8 * q));
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int h2 = 0; h2 < 4; ++h2) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[h2]));
+                        v[8 * q + 2 * h2] += f.x;
+                        v[8 * q + 2 * h2 + 1] += f.y;
+                    }
+                }
+            }
             if (p.out_f32) {
                 float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) +
                                                          ((size_t)bh * p.T + (size_t)chunk * 64 + i) * 64 + 32 * g);
@@ -1436,7 +1439,7 @@ __global__ void __launch_bounds__(FX_THREADS)
             if (c0 + 1 < c_end) tma_store_3d(&tm_out, sbase + FX_OFF_OUT + FX_PANEL, 0, (c0 + 1) * 64, bh);
             bulk_commit();
         }
-        bulk_wait_all();
+        bulk_wait_read();  // the output tile has been read (its writes complete with the grid)
         if (abort_s) {  // drain after an expired wait
             if (loads_pending) (void)mbar_wait(mb_t, 0, 1000000000ull);
             const uint32_t mb_drain = smem_u32(&mbar[2]);
@@ -1600,7 +1603,7 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
     }
     if (w.P > 1 || a.S_init) {
         tm.begin("tc_fixup");
-        CUtensorMap ms, mqh, mo;
+        CUtensorMap ms, mqh, mo, mo0;
         {
             cuuint64_t str[1] = {(cuuint64_t)D * 2};
             cuuint64_t dS[2] = {(cuuint64_t)D, (cuuint64_t)s.BH * w.P * 64}, dQ[2] = {(cuuint64_t)D, (cuuint64_t)s.BH * s.NC * 64};
@@ -1609,8 +1612,10 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
                 !encode(&mqh, w.stash_q, 2, dQ, str, b128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
                 return cudaErrorInvalidValue;
             if (out_f32) {
-                mo = mqh;  // not read: an fp32 output is written directly
+                mo = mo0 = mqh;  // not read: an fp32 output is written directly, its o0 read by the threads
             } else {
+                if (!encode(&mo0, w.stash_o, 2, dQ, str, b128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
+                    return cudaErrorInvalidValue;
                 cuuint64_t dims[3] = {(cuuint64_t)D, T, BH};
                 cuuint64_t ostr[2] = {(cuuint64_t)D * 2, T * D * 2};
                 cuuint32_t box[3] = {64, 64, 1};
@@ -1631,7 +1636,7 @@ cudaError_t tc_forward(const Shape &s, const ForwardArgs &a, bool out_f32, const
         cfg.gridDim = dim3(s.BH * w.P, max_pairs);
         cfg.blockDim = dim3(FX_THREADS);
         cfg.dynamicSmemBytes = FX_SMEM;
-        e = cudaLaunchKernelEx(&cfg, fixup_kernel, ms, mqh, mo, fp);
+        e = cudaLaunchKernelEx(&cfg, fixup_kernel, ms, mqh, mo, mo0, fp);
         tm.end();
         if (e != cudaSuccess) return e;
     }
