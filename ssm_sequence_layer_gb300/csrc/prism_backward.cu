@@ -959,6 +959,9 @@ __global__ void __launch_bounds__(TAIL_NT) tail_kernel(const __nv_bfloat16 *__re
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, tile = blockIdx.x, bh = blockIdx.y, h = bh % H;
     const int t0 = tile * CT;
     const size_t base = (size_t)bh * T;
+    // dX and dv of the gradient kernel (launched behind it).  The weight reduction behind this kernel
+    // is not let in early: its 1024-thread blocks would hold half of an SM's threads while they wait.
+    prism::tc::grid_dependency_wait();
     auto vpair = [&](int t, int c) -> __nv_bfloat162 {  // v_t, channels c, c + 1 (history before 0)
         if (t >= 0) return *reinterpret_cast<const __nv_bfloat162 *>(v + (base + t) * D + c);
         if (v_hist) return *reinterpret_cast<const __nv_bfloat162 *>(v_hist + ((size_t)bh * 3 + 3 + t) * D + c);
@@ -1091,6 +1094,7 @@ __global__ void __launch_bounds__(1024) conv_reduce_kernel(const float *__restri
 {
     __shared__ float part[32][33];
     const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+    prism::tc::grid_dependency_wait();  // dWp (a no-op unless launched behind the kernel writing it)
     const int o = blockIdx.x * 32 + lane, nout = H * 4 * dv;
     float s = 0.f;
     if (o < nout) {
@@ -1147,22 +1151,37 @@ cudaError_t token_local(const Shape &s, const BackwardArgs &a, float *dX, float 
     const long long cg_grid = (ntok + NT / 32 - 1) / (NT / 32);  // one warp per token
     if constexpr (std::is_same<io_t, __nv_bfloat16>::value) {
         if (s.dv == 64) {  // the fused tail: dH and the chain's share of dv stay on chip
+            // launched behind the previous kernel (programmatic dependent launch): the blocks wait
+            // for it in griddepcontrol.wait before they read what it wrote
+            cudaLaunchAttribute pdl[1];
+            pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            pdl[0].val.programmaticStreamSerializationAllowed = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.stream = st;
+            cfg.attrs = pdl;
+            cfg.numAttrs = 1;
+            cfg.gridDim = dim3((unsigned)ntile, (unsigned)s.BH);
+            cfg.blockDim = dim3(TAIL_NT);
+            cudaError_t e;
             tm.begin("bwd_tail");
-            const dim3 grid((unsigned)ntile, (unsigned)s.BH);
             if (a.p_gain) {
                 auto kern = s.R <= 3 ? tail_kernel<3, true> : tail_kernel<RMAX, true>;
-                kern<<<grid, TAIL_NT, 0, st>>>(v, vh, cw, a.gamma, nullptr, static_cast<const io_t *>(a.p_gain), dX,
-                                               a.dv, a.dgamma, nullptr, a.dp_gain, a.dv_hist, dWp, s.H, s.T, s.R,
-                                               ntile);
+                e = cudaLaunchKernelEx(&cfg, kern, v, vh, cw, a.gamma, (const float *)nullptr,
+                                       static_cast<const io_t *>(a.p_gain), (const float *)dX, a.dv, a.dgamma,
+                                       (float *)nullptr, a.dp_gain, a.dv_hist, dWp, s.H, s.T, s.R, ntile);
             } else {
                 auto kern = s.R <= 3 ? tail_kernel<3, false> : tail_kernel<RMAX, false>;
-                kern<<<grid, TAIL_NT, 0, st>>>(v, vh, cw, a.gamma, a.eta, nullptr, dX, a.dv, a.dgamma, a.deta,
-                                               nullptr, a.dv_hist, dWp, s.H, s.T, s.R, ntile);
+                e = cudaLaunchKernelEx(&cfg, kern, v, vh, cw, a.gamma, a.eta, (const io_t *)nullptr, (const float *)dX,
+                                       a.dv, a.dgamma, a.deta, (float *)nullptr, a.dv_hist, dWp, s.H, s.T, s.R, ntile);
             }
             tm.end();
+            if (e != cudaSuccess) return e;
             tm.begin("bwd_conv_reduce");
-            conv_reduce_kernel<<<(s.H * 4 * s.dv + 31) / 32, 1024, 0, st>>>(dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
+            cfg.gridDim = dim3((unsigned)((s.H * 4 * s.dv + 31) / 32));
+            cfg.blockDim = dim3(1024);
+            e = cudaLaunchKernelEx(&cfg, conv_reduce_kernel, (const float *)dWp, a.dconv_w, s.B, s.H, s.dv, ntile);
             tm.end();
+            if (e != cudaSuccess) return e;
             return cudaGetLastError();
         }
     }
