@@ -412,6 +412,11 @@ __global__ void __launch_bounds__(NT, 1)
         mbar_expect_tx(mb_v[stage], VBYTES);
         tma_load_3d_hint(sbase + (stage ? OFF_V1 : OFF_V0), &tm_v, mb_v[stage], 0, c * C - 8, bh, l2ef);
         pending |= 4u << stage;
+        if (p.p_gain && R > 0) {  // the non-linear chain's gains of the chunk, read by its prep: into L2 now
+            const uint32_t bytes = (uint32_t)min(C, p.T - c * C) * R * D * 2;
+            const __nv_bfloat16 *src = p.p_gain + ((size_t)bh * p.T + (size_t)c * C) * R * D;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+        }
     };
     // collective bounded wait on one mbarrier phase (thread 0 polls, then a CTA barrier)
     auto wait_one = [&](uint32_t mb, uint32_t &phase, uint32_t bit) -> bool {
