@@ -257,12 +257,6 @@ __global__ void __launch_bounds__(NT, 1)
         float *const sA = reinterpret_cast<float *>(sm + AT);
         float *const sT32 = reinterpret_cast<float *>(sm + AT + AT_T32);
 
-        // ---- U_0, U_1 of this chunk (the level buffers held the previous chunk's outgoing maps) ----
-        if (tid == 0) {
-            bulk_wait_read();
-            if (R > 0) issue_u(bh, t0, 0);
-            if (R > 1) issue_u(bh, t0, 1);
-        }
         // ---- per-token scalars: gates (loaded during the previous chunk), log-decay prefix, decays --
         if (it == 0) load_gates(chunk);
         if (warp == 0) {  // inclusive scan of the 64 log-decays, two per lane
@@ -330,6 +324,12 @@ __global__ void __launch_bounds__(NT, 1)
                 mma_f16(tmem + TM_GRAM, dsc(dbase, QK + ko, 16, 1024), dsc(dbase, QK + PANEL + ko, 16, 1024), id, s > 0);
             }
             mma_commit(mb_gram);
+            // U_0, U_1 of this chunk into the level buffers, which held the previous chunk's outgoing
+            // maps: requested once those stores have read them (they had the chunk's start and the
+            // Gram's issue to do so; nothing before the levels touches the buffers)
+            bulk_wait_read();
+            if (R > 0) issue_u(bh, t0, 0);
+            if (R > 1) issue_u(bh, t0, 1);
         }
         // prep, level-independent part: anchor h, gain g, residual r = v - GELU(h)
         float g_[8][2], r_[8][2];
