@@ -1300,8 +1300,10 @@ constexpr uint32_t FX_PANEL = 8192;
 constexpr uint32_t FX_OFF_S = 0;                      // S_start [64][64] fp16
 constexpr uint32_t FX_OFF_Q = FX_PANEL;               // [Qhat_c; Qhat_{c+1}] [128][64] fp16
 constexpr uint32_t FX_OFF_OUT = FX_OFF_Q + 2 * FX_PANEL;  // output tile [128][64] bf16
-constexpr uint32_t FX_OFF_O0 = FX_OFF_OUT + 2 * FX_PANEL;  // [o0_c; o0_{c+1}] [128][64] fp16 (bf16 output)
-constexpr uint32_t FX_SMEM = FX_OFF_O0 + 2 * FX_PANEL + 1024;
+// [o0_c; o0_{c+1}] [128][64] fp16 (bf16 output) in the output tile's place: each thread reads its
+// row's o0 there before it writes the same bytes of its row's output
+constexpr uint32_t FX_OFF_O0 = FX_OFF_OUT;
+constexpr uint32_t FX_SMEM = FX_OFF_OUT + 2 * FX_PANEL + 1024;
 
 struct FixParams {
     const void *stash_o;  // [BH][NC][64][64] o0 (fp16, or fp32 with out_f32)
