@@ -1100,10 +1100,19 @@ __global__ void __launch_bounds__(1024) conv_reduce_kernel(const float *__restri
     if (o < nout) {
         const int h = o / (4 * dv), jc = o % (4 * dv);
         const int nterm = B * ntile;
-#pragma unroll 4
-        for (int e = wp; e < nterm; e += 32) {
-            const int b = e / ntile, tile = e % ntile;
-            s += dWp[(((size_t)b * H + h) * ntile + tile) * 4 * dv + jc];
+        // the warp's terms e = wp, wp + 32, ... in batches of 16 whose loads are all in flight
+        // before the first is added (the sum keeps the order of e)
+        for (int e0 = wp; e0 < nterm; e0 += 32 * 16) {
+            float x[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int e = e0 + 32 * q;
+                const int b = e / ntile, tile = e % ntile;
+                x[q] = e < nterm ? dWp[(((size_t)b * H + h) * ntile + tile) * 4 * dv + jc] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                if (e0 + 32 * q < nterm) s += x[q];
         }
     }
     part[wp][lane] = s;
