@@ -115,6 +115,7 @@ SERIAL = [
     (2, 1, 130, 128, 128, 8, "bf16", True),
     (1, 1, 97, 64, 128, 16, "f32", False),
     (1, 2, 150, 128, 64, 4, "bf16", False),
+    (1, 1, 90, 64, 64, 7, "bf16", True),  # bf16, dv = 64: the fused tail with the largest level arrays
 ]
 
 
