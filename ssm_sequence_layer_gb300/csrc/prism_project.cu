@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(256) anchor_kernel(const __nv_bfloat16 *__rest
 // lane quarter each (token rows), all 128 columns per thread: they wait for an accumulator,
 // drain it and release it on its "empty" barrier, so a tile's epilogue runs under the next
 // tile's products.
-constexpr int PTHREADS = 160;  // warp 0: main loop; warps 1-4: epilogue
+constexpr int PTHREADS = 192;  // warp 0: products; warp 1: operand loads; warps 2-5: epilogue
 
 __global__ void __launch_bounds__(PTHREADS, 2)
     project_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w, ProjParams p)
@@ -133,22 +133,31 @@ __global__ void __launch_bounds__(PTHREADS, 2)
     fence_after_sync();
     const uint32_t tmem = tmem_base_s;
 
-    // thread 0's view of the copies and products in flight (for the drain after an expired wait)
-    int loads_issued = 0, loads_waited = 0, mmas_issued = 0, mmas_waited = 0;
-    if (tid == 0) {
-        // global step g = tile i * KS + ks; stage g % STAGES
-        const int total = my_tiles * KS;
-        auto tile_of = [&](int i, int &b, int &t0, int &n0) {
-            const int tile = (int)blockIdx.x + i * (int)gridDim.x;
-            const int bt = tile / tiles_n;
-            n0 = (tile % tiles_n) * PN;
-            b = bt / p.tiles_t;
-            t0 = (bt % p.tiles_t) * PM;
-        };
-        auto issue = [&](int g) {
+    // global step g = tile i * KS + ks uses stage g % STAGES.  Lane 0 of warp 1 refills a stage as
+    // soon as the products that read it have completed; lane 0 of warp 0 issues the products as the
+    // stages fill, so it never waits for a product before issuing the next.
+    const int total = my_tiles * KS;
+    auto tile_of = [&](int i, int &b, int &t0, int &n0) {
+        const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+        const int bt = tile / tiles_n;
+        n0 = (tile % tiles_n) * PN;
+        b = bt / p.tiles_t;
+        t0 = (bt % p.tiles_t) * PM;
+    };
+    int loads_issued = 0, mmas_issued = 0;  // the producers' counts (for the drain after an expired wait)
+    if (tid == 32) {  // ---- operand loads ----
+        for (int g = 0; g < total; ++g) {
+            const int s = g % STAGES;
+            if (g >= STAGES &&
+                !mbar_wait(smem_u32(&mmad[s]), (uint32_t)((g / STAGES - 1) & 1), p.wait_ns)) {  // step g - STAGES read it
+                abort_s = 1;
+                atomicCAS(p.status, 0, kDevTimeout);
+                break;
+            }
+            if (*(volatile int *)&abort_s) break;
             int b, t0, n0;
             tile_of(g / KS, b, t0, n0);
-            const int ks = g % KS, s = g % STAGES;
+            const int ks = g % KS;
             const uint32_t mb = smem_u32(&full[s]);
             mbar_expect_tx(mb, 2 * TILE);
             tma_load_3d(sbase + OFF_A + s * TILE, &tm_a, mb, ks * PK, t0, b);
@@ -157,27 +166,21 @@ __global__ void __launch_bounds__(PTHREADS, 2)
                     sbase + OFF_B + s * TILE),
                 "l"((uint64_t)&tm_w), "r"(mb), "r"(ks * PK), "r"(n0)
                 : "memory");
-            ++loads_issued;
-        };
-        auto wait_mma_upto = [&](int j) -> bool {  // products 0..j complete (each phase waited once, in order)
-            while (mmas_waited <= j) {
-                const int k = mmas_waited;
-                if (!mbar_wait(smem_u32(&mmad[k % STAGES]), (uint32_t)((k / STAGES) & 1), p.wait_ns)) return false;
-                ++mmas_waited;
-            }
-            return true;
-        };
-        bool ok = true;
-        for (int g = 0; g < STAGES && g < total; ++g) issue(g);
-        for (int g = 0; g < total && ok; ++g) {
+            loads_issued = g + 1;
+        }
+    } else if (tid == 0) {  // ---- products ----
+        for (int g = 0; g < total; ++g) {
             const int i = g / KS, ks = g % KS, s = g % STAGES, buf = i & 1;
-            if (ks == 0 && i >= 2) {  // the accumulator's previous tile (i - 2) has been drained
+            bool ok = true;
+            if (ks == 0 && i >= 2)  // the accumulator's previous tile (i - 2) has been drained
                 ok = mbar_wait(smem_u32(&acc_empty[buf]), (uint32_t)(((i - 2) / 2) & 1), p.wait_ns);
-                if (!ok) break;
+            if (ok) ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((g / STAGES) & 1), p.wait_ns);
+            if (!ok) {
+                abort_s = 1;
+                atomicCAS(p.status, 0, kDevTimeout);
+                break;
             }
-            ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((g / STAGES) & 1), p.wait_ns);
-            if (!ok) break;
-            ++loads_waited;
+            if (*(volatile int *)&abort_s) break;
             fence_after_sync();
 #pragma unroll
             for (int j = 0; j < PK / 16; ++j)
@@ -185,17 +188,9 @@ __global__ void __launch_bounds__(PTHREADS, 2)
                         idesc, (ks > 0 || j > 0) ? 1u : 0u);
             mma_commit(smem_u32(&mmad[s]));
             if (ks == KS - 1) mma_commit(smem_u32(&acc_full[buf]));  // the tile's products are in the accumulator
-            ++mmas_issued;
-            if (g >= 1 && g - 1 + STAGES < total) {  // stage of step g - 1 -> step g - 1 + STAGES
-                ok = wait_mma_upto(g - 1);
-                if (ok) issue(g - 1 + STAGES);
-            }
+            mmas_issued = g + 1;
         }
-        if (!ok) {
-            abort_s = 1;
-            atomicCAS(p.status, 0, kDevTimeout);
-        }
-    } else if (warp >= 1) {  // epilogue warps 1-4: lane quarter q = warp & 3
+    } else if (warp >= 2) {  // epilogue warps 2-5: lane quarter q = warp & 3
         const int q = warp & 3;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const int NU = p.H * p.R * p.dk, NP = p.H * p.R * p.dv;
@@ -268,11 +263,13 @@ __global__ void __launch_bounds__(PTHREADS, 2)
     }
     // drain: after an expired wait, the copies and products in flight land before the CTA exits
     __syncthreads();
-    if (tid == 0 && abort_s) {
-        for (int k = mmas_waited; k < mmas_issued; ++k)
-            (void)mbar_wait(smem_u32(&mmad[k % STAGES]), (uint32_t)((k / STAGES) & 1), 1000000000ull);
-        for (int k = loads_waited; k < loads_issued; ++k)
-            (void)mbar_wait(smem_u32(&full[k % STAGES]), (uint32_t)((k / STAGES) & 1), 1000000000ull);
+    if (abort_s) {
+        if (tid == 0 && mmas_issued > 0)  // the last product of each stage (products complete in order)
+            (void)mbar_wait(smem_u32(&mmad[(mmas_issued - 1) % STAGES]), (uint32_t)(((mmas_issued - 1) / STAGES) & 1),
+                            1000000000ull);
+        if (tid == 32)  // the last load of each stage
+            for (int g = max(0, loads_issued - STAGES); g < loads_issued; ++g)
+                (void)mbar_wait(smem_u32(&full[g % STAGES]), (uint32_t)((g / STAGES) & 1), 1000000000ull);
     }
     fence_before_sync();
     __syncthreads();
