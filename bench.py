@@ -111,6 +111,8 @@ def kernel_alg_bytes(name, w, nonlinear=False):
     table = {
         "map_chunks": q + k + v + u + gates,      # every input read once (the maps are its own output)
         "map_scan": out,                          # the outputs written once (the maps are read back)
+        "map_compose": chunks * 2 * w.dk * w.dv * 2,  # long sequences: every chunk's A_c and B_c read once
+        "map_carry": w.B * w.H * w.dk * w.dv * 4,     # the segments' start states (a floor: one state)
         "simt_prep": v + th * 4 * R + p_or_eta + X,
         "simt_chunk_solve": k + th * 8 + lam + Tm,
         "simt_wy": k + v + th * 4 + u + X + lam + Tm + W + Up,

@@ -775,6 +775,9 @@ constexpr uint32_t TM_D1 = 0, TM_D2 = 128;
 struct ScanParams {
     const float *S_init;  // [BH][D][D] or null
     float *S_final;       // [BH][D][D] or null
+    float *S_seg;         // with G > 1: the state entering each segment, [BH][G][D][D]
+    float *seg_maps;      // the compose pass's output: [BH][G][2][D][D] (B_seg, A_seg)
+    int G;                // segments a sequence (the chunks of segment g: g NC / G .. (g + 1) NC / G - 1)
     const __half *mO;     // [BH*NC][64][128] O_loc
     void *out;            // [BH][T][D] bf16, or fp32 with out_f32
     int *status;
@@ -795,8 +798,12 @@ __global__ void __launch_bounds__(ST, 1)
     const int quad = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half of the epilogues
     const int row = quad * 32 + lane;             // state row / token within this half (< 64: live)
     const bool live = quad < 2;
-    const int bh = blockIdx.x >> 1, vh = blockIdx.x & 1;  // sequence; half of the value rows
-    const int r0 = 64 * vh;                               // first state row / channel of this half
+    // block (sequence bh, segment seg, half vh of the value rows)
+    const int vh = blockIdx.x & 1, seg = (int)(blockIdx.x >> 1) % p.G, bh = (int)(blockIdx.x >> 1) / p.G;
+    const int r0 = 64 * vh;  // first state row / channel of this half
+    const int cb = (int)((long long)seg * p.NC / p.G), ce = (int)((long long)(seg + 1) * p.NC / p.G);
+    const float *s_in = p.G > 1 ? p.S_seg + ((size_t)bh * p.G + seg) * D * D
+                                : (p.S_init ? p.S_init + (size_t)bh * D * D : nullptr);
     const uint32_t sbase = smem_u32(sm);
     const uint64_t dbase = sdesc(sbase, 0, 0);
     const uint32_t mb_mma = smem_u32(&mbar[SC_STAGES]);
@@ -810,6 +817,7 @@ __global__ void __launch_bounds__(ST, 1)
         prefetch_tmap(&tm_b);
         prefetch_tmap(&tm_out);
     }
+    grid_dependency_wait();  // the maps of the map kernel (and the segments' start states)
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 256);
     // the initial state (fp16 operand copy): row `row`, 64 columns of this thread's half
     if (live) {
@@ -819,7 +827,7 @@ __global__ void __launch_bounds__(ST, 1)
             float w[32];
 #pragma unroll
             for (int q = 0; q < 32; ++q)
-                w[q] = p.S_init ? p.S_init[((size_t)bh * D + r0 + row) * D + 64 * half + 32 * g + q] : 0.f;
+                w[q] = s_in ? s_in[(size_t)(r0 + row) * D + 64 * half + 32 * g + q] : 0.f;
             st_row_h(sp, row, 32 * g, w);
         }
     }
@@ -829,13 +837,12 @@ __global__ void __launch_bounds__(ST, 1)
     fence_after_sync();
     const uint32_t tmem = tmem_base_s;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    grid_dependency_wait();  // the maps of the map kernel
     allow_dependent_launch();
 
-    const int NC = p.NC;
+    const int NC = p.NC, nk = ce - cb;
     const size_t ch0 = (size_t)bh * NC;
-    auto issue = [&](int c) {  // chunk c's A_c, Q~ and this half of B_c into stage c % SC_STAGES
-        const int st = c % SC_STAGES;
+    auto issue = [&](int k) {  // chunk cb + k's A_c, Q~ and this half of B_c into stage k % SC_STAGES
+        const int c = cb + k, st = k % SC_STAGES;
         const uint32_t base = sbase + SC_OFF_ST + st * STAGE, mb = smem_u32(&mbar[st]);
         const int ra = (int)((ch0 + c) * 128), rq = (int)((ch0 + c) * 64);
         mbar_expect_tx(mb, STAGE);
@@ -849,18 +856,18 @@ __global__ void __launch_bounds__(ST, 1)
     uint32_t ph_mma = 0;
     int issued = 0, consumed = 0;  // thread 0: chunks whose maps were requested / have landed
     if (tid == 0) {
-        for (; issued < SC_STAGES && issued < NC; ++issued) issue(issued);
+        for (; issued < SC_STAGES && issued < nk; ++issued) issue(issued);
     }
     bool finite = true;
 #ifdef PRISM_PHASE_TIMERS
     unsigned long long ph_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     long long ph_last = clock64();
 #endif
-    for (int c = 0; c < NC && abort_s == 0; ++c) {
-        const int st = c % SC_STAGES;
+    for (int k = 0; k < nk && abort_s == 0; ++k) {
+        const int c = cb + k, st = k % SC_STAGES;
         const uint32_t sb = SC_OFF_ST + st * STAGE;
         if (tid == 0) {
-            if (mbar_wait(smem_u32(&mbar[st]), (uint32_t)((c / SC_STAGES) & 1), p.wait_ns)) {
+            if (mbar_wait(smem_u32(&mbar[st]), (uint32_t)((k / SC_STAGES) & 1), p.wait_ns)) {
                 ++consumed;
                 fence_after_sync();
                 // D1 = S_h A_c (A = S_h [c][m] K-major, rows 64.. unused; B = A_c [m][n] MN-major);
@@ -910,7 +917,7 @@ __global__ void __launch_bounds__(ST, 1)
         fence_before_sync();
         __syncthreads();  // stage st is consumed: refill it with chunk c + SC_STAGES
         fence_after_sync();
-        if (tid == 0 && issued < NC && abort_s == 0) issue(issued++);
+        if (tid == 0 && issued < nk && abort_s == 0) issue(issued++);
         MAP_MARK(1);
         if (live) {
             // S_h <- S_h A_c + B_c (row `row`, columns 64 half .. 64 half + 63)
@@ -974,8 +981,8 @@ __global__ void __launch_bounds__(ST, 1)
     if (tid == 0) {
         bulk_wait_all();
         if (abort_s) {
-            for (int c = consumed; c < issued; ++c)
-                (void)mbar_wait(smem_u32(&mbar[c % SC_STAGES]), (uint32_t)((c / SC_STAGES) & 1), 1000000000ull);
+            for (int k = consumed; k < issued; ++k)
+                (void)mbar_wait(smem_u32(&mbar[k % SC_STAGES]), (uint32_t)((k / SC_STAGES) & 1), 1000000000ull);
             const uint32_t mb_drain = smem_u32(&mbar[SC_STAGES + 1]);
             mma_commit(mb_drain);
             (void)mbar_wait(mb_drain, 0, 1000000000ull);
@@ -984,6 +991,184 @@ __global__ void __launch_bounds__(ST, 1)
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Segment maps of the chunk scan, for sequences of many chunks and few sequences.  The compose pass
+// runs the scan's step over one segment of G for the block rows [S_h; P_h] of the product's A
+// operand: S_h (rows 0-63) starts at zero and takes B_c, P_h (rows 64-127) starts at the identity
+// rows r0 .. r0 + 63, so that one product per chunk carries both the segment's offset
+// B_seg = (... (B_cb A_cb+1 + B_cb+1) ...) and the rows of its transition A_seg = A_cb ... A_ce-1;
+// S_out = S_in A_seg + B_seg.  Shared memory: the two K blocks of [S_h; P_h] (128 rows each, fp16,
+// 128B-swizzled), then a ring of A_c and this half's rows of B_c.
+constexpr uint32_t CP_STAGE = 4 * PANEL + 2 * PANEL;  // A_c | B_c rows of this half
+constexpr uint32_t CP_OFF_ST = 4 * PANEL;
+constexpr uint32_t CP_SMEM = CP_OFF_ST + SC_STAGES * CP_STAGE + 1024;
+static_assert(CP_SMEM <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(ST, 1)
+    compose_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, ScanParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint32_t tmem_base_s;
+    __shared__ __align__(8) uint64_t mbar[SC_STAGES + 2];  // ring stages; products; drain
+    __shared__ int abort_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half (= K block)
+    const int row = quad * 32 + lane;             // 0-63: a row of S_h, 64-127: a row of P_h
+    const int vh = blockIdx.x & 1, seg = (int)(blockIdx.x >> 1) % p.G, bh = (int)(blockIdx.x >> 1) / p.G;
+    const int r0 = 64 * vh;
+    const int cb = (int)((long long)seg * p.NC / p.G), ce = (int)((long long)(seg + 1) * p.NC / p.G), nk = ce - cb;
+    const uint32_t sbase = smem_u32(sm);
+    const uint64_t dbase = sdesc(sbase, 0, 0);
+    const uint32_t mb_mma = smem_u32(&mbar[SC_STAGES]);
+    if (tid == 0) {
+        abort_s = 0;
+        for (int i = 0; i < SC_STAGES + 2; ++i) mbar_init(smem_u32(&mbar[i]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tm_a);
+        prefetch_tmap(&tm_b);
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 128);
+    {  // S_h = 0, P_h = the identity rows of this half: row `row`, the 64 columns of K block `half`
+        uint8_t *sp = sm + (uint32_t)half * 2 * PANEL;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            float w[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) w[q] = (row >= 64 && 64 * half + 32 * g + q == r0 + row - 64) ? 1.f : 0.f;
+            st_row_h(sp, row, 32 * g, w);
+        }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_base_s;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    grid_dependency_wait();  // the maps of the map kernel
+    allow_dependent_launch();
+    const size_t ch0 = (size_t)bh * p.NC;
+    auto issue = [&](int k) {  // chunk cb + k's A_c and this half of B_c into stage k % SC_STAGES
+        const int st = k % SC_STAGES;
+        const uint32_t base = sbase + CP_OFF_ST + st * CP_STAGE, mb = smem_u32(&mbar[st]);
+        const int ra = (int)((ch0 + cb + k) * 128);
+        mbar_expect_tx(mb, CP_STAGE);
+        tma_load_2d(base, &tm_a, mb, 0, ra);
+        tma_load_2d(base + 2 * PANEL, &tm_a, mb, 64, ra);
+        tma_load_2d(base + 4 * PANEL, &tm_b, mb, 0, ra + r0);
+        tma_load_2d(base + 5 * PANEL, &tm_b, mb, 64, ra + r0);
+    };
+    uint32_t ph_mma = 0;
+    int issued = 0, consumed = 0;
+    if (tid == 0)
+        for (; issued < SC_STAGES && issued < nk; ++issued) issue(issued);
+    for (int k = 0; k < nk && abort_s == 0; ++k) {
+        const int st = k % SC_STAGES;
+        const uint32_t sb = CP_OFF_ST + st * CP_STAGE;
+        if (tid == 0) {
+            if (mbar_wait(smem_u32(&mbar[st]), (uint32_t)((k / SC_STAGES) & 1), p.wait_ns)) {
+                ++consumed;
+                fence_after_sync();
+                // D1 = [S_h; P_h] A_c (A = [S_h; P_h] [r][m] K-major, 128 rows a K block; B = A_c MN-major)
+                const uint32_t id1 = idesc_f16(128, 128, 0, 1);
+#pragma unroll
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    const uint32_t so = (uint32_t)(s2 >> 2) * 2 * PANEL + (uint32_t)(s2 & 3) * 32;
+                    mma_f16(tmem, dsc(dbase, so, 16, 1024), dsc(dbase, sb + s2 * 2048, 2 * PANEL, 1024), id1, s2 > 0);
+                }
+                mma_commit(mb_mma);
+            } else {
+                abort_s = 1;
+                set_status(p.status, kDevTimeout);
+            }
+        }
+        __syncthreads();
+        if (abort_s) break;
+        uint4 bc[8];  // B_c of this thread's S row (rows < 64), read before the stage is refilled
+        if (row < 64) {
+            const uint8_t *bp = sm + sb + 4 * PANEL + (uint32_t)half * PANEL;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bc[e] = *reinterpret_cast<const uint4 *>(bp + sw128(row, 8 * e));
+        }
+        if (!mbar_wait(mb_mma, ph_mma, p.wait_ns)) {
+            abort_s = 1;
+            set_status(p.status, kDevTimeout);
+        }
+        ph_mma ^= 1u;
+        fence_before_sync();
+        __syncthreads();  // stage st and the operand rows are consumed
+        fence_after_sync();
+        if (tid == 0 && issued < nk && abort_s == 0) issue(issued++);
+        uint8_t *sp = sm + (uint32_t)half * 2 * PANEL;
+        const bool last = k + 1 == nk;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            float v[32];
+            tmem_ld(tmem + lane_off + (uint32_t)(64 * half + 32 * g), v);
+            if (row < 64) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) add_h8(v, 8 * e, bc[4 * g + e]);
+            }
+            if (last) {  // the segment's map: B_seg row r0 + row (row < 64), A_seg row r0 + row - 64
+                float *dst = p.seg_maps + ((((size_t)bh * p.G + seg) * 2 + (row >= 64)) * D + r0 + (row & 63)) * D +
+                             64 * half + 32 * g;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+                st_row_h(sp, row, 32 * g, v);
+            }
+        }
+        fence_async_smem();  // [S_h; P_h] is the next chunk's MMA operand
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    }
+    if (tid == 0 && abort_s) {  // drain after an expired wait
+        for (int k = consumed; k < issued; ++k)
+            (void)mbar_wait(smem_u32(&mbar[k % SC_STAGES]), (uint32_t)((k / SC_STAGES) & 1), 1000000000ull);
+        const uint32_t mb_drain = smem_u32(&mbar[SC_STAGES + 1]);
+        mma_commit(mb_drain);
+        (void)mbar_wait(mb_drain, 0, 1000000000ull);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// The segments' start states: S_0 = S_init (or 0), S_{g+1} = S_g A_seg(g) + B_seg(g), fp32.  Block
+// (bh, rb) takes 8 state rows; warp w row 8 rb + w, lane the columns 4 lane .. 4 lane + 3.
+__global__ void __launch_bounds__(256) carry_kernel(ScanParams p)
+{
+    __shared__ float s[8][D];
+    const int bh = blockIdx.x, rb = blockIdx.y, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = 8 * rb + w, c4 = 4 * lane;
+    grid_dependency_wait();  // the segment maps of the compose pass
+    allow_dependent_launch();
+    float4 cur = p.S_init ? *reinterpret_cast<const float4 *>(p.S_init + ((size_t)bh * D + r) * D + c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < p.G; ++g) {
+        *reinterpret_cast<float4 *>(p.S_seg + (((size_t)bh * p.G + g) * D + r) * D + c4) = cur;
+        if (g + 1 == p.G) break;
+        *reinterpret_cast<float4 *>(&s[w][c4]) = cur;
+        __syncwarp();
+        const float *Bm = p.seg_maps + (((size_t)bh * p.G + g) * 2 + 0) * D * D;
+        const float *Am = p.seg_maps + (((size_t)bh * p.G + g) * 2 + 1) * D * D;
+        float4 acc = *reinterpret_cast<const float4 *>(Bm + (size_t)r * D + c4);
+#pragma unroll 8
+        for (int m = 0; m < D; ++m) {
+            const float sm_ = s[w][m];
+            const float4 a = *reinterpret_cast<const float4 *>(Am + (size_t)m * D + c4);
+            acc.x = fmaf(sm_, a.x, acc.x);
+            acc.y = fmaf(sm_, a.y, acc.y);
+            acc.z = fmaf(sm_, a.z, acc.z);
+            acc.w = fmaf(sm_, a.w, acc.w);
+        }
+        __syncwarp();
+        cur = acc;
+    }
 }
 
 }  // namespace mp
@@ -1023,10 +1208,29 @@ bool map_supported(const Shape &s, prism_dtype io)
     return io == PRISM_BF16 && s.dk == mp::D && s.dv == mp::D && s.L >= 1 && s.L <= 1 + mp::RM;
 }
 
+// Segments of the chunk scan: long sequences (256 chunks or more) of few heads run the scan as G
+// segments (compose, carry, then the scan of each segment from its start state) so that the
+// scan's blocks fill more of the SMs; G <= kMaxScanSegments.  The segment maps and start states
+// follow the other map buffers in the workspace.
+constexpr int kMaxScanSegments = 8;
+bool scan_segments_eligible(const Shape &s) { return s.NC >= 256 && 4 * s.BH <= 152; }
+int scan_segments(const Shape &s, int sm_count)
+{
+    if (!scan_segments_eligible(s)) return 1;
+    int g = sm_count / (2 * s.BH);
+    g = g < kMaxScanSegments ? g : kMaxScanSegments;
+    g = g < s.NC / 64 ? g : s.NC / 64;
+    return g > 1 ? g : 1;
+}
+size_t scan_segment_bytes(const Shape &s)
+{
+    return scan_segments_eligible(s) ? (size_t)s.BH * kMaxScanSegments * 3 * mp::D * mp::D * 4 + 256 : 0;
+}
+
 size_t map_workspace_bytes(const Shape &s)
 {
     const size_t chunks = (size_t)s.BH * s.NC;
-    return chunks * (2 * 128 + 2 * 64) * mp::D * 2 + 4 * 256;
+    return chunks * (2 * 128 + 2 * 64) * mp::D * 2 + 4 * 256 + scan_segment_bytes(s);
 }
 
 void map_carve(const Shape &s, void *base, MapWorkspace *w)
@@ -1045,6 +1249,8 @@ void map_carve(const Shape &s, void *base, MapWorkspace *w)
 cudaError_t map_prepare()
 {
     cudaError_t e = cudaFuncSetAttribute(mp::map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mp::MAP_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mp::compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mp::CP_SMEM);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(mp::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mp::SCAN_SMEM);
 }
@@ -1123,6 +1329,16 @@ cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, cons
     sp.NC = s.NC;
     sp.out_f32 = out_f32 ? 1 : 0;
     sp.wait_ns = wns;
+    const int G = scan_segments(s, sm_count);
+    sp.G = G;
+    sp.S_seg = nullptr;
+    sp.seg_maps = nullptr;
+    if (G > 1) {  // after the O_loc maps (map_workspace_bytes counted the room)
+        const size_t chunks = (size_t)s.BH * s.NC;
+        const uintptr_t q = ((uintptr_t)(w.O + chunks * 64 * D) + 255) & ~(uintptr_t)255;
+        sp.seg_maps = reinterpret_cast<float *>(q);
+        sp.S_seg = sp.seg_maps + (size_t)s.BH * G * 2 * D * D;
+    }
 
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1138,8 +1354,24 @@ cudaError_t map_forward(const Shape &s, const ForwardArgs &a, bool out_f32, cons
     cudaError_t e = cudaLaunchKernelEx(&cfg, map_kernel, mq, mk, mv, mu, ma, mqt, mb, mo, mp_);
     tm.end();
     if (e != cudaSuccess) return e;
+    if (G > 1) {
+        tm.begin("map_compose");
+        cfg.gridDim = dim3((unsigned)(2 * s.BH * G));
+        cfg.blockDim = dim3(ST);
+        cfg.dynamicSmemBytes = CP_SMEM;
+        e = cudaLaunchKernelEx(&cfg, compose_kernel, ma, mbh, sp);
+        tm.end();
+        if (e != cudaSuccess) return e;
+        tm.begin("map_carry");
+        cfg.gridDim = dim3((unsigned)s.BH, (unsigned)(D / 8));
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, carry_kernel, sp);
+        tm.end();
+        if (e != cudaSuccess) return e;
+    }
     tm.begin("map_scan");
-    cfg.gridDim = dim3((unsigned)(2 * s.BH));
+    cfg.gridDim = dim3((unsigned)(2 * s.BH * G));
     cfg.blockDim = dim3(ST);
     cfg.dynamicSmemBytes = SCAN_SMEM;
     e = cudaLaunchKernelEx(&cfg, scan_kernel, ma, mqt, mbh, mout, sp);

@@ -248,3 +248,24 @@ def test_state_arguments_are_checked():
         with pytest.raises(B.PrismError) as ei:
             B.prism_decode_step(p.handle, *p._tensors(token(inp, 0)), None, bad, hist)
         assert ei.value.status == B.PRISM_ERR_INVALID_ARG
+
+
+def test_long_sequence_segmented_map_scan(oracle_mod):
+    """A sequence of 257 chunks with dk = dv = 128 and two heads: the chunk-map path runs its scan
+    as segments (compose, carry, then each segment from its start state).  With S_init given and
+    S_final asked for, bf16 output: the whole output and the final state against one oracle call."""
+    B_, H, T, L = 1, 2, 257 * 64 - 27, 3
+    inp = make_inputs(B_, H, T, 128, 128, L, dtype="bf16", seed=71)
+    S0 = init_state(B_, H, 128, 128, seed=72)
+    d = to_device(inp)
+    S_fin = torch.empty(B_, H, 128, 128, device="cuda")
+    with B.Plan.for_inputs(d, out="f32") as p:
+        out = p.forward_state(d, S_init=S0.cuda(), S_final=S_fin)
+        torch.cuda.synchronize()
+        p.last_device_status()
+    ref = oracle_forward(oracle_mod, inp, S_init=S0.double().numpy(), want_state=True)
+    got = out.double().cpu().numpy()
+    err_o, err_s = rel_err(got, ref["out"]), rel_err(S_fin.double().cpu().numpy(), ref["S_final"])
+    print(f"segmented map scan: rel err out {err_o:.3e}, S_final {err_s:.3e}")
+    assert np.all(np.isfinite(got))
+    assert err_o <= TOL["bf16"] and err_s <= TOL["bf16"]
