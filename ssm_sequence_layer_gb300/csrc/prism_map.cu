@@ -817,7 +817,7 @@ __global__ void __launch_bounds__(ST, 1)
         prefetch_tmap(&tm_b);
         prefetch_tmap(&tm_out);
     }
-    grid_dependency_wait();  // the maps of the map kernel (and the segments' start states)
+    if (p.G > 1) grid_dependency_wait();  // the segments' start states (the carry pass)
     if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 256);
     // the initial state (fp16 operand copy): row `row`, 64 columns of this thread's half
     if (live) {
@@ -837,6 +837,7 @@ __global__ void __launch_bounds__(ST, 1)
     fence_after_sync();
     const uint32_t tmem = tmem_base_s;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    grid_dependency_wait();  // the maps of the map kernel
     allow_dependent_launch();
 
     const int NC = p.NC, nk = ce - cb;
